@@ -1,0 +1,291 @@
+"""CPU oracle for the MoE expert-FFN layer -- ctypes wrapper around ``moe_oracle.c``.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this module.  It shares no code with the CUDA
+library and never imports it; inputs come from the seeded generators and are passed in
+as numpy arrays.
+
+Each function follows one step of the layer as the sources state it (see the header of
+``moe_oracle.c`` for the citations and the readings R1-R7 taken where they are silent):
+
+* ``router_logits``  -- Muse Spark Open explainer, section 8 (one FP32 matrix product)
+* ``topk_softmax``   -- section 8 (best k of E, a set) and section 9 (weights sum to 1)
+* ``permute``        -- section 12 (tokens gathered per expert, one batch per expert)
+* ``expert_ffn``     -- section 9 (gate / up / down) on MXFP4 weights (section 11, and the
+                        DGX Spark news item, section 2)
+* ``combine``        -- section 9 (weighted sum over the chosen experts)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+from typing import Callable, Dict, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_%s.so" % platform.machine())
+
+ACT_BF16 = 0
+ACT_MXFP4 = 1
+ACT_EXACT = 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (ISO C, no FP contraction, OpenMP)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P = ctypes.c_void_p
+    i32, i64 = ctypes.c_int, ctypes.c_int64
+    sig = {
+        "oracle_e2m1_value": (ctypes.c_double, [i32]),
+        "oracle_e8m0_value": (ctypes.c_double, [i32]),
+        "oracle_e2m1_encode_magnitude": (i32, [ctypes.c_double]),
+        "oracle_mx_block_quantize": (None, [P, i32, P, P]),
+        "oracle_mxfp4_pack": (i32, [P, i64, i64, P, P]),
+        "oracle_mxfp4_unpack": (i32, [P, P, i64, i64, P]),
+        "oracle_router_logits": (None, [P, P, P, i32, i32, i32, P]),
+        "oracle_topk_softmax": (None, [P, i32, i32, i32, P, P]),
+        "oracle_permute": (i32, [P, i32, i32, i32, P, P, P, P]),
+        "oracle_activation_row": (None, [P, i32, i32, P, P, P]),
+        "oracle_expert_ffn": (None, [P, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P, P]),
+        "oracle_combine": (None, [P, P, P, i32, P, i32, i32, P]),
+        "oracle_float_to_bf16_bits": (ctypes.c_uint16, [ctypes.c_float]),
+        "oracle_bf16_bits_to_float": (ctypes.c_float, [ctypes.c_uint16]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def set_threads(n: int) -> None:
+    """Thread count used by the OpenMP loops (applies to later calls)."""
+    os.environ["OMP_NUM_THREADS"] = str(int(n))
+
+
+# ------------------------------------------------------------------ scalar formats
+
+def e2m1_value(code: int) -> float:
+    return _load().oracle_e2m1_value(int(code))
+
+
+def e8m0_value(s: int) -> float:
+    return _load().oracle_e8m0_value(int(s))
+
+
+def e2m1_encode_magnitude(a: float) -> int:
+    return _load().oracle_e2m1_encode_magnitude(float(a))
+
+
+def float_to_bf16_bits(f: float) -> int:
+    return int(_load().oracle_float_to_bf16_bits(float(f)))
+
+
+def mx_block_quantize(v: np.ndarray):
+    """Quantise one block (any length) with a shared scale: returns (codes uint8[n], scale byte)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    codes = np.zeros(v.shape[0], dtype=np.uint8)
+    sb = np.zeros(1, dtype=np.uint8)
+    _load().oracle_mx_block_quantize(_ptr(v), v.shape[0], _ptr(codes), _ptr(sb))
+    return codes, int(sb[0])
+
+
+# ------------------------------------------------------------------ MXFP4 tensors
+
+def mxfp4_pack(w: np.ndarray):
+    """fp32 [rows][K] -> (q uint8 [rows][K/2], s uint8 [rows][K/32])."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    rows, K = w.shape
+    q = np.empty((rows, K // 2), dtype=np.uint8)
+    s = np.empty((rows, K // 32), dtype=np.uint8)
+    rc = _load().oracle_mxfp4_pack(_ptr(w), rows, K, _ptr(q), _ptr(s))
+    if rc != 0:
+        raise ValueError("K must be a multiple of 32")
+    return q, s
+
+
+def mxfp4_unpack(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    rows, K = q.shape[0], q.shape[1] * 2
+    w = np.empty((rows, K), dtype=np.float32)
+    rc = _load().oracle_mxfp4_unpack(_ptr(q), _ptr(s), rows, K, _ptr(w))
+    if rc != 0:
+        raise ValueError("NaN scale byte (0xFF) in MXFP4 tensor")
+    return w
+
+
+# ------------------------------------------------------------------ router / permute
+
+def router_logits(x_bits: np.ndarray, W_r: np.ndarray, b: Optional[np.ndarray]) -> np.ndarray:
+    """x_bits uint16 bf16 [T][d]; W_r fp32 [E][d]; b fp32 [E] or None -> fp32 [T][E]."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    W_r = np.ascontiguousarray(W_r, dtype=np.float32)
+    T, d = x_bits.shape
+    E = W_r.shape[0]
+    out = np.empty((T, E), dtype=np.float32)
+    bb = None if b is None else np.ascontiguousarray(b, dtype=np.float32)
+    _load().oracle_router_logits(_ptr(x_bits), _ptr(W_r), _ptr(bb), T, d, E, _ptr(out))
+    return out
+
+
+def topk_softmax(logits: np.ndarray, k: int):
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, k), dtype=np.int32)
+    w = np.empty((T, k), dtype=np.float32)
+    _load().oracle_topk_softmax(_ptr(logits), T, E, k, _ptr(ids), _ptr(w))
+    return ids, w
+
+
+def permute(ids: np.ndarray, E: int):
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    counts = np.empty(E, dtype=np.int32)
+    offsets = np.empty(E + 1, dtype=np.int32)
+    perm_token = np.empty(T * k, dtype=np.int32)
+    inv_pos = np.empty(T * k, dtype=np.int32)
+    rc = _load().oracle_permute(_ptr(ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(perm_token), _ptr(inv_pos))
+    if rc != 0:
+        raise ValueError("expert id out of range")
+    return counts, offsets, perm_token, inv_pos
+
+
+# ------------------------------------------------------------------ activations / experts
+
+def activation_rows(x_bits: np.ndarray, act_fmt: int, want_codes: bool = False):
+    """Activation operand values of token rows (fp32 [n][d]); with want_codes also the
+    MXFP4 codes/scales (only meaningful for ACT_MXFP4)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    n, d = x_bits.shape
+    out = np.empty((n, d), dtype=np.float32)
+    q = np.zeros((n, d // 2), dtype=np.uint8) if want_codes else None
+    s = np.zeros((n, d // 32), dtype=np.uint8) if want_codes else None
+    lib = _load()
+    for r in range(n):
+        lib.oracle_activation_row(_ptr(x_bits[r]), d, act_fmt, _ptr(out[r]),
+                                  None if q is None else _ptr(q[r]), None if s is None else _ptr(s[r]))
+    if want_codes:
+        return out, q, s
+    return out
+
+
+def expert_ffn(a: np.ndarray, wg, wu, wd, act_fmt: int, want_h: bool = False):
+    """One expert on n activation rows.  wg/wu/wd are (q, s) MXFP4 pairs with
+    wg/wu of shape [I][d] and wd of shape [d][I].  Returns y [n][d] (bf16 values as fp32)
+    and optionally (h [n][I], hq, hs)."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    n, d = a.shape
+    I = wg[0].shape[0]
+    assert wg[0].shape == (I, d // 2) and wu[0].shape == (I, d // 2) and wd[0].shape == (d, I // 2)
+    y = np.empty((n, d), dtype=np.float32)
+    h = np.empty((n, I), dtype=np.float32) if want_h else None
+    hq = np.zeros((n, I // 2), dtype=np.uint8) if want_h else None
+    hs = np.zeros((n, I // 32), dtype=np.uint8) if want_h else None
+    ws = [np.ascontiguousarray(m, dtype=np.uint8) for pair in (wg, wu, wd) for m in pair]
+    _load().oracle_expert_ffn(_ptr(a), n, d, I, *[_ptr(m) for m in ws], act_fmt,
+                              _ptr(h), _ptr(hq), _ptr(hs), _ptr(y))
+    if want_h:
+        return y, (h, hq, hs)
+    return y
+
+
+def combine(y_perm: np.ndarray, rows: np.ndarray, w: np.ndarray, tokens: np.ndarray) -> np.ndarray:
+    y_perm = np.ascontiguousarray(y_perm, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    k = w.shape[1]
+    d = y_perm.shape[1]
+    y = np.empty((tokens.shape[0], d), dtype=np.float32)
+    _load().oracle_combine(_ptr(y_perm), _ptr(rows.reshape(-1)), _ptr(w), tokens.shape[0], _ptr(tokens), k, d, _ptr(y))
+    return y
+
+
+# ------------------------------------------------------------------ the layer
+
+def moe_layer(x_bits: np.ndarray, W_r: np.ndarray, b: Optional[np.ndarray], k: int,
+              expert_weights: Callable[[int], Dict[str, tuple]], act_fmt: int,
+              tokens: Optional[Sequence[int]] = None, want_intermediates: bool = False) -> Dict:
+    """The whole layer: routing and permutation for every token, expert outputs and the
+    weighted sum for ``tokens`` (all tokens when None).
+
+    ``expert_weights(e)`` returns {"gate": (q, s), "up": (q, s), "down": (q, s)} for expert e
+    (MXFP4 packed by this oracle's own packer), so only the experts the sampled tokens
+    touch need to exist on the host.
+    """
+    T, d = x_bits.shape
+    E = W_r.shape[0]
+    logits = router_logits(x_bits, W_r, b)
+    ids, w = topk_softmax(logits, k)
+    counts, offsets, perm_token, inv_pos = permute(ids, E)
+    tok = np.arange(T, dtype=np.int32) if tokens is None else np.asarray(tokens, dtype=np.int32)
+    a_tok = activation_rows(x_bits[tok], act_fmt)
+    # expert outputs of the sampled pairs, grouped by expert
+    pair_rows = {}  # (t, j) -> row in y_sel
+    y_sel_rows = []
+    h_rows = {}
+    by_expert: Dict[int, list] = {}
+    tok_index = {int(t): n for n, t in enumerate(tok)}
+    for t in tok:
+        for j in range(k):
+            by_expert.setdefault(int(ids[t, j]), []).append((int(t), j))
+    n_rows = 0
+    y_blocks = []
+    for e in sorted(by_expert):
+        pairs = by_expert[e]
+        a = np.stack([a_tok[tok_index[t]] for (t, _) in pairs])
+        wts = expert_weights(e)
+        if want_intermediates:
+            y_e, (h_e, hq_e, hs_e) = expert_ffn(a, wts["gate"], wts["up"], wts["down"], act_fmt, want_h=True)
+        else:
+            y_e = expert_ffn(a, wts["gate"], wts["up"], wts["down"], act_fmt)
+        for n, (t, j) in enumerate(pairs):
+            pair_rows[(t, j)] = n_rows + n
+            if want_intermediates:
+                h_rows[(t, j)] = (h_e[n], hq_e[n], hs_e[n])
+        n_rows += len(pairs)
+        y_blocks.append(y_e)
+    y_perm_sel = np.concatenate(y_blocks, axis=0) if y_blocks else np.zeros((0, d), np.float32)
+    rows_full = np.zeros((T, k), dtype=np.int32)
+    for (t, j), r in pair_rows.items():
+        rows_full[t, j] = r
+    y = combine(y_perm_sel, rows_full, w, tok)
+    out = dict(logits=logits, ids=ids, w=w, counts=counts, offsets=offsets, perm_token=perm_token,
+               inv_pos=inv_pos, tokens=tok, y=y)
+    if want_intermediates:
+        out["y_perm"] = {pair: y_perm_sel[r] for pair, r in pair_rows.items()}
+        out["h"] = h_rows
+        out["a"] = a_tok
+    return out
