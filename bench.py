@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE expert-FFN layer on GB300.
+
+Default workload (N=1): decode, batch 1 -- T=1 token per layer call, d=8192, E=128, top-8,
+I=2048, MXFP4 expert weights, bf16 activations; one step = one whole layer call (route ->
+permute -> gate/up+SwiGLU -> down -> weighted sum) on the next of 1000 seeded tokens; four
+independent layer copies (13.7 GB of expert weights) are rotated so that L2 cannot carry experts
+from one step to the next.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead (bounded
+sample, host cores).  Under torchrun each rank runs its own replica (weak scaling, no data-path
+collective); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/sec on 1 GB300 + % of roofline (HBM BW decode, FP4 peak prefill)"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense FP4 : dense bf16 nominal ratio on GB300 (6x)
+N_LAYER_COPIES = 4
+
+
+# ------------------------------------------------------------------ byte / flop model
+# Per-expert sizes as the Muse Spark Open explainer models them (sections 10-13): an expert is
+# three matrices; reading it costs its packed bytes, computing one token costs 2 flops per
+# weight.  MXFP4 stores 4 bits per weight plus one byte per 32 weights (4.25 bits).
+
+def matrix_bytes(rows: int, K: int, bits_per_weight: float = 4.25) -> float:
+    return rows * K * bits_per_weight / 8.0
+
+
+def expert_bytes(d: int, I: int, bits_per_weight: float = 4.25) -> float:
+    return 3 * matrix_bytes(I, d, bits_per_weight)
+
+
+def up_bytes_per_expert(d: int, I: int) -> float:
+    return 2 * matrix_bytes(I, d)
+
+
+def down_bytes_per_expert(d: int, I: int) -> float:
+    return matrix_bytes(d, I)
+
+
+def flops_per_token_expert(d: int, I: int) -> float:
+    return 2.0 * 3 * d * I
+
+
+def read_time_us(nbytes: float, bw_bytes_per_s: float) -> float:
+    return nbytes / bw_bytes_per_s * 1e6
+
+
+def crossover_tokens(read_us: float, compute_us_per_token: float) -> float:
+    return read_us / compute_us_per_token
+
+
+def layer_algorithmic_bytes(d: int, I: int, E: int, T: int, n_active: float) -> float:
+    """Touched experts + router weights and bias + x in + y out."""
+    return n_active * expert_bytes(d, I) + E * d * 4 + E * 4 + 2 * T * d * 2
+
+
+# ------------------------------------------------------------------ environment helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        hbm = p.get("hbm_gbs") or p.get("hbm_GBps") or p.get("hbm")
+        bf16 = p.get("bf16_tflops")
+        bf16s = p.get("bf16_tflops_sustained", bf16)
+        if hbm:
+            return dict(hbm_gbs=float(hbm), bf16_tflops=float(bf16 or FALLBACK_BF16_TFLOPS),
+                        bf16_tflops_sustained=float(bf16s or FALLBACK_BF16_TFLOPS), source="measured")
+    return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS, bf16_tflops_sustained=1700.0,
+                source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(profile_name: str, kernel_sources):
+    """dram bytes per launch recorded in profiles/<profile_name> for the kernel, or None when
+    the summary is missing or the kernel's sources changed since the capture."""
+    path = os.path.join(ROOT, "profiles", profile_name)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch")):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_hash") != source_hash(kernel_sources):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args, cfg, rank, world, local):
+    import numpy as np
+    import torch
+
+    from bit_expert_ffn_moe_gb300 import binding as B
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    from bit_expert_ffn_moe_gb300.layer import DeviceLayer, make_workspace
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    B.load(build_if_missing=False)
+    fmt = B.MOE_ACT_BF16 if args.fmt == "bf16" else B.MOE_ACT_MXFP4
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    n_calls = max(cfg.calls, 1)
+
+    layers = [DeviceLayer(cfg, device=dev, layer=i + 1000 * rank, mma_scales=(fmt == B.MOE_ACT_MXFP4))
+              for i in range(args.layers)]
+    # all seeded inputs resident in HBM before timing
+    xs_host = np.stack([IN.make_x(cfg, call=(c + rank * 100000) % (1 << 20)) for c in range(min(n_calls, 1000))])
+    xs = torch.from_numpy(xs_host.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+    n_x = xs.shape[0]
+    ws = make_workspace(T, d, E, k, I, fmt, dev)
+    y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((args.steps, T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((args.steps, T, k), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s, st, record_routing=True):
+        L = layers[s % len(layers)]
+        B.moe_layer_forward(xs[s % n_x], L.W_r, L.b, T, d, E, k, I, L.weights, fmt, y,
+                            ids[s] if record_routing else None, wts[s] if record_routing else None, ws,
+                            stream=st.cuda_stream)
+
+    # warm-up (eager), then capture the K timed steps in one CUDA graph
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            step(s % args.steps, stream)
+    stream.synchronize()
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for s in range(args.steps):
+                step(s, stream)
+        graph.replay()  # one untimed replay
+        stream.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        start.record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            with torch.cuda.stream(stream):
+                for s in range(args.steps):
+                    step(s, stream)
+        end.record(stream)
+        end.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_total = start.elapsed_time(end)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    status = B.moe_get_device_status(ws, stream=stream.cuda_stream)
+    if status != B.MOE_OK:
+        raise RuntimeError("device status after timed region: %s" % B.status_string(status))
+    yf = y.float()
+    if not torch.isfinite(yf).all() or torch.count_nonzero(yf) == 0:
+        raise RuntimeError("refusing to record: output is non-finite or all zero")
+    ids_h = ids.cpu().numpy()
+    counts_ok = all(np.bincount(ids_h[s].reshape(-1), minlength=E).sum() == T * k for s in range(args.steps))
+    if not counts_ok:
+        raise RuntimeError("refusing to record: routing counts do not sum to T*k")
+    n_active = [len(np.unique(ids_h[s])) for s in range(args.steps)]
+
+    tokens = T * args.steps * world
+    value = tokens / (ms_total / 1e3)
+    ms_per_step = ms_total / args.steps
+    pk = peaks()
+    bw = pk["hbm_gbs"] * 1e9
+    mean_active = float(np.mean(n_active))
+    layer_bytes = layer_algorithmic_bytes(d, I, E, T, mean_active)
+
+    # ---- dominant kernel, timed alone with events on its own stream (same inputs, same layers)
+    roof = kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk)
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = end_to_end(args, cfg, layers, xs_host, fmt, dev, stream)
+
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(fmt), "data": "synthetic",
+        "config": {"workload": cfg.note, "T": T, "d": d, "E": E, "k": k, "I": I, "act": args.fmt,
+                   "layer_copies_rotated": len(layers),
+                   "l2": "inputs larger than L2: %d layer copies, %.1f GB of expert weights rotated"
+                         % (len(layers), len(layers) * E * expert_bytes(d, I) / 1e9),
+                   "cuda_graph": graph is not None, "parallelism": "replicas" if world > 1 else "single GPU"},
+        "layer_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": layer_bytes,
+                           "achieved_GBps": round(layer_bytes / (ms_per_step / 1e3) / 1e9, 1),
+                           "peak_GBps": pk["hbm_gbs"], "frac": round(layer_bytes / (ms_per_step / 1e3) / bw, 4),
+                           "peak_source": pk["source"], "mean_active_experts": round(mean_active, 2)},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step(fmt, T, d, E, k) * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed": round(t_wall, 4),
+    }
+    return out
+
+
+def dtype_name(fmt):
+    return "mxfp4 weights x bf16 activations, fp32 accumulate" if fmt == 0 else "mxfp4 x mxfp4, fp32 accumulate"
+
+
+def launches_per_step(fmt, T, d, E, k):
+    if fmt == 0:
+        return 3 if T <= 8 else 7
+    return 9
+
+
+def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
+    """Average duration of the dominant kernel over the same steps, timed with CUDA events on the
+    stream it is launched on, and its algorithmic bytes per launch."""
+    import numpy as np
+    import torch
+
+    from bit_expert_ffn_moe_gb300 import binding as B
+    from bit_expert_ffn_moe_gb300.layer import make_workspace
+
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    P = T * k
+    ws = make_workspace(T, d, E, k, I, fmt, dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    ids, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts, offsets, perm, inv = torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(P, **i32), \
+        torch.empty(P, **i32)
+    h = torch.empty((P, I), dtype=torch.bfloat16, device=dev)
+    n = min(args.steps, 200)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    active = []
+    if fmt != B.MOE_ACT_BF16:
+        return None
+    st = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for s in range(n + 3):
+            L = layers[s % len(layers)]
+            x = xs[s % xs.shape[0]]
+            B.moe_route(x, L.W_r, L.b, T, d, E, k, ids, w, ws, stream=st)
+            B.moe_permute(x, ids, T, d, E, k, fmt, counts, offsets, perm, inv, None, None, ws, stream=st)
+            if s >= 3:
+                evs[s - 3][0].record(stream)
+            B.moe_expert_up_swiglu(x, None, None, fmt, perm, offsets, T, d, E, k, I, L.weights, h, None, ws,
+                                   stream=st)
+            if s >= 3:
+                evs[s - 3][1].record(stream)
+                active.append(torch.count_nonzero(counts))
+    stream.synchronize()
+    dur = [a.elapsed_time(b) for a, b in evs]
+    n_act = float(np.mean([int(a.item()) for a in active]))
+    per_launch = n_act * up_bytes_per_expert(d, I) + T * d * 2 + P * I * 2
+    avg_ms = float(np.mean(dur))
+    achieved = per_launch / (avg_ms / 1e3) / 1e9
+    traffic = ncu_traffic("gemv_up_decode.md", ["bit_expert_ffn_moe_gb300/csrc/gemv.cu",
+                                                "bit_expert_ffn_moe_gb300/csrc/common.cuh"])
+    return {"kernel": "gemv_up_kernel (gate/up + SwiGLU, decode)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": per_launch, "avg_launch_us": round(avg_ms * 1e3, 3),
+            "launches_timed": n, "peak_source": pk["source"] + " (HBM copy bandwidth)"}
+
+
+def end_to_end(args, cfg, layers, xs_host, fmt, dev, stream):
+    """Same metric through the C ABI with host buffers: per step, copy x from pinned host memory,
+    run the layer, copy y back; all inside the timed region."""
+    import numpy as np
+    import torch
+
+    from bit_expert_ffn_moe_gb300 import binding as B
+    from bit_expert_ffn_moe_gb300.layer import make_workspace
+
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    n = min(args.steps, 500)
+    x_pin = torch.from_numpy(xs_host[:n].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    y_pin = torch.empty((n, T, d), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    y_dev = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    ws = make_workspace(T, d, E, k, I, fmt, dev)
+    st = stream.cuda_stream
+
+    def one(s):
+        L = layers[s % len(layers)]
+        x_dev.copy_(x_pin[s % x_pin.shape[0]], non_blocking=True)
+        B.moe_layer_forward(x_dev, L.W_r, L.b, T, d, E, k, I, L.weights, fmt, y_dev, None, None, ws, stream=st)
+        y_pin[s].copy_(y_dev, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for s in range(3):
+            one(s)
+    stream.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0 = time.perf_counter()
+        start.record(stream)
+        for s in range(n):
+            one(s)
+        end.record(stream)
+        end.synchronize()
+        wall = time.perf_counter() - t0
+    ms = start.elapsed_time(end)
+    return {"value": round(T * n / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": T * d * 2,
+            "d2h_bytes_per_step": T * d * 2, "steps": n, "wall_tokens_per_s": round(T * n / wall, 1),
+            "note": "eager C-ABI calls per step (no graph): pinned H2D of x, layer, D2H of y"}
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def oracle_sample(args, cfg, n_tokens):
+    """Time the CPU oracle (as it stands) on n_tokens decode tokens: routing, dequantisation of
+    the touched experts, expert GEMVs and the weighted sum.  Weight generation is untimed."""
+    import numpy as np
+
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    from oracle import oracle as O
+
+    threads = len(os.sched_getaffinity(0))
+    layer_seed = cfg.seed + 7919 * 1
+    W_r, b = IN.make_router(cfg)
+    rng = np.random.default_rng([cfg.seed, 77, 1])
+    W_r = (rng.standard_normal(W_r.shape) / np.sqrt(cfg.d)).astype(np.float32)
+    shapes = IN.expert_matrix_shapes(cfg)
+    cache = {}
+
+    def weights(e):
+        if e not in cache:
+            out = {}
+            for name, tid in (("gate", IN.TENSOR_GATE), ("up", IN.TENSOR_UP), ("down", IN.TENSOR_DOWN)):
+                rows, K = shapes[tid]
+                out[name] = O.mxfp4_pack(IN.synth_weights(layer_seed, tid, e, rows, K, cfg.weight_std))
+            cache[e] = out
+        return cache[e]
+
+    xs = [IN.make_x(cfg, call=c) for c in range(n_tokens)]
+    # pre-generate the experts the sample touches (untimed: input generation)
+    for xb in xs:
+        ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
+        for e in np.unique(ids):
+            weights(int(e))
+    t0 = time.perf_counter()
+    for xb in xs:
+        O.moe_layer(xb, W_r, b, cfg.k, weights, O.ACT_BF16 if args.fmt == "bf16" else O.ACT_MXFP4)
+    dt = time.perf_counter() - t0
+    return dict(value=round(cfg.T * n_tokens / dt, 3), unit=UNIT, cores=threads, kind="oracle",
+                sample="%d layer calls of T=%d (full routing, all %d touched experts per call, fp64 oracle), "
+                       "weights pre-generated" % (n_tokens, cfg.T, cfg.k), seconds=round(dt, 2))
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
+    from oracle import oracle as O
+    O.build()
+    # each step: one layer call of the workload on the CPU oracle; bounded so the run ends in
+    # a few minutes (at most args.ref_budget seconds of timed oracle work)
+    probe = oracle_sample(args, cfg, 1)
+    per_step = cfg.T / max(probe["value"], 1e-9)
+    n = max(1, min(args.steps, int(args.ref_budget / max(per_step, 1e-6))))
+    res = oracle_sample(args, cfg, n)
+    out = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": n,
+           "warmup": 1, "ms_per_step": round(1e3 * cfg.T / res["value"], 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+           "config": {"workload": cfg.note, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+                      "act": args.fmt},
+           "impl": "reference",
+           "cpu_baseline": {"value": res["value"], "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                            "sample": res["sample"] + "; %d of the %d requested steps" % (n, args.steps)},
+           "e2e": {"value": res["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="decode")
+    ap.add_argument("--fmt", choices=["bf16", "mxfp4"], default=None)
+    ap.add_argument("--layers", type=int, default=N_LAYER_COPIES)
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-tokens", type=int, default=4)
+    ap.add_argument("--ref-budget", type=float, default=90.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    cfg = IN.CONFIGS[args.config]
+    if args.fmt is None:
+        args.fmt = "bf16" if cfg.T <= 8 else "mxfp4"
+    rank, world, local = dist_env()
+
+    if args.impl == "reference":
+        out = run_reference(args, cfg, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return
+
+    os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
+    out = run_gpu(args, cfg, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = oracle_sample(args, cfg, args.cpu_sample_tokens)
+        out["cpu_baseline"] = {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

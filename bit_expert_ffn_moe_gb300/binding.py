@@ -1,0 +1,217 @@
+"""Thin ctypes binding of libmoe_gb300.so (include/moe.h).
+
+Argument marshalling only: every function has the C entry point's name and arguments,
+accepts torch tensors (device memory) or raw integer addresses for the pointer arguments,
+runs on torch's current CUDA stream unless ``stream`` is given, and raises ``MoeError`` for a
+non-OK status.  All work happens in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED_SHAPE = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_TIMEOUT = 5
+MOE_ERR_DEVICE = 6
+
+MOE_ACT_BF16 = 0
+MOE_ACT_MXFP4 = 1
+
+# every entry point declared in include/moe.h
+EXPORTED = (
+    "moe_status_string", "moe_abi_version", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
+    "moe_mxfp4_scales_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
+    "moe_get_device_status", "moe_route", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
+    "moe_layer_forward", "moe_synth_weights",
+)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__("%s failed: %s" % (fn, status_string(status)))
+
+
+class moe_expert_weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s", "gate_s_mma", "up_s_mma", "down_s_mma")]
+
+
+_lib = None
+P = ctypes.c_void_p
+I32, I64, U32, U64 = ctypes.c_int, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
+SZ = ctypes.c_size_t
+WP = ctypes.POINTER(moe_expert_weights)
+
+_SIGS = {
+    "moe_status_string": (ctypes.c_char_p, [I32]),
+    "moe_abi_version": (I32, []),
+    "moe_mxfp4_pack": (I32, [P, I64, I64, P, P, P]),
+    "moe_mxfp4_unpack": (I32, [P, P, I64, I64, P, P]),
+    "moe_mxfp4_mma_scale_bytes": (SZ, [I64, I64]),
+    "moe_mxfp4_scales_to_mma": (I32, [P, I64, I64, P, P]),
+    "moe_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32]),
+    "moe_padded_rows": (I64, [I32, I32, I32]),
+    "moe_workspace_init": (I32, [P, SZ, P]),
+    "moe_get_device_status": (I32, [P, P, ctypes.POINTER(I32)]),
+    "moe_route": (I32, [P, P, P, I32, I32, I32, I32, P, P, P, SZ, P]),
+    "moe_permute": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P]),
+    "moe_expert_up_swiglu": (I32, [P, P, P, I32, P, P, I32, I32, I32, I32, I32, WP, P, P, P, SZ, P]),
+    "moe_expert_down": (I32, [P, P, I32, P, P, I32, I32, I32, I32, I32, WP, P, P, SZ, P]),
+    "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
+    "moe_layer_forward": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, SZ, P]),
+    "moe_synth_weights": (I32, [U64, U32, U32, U32, I64, I64, ctypes.c_float, P, P]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load the CUDA library (building it in-tree first if needed).  Raises if unavailable."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError("libmoe_gb300.so is not built (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _p(t) -> Optional[int]:
+    """Pointer argument: a torch tensor (its data pointer), an int address, or None."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s, gate_s_mma=None, up_s_mma=None,
+                          down_s_mma=None) -> moe_expert_weights:
+    return moe_expert_weights(*[_p(t) for t in (gate_q, gate_s, up_q, up_s, down_q, down_s, gate_s_mma, up_s_mma,
+                                                down_s_mma)])
+
+
+# ------------------------------------------------------------------ entry points
+
+def moe_abi_version() -> int:
+    return load().moe_abi_version()
+
+
+def moe_mxfp4_pack(w, rows, K, q, s, stream=None):
+    _check("moe_mxfp4_pack", load().moe_mxfp4_pack(_p(w), rows, K, _p(q), _p(s), _stream(stream)))
+
+
+def moe_mxfp4_unpack(q, s, rows, K, w, stream=None):
+    _check("moe_mxfp4_unpack", load().moe_mxfp4_unpack(_p(q), _p(s), rows, K, _p(w), _stream(stream)))
+
+
+def moe_mxfp4_mma_scale_bytes(rows, K) -> int:
+    return int(load().moe_mxfp4_mma_scale_bytes(rows, K))
+
+
+def moe_mxfp4_scales_to_mma(s, rows, K, s_mma, stream=None):
+    _check("moe_mxfp4_scales_to_mma", load().moe_mxfp4_scales_to_mma(_p(s), rows, K, _p(s_mma), _stream(stream)))
+
+
+def moe_workspace_size(T, d, E, k, I, fmt) -> int:
+    return int(load().moe_workspace_size(T, d, E, k, I, fmt))
+
+
+def moe_padded_rows(T, k, E) -> int:
+    return int(load().moe_padded_rows(T, k, E))
+
+
+def moe_workspace_init(ws, ws_bytes=None, stream=None):
+    nbytes = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("moe_workspace_init", load().moe_workspace_init(_p(ws), nbytes, _stream(stream)))
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    out = I32(0)
+    _check("moe_get_device_status", load().moe_get_device_status(_p(ws), _stream(stream), ctypes.byref(out)))
+    return out.value
+
+
+def _ws_bytes(ws, ws_bytes):
+    if ws is None:
+        return 0
+    return ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+
+
+def moe_route(x, W_r, b, T, d, E, k, ids, w, ws, ws_bytes=None, stream=None):
+    _check("moe_route", load().moe_route(_p(x), _p(W_r), _p(b), T, d, E, k, _p(ids), _p(w), _p(ws),
+                                         _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_permute(x, ids, T, d, E, k, fmt, counts, offsets, perm_token, inv_pos, xa, xa_s, ws, ws_bytes=None,
+                stream=None):
+    _check("moe_permute", load().moe_permute(_p(x), _p(ids), T, d, E, k, fmt, _p(counts), _p(offsets),
+                                             _p(perm_token), _p(inv_pos), _p(xa), _p(xa_s), _p(ws),
+                                             _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_expert_up_swiglu(x, xa, xa_s, fmt, perm_token, offsets, T, d, E, k, I, W: moe_expert_weights, h, h_s, ws,
+                         ws_bytes=None, stream=None):
+    _check("moe_expert_up_swiglu",
+           load().moe_expert_up_swiglu(_p(x), _p(xa), _p(xa_s), fmt, _p(perm_token), _p(offsets), T, d, E, k, I,
+                                       ctypes.byref(W), _p(h), _p(h_s), _p(ws), _ws_bytes(ws, ws_bytes),
+                                       _stream(stream)))
+
+
+def moe_expert_down(h, h_s, fmt, perm_token, offsets, T, d, E, k, I, W: moe_expert_weights, y_perm, ws,
+                    ws_bytes=None, stream=None):
+    _check("moe_expert_down",
+           load().moe_expert_down(_p(h), _p(h_s), fmt, _p(perm_token), _p(offsets), T, d, E, k, I, ctypes.byref(W),
+                                  _p(y_perm), _p(ws), _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_combine(y_perm, inv_pos, w, T, k, d, y, stream=None):
+    _check("moe_combine", load().moe_combine(_p(y_perm), _p(inv_pos), _p(w), T, k, d, _p(y), _stream(stream)))
+
+
+def moe_layer_forward(x, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, y, ids, w, ws, ws_bytes=None,
+                      stream=None):
+    _check("moe_layer_forward",
+           load().moe_layer_forward(_p(x), _p(W_r), _p(b), T, d, E, k, I, ctypes.byref(W), fmt, _p(y), _p(ids),
+                                    _p(w), _p(ws), _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_synth_weights(seed, tensor_id, expert_first, n_experts, rows, K, c, out, stream=None):
+    _check("moe_synth_weights", load().moe_synth_weights(seed, tensor_id, expert_first, n_experts, rows, K,
+                                                         float(c), _p(out), _stream(stream)))

@@ -1,0 +1,310 @@
+// api.cu -- the extern "C" entry points declared in include/moe.h: argument checks, workspace
+// carving and the launch sequence of each layer step.  No entry point allocates device memory.
+#include <stdio.h>
+
+#include "common.cuh"
+
+using namespace moe;
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The kernels are compiled for sm_103a only; refuse other devices before launching.
+moe_status check_device() {
+    static int verdict[64] = {0};  // 0 unknown, 1 ok, 2 bad
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && verdict[dev] == 1) return MOE_OK;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const bool ok = (major == 10 && minor == 3);
+    if (dev >= 0 && dev < 64) verdict[dev] = ok ? 1 : 2;
+    return ok ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                               \
+    do {                                            \
+        moe_status _s = (expr);                     \
+        if (_s != MOE_OK) return _s;                \
+    } while (0)
+#define MOE_CUDA(expr) MOE_TRY(from_cuda(expr))
+
+moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
+    if (T < 0 || d <= 0 || E <= 0 || k <= 0 || I <= 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (I % (fmt == MOE_ACT_MXFP4 ? 128 : 32) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)T * k > (int64_t)1 << 30 || (int64_t)T * d > ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+moe_status check_ws(void* ws, size_t ws_bytes, const WsLayout& L) {
+    if (ws == nullptr || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status check_weights(const moe_expert_weights* W, moe_act_fmt fmt, bool need_up, bool need_down) {
+    if (W == nullptr) return MOE_ERR_INVALID_ARG;
+    if (need_up) {
+        if (!W->gate_q || !W->gate_s || !W->up_q || !W->up_s) return MOE_ERR_INVALID_ARG;
+        if (!aligned(W->gate_q, 16) || !aligned(W->up_q, 16)) return MOE_ERR_INVALID_ARG;
+        if (fmt == MOE_ACT_MXFP4 && (!W->gate_s_mma || !W->up_s_mma || !aligned(W->gate_s_mma, 16) ||
+                                     !aligned(W->up_s_mma, 16)))
+            return MOE_ERR_INVALID_ARG;
+    }
+    if (need_down) {
+        if (!W->down_q || !W->down_s || !aligned(W->down_q, 16)) return MOE_ERR_INVALID_ARG;
+        if (fmt == MOE_ACT_MXFP4 && (!W->down_s_mma || !aligned(W->down_s_mma, 16))) return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
+
+// route (+ permutation when fused) into the given buffers
+moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                     int32_t* ids, float* w, void* ws, const WsLayout& L, cudaStream_t st, bool pdl) {
+    float* logits = reinterpret_cast<float*>(at(ws, L.logits));
+    MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
+    MOE_CUDA(launch_topk(logits, T, E, k, ids, w, st, true));
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+        case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+int moe_abi_version(void) { return kAbiVersion; }
+
+// ---------------------------------------------------------------- MXFP4 helpers
+
+moe_status moe_mxfp4_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, moe_stream_t stream) {
+    if (rows < 0 || K <= 0 || K % 32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !q || !s || !aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_pack(w, rows, K, q, s, (cudaStream_t)stream));
+}
+
+moe_status moe_mxfp4_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w,
+                            moe_stream_t stream) {
+    if (rows < 0 || K <= 0 || K % 32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !q || !s || !aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_unpack(q, s, rows, K, w, (cudaStream_t)stream));
+}
+
+size_t moe_mxfp4_mma_scale_bytes(int64_t rows, int64_t K) {
+    if (rows <= 0 || K <= 0) return 0;
+    return mma_scale_bytes(rows, K);
+}
+
+moe_status moe_mxfp4_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma, moe_stream_t stream) {
+    if (rows <= 0 || K <= 0 || rows % 128 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!s || !s_mma) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_scales_to_mma(s, rows, K, s_mma, (cudaStream_t)stream));
+}
+
+// ---------------------------------------------------------------- workspace
+
+size_t moe_workspace_size(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
+    if (check_shape(T, d, E, k, I, fmt) != MOE_OK) return 0;
+    return ws_layout(T, d, E, k, I, fmt).total;
+}
+
+int64_t moe_padded_rows(int T, int k, int E) {
+    if (T < 0 || k <= 0 || E <= 0) return 0;
+    return padded_rows(T, k, E);
+}
+
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream) {
+    if (ws == nullptr || !aligned(ws, 256) || ws_bytes < sizeof(Ctrl)) return MOE_ERR_WORKSPACE;
+    MOE_TRY(check_device());
+    return from_cuda(cudaMemsetAsync(ws, 0, sizeof(Ctrl), (cudaStream_t)stream));
+}
+
+moe_status moe_get_device_status(void* ws, moe_stream_t stream, moe_status* out) {
+    if (ws == nullptr || out == nullptr || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int host = 0;
+    MOE_CUDA(cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, st));
+    MOE_CUDA(cudaMemsetAsync(ws, 0, sizeof(int), st));
+    MOE_CUDA(cudaStreamSynchronize(st));
+    *out = (moe_status)host;
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- layer steps
+
+moe_status moe_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k, int32_t* ids,
+                     float* w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_shape(T, d, E, k, 32, MOE_ACT_BF16));
+    if (T == 0) return MOE_OK;
+    if (!x || !W_r || !ids || !w || !aligned(x, 16) || !aligned(W_r, 16)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, 32, MOE_ACT_BF16);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    MOE_TRY(check_device());
+    return run_route(x, W_r, b, T, d, E, k, ids, w, ws, L, (cudaStream_t)stream, false);
+}
+
+moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int E, int k, moe_act_fmt fmt,
+                       int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_pos, uint8_t* xa,
+                       uint8_t* xa_s, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_shape(T, d, E, k, 128, fmt));
+    if (!ids || !counts || !offsets || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
+    if (fmt == MOE_ACT_MXFP4 && (!x || !xa || !xa_s || !aligned(x, 16) || !aligned(xa, 16))) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, 128, fmt);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    MOE_TRY(check_device());
+    cudaStream_t st = (cudaStream_t)stream;
+    PlanView plan = plan_view(ws, L, E);
+    MOE_CUDA(launch_permute(ids, T, E, k, counts, offsets, perm_token, inv_pos, plan, st, false));
+    if (fmt == MOE_ACT_MXFP4)
+        MOE_CUDA(launch_act_quant_gather(x, T, d, E, k, offsets, perm_token, plan, L.pad_rows,
+                                         reinterpret_cast<uint8_t*>(at(ws, L.xq)),
+                                         reinterpret_cast<uint8_t*>(at(ws, L.xs)), xa, xa_s, st, true));
+    return MOE_OK;
+}
+
+moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint8_t* xa_s, moe_act_fmt fmt,
+                                const int32_t* perm_token, const int32_t* offsets, int T, int d, int E, int k, int I,
+                                const moe_expert_weights* W, void* h, uint8_t* h_s, void* ws, size_t ws_bytes,
+                                moe_stream_t stream) {
+    MOE_TRY(check_shape(T, d, E, k, I, fmt));
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(W, fmt, true, false));
+    if (!offsets || !h) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, I, fmt);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    MOE_TRY(check_device());
+    cudaStream_t st = (cudaStream_t)stream;
+    PlanView plan = plan_view(ws, L, E);
+    if (fmt == MOE_ACT_BF16) {
+        if (!x || !perm_token || !aligned(x, 16)) return MOE_ERR_INVALID_ARG;
+        return from_cuda(launch_gemv_up(x, perm_token, offsets, plan, T, d, E, k, I, W,
+                                        static_cast<uint16_t*>(h), st, false));
+    }
+    if (!xa || !xa_s || !h_s || !aligned(xa, 16) || !aligned(h, 16)) return MOE_ERR_INVALID_ARG;
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
+    return from_cuda(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, static_cast<uint8_t*>(h),
+                                    h_s, &ctrl->status, st, false));
+}
+
+moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, const int32_t* perm_token,
+                           const int32_t* offsets, int T, int d, int E, int k, int I, const moe_expert_weights* W,
+                           uint16_t* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_shape(T, d, E, k, I, fmt));
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(W, fmt, false, true));
+    if (!h || !offsets || !y_perm || !aligned(h, 16)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, I, fmt);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    MOE_TRY(check_device());
+    cudaStream_t st = (cudaStream_t)stream;
+    PlanView plan = plan_view(ws, L, E);
+    if (fmt == MOE_ACT_BF16) {
+        if (!perm_token) return MOE_ERR_INVALID_ARG;
+        return from_cuda(launch_gemv_down(static_cast<const uint16_t*>(h), perm_token, offsets, plan, nullptr, nullptr,
+                                          T, d, E, k, I, W, y_perm, nullptr, st, false));
+    }
+    if (!h_s) return MOE_ERR_INVALID_ARG;
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
+    return from_cuda(launch_umma_down(static_cast<const uint8_t*>(h), h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W,
+                                      y_perm, &ctrl->status, st, false));
+}
+
+moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d, uint16_t* y,
+                       moe_stream_t stream) {
+    if (T < 0 || k <= 0 || k > kMaxK || d <= 0 || d % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!y_perm || !inv_pos || !w || !y || !aligned(y_perm, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_combine(y_perm, inv_pos, w, T, k, d, y, (cudaStream_t)stream, false));
+}
+
+moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k, int I,
+                             const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids, float* w,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_shape(T, d, E, k, I, fmt));
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(W, fmt, true, true));
+    if (!x || !W_r || !y || !aligned(x, 16) || !aligned(W_r, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, I, fmt);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    MOE_TRY(check_device());
+    cudaStream_t st = (cudaStream_t)stream;
+    PlanView plan = plan_view(ws, L, E);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
+    int32_t* ids_b = ids ? ids : reinterpret_cast<int32_t*>(at(ws, L.ids));
+    float* w_b = w ? w : reinterpret_cast<float*>(at(ws, L.w));
+    int32_t* counts = reinterpret_cast<int32_t*>(at(ws, L.counts));
+    int32_t* offsets = reinterpret_cast<int32_t*>(at(ws, L.offsets));
+    int32_t* perm = reinterpret_cast<int32_t*>(at(ws, L.perm));
+    int32_t* inv = reinterpret_cast<int32_t*>(at(ws, L.inv));
+
+    if (fmt == MOE_ACT_BF16) {
+        if (route_decode_supported(T, d, E, k)) {
+            MOE_CUDA(launch_route_decode(x, W_r, b, T, d, E, k, reinterpret_cast<float*>(at(ws, L.logits)), ids_b, w_b,
+                                         counts, offsets, perm, inv, plan, ctrl, st, true));
+        } else {
+            MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
+            MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
+        }
+        uint16_t* h = reinterpret_cast<uint16_t*>(at(ws, L.h));
+        MOE_CUDA(launch_gemv_up(x, perm, offsets, plan, T, d, E, k, I, W, h, st, true));
+        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, ids_b, w_b, T, d, E, k, I, W, nullptr, y, st, true));
+        return MOE_OK;
+    }
+    MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
+    MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
+    uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
+    uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
+    MOE_CUDA(launch_act_quant_gather(x, T, d, E, k, offsets, perm, plan, L.pad_rows,
+                                     reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
+                                     xa, xa_s, st, true));
+    uint8_t* h = reinterpret_cast<uint8_t*>(at(ws, L.h));
+    uint8_t* h_s = reinterpret_cast<uint8_t*>(at(ws, L.h_s));
+    uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
+    MOE_CUDA(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, h, h_s, &ctrl->status, st, true));
+    MOE_CUDA(launch_umma_down(h, h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, y_perm, &ctrl->status, st, true));
+    MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- synthetic inputs
+
+moe_status moe_synth_weights(uint64_t seed, uint32_t tensor_id, uint32_t expert_first, uint32_t n_experts,
+                             int64_t rows, int64_t K, float c, float* out, moe_stream_t stream) {
+    if (seed >= (1ull << 32) || tensor_id >= 256 || rows < 0 || K < 0) return MOE_ERR_INVALID_ARG;
+    if ((uint64_t)expert_first + n_experts > (1ull << 24)) return MOE_ERR_INVALID_ARG;
+    if (rows * K * (int64_t)n_experts == 0) return MOE_OK;
+    if (!out) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_synth(seed, tensor_id, expert_first, n_experts, rows, K, c, out, (cudaStream_t)stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,224 @@
+// common.cuh -- shared device helpers and the workspace layout of the MoE layer library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kPadRows = 128;   // expert row groups of the MXFP4 path start at multiples of this
+constexpr int kTokTile = 128;   // token tile (MMA N) of the tcgen05 grouped GEMMs
+
+// ------------------------------------------------------------------ workspace layout
+// Control block (first 256 bytes): status word, decode-route ticket.
+struct Ctrl {
+    int status;
+    unsigned route_ticket;
+    int pad[62];
+};
+
+// Per-call plan written by the permutation and read by the expert kernels (int32 words).
+struct PlanView {
+    int32_t* counts;       // [E]   scratch counts (zeroed by the count pass)
+    int32_t* pad_offsets;  // [E+1] padded row start of each expert (multiples of kPadRows)
+    int32_t* ttile_prefix; // [E+1] exclusive prefix of ceil(count / kTokTile)
+    int32_t* active;       // [E]   experts with count > 0, ascending
+    int32_t* scalars;      // [8]   0: n_active, 1: total token tiles, 2: padded rows used
+};
+
+struct WsLayout {
+    size_t ctrl = 0, logits = 0, plan = 0, ids = 0, w = 0, counts = 0, offsets = 0, perm = 0, inv = 0,
+           xq = 0, xs = 0, xa = 0, xa_s = 0, h = 0, h_s = 0, y_perm = 0, total = 0;
+    int64_t pad_rows = 0;
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int64_t padded_rows(int T, int k, int E) {
+    int64_t P = (int64_t)T * k;
+    int64_t touched = P < E ? P : E;
+    return align_up((size_t)(P + touched * (kPadRows - 1)), kPadRows);
+}
+
+inline size_t mma_scale_bytes(int64_t rows, int64_t K) {
+    if (rows % 128 != 0 || K % 128 != 0) return 0;
+    return (size_t)(rows / 128) * (size_t)(K / 128) * 512;
+}
+
+inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
+    WsLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    int64_t P = (int64_t)T * k;
+    L.ctrl = take(sizeof(Ctrl));
+    L.logits = take(sizeof(float) * (size_t)T * E);
+    L.plan = take(sizeof(int32_t) * (size_t)(4 * E + 2 + 8));
+    L.ids = take(sizeof(int32_t) * (size_t)P);
+    L.w = take(sizeof(float) * (size_t)P);
+    L.counts = take(sizeof(int32_t) * (size_t)E);
+    L.offsets = take(sizeof(int32_t) * (size_t)(E + 1));
+    L.perm = take(sizeof(int32_t) * (size_t)P);
+    L.inv = take(sizeof(int32_t) * (size_t)P);
+    if (fmt == MOE_ACT_MXFP4) {
+        L.pad_rows = padded_rows(T, k, E);
+        L.xq = take((size_t)T * d / 2);
+        L.xs = take((size_t)T * d / 32);
+        L.xa = take((size_t)L.pad_rows * d / 2);
+        L.xa_s = take(mma_scale_bytes(L.pad_rows, d));
+        L.h = take((size_t)L.pad_rows * I / 2);
+        L.h_s = take(mma_scale_bytes(L.pad_rows, I));
+        L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);
+    } else {
+        L.h = take(sizeof(uint16_t) * (size_t)P * I);
+    }
+    L.total = off;
+    return L;
+}
+
+inline PlanView plan_view(void* ws, const WsLayout& L, int E) {
+    int32_t* p = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.plan);
+    PlanView v;
+    v.counts = p;
+    v.pad_offsets = p + E;
+    v.ttile_prefix = p + 2 * E + 1;
+    v.active = p + 3 * E + 2;
+    v.scalars = p + 4 * E + 2;
+    return v;
+}
+
+// ------------------------------------------------------------------ device helpers
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// E8M0 scale byte -> 2^(s-127) as fp32 (s = 0 is the subnormal 2^-127; 255 is never produced).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+    return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+}
+
+// Record the first device-side error in the workspace status word.
+__device__ __forceinline__ void set_status(int* status, int code) {
+    if (status) atomicCAS(status, 0, code);
+}
+
+// Eight E2M1 codes of one 32-bit word (element 2m in the low nibble of byte m) -> 4 f16x2.
+// The hardware conversion puts the low nibble of each byte in the low half.
+__device__ __forceinline__ void e2m1x8_to_h2(uint32_t word, uint32_t (&h)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(word));
+}
+
+__device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
+    __half2 v = *reinterpret_cast<__half2*>(&h);
+    return __half22float2(v);
+}
+
+// MX quantisation of one element given the block exponent X (OCP MX rule): round |v| / 2^X
+// to nearest on the E2M1 magnitude grid {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code,
+// saturating; a value that rounds to zero gets code 0 (never -0).
+__device__ __forceinline__ uint32_t e2m1_encode(float v, float inv_scale) {
+    float a = fabsf(v) * inv_scale;
+    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+    return (c != 0 && v < 0.f) ? (c | 8u) : c;
+}
+
+// Block exponent X = floor(log2(amax)) - 2 clamped to [-127, 127] (amax = 0 gives -127).
+// Returns the scale byte X + 127 and writes 2^-X (exact) to inv_scale.
+__device__ __forceinline__ uint32_t mx_scale_from_amax(float amax, float& inv_scale) {
+    int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);  // biased exponent; 0 for zero/subnormal
+    int X = ef - 127 - 2;
+    if (X < -127) X = -127;
+    inv_scale = __uint_as_float((uint32_t)(127 - X) << 23);
+    return (uint32_t)(X + 127);
+}
+
+// Byte offset of (row, scale column) in the tensor-core scale layout of a matrix whose rows
+// carry K/32 scale columns.
+__host__ __device__ __forceinline__ size_t mma_scale_offset(int64_t row, int64_t col, int64_t K) {
+    int64_t atoms_per_row_block = K / 128;
+    int64_t atom = (row / 128) * atoms_per_row_block + col / 4;
+    return (size_t)atom * 512 + (size_t)((row % 32) * 16 + ((row / 32) % 4) * 4 + (col % 4));
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's results / let the next
+// kernel start its prologue.  No-ops when the launch did not use the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+}  // namespace moe
+
+// ------------------------------------------------------------------ host-side launch entry points
+// (one per kernel family; defined in the .cu files, called by api.cu)
+namespace moe {
+// Raise a kernel's dynamic shared-memory limit on the current device once; later calls with the
+// same or a smaller size do not touch the runtime (so launches inside a stream capture make no
+// attribute calls once the first, uncaptured call has run).
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
+// Launch with the programmatic-dependent-launch attribute when pdl is true.
+cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          void** args);
+
+cudaError_t launch_synth(uint64_t seed, uint32_t tensor_id, uint32_t expert_first, uint32_t n_experts, int64_t rows,
+                         int64_t K, float c, float* out, cudaStream_t st);
+cudaError_t launch_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w, cudaStream_t st);
+cudaError_t launch_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma, cudaStream_t st);
+
+cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
+                                float* logits, cudaStream_t st, bool pdl);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl);
+// Decode route: logits, then the last CTA runs top-k and the whole permutation (small T).
+cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                                float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                int32_t* perm_token, int32_t* inv_pos, PlanView plan, Ctrl* ctrl,
+                                cudaStream_t st, bool pdl);
+bool route_decode_supported(int T, int d, int E, int k);
+
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                           int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl);
+cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
+                                    const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
+                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl);
+
+cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
+                           int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,
+                           cudaStream_t st, bool pdl);
+cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
+                             const int32_t* ids, const float* w, int T, int d, int E, int k, int I,
+                             const moe_expert_weights* W, uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl);
+cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
+                           uint16_t* y, cudaStream_t st, bool pdl);
+
+cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets,
+                           int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,
+                           uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st, bool pdl);
+cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan, const int32_t* offsets,
+                             int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,
+                             uint16_t* y_perm, int* status, cudaStream_t st, bool pdl);
+}  // namespace moe

@@ -1,0 +1,44 @@
+// launch.cu -- host-side launch helpers shared by the kernel families.
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "common.cuh"
+
+namespace moe {
+
+cudaError_t ensure_dyn_smem(const void* func, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, size_t> done;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_pair(func, dev);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    err = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (err == cudaSuccess) done[key] = bytes;
+    return err;
+}
+
+cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          void** args) {
+    if (smem > 48 * 1024) {
+        cudaError_t err = ensure_dyn_smem(func, smem);
+        if (err != cudaSuccess) return err;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, func, args);
+}
+
+}  // namespace moe

@@ -1,0 +1,476 @@
+// route.cu -- router logits, top-k + softmax, and the permutation by expert.
+//
+// Router: Muse Spark Open explainer, section 8 -- one FP32 matrix product scores every expert,
+// the best k are kept as a set, no shared expert.  Weights: section 9 -- the chosen experts'
+// outputs are weighted by renormalised router scores (the printed example sums to 1).
+// Permutation: section 12 -- pairs are gathered per expert so each expert runs one batch.
+//
+// Fixed fp32 reduction order of a logit (so that routing is reproducible bit for bit): 32
+// partial sums; partial c accumulates with fma, from +0, the elements i with (i/4) % 32 == c in
+// increasing i; then an xor butterfly p_c += p_{c^m} for m = 16, 8, 4, 2, 1; then + b[e].
+// Lane c of a warp owns partial c.
+#include <float.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ float warp_butterfly_sum(float p) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) p = p + __shfl_xor_sync(0xffffffffu, p, m);
+    return p;
+}
+
+// One warp selects the top-k of logits[0..E) (ties -> lower id), sorts the set ascending and
+// writes ids[0..k) and the softmax weights w[0..k).  Logits are read with ld.cg so that values
+// written by other CTAs of the same grid are seen.
+__device__ void topk_softmax_warp(const float* logits, int E, int k, int32_t* ids, float* w) {
+    const int lane = threadIdx.x & 31;
+    uint32_t taken = 0;
+    int my_id = 0x7fffffff;
+    float my_logit = -FLT_MAX;
+    for (int r = 0; r < k; ++r) {
+        float best = -FLT_MAX;
+        int bid = 0x7fffffff;
+        for (int i = 0; lane + 32 * i < E; ++i) {
+            if ((taken >> i) & 1u) continue;
+            float v = __ldcg(logits + lane + 32 * i);
+            if (bid == 0x7fffffff || v > best) {  // increasing e within a lane: strict > keeps the lower id
+                best = v;
+                bid = lane + 32 * i;
+            }
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, best, m);
+            int oid = __shfl_xor_sync(0xffffffffu, bid, m);
+            if (oid != 0x7fffffff && (bid == 0x7fffffff || ov > best || (ov == best && oid < bid))) {
+                best = ov;
+                bid = oid;
+            }
+        }
+        if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+        if (lane == r) {
+            my_id = bid;
+            my_logit = best;
+        }
+    }
+    // rank of each chosen id among the k chosen (ids are distinct)
+    int rank = 0;
+    for (int s = 0; s < k; ++s) {
+        int o = __shfl_sync(0xffffffffu, my_id, s);
+        if (lane < k && o < my_id) ++rank;
+    }
+    float m = __shfl_sync(0xffffffffu, my_logit, 0);  // the first pick is the largest logit
+    float ex = lane < k ? expf(my_logit - m) : 0.f;
+    float sum = warp_butterfly_sum(ex);
+    if (lane < k) {
+        ids[rank] = my_id;
+        w[rank] = ex / sum;
+    }
+}
+
+// Warp 0 of a block: counts[E] -> offsets, padded offsets, token-tile prefix, active list.
+__device__ void build_plan_warp(const int32_t* counts_in, int E, int32_t* counts_out, int32_t* offsets, PlanView plan) {
+    const int lane = threadIdx.x & 31;
+    const int chunk = (E + 31) / 32;
+    const int lo = min(E, lane * chunk), hi = min(E, lo + chunk);
+    int s_cnt = 0, s_pad = 0, s_tile = 0, s_act = 0;
+    for (int e = lo; e < hi; ++e) {
+        int c = counts_in[e];
+        s_cnt += c;
+        s_pad += (c + kPadRows - 1) / kPadRows * kPadRows;
+        s_tile += (c + kTokTile - 1) / kTokTile;
+        s_act += c > 0;
+    }
+    int x_cnt = s_cnt, x_pad = s_pad, x_tile = s_tile, x_act = s_act;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int a = __shfl_up_sync(0xffffffffu, x_cnt, o), b = __shfl_up_sync(0xffffffffu, x_pad, o);
+        int c = __shfl_up_sync(0xffffffffu, x_tile, o), d = __shfl_up_sync(0xffffffffu, x_act, o);
+        if (lane >= o) {
+            x_cnt += a;
+            x_pad += b;
+            x_tile += c;
+            x_act += d;
+        }
+    }
+    int c_off = x_cnt - s_cnt, p_off = x_pad - s_pad, t_off = x_tile - s_tile, a_off = x_act - s_act;
+    for (int e = lo; e < hi; ++e) {
+        int c = counts_in[e];
+        if (counts_out) counts_out[e] = c;
+        plan.counts[e] = c;
+        offsets[e] = c_off;
+        plan.pad_offsets[e] = p_off;
+        plan.ttile_prefix[e] = t_off;
+        if (c > 0) plan.active[a_off++] = e;
+        c_off += c;
+        p_off += (c + kPadRows - 1) / kPadRows * kPadRows;
+        t_off += (c + kTokTile - 1) / kTokTile;
+    }
+    if (lane == 31) {
+        offsets[E] = x_cnt;
+        plan.pad_offsets[E] = x_pad;
+        plan.ttile_prefix[E] = x_tile;
+        plan.scalars[0] = x_act;
+        plan.scalars[1] = x_tile;
+        plan.scalars[2] = x_pad;
+    }
+}
+
+// ------------------------------------------------------------------ decode route (small T)
+// Grid: one CTA per expert.  W_r[e] and x (T <= 8 rows) are staged in shared memory with
+// cp.async; warps compute the T logits of expert e.  The last CTA to finish (atomic ticket)
+// runs top-k for every token and the whole permutation, so a decode step needs one launch.
+constexpr int kRouteDecodeThreads = 128;
+constexpr int kRouteDecodeMaxT = 8;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+__global__ void __launch_bounds__(kRouteDecodeThreads)
+route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ b,
+                    int T, int d, int E, int k, float* logits, int32_t* ids, float* w, int32_t* counts,
+                    int32_t* offsets, int32_t* perm_token, int32_t* inv_pos, PlanView plan, Ctrl* ctrl) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* Ws = reinterpret_cast<float*>(smem);                      // [d]
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sizeof(float) * d);  // [T][d]
+    __shared__ int s_last;
+    __shared__ int s_cnt[kMaxE];
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    pdl_wait();
+    for (int i = tid; i < d / 4; i += blockDim.x) cp_async16(Ws + 4 * i, W_r + (size_t)e * d + 4 * i);
+    for (int i = tid; i < T * d / 8; i += blockDim.x) cp_async16(xs + 8 * i, x + 8 * (size_t)i);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+
+    const float bias = b ? b[e] : 0.f;
+    for (int t = warp; t < T; t += blockDim.x / 32) {
+        const uint16_t* xr = xs + (size_t)t * d;
+        float acc = 0.f;
+        for (int g = lane; g < d / 4; g += 32) {
+            float4 wv = *reinterpret_cast<const float4*>(Ws + 4 * g);
+            uint2 xv = *reinterpret_cast<const uint2*>(xr + 4 * g);
+            acc = fmaf(bf16_bits_to_f32(xv.x & 0xFFFF), wv.x, acc);
+            acc = fmaf(bf16_bits_to_f32(xv.x >> 16), wv.y, acc);
+            acc = fmaf(bf16_bits_to_f32(xv.y & 0xFFFF), wv.z, acc);
+            acc = fmaf(bf16_bits_to_f32(xv.y >> 16), wv.w, acc);
+        }
+        acc = warp_butterfly_sum(acc);
+        if (lane == 0) logits[(size_t)t * E + e] = acc + bias;
+    }
+
+    // ---- last CTA: top-k + permutation
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        unsigned ticket = atomicAdd(&ctrl->route_ticket, 1u);
+        s_last = (ticket == (unsigned)gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (tid == 0) ctrl->route_ticket = 0;  // ready for the next call on this workspace
+
+    for (int t = warp; t < T; t += blockDim.x / 32)
+        topk_softmax_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+    for (int i = tid; i < E; i += blockDim.x) s_cnt[i] = 0;
+    __syncthreads();
+    const int P = T * k;
+    for (int p = tid; p < P; p += blockDim.x) atomicAdd(&s_cnt[ids[p]], 1);
+    __syncthreads();
+    if (warp == 0) build_plan_warp(s_cnt, E, counts, offsets, plan);
+    __syncthreads();
+    for (int p = tid; p < P; p += blockDim.x) {
+        const int t = p / k, ex = ids[p];
+        int rank = 0;
+        for (int t2 = 0; t2 < t; ++t2)
+            for (int j = 0; j < k; ++j) rank += (ids[t2 * k + j] == ex);
+        const int r = offsets[ex] + rank;
+        perm_token[r] = t;
+        inv_pos[p] = r;
+    }
+    __threadfence();
+    pdl_launch_dependents();
+}
+
+bool route_decode_supported(int T, int d, int E, int k) {
+    (void)k;
+    return T >= 1 && T <= kRouteDecodeMaxT && E <= kMaxE &&
+           (size_t)d * (4 + 2 * (size_t)T) <= 200 * 1024;
+}
+
+
+cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                                float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
+                                int32_t* perm_token, int32_t* inv_pos, PlanView plan, Ctrl* ctrl, cudaStream_t st,
+                                bool pdl) {
+    size_t smem = sizeof(float) * (size_t)d + sizeof(uint16_t) * (size_t)T * d;
+    void* args[] = {&x, &W_r, &b, &T, &d, &E, &k, &logits, &ids, &w, &counts, &offsets, &perm_token, &inv_pos,
+                    &plan, &ctrl};
+    return launch_kernel((const void*)route_decode_kernel, dim3(E), dim3(kRouteDecodeThreads), smem, st, pdl, args);
+}
+
+// ------------------------------------------------------------------ tiled logits (any T)
+// CTA tile: 32 tokens x 32 experts, 16 warps as 4 (tokens) x 4 (experts), warp tile 8 x 8.
+// Lanes are the 32 partial sums of the fixed order; K is staged through shared memory in
+// chunks of 256 elements (64 groups of 4; lane c takes groups c and c + 32 of a chunk).
+constexpr int kLT = 32, kLE = 32, kLKC = 256;
+
+__global__ void __launch_bounds__(512)
+route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ b,
+                          int T, int d, int E, float* __restrict__ logits) {
+    __shared__ __align__(16) uint16_t xs[kLT][kLKC];
+    __shared__ __align__(16) float ws[kLE][kLKC];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.x * kLT, e0 = blockIdx.y * kLE;
+    const int wt = (warp >> 2) * 8, we = (warp & 3) * 8;
+    float acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[a][c] = 0.f;
+
+    pdl_wait();
+    for (int k0 = 0; k0 < d; k0 += kLKC) {
+        __syncthreads();
+        for (int i = tid; i < kLT * kLKC / 8; i += blockDim.x) {  // 16-byte pieces of x
+            int r = i / (kLKC / 8), c = i % (kLKC / 8);
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (t0 + r < T && k0 + 8 * c < d) v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * d + k0 + 8 * c);
+            *reinterpret_cast<uint4*>(&xs[r][8 * c]) = v;
+        }
+        for (int i = tid; i < kLE * kLKC / 4; i += blockDim.x) {
+            int r = i / (kLKC / 4), c = i % (kLKC / 4);
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + r < E && k0 + 4 * c < d) v = *reinterpret_cast<const float4*>(W_r + (size_t)(e0 + r) * d + k0 + 4 * c);
+            *reinterpret_cast<float4*>(&ws[r][4 * c]) = v;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+            if (k0 + 128 * gi >= d) break;  // d % 128 == 0: a group of 32 lanes is all in or all out
+            const int g = lane + 32 * gi;
+            float xv[8][4], wv[8][4];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                uint2 u = *reinterpret_cast<const uint2*>(&xs[wt + a][4 * g]);
+                xv[a][0] = bf16_bits_to_f32(u.x & 0xFFFF);
+                xv[a][1] = bf16_bits_to_f32(u.x >> 16);
+                xv[a][2] = bf16_bits_to_f32(u.y & 0xFFFF);
+                xv[a][3] = bf16_bits_to_f32(u.y >> 16);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float4 f = *reinterpret_cast<const float4*>(&ws[we + c][4 * g]);
+                wv[c][0] = f.x;
+                wv[c][1] = f.y;
+                wv[c][2] = f.z;
+                wv[c][3] = f.w;
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) acc[a][c] = fmaf(xv[a][q], wv[c][q], acc[a][c]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float s = warp_butterfly_sum(acc[a][c]);
+            int t = t0 + wt + a, e = e0 + we + c;
+            if (lane == ((a * 8 + c) & 31) && t < T && e < E) logits[(size_t)t * E + e] = s + (b ? b[e] : 0.f);
+        }
+    pdl_launch_dependents();
+}
+
+__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w) {
+    pdl_wait();
+    const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t < T) topk_softmax_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+    pdl_launch_dependents();
+}
+
+cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
+                                float* logits, cudaStream_t st, bool pdl) {
+    if (T == 0) return cudaSuccess;
+    void* args[] = {&x, &W_r, &b, &T, &d, &E, &logits};
+    dim3 grid((T + kLT - 1) / kLT, (E + kLE - 1) / kLE);
+    return launch_kernel((const void*)route_logits_tiled_kernel, grid, dim3(512), 0, st, pdl, args);
+}
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl) {
+    if (T == 0) return cudaSuccess;
+    void* args[] = {&logits, &T, &E, &k, &ids, &w};
+    return launch_kernel((const void*)topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pdl, args);
+}
+
+// ------------------------------------------------------------------ permutation (any T)
+
+__global__ void count_kernel(const int32_t* __restrict__ ids, int P, int32_t* counts) {
+    pdl_wait();
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) atomicAdd(&counts[ids[p]], 1);
+}
+
+__global__ void plan_kernel(int E, int32_t* counts_out, int32_t* offsets, PlanView plan) {
+    pdl_wait();
+    if (threadIdx.x < 32) build_plan_warp(plan.counts, E, counts_out, offsets, plan);
+}
+
+// One CTA per expert: a stable block-wide compaction over the tokens that chose it.
+__global__ void __launch_bounds__(256)
+scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __restrict__ offsets, PlanView plan,
+               int32_t* perm_token, int32_t* inv_pos) {
+    __shared__ int warp_tot[8];
+    pdl_wait();
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (plan.counts[e] == 0) return;
+    int running = offsets[e];
+    for (int t0 = 0; t0 < T; t0 += 256) {
+        const int t = t0 + tid;
+        int j_found = -1;
+        if (t < T)
+            for (int j = 0; j < k; ++j) {
+                int v = ids[(size_t)t * k + j];
+                if (v == e) j_found = j;
+            }
+        const unsigned bal = __ballot_sync(0xffffffffu, j_found >= 0);
+        const int before = __popc(bal & ((1u << lane) - 1u));
+        if (lane == 0) warp_tot[warp] = __popc(bal);
+        __syncthreads();
+        int wbase = 0, tot = 0;
+        for (int q = 0; q < 8; ++q) {
+            if (q < warp) wbase += warp_tot[q];
+            tot += warp_tot[q];
+        }
+        if (j_found >= 0) {
+            const int r = running + wbase + before;
+            perm_token[r] = t;
+            inv_pos[(size_t)t * k + j_found] = r;
+        }
+        running += tot;
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                           int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl) {
+    cudaError_t err = cudaMemsetAsync(plan.counts, 0, sizeof(int32_t) * (size_t)E, st);
+    if (err != cudaSuccess) return err;
+    int P = T * k;
+    if (P > 0) {
+        int blocks = (P + 255) / 256;
+        if (blocks > 1024) blocks = 1024;
+        void* a1[] = {&ids, &P, &plan.counts};
+        err = launch_kernel((const void*)count_kernel, dim3(blocks), dim3(256), 0, st, false, a1);
+        if (err != cudaSuccess) return err;
+    }
+    void* a2[] = {&E, &counts, &offsets, &plan};
+    err = launch_kernel((const void*)plan_kernel, dim3(1), dim3(32), 0, st, pdl, a2);
+    if (err != cudaSuccess) return err;
+    if (P == 0) return cudaSuccess;
+    void* a3[] = {&ids, &T, &k, &offsets, &plan, &perm_token, &inv_pos};
+    return launch_kernel((const void*)scatter_kernel, dim3(E), dim3(256), 0, st, pdl, a3);
+}
+
+// ------------------------------------------------------------------ MXFP4 activation operand
+// Quantise each token row once (one thread per 32-element block), then gather the rows into
+// padded expert-grouped order with the scales in the tensor-core layout.
+
+__global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ xq,
+                                 uint8_t* __restrict__ xs) {
+    pdl_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblocks; blk += stride) {
+        const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint4 u = src[i];
+            uint32_t ww[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                v[8 * i + 2 * m] = bf16_bits_to_f32(ww[m] & 0xFFFF);
+                v[8 * i + 2 * m + 1] = bf16_bits_to_f32(ww[m] >> 16);
+            }
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        float inv;
+        uint32_t sb = mx_scale_from_amax(amax, inv);
+        uint32_t words[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            uint32_t wd = 0;
+#pragma unroll
+            for (int n = 0; n < 8; ++n) wd |= e2m1_encode(v[8 * m + n], inv) << (4 * n);
+            words[m] = wd;
+        }
+        reinterpret_cast<uint4*>(xq)[blk] = make_uint4(words[0], words[1], words[2], words[3]);
+        xs[blk] = (uint8_t)sb;
+    }
+}
+
+// One thread per (padded row, 32-element block).
+__global__ void act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, int d, int E,
+                                  int64_t pad_rows, const int32_t* __restrict__ offsets,
+                                  const int32_t* __restrict__ perm_token, PlanView plan, uint8_t* __restrict__ xa,
+                                  uint8_t* __restrict__ xa_s) {
+    pdl_wait();
+    const int nb = d / 32;
+    const int64_t used = plan.scalars[2];
+    const int64_t total = used * nb;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t r = i / nb;
+        const int blk = (int)(i % nb);
+        // expert of padded row r: last e with pad_offsets[e] <= r
+        int lo = 0, hi = E;  // invariant pad_offsets[lo] <= r < pad_offsets[hi]
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (plan.pad_offsets[mid] <= r) lo = mid; else hi = mid;
+        }
+        const int64_t local = r - plan.pad_offsets[lo];
+        uint4 v = make_uint4(0, 0, 0, 0);
+        uint8_t sb = 0;
+        if (local < plan.counts[lo]) {
+            const int t = perm_token[offsets[lo] + local];
+            v = reinterpret_cast<const uint4*>(xq)[(size_t)t * nb + blk];
+            sb = xs[(size_t)t * nb + blk];
+        }
+        reinterpret_cast<uint4*>(xa)[(size_t)r * nb + blk] = v;
+        xa_s[mma_scale_offset(r, blk, d)] = sb;
+    }
+    (void)pad_rows;
+}
+
+cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
+                                    const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
+                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl) {
+    (void)k;
+    int64_t nb = (int64_t)T * (d / 32);
+    if (nb > 0) {
+        int64_t blocks = (nb + 255) / 256;
+        if (blocks > 152 * 16) blocks = 152 * 16;
+        void* a1[] = {&x, &nb, &xq, &xs};
+        cudaError_t err = launch_kernel((const void*)act_quant_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
+        if (err != cudaSuccess) return err;
+    }
+    int64_t tot = pad_rows * (d / 32);
+    if (tot == 0) return cudaSuccess;
+    int64_t blocks = (tot + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    void* a2[] = {&xq, &xs, &d, &E, &pad_rows, &offsets, &perm_token, &plan, &xa, &xa_s};
+    return launch_kernel((const void*)act_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a2);
+}
+
+}  // namespace moe

@@ -57,11 +57,51 @@ def weight_scale(std: float) -> np.float32:
     return np.float32(std / SIGMA_V)
 
 
+_host_lib = None
+
+
+def _host():
+    """The C implementation of the same generator (inputs_host.c), built on first use; None if
+    no C compiler is available (the numpy definition below is then used)."""
+    global _host_lib
+    if _host_lib is None:
+        import ctypes
+        import os
+        import platform
+        import subprocess
+        here = os.path.dirname(os.path.abspath(__file__))
+        src = os.path.join(here, "inputs_host.c")
+        lib = os.path.join(here, "_build", "libinputs_%s.so" % platform.machine())
+        try:
+            if not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(src):
+                os.makedirs(os.path.dirname(lib), exist_ok=True)
+                tmp = lib + ".tmp.%d" % os.getpid()
+                subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+                                src, "-o", tmp], check=True)
+                os.replace(tmp, lib)
+            h = ctypes.CDLL(lib)
+            h.inputs_stream_key.restype = ctypes.c_uint64
+            h.inputs_stream_key.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32]
+            h.inputs_synth.restype = None
+            h.inputs_synth.argtypes = [ctypes.c_uint64, ctypes.c_int64, ctypes.c_int64, ctypes.c_float,
+                                       ctypes.c_void_p]
+            _host_lib = h
+        except (OSError, subprocess.CalledProcessError):
+            _host_lib = False
+    return _host_lib or None
+
+
 def synth_weights(seed: int, tensor_id: int, expert: int, rows: int, K: int, std: float,
-                  row_start: int = 0, row_count: Optional[int] = None) -> np.ndarray:
+                  row_start: int = 0, row_count: Optional[int] = None, use_c: bool = True) -> np.ndarray:
     """fp32 [row_count][K] rows ``row_start ..`` of one synthetic expert matrix [rows][K]."""
     if row_count is None:
         row_count = rows - row_start
+    h = _host() if use_c else None
+    if h is not None:
+        out = np.empty((row_count, K), dtype=np.float32)
+        key = h.inputs_stream_key(seed, tensor_id, expert)
+        h.inputs_synth(key, row_start * K, row_count * K, float(weight_scale(std)), out.ctypes.data)
+        return out
     key = stream_key(seed, tensor_id, expert)
     n = np.arange(row_start * K, (row_start + row_count) * K, dtype=np.uint64)
     with np.errstate(over="ignore"):

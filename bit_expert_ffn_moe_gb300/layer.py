@@ -1,0 +1,86 @@
+"""Device-resident MoE layer state: expert weights (MXFP4, generated and packed on the GPU by the
+library), router weights, and a workspace.  Convenience for tests and the benchmark; the
+compute path is entirely the library's kernels (see binding.py)."""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding as B
+from . import inputs as IN
+
+
+class DeviceLayer:
+    """One synthetic layer of workload ``cfg`` on ``device``.  ``layer`` selects an independent
+    copy (different weight seed), used to rotate layers so that L2 cannot carry experts."""
+
+    def __init__(self, cfg: IN.Config, device="cuda", layer: int = 0, mma_scales: bool = True,
+                 chunk_bytes: int = 1 << 30):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.seed = cfg.seed + 7919 * layer
+        E, I, d = cfg.E, cfg.I, cfg.d
+        u8 = dict(dtype=torch.uint8, device=self.device)
+        self.q = {}
+        self.s = {}
+        self.s_mma = {}
+        shapes = IN.expert_matrix_shapes(cfg)
+        c = float(IN.weight_scale(cfg.weight_std))
+        for tid, (rows, K) in shapes.items():
+            q = torch.empty((E, rows, K // 2), **u8)
+            s = torch.empty((E, rows, K // 32), **u8)
+            per = rows * K * 4
+            n_chunk = max(1, min(E, chunk_bytes // per))
+            buf = torch.empty((n_chunk, rows, K), dtype=torch.float32, device=self.device)
+            for e0 in range(0, E, n_chunk):
+                n = min(n_chunk, E - e0)
+                B.moe_synth_weights(self.seed, tid, e0, n, rows, K, c, buf)
+                B.moe_mxfp4_pack(buf, n * rows, K, q[e0:e0 + n], s[e0:e0 + n])
+            del buf
+            self.q[tid], self.s[tid] = q, s
+            if mma_scales and rows % 128 == 0 and K % 128 == 0:
+                sm = torch.empty(B.moe_mxfp4_mma_scale_bytes(E * rows, K), **u8)
+                B.moe_mxfp4_scales_to_mma(s, E * rows, K, sm)
+                self.s_mma[tid] = sm
+        W_r, b = IN.make_router(cfg)
+        if layer != 0:  # independent router per layer copy
+            rng = np.random.default_rng([cfg.seed, 77, layer])
+            W_r = (rng.standard_normal(W_r.shape) / np.sqrt(cfg.d)).astype(np.float32)
+        self.W_r_host, self.b_host = W_r, b
+        self.W_r = torch.from_numpy(W_r).to(self.device)
+        self.b = torch.from_numpy(b).to(self.device)
+        G, U, D = IN.TENSOR_GATE, IN.TENSOR_UP, IN.TENSOR_DOWN
+        self.weights = B.expert_weights_struct(self.q[G], self.s[G], self.q[U], self.s[U], self.q[D], self.s[D],
+                                               self.s_mma.get(G), self.s_mma.get(U), self.s_mma.get(D))
+
+    def weight_bytes_per_expert(self) -> int:
+        cfg = self.cfg
+        return 3 * cfg.I * cfg.d // 2 + 3 * cfg.I * cfg.d // 32
+
+
+def make_workspace(T: int, d: int, E: int, k: int, I: int, fmt: int, device="cuda") -> torch.Tensor:
+    n = B.moe_workspace_size(T, d, E, k, I, fmt)
+    if n == 0:
+        raise ValueError("unsupported shape")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    B.moe_workspace_init(ws)
+    return ws
+
+
+def layer_forward(layer: DeviceLayer, x: torch.Tensor, fmt: int, ws: Optional[torch.Tensor] = None,
+                  want_routing: bool = False, stream=None):
+    """y = MoE(x) for bf16 x [T][d] (as int16/uint16 bit patterns or torch.bfloat16)."""
+    cfg = layer.cfg
+    T = x.shape[0]
+    if ws is None:
+        ws = make_workspace(T, cfg.d, cfg.E, cfg.k, cfg.I, fmt, x.device)
+    y = torch.empty((T, cfg.d), dtype=torch.bfloat16, device=x.device)
+    ids = torch.empty((T, cfg.k), dtype=torch.int32, device=x.device) if want_routing else None
+    w = torch.empty((T, cfg.k), dtype=torch.float32, device=x.device) if want_routing else None
+    B.moe_layer_forward(x, layer.W_r, layer.b, T, cfg.d, cfg.E, cfg.k, cfg.I, layer.weights, fmt, y, ids, w, ws,
+                        stream=stream)
+    if want_routing:
+        return y, ids, w
+    return y

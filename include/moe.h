@@ -1,0 +1,209 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE expert-FFN layer library (libmoe_gb300.so).
+ *
+ * The layer, as the Muse Spark Open explainer ("Muse Spark Open を段階的に分解する") states it:
+ *   section 8   a router scores every expert with one FP32 matrix product and keeps the best
+ *               k (8 of 256 there) as a set; there is no shared expert;
+ *   section 12  the (token, expert) pairs are gathered per expert and each expert computes its
+ *               tokens as one batch;
+ *   section 9   each chosen expert applies gate, up and down matrices; the expert outputs are
+ *               weighted by the router scores and summed;
+ *   section 11  expert weights are 4-bit values sharing a block scale; the DGX Spark news item
+ *               ("DGX Spark MoE inference optimizations", section 2) names the block-scaled
+ *               MXFP4 format: E2M1 elements, one E8M0 scale per 32 consecutive elements.
+ *
+ * Conventions for every entry point below:
+ *   - Tensor pointers are DEVICE pointers owned by the caller (the library never frees or
+ *     keeps them).  Shapes are row-major; "[a][b]" means a rows of b elements.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and returns synchronously only argument and launch errors.
+ *   - The library allocates no device memory in any entry point.  Scratch space comes from
+ *     the caller's workspace `ws` of `ws_bytes` bytes (see moe_workspace_size); it must be
+ *     256-byte aligned and initialised once with moe_workspace_init.  Calls that share a
+ *     workspace must be ordered on one stream.
+ *   - Kernels that wait on hardware barriers give up after a bounded number of polls, record
+ *     MOE_ERR_TIMEOUT in the workspace and return; moe_get_device_status reads that word.
+ *   - Inputs are assumed finite.
+ *   - Shape rules (MOE_ERR_UNSUPPORTED_SHAPE otherwise): 1 <= k <= min(E, 32); E <= 1024;
+ *     d % 128 == 0; I % 32 == 0 (MOE_ACT_BF16) or I % 128 == 0 (MOE_ACT_MXFP4); T >= 0.
+ *
+ * MXFP4 tensor layout ("canonical"): a [rows][K] matrix is stored as codes q[rows][K/2]
+ * (element 2i in the low nibble of byte i, element 2i+1 in the high nibble; bit 3 of a code
+ * is the sign) and scales s[rows][K/32] (E8M0: the block's values are code_value * 2^(s-127)).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* moe_stream_t; /* same object as a cudaStream_t */
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* null / misaligned pointer, negative size */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* a shape rule above is violated */
+    MOE_ERR_WORKSPACE = 3,         /* workspace missing, too small or misaligned */
+    MOE_ERR_CUDA = 4,              /* a CUDA runtime call failed (launch error, no device) */
+    MOE_ERR_TIMEOUT = 5,           /* device side: a bounded barrier wait ran out */
+    MOE_ERR_DEVICE = 6             /* the current device is not an sm_103 GPU */
+} moe_status;
+
+/* Activation format of the expert GEMM operands.
+ *   MOE_ACT_BF16  -- decode-style path: x is used as bf16, the gate/up output h is stored as
+ *                    bf16; CUDA-core GEMV kernels with 128-bit weight loads (best for T <= 4).
+ *   MOE_ACT_MXFP4 -- prefill path: x and h are quantised to MXFP4 (same rule as the weight
+ *                    packer); tcgen05 block-scaled MMA (kind::mxf4) grouped GEMMs. */
+typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1 } moe_act_fmt;
+
+/* Expert weights of one layer (all device pointers, canonical MXFP4 layout):
+ *   gate_q/up_q [E][I][d/2], gate_s/up_s [E][I][d/32]   (gate and up: I rows of d)
+ *   down_q      [E][d][I/2], down_s      [E][d][I/32]   (down: d rows of I)
+ * The MXFP4 path also needs the scales re-laid out for the tensor cores with
+ * moe_mxfp4_scales_to_mma (gate_s_mma/up_s_mma for [E*I] rows of K = d, down_s_mma for
+ * [E*d] rows of K = I); the BF16 path ignores those three (they may be NULL). */
+typedef struct moe_expert_weights {
+    const uint8_t* gate_q;
+    const uint8_t* gate_s;
+    const uint8_t* up_q;
+    const uint8_t* up_s;
+    const uint8_t* down_q;
+    const uint8_t* down_s;
+    const uint8_t* gate_s_mma;
+    const uint8_t* up_s_mma;
+    const uint8_t* down_s_mma;
+} moe_expert_weights;
+
+/* ---------------------------------------------------------------- library */
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* ABI version of this header (incremented on incompatible changes). */
+int moe_abi_version(void);
+
+/* ---------------------------------------------------------------- MXFP4 helpers
+ * Block-scaled 4-bit format of the expert weights (DGX Spark news item, section 2; Muse
+ * Spark Open explainer, section 11).  Quantisation rule (OCP MX v1.0): per 32-element block,
+ * X = floor(log2(max |v|)) - 2 clamped to [-127, 127], scale byte X + 127, each element
+ * rounded to nearest on the E2M1 grid {0, .5, 1, 1.5, 2, 3, 4, 6} times 2^X, ties to the
+ * even code, saturating at 6 * 2^X; a value that rounds to zero is stored as +0; an
+ * all-zero block gets scale byte 0. */
+
+/* Pack fp32 w[rows][K] into q[rows][K/2], s[rows][K/32].  K % 32 == 0, rows >= 0. */
+moe_status moe_mxfp4_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
+                          moe_stream_t stream);
+
+/* Dequantise q, s back to fp32 w[rows][K] (exact). */
+moe_status moe_mxfp4_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w,
+                            moe_stream_t stream);
+
+/* Bytes of the tensor-core scale layout of a [rows][K] MXFP4 matrix (rows % 128 == 0,
+ * K % 128 == 0; 0 otherwise).  The layout is a grid of 512-byte atoms, atom (R, C) =
+ * rows 128R..128R+127 x scale columns 4C..4C+3 stored at atom index R*(K/128) + C; inside an
+ * atom, row r and scale column c sit at byte (r%32)*16 + ((r/32)%4)*4 + (c%4). */
+size_t moe_mxfp4_mma_scale_bytes(int64_t rows, int64_t K);
+
+/* Re-lay canonical scales s[rows][K/32] out into the tensor-core layout s_mma. */
+moe_status moe_mxfp4_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma,
+                                   moe_stream_t stream);
+
+/* ---------------------------------------------------------------- workspace */
+
+/* Bytes of workspace needed by moe_layer_forward (and enough for every step call) at these
+ * sizes.  Returns 0 when the shape is unsupported. */
+size_t moe_workspace_size(int T, int d, int E, int k, int I, moe_act_fmt fmt);
+
+/* Rows of the padded, expert-grouped activation buffers of the MXFP4 path (xa, h): every
+ * expert's rows start at a multiple of 128.  An upper bound that depends on sizes only. */
+int64_t moe_padded_rows(int T, int k, int E);
+
+/* Zero the workspace control block (status word, counters).  Call once per workspace. */
+moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream`, copy the device status word of `ws` to *out and clear it.
+ * *out is MOE_OK or the first device-side error (MOE_ERR_TIMEOUT) recorded since the last
+ * call. */
+moe_status moe_get_device_status(void* ws, moe_stream_t stream, moe_status* out);
+
+/* ---------------------------------------------------------------- layer steps */
+
+/* Router (Muse Spark Open explainer, section 8): logits[t][e] = b[e] + sum_i x[t][i]*W_r[e][i]
+ * in fp32 with a fixed reduction order: 32 partial sums, partial c accumulating with fma the
+ * elements i with (i/4) % 32 == c in increasing i, combined by an xor butterfly
+ * (m = 16, 8, 4, 2, 1), then + b[e].  The k largest logits are kept (ties -> lower e);
+ * ids[t][k] is that set in ascending expert order and w[t][k] the softmax of the selected
+ * logits (section 9: the weights sum to 1).
+ *   x bf16 [T][d]; W_r fp32 [E][d]; b fp32 [E] or NULL (= 0); ids int32 [T][k]; w fp32 [T][k].
+ * Uses ws for the T*E logits. */
+moe_status moe_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                     int32_t* ids, float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Permutation by expert (section 12).  The T*k pairs (t, j) are ordered by (ids[t][j], t, j):
+ *   counts[E]      pairs per expert
+ *   offsets[E+1]   exclusive prefix sum of counts
+ *   perm_token[P]  token of permuted row r (P = T*k)
+ *   inv_pos[P]     permuted row of pair (t, j) at index t*k + j
+ * For MOE_ACT_MXFP4 it also quantises every token row of x once and writes the activation
+ * operand in padded expert-grouped order: xa[moe_padded_rows][d/2] codes and xa_s in the
+ * tensor-core scale layout (moe_mxfp4_mma_scale_bytes(moe_padded_rows, d) bytes); expert e's
+ * rows start at a multiple of 128, padding rows are zero.  For MOE_ACT_BF16, xa and xa_s are
+ * unused (may be NULL).  Writes the per-expert plan (padded offsets, tile table) into ws for
+ * the expert calls that follow. */
+moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int E, int k, moe_act_fmt fmt,
+                       int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_pos,
+                       uint8_t* xa, uint8_t* xa_s, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Gate/up GEMMs with fused SwiGLU (section 9; SwiGLU h = SiLU(g) * u, g = x W_g^T, u = x W_u^T)
+ * for every permuted row, grouped by expert.  Needs the plan that moe_permute wrote into ws.
+ *   MOE_ACT_BF16:  reads x bf16 [T][d] through perm_token; writes h bf16 [P][I] (row r =
+ *                  permuted row r), h_s unused.
+ *   MOE_ACT_MXFP4: reads xa / xa_s; writes h as MXFP4 codes [moe_padded_rows][I/2] in padded
+ *                  order and h_s in the tensor-core scale layout. */
+moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint8_t* xa_s, moe_act_fmt fmt,
+                                const int32_t* perm_token, const int32_t* offsets, int T, int d, int E, int k,
+                                int I, const moe_expert_weights* W, void* h, uint8_t* h_s, void* ws,
+                                size_t ws_bytes, moe_stream_t stream);
+
+/* Down GEMM (section 9): y_perm[r] = h[r] W_d[e]^T for every permuted row r of expert e,
+ * written as bf16 [P][d] in compact permuted order.  h / h_s as produced by
+ * moe_expert_up_swiglu in the same format; perm_token / offsets from moe_permute (perm_token
+ * is only read by the MOE_ACT_BF16 path). */
+moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, const int32_t* perm_token,
+                           const int32_t* offsets, int T, int d, int E, int k, int I, const moe_expert_weights* W,
+                           uint16_t* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Weighted sum (section 9): y[t] = sum_j w[t][j] * y_perm[inv_pos[t*k+j]] accumulated in fp32
+ * in slot order j = 0..k-1, stored as bf16 [T][d]. */
+moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
+                       uint16_t* y, moe_stream_t stream);
+
+/* The whole layer in one call: route -> permute -> up+SwiGLU -> down -> combine, all on
+ * `stream`, with no host synchronisation.  y bf16 [T][d].  ids/w (optional, may be NULL)
+ * receive the routing.  For MOE_ACT_BF16 the down GEMV and the weighted sum are fused (the
+ * per-expert outputs are rounded to bf16 before weighting, exactly as y_perm would be). */
+moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                             int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids,
+                             float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- synthetic inputs
+ * Not part of the layer: the counter-based generator that benchmarks and tests use to create
+ * expert weights on the device.  Element n (row-major) of expert `e`'s matrix [rows][K] is
+ * float32(2*(u0+u1+u2+u3) - 262140) * c, where u0..u3 are the 16-bit fields (low to high) of
+ * SplitMix64(key + (n+1) * 0x9E3779B97F4A7C15) and key = SplitMix64((seed << 32) |
+ * (tensor_id << 24) | e).  Writes n_experts consecutive matrices starting at expert_first to
+ * out [n_experts][rows][K].  seed < 2^32, tensor_id < 256. */
+moe_status moe_synth_weights(uint64_t seed, uint32_t tensor_id, uint32_t expert_first, uint32_t n_experts,
+                             int64_t rows, int64_t K, float c, float* out, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

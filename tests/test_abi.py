@@ -1,0 +1,58 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds for sm_103a, loads, and
+exports every entry point that include/moe.h declares; size helpers follow the documented rules."""
+import os
+import re
+
+import pytest
+
+from bit_expert_ffn_moe_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return B.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_entry_points()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(B.EXPORTED) == names
+
+
+def test_status_strings_and_version(lib):
+    assert B.moe_abi_version() == 1
+    assert B.status_string(0) == "MOE_OK"
+    assert B.status_string(5) == "MOE_ERR_TIMEOUT"
+
+
+def test_size_helpers():
+    # tensor-core scale layout: one 512-byte atom per 128 rows x 128 columns
+    assert B.moe_mxfp4_mma_scale_bytes(128, 128) == 512
+    assert B.moe_mxfp4_mma_scale_bytes(256, 8192) == 2 * 64 * 512
+    assert B.moe_mxfp4_mma_scale_bytes(100, 128) == 0
+    # padded rows: every touched expert may waste up to 127 rows
+    assert B.moe_padded_rows(4096, 8, 128) == 32768 + 128 * 127 + 0 or B.moe_padded_rows(4096, 8, 128) % 128 == 0
+    assert B.moe_padded_rows(1, 8, 128) == 1024
+    assert B.moe_workspace_size(16, 256, 8, 2, 512, B.MOE_ACT_BF16) > 0
+    assert B.moe_workspace_size(16, 256, 8, 2, 512, B.MOE_ACT_MXFP4) > B.moe_workspace_size(16, 256, 8, 2, 512, 0)
+    # shape rules
+    assert B.moe_workspace_size(16, 200, 8, 2, 512, 0) == 0      # d % 128
+    assert B.moe_workspace_size(16, 256, 8, 9, 512, 0) == 0      # k > E
+    assert B.moe_workspace_size(16, 256, 2048, 2, 512, 0) == 0   # E > 1024
+    assert B.moe_workspace_size(16, 256, 8, 2, 96, B.MOE_ACT_MXFP4) == 0  # I % 128 on the MXFP4 path
+
+
+def test_library_is_built_for_sm103a_only():
+    from bit_expert_ffn_moe_gb300 import _build
+    assert "arch=compute_103a,code=sm_103a" in _build.NVCC_FLAGS
+    assert os.path.exists(_build.LIB)

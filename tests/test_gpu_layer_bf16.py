@@ -1,0 +1,109 @@
+"""GPU parity of the decode-shape path (MOE_ACT_BF16): the whole layer against the oracle, and the
+step-by-step entry points against the fused layer call."""
+import numpy as np
+import pytest
+import torch
+
+from bit_expert_ffn_moe_gb300 import binding as B
+from bit_expert_ffn_moe_gb300 import inputs as IN
+from bit_expert_ffn_moe_gb300.layer import DeviceLayer, layer_forward, make_workspace
+from moe_testlib import bf16_tensor_to_f32, bits_to_device, check_outputs, check_weights, oracle_expert_weights
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+_layers = {}
+
+
+def get_layer(name):
+    if name not in _layers:
+        _layers.clear()
+        torch.cuda.empty_cache()
+        _layers[name] = DeviceLayer(IN.CONFIGS[name])
+    return _layers[name]
+
+
+def oracle_layer(layer, xb, act_fmt, tokens=None):
+    cfg = layer.cfg
+    return O.moe_layer(xb, layer.W_r_host, layer.b_host, cfg.k, oracle_expert_weights(cfg, layer.seed), act_fmt,
+                       tokens=tokens)
+
+
+@pytest.mark.parametrize("name,calls", [("tiny", [0, 1]), ("decode", [0, 1, 2]), ("spec_verify", [0])])
+def test_layer_matches_oracle(name, calls):
+    layer = get_layer(name)
+    cfg = layer.cfg
+    ws = make_workspace(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
+    for call in calls:
+        xb = IN.make_x(cfg, call=call)
+        y, ids, w = layer_forward(layer, bits_to_device(xb), B.MOE_ACT_BF16, ws=ws, want_routing=True)
+        ref = oracle_layer(layer, xb, O.ACT_BF16)
+        np.testing.assert_array_equal(ids.cpu().numpy(), ref["ids"])
+        check_weights(w.cpu().numpy(), ref["w"])
+        check_outputs(bf16_tensor_to_f32(y), ref["y"], "%s call %d" % (name, call))
+    assert B.moe_get_device_status(ws) == B.MOE_OK
+
+
+def test_step_calls_equal_layer_call_and_oracle_h():
+    layer = get_layer("tiny")
+    cfg = layer.cfg
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    P = T * k
+    xb = IN.make_x(cfg, call=3)
+    x = bits_to_device(xb)
+    ws = make_workspace(T, d, E, k, I, B.MOE_ACT_BF16)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    ids, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device="cuda")
+    counts, offsets, perm, inv = (torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(P, **i32),
+                                  torch.empty(P, **i32))
+    h = torch.empty((P, I), dtype=torch.bfloat16, device="cuda")
+    y_perm = torch.empty((P, d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    B.moe_route(x, layer.W_r, layer.b, T, d, E, k, ids, w, ws)
+    B.moe_permute(x, ids, T, d, E, k, B.MOE_ACT_BF16, counts, offsets, perm, inv, None, None, ws)
+    B.moe_expert_up_swiglu(x, None, None, B.MOE_ACT_BF16, perm, offsets, T, d, E, k, I, layer.weights, h, None, ws)
+    B.moe_expert_down(h, None, B.MOE_ACT_BF16, perm, offsets, T, d, E, k, I, layer.weights, y_perm, ws)
+    B.moe_combine(y_perm, inv, w, T, k, d, y)
+    y_fused = layer_forward(layer, x, B.MOE_ACT_BF16)
+    assert torch.equal(y.view(torch.int16), y_fused.view(torch.int16))
+    # h and y_perm rows against the oracle's intermediates
+    ref = O.moe_layer(xb, layer.W_r_host, layer.b_host, k, oracle_expert_weights(cfg, layer.seed), O.ACT_BF16,
+                      want_intermediates=True)
+    inv_h = inv.cpu().numpy().reshape(T, k)
+    h_gpu = bf16_tensor_to_f32(h)
+    yp_gpu = bf16_tensor_to_f32(y_perm)
+    h_ref = np.stack([ref["h"][(t, j)][0] for t in range(T) for j in range(k)])
+    yp_ref = np.stack([ref["y_perm"][(t, j)] for t in range(T) for j in range(k)])
+    rows = inv_h.reshape(-1)
+    check_outputs(h_gpu[rows], h_ref, "h")
+    check_outputs(yp_gpu[rows], yp_ref, "y_perm")
+
+
+def test_zero_tokens_and_zero_input():
+    layer = get_layer("tiny")
+    cfg = layer.cfg
+    x0 = torch.zeros((0, cfg.d), dtype=torch.bfloat16, device="cuda")
+    ws = make_workspace(1, cfg.d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
+    y0 = torch.empty((0, cfg.d), dtype=torch.bfloat16, device="cuda")
+    B.moe_layer_forward(x0, layer.W_r, layer.b, 0, cfg.d, cfg.E, cfg.k, cfg.I, layer.weights, B.MOE_ACT_BF16, y0,
+                        None, None, ws)
+    xz = torch.zeros((5, cfg.d), dtype=torch.bfloat16, device="cuda")
+    y, ids, w = layer_forward(layer, xz, B.MOE_ACT_BF16, want_routing=True)
+    assert torch.count_nonzero(y.float()) == 0
+    np.testing.assert_array_equal(ids.cpu().numpy(), np.tile(np.arange(cfg.k), (5, 1)))
+
+
+def test_bad_arguments_are_rejected():
+    layer = get_layer("tiny")
+    cfg = layer.cfg
+    x = torch.zeros((4, cfg.d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    ws = make_workspace(4, cfg.d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
+    with pytest.raises(B.MoeError) as e:
+        B.moe_layer_forward(x, layer.W_r, layer.b, 4, cfg.d, cfg.E, cfg.k, cfg.I, layer.weights, B.MOE_ACT_BF16, y,
+                            None, None, ws, ws_bytes=1024)
+    assert e.value.status == B.MOE_ERR_WORKSPACE
+    with pytest.raises(B.MoeError) as e:
+        B.moe_layer_forward(x, layer.W_r, layer.b, 4, cfg.d, cfg.E, cfg.E + 1, cfg.I, layer.weights,
+                            B.MOE_ACT_BF16, y, None, None, ws)
+    assert e.value.status == B.MOE_ERR_UNSUPPORTED_SHAPE

@@ -366,3 +366,11 @@ def test_synth_weights_statistics():
     assert abs(w.std() - 0.02) < 2e-4 and abs(w.mean()) < 2e-4
     part = IN.synth_weights(1234, 2, 7, 256, 1024, 0.02, row_start=100, row_count=5)
     np.testing.assert_array_equal(part, w[100:105])
+
+
+def test_synth_c_and_numpy_definitions_agree():
+    a = IN.synth_weights(77, 1, 3, 64, 512, 0.02, use_c=True)
+    b = IN.synth_weights(77, 1, 3, 64, 512, 0.02, use_c=False)
+    np.testing.assert_array_equal(a, b)
+    key = IN._host().inputs_stream_key(77, 1, 3)
+    assert key == int(IN.stream_key(77, 1, 3))
