@@ -255,7 +255,8 @@ def run_gpu(args, cfg, rank, world, local):
         with torch.cuda.graph(graph, stream=stream):
             for s in range(args.steps):
                 step(s, stream)
-        graph.replay()  # one untimed replay
+        with torch.cuda.stream(stream):
+            graph.replay()  # one untimed replay
         stream.synchronize()
 
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -263,14 +264,14 @@ def run_gpu(args, cfg, rank, world, local):
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         t_wall0 = time.perf_counter()
-        start.record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            with torch.cuda.stream(stream):
+        with torch.cuda.stream(stream):  # the graph replays on the current stream
+            start.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
                 for s in range(args.steps):
                     step(s, stream)
-        end.record(stream)
+            end.record(stream)
         end.synchronize()
         t_wall = time.perf_counter() - t_wall0
     torch.cuda.synchronize(dev)
@@ -330,9 +331,11 @@ def dtype_name(fmt):
 
 
 def launches_per_step(fmt, T, d, E, k):
+    # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
+    # gate/up, down+sum.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum
     if fmt == 0:
         return 3 if T <= 8 else 7
-    return 9
+    return 10
 
 
 def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):

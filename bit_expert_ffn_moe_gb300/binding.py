@@ -26,7 +26,7 @@ MOE_ACT_MXFP4 = 1
 
 # every entry point declared in include/moe.h
 EXPORTED = (
-    "moe_status_string", "moe_abi_version", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
+    "moe_status_string", "moe_abi_version", "moe_last_cuda_error", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
     "moe_mxfp4_scales_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_layer_forward", "moe_synth_weights",
@@ -36,7 +36,10 @@ EXPORTED = (
 class MoeError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
-        super().__init__("%s failed: %s" % (fn, status_string(status)))
+        msg = "%s failed: %s" % (fn, status_string(status))
+        if status == MOE_ERR_CUDA:
+            msg += " (%s)" % load().moe_last_cuda_error().decode()
+        super().__init__(msg)
 
 
 class moe_expert_weights(ctypes.Structure):
@@ -53,6 +56,7 @@ WP = ctypes.POINTER(moe_expert_weights)
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [I32]),
     "moe_abi_version": (I32, []),
+    "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_mxfp4_pack": (I32, [P, I64, I64, P, P, P]),
     "moe_mxfp4_unpack": (I32, [P, P, I64, I64, P, P]),
     "moe_mxfp4_mma_scale_bytes": (SZ, [I64, I64]),

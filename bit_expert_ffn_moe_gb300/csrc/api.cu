@@ -27,7 +27,13 @@ moe_status check_device() {
     return ok ? MOE_OK : MOE_ERR_DEVICE;
 }
 
-moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+moe_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    g_last_cuda_error = e;
+    return MOE_ERR_CUDA;
+}
 
 #define MOE_TRY(expr)                               \
     do {                                            \
@@ -97,6 +103,10 @@ const char* moe_status_string(moe_status s) {
 }
 
 int moe_abi_version(void) { return kAbiVersion; }
+
+const char* moe_last_cuda_error(void) {
+    return g_last_cuda_error == cudaSuccess ? "no error" : cudaGetErrorString(g_last_cuda_error);
+}
 
 // ---------------------------------------------------------------- MXFP4 helpers
 

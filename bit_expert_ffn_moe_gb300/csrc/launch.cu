@@ -24,7 +24,7 @@ cudaError_t ensure_dyn_smem(const void* func, size_t bytes) {
 
 cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
                           void** args) {
-    if (smem > 48 * 1024) {
+    if (smem > 0) {  // static + dynamic shared memory may pass 48 KB even when smem alone does not
         cudaError_t err = ensure_dyn_smem(func, smem);
         if (err != cudaSuccess) return err;
     }

@@ -88,6 +88,9 @@ const char* moe_status_string(moe_status s);
 /* ABI version of this header (incremented on incompatible changes). */
 int moe_abi_version(void);
 
+/* Description of the CUDA error behind the calling thread's last MOE_ERR_CUDA (static string). */
+const char* moe_last_cuda_error(void);
+
 /* ---------------------------------------------------------------- MXFP4 helpers
  * Block-scaled 4-bit format of the expert weights (DGX Spark news item, section 2; Muse
  * Spark Open explainer, section 11).  Quantisation rule (OCP MX v1.0): per 32-element block,

@@ -1,0 +1,79 @@
+"""Host-side logic of the benchmark: the byte/flop model against the Muse Spark Open explainer's
+own worked numbers (sections 10-14), and the multi-process (replica) timing path on CPU with
+gloo ranks."""
+import math
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_expert_size_model_matches_the_explainer():
+    # section 10: one expert holds about 50 million weights (3 matrices of 4096 x 4096)
+    d = I = 4096
+    assert abs(3 * d * I / 1e6 - 50.3) < 0.1
+    # section 11/13: at about 4.5 bits per weight one expert is about 28 MB ...
+    b = bench.expert_bytes(d, I, bits_per_weight=4.5)
+    assert abs(b / 1e6 - 28.3) < 0.1
+    # ... read in about 5.9 us (an H200-class 4.8 TB/s), and about 21 us in bf16
+    assert abs(bench.read_time_us(b, 4.8e12) - 5.9) < 0.05
+    assert abs(bench.read_time_us(bench.expert_bytes(d, I, 16), 4.8e12) - 21.0) < 0.1
+    # compute: 2 flops per weight per token, about 0.1 us per token at about 1 PFLOP/s
+    f = bench.flops_per_token_expert(d, I)
+    assert abs(f / 1e6 - 100.7) < 0.1
+    t_tok = f / 1.0e15 * 1e6
+    assert abs(t_tok - 0.1) < 0.001
+    # crossover where reading and computing take equally long: about 58 tokens per expert
+    assert 56 <= bench.crossover_tokens(5.9, 0.1) <= 60
+    # section 12: 753 tokens x 8 choices over 256 experts is about 24 tokens per expert
+    assert abs(753 * 8 / 256 - 23.5) < 0.1
+    # section 14: 32 experts per GPU read once is about 190 us; 3,012 tokens x 8 / 8 GPUs of
+    # compute at 0.1 us is about 300 us
+    assert abs(32 * 5.9 - 189) < 1
+    assert abs(3012 * 8 / 8 * 0.1 - 301) < 1
+
+
+def test_mxfp4_bytes_per_weight():
+    # 4 bits + one 8-bit scale per 32 weights = 4.25 bits; a decode-config expert is 26.7 MB
+    assert bench.matrix_bytes(32, 32) == 32 * 32 * 4.25 / 8
+    assert abs(bench.expert_bytes(8192, 2048) / 1e6 - 26.74) < 0.01
+    lb = bench.layer_algorithmic_bytes(8192, 2048, 128, 1, 8)
+    assert abs(lb / 1e6 - 218.1) < 0.2
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+    r, w, lr = bench.dist_env()
+    bench.init_dist(w, "gloo")
+    bench.barrier(w)
+    worst = bench.max_over_ranks(10.0 + r, w, "cpu")
+    q.put((r, w, lr, worst))
+    dist.destroy_process_group()
+
+
+def test_replica_timing_takes_the_max_over_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    res = sorted(q.get(timeout=5) for _ in range(2))
+    assert [r[0] for r in res] == [0, 1] and all(r[1] == 2 for r in res)
+    assert all(r[3] == 11.0 for r in res)
