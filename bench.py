@@ -459,19 +459,38 @@ def oracle_sample(args, cfg, n_tokens):
             cache[e] = out
         return cache[e]
 
-    xs = [IN.make_x(cfg, call=c) for c in range(n_tokens)]
-    # pre-generate the experts the sample touches (untimed: input generation)
-    for xb in xs:
-        ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
-        for e in np.unique(ids):
-            weights(int(e))
+    act = O.ACT_BF16 if args.fmt == "bf16" else O.ACT_MXFP4
+    if cfg.T <= 8:
+        # decode sizes: whole layer calls
+        xs = [IN.make_x(cfg, call=c) for c in range(n_tokens)]
+        for xb in xs:  # pre-generate the experts the sample touches (untimed: input generation)
+            ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
+            for e in np.unique(ids):
+                weights(int(e))
+        t0 = time.perf_counter()
+        for xb in xs:
+            O.moe_layer(xb, W_r, b, cfg.k, weights, act)
+        dt = time.perf_counter() - t0
+        return dict(value=round(cfg.T * n_tokens / dt, 3), unit=UNIT, cores=threads, kind="oracle",
+                    sample="%d layer calls of T=%d (full routing, all %d touched experts per call, fp64 oracle), "
+                           "weights pre-generated" % (n_tokens, cfg.T, cfg.k), seconds=round(dt, 2))
+    # prefill sizes: routing of the whole chunk, expert work for a token sample; per-token cost =
+    # routing time / T + expert time / sample size
+    xb = IN.make_x(cfg, call=0)
+    tokens = np.arange(0, cfg.T, max(1, cfg.T // n_tokens))[:n_tokens]
     t0 = time.perf_counter()
-    for xb in xs:
-        O.moe_layer(xb, W_r, b, cfg.k, weights, O.ACT_BF16 if args.fmt == "bf16" else O.ACT_MXFP4)
-    dt = time.perf_counter() - t0
-    return dict(value=round(cfg.T * n_tokens / dt, 3), unit=UNIT, cores=threads, kind="oracle",
-                sample="%d layer calls of T=%d (full routing, all %d touched experts per call, fp64 oracle), "
-                       "weights pre-generated" % (n_tokens, cfg.T, cfg.k), seconds=round(dt, 2))
+    ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
+    t_route = time.perf_counter() - t0
+    for e in np.unique(ids[tokens]):
+        weights(int(e))
+    t0 = time.perf_counter()
+    O.moe_layer(xb[tokens], W_r, b, cfg.k, weights, act)
+    t_exp = time.perf_counter() - t0
+    per_tok = t_route / cfg.T + t_exp / len(tokens)
+    return dict(value=round(1.0 / per_tok, 3), unit=UNIT, cores=threads, kind="oracle",
+                sample="routing of all %d tokens (%.2f s) + expert FFNs and sum for %d sampled tokens (%.2f s), "
+                       "fp64 oracle, weights pre-generated; tokens/s = 1 / (route/T + experts/sample)"
+                       % (cfg.T, t_route, len(tokens), t_exp), seconds=round(t_route + t_exp, 2))
 
 
 def run_reference(args, cfg, rank, world):
