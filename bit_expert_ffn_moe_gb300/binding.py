@@ -28,7 +28,7 @@ MOE_ACT_MXFP4 = 1
 EXPORTED = (
     "moe_status_string", "moe_abi_version", "moe_last_cuda_error", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
     "moe_mxfp4_scales_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
-    "moe_get_device_status", "moe_route", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
+    "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_layer_forward", "moe_synth_weights",
 )
 
@@ -66,6 +66,7 @@ _SIGS = {
     "moe_workspace_init": (I32, [P, SZ, P]),
     "moe_get_device_status": (I32, [P, P, ctypes.POINTER(I32)]),
     "moe_route": (I32, [P, P, P, I32, I32, I32, I32, P, P, P, SZ, P]),
+    "moe_route_noalloc": (I32, [P, P, P, I32, I32, I32, I32, P, P, P]),
     "moe_permute": (I32, [P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P]),
     "moe_expert_up_swiglu": (I32, [P, P, P, I32, P, P, I32, I32, I32, I32, I32, WP, P, P, P, SZ, P]),
     "moe_expert_down": (I32, [P, P, I32, P, P, I32, I32, I32, I32, I32, WP, P, P, SZ, P]),
@@ -181,6 +182,11 @@ def _ws_bytes(ws, ws_bytes):
 def moe_route(x, W_r, b, T, d, E, k, ids, w, ws, ws_bytes=None, stream=None):
     _check("moe_route", load().moe_route(_p(x), _p(W_r), _p(b), T, d, E, k, _p(ids), _p(w), _p(ws),
                                          _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_route_noalloc(x, W_r, b, T, d, E, k, ids, w, stream=None):
+    _check("moe_route_noalloc", load().moe_route_noalloc(_p(x), _p(W_r), _p(b), T, d, E, k, _p(ids), _p(w),
+                                                         _stream(stream)))
 
 
 def moe_permute(x, ids, T, d, E, k, fmt, counts, offsets, perm_token, inv_pos, xa, xa_s, ws, ws_bytes=None,

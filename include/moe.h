@@ -148,6 +148,21 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream, moe_status* out)
 moe_status moe_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                      int32_t* ids, float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_route without a workspace and without any allocation (no counterpart in the paper: this
+ * serves callers that cannot allocate device memory or own a scratch buffer when they route --
+ * code running inside a global-mode CUDA graph capture, where allocation calls are not
+ * permitted; hosts whose fixed device memory pool refuses further allocations; foreign-function
+ * callers that cannot size and keep a workspace).  Same arguments and results as moe_route.
+ * Its scratch (the T*E fp32 logits) is one fixed array of 524288 floats (2 MiB) in the
+ * library's device memory, held by every GPU that loads the library until the process exits;
+ * T*E > 524288 returns MOE_ERR_UNSUPPORTED_SHAPE.  The first call on a device, with that device
+ * current, looks up the array's address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  All calls share the array: every call writes the logits it reads, so nothing
+ * carries over, but calls whose work overlaps on the GPU (different streams, or different host
+ * threads) race on it and must be serialised by the caller. */
+moe_status moe_route_noalloc(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                             int32_t* ids, float* w, moe_stream_t stream);
+
 /* Permutation by expert (section 12).  The T*k pairs (t, j) are ordered by (ids[t][j], t, j):
  *   counts[E]      pairs per expert
  *   offsets[E+1]   exclusive prefix sum of counts
