@@ -215,6 +215,7 @@ moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint
     PlanView plan = plan_view(ws, L, E);
     if (fmt == MOE_ACT_BF16) {
         if (!x || !perm_token || !aligned(x, 16)) return MOE_ERR_INVALID_ARG;
+        if (!gemv_supported(d, I)) return MOE_ERR_UNSUPPORTED_SHAPE;
         return from_cuda(launch_gemv_up(x, perm_token, offsets, plan, T, d, E, k, I, W,
                                         static_cast<uint16_t*>(h), st, false));
     }
@@ -238,8 +239,9 @@ moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, c
     PlanView plan = plan_view(ws, L, E);
     if (fmt == MOE_ACT_BF16) {
         if (!perm_token) return MOE_ERR_INVALID_ARG;
-        return from_cuda(launch_gemv_down(static_cast<const uint16_t*>(h), perm_token, offsets, plan, nullptr, nullptr,
-                                          T, d, E, k, I, W, y_perm, nullptr, st, false));
+        if (!gemv_supported(d, I)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        return from_cuda(launch_gemv_down(static_cast<const uint16_t*>(h), perm_token, offsets, plan, nullptr, T, d, E,
+                                          k, I, W, y_perm, nullptr, st, false));
     }
     if (!h_s) return MOE_ERR_INVALID_ARG;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
@@ -275,18 +277,20 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
     int32_t* offsets = reinterpret_cast<int32_t*>(at(ws, L.offsets));
     int32_t* perm = reinterpret_cast<int32_t*>(at(ws, L.perm));
     int32_t* inv = reinterpret_cast<int32_t*>(at(ws, L.inv));
+    float* row_w = reinterpret_cast<float*>(at(ws, L.row_w));
 
     if (fmt == MOE_ACT_BF16) {
+        if (!gemv_supported(d, I)) return MOE_ERR_UNSUPPORTED_SHAPE;
         if (route_decode_supported(T, d, E, k)) {
             MOE_CUDA(launch_route_decode(x, W_r, b, T, d, E, k, reinterpret_cast<float*>(at(ws, L.logits)), ids_b, w_b,
-                                         counts, offsets, perm, inv, plan, ctrl, st, true));
+                                         counts, offsets, perm, inv, row_w, plan, ctrl, st, true));
         } else {
             MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
-            MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
+            MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true, w_b, row_w));
         }
         uint16_t* h = reinterpret_cast<uint16_t*>(at(ws, L.h));
         MOE_CUDA(launch_gemv_up(x, perm, offsets, plan, T, d, E, k, I, W, h, st, true));
-        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, ids_b, w_b, T, d, E, k, I, W, nullptr, y, st, true));
+        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, row_w, T, d, E, k, I, W, nullptr, y, st, true));
         return MOE_OK;
     }
     MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));

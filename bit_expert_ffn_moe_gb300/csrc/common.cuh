@@ -33,7 +33,7 @@ struct PlanView {
 };
 
 struct WsLayout {
-    size_t ctrl = 0, logits = 0, plan = 0, ids = 0, w = 0, counts = 0, offsets = 0, perm = 0, inv = 0,
+    size_t ctrl = 0, logits = 0, plan = 0, ids = 0, w = 0, counts = 0, offsets = 0, perm = 0, inv = 0, row_w = 0,
            xq = 0, xs = 0, xa = 0, xa_s = 0, h = 0, h_s = 0, y_perm = 0, total = 0;
     int64_t pad_rows = 0;
 };
@@ -69,6 +69,7 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     L.offsets = take(sizeof(int32_t) * (size_t)(E + 1));
     L.perm = take(sizeof(int32_t) * (size_t)P);
     L.inv = take(sizeof(int32_t) * (size_t)P);
+    L.row_w = take(sizeof(float) * (size_t)P);
     if (fmt == MOE_ACT_MXFP4) {
         L.pad_rows = padded_rows(T, k, E);
         L.xq = take((size_t)T * d / 2);
@@ -196,12 +197,14 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, 
 // Decode route: logits, then the last CTA runs top-k and the whole permutation (small T).
 cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                 float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
-                                int32_t* perm_token, int32_t* inv_pos, PlanView plan, Ctrl* ctrl,
+                                int32_t* perm_token, int32_t* inv_pos, float* row_w, PlanView plan, Ctrl* ctrl,
                                 cudaStream_t st, bool pdl);
 bool route_decode_supported(int T, int d, int E, int k);
 
+// row_w (optional, with w): gate weight of each permuted row, row_w[inv_pos[t*k+j]] = w[t][j].
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
-                           int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl);
+                           int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl,
+                           const float* w = nullptr, float* row_w = nullptr);
 cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
                                     const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
                                     uint8_t* xs, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl);
@@ -209,9 +212,11 @@ cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int 
 cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,
                            cudaStream_t st, bool pdl);
+// y != nullptr: fused weighted sum into y [T][d] using row_w; otherwise bf16 y_perm [P][d].
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
-                             const int32_t* ids, const float* w, int T, int d, int E, int k, int I,
-                             const moe_expert_weights* W, uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl);
+                             const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
+                             uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl);
+bool gemv_supported(int d, int I);
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                            uint16_t* y, cudaStream_t st, bool pdl);
 

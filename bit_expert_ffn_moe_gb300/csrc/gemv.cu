@@ -2,135 +2,296 @@
 //
 // At decode sizes every chosen expert sees one or a few tokens, so the expert matrices are read
 // once and used for very little arithmetic: the time is the weight read (Muse Spark Open
-// explainer, section 13: about 98% of the time waiting on the 4-bit weight read at one token per
-// expert; DGX Spark news item, section 1: batch-1 generation is bound by weight reads).  These
-// kernels therefore stream each weight row once with coalesced 128-bit loads (one 16-byte load
-// = one 32-element MXFP4 block), decode E2M1 with the hardware conversion, and accumulate in
-// fp32 with packed fp32x2 FMAs; the block scale is applied once per 32-element partial.
-//
-// Activations are held in shared memory as fp32 in a "block-interleaved" order: float4 number q
-// (elements 4q..4q+3) of block b sits at float4 index q*NB + b, so the 32 lanes of a warp,
-// which work on 32 consecutive blocks, read 32 consecutive float4s (no bank conflicts).
+// explainer, section 13: at one token per expert about 98% of the time waits on the 4-bit weight
+// read; DGX Spark news item, section 1: batch-1 generation is bound by weight reads).  These
+// kernels therefore stream each weight row exactly once with coalesced 128-bit loads (16 bytes =
+// one 32-element MXFP4 block) and keep the work per weight byte small:
+//   - E2M1 codes become exact f16 pairs with the hardware conversion (cvt.rn.f16x2.e2m1x2);
+//   - activation rows are staged once per CTA as f16, each row prescaled by a power of two so
+//     that its largest magnitude lies in [2^14, 2^15) (a bf16 value then converts exactly unless
+//     it is more than 2^28 times smaller than the row maximum);
+//   - products w*x are exact and accumulate in fp32 (fma.rn.f32.f16); the block scale and the
+//     row's prescale are applied once per 32-element partial.
+// Work split: a "row group" of G threads covers one weight row, thread j owning K-block j (and
+// j + G when K > 8192), so each thread reads its activation block from shared memory once per
+// batch of kR weight rows rather than once per row.  The kR x Q partial dot products are summed
+// over the group by a warp transpose-reduction and a cross-warp pass through shared memory.
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kGemvThreads = 256;  // 8 warps
-constexpr int kRowsPerWarp = 4;
-constexpr int kRowsPerCta = 8 * kRowsPerWarp;
+constexpr int kThr = 256;       // threads per CTA
+constexpr int kR = 8;           // weight rows per batch per row group
+constexpr int kMaxQ = 4;        // activation rows (tokens / pairs) per pass
+constexpr int kDownMaxRows = 64;  // staged permuted rows per down CTA
 
-// Stage one bf16 row of n elements (n % 32 == 0) into shared memory in block-interleaved fp32.
-__device__ __forceinline__ void stage_row_bf16(const uint16_t* __restrict__ src, int n, float4* dst) {
-    const int nb = n / 32;
-    for (int i = threadIdx.x; i < n / 8; i += blockDim.x) {  // 8 bf16 = 16 bytes per step
-        uint4 u = *reinterpret_cast<const uint4*>(src + 8 * i);
-        const int b = i / 4, q = (i % 4) * 2;  // elements 8i..8i+7 = float4s q, q+1 of block b
-        dst[q * nb + b] = make_float4(bf16_bits_to_f32(u.x & 0xFFFF), bf16_bits_to_f32(u.x >> 16),
-                                      bf16_bits_to_f32(u.y & 0xFFFF), bf16_bits_to_f32(u.y >> 16));
-        dst[(q + 1) * nb + b] = make_float4(bf16_bits_to_f32(u.z & 0xFFFF), bf16_bits_to_f32(u.z >> 16),
-                                            bf16_bits_to_f32(u.w & 0xFFFF), bf16_bits_to_f32(u.w >> 16));
-    }
+// ------------------------------------------------------------------ helpers
+
+// acc += w.lo * x.lo + w.hi * x.hi with f16 operands and an fp32 accumulator (exact products).
+__device__ __forceinline__ float dot2_f16(uint32_t w2, uint32_t x2, float acc) {
+    asm("{\n\t.reg .f16 a0, a1, b0, b1;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\t"
+        "mov.b32 {b0, b1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, a0, b0, %0;\n\t"
+        "fma.rn.f32.f16 %0, a1, b1, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w2), "r"(x2));
+    return acc;
 }
 
-// Partial dot product of one 32-element MXFP4 block (16 bytes of codes) with a block of
-// activations in block-interleaved shared memory; returns the unscaled fp32 sum.
-__device__ __forceinline__ float block_dot(const uint4& codes, const float4* __restrict__ act, int nb, int b) {
-    float2 acc = make_float2(0.f, 0.f);
+// Unscaled dot product of one 32-element MXFP4 block (16 bytes of codes) with 32 f16 activations
+// held as 16 f16x2 words (elements 2m, 2m+1 in word m, low half first).
+__device__ __forceinline__ float block_dot(const uint4& codes, const uint32_t (&x)[16]) {
     const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
+    float a0 = 0.f, a1 = 0.f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
         uint32_t h[4];
-        e2m1x8_to_h2(words[m], h);
-        const float4 xa = act[(2 * m) * nb + b];
-        const float4 xb = act[(2 * m + 1) * nb + b];
-        acc = __ffma2_rn(h2_to_f2(h[0]), make_float2(xa.x, xa.y), acc);
-        acc = __ffma2_rn(h2_to_f2(h[1]), make_float2(xa.z, xa.w), acc);
-        acc = __ffma2_rn(h2_to_f2(h[2]), make_float2(xb.x, xb.y), acc);
-        acc = __ffma2_rn(h2_to_f2(h[3]), make_float2(xb.z, xb.w), acc);
+        e2m1x8_to_h2(words[m], h);  // elements 8m .. 8m+7 as 4 f16x2
+        a0 = dot2_f16(h[0], x[4 * m + 0], a0);
+        a1 = dot2_f16(h[1], x[4 * m + 1], a1);
+        a0 = dot2_f16(h[2], x[4 * m + 2], a0);
+        a1 = dot2_f16(h[3], x[4 * m + 3], a1);
     }
-    return acc.x + acc.y;
+    return a0 + a1;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Sum V values over the 32 lanes of a warp; afterwards lane l holds the warp sum of value
+// l >> (5 - log2 V), for V in {8, 16, 32}.
+template <int V>
+__device__ __forceinline__ float warp_transpose_reduce(float (&a)[V], int lane) {
 #pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    for (int half = V / 2, mask = 16; half >= 1; half /= 2, mask /= 2) {
+        const bool upper = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? a[i] : a[i + half];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, mask);
+            a[i] = (upper ? a[i + half] : a[i]) + recv;
+        }
+    }
+    float v = a[0];
+#pragma unroll
+    for (int mask = (32 / V) / 2; mask >= 1; mask /= 2) v += __shfl_xor_sync(0xffffffffu, v, mask);
     return v;
 }
 
-// ------------------------------------------------------------------ gate/up + SwiGLU
-// Grid: (I / kRowsPerCta, slots).  Slot u handles the u-th active expert; each warp computes
-// kRowsPerWarp rows i of W_g and W_u for the expert's tokens, TC tokens at a time.
-// CPL = 16-byte chunks per lane per pass over a row.
-template <int TC, int CPL>
-__global__ void __launch_bounds__(kGemvThreads)
-gemv_up_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm_token,
-               const int32_t* __restrict__ offsets, PlanView plan, int d, int I, const uint8_t* __restrict__ gq,
-               const uint8_t* __restrict__ gs, const uint8_t* __restrict__ uq, const uint8_t* __restrict__ us,
-               uint16_t* __restrict__ h) {
-    extern __shared__ float4 xs4[];  // [TC][d/4] block-interleaved
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    pdl_wait();
-    const int slot = blockIdx.y;
-    if (slot >= plan.scalars[0]) return;
-    const int e = plan.active[slot];
-    const int r0 = offsets[e], n = offsets[e + 1] - r0;
-    const int nb = d / 32;
-    const size_t row_bytes = (size_t)d / 2;
+// Stage activation rows (bf16, K elements each) as prescaled f16 in block-interleaved order:
+// 16-byte unit c (elements 8c..8c+7) of block b of staged row q sits at uint4 index
+// (q * 4 + c) * nb + b, so threads owning consecutive blocks read consecutive units.
+// inv[q] receives 2^-p, the factor that undoes the row's prescale 2^p.  One warp per row.
+__device__ void stage_rows_f16(const uint16_t* __restrict__ src, const int* rows, int nq, int K, uint4* dst,
+                               float* inv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int nb = K / 32, units = K / 8;
+    for (int q = warp; q < nq; q += nwarps) {
+        const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K);
+        uint32_t mx = 0;
+        for (int u = lane; u < units; u += 32) {
+            const uint4 v = s[u];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+        }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        // biased exponent E of max |x|; p = 141 - E puts the maximum in [2^14, 2^15)
+        int p = (mx == 0) ? 0 : 141 - (int)(mx >> 7);
+        p = max(-126, min(126, p));
+        const float up = __uint_as_float((uint32_t)(127 + p) << 23);
+        const float down = __uint_as_float((uint32_t)(127 - p) << 23);
+        for (int u = lane; u < units; u += 32) {
+            const uint4 v = s[u];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half lo = __float2half_rn(bf16_bits_to_f32(w[i] & 0xFFFFu) * up);
+                const __half hi = __float2half_rn(bf16_bits_to_f32(w[i] >> 16) * up);
+                o[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+            }
+            const int b = u >> 2, c = u & 3;
+            dst[((size_t)q * 4 + c) * nb + b] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (lane == 0) inv[q] = down;
+    }
+}
 
-    for (int tc0 = 0; tc0 < n; tc0 += TC) {
-        const int nt = min(TC, n - tc0);
-        __syncthreads();
-        for (int t = 0; t < nt; ++t)
-            stage_row_bf16(x + (size_t)perm_token[r0 + tc0 + t] * d, d, xs4 + (size_t)t * (d / 4));
-        __syncthreads();
-        for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-            const int i = blockIdx.x * kRowsPerCta + warp * kRowsPerWarp + rr;
-            const size_t grow = (size_t)e * I + i;
-            const uint8_t* gq_row = gq + grow * row_bytes;
-            const uint8_t* uq_row = uq + grow * row_bytes;
-            const uint8_t* gs_row = gs + grow * nb;
-            const uint8_t* us_row = us + grow * nb;
-            float ag[TC], au[TC];
+__device__ __forceinline__ void load_x_block(const uint4* xs, int q, int nb, int b, uint32_t (&x)[16]) {
 #pragma unroll
-            for (int t = 0; t < TC; ++t) ag[t] = au[t] = 0.f;
-            for (int cb = 0; cb < nb; cb += 32 * CPL) {
-                uint4 wg[CPL], wu[CPL];
-                uint32_t sg[CPL], su[CPL];
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v = xs[((size_t)q * 4 + c) * nb + b];
+        x[4 * c + 0] = v.x;
+        x[4 * c + 1] = v.y;
+        x[4 * c + 2] = v.z;
+        x[4 * c + 3] = v.w;
+    }
+}
+
+// Row-group geometry for a contraction of K elements: nb = K/32 blocks, bpt blocks per thread,
+// G threads per group (a power of two >= 32 covering nb / bpt), RG = kThr / G groups per CTA.
+struct Geo {
+    int nb, bpt, G, RG;
+};
+
+__host__ __device__ inline Geo make_geo(int K) {
+    Geo g;
+    g.nb = K / 32;
+    g.bpt = (g.nb + kThr - 1) / kThr;
+    const int need = (g.nb + g.bpt - 1) / g.bpt;
+    int G = 32;
+    while (G < need) G *= 2;
+    g.G = G;
+    g.RG = kThr / G;
+    return g;
+}
+
+struct GemvArgs {
+    const uint8_t* q0;  // up: gate codes; down: down codes
+    const uint8_t* s0;
+    const uint8_t* q1;  // up: up codes
+    const uint8_t* s1;
+    const uint16_t* act;  // up: x [T][d]; down: h [P][I]
+    const int32_t* perm_token;
+    const int32_t* offsets;
+    PlanView plan;
+    const float* row_w;  // down, fused: gate weight of each permuted row
+    int T, K, M_exp, P, E;
+    int tch;             // down: tokens per chunk
+    int outs;            // output features per CTA
+    uint16_t* out;       // up: h [P][I]; down: y_perm [P][d] or y [T][d]
+};
+
+// Weight rows of one batch into registers (rows[j] = global row index, or -1 to skip).
+template <int BPT>
+__device__ __forceinline__ void load_rows(const uint8_t* const (&q)[kR], const uint8_t* const (&s)[kR],
+                                          const size_t (&grow)[kR], int gl, const Geo& geo, size_t row_bytes,
+                                          uint4 (&wv)[kR][BPT], uint32_t (&sv)[kR][BPT]) {
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const int b = cb + lane + 32 * c;
-                    if (b < nb) {
-                        wg[c] = ldg_stream(gq_row + 16 * (size_t)b);
-                        wu[c] = ldg_stream(uq_row + 16 * (size_t)b);
-                        sg[c] = __ldg(gs_row + b);
-                        su[c] = __ldg(us_row + b);
-                    }
-                }
+    for (int j = 0; j < kR; ++j)
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const int b = cb + lane + 32 * c;
-                    if (b < nb) {
-                        const float fg = e8m0_to_f32(sg[c]), fu = e8m0_to_f32(su[c]);
+        for (int c = 0; c < BPT; ++c) {
+            const int b = gl + c * geo.G;
+            if (b < geo.nb) {
+                wv[j][c] = ldg_stream(q[j] + grow[j] * row_bytes + 16 * (size_t)b);
+                sv[j][c] = __ldg(s[j] + grow[j] * geo.nb + b);
+            }
+        }
+}
+
+// kR x Q partial dot products of the thread's blocks: acc[qq * kR + j] for staged row q0 + qq
+// (qq < nq) against weight row j.
+template <int BPT, int Q>
+__device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int gl, const Geo& geo,
+                                           const uint4 (&wv)[kR][BPT], const uint32_t (&sv)[kR][BPT],
+                                           float (&acc)[kR * Q]) {
 #pragma unroll
-                        for (int t = 0; t < TC; ++t) {
-                            if (t < nt) {
-                                const float4* act = xs4 + (size_t)t * (d / 4);
-                                ag[t] = fmaf(block_dot(wg[c], act, nb, b), fg, ag[t]);
-                                au[t] = fmaf(block_dot(wu[c], act, nb, b), fu, au[t]);
-                            }
-                        }
-                    }
+    for (int v = 0; v < kR * Q; ++v) acc[v] = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < Q; ++qq) {
+        if (qq < nq) {
+#pragma unroll
+            for (int c = 0; c < BPT; ++c) {
+                const int b = gl + c * geo.G;
+                if (b < geo.nb) {
+                    uint32_t x[16];
+                    load_x_block(xs, q0 + qq, geo.nb, b, x);
+#pragma unroll
+                    for (int j = 0; j < kR; ++j)
+                        acc[qq * kR + j] = fmaf(block_dot(wv[j][c], x), e8m0_to_f32(sv[j][c]), acc[qq * kR + j]);
                 }
             }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ gate/up + SwiGLU
+// Grid (M_exp / outs, slots): slot u is the u-th active expert.  A batch gives each row group
+// kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens.
+template <int BPT, int Q>
+__global__ void __launch_bounds__(kThr)
+gemv_up_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int kOut = kR / 2;
+    constexpr int V = kR * Q;
+    const Geo geo = make_geo(a.K);
+    uint4* xs = reinterpret_cast<uint4*>(smem);                              // [Q][K/8]
+    float* inv = reinterpret_cast<float*>(smem + (size_t)Q * a.K * 2);      // [Q]
+    float* red = inv + Q;                                                   // [8 warps][32]
+    int* rows = reinterpret_cast<int*>(red + 8 * 32);                       // [Q]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = tid / geo.G, gl = tid % geo.G;
+    const int wpg = geo.G / 32;  // warps per group
+
+    pdl_wait();
+    const int slot = blockIdx.y;
+    if (slot >= a.plan.scalars[0]) return;
+    const int e = a.plan.active[slot];
+    const size_t row_bytes = (size_t)a.K / 2;
+    const int outs_per_group = a.outs / geo.RG;
+    const int nbatch = outs_per_group / kOut;
+    const int i_base = blockIdx.x * a.outs + grp * outs_per_group;
+    const uint8_t* const qsel[kR] = {a.q0, a.q0, a.q0, a.q0, a.q1, a.q1, a.q1, a.q1};
+    const uint8_t* const ssel[kR] = {a.s0, a.s0, a.s0, a.s0, a.s1, a.s1, a.s1, a.s1};
+    auto grows = [&](int bi, size_t (&g)[kR]) {
 #pragma unroll
-            for (int t = 0; t < TC; ++t) {
-                if (t < nt) {
-                    const float g = warp_sum(ag[t]), u = warp_sum(au[t]);
-                    if (lane == t) {
-                        const float hv = g / (1.f + expf(-g)) * u;  // SiLU(g) * u
-                        h[(size_t)(r0 + tc0 + t) * I + i] = f32_to_bf16_bits(hv);
+        for (int j = 0; j < kR; ++j) g[j] = (size_t)e * a.M_exp + i_base + bi * kOut + (j % kOut);
+    };
+
+    uint4 wcur[kR][BPT], wnxt[kR][BPT];
+    uint32_t scur[kR][BPT], snxt[kR][BPT];
+    {
+        size_t g[kR];
+        grows(0, g);
+        load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wcur, scur);  // weights depend only on e
+    }
+    const int r0 = a.offsets[e], n = a.offsets[e + 1] - r0;
+
+    for (int tc0 = 0; tc0 < n; tc0 += Q) {
+        const int nq = min(Q, n - tc0);
+        __syncthreads();
+        if (tid < nq) rows[tid] = a.perm_token[r0 + tc0 + tid];
+        __syncthreads();
+        stage_rows_f16(a.act, rows, nq, a.K, xs, inv);
+        __syncthreads();
+        for (int bi = 0; bi < nbatch; ++bi) {
+            const bool more = bi + 1 < nbatch || tc0 + Q < n;
+            if (more) {
+                size_t g[kR];
+                grows(bi + 1 < nbatch ? bi + 1 : 0, g);
+                load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wnxt, snxt);
+            }
+            float acc[V];
+            batch_dots<BPT, Q>(xs, 0, nq, gl, geo, wcur, scur, acc);
+            red[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
+            __syncthreads();
+            if (gl < 32) {
+                // lane l holds value v = l >> (5 - log2 V); v = qq * kR + j
+                const int v = lane >> (5 - (V == 8 ? 3 : V == 16 ? 4 : 5));
+                const int qq = v / kR, j = v % kR;
+                const bool leader = (lane & ((32 / V) - 1)) == 0;
+                if (leader && qq < nq && j < kOut) {
+                    float g = 0.f, u = 0.f;
+                    for (int w = 0; w < wpg; ++w) {
+                        const int wi = (grp * wpg + w) * 32;
+                        g += red[wi + lane];
+                        u += red[wi + lane + kOut * (32 / V)];
                     }
+                    g *= inv[qq];
+                    u *= inv[qq];
+                    const float hv = g / (1.f + expf(-g)) * u;  // SiLU(g) * u
+                    const int i = i_base + bi * kOut + j;
+                    a.out[(size_t)(r0 + tc0 + qq) * a.M_exp + i] = f32_to_bf16_bits(hv);
                 }
+            }
+            __syncthreads();
+            if (more) {
+#pragma unroll
+                for (int j = 0; j < kR; ++j)
+#pragma unroll
+                    for (int c = 0; c < BPT; ++c) {
+                        wcur[j][c] = wnxt[j][c];
+                        scur[j][c] = snxt[j][c];
+                    }
             }
         }
     }
@@ -138,151 +299,139 @@ gemv_up_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm_
 }
 
 // ------------------------------------------------------------------ down (+ weighted sum)
-// Grid: (d / kRowsPerCta, token chunks of TCH <= 8 tokens).  The CTA stages, for every permuted
-// row whose token lies in its chunk, the bf16 h row (as fp32) and the pair's gate weight.  Rows
-// are in expert-major order, so the active experts form consecutive segments of at most TCH
-// pairs.  Each warp computes kRowsPerWarp output features for every segment, prefetching the
-// next segment's weight rows while it computes the current one.
+// Grid (d / outs, token chunks).  The CTA stages every permuted row whose token lies in its chunk
+// (rows are expert-major, so each active expert forms a consecutive segment), then for each
+// segment computes its outputs: each row group owns kR output features.
 // FUSED: y[t] accumulates w * bf16(expert output) in ascending expert order, which is the slot
-// order j of the token (ids are ascending); otherwise the bf16 expert outputs go to y_perm.
-constexpr int kDownMaxPairs = 64;
-constexpr int kDownMaxTok = 8;
+// order j of the token (ids are ascending); otherwise the bf16 outputs go to y_perm.
+template <int BPT, int Q, bool FUSED>
+__global__ void __launch_bounds__(kThr)
+gemv_down_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int V = kR * Q;
+    const Geo geo = make_geo(a.K);
+    uint4* hs = reinterpret_cast<uint4*>(smem);                                       // [rows][K/8]
+    float* inv = reinterpret_cast<float*>(smem + (size_t)kDownMaxRows * a.K * 2);    // [rows]
+    float* red = inv + kDownMaxRows;                                                 // [8][32]
+    float* ys = red + 8 * 32;                                                        // [tch][outs]
+    int* s_row = reinterpret_cast<int*>(ys + 8 * a.outs);                            // [rows]
+    int* s_tok = s_row + kDownMaxRows;
+    int* s_exp = s_tok + kDownMaxRows;
+    float* s_w = reinterpret_cast<float*>(s_exp + kDownMaxRows);
+    int* s_off = reinterpret_cast<int*>(s_w + kDownMaxRows);                         // [E+1]
+    __shared__ int wtot[8];
+    __shared__ int s_cnt;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = tid / geo.G, gl = tid % geo.G;
+    const int wpg = geo.G / 32;
+    const int t0 = blockIdx.y * a.tch, t1 = min(a.T, t0 + a.tch);
+    const size_t row_bytes = (size_t)a.K / 2;
+    const int n_base = blockIdx.x * a.outs + grp * kR;
 
-template <int CPL>
-__device__ __forceinline__ void load_down_rows(const uint8_t* __restrict__ dq, const uint8_t* __restrict__ ds, int e,
-                                               int d, int nb, int n0, int cb, int lane,
-                                               uint4 (&wv)[kRowsPerWarp][CPL], uint32_t (&sv)[kRowsPerWarp][CPL]) {
-    const size_t row_bytes = (size_t)nb * 16;
-#pragma unroll
-    for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-        const size_t grow = (size_t)e * d + n0 + rr;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            const int b = cb + lane + 32 * c;
-            if (b < nb) {
-                wv[rr][c] = ldg_stream(dq + grow * row_bytes + 16 * (size_t)b);
-                sv[rr][c] = __ldg(ds + grow * nb + b);
-            }
-        }
-    }
-}
-
-template <int CPL, bool FUSED>
-__global__ void __launch_bounds__(kGemvThreads)
-gemv_down_kernel(const uint16_t* __restrict__ h, const int32_t* __restrict__ perm_token,
-                 const int32_t* __restrict__ offsets, PlanView plan, const int32_t* __restrict__ ids,
-                 const float* __restrict__ wts, int T, int TCH, int d, int k, int I, const uint8_t* __restrict__ dq,
-                 const uint8_t* __restrict__ ds, uint16_t* __restrict__ y_perm, uint16_t* __restrict__ y) {
-    extern __shared__ float4 hs4[];  // [pairs][I/4] block-interleaved
-    __shared__ int s_row[kDownMaxPairs], s_tok[kDownMaxPairs], s_exp[kDownMaxPairs];
-    __shared__ float s_w[kDownMaxPairs];
-    __shared__ int s_np;
-    __shared__ float ys[kRowsPerCta][kDownMaxTok];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t0 = blockIdx.y * TCH, t1 = min(T, t0 + TCH);
-    const int nb = I / 32;
     pdl_wait();
-
-    if (threadIdx.x == 0) {
-        int np = 0;
-        const int n_act = plan.scalars[0];
-        for (int u = 0; u < n_act; ++u) {
-            const int e = plan.active[u];
-            for (int r = offsets[e]; r < offsets[e + 1]; ++r) {
-                const int t = perm_token[r];
-                if (t < t0 || t >= t1) continue;
-                float wv = 0.f;
-                if (FUSED) {
-                    int j = 0;
-                    while (j < k - 1 && ids[(size_t)t * k + j] != e) ++j;
-                    wv = wts[(size_t)t * k + j];
-                }
-                s_row[np] = r;
-                s_tok[np] = t - t0;
-                s_exp[np] = e;
-                s_w[np] = wv;
-                ++np;
+    for (int i = tid; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
+    for (int i = tid; i < 8 * a.outs; i += blockDim.x) ys[i] = 0.f;
+    if (tid == 0) s_cnt = 0;
+    __syncthreads();
+    // rows of the chunk in permuted order (stable compaction over all P rows), with their expert
+    for (int base = 0; base < a.P; base += blockDim.x) {
+        const int r = base + tid;
+        const int t = r < a.P ? a.perm_token[r] : -1;
+        const bool in = (t >= t0 && t < t1);
+        const unsigned bal = __ballot_sync(0xffffffffu, in);
+        if (lane == 0) wtot[warp] = __popc(bal);
+        __syncthreads();
+        int before = s_cnt;
+        for (int w = 0; w < warp; ++w) before += wtot[w];
+        if (in) {
+            const int pos = before + __popc(bal & ((1u << lane) - 1u));
+            int lo = 0, hi = a.E;  // expert: last e with offsets[e] <= r
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_off[mid] <= r) lo = mid; else hi = mid;
             }
+            s_row[pos] = r;
+            s_tok[pos] = t - t0;
+            s_exp[pos] = lo;
+            s_w[pos] = FUSED ? a.row_w[r] : 0.f;
         }
-        s_np = np;
+        __syncthreads();
+        if (tid == 0) {
+            int tot = 0;
+            for (int w = 0; w < 8; ++w) tot += wtot[w];
+            s_cnt += tot;
+        }
+        __syncthreads();
     }
-    for (int i = threadIdx.x; i < kRowsPerCta * kDownMaxTok; i += blockDim.x) (&ys[0][0])[i] = 0.f;
-    __syncthreads();
-    const int np = s_np;
-    for (int q = 0; q < np; ++q) stage_row_bf16(h + (size_t)s_row[q] * I, I, hs4 + (size_t)q * (I / 4));
+    const int nrows = s_cnt;
+    stage_rows_f16(a.act, s_row, nrows, a.K, hs, inv);
     __syncthreads();
 
-    const int n0 = blockIdx.x * kRowsPerCta + warp * kRowsPerWarp;
-    const bool single = nb <= 32 * CPL;
-    uint4 wcur[kRowsPerWarp][CPL], wnxt[kRowsPerWarp][CPL];
-    uint32_t scur[kRowsPerWarp][CPL], snxt[kRowsPerWarp][CPL];
-    if (np > 0 && single) load_down_rows<CPL>(dq, ds, s_exp[0], d, nb, n0, 0, lane, wcur, scur);
-    int q0 = 0;
-    while (q0 < np) {
-        const int e = s_exp[q0];
-        int q1 = q0 + 1;
-        while (q1 < np && s_exp[q1] == e) ++q1;
-        float acc[kRowsPerWarp][kDownMaxTok];
+    const uint8_t* const qsel[kR] = {a.q0, a.q0, a.q0, a.q0, a.q0, a.q0, a.q0, a.q0};
+    const uint8_t* const ssel[kR] = {a.s0, a.s0, a.s0, a.s0, a.s0, a.s0, a.s0, a.s0};
+    auto grows = [&](int e, size_t (&g)[kR]) {
 #pragma unroll
-        for (int rr = 0; rr < kRowsPerWarp; ++rr)
-#pragma unroll
-            for (int qi = 0; qi < kDownMaxTok; ++qi) acc[rr][qi] = 0.f;
-        for (int cb = 0; cb < nb; cb += 32 * CPL) {
-            if (single) {
-                if (q1 < np) load_down_rows<CPL>(dq, ds, s_exp[q1], d, nb, n0, 0, lane, wnxt, snxt);
-            } else {
-                load_down_rows<CPL>(dq, ds, e, d, nb, n0, cb, lane, wcur, scur);
-            }
-#pragma unroll
-            for (int qi = 0; qi < kDownMaxTok; ++qi) {
-                if (q0 + qi < q1) {
-                    const float4* act = hs4 + (size_t)(q0 + qi) * (I / 4);
-#pragma unroll
-                    for (int rr = 0; rr < kRowsPerWarp; ++rr)
-#pragma unroll
-                        for (int c = 0; c < CPL; ++c) {
-                            const int b = cb + lane + 32 * c;
-                            if (b < nb)
-                                acc[rr][qi] = fmaf(block_dot(wcur[rr][c], act, nb, b), e8m0_to_f32(scur[rr][c]),
-                                                   acc[rr][qi]);
-                        }
-                }
-            }
+        for (int j = 0; j < kR; ++j) g[j] = (size_t)e * a.M_exp + n_base + j;
+    };
+    uint4 wcur[kR][BPT], wnxt[kR][BPT];
+    uint32_t scur[kR][BPT], snxt[kR][BPT];
+    int qs = 0;
+    if (nrows > 0) {
+        size_t g[kR];
+        grows(s_exp[0], g);
+        load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wcur, scur);
+    }
+    while (qs < nrows) {
+        const int e = s_exp[qs];
+        int qe = qs + 1;
+        while (qe < nrows && s_exp[qe] == e) ++qe;
+        const bool more = qe < nrows;
+        if (more) {
+            size_t g[kR];
+            grows(s_exp[qe], g);
+            load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wnxt, snxt);
         }
-#pragma unroll
-        for (int qi = 0; qi < kDownMaxTok; ++qi) {
-            if (q0 + qi < q1) {
-#pragma unroll
-                for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-                    const float s = warp_sum(acc[rr][qi]);
-                    if (lane == 0) {
-                        const uint16_t sb = f32_to_bf16_bits(s);
-                        if (FUSED) {
-                            float& a = ys[warp * kRowsPerWarp + rr][s_tok[q0 + qi]];
-                            a = fmaf(s_w[q0 + qi], bf16_bits_to_f32(sb), a);
-                        } else {
-                            y_perm[(size_t)s_row[q0 + qi] * d + n0 + rr] = sb;
-                        }
+        for (int qa = qs; qa < qe; qa += Q) {
+            const int nq = min(Q, qe - qa);
+            float acc[V];
+            batch_dots<BPT, Q>(hs, qa, nq, gl, geo, wcur, scur, acc);
+            red[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
+            __syncthreads();
+            if (gl < 32) {
+                const int v = lane >> (5 - (V == 8 ? 3 : V == 16 ? 4 : 5));
+                const int qq = v / kR, j = v % kR;
+                const bool leader = (lane & ((32 / V) - 1)) == 0;
+                if (leader && qq < nq) {
+                    float s = 0.f;
+                    for (int w = 0; w < wpg; ++w) s += red[(grp * wpg + w) * 32 + lane];
+                    const int q = qa + qq;
+                    const uint16_t sb = f32_to_bf16_bits(s * inv[q]);
+                    const int nn = grp * kR + j;
+                    if (FUSED) {
+                        float& yv = ys[s_tok[q] * a.outs + nn];
+                        yv = fmaf(s_w[q], bf16_bits_to_f32(sb), yv);
+                    } else {
+                        a.out[(size_t)s_row[q] * a.M_exp + blockIdx.x * a.outs + nn] = sb;
                     }
                 }
             }
+            __syncthreads();
         }
-        if (single && q1 < np) {
+        if (more) {
 #pragma unroll
-            for (int rr = 0; rr < kRowsPerWarp; ++rr)
+            for (int j = 0; j < kR; ++j)
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    wcur[rr][c] = wnxt[rr][c];
-                    scur[rr][c] = snxt[rr][c];
+                for (int c = 0; c < BPT; ++c) {
+                    wcur[j][c] = wnxt[j][c];
+                    scur[j][c] = snxt[j][c];
                 }
         }
-        q0 = q1;
+        qs = qe;
     }
     if (FUSED) {
-        __syncthreads();
-        for (int i = threadIdx.x; i < kRowsPerCta * (t1 - t0); i += blockDim.x) {
-            const int tt = i / kRowsPerCta, rr = i % kRowsPerCta;
-            y[(size_t)(t0 + tt) * d + blockIdx.x * kRowsPerCta + rr] = f32_to_bf16_bits(ys[rr][tt]);
+        for (int i = tid; i < a.outs * (t1 - t0); i += blockDim.x) {
+            const int tt = i / a.outs, nn = i % a.outs;
+            a.out[(size_t)(t0 + tt) * a.M_exp + blockIdx.x * a.outs + nn] = f32_to_bf16_bits(ys[tt * a.outs + nn]);
         }
     }
     pdl_launch_dependents();
@@ -319,19 +468,18 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_
 
 // ------------------------------------------------------------------ launchers
 
+bool gemv_supported(int d, int I) { return d / 32 <= 2 * kThr && I / 32 <= 2 * kThr; }
 
-template <int TC, int CPL>
-static cudaError_t up_variant(dim3 grid, size_t smem, cudaStream_t st, bool pdl, void** args) {
-    const void* f = (const void*)gemv_up_kernel<TC, CPL>;
-    return launch_kernel(f, grid, dim3(kGemvThreads), smem, st, pdl, args);
-}
+static int pow2_q(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : 4; }
 
-template <int TC>
-static cudaError_t up_cpl(int nb, dim3 grid, size_t smem, cudaStream_t st, bool pdl, void** args) {
-    if (nb <= 32) return up_variant<TC, 1>(grid, smem, st, pdl, args);
-    if (nb <= 64) return up_variant<TC, 2>(grid, smem, st, pdl, args);
-    if (nb <= 128) return up_variant<TC, 4>(grid, smem, st, pdl, args);
-    return up_variant<TC, 8>(grid, smem, st, pdl, args);
+template <int BPT, int Q>
+static const void* up_kernel() { return (const void*)gemv_up_kernel<BPT, Q>; }
+
+template <int BPT, bool F>
+static const void* down_kernel(int q) {
+    if (q == 1) return (const void*)gemv_down_kernel<BPT, 1, F>;
+    if (q == 2) return (const void*)gemv_down_kernel<BPT, 2, F>;
+    return (const void*)gemv_down_kernel<BPT, 4, F>;
 }
 
 cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
@@ -339,51 +487,75 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
                            cudaStream_t st, bool pdl) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
-    const int slots = P < E ? P : E;
-    // token chunk: all of a decode step's tokens when they fit in <= 128 KB of fp32 staging
-    int TC = 1;
-    while (TC < T && TC < 4 && (size_t)(2 * TC) * d * 4 <= 128 * 1024) TC *= 2;
-    const size_t smem = (size_t)TC * d * 4;
-    dim3 grid(I / kRowsPerCta, slots);
-    const int nb = d / 32;
-    const uint8_t *gq = W->gate_q, *gs = W->gate_s, *uq = W->up_q, *us = W->up_s;
-    void* args[] = {&x, &perm_token, &offsets, &plan, &d, &I, &gq, &gs, &uq, &us, &h};
-    switch (TC) {
-        case 1: return up_cpl<1>(nb, grid, smem, st, pdl, args);
-        case 2: return up_cpl<2>(nb, grid, smem, st, pdl, args);
-        default: return up_cpl<4>(nb, grid, smem, st, pdl, args);
-    }
-}
-
-template <int CPL, bool FUSED>
-static cudaError_t down_variant(dim3 grid, size_t smem, cudaStream_t st, bool pdl, void** args) {
-    const void* f = (const void*)gemv_down_kernel<CPL, FUSED>;
-    return launch_kernel(f, grid, dim3(kGemvThreads), smem, st, pdl, args);
-}
-
-template <bool FUSED>
-static cudaError_t down_cpl(int nb, dim3 grid, size_t smem, cudaStream_t st, bool pdl, void** args) {
-    if (nb <= 32) return down_variant<1, FUSED>(grid, smem, st, pdl, args);
-    if (nb <= 64) return down_variant<2, FUSED>(grid, smem, st, pdl, args);
-    return down_variant<4, FUSED>(grid, smem, st, pdl, args);
+    if (!gemv_supported(d, I)) return cudaErrorInvalidValue;
+    const Geo geo = make_geo(d);
+    const int unit = geo.RG * (kR / 2);
+    if (I % unit != 0) return cudaErrorInvalidValue;
+    int outs = unit;  // outputs per CTA: a multiple of unit dividing I, at most 64
+    for (int o = unit; o <= 64 && o <= I; o += unit)
+        if (I % o == 0) outs = o;
+    GemvArgs a = {};
+    a.q0 = W->gate_q;
+    a.s0 = W->gate_s;
+    a.q1 = W->up_q;
+    a.s1 = W->up_s;
+    a.act = x;
+    a.perm_token = perm_token;
+    a.offsets = offsets;
+    a.plan = plan;
+    a.T = T;
+    a.K = d;
+    a.M_exp = I;
+    a.P = P;
+    a.E = E;
+    a.outs = outs;
+    a.out = h;
+    const int Q = pow2_q(T);
+    const size_t smem = (size_t)Q * d * 2 + sizeof(float) * (Q + 8 * 32) + sizeof(int) * Q;
+    void* args[] = {&a};
+    const dim3 grid(I / outs, P < E ? P : E);
+    const void* f;
+    if (geo.bpt == 1) f = Q == 1 ? up_kernel<1, 1>() : Q == 2 ? up_kernel<1, 2>() : up_kernel<1, 4>();
+    else f = Q == 1 ? up_kernel<2, 1>() : Q == 2 ? up_kernel<2, 2>() : up_kernel<2, 4>();
+    return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
 }
 
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
-                             const int32_t* ids, const float* w, int T, int d, int E, int k, int I,
-                             const moe_expert_weights* W, uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl) {
-    (void)E;
+                             const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
+                             uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
-    // token chunk: at most kDownMaxTok tokens and kDownMaxPairs pairs, staged h <= 160 KB
-    int TCH = T < kDownMaxTok ? T : kDownMaxTok;
-    while (TCH > 1 && ((size_t)TCH * k > kDownMaxPairs || (size_t)TCH * k * I * 4 > 160 * 1024)) TCH /= 2;
-    if ((size_t)TCH * k > kDownMaxPairs || (size_t)TCH * k * I * 4 > 200 * 1024) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)TCH * k * I * 4;
-    dim3 grid(d / kRowsPerCta, (T + TCH - 1) / TCH);
-    const int nb = I / 32;
-    const uint8_t *dq = W->down_q, *ds = W->down_s;
-    void* args[] = {&h, &perm_token, &offsets, &plan, &ids, &w, &T, &TCH, &d, &k, &I, &dq, &ds, &y_perm, &y};
-    if (y != nullptr) return down_cpl<true>(nb, grid, smem, st, pdl, args);
-    return down_cpl<false>(nb, grid, smem, st, pdl, args);
+    if (!gemv_supported(d, I)) return cudaErrorInvalidValue;
+    const Geo geo = make_geo(I);
+    const int outs = geo.RG * kR;  // each row group owns kR output features
+    if (d % outs != 0) return cudaErrorInvalidValue;
+    int tch = kDownMaxRows / k;
+    if (tch > 8) tch = 8;
+    if (tch > T) tch = T;
+    GemvArgs a = {};
+    a.q0 = W->down_q;
+    a.s0 = W->down_s;
+    a.act = h;
+    a.perm_token = perm_token;
+    a.offsets = offsets;
+    a.plan = plan;
+    a.row_w = row_w;
+    a.T = T;
+    a.K = I;
+    a.M_exp = d;
+    a.P = T * k;
+    a.E = E;
+    a.tch = tch;
+    a.outs = outs;
+    a.out = y ? y : y_perm;
+    const size_t smem = (size_t)kDownMaxRows * I * 2 + sizeof(float) * (kDownMaxRows + 8 * 32 + 8 * outs) +
+                        sizeof(int) * (3 * kDownMaxRows) + sizeof(float) * kDownMaxRows + sizeof(int) * (E + 1);
+    void* args[] = {&a};
+    const dim3 grid(d / outs, (T + tch - 1) / tch);
+    const int Q = pow2_q(tch);  // rows of one expert in a chunk: at most one per token
+    const void* f;
+    if (y) f = geo.bpt == 1 ? down_kernel<1, true>(Q) : down_kernel<2, true>(Q);
+    else f = geo.bpt == 1 ? down_kernel<1, false>(Q) : down_kernel<2, false>(Q);
+    return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
 }
 
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,

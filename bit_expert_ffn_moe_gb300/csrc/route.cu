@@ -24,8 +24,7 @@ __device__ __forceinline__ float warp_butterfly_sum(float p) {
 }
 
 // One warp selects the top-k of logits[0..E) (ties -> lower id), sorts the set ascending and
-// writes ids[0..k) and the softmax weights w[0..k).  Logits are read with ld.cg so that values
-// written by other CTAs of the same grid are seen.
+// writes ids[0..k) and the softmax weights w[0..k).
 __device__ void topk_softmax_warp(const float* logits, int E, int k, int32_t* ids, float* w) {
     const int lane = threadIdx.x & 31;
     uint32_t taken = 0;
@@ -36,7 +35,7 @@ __device__ void topk_softmax_warp(const float* logits, int E, int k, int32_t* id
         int bid = 0x7fffffff;
         for (int i = 0; lane + 32 * i < E; ++i) {
             if ((taken >> i) & 1u) continue;
-            float v = __ldcg(logits + lane + 32 * i);
+            float v = logits[lane + 32 * i];
             if (bid == 0x7fffffff || v > best) {  // increasing e within a lane: strict > keeps the lower id
                 best = v;
                 bid = lane + 32 * i;
@@ -135,7 +134,8 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 __global__ void __launch_bounds__(kRouteDecodeThreads)
 route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ b,
                     int T, int d, int E, int k, float* logits, int32_t* ids, float* w, int32_t* counts,
-                    int32_t* offsets, int32_t* perm_token, int32_t* inv_pos, PlanView plan, Ctrl* ctrl) {
+                    int32_t* offsets, int32_t* perm_token, int32_t* inv_pos, float* row_w, PlanView plan,
+                    Ctrl* ctrl) {
     extern __shared__ __align__(16) unsigned char smem[];
     float* Ws = reinterpret_cast<float*>(smem);                      // [d]
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sizeof(float) * d);  // [T][d]
@@ -165,7 +165,7 @@ route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_
         if (lane == 0) logits[(size_t)t * E + e] = acc + bias;
     }
 
-    // ---- last CTA: top-k + permutation
+    // ---- last CTA: top-k + permutation, working from shared memory
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -177,42 +177,55 @@ route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_
     __threadfence();
     if (tid == 0) ctrl->route_ticket = 0;  // ready for the next call on this workspace
 
-    for (int t = warp; t < T; t += blockDim.x / 32)
-        topk_softmax_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+    __shared__ int32_t s_ids[kRouteDecodeMaxT * kMaxK];
+    __shared__ float s_w[kRouteDecodeMaxT * kMaxK];
+    float* sl = reinterpret_cast<float*>(smem);  // [T][E]; the staging area is free now
+    for (int i = tid; i < T * E; i += blockDim.x) sl[i] = __ldcg(logits + i);  // other CTAs' results
     for (int i = tid; i < E; i += blockDim.x) s_cnt[i] = 0;
     __syncthreads();
+    for (int t = warp; t < T; t += blockDim.x / 32)
+        topk_softmax_warp(sl + (size_t)t * E, E, k, s_ids + t * k, s_w + t * k);
+    __syncthreads();
     const int P = T * k;
-    for (int p = tid; p < P; p += blockDim.x) atomicAdd(&s_cnt[ids[p]], 1);
+    for (int p = tid; p < P; p += blockDim.x) {
+        ids[p] = s_ids[p];
+        w[p] = s_w[p];
+        atomicAdd(&s_cnt[s_ids[p]], 1);
+    }
     __syncthreads();
     if (warp == 0) build_plan_warp(s_cnt, E, counts, offsets, plan);
     __syncthreads();
     for (int p = tid; p < P; p += blockDim.x) {
-        const int t = p / k, ex = ids[p];
-        int rank = 0;
+        const int t = p / k, ex = s_ids[p];
+        int rank = 0;  // tokens before t that chose ex (each token picks an expert at most once)
         for (int t2 = 0; t2 < t; ++t2)
-            for (int j = 0; j < k; ++j) rank += (ids[t2 * k + j] == ex);
+            for (int j = 0; j < k; ++j) rank += (s_ids[t2 * k + j] == ex);
         const int r = offsets[ex] + rank;
         perm_token[r] = t;
         inv_pos[p] = r;
+        row_w[r] = s_w[p];
     }
     __threadfence();
     pdl_launch_dependents();
 }
 
-bool route_decode_supported(int T, int d, int E, int k) {
-    (void)k;
-    return T >= 1 && T <= kRouteDecodeMaxT && E <= kMaxE &&
-           (size_t)d * (4 + 2 * (size_t)T) <= 200 * 1024;
+static size_t route_decode_smem(int T, int d, int E) {
+    const size_t staging = sizeof(float) * (size_t)d + sizeof(uint16_t) * (size_t)T * d;
+    const size_t logits = sizeof(float) * (size_t)T * E;
+    return staging > logits ? staging : logits;
 }
 
+bool route_decode_supported(int T, int d, int E, int k) {
+    return T >= 1 && T <= kRouteDecodeMaxT && E <= kMaxE && k <= kMaxK && route_decode_smem(T, d, E) <= 200 * 1024;
+}
 
 cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                 float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
-                                int32_t* perm_token, int32_t* inv_pos, PlanView plan, Ctrl* ctrl, cudaStream_t st,
-                                bool pdl) {
-    size_t smem = sizeof(float) * (size_t)d + sizeof(uint16_t) * (size_t)T * d;
+                                int32_t* perm_token, int32_t* inv_pos, float* row_w, PlanView plan, Ctrl* ctrl,
+                                cudaStream_t st, bool pdl) {
+    const size_t smem = route_decode_smem(T, d, E);
     void* args[] = {&x, &W_r, &b, &T, &d, &E, &k, &logits, &ids, &w, &counts, &offsets, &perm_token, &inv_pos,
-                    &plan, &ctrl};
+                    &row_w, &plan, &ctrl};
     return launch_kernel((const void*)route_decode_kernel, dim3(E), dim3(kRouteDecodeThreads), smem, st, pdl, args);
 }
 
@@ -328,7 +341,7 @@ __global__ void plan_kernel(int E, int32_t* counts_out, int32_t* offsets, PlanVi
 // One CTA per expert: a stable block-wide compaction over the tokens that chose it.
 __global__ void __launch_bounds__(256)
 scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __restrict__ offsets, PlanView plan,
-               int32_t* perm_token, int32_t* inv_pos) {
+               int32_t* perm_token, int32_t* inv_pos, const float* __restrict__ w, float* row_w) {
     __shared__ int warp_tot[8];
     pdl_wait();
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -355,6 +368,7 @@ scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __r
             const int r = running + wbase + before;
             perm_token[r] = t;
             inv_pos[(size_t)t * k + j_found] = r;
+            if (row_w) row_w[r] = w[(size_t)t * k + j_found];
         }
         running += tot;
         __syncthreads();
@@ -362,7 +376,8 @@ scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __r
 }
 
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
-                           int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl) {
+                           int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl,
+                           const float* w, float* row_w) {
     cudaError_t err = cudaMemsetAsync(plan.counts, 0, sizeof(int32_t) * (size_t)E, st);
     if (err != cudaSuccess) return err;
     int P = T * k;
@@ -377,7 +392,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
     err = launch_kernel((const void*)plan_kernel, dim3(1), dim3(32), 0, st, pdl, a2);
     if (err != cudaSuccess) return err;
     if (P == 0) return cudaSuccess;
-    void* a3[] = {&ids, &T, &k, &offsets, &plan, &perm_token, &inv_pos};
+    if (w == nullptr) row_w = nullptr;
+    void* a3[] = {&ids, &T, &k, &offsets, &plan, &perm_token, &inv_pos, &w, &row_w};
     return launch_kernel((const void*)scatter_kernel, dim3(E), dim3(256), 0, st, pdl, a3);
 }
 
