@@ -157,6 +157,7 @@ struct GemvArgs {
     const float* row_w;  // down, fused: gate weight of each permuted row
     int T, K, M_exp, P, E;
     int tch;             // down: tokens per chunk
+    int maxrows;         // down: staged permuted rows per CTA (tch * k)
     int outs;            // output features per CTA
     uint16_t* out;       // up: h [P][I]; down: y_perm [P][d] or y [T][d]
 };
@@ -310,15 +311,16 @@ gemv_down_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int V = kR * Q;
     const Geo geo = make_geo(a.K);
-    uint4* hs = reinterpret_cast<uint4*>(smem);                                       // [rows][K/8]
-    float* inv = reinterpret_cast<float*>(smem + (size_t)kDownMaxRows * a.K * 2);    // [rows]
-    float* red = inv + kDownMaxRows;                                                 // [8][32]
+    const int mr = a.maxrows;
+    uint4* hs = reinterpret_cast<uint4*>(smem);                                       // [mr][K/8]
+    float* inv = reinterpret_cast<float*>(smem + (size_t)mr * a.K * 2);              // [mr]
+    float* red = inv + mr;                                                           // [8][32]
     float* ys = red + 8 * 32;                                                        // [tch][outs]
-    int* s_row = reinterpret_cast<int*>(ys + 8 * a.outs);                            // [rows]
-    int* s_tok = s_row + kDownMaxRows;
-    int* s_exp = s_tok + kDownMaxRows;
-    float* s_w = reinterpret_cast<float*>(s_exp + kDownMaxRows);
-    int* s_off = reinterpret_cast<int*>(s_w + kDownMaxRows);                         // [E+1]
+    int* s_row = reinterpret_cast<int*>(ys + 8 * a.outs);                            // [mr]
+    int* s_tok = s_row + mr;
+    int* s_exp = s_tok + mr;
+    float* s_w = reinterpret_cast<float*>(s_exp + mr);
+    int* s_off = reinterpret_cast<int*>(s_w + mr);                                   // [E+1]
     __shared__ int wtot[8];
     __shared__ int s_cnt;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -528,9 +530,11 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
     const Geo geo = make_geo(I);
     const int outs = geo.RG * kR;  // each row group owns kR output features
     if (d % outs != 0) return cudaErrorInvalidValue;
-    int tch = kDownMaxRows / k;
-    if (tch > 8) tch = 8;
+    // tokens per chunk: at most 8, at most kDownMaxRows staged rows, staged h <= 160 KB
+    int tch = 8;
+    while (tch > 1 && ((size_t)tch * k > kDownMaxRows || (size_t)tch * k * I * 2 > 160 * 1024)) tch /= 2;
     if (tch > T) tch = T;
+    if ((size_t)tch * k > kDownMaxRows || (size_t)tch * k * I * 2 > 200 * 1024) return cudaErrorInvalidValue;
     GemvArgs a = {};
     a.q0 = W->down_q;
     a.s0 = W->down_s;
@@ -545,10 +549,12 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
     a.P = T * k;
     a.E = E;
     a.tch = tch;
+    a.maxrows = tch * k;
     a.outs = outs;
     a.out = y ? y : y_perm;
-    const size_t smem = (size_t)kDownMaxRows * I * 2 + sizeof(float) * (kDownMaxRows + 8 * 32 + 8 * outs) +
-                        sizeof(int) * (3 * kDownMaxRows) + sizeof(float) * kDownMaxRows + sizeof(int) * (E + 1);
+    const size_t mr = (size_t)tch * k;
+    const size_t smem = mr * I * 2 + sizeof(float) * (mr + 8 * 32 + 8 * outs) + sizeof(int) * (3 * mr) +
+                        sizeof(float) * mr + sizeof(int) * (E + 1);
     void* args[] = {&a};
     const dim3 grid(d / outs, (T + tch - 1) / tch);
     const int Q = pow2_q(tch);  // rows of one expert in a chunk: at most one per token
