@@ -22,7 +22,6 @@ namespace moe {
 
 constexpr int kThr = 256;       // threads per CTA
 constexpr int kR = 8;           // weight rows per batch per row group
-constexpr int kMaxQ = 4;        // activation rows (tokens / pairs) per pass
 constexpr int kDownMaxRows = 64;  // staged permuted rows per down CTA
 
 // ------------------------------------------------------------------ helpers
