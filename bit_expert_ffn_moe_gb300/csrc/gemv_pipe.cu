@@ -54,6 +54,8 @@ struct PipeArgs {
     PlanView plan;
     const float* row_w;  // down: gate weight of each permuted row
     int T, K, M_exp, E, stages;
+    int xs_rows;    // staged activation rows: Q, or all P permuted rows when stage_all
+    int stage_all;  // down: stage every h row once at the start
     size_t stage_bytes, codes_bytes, scale_bytes;  // per stage: codes region (per matrix), scales region
     uint16_t* out;  // up: h [P][I]; down: y [T][d]
     int* status;
@@ -104,38 +106,49 @@ __device__ __forceinline__ float warp_transpose_reduce(float (&a)[V], int lane) 
     return v;
 }
 
-// Stage nq activation rows as prescaled f16 (row maximum in [2^14, 2^15)), block-interleaved:
-// 16-byte unit c of block b of row q at uint4 index (q * 4 + c) * nb + b.  Consumer warps only.
+// Prescale exponent p of a row whose largest |bf16| has bit pattern mx (sign cleared): the row
+// maximum times 2^p lies in [2^14, 2^15).
+__device__ __forceinline__ int prescale_exp(uint32_t mx) {
+    const int p = (mx == 0) ? 0 : 141 - (int)(mx >> 7);
+    return max(-126, min(126, p));
+}
+
+// All consumer threads stage nq activation rows as prescaled f16, block-interleaved: 16-byte
+// unit c of block b of staged row q at uint4 index (q * 4 + c) * nb + b.  inv[q] = 2^-p.
+// smax: nq ints of shared scratch.  Ends with the consumer barrier.
 __device__ void stage_rows(const uint16_t* __restrict__ src, const int* rows, int nq, int K, uint4* dst, float* inv,
-                           int cwarp, int lane) {
-    const int nb = K / 32, units = K / 8;
-    for (int q = cwarp; q < nq; q += kCons / 32) {
-        const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K);
+                           unsigned* smax, int tid) {
+    const int nb = K / 32, units = K / 8, total = nq * units;
+    if (tid < nq) smax[tid] = 0;
+    ptx::named_sync(kRedId, kCons);
+#pragma unroll 4
+    for (int i = tid; i < total; i += kCons) {
+        const int q = i / units, u = i - q * units;
+        const uint4 v = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K)[u];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t mx = 0;
-        for (int u = lane; u < units; u += 32) {
-            const uint4 v = s[u];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-        }
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        int p = (mx == 0) ? 0 : 141 - (int)(mx >> 7);
-        p = max(-126, min(126, p));
-        const float up = __uint_as_float((uint32_t)(127 + p) << 23);
-        for (int u = lane; u < units; u += 32) {
-            const uint4 v = s[u];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __half lo = __float2half_rn(bf16_bits_to_f32(w[i] & 0xFFFFu) * up);
-                const __half hi = __float2half_rn(bf16_bits_to_f32(w[i] >> 16) * up);
-                o[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-            }
-            dst[((size_t)q * 4 + (u & 3)) * nb + (u >> 2)] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (lane == 0) inv[q] = __uint_as_float((uint32_t)(127 - p) << 23);
+        for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+        atomicMax(&smax[q], mx);
     }
+    ptx::named_sync(kRedId, kCons);
+#pragma unroll 4
+    for (int i = tid; i < total; i += kCons) {
+        const int q = i / units, u = i - q * units;
+        const uint4 v = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K)[u];
+        const float up = __uint_as_float((uint32_t)(127 + prescale_exp(smax[q])) << 23);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half lo = __float2half_rn(bf16_bits_to_f32(w[j] & 0xFFFFu) * up);
+            const __half hi = __float2half_rn(bf16_bits_to_f32(w[j] >> 16) * up);
+            o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        }
+        dst[((size_t)q * 4 + (u & 3)) * nb + (u >> 2)] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid < nq) inv[tid] = __uint_as_float((uint32_t)(127 - prescale_exp(smax[tid])) << 23);
+    ptx::named_sync(kRedId, kCons);
 }
 
 // Item of the producer / consumer sequence: matrix rows [row, row + m) of expert e.
@@ -212,11 +225,13 @@ gemv_pipe_kernel(const PipeArgs a) {
     constexpr int V = kRowsPerGroup * Q;
     const Geo geo = make_geo(a.K);
     unsigned char* stages = smem;
-    uint4* xs = reinterpret_cast<uint4*>(smem + (size_t)a.stages * a.stage_bytes);     // [Q][K/8]
-    float* inv = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xs) + (size_t)Q * a.K * 2);  // [Q]
-    float* red = inv + Q;                                                               // [2][8][32]
-    int* rows = reinterpret_cast<int*>(red + 2 * 8 * 32);                               // [Q]
-    int* toks = rows + Q;                                                               // [Q]
+    const int XR = a.xs_rows;                                                           // Q, or P when staged once
+    uint4* xs = reinterpret_cast<uint4*>(smem + (size_t)a.stages * a.stage_bytes);     // [XR][K/8]
+    float* inv = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(xs) + (size_t)XR * a.K * 2);  // [XR]
+    unsigned* smax = reinterpret_cast<unsigned*>(inv + XR);                             // [XR]
+    float* red = reinterpret_cast<float*>(smax + XR);                                   // [2][8][32]
+    int* rows = reinterpret_cast<int*>(red + 2 * 8 * 32);                               // [XR]
+    int* toks = rows + XR;                                                              // [Q]
     float* pw = reinterpret_cast<float*>(toks + Q);                                     // [Q]
     float* ys = pw + Q;                                                                 // [T][rows per CTA]
     const int ys_rows = UP ? 0 : (a.M_exp + gridDim.x - 1) / gridDim.x;
@@ -275,28 +290,35 @@ gemv_pipe_kernel(const PipeArgs a) {
         // ------------------------------------------------------------ consumers
         const int grp = tid / geo.G, gl = tid % geo.G, wpg = geo.G / 32;
         const int cwarp = warp;
+        (void)cwarp;
         uint32_t xr[Q][BPT][16];
-        int cur_slot = -1, nq = 0, r0 = 0;
+        int cur_slot = -1, nq = 0, r0 = 0, xbase = 0;
         Item it;
         int n = 0;
         if (!UP)
             for (int i = tid; i < a.T * ys_rows; i += kCons) ys[i] = 0.f;
+        if (a.stage_all) {
+            // down, small P: stage every permuted h row once (rows are compact permuted rows)
+            for (int i = tid; i < XR; i += kCons) rows[i] = i;
+            ptx::named_sync(kRedId, kCons);
+            stage_rows(a.act, rows, XR, a.K, xs, inv, smax, tid);
+        }
         while (next_item(it)) {
             if (it.slot != cur_slot) {
-                // new expert: stage its tokens' activation rows (or its pairs' h rows)
+                // new expert: its tokens' activation rows (or its pairs' h rows) into registers
                 cur_slot = it.slot;
                 r0 = a.offsets[it.e];
                 nq = a.offsets[it.e + 1] - r0;
                 if (nq > Q) nq = Q;  // callers guarantee at most Q rows per expert (T <= Q)
-                ptx::named_sync(kRedId, kCons);
+                ptx::named_sync(kRedId, kCons);  // the previous item's output phase is done
                 if (tid < nq) {
-                    rows[tid] = UP ? a.perm_token[r0 + tid] : r0 + tid;
+                    if (!a.stage_all) rows[tid] = UP ? a.perm_token[r0 + tid] : r0 + tid;
                     toks[tid] = a.perm_token[r0 + tid];
                     pw[tid] = UP ? 0.f : a.row_w[r0 + tid];
                 }
                 ptx::named_sync(kRedId, kCons);
-                stage_rows(a.act, rows, nq, a.K, xs, inv, cwarp, lane);
-                ptx::named_sync(kRedId, kCons);
+                if (!a.stage_all) stage_rows(a.act, rows, nq, a.K, xs, inv, smax, tid);
+                xbase = a.stage_all ? r0 : 0;
 #pragma unroll
                 for (int qq = 0; qq < Q; ++qq)
 #pragma unroll
@@ -305,7 +327,7 @@ gemv_pipe_kernel(const PipeArgs a) {
 #pragma unroll
                         for (int cu = 0; cu < 4; ++cu) {
                             uint4 v = make_uint4(0, 0, 0, 0);
-                            if (qq < nq && b < geo.nb) v = xs[((size_t)qq * 4 + cu) * geo.nb + b];
+                            if (qq < nq && b < geo.nb) v = xs[((size_t)(xbase + qq) * 4 + cu) * geo.nb + b];
                             xr[qq][c][4 * cu + 0] = v.x;
                             xr[qq][c][4 * cu + 1] = v.y;
                             xr[qq][c][4 * cu + 2] = v.z;
@@ -369,8 +391,8 @@ gemv_pipe_kernel(const PipeArgs a) {
                                 g += rb[(grp * wpg + w) * 32 + lane];
                                 u += rb[(grp * wpg + w) * 32 + lane + (4 << sh)];
                             }
-                            g *= inv[qq];
-                            u *= inv[qq];
+                            g *= inv[xbase + qq];
+                            u *= inv[xbase + qq];
                             const float hv = g / (1.f + expf(-g)) * u;  // SiLU(g) * u
                             a.out[(size_t)(r0 + qq) * a.M_exp + it.row + lr] = f32_to_bf16_bits(hv);
                         }
@@ -379,7 +401,7 @@ gemv_pipe_kernel(const PipeArgs a) {
                         if (lr < it.m) {
                             float sum = 0.f;
                             for (int w = 0; w < wpg; ++w) sum += rb[(grp * wpg + w) * 32 + lane];
-                            const float yv = bf16_bits_to_f32(f32_to_bf16_bits(sum * inv[qq]));
+                            const float yv = bf16_bits_to_f32(f32_to_bf16_bits(sum * inv[xbase + qq]));
                             float& acc_y = ys[toks[qq] * ys_rows + (it.row + lr - n0)];
                             acc_y = fmaf(pw[qq], yv, acc_y);
                         }
@@ -426,7 +448,7 @@ int q_for(int T) { return T <= 1 ? 1 : T <= 2 ? 2 : 4; }
 
 // Shared memory of a configuration, or 0 when it does not fit.
 size_t pipe_smem(bool up, int T, int K, int M_exp, int E, int stages, size_t* stage_bytes, size_t* codes_bytes,
-                 size_t* scale_bytes, int ctas) {
+                 size_t* scale_bytes, int ctas, int xs_rows) {
     const Geo geo = make_geo(K);
     const int mmax = up ? 4 * geo.RG : kRowsPerGroup * geo.RG;
     const int Q = q_for(T);
@@ -434,9 +456,10 @@ size_t pipe_smem(bool up, int T, int K, int M_exp, int E, int stages, size_t* st
     *scale_bytes = ((size_t)mmax * K / 32 + 32 + 15) & ~size_t(15);
     *stage_bytes = ((2 * *codes_bytes + 2 * *scale_bytes) + 127) & ~size_t(127);
     const int ys_rows = up ? 0 : (M_exp + ctas - 1) / ctas;
-    size_t bytes = (size_t)stages * *stage_bytes + (size_t)Q * K * 2 + sizeof(float) * (Q + 2 * 8 * 32) +
-                   sizeof(int) * 2 * Q + sizeof(float) * Q + sizeof(float) * (size_t)T * ys_rows + 16 +
-                   sizeof(uint64_t) * 2 * stages + 32 + 128;
+    const int XR = xs_rows;
+    size_t bytes = (size_t)stages * *stage_bytes + (size_t)XR * K * 2 + sizeof(float) * XR + sizeof(unsigned) * XR +
+                   sizeof(float) * 2 * 8 * 32 + sizeof(int) * (XR + Q) + sizeof(float) * Q +
+                   sizeof(float) * (size_t)T * ys_rows + 16 + sizeof(uint64_t) * 2 * stages + 32 + 128;
     (void)E;
     return bytes;
 }
@@ -450,16 +473,21 @@ bool gemv_pipe_supported(int T, int d, int I) {
            (I % (4 * gu.RG)) == 0;
 }
 
-static cudaError_t launch_pipe(bool up, PipeArgs& a, int T, cudaStream_t st, bool pdl) {
+static cudaError_t launch_pipe(bool up, PipeArgs& a, int T, int P, cudaStream_t st, bool pdl) {
     const int ctas = sm_count_cached();
     const Geo geo = make_geo(a.K);
+    const int Q = q_for(T);
+    // down: stage all P = T*k permuted h rows once when they take at most 48 KB
+    a.stage_all = (!up && (size_t)P * a.K * 2 <= 48 * 1024) ? 1 : 0;
+    a.xs_rows = a.stage_all ? P : Q;
     int stages = 8;
     size_t smem = 0;
-    for (; stages >= 2; --stages) {
-        smem = pipe_smem(up, T, a.K, a.M_exp, a.E, stages, &a.stage_bytes, &a.codes_bytes, &a.scale_bytes, ctas);
+    for (; stages >= 3; --stages) {
+        smem = pipe_smem(up, T, a.K, a.M_exp, a.E, stages, &a.stage_bytes, &a.codes_bytes, &a.scale_bytes, ctas,
+                         a.xs_rows);
         if (smem <= 220 * 1024) break;
     }
-    if (stages < 2) return cudaErrorInvalidValue;
+    if (stages < 3) return cudaErrorInvalidValue;
     a.stages = stages;
     void* args[] = {&a};
     const void* f = up ? pick_q<true>(q_for(T), geo.bpt) : pick_q<false>(q_for(T), geo.bpt);
@@ -469,7 +497,6 @@ static cudaError_t launch_pipe(bool up, PipeArgs& a, int T, cudaStream_t st, boo
 cudaError_t launch_gemv_up_pipe(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                                 int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h, int* status,
                                 cudaStream_t st, bool pdl) {
-    (void)k;
     PipeArgs a = {};
     a.q0 = W->gate_q;
     a.s0 = W->gate_s;
@@ -485,13 +512,12 @@ cudaError_t launch_gemv_up_pipe(const uint16_t* x, const int32_t* perm_token, co
     a.E = E;
     a.out = h;
     a.status = status;
-    return launch_pipe(true, a, T, st, pdl);
+    return launch_pipe(true, a, T, T * k, st, pdl);
 }
 
 cudaError_t launch_gemv_down_pipe(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                                   const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
                                   uint16_t* y, int* status, cudaStream_t st, bool pdl) {
-    (void)k;
     PipeArgs a = {};
     a.q0 = W->down_q;
     a.s0 = W->down_s;
@@ -506,7 +532,7 @@ cudaError_t launch_gemv_down_pipe(const uint16_t* h, const int32_t* perm_token, 
     a.E = E;
     a.out = y;
     a.status = status;
-    return launch_pipe(false, a, T, st, pdl);
+    return launch_pipe(false, a, T, T * k, st, pdl);
 }
 
 }  // namespace moe
