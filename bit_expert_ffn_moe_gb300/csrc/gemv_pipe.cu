@@ -208,10 +208,10 @@ __device__ __forceinline__ void issue_item(const PipeArgs& a, bool up, const Ite
     const int nmat = up ? 2 : 1;
     ptx::mbar_arrive_expect_tx(bar, nmat * (cbytes + sbytes));
     ptx::bulk_load(st, a.q0 + g0 * row_bytes, cbytes, bar);
-    ptx::bulk_load(st + 2 * a.codes_bytes, a.s0 + s_lo16, sbytes, bar);
+    ptx::bulk_load(st + nmat * a.codes_bytes, a.s0 + s_lo16, sbytes, bar);
     if (up) {
         ptx::bulk_load(st + a.codes_bytes, a.q1 + g0 * row_bytes, cbytes, bar);
-        ptx::bulk_load(st + 2 * a.codes_bytes + a.scale_bytes, a.s1 + s_lo16, sbytes, bar);
+        ptx::bulk_load(st + nmat * a.codes_bytes + a.scale_bytes, a.s1 + s_lo16, sbytes, bar);
     }
 }
 
@@ -358,7 +358,8 @@ gemv_pipe_kernel(const PipeArgs a) {
                 const int lr = UP ? (4 * grp + (j % 4)) : (kRowsPerGroup * grp + j);
                 if (lr < it.m) {
                     const unsigned char* codes = st + (size_t)mat * a.codes_bytes + (size_t)lr * row_bytes;
-                    const unsigned char* scl = st + 2 * a.codes_bytes + (size_t)mat * a.scale_bytes + sadj + (size_t)lr * srow;
+                    const unsigned char* scl =
+                        st + (UP ? 2 : 1) * a.codes_bytes + (size_t)mat * a.scale_bytes + sadj + (size_t)lr * srow;
 #pragma unroll
                     for (int c = 0; c < BPT; ++c) {
                         const int b = gl + c * geo.G;
@@ -454,7 +455,8 @@ size_t pipe_smem(bool up, int T, int K, int M_exp, int E, int stages, size_t* st
     const int Q = q_for(T);
     *codes_bytes = (size_t)mmax * K / 2;
     *scale_bytes = ((size_t)mmax * K / 32 + 32 + 15) & ~size_t(15);
-    *stage_bytes = ((2 * *codes_bytes + 2 * *scale_bytes) + 127) & ~size_t(127);
+    const size_t nmat = up ? 2 : 1;  // gate and up matrices, or the down matrix
+    *stage_bytes = ((nmat * *codes_bytes + nmat * *scale_bytes) + 127) & ~size_t(127);
     const int ys_rows = up ? 0 : (M_exp + ctas - 1) / ctas;
     const int XR = xs_rows;
     size_t bytes = (size_t)stages * *stage_bytes + (size_t)XR * K * 2 + sizeof(float) * XR + sizeof(unsigned) * XR +
