@@ -76,11 +76,6 @@ moe_status check_weights(const moe_expert_weights* W, moe_act_fmt fmt, bool need
 
 char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 
-// The pipelined decode kernels copy scale rows with 16-byte bulk copies.
-bool scales_aligned(const moe_expert_weights* W) {
-    return aligned(W->gate_s, 16) && aligned(W->up_s, 16) && aligned(W->down_s, 16);
-}
-
 // route (+ permutation when fused) into the given buffers
 moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                      int32_t* ids, float* w, void* ws, const WsLayout& L, cudaStream_t st, bool pdl) {
@@ -294,13 +289,8 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
             MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true, w_b, row_w));
         }
         uint16_t* h = reinterpret_cast<uint16_t*>(at(ws, L.h));
-        if (gemv_pipe_supported(T, d, I) && scales_aligned(W)) {
-            MOE_CUDA(launch_gemv_up_pipe(x, perm, offsets, plan, T, d, E, k, I, W, h, &ctrl->status, st, true));
-            MOE_CUDA(launch_gemv_down_pipe(h, perm, offsets, plan, row_w, T, d, E, k, I, W, y, &ctrl->status, st, true));
-        } else {
-            MOE_CUDA(launch_gemv_up(x, perm, offsets, plan, T, d, E, k, I, W, h, st, true));
-            MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, row_w, T, d, E, k, I, W, nullptr, y, st, true));
-        }
+        MOE_CUDA(launch_gemv_up(x, perm, offsets, plan, T, d, E, k, I, W, h, st, true));
+        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, row_w, T, d, E, k, I, W, nullptr, y, st, true));
         return MOE_OK;
     }
     MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));

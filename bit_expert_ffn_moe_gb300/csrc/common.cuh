@@ -228,13 +228,3 @@ cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan
                              uint16_t* y_perm, int* status, cudaStream_t st, bool pdl);
 }  // namespace moe
 
-namespace moe {
-// Pipelined decode kernels (bulk-copy weight ring), for T <= 4.
-bool gemv_pipe_supported(int T, int d, int I);
-cudaError_t launch_gemv_up_pipe(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
-                                int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h, int* status,
-                                cudaStream_t st, bool pdl);
-cudaError_t launch_gemv_down_pipe(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
-                                  const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
-                                  uint16_t* y, int* status, cudaStream_t st, bool pdl);
-}  // namespace moe
