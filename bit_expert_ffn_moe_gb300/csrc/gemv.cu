@@ -4,25 +4,29 @@
 // once and used for very little arithmetic: the time is the weight read (Muse Spark Open
 // explainer, section 13: at one token per expert about 98% of the time waits on the 4-bit weight
 // read; DGX Spark news item, section 1: batch-1 generation is bound by weight reads).  These
-// kernels therefore stream each weight row exactly once with coalesced 128-bit loads (16 bytes =
-// one 32-element MXFP4 block) and keep the work per weight byte small:
+// kernels stream each weight row once with coalesced 128-bit loads (16 bytes = one 32-element
+// MXFP4 block) and keep the work per weight byte small:
 //   - E2M1 codes become exact f16 pairs with the hardware conversion (cvt.rn.f16x2.e2m1x2);
 //   - activation rows are staged once per CTA as f16, each row prescaled by a power of two so
 //     that its largest magnitude lies in [2^14, 2^15) (a bf16 value then converts exactly unless
 //     it is more than 2^28 times smaller than the row maximum);
 //   - products w*x are exact and accumulate in fp32 (fma.rn.f32.f16); the block scale and the
 //     row's prescale are applied once per 32-element partial.
-// Work split: a "row group" of G threads covers one weight row, thread j owning K-block j (and
-// j + G when K > 8192), so each thread reads its activation block from shared memory once per
-// batch of kR weight rows rather than once per row.  The kR x Q partial dot products are summed
-// over the group by a warp transpose-reduction and a cross-warp pass through shared memory.
+// One warp owns whole weight rows: lane l takes K-blocks l, l+32, ..., so each row's dot product
+// is finished with warp shuffles and no CTA-wide barrier sits in the streaming loop.  Activation
+// blocks are read from shared memory in an order where the lanes of a warp touch consecutive
+// 16-byte units, and each read serves every weight row of the batch.
 #include "common.cuh"
 
 namespace moe {
 
-constexpr int kThr = 256;       // threads per CTA
-constexpr int kR = 8;           // weight rows per batch per row group
-constexpr int kDownMaxRows = 64;  // staged permuted rows per down CTA
+constexpr int kThr = 256;  // threads per CTA (8 warps)
+constexpr int kWarps = kThr / 32;
+constexpr int kQ = 4;               // activation rows staged per pass (gate/up)
+constexpr int kDownMaxRows = 64;    // staged permuted rows per down CTA
+// rows per warp in the down kernel: fewer for long rows so the double-buffered weights fit
+__host__ __device__ constexpr int down_rows_per_warp(int bpl) { return bpl <= 2 ? 4 : bpl == 4 ? 2 : 1; }
+constexpr int kUpOutsPerWarp = 4;
 
 // ------------------------------------------------------------------ helpers
 
@@ -55,64 +59,54 @@ __device__ __forceinline__ float block_dot(const uint4& codes, const uint32_t (&
     return a0 + a1;
 }
 
-// Sum V values over the 32 lanes of a warp; afterwards lane l holds the warp sum of value
-// l >> (5 - log2 V), for V in {8, 16, 32}.
-template <int V>
-__device__ __forceinline__ float warp_transpose_reduce(float (&a)[V], int lane) {
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
-    for (int half = V / 2, mask = 16; half >= 1; half /= 2, mask /= 2) {
-        const bool upper = (lane & mask) != 0;
-#pragma unroll
-        for (int i = 0; i < half; ++i) {
-            const float send = upper ? a[i] : a[i + half];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, mask);
-            a[i] = (upper ? a[i + half] : a[i]) + recv;
-        }
-    }
-    float v = a[0];
-#pragma unroll
-    for (int mask = (32 / V) / 2; mask >= 1; mask /= 2) v += __shfl_xor_sync(0xffffffffu, v, mask);
+    for (int m = 16; m >= 1; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
     return v;
 }
 
-// Stage activation rows (bf16, K elements each) as prescaled f16 in block-interleaved order:
-// 16-byte unit c (elements 8c..8c+7) of block b of staged row q sits at uint4 index
-// (q * 4 + c) * nb + b, so threads owning consecutive blocks read consecutive units.
-// inv[q] receives 2^-p, the factor that undoes the row's prescale 2^p.  One warp per row.
+__device__ __forceinline__ int prescale_exp(uint32_t mx) {
+    const int p = (mx == 0) ? 0 : 141 - (int)(mx >> 7);  // row maximum * 2^p in [2^14, 2^15)
+    return max(-126, min(126, p));
+}
+
+// All threads of the CTA stage nq activation rows (bf16, K elements) as prescaled f16 in
+// block-interleaved order: 16-byte unit c (elements 8c..8c+7) of block b of staged row q sits at
+// uint4 index (q * 4 + c) * nb + b.  inv[q] = 2^-p undoes the row's prescale.  smax: nq words of
+// shared scratch.  Ends with __syncthreads.
 __device__ void stage_rows_f16(const uint16_t* __restrict__ src, const int* rows, int nq, int K, uint4* dst,
-                               float* inv) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const int nb = K / 32, units = K / 8;
-    for (int q = warp; q < nq; q += nwarps) {
-        const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K);
+                               float* inv, unsigned* smax) {
+    const int tid = threadIdx.x, nb = K / 32, units = K / 8, total = nq * units;
+    if (tid < nq) smax[tid] = 0;
+    __syncthreads();
+#pragma unroll 4
+    for (int i = tid; i < total; i += blockDim.x) {
+        const int q = i / units, u = i - q * units;
+        const uint4 v = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K)[u];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t mx = 0;
-        for (int u = lane; u < units; u += 32) {
-            const uint4 v = s[u];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-        }
-        mx = __reduce_max_sync(0xffffffffu, mx);
-        // biased exponent E of max |x|; p = 141 - E puts the maximum in [2^14, 2^15)
-        int p = (mx == 0) ? 0 : 141 - (int)(mx >> 7);
-        p = max(-126, min(126, p));
-        const float up = __uint_as_float((uint32_t)(127 + p) << 23);
-        const float down = __uint_as_float((uint32_t)(127 - p) << 23);
-        for (int u = lane; u < units; u += 32) {
-            const uint4 v = s[u];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __half lo = __float2half_rn(bf16_bits_to_f32(w[i] & 0xFFFFu) * up);
-                const __half hi = __float2half_rn(bf16_bits_to_f32(w[i] >> 16) * up);
-                o[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-            }
-            const int b = u >> 2, c = u & 3;
-            dst[((size_t)q * 4 + c) * nb + b] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        if (lane == 0) inv[q] = down;
+        for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+        atomicMax(&smax[q], mx);
     }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = tid; i < total; i += blockDim.x) {
+        const int q = i / units, u = i - q * units;
+        const uint4 v = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K)[u];
+        const float up = __uint_as_float((uint32_t)(127 + prescale_exp(smax[q])) << 23);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half lo = __float2half_rn(bf16_bits_to_f32(w[j] & 0xFFFFu) * up);
+            const __half hi = __float2half_rn(bf16_bits_to_f32(w[j] >> 16) * up);
+            o[j] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+        }
+        dst[((size_t)q * 4 + (u & 3)) * nb + (u >> 2)] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (tid < nq) inv[tid] = __uint_as_float((uint32_t)(127 - prescale_exp(smax[tid])) << 23);
+    __syncthreads();
 }
 
 __device__ __forceinline__ void load_x_block(const uint4* xs, int q, int nb, int b, uint32_t (&x)[16]) {
@@ -126,24 +120,6 @@ __device__ __forceinline__ void load_x_block(const uint4* xs, int q, int nb, int
     }
 }
 
-// Row-group geometry for a contraction of K elements: nb = K/32 blocks, bpt blocks per thread,
-// G threads per group (a power of two >= 32 covering nb / bpt), RG = kThr / G groups per CTA.
-struct Geo {
-    int nb, bpt, G, RG;
-};
-
-__host__ __device__ inline Geo make_geo(int K) {
-    Geo g;
-    g.nb = K / 32;
-    g.bpt = (g.nb + kThr - 1) / kThr;
-    const int need = (g.nb + g.bpt - 1) / g.bpt;
-    int G = 32;
-    while (G < need) G *= 2;
-    g.G = G;
-    g.RG = kThr / G;
-    return g;
-}
-
 struct GemvArgs {
     const uint8_t* q0;  // up: gate codes; down: down codes
     const uint8_t* s0;
@@ -155,143 +131,92 @@ struct GemvArgs {
     PlanView plan;
     const float* row_w;  // down, fused: gate weight of each permuted row
     int T, K, M_exp, P, E;
-    int tch;             // down: tokens per chunk
-    int maxrows;         // down: staged permuted rows per CTA (tch * k)
-    int outs;            // output features per CTA
-    uint16_t* out;       // up: h [P][I]; down: y_perm [P][d] or y [T][d]
+    int tch;       // down: tokens per chunk
+    int maxrows;   // down: staged rows per CTA (tch * k)
+    int outs;      // up: output features per CTA; down: rows per CTA
+    uint16_t* out; // up: h [P][I]; down: y_perm [P][d] or y [T][d]
 };
 
-// Weight rows of one batch into registers (rows[j] = global row index, or -1 to skip).
-template <int BPT>
-__device__ __forceinline__ void load_rows(const uint8_t* const (&q)[kR], const uint8_t* const (&s)[kR],
-                                          const size_t (&grow)[kR], int gl, const Geo& geo, size_t row_bytes,
-                                          uint4 (&wv)[kR][BPT], uint32_t (&sv)[kR][BPT]) {
-#pragma unroll
-    for (int j = 0; j < kR; ++j)
-#pragma unroll
-        for (int c = 0; c < BPT; ++c) {
-            const int b = gl + c * geo.G;
-            if (b < geo.nb) {
-                wv[j][c] = ldg_stream(q[j] + grow[j] * row_bytes + 16 * (size_t)b);
-                sv[j][c] = __ldg(s[j] + grow[j] * geo.nb + b);
-            }
-        }
-}
-
-// kR x Q partial dot products of the thread's blocks: acc[qq * kR + j] for staged row q0 + qq
-// (qq < nq) against weight row j.
-template <int BPT, int Q>
-__device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int gl, const Geo& geo,
-                                           const uint4 (&wv)[kR][BPT], const uint32_t (&sv)[kR][BPT],
-                                           float (&acc)[kR * Q]) {
-#pragma unroll
-    for (int v = 0; v < kR * Q; ++v) acc[v] = 0.f;
-#pragma unroll
-    for (int qq = 0; qq < Q; ++qq) {
-        if (qq < nq) {
-#pragma unroll
-            for (int c = 0; c < BPT; ++c) {
-                const int b = gl + c * geo.G;
-                if (b < geo.nb) {
-                    uint32_t x[16];
-                    load_x_block(xs, q0 + qq, geo.nb, b, x);
-#pragma unroll
-                    for (int j = 0; j < kR; ++j)
-                        acc[qq * kR + j] = fmaf(block_dot(wv[j][c], x), e8m0_to_f32(sv[j][c]), acc[qq * kR + j]);
-                }
-            }
-        }
-    }
-}
-
 // ------------------------------------------------------------------ gate/up + SwiGLU
-// Grid (M_exp / outs, slots): slot u is the u-th active expert.  A batch gives each row group
-// kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens.
-template <int BPT, int Q>
-__global__ void __launch_bounds__(kThr)
+// Grid (I / outs, slots): slot u is the u-th active expert.  Warp w computes outputs
+// i = blockIdx.x * outs + w * kUpOutsPerWarp + o, reading gate row i and up row i (lane l owns
+// K-blocks l + 32 j, j < BPL) and the staged activation blocks of up to kQ tokens.
+template <int BPL>
+__global__ void __launch_bounds__(kThr, 2)
 gemv_up_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
-    constexpr int kOut = kR / 2;
-    constexpr int V = kR * Q;
-    const Geo geo = make_geo(a.K);
-    uint4* xs = reinterpret_cast<uint4*>(smem);                              // [Q][K/8]
-    float* inv = reinterpret_cast<float*>(smem + (size_t)Q * a.K * 2);      // [Q]
-    float* red = inv + Q;                                                   // [8 warps][32]
-    int* rows = reinterpret_cast<int*>(red + 8 * 32);                       // [Q]
+    const int nb = a.K / 32;
+    uint4* xs = reinterpret_cast<uint4*>(smem);                                 // [kQ][K/8]
+    float* inv = reinterpret_cast<float*>(smem + (size_t)kQ * a.K * 2);        // [kQ]
+    unsigned* smax = reinterpret_cast<unsigned*>(inv + kQ);                    // [kQ]
+    int* rows = reinterpret_cast<int*>(smax + kQ);                             // [kQ]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int grp = tid / geo.G, gl = tid % geo.G;
-    const int wpg = geo.G / 32;  // warps per group
 
     pdl_wait();
     const int slot = blockIdx.y;
     if (slot >= a.plan.scalars[0]) return;
     const int e = a.plan.active[slot];
     const size_t row_bytes = (size_t)a.K / 2;
-    const int outs_per_group = a.outs / geo.RG;
-    const int nbatch = outs_per_group / kOut;
-    const int i_base = blockIdx.x * a.outs + grp * outs_per_group;
-    const uint8_t* const qsel[kR] = {a.q0, a.q0, a.q0, a.q0, a.q1, a.q1, a.q1, a.q1};
-    const uint8_t* const ssel[kR] = {a.s0, a.s0, a.s0, a.s0, a.s1, a.s1, a.s1, a.s1};
-    auto grows = [&](int bi, size_t (&g)[kR]) {
+    const int i0 = blockIdx.x * a.outs + warp * kUpOutsPerWarp;
+
+    auto load_out = [&](int i, uint4 (&wg)[BPL], uint4 (&wu)[BPL], uint32_t (&sg)[BPL], uint32_t (&su)[BPL]) {
+        const size_t grow = (size_t)e * a.M_exp + i;
 #pragma unroll
-        for (int j = 0; j < kR; ++j) g[j] = (size_t)e * a.M_exp + i_base + bi * kOut + (j % kOut);
+        for (int j = 0; j < BPL; ++j) {
+            const int b = lane + 32 * j;
+            if (b < nb) {
+                wg[j] = ldg_stream(a.q0 + grow * row_bytes + 16 * (size_t)b);
+                wu[j] = ldg_stream(a.q1 + grow * row_bytes + 16 * (size_t)b);
+                sg[j] = __ldg(a.s0 + grow * nb + b);
+                su[j] = __ldg(a.s1 + grow * nb + b);
+            }
+        }
     };
+    uint4 wg[BPL], wu[BPL];
+    uint32_t sg[BPL], su[BPL];
+    load_out(i0, wg, wu, sg, su);  // weights depend only on the expert: start streaming now
 
-    uint4 wcur[kR][BPT], wnxt[kR][BPT];
-    uint32_t scur[kR][BPT], snxt[kR][BPT];
-    {
-        size_t g[kR];
-        grows(0, g);
-        load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wcur, scur);  // weights depend only on e
-    }
     const int r0 = a.offsets[e], n = a.offsets[e + 1] - r0;
-
-    for (int tc0 = 0; tc0 < n; tc0 += Q) {
-        const int nq = min(Q, n - tc0);
-        __syncthreads();
+    for (int tc0 = 0; tc0 < n; tc0 += kQ) {
+        const int nq = min(kQ, n - tc0);
+        if (tc0 > 0) {
+            __syncthreads();
+            load_out(i0, wg, wu, sg, su);
+        }
         if (tid < nq) rows[tid] = a.perm_token[r0 + tc0 + tid];
         __syncthreads();
-        stage_rows_f16(a.act, rows, nq, a.K, xs, inv);
-        __syncthreads();
-        for (int bi = 0; bi < nbatch; ++bi) {
-            const bool more = bi + 1 < nbatch || tc0 + Q < n;
-            if (more) {
-                size_t g[kR];
-                grows(bi + 1 < nbatch ? bi + 1 : 0, g);
-                load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wnxt, snxt);
-            }
-            float acc[V];
-            batch_dots<BPT, Q>(xs, 0, nq, gl, geo, wcur, scur, acc);
-            red[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
-            __syncthreads();
-            if (gl < 32) {
-                // lane l holds value v = l >> (5 - log2 V); v = qq * kR + j
-                const int v = lane >> (5 - (V == 8 ? 3 : V == 16 ? 4 : 5));
-                const int qq = v / kR, j = v % kR;
-                const bool leader = (lane & ((32 / V) - 1)) == 0;
-                if (leader && qq < nq && j < kOut) {
-                    float g = 0.f, u = 0.f;
-                    for (int w = 0; w < wpg; ++w) {
-                        const int wi = (grp * wpg + w) * 32;
-                        g += red[wi + lane];
-                        u += red[wi + lane + kOut * (32 / V)];
+        stage_rows_f16(a.act, rows, nq, a.K, xs, inv, smax);
+        for (int o = 0; o < kUpOutsPerWarp; ++o) {
+            float g[kQ], u[kQ];
+#pragma unroll
+            for (int q = 0; q < kQ; ++q) g[q] = u[q] = 0.f;
+#pragma unroll
+            for (int j = 0; j < BPL; ++j) {
+                const int b = lane + 32 * j;
+                if (b < nb) {
+                    const float fg = e8m0_to_f32(sg[j]), fu = e8m0_to_f32(su[j]);
+#pragma unroll
+                    for (int q = 0; q < kQ; ++q) {
+                        if (q < nq) {
+                            uint32_t x[16];
+                            load_x_block(xs, q, nb, b, x);
+                            g[q] = fmaf(block_dot(wg[j], x), fg, g[q]);
+                            u[q] = fmaf(block_dot(wu[j], x), fu, u[q]);
+                        }
                     }
-                    g *= inv[qq];
-                    u *= inv[qq];
-                    const float hv = g / (1.f + expf(-g)) * u;  // SiLU(g) * u
-                    const int i = i_base + bi * kOut + j;
-                    a.out[(size_t)(r0 + tc0 + qq) * a.M_exp + i] = f32_to_bf16_bits(hv);
                 }
             }
-            __syncthreads();
-            if (more) {
+            // next output's rows are independent of this one's arithmetic
+            if (o + 1 < kUpOutsPerWarp) load_out(i0 + o + 1, wg, wu, sg, su);
 #pragma unroll
-                for (int j = 0; j < kR; ++j)
-#pragma unroll
-                    for (int c = 0; c < BPT; ++c) {
-                        wcur[j][c] = wnxt[j][c];
-                        scur[j][c] = snxt[j][c];
+            for (int q = 0; q < kQ; ++q) {
+                if (q < nq) {
+                    const float gs = warp_sum(g[q]) * inv[q], us = warp_sum(u[q]) * inv[q];
+                    if (lane == q) {
+                        const float hv = gs / (1.f + expf(-gs)) * us;  // SiLU(g) * u
+                        a.out[(size_t)(r0 + tc0 + q) * a.M_exp + i0 + o] = f32_to_bf16_bits(hv);
                     }
+                }
             }
         }
     }
@@ -300,38 +225,37 @@ gemv_up_kernel(const GemvArgs a) {
 
 // ------------------------------------------------------------------ down (+ weighted sum)
 // Grid (d / outs, token chunks).  The CTA stages every permuted row whose token lies in its chunk
-// (rows are expert-major, so each active expert forms a consecutive segment), then for each
-// segment computes its outputs: each row group owns kR output features.
-// FUSED: y[t] accumulates w * bf16(expert output) in ascending expert order, which is the slot
-// order j of the token (ids are ascending); otherwise the bf16 outputs go to y_perm.
-template <int BPT, int Q, bool FUSED>
-__global__ void __launch_bounds__(kThr)
+// (rows are expert-major, so each active expert forms a consecutive segment).  Warp w owns rows
+// n = blockIdx.x * outs + w * RPW + rr and walks the segments in ascending expert
+// order, prefetching the next segment's weight rows.
+// FUSED: y[t] accumulates w * bf16(expert output) in that order, which is the slot order j of the
+// token (ids are ascending); otherwise the bf16 expert outputs go to y_perm.
+template <int BPL, bool FUSED>
+__global__ void __launch_bounds__(kThr, 2)
 gemv_down_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
-    constexpr int V = kR * Q;
-    const Geo geo = make_geo(a.K);
-    const int mr = a.maxrows;
-    uint4* hs = reinterpret_cast<uint4*>(smem);                                       // [mr][K/8]
-    float* inv = reinterpret_cast<float*>(smem + (size_t)mr * a.K * 2);              // [mr]
-    float* red = inv + mr;                                                           // [8][32]
-    float* ys = red + 8 * 32;                                                        // [tch][outs]
-    int* s_row = reinterpret_cast<int*>(ys + 8 * a.outs);                            // [mr]
+    constexpr int RPW = down_rows_per_warp(BPL);
+    const int nb = a.K / 32, mr = a.maxrows;
+    uint4* hs = reinterpret_cast<uint4*>(smem);                                  // [mr][K/8]
+    float* inv = reinterpret_cast<float*>(smem + (size_t)mr * a.K * 2);         // [mr]
+    unsigned* smax = reinterpret_cast<unsigned*>(inv + mr);                     // [mr]
+    float* ys = reinterpret_cast<float*>(smax + mr);                            // [tch][outs]
+    int* s_row = reinterpret_cast<int*>(ys + (size_t)a.tch * a.outs);          // [mr]
     int* s_tok = s_row + mr;
     int* s_exp = s_tok + mr;
     float* s_w = reinterpret_cast<float*>(s_exp + mr);
-    int* s_off = reinterpret_cast<int*>(s_w + mr);                                   // [E+1]
-    __shared__ int wtot[8];
+    int* s_off = reinterpret_cast<int*>(s_w + mr);                              // [E+1]
+    __shared__ int wtot[kWarps];
     __shared__ int s_cnt;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int grp = tid / geo.G, gl = tid % geo.G;
-    const int wpg = geo.G / 32;
     const int t0 = blockIdx.y * a.tch, t1 = min(a.T, t0 + a.tch);
     const size_t row_bytes = (size_t)a.K / 2;
-    const int n_base = blockIdx.x * a.outs + grp * kR;
+    const int nl0 = warp * RPW;                       // first local row of this warp
+    const int n0 = blockIdx.x * a.outs + nl0;         // first global row of this warp
 
     pdl_wait();
     for (int i = tid; i <= a.E; i += blockDim.x) s_off[i] = a.offsets[i];
-    for (int i = tid; i < 8 * a.outs; i += blockDim.x) ys[i] = 0.f;
+    for (int i = tid; i < a.tch * a.outs; i += blockDim.x) ys[i] = 0.f;
     if (tid == 0) s_cnt = 0;
     __syncthreads();
     // rows of the chunk in permuted order (stable compaction over all P rows), with their expert
@@ -346,7 +270,7 @@ gemv_down_kernel(const GemvArgs a) {
         for (int w = 0; w < warp; ++w) before += wtot[w];
         if (in) {
             const int pos = before + __popc(bal & ((1u << lane) - 1u));
-            int lo = 0, hi = a.E;  // expert: last e with offsets[e] <= r
+            int lo = 0, hi = a.E;  // expert of row r: last e with offsets[e] <= r
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
                 if (s_off[mid] <= r) lo = mid; else hi = mid;
@@ -359,77 +283,80 @@ gemv_down_kernel(const GemvArgs a) {
         __syncthreads();
         if (tid == 0) {
             int tot = 0;
-            for (int w = 0; w < 8; ++w) tot += wtot[w];
+            for (int w = 0; w < kWarps; ++w) tot += wtot[w];
             s_cnt += tot;
         }
         __syncthreads();
     }
     const int nrows = s_cnt;
-    stage_rows_f16(a.act, s_row, nrows, a.K, hs, inv);
-    __syncthreads();
+    stage_rows_f16(a.act, s_row, nrows, a.K, hs, inv, smax);
 
-    const uint8_t* const qsel[kR] = {a.q0, a.q0, a.q0, a.q0, a.q0, a.q0, a.q0, a.q0};
-    const uint8_t* const ssel[kR] = {a.s0, a.s0, a.s0, a.s0, a.s0, a.s0, a.s0, a.s0};
-    auto grows = [&](int e, size_t (&g)[kR]) {
+    auto load_rows = [&](int e, uint4 (&wv)[RPW][BPL], uint32_t (&sv)[RPW][BPL]) {
 #pragma unroll
-        for (int j = 0; j < kR; ++j) g[j] = (size_t)e * a.M_exp + n_base + j;
+        for (int rr = 0; rr < RPW; ++rr) {
+            const size_t grow = (size_t)e * a.M_exp + n0 + rr;
+#pragma unroll
+            for (int j = 0; j < BPL; ++j) {
+                const int b = lane + 32 * j;
+                if (b < nb) {
+                    wv[rr][j] = ldg_stream(a.q0 + grow * row_bytes + 16 * (size_t)b);
+                    sv[rr][j] = __ldg(a.s0 + grow * nb + b);
+                }
+            }
+        }
     };
-    uint4 wcur[kR][BPT], wnxt[kR][BPT];
-    uint32_t scur[kR][BPT], snxt[kR][BPT];
+    uint4 wcur[RPW][BPL], wnxt[RPW][BPL];
+    uint32_t scur[RPW][BPL], snxt[RPW][BPL];
     int qs = 0;
-    if (nrows > 0) {
-        size_t g[kR];
-        grows(s_exp[0], g);
-        load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wcur, scur);
-    }
+    if (nrows > 0) load_rows(s_exp[0], wcur, scur);
     while (qs < nrows) {
         const int e = s_exp[qs];
         int qe = qs + 1;
         while (qe < nrows && s_exp[qe] == e) ++qe;
         const bool more = qe < nrows;
-        if (more) {
-            size_t g[kR];
-            grows(s_exp[qe], g);
-            load_rows<BPT>(qsel, ssel, g, gl, geo, row_bytes, wnxt, snxt);
-        }
-        for (int qa = qs; qa < qe; qa += Q) {
-            const int nq = min(Q, qe - qa);
-            float acc[V];
-            batch_dots<BPT, Q>(hs, qa, nq, gl, geo, wcur, scur, acc);
-            red[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
-            __syncthreads();
-            if (gl < 32) {
-                const int v = lane >> (5 - (V == 8 ? 3 : V == 16 ? 4 : 5));
-                const int qq = v / kR, j = v % kR;
-                const bool leader = (lane & ((32 / V) - 1)) == 0;
-                if (leader && qq < nq) {
-                    float s = 0.f;
-                    for (int w = 0; w < wpg; ++w) s += red[(grp * wpg + w) * 32 + lane];
-                    const int q = qa + qq;
-                    const uint16_t sb = f32_to_bf16_bits(s * inv[q]);
-                    const int nn = grp * kR + j;
+        if (more) load_rows(s_exp[qe], wnxt, snxt);
+        for (int q = qs; q < qe; ++q) {
+            float acc[RPW];
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) acc[rr] = 0.f;
+#pragma unroll
+            for (int j = 0; j < BPL; ++j) {
+                const int b = lane + 32 * j;
+                if (b < nb) {
+                    uint32_t x[16];
+                    load_x_block(hs, q, nb, b, x);
+#pragma unroll
+                    for (int rr = 0; rr < RPW; ++rr)
+                        acc[rr] = fmaf(block_dot(wcur[rr][j], x), e8m0_to_f32(scur[rr][j]), acc[rr]);
+                }
+            }
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+                const float s = warp_sum(acc[rr]) * inv[q];
+                if (lane == rr) {
+                    const uint16_t sb = f32_to_bf16_bits(s);
                     if (FUSED) {
-                        float& yv = ys[s_tok[q] * a.outs + nn];
+                        float& yv = ys[s_tok[q] * a.outs + nl0 + rr];
                         yv = fmaf(s_w[q], bf16_bits_to_f32(sb), yv);
                     } else {
-                        a.out[(size_t)s_row[q] * a.M_exp + blockIdx.x * a.outs + nn] = sb;
+                        a.out[(size_t)s_row[q] * a.M_exp + n0 + rr] = sb;
                     }
                 }
             }
-            __syncthreads();
         }
         if (more) {
 #pragma unroll
-            for (int j = 0; j < kR; ++j)
+            for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
-                for (int c = 0; c < BPT; ++c) {
-                    wcur[j][c] = wnxt[j][c];
-                    scur[j][c] = snxt[j][c];
+                for (int j = 0; j < BPL; ++j) {
+                    wcur[rr][j] = wnxt[rr][j];
+                    scur[rr][j] = snxt[rr][j];
                 }
         }
         qs = qe;
     }
     if (FUSED) {
+        __syncthreads();
         for (int i = tid; i < a.outs * (t1 - t0); i += blockDim.x) {
             const int tt = i / a.outs, nn = i % a.outs;
             a.out[(size_t)(t0 + tt) * a.M_exp + blockIdx.x * a.outs + nn] = f32_to_bf16_bits(ys[tt * a.outs + nn]);
@@ -469,32 +396,21 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_
 
 // ------------------------------------------------------------------ launchers
 
-bool gemv_supported(int d, int I) { return d / 32 <= 2 * kThr && I / 32 <= 2 * kThr; }
-
-static int pow2_q(int n) { return n <= 1 ? 1 : n <= 2 ? 2 : 4; }
-
-template <int BPT, int Q>
-static const void* up_kernel() { return (const void*)gemv_up_kernel<BPT, Q>; }
-
-template <int BPT, bool F>
-static const void* down_kernel(int q) {
-    if (q == 1) return (const void*)gemv_down_kernel<BPT, 1, F>;
-    if (q == 2) return (const void*)gemv_down_kernel<BPT, 2, F>;
-    return (const void*)gemv_down_kernel<BPT, 4, F>;
+static int bpl_for(int K) {
+    const int nb = K / 32;
+    return nb <= 32 ? 1 : nb <= 64 ? 2 : nb <= 128 ? 4 : nb <= 256 ? 8 : 0;
 }
+
+bool gemv_supported(int d, int I) { return bpl_for(d) != 0 && bpl_for(I) != 0; }
 
 cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,
                            cudaStream_t st, bool pdl) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
-    if (!gemv_supported(d, I)) return cudaErrorInvalidValue;
-    const Geo geo = make_geo(d);
-    const int unit = geo.RG * (kR / 2);
-    if (I % unit != 0) return cudaErrorInvalidValue;
-    int outs = unit;  // outputs per CTA: a multiple of unit dividing I, at most 64
-    for (int o = unit; o <= 64 && o <= I; o += unit)
-        if (I % o == 0) outs = o;
+    const int bpl = bpl_for(d);
+    const int outs = kWarps * kUpOutsPerWarp;
+    if (bpl == 0 || I % outs != 0) return cudaErrorInvalidValue;
     GemvArgs a = {};
     a.q0 = W->gate_q;
     a.s0 = W->gate_s;
@@ -511,27 +427,30 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
     a.E = E;
     a.outs = outs;
     a.out = h;
-    const int Q = pow2_q(T);
-    const size_t smem = (size_t)Q * d * 2 + sizeof(float) * (Q + 8 * 32) + sizeof(int) * Q;
+    const size_t smem = (size_t)kQ * d * 2 + sizeof(float) * kQ + sizeof(unsigned) * kQ + sizeof(int) * kQ;
     void* args[] = {&a};
     const dim3 grid(I / outs, P < E ? P : E);
-    const void* f;
-    if (geo.bpt == 1) f = Q == 1 ? up_kernel<1, 1>() : Q == 2 ? up_kernel<1, 2>() : up_kernel<1, 4>();
-    else f = Q == 1 ? up_kernel<2, 1>() : Q == 2 ? up_kernel<2, 2>() : up_kernel<2, 4>();
+    const void* f = bpl == 1 ? (const void*)gemv_up_kernel<1> : bpl == 2 ? (const void*)gemv_up_kernel<2>
+                  : bpl == 4 ? (const void*)gemv_up_kernel<4> : (const void*)gemv_up_kernel<8>;
     return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
+}
+
+template <bool F>
+static const void* down_kernel(int bpl) {
+    return bpl == 1 ? (const void*)gemv_down_kernel<1, F> : bpl == 2 ? (const void*)gemv_down_kernel<2, F>
+         : bpl == 4 ? (const void*)gemv_down_kernel<4, F> : (const void*)gemv_down_kernel<8, F>;
 }
 
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                              const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
                              uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
-    if (!gemv_supported(d, I)) return cudaErrorInvalidValue;
-    const Geo geo = make_geo(I);
-    const int outs = geo.RG * kR;  // each row group owns kR output features
-    if (d % outs != 0) return cudaErrorInvalidValue;
-    // tokens per chunk: at most 8, at most kDownMaxRows staged rows, staged h <= 160 KB
+    const int bpl = bpl_for(I);
+    const int outs = kWarps * down_rows_per_warp(bpl);
+    if (bpl == 0 || d % outs != 0) return cudaErrorInvalidValue;
+    // tokens per chunk: at most 8, at most kDownMaxRows staged rows, staged h <= 100 KB
     int tch = 8;
-    while (tch > 1 && ((size_t)tch * k > kDownMaxRows || (size_t)tch * k * I * 2 > 160 * 1024)) tch /= 2;
+    while (tch > 1 && ((size_t)tch * k > kDownMaxRows || (size_t)tch * k * I * 2 > 100 * 1024)) tch /= 2;
     if (tch > T) tch = T;
     if ((size_t)tch * k > kDownMaxRows || (size_t)tch * k * I * 2 > 200 * 1024) return cudaErrorInvalidValue;
     GemvArgs a = {};
@@ -552,14 +471,11 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
     a.outs = outs;
     a.out = y ? y : y_perm;
     const size_t mr = (size_t)tch * k;
-    const size_t smem = mr * I * 2 + sizeof(float) * (mr + 8 * 32 + 8 * outs) + sizeof(int) * (3 * mr) +
-                        sizeof(float) * mr + sizeof(int) * (E + 1);
+    const size_t smem = mr * I * 2 + sizeof(float) * mr + sizeof(unsigned) * mr + sizeof(float) * tch * outs +
+                        sizeof(int) * 3 * mr + sizeof(float) * mr + sizeof(int) * (E + 1);
     void* args[] = {&a};
     const dim3 grid(d / outs, (T + tch - 1) / tch);
-    const int Q = pow2_q(tch);  // rows of one expert in a chunk: at most one per token
-    const void* f;
-    if (y) f = geo.bpt == 1 ? down_kernel<1, true>(Q) : down_kernel<2, true>(Q);
-    else f = geo.bpt == 1 ? down_kernel<1, false>(Q) : down_kernel<2, false>(Q);
+    const void* f = y ? down_kernel<true>(bpl) : down_kernel<false>(bpl);
     return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
 }
 
