@@ -223,6 +223,227 @@ gemv_up_kernel(const GemvArgs a) {
     pdl_launch_dependents();
 }
 
+
+// ------------------------------------------------------------------ gate/up + SwiGLU, T <= 2
+// For one or two tokens a CTA-wide split of K is faster than whole rows per warp: the weight
+// rows of a batch are prefetched into registers one batch ahead and every thread owns one
+// K-block, so the activations need no shared-memory traffic per row.
+constexpr int kR = 8;  // weight rows per batch per row group
+
+// Sum V values over the 32 lanes of a warp; afterwards lane l holds the warp sum of value
+// l >> (5 - log2 V), for V in {8, 16, 32}.
+template <int V>
+__device__ __forceinline__ float warp_transpose_reduce(float (&a)[V], int lane) {
+#pragma unroll
+    for (int half = V / 2, mask = 16; half >= 1; half /= 2, mask /= 2) {
+        const bool upper = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? a[i] : a[i + half];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, mask);
+            a[i] = (upper ? a[i + half] : a[i]) + recv;
+        }
+    }
+    float v = a[0];
+#pragma unroll
+    for (int mask = (32 / V) / 2; mask >= 1; mask /= 2) v += __shfl_xor_sync(0xffffffffu, v, mask);
+    return v;
+}
+
+// Row-group geometry for a contraction of K elements: nb = K/32 blocks, bpt blocks per thread,
+// G threads per group (a power of two >= 32 covering nb / bpt), RG = kThr / G groups per CTA.
+struct CtaGeo {
+    int nb, bpt, G, RG;
+};
+
+__host__ __device__ inline CtaGeo make_cta_geo(int K) {
+    CtaGeo g;
+    g.nb = K / 32;
+    g.bpt = (g.nb + kThr - 1) / kThr;
+    const int need = (g.nb + g.bpt - 1) / g.bpt;
+    int G = 32;
+    while (G < need) G *= 2;
+    g.G = G;
+    g.RG = kThr / G;
+    return g;
+}
+
+// Stage activation rows (bf16, K elements each) as prescaled f16 in block-interleaved order:
+// 16-byte unit c (elements 8c..8c+7) of block b of staged row q sits at uint4 index
+// (q * 4 + c) * nb + b, so threads owning consecutive blocks read consecutive units.
+// inv[q] receives 2^-p, the factor that undoes the row's prescale 2^p.  One warp per row.
+__device__ void stage_rows_warp(const uint16_t* __restrict__ src, const int* rows, int nq, int K, uint4* dst,
+                               float* inv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const int nb = K / 32, units = K / 8;
+    for (int q = warp; q < nq; q += nwarps) {
+        const uint4* s = reinterpret_cast<const uint4*>(src + (size_t)rows[q] * K);
+        uint32_t mx = 0;
+        for (int u = lane; u < units; u += 32) {
+            const uint4 v = s[u];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mx = max(mx, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+        }
+        mx = __reduce_max_sync(0xffffffffu, mx);
+        // biased exponent E of max |x|; p = 141 - E puts the maximum in [2^14, 2^15)
+        int p = (mx == 0) ? 0 : 141 - (int)(mx >> 7);
+        p = max(-126, min(126, p));
+        const float up = __uint_as_float((uint32_t)(127 + p) << 23);
+        const float down = __uint_as_float((uint32_t)(127 - p) << 23);
+        for (int u = lane; u < units; u += 32) {
+            const uint4 v = s[u];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __half lo = __float2half_rn(bf16_bits_to_f32(w[i] & 0xFFFFu) * up);
+                const __half hi = __float2half_rn(bf16_bits_to_f32(w[i] >> 16) * up);
+                o[i] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+            }
+            const int b = u >> 2, c = u & 3;
+            dst[((size_t)q * 4 + c) * nb + b] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (lane == 0) inv[q] = down;
+    }
+}
+
+// Weight rows of one batch into registers (rows[j] = global row index, or -1 to skip).
+template <int BPT>
+__device__ __forceinline__ void load_rows_cta(const uint8_t* const (&q)[kR], const uint8_t* const (&s)[kR],
+                                          const size_t (&grow)[kR], int gl, const CtaGeo& geo, size_t row_bytes,
+                                          uint4 (&wv)[kR][BPT], uint32_t (&sv)[kR][BPT]) {
+#pragma unroll
+    for (int j = 0; j < kR; ++j)
+#pragma unroll
+        for (int c = 0; c < BPT; ++c) {
+            const int b = gl + c * geo.G;
+            if (b < geo.nb) {
+                wv[j][c] = ldg_stream(q[j] + grow[j] * row_bytes + 16 * (size_t)b);
+                sv[j][c] = __ldg(s[j] + grow[j] * geo.nb + b);
+            }
+        }
+}
+
+// kR x Q partial dot products of the thread's blocks: acc[qq * kR + j] for staged row q0 + qq
+// (qq < nq) against weight row j.
+template <int BPT, int Q>
+__device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int gl, const CtaGeo& geo,
+                                           const uint4 (&wv)[kR][BPT], const uint32_t (&sv)[kR][BPT],
+                                           float (&acc)[kR * Q]) {
+#pragma unroll
+    for (int v = 0; v < kR * Q; ++v) acc[v] = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < Q; ++qq) {
+        if (qq < nq) {
+#pragma unroll
+            for (int c = 0; c < BPT; ++c) {
+                const int b = gl + c * geo.G;
+                if (b < geo.nb) {
+                    uint32_t x[16];
+                    load_x_block(xs, q0 + qq, geo.nb, b, x);
+#pragma unroll
+                    for (int j = 0; j < kR; ++j)
+                        acc[qq * kR + j] = fmaf(block_dot(wv[j][c], x), e8m0_to_f32(sv[j][c]), acc[qq * kR + j]);
+                }
+            }
+        }
+    }
+}
+
+// Grid (M_exp / outs, slots): slot u is the u-th active expert.  A batch gives each row group
+// kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens.
+template <int BPT, int Q>
+__global__ void __launch_bounds__(kThr)
+gemv_up_cta_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int kOut = kR / 2;
+    constexpr int V = kR * Q;
+    const CtaGeo geo = make_cta_geo(a.K);
+    uint4* xs = reinterpret_cast<uint4*>(smem);                              // [Q][K/8]
+    float* inv = reinterpret_cast<float*>(smem + (size_t)Q * a.K * 2);      // [Q]
+    float* red = inv + Q;                                                   // [8 warps][32]
+    int* rows = reinterpret_cast<int*>(red + 8 * 32);                       // [Q]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = tid / geo.G, gl = tid % geo.G;
+    const int wpg = geo.G / 32;  // warps per group
+
+    pdl_wait();
+    const int slot = blockIdx.y;
+    if (slot >= a.plan.scalars[0]) return;
+    const int e = a.plan.active[slot];
+    const size_t row_bytes = (size_t)a.K / 2;
+    const int outs_per_group = a.outs / geo.RG;
+    const int nbatch = outs_per_group / kOut;
+    const int i_base = blockIdx.x * a.outs + grp * outs_per_group;
+    const uint8_t* const qsel[kR] = {a.q0, a.q0, a.q0, a.q0, a.q1, a.q1, a.q1, a.q1};
+    const uint8_t* const ssel[kR] = {a.s0, a.s0, a.s0, a.s0, a.s1, a.s1, a.s1, a.s1};
+    auto grows = [&](int bi, size_t (&g)[kR]) {
+#pragma unroll
+        for (int j = 0; j < kR; ++j) g[j] = (size_t)e * a.M_exp + i_base + bi * kOut + (j % kOut);
+    };
+
+    uint4 wcur[kR][BPT], wnxt[kR][BPT];
+    uint32_t scur[kR][BPT], snxt[kR][BPT];
+    {
+        size_t g[kR];
+        grows(0, g);
+        load_rows_cta<BPT>(qsel, ssel, g, gl, geo, row_bytes, wcur, scur);  // weights depend only on e
+    }
+    const int r0 = a.offsets[e], n = a.offsets[e + 1] - r0;
+
+    for (int tc0 = 0; tc0 < n; tc0 += Q) {
+        const int nq = min(Q, n - tc0);
+        __syncthreads();
+        if (tid < nq) rows[tid] = a.perm_token[r0 + tc0 + tid];
+        __syncthreads();
+        stage_rows_warp(a.act, rows, nq, a.K, xs, inv);
+        __syncthreads();
+        for (int bi = 0; bi < nbatch; ++bi) {
+            const bool more = bi + 1 < nbatch || tc0 + Q < n;
+            if (more) {
+                size_t g[kR];
+                grows(bi + 1 < nbatch ? bi + 1 : 0, g);
+                load_rows_cta<BPT>(qsel, ssel, g, gl, geo, row_bytes, wnxt, snxt);
+            }
+            float acc[V];
+            batch_dots<BPT, Q>(xs, 0, nq, gl, geo, wcur, scur, acc);
+            red[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
+            __syncthreads();
+            if (gl < 32) {
+                // lane l holds value v = l >> (5 - log2 V); v = qq * kR + j
+                const int v = lane >> (5 - (V == 8 ? 3 : V == 16 ? 4 : 5));
+                const int qq = v / kR, j = v % kR;
+                const bool leader = (lane & ((32 / V) - 1)) == 0;
+                if (leader && qq < nq && j < kOut) {
+                    float g = 0.f, u = 0.f;
+                    for (int w = 0; w < wpg; ++w) {
+                        const int wi = (grp * wpg + w) * 32;
+                        g += red[wi + lane];
+                        u += red[wi + lane + kOut * (32 / V)];
+                    }
+                    g *= inv[qq];
+                    u *= inv[qq];
+                    const float hv = g / (1.f + expf(-g)) * u;  // SiLU(g) * u
+                    const int i = i_base + bi * kOut + j;
+                    a.out[(size_t)(r0 + tc0 + qq) * a.M_exp + i] = f32_to_bf16_bits(hv);
+                }
+            }
+            __syncthreads();
+            if (more) {
+#pragma unroll
+                for (int j = 0; j < kR; ++j)
+#pragma unroll
+                    for (int c = 0; c < BPT; ++c) {
+                        wcur[j][c] = wnxt[j][c];
+                        scur[j][c] = snxt[j][c];
+                    }
+            }
+        }
+    }
+    pdl_launch_dependents();
+}
+
 // ------------------------------------------------------------------ down (+ weighted sum)
 // Grid (d / outs, token chunks).  The CTA stages every permuted row whose token lies in its chunk
 // (rows are expert-major, so each active expert forms a consecutive segment).  Warp w owns rows
@@ -409,6 +630,39 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
     const int P = T * k;
     if (P == 0) return cudaSuccess;
     const int bpl = bpl_for(d);
+    if (T <= 2 && make_cta_geo(d).bpt <= 2) {
+        // one or two tokens: CTA-wide split of K (see gemv_up_cta_kernel)
+        const CtaGeo geo = make_cta_geo(d);
+        const int unit = geo.RG * (kR / 2);
+        if (I % unit != 0) return cudaErrorInvalidValue;
+        int outs = unit;  // outputs per CTA: a multiple of unit dividing I, at most 64
+        for (int o = unit; o <= 64 && o <= I; o += unit)
+            if (I % o == 0) outs = o;
+        GemvArgs a = {};
+        a.q0 = W->gate_q;
+        a.s0 = W->gate_s;
+        a.q1 = W->up_q;
+        a.s1 = W->up_s;
+        a.act = x;
+        a.perm_token = perm_token;
+        a.offsets = offsets;
+        a.plan = plan;
+        a.T = T;
+        a.K = d;
+        a.M_exp = I;
+        a.P = P;
+        a.E = E;
+        a.outs = outs;
+        a.out = h;
+        const int Q = T;
+        const size_t smem = (size_t)Q * d * 2 + sizeof(float) * (Q + 8 * 32) + sizeof(int) * Q;
+        void* args[] = {&a};
+        const dim3 grid(I / outs, P < E ? P : E);
+        const void* f;
+        if (geo.bpt == 1) f = Q == 1 ? (const void*)gemv_up_cta_kernel<1, 1> : (const void*)gemv_up_cta_kernel<1, 2>;
+        else f = Q == 1 ? (const void*)gemv_up_cta_kernel<2, 1> : (const void*)gemv_up_cta_kernel<2, 2>;
+        return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
+    }
     const int outs = kWarps * kUpOutsPerWarp;
     if (bpl == 0 || I % outs != 0) return cudaErrorInvalidValue;
     GemvArgs a = {};
