@@ -132,13 +132,24 @@ __device__ __forceinline__ float2 h2_to_f2(uint32_t h) {
     return __half22float2(v);
 }
 
-// MX quantisation of one element given the block exponent X (OCP MX rule): round |v| / 2^X
-// to nearest on the E2M1 magnitude grid {0, .5, 1, 1.5, 2, 3, 4, 6}, ties to the even code,
-// saturating; a value that rounds to zero gets code 0 (never -0).
-__device__ __forceinline__ uint32_t e2m1_encode(float v, float inv_scale) {
-    float a = fabsf(v) * inv_scale;
-    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
-    return (c != 0 && v < 0.f) ? (c | 8u) : c;
+// MX quantisation of eight elements already divided by the block scale 2^X (an exact power-of-
+// two product): each is rounded to nearest on the E2M1 magnitude grid {0, .5, 1, 1.5, 2, 3, 4, 6},
+// ties to the even code, saturating at 6 (OCP MX rule).  That is what the hardware conversion to
+// E2M1 does (round to nearest even, satfinite); it returns -0 for a negative value that rounds to
+// zero, which is cleared to code 0.  Element 0 lands in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x8_encode(const float* a) {
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(a[0]), "f"(a[1]), "f"(a[2]), "f"(a[3]), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7]));
+    const uint32_t mag = r & 0x77777777u;
+    const uint32_t nonzero = (mag + 0x77777777u) & 0x88888888u;  // bit 3 of a nibble: magnitude != 0
+    return mag | (r & nonzero);
 }
 
 // Block exponent X = floor(log2(amax)) - 2 clamped to [-127, 127] (amax = 0 gives -127).
@@ -149,6 +160,23 @@ __device__ __forceinline__ uint32_t mx_scale_from_amax(float amax, float& inv_sc
     if (X < -127) X = -127;
     inv_scale = __uint_as_float((uint32_t)(127 - X) << 23);
     return (uint32_t)(X + 127);
+}
+
+// A whole 32-element block: returns the scale byte and writes the 16 bytes of codes
+// (v is overwritten with v / 2^X).
+__device__ __forceinline__ uint32_t mx_block_encode(float (&v)[32], uint4& codes) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float inv;
+    const uint32_t sb = mx_scale_from_amax(amax, inv);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= inv;
+    codes.x = e2m1x8_encode(v);
+    codes.y = e2m1x8_encode(v + 8);
+    codes.z = e2m1x8_encode(v + 16);
+    codes.w = e2m1x8_encode(v + 24);
+    return sb;
 }
 
 // Byte offset of (row, scale column) in the tensor-core scale layout of a matrix whose rows
@@ -190,6 +218,8 @@ cudaError_t launch_synth(uint64_t seed, uint32_t tensor_id, uint32_t expert_firs
 cudaError_t launch_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w, cudaStream_t st);
 cudaError_t launch_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma, cudaStream_t st);
+cudaError_t launch_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
+                                       uint8_t* s_mma, cudaStream_t st);
 
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
                                 float* logits, cudaStream_t st, bool pdl);

@@ -22,20 +22,9 @@ __global__ void pack_kernel(const float* __restrict__ w, int64_t nblocks, uint8_
             v[4 * i + 2] = f.z;
             v[4 * i + 3] = f.w;
         }
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        float inv;
-        uint32_t sb = mx_scale_from_amax(amax, inv);
-        uint32_t words[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            uint32_t wd = 0;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) wd |= e2m1_encode(v[8 * m + n], inv) << (4 * n);
-            words[m] = wd;
-        }
-        reinterpret_cast<uint4*>(q)[blk] = make_uint4(words[0], words[1], words[2], words[3]);
+        uint4 codes;
+        const uint32_t sb = mx_block_encode(v, codes);
+        reinterpret_cast<uint4*>(q)[blk] = codes;
         s[blk] = (uint8_t)sb;
     }
 }
@@ -70,6 +59,21 @@ __global__ void scales_to_mma_kernel(const uint8_t* __restrict__ s, int64_t rows
     }
 }
 
+// Paired layout: row block m of the virtual [2*rows][K] matrix = rows 64m..64m+63 of a, then
+// the same rows of b.  One thread per output byte.
+__global__ void scales_to_mma_paired_kernel(const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
+                                            int64_t rows, int64_t K, uint8_t* __restrict__ out) {
+    const int64_t cols = K / 32, total = 2 * rows * cols;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t vr = i / cols, c = i % cols;  // row of the virtual paired matrix
+        const int64_t m = vr / 128, r = vr % 128;
+        const int64_t src_row = 64 * m + (r & 63);
+        const uint8_t* src = r < 64 ? sa : sb;
+        out[mma_scale_offset(vr, c, K)] = src[src_row * cols + c];
+    }
+}
+
 static unsigned grid_for(int64_t n, int threads) {
     int64_t b = (n + threads - 1) / threads;
     if (b > 152 * 64) b = 152 * 64;
@@ -94,6 +98,14 @@ cudaError_t launch_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint
     int64_t n = rows * (K / 32);
     if (n == 0) return cudaSuccess;
     scales_to_mma_kernel<<<grid_for(n, 256), 256, 0, st>>>(s, rows, K, s_mma);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
+                                       uint8_t* s_mma, cudaStream_t st) {
+    int64_t n = 2 * rows * (K / 32);
+    if (n == 0) return cudaSuccess;
+    scales_to_mma_paired_kernel<<<grid_for(n, 256), 256, 0, st>>>(s_a, s_b, rows, K, s_mma);
     return cudaGetLastError();
 }
 

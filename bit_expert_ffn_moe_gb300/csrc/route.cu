@@ -418,20 +418,9 @@ __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks
                 v[8 * i + 2 * m + 1] = bf16_bits_to_f32(ww[m] >> 16);
             }
         }
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        float inv;
-        uint32_t sb = mx_scale_from_amax(amax, inv);
-        uint32_t words[4];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            uint32_t wd = 0;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) wd |= e2m1_encode(v[8 * m + n], inv) << (4 * n);
-            words[m] = wd;
-        }
-        reinterpret_cast<uint4*>(xq)[blk] = make_uint4(words[0], words[1], words[2], words[3]);
+        uint4 codes;
+        const uint32_t sb = mx_block_encode(v, codes);
+        reinterpret_cast<uint4*>(xq)[blk] = codes;
         xs[blk] = (uint8_t)sb;
     }
 }

@@ -6,19 +6,27 @@
 // batch).  Expert weights and activations are both MXFP4 (DGX Spark news item, section 2: the
 // block-scaled 4-bit MXFP4 expert path), so the MMA consumes them without any dequantisation.
 //
-// Roles: the weights are the MMA "A" operand (M = 128 weight rows per tile) and the tokens of
-// one expert are "B" (N = 32..128 tokens), so an expert with few tokens costs a narrow MMA rather
-// than a padded 128-token tile.  D[m][n] = sum_k A[m][k] * B[n][k] lives in tensor memory.
+// Roles: the tokens of one expert are the MMA "A" operand (M = 128 padded token rows) and a
+// block of weight rows is "B" (N = 128).  D[m][n] = sum_k A[m][k] * B[n][k] lives in tensor
+// memory with lane m = token and column n = weight row, so an epilogue thread owns one token
+// row and one tcgen05.ld of 32 columns hands it a whole 32-element block of the output: the
+// SwiGLU result is requantised to MXFP4 with no cross-lane traffic, and y rows are written as
+// contiguous 64-byte pieces.
+//   up:   B = 64 gate rows followed by the same 64 up rows (two TMA boxes), so D holds g in
+//         columns 0..63 and u in columns 64..127 of 64 consecutive intermediate rows; the block
+//         scales of the pair come pre-arranged side by side (paired tensor-core layout).
+//   down: B = 128 rows of W_down (128 output features).
+// Tiles are (expert e, token tile j, weight block p) with p fastest: CTAs that run at the same
+// time share a token tile through L2 and walk the expert's weight blocks, each of which stays in
+// L2 while the expert's other token tiles use it.
 //
-// One persistent CTA per SM walks the tile list (expert, 128-row weight block, token tile):
-//   warp 0    TMA producer: weight and activation tiles (128-byte swizzle) + their block
-//             scales (1-D bulk copies of the pre-arranged scale atoms) into a ring of stages;
+// One persistent CTA per SM walks the tile list:
+//   warp 0    TMA producer: token tile, weight tile (128-byte swizzle) and the two 1 KB scale
+//             pieces (bulk copies of pre-arranged scale atoms) into a ring of stages;
 //   warp 1    allocates tensor memory, copies each stage's scales into it (tcgen05.cp) and
-//             issues the MMAs from one thread; tcgen05.commit releases stages / publishes tiles;
-//   warps 2-5 epilogue: tcgen05.ld of the accumulators;
-//             up:   h = SiLU(g) * u, quantised to MXFP4 along I (one warp = one 32-block),
-//                   written as the down GEMM's padded activation operand;
-//             down: bf16 expert outputs y_perm in compact permuted row order.
+//             issues the MMAs from one thread; tcgen05.commit frees stages and publishes tiles;
+//   warps 2-5 epilogue, one tensor-memory lane quarter (32 token rows) each, on a ring of three
+//             accumulator buffers so that the MMAs of the next tiles overlap it.
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include <cuda.h>
@@ -30,22 +38,22 @@ namespace {
 
 constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, 4 epilogue warps
-constexpr int kTileA = 128 * 128;               // 128 rows x 128 bytes (256 FP4 values) per stage
-constexpr int kTileB = 128 * 128;
-constexpr int kSfBytes = 1024;                  // two 512-byte scale atoms = 128 rows x 8 scales
+constexpr int kTile = 128 * 128;                // 128 rows x 128 bytes (256 FP4 values)
+constexpr int kAtom = 512;                      // scale atom: 128 rows x 4 scales
+constexpr int kStages = 6;
+constexpr int kStageBytes = 2 * kTile + 4 * kAtom;  // A tile, B tile, 2 atoms of A scales, 2 of B
+constexpr int kAccBufs = 3;
+constexpr int kAccCols = 128;
+constexpr int kSfBase = kAccBufs * kAccCols;  // scale slots after the accumulators
+constexpr int kSfCols = 16;                   // per stage: A scales 8 columns, B scales 8
 constexpr uint32_t kTmemCols = 512;
+constexpr int kBarBytes = 256;
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds at GB300 clocks
+static_assert(kSfBase + kStages * kSfCols <= (int)kTmemCols, "tensor memory budget");
 
-template <bool IS_UP>
-struct Shape {
-    static constexpr int kNumA = IS_UP ? 2 : 1;
-    static constexpr int kStages = IS_UP ? 4 : 6;
-    static constexpr int kStageBytes = kNumA * kTileA + kTileB + (kNumA + 1) * kSfBytes;
-    static constexpr int kSfCols = (kNumA + 1) * 8;  // tensor-memory columns of one stage's scales
-    static constexpr int kSfBase = 256;              // accumulators use columns [0, 256)
-    static constexpr int kAccBufs = IS_UP ? 1 : 2;
-    static constexpr int kSmem = kStages * kStageBytes + 1024 /* alignment */ + 512 /* barriers */;
-};
+constexpr size_t smem_bytes(int E) {
+    return (size_t)kStages * kStageBytes + 1024 /* alignment */ + kBarBytes + (size_t)4 * (E + 1) * sizeof(int32_t);
+}
 
 // ------------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -160,74 +168,85 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 // ------------------------------------------------------------------ kernel arguments / tiles
 struct UmmaArgs {
-    const uint8_t* sfa0;   // weight scales (tensor-core layout): gate (up) or down
-    const uint8_t* sfa1;   // up-matrix scales (up only)
-    const uint8_t* sfb;    // activation scales (tensor-core layout, padded rows)
+    const uint8_t* sfa;  // token-operand scales (tensor-core layout over padded rows)
+    const uint8_t* sfb;  // weight scales: paired gate/up layout (up) or down layout
     PlanView plan;
     const int32_t* offsets;
     int E;
-    int K;        // contraction length: d (up) or I (down)
-    int M_exp;    // weight rows per expert: I (up) or d (down)
-    uint8_t* h;   // up: MXFP4 codes [pad_rows][I/2]
-    uint8_t* h_s; // up: scales, tensor-core layout
+    int K;       // contraction length: d (up) or I (down)
+    int NB;      // weight blocks per expert: I/64 (up) or d/128 (down)
+    int rows_b;  // weight rows per expert in the tensor map: I (up) or d (down)
+    int n_out;   // output row length: I (h, up) or d (y_perm, down)
+    uint8_t* h;    // up: MXFP4 codes [pad_rows][I/2]
+    uint8_t* h_s;  // up: scales, tensor-core layout
     uint16_t* y_perm;  // down: bf16 [P][d]
     int* status;
 };
 
-struct Tile {
-    int e, mb, j, n_valid, N, a_row, b_row;
+// Plan copied to shared memory once per CTA.
+struct SmemPlan {
+    int32_t* ttile_prefix;  // [E+1]
+    int32_t* counts;        // [E]
+    int32_t* pad_offsets;   // [E+1]
+    int32_t* offsets;       // [E+1]
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const UmmaArgs& a) {
-    const int MB = a.M_exp / 128;
-    int lo = 0, hi = a.E;  // last expert e with ttile_prefix[e] * MB <= t
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (a.plan.ttile_prefix[mid] * MB <= t) lo = mid; else hi = mid;
-    }
+struct Tile {
+    int e, j, p, n_valid, a_row, y_row, b_row, b_blk;
+};
+
+// Advance `e` (monotone over a CTA's tiles) to the expert owning tile t and fill in the tile.
+template <bool IS_UP>
+__device__ __forceinline__ Tile decode_tile(int t, int& e, const SmemPlan& sp, const UmmaArgs& a) {
+    while (sp.ttile_prefix[e + 1] * a.NB <= t) ++e;
     Tile T;
-    T.e = lo;
-    const int ntt = a.plan.ttile_prefix[lo + 1] - a.plan.ttile_prefix[lo];
-    const int local = t - a.plan.ttile_prefix[lo] * MB;
-    T.mb = local / ntt;
-    T.j = local % ntt;
-    T.n_valid = min(kTokTile, a.plan.counts[lo] - T.j * kTokTile);
-    T.N = (T.n_valid + 31) / 32 * 32;
-    T.a_row = lo * a.M_exp + T.mb * 128;
-    T.b_row = a.plan.pad_offsets[lo] + T.j * kTokTile;
+    T.e = e;
+    const int local = t - sp.ttile_prefix[e] * a.NB;
+    T.j = local / a.NB;
+    T.p = local % a.NB;
+    T.n_valid = min(kTokTile, sp.counts[e] - T.j * kTokTile);
+    T.a_row = sp.pad_offsets[e] + T.j * kTokTile;
+    T.y_row = sp.offsets[e] + T.j * kTokTile;
+    T.b_row = e * a.rows_b + (IS_UP ? 64 : 128) * T.p;
+    T.b_blk = e * a.NB + T.p;  // 128-row block of the (paired) weight scale layout
     return T;
 }
 
 // ------------------------------------------------------------------ the kernel
 template <bool IS_UP>
 __global__ void __launch_bounds__(kThreads, 1)
-umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-                    const __grid_constant__ CUtensorMap tmB, const UmmaArgs args) {
-    using S = Shape<IS_UP>;
+umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const UmmaArgs args) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kStages * S::kStageBytes);
-    uint64_t* empty = full + S::kStages;
-    uint64_t* acc_full = empty + S::kStages;     // [kAccBufs]
-    uint64_t* acc_empty = acc_full + 2;          // [kAccBufs]
-    uint64_t* mma_done = acc_empty + 2;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* empty = full + kStages;
+    uint64_t* acc_full = empty + kStages;       // [kAccBufs]
+    uint64_t* acc_empty = acc_full + kAccBufs;  // [kAccBufs]
+    uint64_t* mma_done = acc_empty + kAccBufs;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int32_t* plan_smem = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + kBarBytes);
+    const int E = args.E;
+    SmemPlan sp;
+    sp.ttile_prefix = plan_smem;
+    sp.counts = plan_smem + (E + 1);
+    sp.pad_offsets = plan_smem + 2 * (E + 1);
+    sp.offsets = plan_smem + 3 * (E + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    auto stage_a = [&](int s, int i) { return smem + (size_t)s * S::kStageBytes + (size_t)i * kTileA; };
-    auto stage_b = [&](int s) { return smem + (size_t)s * S::kStageBytes + S::kNumA * kTileA; };
-    auto stage_sf = [&](int s, int i) {  // i < kNumA: weight scales; i == kNumA: activation scales
-        return smem + (size_t)s * S::kStageBytes + S::kNumA * kTileA + kTileB + (size_t)i * kSfBytes;
-    };
+    auto stage_a = [&](int s) { return smem + (size_t)s * kStageBytes; };
+    auto stage_b = [&](int s) { return smem + (size_t)s * kStageBytes + kTile; };
+    auto stage_sfa = [&](int s) { return smem + (size_t)s * kStageBytes + 2 * kTile; };
+    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + 2 * kTile + 2 * kAtom; };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S::kStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], kEpiWarps);
         }
@@ -241,92 +260,94 @@ umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+
+    pdl_wait();  // the plan, offsets and token operand come from the preceding kernels
+    for (int i = threadIdx.x; i <= E; i += kThreads) {
+        sp.ttile_prefix[i] = args.plan.ttile_prefix[i];
+        sp.pad_offsets[i] = args.plan.pad_offsets[i];
+        sp.offsets[i] = args.offsets[i];
+        if (i < E) sp.counts[i] = args.plan.counts[i];
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    pdl_wait();  // the plan, offsets and activation operand come from the preceding kernels
-    const int MB = args.M_exp / 128;
-    const int n_tiles = args.plan.scalars[1] * MB;
-    const int KT = args.K / 256;  // K tiles of 256 FP4 values (128 bytes per row)
+    const int n_tiles = args.plan.scalars[1] * args.NB;
+    const int KT = args.K / 256;  // K steps of 256 FP4 values (128 bytes per row)
+    const int atoms_per_rowblk = args.K / 128;
 
     if (warp == 0) {
         // ---------------------------------------------------------- TMA producer
         if (lane == 0) {
-            int kiter = 0;
+            int kiter = 0, e = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile T = decode_tile(t, args);
-                const uint32_t bytes = S::kNumA * kTileA + T.N * 128 + (S::kNumA + 1) * kSfBytes;
-                const size_t sfa_base = ((size_t)(T.a_row / 128) * (args.K / 128)) * 512;
-                const size_t sfb_base = ((size_t)(T.b_row / 128) * (args.K / 128)) * 512;
+                const Tile T = decode_tile<IS_UP>(t, e, sp, args);
+                const uint8_t* sfa = args.sfa + ((size_t)(T.a_row / 128) * atoms_per_rowblk) * kAtom;
+                const uint8_t* sfb = args.sfb + ((size_t)T.b_blk * atoms_per_rowblk) * kAtom;
                 for (int kt = 0; kt < KT; ++kt, ++kiter) {
-                    const int s = kiter % S::kStages;
-                    const uint32_t ph = (kiter / S::kStages) & 1;
+                    const int s = kiter % kStages;
+                    const uint32_t ph = (kiter / kStages) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    tma_load_2d(stage_a(s, 0), &tmA0, &full[s], kt * 128, T.a_row);
-                    if (IS_UP) tma_load_2d(stage_a(s, 1), &tmA1, &full[s], kt * 128, T.a_row);
-                    for (int c = 0; c < T.N / 32; ++c)
-                        tma_load_2d(stage_b(s) + c * 32 * 128, &tmB, &full[s], kt * 128, T.b_row + 32 * c);
-                    bulk_load(stage_sf(s, 0), args.sfa0 + sfa_base + (size_t)kt * 1024, kSfBytes, &full[s]);
-                    if (IS_UP) bulk_load(stage_sf(s, 1), args.sfa1 + sfa_base + (size_t)kt * 1024, kSfBytes, &full[s]);
-                    bulk_load(stage_sf(s, S::kNumA), args.sfb + sfb_base + (size_t)kt * 1024, kSfBytes, &full[s]);
+                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    tma_load_2d(stage_a(s), &tmA, &full[s], kt * 128, T.a_row);
+                    if (IS_UP) {
+                        tma_load_2d(stage_b(s), &tmB0, &full[s], kt * 128, T.b_row);
+                        tma_load_2d(stage_b(s) + kTile / 2, &tmB1, &full[s], kt * 128, T.b_row);
+                    } else {
+                        tma_load_2d(stage_b(s), &tmB0, &full[s], kt * 128, T.b_row);
+                    }
+                    bulk_load(stage_sfa(s), sfa + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
+                    bulk_load(stage_sfb(s), sfb + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
                 }
             }
             if (*abort_flag) {
                 // let the copies already issued land before the CTA's shared memory is released
-                for (int q = 0; q < S::kStages && q < kiter; ++q) {
+                for (int q = 0; q < kStages && q < kiter; ++q) {
                     const int it = kiter - 1 - q;
-                    mbar_wait(&full[it % S::kStages], (it / S::kStages) & 1, abort_flag, nullptr, 100000000LL);
+                    mbar_wait(&full[it % kStages], (it / kStages) & 1, abort_flag, nullptr, 100000000LL);
                 }
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            int kiter = 0, it = 0;
+            int kiter = 0, it = 0, e = 0;
             bool ok = true;
-            const uint32_t idesc0 = 0;
-            (void)idesc0;
+            const uint32_t idesc = idesc_mxf4(128, 128);
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
-                const Tile T = decode_tile(t, args);
-                const int buf = it % S::kAccBufs;
-                const uint32_t use = it / S::kAccBufs;
+                (void)decode_tile<IS_UP>(t, e, sp, args);
+                const int buf = it % kAccBufs;
+                const uint32_t use = it / kAccBufs;
                 if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, args.status)) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem + (IS_UP ? 0u : (uint32_t)(buf * 128));
-                const uint32_t idesc = idesc_mxf4(128, T.N);
+                const uint32_t d_tmem = tmem + (uint32_t)(buf * kAccCols);
                 for (int kt = 0; kt < KT; ++kt, ++kiter) {
-                    const int s = kiter % S::kStages;
-                    const uint32_t ph = (kiter / S::kStages) & 1;
+                    const int s = kiter % kStages;
+                    const uint32_t ph = (kiter / kStages) & 1;
                     if (!mbar_wait(&full[s], ph, abort_flag, args.status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sf_col = tmem + S::kSfBase + s * S::kSfCols;
-                    for (int i = 0; i <= S::kNumA; ++i)
-                        for (int hh = 0; hh < 2; ++hh)
-                            tc_cp_sf(sf_col + i * 8 + hh * 4, desc_sf(stage_sf(s, i) + hh * 512));
-                    const uint64_t adesc0 = desc_sw128(stage_a(s, 0));
-                    const uint64_t adesc1 = IS_UP ? desc_sw128(stage_a(s, 1)) : 0;
+                    const uint32_t sf = tmem + kSfBase + s * kSfCols;
+                    tc_cp_sf(sf + 0, desc_sf(stage_sfa(s)));
+                    tc_cp_sf(sf + 4, desc_sf(stage_sfa(s) + kAtom));
+                    tc_cp_sf(sf + 8, desc_sf(stage_sfb(s)));
+                    tc_cp_sf(sf + 12, desc_sf(stage_sfb(s) + kAtom));
+                    const uint64_t adesc = desc_sw128(stage_a(s));
                     const uint64_t bdesc = desc_sw128(stage_b(s));
 #pragma unroll
-                    for (int sub = 0; sub < 4; ++sub) {
+                    for (int sub = 0; sub < 4; ++sub) {  // K = 64 per MMA
                         const uint32_t sfid = (uint32_t)(sub & 1) * 2;
                         const uint32_t id = idesc | (sfid << 29) | (sfid << 4);
                         const uint32_t col = (uint32_t)(sub >> 1) * 4;
-                        const uint32_t acc = (kt > 0 || sub > 0) ? 1u : 0u;
-                        mma_mxf4(d0, adesc0 + 2 * sub, bdesc + 2 * sub, id, sf_col + col, sf_col + S::kNumA * 8 + col,
-                                 acc);
-                        if (IS_UP)
-                            mma_mxf4(tmem + 128, adesc1 + 2 * sub, bdesc + 2 * sub, id, sf_col + 8 + col,
-                                     sf_col + S::kNumA * 8 + col, acc);
+                        mma_mxf4(d_tmem, adesc + 2 * sub, bdesc + 2 * sub, id, sf + col, sf + 8 + col,
+                                 (kt > 0 || sub > 0) ? 1u : 0u);
                     }
                     tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
                 }
@@ -341,56 +362,54 @@ umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_const
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may access
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        int it = 0;
+        const int m = 32 * q + lane;  // token row within the tile
+        int it = 0, e = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
-            const Tile T = decode_tile(t, args);
-            const int buf = it % S::kAccBufs;
-            const uint32_t use = it / S::kAccBufs;
+            const Tile T = decode_tile<IS_UP>(t, e, sp, args);
+            const int buf = it % kAccBufs;
+            const uint32_t use = it / kAccBufs;
             if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, args.status)) break;
             tc_fence_after();
-            const uint32_t acc0 = tmem + lane_base + (IS_UP ? 0u : (uint32_t)(buf * 128));
-            const int m = 32 * q + lane;  // weight row within the tile
-            for (int c0 = 0; c0 < T.n_valid; c0 += 32) {
-                uint32_t g[32];
-                tmem_ld32(acc0 + c0, g);
-                if (IS_UP) {
-                    uint32_t u[32];
-                    tmem_ld32(tmem + lane_base + 128 + c0, u);
-                    tmem_ld_wait();
-                    const int I = args.M_exp;
-                    const int blk = (T.mb * 128 + 32 * q) / 32;  // 32-block of h along I
+            const uint32_t acc = tmem + lane_base + (uint32_t)(buf * kAccCols);
+            if (IS_UP) {
+                const int I = args.n_out;
+                const size_t row = (size_t)T.a_row + m;  // every padded row is written (zeros there)
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const int n = c0 + cc;
-                        if (n >= T.n_valid) continue;  // uniform across the warp
-                        const float gv = __uint_as_float(g[cc]), uv = __uint_as_float(u[cc]);
-                        const float hv = gv / (1.f + expf(-gv)) * uv;  // SiLU(g) * u
-                        const uint32_t amax_bits = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(hv)));
-                        float inv;
-                        const uint32_t sb = mx_scale_from_amax(__uint_as_float(amax_bits), inv);
-                        const uint32_t code = e2m1_encode(hv, inv);
-                        // gather the 32 nibbles of the warp (lane l = element l of the block)
-                        uint32_t v = code | (__shfl_down_sync(0xffffffffu, code, 1) << 4);  // even lanes: a byte
-                        v = v | (__shfl_down_sync(0xffffffffu, v, 2) << 8);                 // lanes % 4 == 0
-                        v = v | (__shfl_down_sync(0xffffffffu, v, 4) << 16);                // lanes % 8 == 0
-                        const uint32_t w1 = __shfl_sync(0xffffffffu, v, 8);
-                        const uint32_t w2 = __shfl_sync(0xffffffffu, v, 16);
-                        const uint32_t w3 = __shfl_sync(0xffffffffu, v, 24);
-                        if (lane == 0) {
-                            const size_t row = (size_t)(T.b_row + n);
-                            *reinterpret_cast<uint4*>(args.h + row * (I / 2) + (size_t)blk * 16) = make_uint4(v, w1, w2, w3);
-                            args.h_s[mma_scale_offset((int64_t)row, blk, I)] = (uint8_t)sb;
-                        }
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(acc + 32 * c, g);
+                    tmem_ld32(acc + 64 + 32 * c, u);
+                    tmem_ld_wait();
+                    float hv[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+                        hv[i] = __fdividef(gv, 1.f + __expf(-gv)) * uv;  // SiLU(g) * u
                     }
-                } else {
-                    tmem_ld_wait();
-                    const int d = args.M_exp;
-                    const size_t row0 = (size_t)args.offsets[T.e] + (size_t)T.j * kTokTile;
+                    uint4 codes;
+                    const uint32_t sb = mx_block_encode(hv, codes);
+                    const int blk = 2 * T.p + c;  // 32-block of h along I
+                    *reinterpret_cast<uint4*>(args.h + row * (I / 2) + (size_t)blk * 16) = codes;
+                    args.h_s[mma_scale_offset((int64_t)row, blk, I)] = (uint8_t)sb;
+                }
+            } else {
+                const int d = args.n_out;
+                uint16_t* yrow = args.y_perm + ((size_t)T.y_row + m) * d + (size_t)T.p * 128;
 #pragma unroll
-                    for (int cc = 0; cc < 32; ++cc) {
-                        const int n = c0 + cc;
-                        if (n >= T.n_valid) continue;
-                        args.y_perm[(row0 + n) * d + T.mb * 128 + m] = f32_to_bf16_bits(__uint_as_float(g[cc]));
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(acc + 32 * c, v);
+                    tmem_ld_wait();
+                    if (m < T.n_valid) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                            pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
                     }
                 }
             }
@@ -448,12 +467,12 @@ int sm_count() {
 }
 
 template <bool IS_UP>
-cudaError_t launch_grouped(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b, const UmmaArgs& args,
+cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const UmmaArgs& args,
                            cudaStream_t st, bool pdl) {
     const void* f = (const void*)umma_grouped_kernel<IS_UP>;
-    void* kargs[] = {const_cast<CUtensorMap*>(&a0), const_cast<CUtensorMap*>(&a1), const_cast<CUtensorMap*>(&b),
+    void* kargs[] = {const_cast<CUtensorMap*>(&a), const_cast<CUtensorMap*>(&b0), const_cast<CUtensorMap*>(&b1),
                      const_cast<UmmaArgs*>(&args)};
-    return launch_kernel(f, dim3(sm_count()), dim3(kThreads), Shape<IS_UP>::kSmem, st, pdl, kargs);
+    return launch_kernel(f, dim3(sm_count()), dim3(kThreads), smem_bytes(args.E), st, pdl, kargs);
 }
 
 }  // namespace
@@ -464,23 +483,24 @@ cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan
     (void)T;
     (void)k;
     if (pad_rows == 0) return cudaSuccess;
-    alignas(64) CUtensorMap ma0, ma1, mb;
-    if (!make_map(&ma0, W->gate_q, (uint64_t)E * I, d / 2, 128) || !make_map(&ma1, W->up_q, (uint64_t)E * I, d / 2, 128) ||
-        !make_map(&mb, xa, (uint64_t)pad_rows, d / 2, 32))
+    alignas(64) CUtensorMap ma, mb0, mb1;
+    if (!make_map(&ma, xa, (uint64_t)pad_rows, d / 2, 128) || !make_map(&mb0, W->gate_q, (uint64_t)E * I, d / 2, 64) ||
+        !make_map(&mb1, W->up_q, (uint64_t)E * I, d / 2, 64))
         return cudaErrorInvalidValue;
     UmmaArgs a = {};
-    a.sfa0 = W->gate_s_mma;
-    a.sfa1 = W->up_s_mma;
-    a.sfb = xa_s;
+    a.sfa = xa_s;
+    a.sfb = W->gate_up_s_mma;
     a.plan = plan;
     a.offsets = offsets;
     a.E = E;
     a.K = d;
-    a.M_exp = I;
+    a.NB = I / 64;
+    a.rows_b = I;
+    a.n_out = I;
     a.h = h;
     a.h_s = h_s;
     a.status = status;
-    return launch_grouped<true>(ma0, ma1, mb, a, st, pdl);
+    return launch_grouped<true>(ma, mb0, mb1, a, st, pdl);
 }
 
 cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan, const int32_t* offsets, int T,
@@ -489,21 +509,22 @@ cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan
     (void)T;
     (void)k;
     if (pad_rows == 0) return cudaSuccess;
-    alignas(64) CUtensorMap ma0, mb;
-    if (!make_map(&ma0, W->down_q, (uint64_t)E * d, I / 2, 128) || !make_map(&mb, h, (uint64_t)pad_rows, I / 2, 32))
+    alignas(64) CUtensorMap ma, mb;
+    if (!make_map(&ma, h, (uint64_t)pad_rows, I / 2, 128) || !make_map(&mb, W->down_q, (uint64_t)E * d, I / 2, 128))
         return cudaErrorInvalidValue;
     UmmaArgs a = {};
-    a.sfa0 = W->down_s_mma;
-    a.sfa1 = nullptr;
-    a.sfb = h_s;
+    a.sfa = h_s;
+    a.sfb = W->down_s_mma;
     a.plan = plan;
     a.offsets = offsets;
     a.E = E;
     a.K = I;
-    a.M_exp = d;
+    a.NB = d / 128;
+    a.rows_b = d;
+    a.n_out = d;
     a.y_perm = y_perm;
     a.status = status;
-    return launch_grouped<false>(ma0, ma0, mb, a, st, pdl);
+    return launch_grouped<false>(ma, mb, mb, a, st, pdl);
 }
 
 }  // namespace moe

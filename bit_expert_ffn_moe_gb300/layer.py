@@ -40,10 +40,12 @@ class DeviceLayer:
                 B.moe_mxfp4_pack(buf, n * rows, K, q[e0:e0 + n], s[e0:e0 + n])
             del buf
             self.q[tid], self.s[tid] = q, s
-            if mma_scales and rows % 128 == 0 and K % 128 == 0:
-                sm = torch.empty(B.moe_mxfp4_mma_scale_bytes(E * rows, K), **u8)
-                B.moe_mxfp4_scales_to_mma(s, E * rows, K, sm)
-                self.s_mma[tid] = sm
+        G, U, D = IN.TENSOR_GATE, IN.TENSOR_UP, IN.TENSOR_DOWN
+        if mma_scales and I % 64 == 0 and d % 128 == 0 and I % 128 == 0:
+            self.s_mma[G] = torch.empty(B.moe_mxfp4_mma_scale_bytes(2 * E * I, d), **u8)
+            B.moe_mxfp4_scales_to_mma_paired(self.s[G], self.s[U], E * I, d, self.s_mma[G])
+            self.s_mma[D] = torch.empty(B.moe_mxfp4_mma_scale_bytes(E * d, I), **u8)
+            B.moe_mxfp4_scales_to_mma(self.s[D], E * d, I, self.s_mma[D])
         W_r, b = IN.make_router(cfg)
         if layer != 0:  # independent router per layer copy
             rng = np.random.default_rng([cfg.seed, 77, layer])
@@ -51,9 +53,8 @@ class DeviceLayer:
         self.W_r_host, self.b_host = W_r, b
         self.W_r = torch.from_numpy(W_r).to(self.device)
         self.b = torch.from_numpy(b).to(self.device)
-        G, U, D = IN.TENSOR_GATE, IN.TENSOR_UP, IN.TENSOR_DOWN
         self.weights = B.expert_weights_struct(self.q[G], self.s[G], self.q[U], self.s[U], self.q[D], self.s[D],
-                                               self.s_mma.get(G), self.s_mma.get(U), self.s_mma.get(D))
+                                               self.s_mma.get(G), self.s_mma.get(D))
 
     def weight_bytes_per_expert(self) -> int:
         cfg = self.cfg

@@ -65,9 +65,12 @@ typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1 } moe_act_fmt;
 /* Expert weights of one layer (all device pointers, canonical MXFP4 layout):
  *   gate_q/up_q [E][I][d/2], gate_s/up_s [E][I][d/32]   (gate and up: I rows of d)
  *   down_q      [E][d][I/2], down_s      [E][d][I/32]   (down: d rows of I)
- * The MXFP4 path also needs the scales re-laid out for the tensor cores with
- * moe_mxfp4_scales_to_mma (gate_s_mma/up_s_mma for [E*I] rows of K = d, down_s_mma for
- * [E*d] rows of K = I); the BF16 path ignores those three (they may be NULL). */
+ * The MXFP4 path also needs the block scales re-laid out for the tensor cores:
+ *   gate_up_s_mma  moe_mxfp4_scales_to_mma_paired(gate_s, up_s, E*I, d): the gate and up
+ *                  scales of each 64-row block side by side (the MMA computes g and u of 64
+ *                  intermediate rows in one 128-row operand);
+ *   down_s_mma     moe_mxfp4_scales_to_mma(down_s, E*d, I).
+ * The BF16 path ignores both (they may be NULL). */
 typedef struct moe_expert_weights {
     const uint8_t* gate_q;
     const uint8_t* gate_s;
@@ -75,8 +78,7 @@ typedef struct moe_expert_weights {
     const uint8_t* up_s;
     const uint8_t* down_q;
     const uint8_t* down_s;
-    const uint8_t* gate_s_mma;
-    const uint8_t* up_s_mma;
+    const uint8_t* gate_up_s_mma;
     const uint8_t* down_s_mma;
 } moe_expert_weights;
 
@@ -116,6 +118,13 @@ size_t moe_mxfp4_mma_scale_bytes(int64_t rows, int64_t K);
 /* Re-lay canonical scales s[rows][K/32] out into the tensor-core layout s_mma. */
 moe_status moe_mxfp4_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma,
                                    moe_stream_t stream);
+
+/* Paired tensor-core scale layout of two [rows][K] matrices a and b (the gate and up matrices):
+ * the layout of the [2*rows][K] matrix whose row block m (128 rows) holds rows 64m..64m+63 of a
+ * followed by rows 64m..64m+63 of b.  rows % 64 == 0, K % 128 == 0; out has
+ * moe_mxfp4_mma_scale_bytes(2*rows, K) bytes. */
+moe_status moe_mxfp4_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
+                                          uint8_t* s_mma, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- workspace */
 
