@@ -226,7 +226,7 @@ def run_gpu(args, cfg, rank, world, local):
     T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
     n_calls = max(cfg.calls, 1)
 
-    layers = [DeviceLayer(cfg, device=dev, layer=i + 1000 * rank, mma_scales=(fmt == B.MOE_ACT_MXFP4))
+    layers = [DeviceLayer(cfg, device=dev, layer=i + 1000 * rank, mma_layouts=(fmt == B.MOE_ACT_MXFP4))
               for i in range(args.layers)]
     # all seeded inputs resident in HBM before timing
     xs_host = np.stack([IN.make_x(cfg, call=(c + rank * 100000) % (1 << 20)) for c in range(min(n_calls, 1000))])

@@ -8,7 +8,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -46,8 +46,8 @@ moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     if (T < 0 || d <= 0 || E <= 0 || k <= 0 || I <= 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
     if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (d % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (I % (fmt == MOE_ACT_MXFP4 ? 128 : 32) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d % (fmt == MOE_ACT_MXFP4 ? 256 : 128) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (I % (fmt == MOE_ACT_MXFP4 ? 256 : 32) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)T * k > (int64_t)1 << 30 || (int64_t)T * d > ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
@@ -63,11 +63,15 @@ moe_status check_weights(const moe_expert_weights* W, moe_act_fmt fmt, bool need
     if (need_up) {
         if (!W->gate_q || !W->gate_s || !W->up_q || !W->up_s) return MOE_ERR_INVALID_ARG;
         if (!aligned(W->gate_q, 16) || !aligned(W->up_q, 16)) return MOE_ERR_INVALID_ARG;
-        if (fmt == MOE_ACT_MXFP4 && (!W->gate_up_s_mma || !aligned(W->gate_up_s_mma, 16))) return MOE_ERR_INVALID_ARG;
+        if (fmt == MOE_ACT_MXFP4 && (!W->gate_up_q_mma || !W->gate_up_s_mma || !aligned(W->gate_up_q_mma, 16) ||
+                                     !aligned(W->gate_up_s_mma, 16)))
+            return MOE_ERR_INVALID_ARG;
     }
     if (need_down) {
         if (!W->down_q || !W->down_s || !aligned(W->down_q, 16)) return MOE_ERR_INVALID_ARG;
-        if (fmt == MOE_ACT_MXFP4 && (!W->down_s_mma || !aligned(W->down_s_mma, 16))) return MOE_ERR_INVALID_ARG;
+        if (fmt == MOE_ACT_MXFP4 && (!W->down_q_mma || !W->down_s_mma || !aligned(W->down_q_mma, 16) ||
+                                     !aligned(W->down_s_mma, 16)))
+            return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;
 }
@@ -145,6 +149,22 @@ moe_status moe_mxfp4_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b
     return from_cuda(launch_scales_to_mma_paired(s_a, s_b, rows, K, s_mma, (cudaStream_t)stream));
 }
 
+moe_status moe_mxfp4_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma, moe_stream_t stream) {
+    if (rows <= 0 || K <= 0 || rows % 128 != 0 || K % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!q || !q_mma || !aligned(q, 16) || !aligned(q_mma, 16)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_codes_to_mma(q, nullptr, rows, K, false, q_mma, (cudaStream_t)stream));
+}
+
+moe_status moe_mxfp4_codes_to_mma_paired(const uint8_t* q_a, const uint8_t* q_b, int64_t rows, int64_t K,
+                                         uint8_t* q_mma, moe_stream_t stream) {
+    if (rows <= 0 || K <= 0 || rows % 64 != 0 || K % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!q_a || !q_b || !q_mma || !aligned(q_a, 16) || !aligned(q_b, 16) || !aligned(q_mma, 16))
+        return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_codes_to_mma(q_a, q_b, rows, K, true, q_mma, (cudaStream_t)stream));
+}
+
 // ---------------------------------------------------------------- workspace
 
 size_t moe_workspace_size(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
@@ -190,10 +210,12 @@ moe_status moe_route(const uint16_t* x, const float* W_r, const float* b, int T,
 moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int E, int k, moe_act_fmt fmt,
                        int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_pos, uint8_t* xa,
                        uint8_t* xa_s, void* ws, size_t ws_bytes, moe_stream_t stream) {
-    MOE_TRY(check_shape(T, d, E, k, 128, fmt));
+    // the buffers this call uses do not depend on I: check against the smallest valid I
+    const int I_min = fmt == MOE_ACT_MXFP4 ? 256 : 32;
+    MOE_TRY(check_shape(T, d, E, k, I_min, fmt));
     if (!ids || !counts || !offsets || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
     if (fmt == MOE_ACT_MXFP4 && (!x || !xa || !xa_s || !aligned(x, 16) || !aligned(xa, 16))) return MOE_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(T, d, E, k, 128, fmt);
+    const WsLayout L = ws_layout(T, d, E, k, I_min, fmt);
     MOE_TRY(check_ws(ws, ws_bytes, L));
     MOE_TRY(check_device());
     cudaStream_t st = (cudaStream_t)stream;

@@ -187,6 +187,15 @@ __host__ __device__ __forceinline__ size_t mma_scale_offset(int64_t row, int64_t
     return (size_t)atom * 512 + (size_t)((row % 32) * 16 + ((row / 32) % 4) * 4 + (col % 4));
 }
 
+// Byte offset of the 16-byte code chunk of (row, 32-element block blk) in the tensor-core code
+// tiles of a matrix with K values per row: tiles of 128 rows x 256 values (16384 bytes) at tile
+// index (row/128)*(K/256) + blk/8, chunk blk%8 of row r stored at r*128 + ((blk%8) ^ (r%8))*16.
+__host__ __device__ __forceinline__ size_t mma_tile_offset(int64_t row, int64_t blk, int64_t K) {
+    const int64_t tile = (row / 128) * (K / 256) + blk / 8;
+    const int64_t r = row % 128;
+    return (size_t)tile * 16384 + (size_t)(r * 128 + (((blk % 8) ^ (r % 8)) * 16));
+}
+
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -218,6 +227,8 @@ cudaError_t launch_synth(uint64_t seed, uint32_t tensor_id, uint32_t expert_firs
 cudaError_t launch_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w, cudaStream_t st);
 cudaError_t launch_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma, cudaStream_t st);
+cudaError_t launch_codes_to_mma(const uint8_t* q_a, const uint8_t* q_b, int64_t rows, int64_t K, bool paired,
+                                uint8_t* q_mma, cudaStream_t st);
 cudaError_t launch_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
                                        uint8_t* s_mma, cudaStream_t st);
 

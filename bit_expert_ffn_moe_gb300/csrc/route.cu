@@ -452,7 +452,7 @@ __global__ void act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t*
             v = reinterpret_cast<const uint4*>(xq)[(size_t)t * nb + blk];
             sb = xs[(size_t)t * nb + blk];
         }
-        reinterpret_cast<uint4*>(xa)[(size_t)r * nb + blk] = v;
+        *reinterpret_cast<uint4*>(xa + mma_tile_offset(r, blk, d)) = v;
         xa_s[mma_scale_offset(r, blk, d)] = sb;
     }
     (void)pad_rows;

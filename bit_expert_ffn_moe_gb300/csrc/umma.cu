@@ -12,25 +12,26 @@
 // row and one tcgen05.ld of 32 columns hands it a whole 32-element block of the output: the
 // SwiGLU result is requantised to MXFP4 with no cross-lane traffic, and y rows are written as
 // contiguous 64-byte pieces.
-//   up:   B = 64 gate rows followed by the same 64 up rows (two TMA boxes), so D holds g in
-//         columns 0..63 and u in columns 64..127 of 64 consecutive intermediate rows; the block
-//         scales of the pair come pre-arranged side by side (paired tensor-core layout).
+//   up:   B = 64 gate rows followed by the same 64 up rows (paired tensor-core layouts), so D
+//         holds g in columns 0..63 and u in columns 64..127 of 64 consecutive intermediate rows.
 //   down: B = 128 rows of W_down (128 output features).
 // Tiles are (expert e, token tile j, weight block p) with p fastest: CTAs that run at the same
 // time share a token tile through L2 and walk the expert's weight blocks, each of which stays in
 // L2 while the expert's other token tiles use it.
 //
 // One persistent CTA per SM walks the tile list:
-//   warp 0    TMA producer: token tile, weight tile (128-byte swizzle) and the two 1 KB scale
-//             pieces (bulk copies of pre-arranged scale atoms) into a ring of stages;
+//   warp 0    producer: per K step, four bulk copies (the copy engine) into a ring of stages --
+//             the 16 KB token tile, the 16 KB weight tile and their two 1 KB scale pieces.  All
+//             operands are stored pre-arranged in the tensor-core layouts (code tiles already
+//             in the 128-byte swizzle, scale atoms), so every piece is one contiguous copy; on
+//             GB300 these run markedly faster than 2-D tensor boxes of 128-byte rows, from L2 as
+//             well as from HBM;
 //   warp 1    allocates tensor memory, copies each stage's scales into it (tcgen05.cp) and
 //             issues the MMAs from one thread; tcgen05.commit frees stages and publishes tiles;
 //   warps 2-5 epilogue, one tensor-memory lane quarter (32 token rows) each, on a ring of three
 //             accumulator buffers so that the MMAs of the next tiles overlap it.
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
-#include <cuda.h>
-
 #include "common.cuh"
 
 namespace moe {
@@ -97,14 +98,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -149,7 +142,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
@@ -168,16 +160,17 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 // ------------------------------------------------------------------ kernel arguments / tiles
 struct UmmaArgs {
+    const uint8_t* qa;   // token-operand code tiles (padded rows)
     const uint8_t* sfa;  // token-operand scales (tensor-core layout over padded rows)
+    const uint8_t* qb;   // weight code tiles: paired gate/up (up) or down
     const uint8_t* sfb;  // weight scales: paired gate/up layout (up) or down layout
     PlanView plan;
     const int32_t* offsets;
     int E;
     int K;       // contraction length: d (up) or I (down)
     int NB;      // weight blocks per expert: I/64 (up) or d/128 (down)
-    int rows_b;  // weight rows per expert in the tensor map: I (up) or d (down)
     int n_out;   // output row length: I (h, up) or d (y_perm, down)
-    uint8_t* h;    // up: MXFP4 codes [pad_rows][I/2]
+    uint8_t* h;    // up: MXFP4 code tiles of [pad_rows][I]
     uint8_t* h_s;  // up: scales, tensor-core layout
     uint16_t* y_perm;  // down: bf16 [P][d]
     int* status;
@@ -192,7 +185,7 @@ struct SmemPlan {
 };
 
 struct Tile {
-    int e, j, p, n_valid, a_row, y_row, b_row, b_blk;
+    int e, j, p, n_valid, a_row, y_row, b_blk;
 };
 
 // Advance `e` (monotone over a CTA's tiles) to the expert owning tile t and fill in the tile.
@@ -207,16 +200,13 @@ __device__ __forceinline__ Tile decode_tile(int t, int& e, const SmemPlan& sp, c
     T.n_valid = min(kTokTile, sp.counts[e] - T.j * kTokTile);
     T.a_row = sp.pad_offsets[e] + T.j * kTokTile;
     T.y_row = sp.offsets[e] + T.j * kTokTile;
-    T.b_row = e * a.rows_b + (IS_UP ? 64 : 128) * T.p;
-    T.b_blk = e * a.NB + T.p;  // 128-row block of the (paired) weight scale layout
+    T.b_blk = e * a.NB + T.p;  // 128-row block of the (paired) weight layouts
     return T;
 }
 
 // ------------------------------------------------------------------ the kernel
 template <bool IS_UP>
-__global__ void __launch_bounds__(kThreads, 1)
-umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const UmmaArgs args) {
+__global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArgs args) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -278,12 +268,14 @@ umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int atoms_per_rowblk = args.K / 128;
 
     if (warp == 0) {
-        // ---------------------------------------------------------- TMA producer
+        // ---------------------------------------------------------- copy producer
         if (lane == 0) {
             int kiter = 0, e = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const Tile T = decode_tile<IS_UP>(t, e, sp, args);
+                const uint8_t* qa = args.qa + (size_t)(T.a_row / 128) * KT * kTile;
+                const uint8_t* qb = args.qb + (size_t)T.b_blk * KT * kTile;
                 const uint8_t* sfa = args.sfa + ((size_t)(T.a_row / 128) * atoms_per_rowblk) * kAtom;
                 const uint8_t* sfb = args.sfb + ((size_t)T.b_blk * atoms_per_rowblk) * kAtom;
                 for (int kt = 0; kt < KT; ++kt, ++kiter) {
@@ -294,33 +286,29 @@ umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         break;
                     }
                     mbar_arrive_expect_tx(&full[s], kStageBytes);
-                    tma_load_2d(stage_a(s), &tmA, &full[s], kt * 128, T.a_row);
-                    if (IS_UP) {
-                        tma_load_2d(stage_b(s), &tmB0, &full[s], kt * 128, T.b_row);
-                        tma_load_2d(stage_b(s) + kTile / 2, &tmB1, &full[s], kt * 128, T.b_row);
-                    } else {
-                        tma_load_2d(stage_b(s), &tmB0, &full[s], kt * 128, T.b_row);
-                    }
+                    bulk_load(stage_a(s), qa + (size_t)kt * kTile, kTile, &full[s]);
+                    bulk_load(stage_b(s), qb + (size_t)kt * kTile, kTile, &full[s]);
                     bulk_load(stage_sfa(s), sfa + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
                     bulk_load(stage_sfb(s), sfb + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
                 }
             }
             if (*abort_flag) {
                 // let the copies already issued land before the CTA's shared memory is released
+                // (bounded waits that the abort flag does not cut short)
+                volatile int never = 0;
                 for (int q = 0; q < kStages && q < kiter; ++q) {
                     const int it = kiter - 1 - q;
-                    mbar_wait(&full[it % kStages], (it / kStages) & 1, abort_flag, nullptr, 100000000LL);
+                    mbar_wait(&full[it % kStages], (it / kStages) & 1, &never, nullptr, 100000000LL);
                 }
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
-            int kiter = 0, it = 0, e = 0;
+            int kiter = 0, it = 0;
             bool ok = true;
             const uint32_t idesc = idesc_mxf4(128, 128);
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
-                (void)decode_tile<IS_UP>(t, e, sp, args);
                 const int buf = it % kAccBufs;
                 const uint32_t use = it / kAccBufs;
                 if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, args.status)) break;
@@ -356,7 +344,8 @@ umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             // all MMAs and scale copies issued by this thread have completed once this fires
             tc_commit(mma_done);
-            mbar_wait(mma_done, 0, abort_flag, nullptr, 100000000LL);
+            volatile int never = 0;  // wait even when aborting: tensor memory is freed next
+            mbar_wait(mma_done, 0, &never, nullptr, 100000000LL);
         }
     } else {
         // ---------------------------------------------------------- epilogue
@@ -389,7 +378,7 @@ umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     uint4 codes;
                     const uint32_t sb = mx_block_encode(hv, codes);
                     const int blk = 2 * T.p + c;  // 32-block of h along I
-                    *reinterpret_cast<uint4*>(args.h + row * (I / 2) + (size_t)blk * 16) = codes;
+                    *reinterpret_cast<uint4*>(args.h + mma_tile_offset((int64_t)row, blk, I)) = codes;
                     args.h_s[mma_scale_offset((int64_t)row, blk, I)] = (uint8_t)sb;
                 }
             } else {
@@ -429,36 +418,6 @@ umma_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }
 
 // ------------------------------------------------------------------ host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-// 2-D byte tensor [rows][row_bytes], box 128 bytes x box_rows, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t row_bytes, uint32_t box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc || rows == 0) return false;
-    const cuuint64_t dims[2] = {row_bytes, rows};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {128, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int sm_count() {
     int dev = 0, n = 0;
     cudaGetDevice(&dev);
@@ -467,11 +426,9 @@ int sm_count() {
 }
 
 template <bool IS_UP>
-cudaError_t launch_grouped(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const UmmaArgs& args,
-                           cudaStream_t st, bool pdl) {
+cudaError_t launch_grouped(const UmmaArgs& args, cudaStream_t st, bool pdl) {
     const void* f = (const void*)umma_grouped_kernel<IS_UP>;
-    void* kargs[] = {const_cast<CUtensorMap*>(&a), const_cast<CUtensorMap*>(&b0), const_cast<CUtensorMap*>(&b1),
-                     const_cast<UmmaArgs*>(&args)};
+    void* kargs[] = {const_cast<UmmaArgs*>(&args)};
     return launch_kernel(f, dim3(sm_count()), dim3(kThreads), smem_bytes(args.E), st, pdl, kargs);
 }
 
@@ -483,24 +440,21 @@ cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan
     (void)T;
     (void)k;
     if (pad_rows == 0) return cudaSuccess;
-    alignas(64) CUtensorMap ma, mb0, mb1;
-    if (!make_map(&ma, xa, (uint64_t)pad_rows, d / 2, 128) || !make_map(&mb0, W->gate_q, (uint64_t)E * I, d / 2, 64) ||
-        !make_map(&mb1, W->up_q, (uint64_t)E * I, d / 2, 64))
-        return cudaErrorInvalidValue;
     UmmaArgs a = {};
+    a.qa = xa;
     a.sfa = xa_s;
+    a.qb = W->gate_up_q_mma;
     a.sfb = W->gate_up_s_mma;
     a.plan = plan;
     a.offsets = offsets;
     a.E = E;
     a.K = d;
     a.NB = I / 64;
-    a.rows_b = I;
     a.n_out = I;
     a.h = h;
     a.h_s = h_s;
     a.status = status;
-    return launch_grouped<true>(ma, mb0, mb1, a, st, pdl);
+    return launch_grouped<true>(a, st, pdl);
 }
 
 cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan, const int32_t* offsets, int T,
@@ -509,22 +463,20 @@ cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan
     (void)T;
     (void)k;
     if (pad_rows == 0) return cudaSuccess;
-    alignas(64) CUtensorMap ma, mb;
-    if (!make_map(&ma, h, (uint64_t)pad_rows, I / 2, 128) || !make_map(&mb, W->down_q, (uint64_t)E * d, I / 2, 128))
-        return cudaErrorInvalidValue;
     UmmaArgs a = {};
+    a.qa = h;
     a.sfa = h_s;
+    a.qb = W->down_q_mma;
     a.sfb = W->down_s_mma;
     a.plan = plan;
     a.offsets = offsets;
     a.E = E;
     a.K = I;
     a.NB = d / 128;
-    a.rows_b = d;
     a.n_out = d;
     a.y_perm = y_perm;
     a.status = status;
-    return launch_grouped<false>(ma, mb, mb, a, st, pdl);
+    return launch_grouped<false>(a, st, pdl);
 }
 
 }  // namespace moe

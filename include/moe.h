@@ -26,7 +26,8 @@
  *     MOE_ERR_TIMEOUT in the workspace and return; moe_get_device_status reads that word.
  *   - Inputs are assumed finite.
  *   - Shape rules (MOE_ERR_UNSUPPORTED_SHAPE otherwise): 1 <= k <= min(E, 32); E <= 1024;
- *     d % 128 == 0; I % 32 == 0 (MOE_ACT_BF16) or I % 128 == 0 (MOE_ACT_MXFP4); T >= 0.
+ *     T >= 0; MOE_ACT_BF16: d % 128 == 0 and I % 32 == 0; MOE_ACT_MXFP4: d % 256 == 0 and
+ *     I % 256 == 0 (whole 256-value MMA tiles along both contractions).
  *
  * MXFP4 tensor layout ("canonical"): a [rows][K] matrix is stored as codes q[rows][K/2]
  * (element 2i in the low nibble of byte i, element 2i+1 in the high nibble; bit 3 of a code
@@ -65,12 +66,14 @@ typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1 } moe_act_fmt;
 /* Expert weights of one layer (all device pointers, canonical MXFP4 layout):
  *   gate_q/up_q [E][I][d/2], gate_s/up_s [E][I][d/32]   (gate and up: I rows of d)
  *   down_q      [E][d][I/2], down_s      [E][d][I/32]   (down: d rows of I)
- * The MXFP4 path also needs the block scales re-laid out for the tensor cores:
- *   gate_up_s_mma  moe_mxfp4_scales_to_mma_paired(gate_s, up_s, E*I, d): the gate and up
- *                  scales of each 64-row block side by side (the MMA computes g and u of 64
- *                  intermediate rows in one 128-row operand);
- *   down_s_mma     moe_mxfp4_scales_to_mma(down_s, E*d, I).
- * The BF16 path ignores both (they may be NULL). */
+ * The MXFP4 path reads copies re-laid out for the tensor cores (see "tensor-core layouts"):
+ *   gate_up_q_mma  moe_mxfp4_codes_to_mma_paired(gate_q, up_q, E*I, d)
+ *   gate_up_s_mma  moe_mxfp4_scales_to_mma_paired(gate_s, up_s, E*I, d)
+ *                  (the gate and up rows of each 64-row block side by side: the MMA computes g
+ *                  and u of 64 intermediate rows in one 128-row operand)
+ *   down_q_mma     moe_mxfp4_codes_to_mma(down_q, E*d, I)
+ *   down_s_mma     moe_mxfp4_scales_to_mma(down_s, E*d, I)
+ * The BF16 path reads only the canonical tensors (the four copies may be NULL). */
 typedef struct moe_expert_weights {
     const uint8_t* gate_q;
     const uint8_t* gate_s;
@@ -78,7 +81,9 @@ typedef struct moe_expert_weights {
     const uint8_t* up_s;
     const uint8_t* down_q;
     const uint8_t* down_s;
+    const uint8_t* gate_up_q_mma;
     const uint8_t* gate_up_s_mma;
+    const uint8_t* down_q_mma;
     const uint8_t* down_s_mma;
 } moe_expert_weights;
 
@@ -109,22 +114,42 @@ moe_status moe_mxfp4_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, u
 moe_status moe_mxfp4_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w,
                             moe_stream_t stream);
 
-/* Bytes of the tensor-core scale layout of a [rows][K] MXFP4 matrix (rows % 128 == 0,
- * K % 128 == 0; 0 otherwise).  The layout is a grid of 512-byte atoms, atom (R, C) =
- * rows 128R..128R+127 x scale columns 4C..4C+3 stored at atom index R*(K/128) + C; inside an
- * atom, row r and scale column c sit at byte (r%32)*16 + ((r/32)%4)*4 + (c%4). */
+/* Tensor-core layouts of a [rows][K] MXFP4 matrix (rows % 128 == 0, K % 256 == 0), read by the
+ * block-scaled MMA path with one contiguous copy per operand tile:
+ *   codes   tiles of 128 rows x 256 values (16384 bytes); tile (R, C) = rows 128R..128R+127 x
+ *           values 256C..256C+255 sits at tile index R*(K/256) + C.  Inside a tile, the 16-byte
+ *           chunk j (values 256C+32j..+31, one 32-element block) of row r is stored at byte
+ *           r*128 + (j XOR (r%8))*16 (the 128-byte swizzle the tensor cores read).  Same size
+ *           as the canonical codes.
+ *   scales  a grid of 512-byte atoms, atom (R, C) = rows 128R..128R+127 x scale columns
+ *           4C..4C+3 at atom index R*(K/128) + C; inside an atom, row r and scale column c sit
+ *           at byte (r%32)*16 + ((r/32)%4)*4 + (c%4).
+ * Paired forms of two matrices a and b (the gate and up matrices, rows % 64 == 0): the layout of
+ * the [2*rows][K] matrix whose 128-row block m holds rows 64m..64m+63 of a followed by rows
+ * 64m..64m+63 of b. */
+
+/* Bytes of the tensor-core scale layout of a [rows][K] matrix (rows % 128 == 0, K % 128 == 0;
+ * 0 otherwise). */
 size_t moe_mxfp4_mma_scale_bytes(int64_t rows, int64_t K);
 
-/* Re-lay canonical scales s[rows][K/32] out into the tensor-core layout s_mma. */
+/* Re-lay canonical scales s[rows][K/32] out into the tensor-core scale layout s_mma. */
 moe_status moe_mxfp4_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma,
                                    moe_stream_t stream);
 
-/* Paired tensor-core scale layout of two [rows][K] matrices a and b (the gate and up matrices):
- * the layout of the [2*rows][K] matrix whose row block m (128 rows) holds rows 64m..64m+63 of a
- * followed by rows 64m..64m+63 of b.  rows % 64 == 0, K % 128 == 0; out has
- * moe_mxfp4_mma_scale_bytes(2*rows, K) bytes. */
+/* Paired tensor-core scale layout of s_a and s_b ([rows][K/32] each; rows % 64 == 0,
+ * K % 128 == 0); s_mma has moe_mxfp4_mma_scale_bytes(2*rows, K) bytes. */
 moe_status moe_mxfp4_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
                                           uint8_t* s_mma, moe_stream_t stream);
+
+/* Re-lay canonical codes q[rows][K/2] out into the tensor-core code tiles q_mma (rows*K/2 bytes;
+ * rows % 128 == 0, K % 256 == 0). */
+moe_status moe_mxfp4_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma,
+                                  moe_stream_t stream);
+
+/* Paired code tiles of q_a and q_b ([rows][K/2] each; rows % 64 == 0, K % 256 == 0); q_mma has
+ * rows*K bytes. */
+moe_status moe_mxfp4_codes_to_mma_paired(const uint8_t* q_a, const uint8_t* q_b, int64_t rows, int64_t K,
+                                         uint8_t* q_mma, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- workspace */
 
@@ -178,9 +203,10 @@ moe_status moe_route_noalloc(const uint16_t* x, const float* W_r, const float* b
  *   perm_token[P]  token of permuted row r (P = T*k)
  *   inv_pos[P]     permuted row of pair (t, j) at index t*k + j
  * For MOE_ACT_MXFP4 it also quantises every token row of x once and writes the activation
- * operand in padded expert-grouped order: xa[moe_padded_rows][d/2] codes and xa_s in the
- * tensor-core scale layout (moe_mxfp4_mma_scale_bytes(moe_padded_rows, d) bytes); expert e's
- * rows start at a multiple of 128, padding rows are zero.  For MOE_ACT_BF16, xa and xa_s are
+ * operand of the [moe_padded_rows][d] matrix of permuted rows in padded expert-grouped order
+ * (expert e's rows start at a multiple of 128; padding rows are zero): xa in the tensor-core
+ * code tiles (moe_padded_rows*d/2 bytes) and xa_s in the tensor-core scale layout
+ * (moe_mxfp4_mma_scale_bytes(moe_padded_rows, d) bytes).  For MOE_ACT_BF16, xa and xa_s are
  * unused (may be NULL).  Writes the per-expert plan (padded offsets, tile table) into ws for
  * the expert calls that follow. */
 moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int E, int k, moe_act_fmt fmt,
@@ -191,8 +217,9 @@ moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int 
  * for every permuted row, grouped by expert.  Needs the plan that moe_permute wrote into ws.
  *   MOE_ACT_BF16:  reads x bf16 [T][d] through perm_token; writes h bf16 [P][I] (row r =
  *                  permuted row r), h_s unused.
- *   MOE_ACT_MXFP4: reads xa / xa_s; writes h as MXFP4 codes [moe_padded_rows][I/2] in padded
- *                  order and h_s in the tensor-core scale layout. */
+ *   MOE_ACT_MXFP4: reads xa / xa_s; writes the [moe_padded_rows][I] matrix h in the same padded
+ *                  order as MXFP4: codes in the tensor-core code tiles (moe_padded_rows*I/2
+ *                  bytes), scales in the tensor-core scale layout (padding rows are zero). */
 moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint8_t* xa_s, moe_act_fmt fmt,
                                 const int32_t* perm_token, const int32_t* offsets, int T, int d, int E, int k,
                                 int I, const moe_expert_weights* W, void* h, uint8_t* h_s, void* ws,

@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 2
+    assert B.moe_abi_version() == 3
     assert B.status_string(0) == "MOE_OK"
     assert B.status_string(5) == "MOE_ERR_TIMEOUT"
 
@@ -49,7 +49,10 @@ def test_size_helpers():
     assert B.moe_workspace_size(16, 200, 8, 2, 512, 0) == 0      # d % 128
     assert B.moe_workspace_size(16, 256, 8, 9, 512, 0) == 0      # k > E
     assert B.moe_workspace_size(16, 256, 2048, 2, 512, 0) == 0   # E > 1024
-    assert B.moe_workspace_size(16, 256, 8, 2, 96, B.MOE_ACT_MXFP4) == 0  # I % 128 on the MXFP4 path
+    assert B.moe_workspace_size(16, 256, 8, 2, 96, B.MOE_ACT_MXFP4) == 0  # I % 256 on the MXFP4 path
+    assert B.moe_workspace_size(16, 256, 8, 2, 384, B.MOE_ACT_MXFP4) == 0
+    assert B.moe_workspace_size(16, 384, 8, 2, 512, B.MOE_ACT_MXFP4) == 0  # d % 256 on the MXFP4 path
+    assert B.moe_workspace_size(16, 384, 8, 2, 384, B.MOE_ACT_BF16) > 0
 
 
 def test_library_is_built_for_sm103a_only():

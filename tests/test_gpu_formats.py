@@ -93,3 +93,38 @@ def test_scales_to_mma_paired_layout():
             atom = (r // 128) * (K // 128) + c // 4
             ref[atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + c % 4] = virt[r, c]
     np.testing.assert_array_equal(got, ref)
+
+
+def _tiles_reference(virt_codes, K):
+    """Documented code tiles of a [rows][K/2] code matrix: tile (R, C) at index R*(K/256) + C,
+    16-byte chunk j of row r inside it at r*128 + (j ^ (r % 8))*16."""
+    rows = virt_codes.shape[0]
+    out = np.empty(rows * K // 2, dtype=np.uint8)
+    for r in range(rows):
+        for b in range(K // 32):
+            tile = (r // 128) * (K // 256) + b // 8
+            off = tile * 16384 + (r % 128) * 128 + ((b % 8) ^ (r % 8)) * 16
+            out[off:off + 16] = virt_codes[r, 16 * b:16 * b + 16]
+    return out
+
+
+def test_codes_to_mma_tiles():
+    rows, K = 256, 512
+    q = np.random.default_rng(5).integers(0, 256, size=(rows, K // 2)).astype(np.uint8)
+    out = torch.empty(rows * K // 2, dtype=torch.uint8, device="cuda")
+    B.moe_mxfp4_codes_to_mma(torch.from_numpy(q).cuda(), rows, K, out)
+    np.testing.assert_array_equal(out.cpu().numpy(), _tiles_reference(q, K))
+
+
+def test_codes_to_mma_tiles_paired():
+    rows, K = 192, 768
+    rng = np.random.default_rng(6)
+    qa = rng.integers(0, 256, size=(rows, K // 2)).astype(np.uint8)
+    qb = rng.integers(0, 256, size=(rows, K // 2)).astype(np.uint8)
+    out = torch.empty(rows * K, dtype=torch.uint8, device="cuda")
+    B.moe_mxfp4_codes_to_mma_paired(torch.from_numpy(qa).cuda(), torch.from_numpy(qb).cuda(), rows, K, out)
+    virt = np.empty((2 * rows, K // 2), dtype=np.uint8)
+    for m in range(rows // 64):
+        virt[128 * m:128 * m + 64] = qa[64 * m:64 * m + 64]
+        virt[128 * m + 64:128 * m + 128] = qb[64 * m:64 * m + 64]
+    np.testing.assert_array_equal(out.cpu().numpy(), _tiles_reference(virt, K))

@@ -32,6 +32,15 @@ def unpad(padded, pad_offsets, counts, offsets):
     return np.concatenate(out, axis=0)
 
 
+def mma_tiles_to_rows(buf, rows, K):
+    """Inverse of the documented tensor-core code tiles: [rows][K/2] canonical codes."""
+    r = np.arange(rows)[:, None]
+    b = np.arange(K // 32)[None, :]
+    off = ((r // 128) * (K // 256) + b // 8) * 16384 + (r % 128) * 128 + (((b % 8) ^ (r % 8)) * 16)
+    idx = off[:, :, None] + np.arange(16)[None, None, :]
+    return buf.reshape(-1)[idx].reshape(rows, K // 2)
+
+
 def mma_scales_to_rows(buf, rows, K):
     """Inverse of the documented tensor-core scale layout: [rows][K/32]."""
     r = np.arange(rows)[:, None]
@@ -83,7 +92,7 @@ def test_step_calls_tiny_against_oracle_intermediates():
     np.testing.assert_array_equal(g["perm"], ref["perm_token"])
     # activation operand: every permuted row is its token's quantised row, bit for bit
     _, xq, xs = O.activation_rows(xb, O.ACT_MXFP4, want_codes=True)
-    xa_rows = unpad(g["xa"], g["pad"], g["counts"], g["offsets"])
+    xa_rows = unpad(mma_tiles_to_rows(g["xa"], g["R"], cfg.d), g["pad"], g["counts"], g["offsets"])
     xs_rows = unpad(mma_scales_to_rows(g["xa_s"], g["R"], cfg.d), g["pad"], g["counts"], g["offsets"])
     np.testing.assert_array_equal(xa_rows, xq[g["perm"]])
     np.testing.assert_array_equal(xs_rows, xs[g["perm"]])
@@ -91,11 +100,11 @@ def test_step_calls_tiny_against_oracle_intermediates():
     used = np.zeros(g["R"], bool)
     for e in range(cfg.E):
         used[g["pad"][e]:g["pad"][e] + g["counts"][e]] = True
-    assert not g["xa"][~used[:g["xa"].shape[0]]].any()
+    assert not mma_tiles_to_rows(g["xa"], g["R"], cfg.d)[~used].any()
     # h: dequantised values against the oracle's h (its quantisation decisions are taken in fp32
     # on both sides, so only values within fp32 rounding of a rounding boundary may differ)
     T, k, I = cfg.T, cfg.k, cfg.I
-    h_rows = unpad(g["h"], g["pad"], g["counts"], g["offsets"])
+    h_rows = unpad(mma_tiles_to_rows(g["h"], g["R"], I), g["pad"], g["counts"], g["offsets"])
     hs_rows = unpad(mma_scales_to_rows(g["h_s"], g["R"], I), g["pad"], g["counts"], g["offsets"])
     from test_oracle_pins import np_unpack
     h_gpu = np_unpack(h_rows, hs_rows)
