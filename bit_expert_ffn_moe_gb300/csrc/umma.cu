@@ -98,6 +98,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// mbar_wait by every lane of a warp with a warp-uniform verdict.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                               long long limit = kWaitCycles) {
+    const bool ok = mbar_wait(bar, parity, abort_flag, status, limit);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -127,23 +134,35 @@ __device__ __forceinline__ uint32_t idesc_mxf4(int M, int N) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The MMA warp runs its loop with all 32 lanes (warp-uniform control flow, so every operand is
+// warp-uniform) and each tcgen05 instruction is issued by one lane chosen by elect.sync inside
+// the instruction's own asm block.
 __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
             d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
         : "memory");
 }
 
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
+        : "memory");
 }
 __device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+        "l"(sdesc)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -303,50 +322,48 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            int kiter = 0, it = 0;
-            bool ok = true;
-            const uint32_t idesc = idesc_mxf4(128, 128);
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
-                const int buf = it % kAccBufs;
-                const uint32_t use = it / kAccBufs;
-                if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort_flag, args.status)) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + (uint32_t)(buf * kAccCols);
-                for (int kt = 0; kt < KT; ++kt, ++kiter) {
-                    const int s = kiter % kStages;
-                    const uint32_t ph = (kiter / kStages) & 1;
-                    if (!mbar_wait(&full[s], ph, abort_flag, args.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sf = tmem + kSfBase + s * kSfCols;
-                    tc_cp_sf(sf + 0, desc_sf(stage_sfa(s)));
-                    tc_cp_sf(sf + 4, desc_sf(stage_sfa(s) + kAtom));
-                    tc_cp_sf(sf + 8, desc_sf(stage_sfb(s)));
-                    tc_cp_sf(sf + 12, desc_sf(stage_sfb(s) + kAtom));
-                    const uint64_t adesc = desc_sw128(stage_a(s));
-                    const uint64_t bdesc = desc_sw128(stage_b(s));
-#pragma unroll
-                    for (int sub = 0; sub < 4; ++sub) {  // K = 64 per MMA
-                        const uint32_t sfid = (uint32_t)(sub & 1) * 2;
-                        const uint32_t id = idesc | (sfid << 29) | (sfid << 4);
-                        const uint32_t col = (uint32_t)(sub >> 1) * 4;
-                        mma_mxf4(d_tmem, adesc + 2 * sub, bdesc + 2 * sub, id, sf + col, sf + 8 + col,
-                                 (kt > 0 || sub > 0) ? 1u : 0u);
-                    }
-                    tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+        // ---------------------------------------------------------- MMA issuer (whole warp)
+        int kiter = 0, it = 0;
+        bool ok = true;
+        const uint32_t idesc = idesc_mxf4(128, 128);
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
+            const int buf = it % kAccBufs;
+            const uint32_t use = it / kAccBufs;
+            if (!mbar_wait_warp(&acc_empty[buf], (use & 1) ^ 1, abort_flag, args.status)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + (uint32_t)(buf * kAccCols);
+            for (int kt = 0; kt < KT; ++kt, ++kiter) {
+                const int s = kiter % kStages;
+                const uint32_t ph = (kiter / kStages) & 1;
+                if (!mbar_wait_warp(&full[s], ph, abort_flag, args.status)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
-                tc_commit(&acc_full[buf]);
+                tc_fence_after();
+                const uint32_t sf = tmem + kSfBase + s * kSfCols;
+                tc_cp_sf(sf + 0, desc_sf(stage_sfa(s)));
+                tc_cp_sf(sf + 4, desc_sf(stage_sfa(s) + kAtom));
+                tc_cp_sf(sf + 8, desc_sf(stage_sfb(s)));
+                tc_cp_sf(sf + 12, desc_sf(stage_sfb(s) + kAtom));
+                const uint64_t adesc = desc_sw128(stage_a(s));
+                const uint64_t bdesc = desc_sw128(stage_b(s));
+#pragma unroll
+                for (int sub = 0; sub < 4; ++sub) {  // K = 64 per MMA
+                    const uint32_t sfid = (uint32_t)(sub & 1) * 2;
+                    const uint32_t id = idesc | (sfid << 29) | (sfid << 4);
+                    const uint32_t col = (uint32_t)(sub >> 1) * 4;
+                    mma_mxf4(d_tmem, adesc + 2 * sub, bdesc + 2 * sub, id, sf + col, sf + 8 + col,
+                             (kt > 0 || sub > 0) ? 1u : 0u);
+                }
+                tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
             }
-            // all MMAs and scale copies issued by this thread have completed once this fires
-            tc_commit(mma_done);
-            volatile int never = 0;  // wait even when aborting: tensor memory is freed next
-            mbar_wait(mma_done, 0, &never, nullptr, 100000000LL);
+            if (!ok) break;
+            tc_commit(&acc_full[buf]);
         }
+        // all MMAs and scale copies issued by this warp have completed once this fires
+        tc_commit(mma_done);
+        volatile int never = 0;  // wait even when aborting: tensor memory is freed next
+        mbar_wait_warp(mma_done, 0, &never, nullptr, 100000000LL);
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;  // tensor-memory lane quarter this warp may access
