@@ -98,6 +98,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// One K step of 256 values: the four scale-atom copies of the stage into tensor memory, then the
+// four K = 64 MMAs and the commit that frees the stage, each group issued by one elected lane.
+__device__ __forceinline__ void stage_scales_to_tmem(uint32_t sf, uint64_t da0, uint64_t da1, uint64_t db0,
+                                                     uint64_t db1) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%2], %3;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%6], %7;\n\t}" ::"r"(sf),
+        "l"(da0), "r"(sf + 4), "l"(da1), "r"(sf + 8), "l"(db0), "r"(sf + 12), "l"(db1)
+        : "memory");
+}
+
+// MMAs of one stage: sub-steps 0..3 use A/B descriptors advanced by 32 bytes each, scale bytes
+// (sub & 1) * 2 of tensor-memory column (sub >> 1) * 4 (A at sf, B at sf + 8).
+__device__ __forceinline__ void stage_mmas_commit(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id0, uint32_t id2,
+                                                  uint32_t sf, uint32_t accumulate, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, q;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "setp.eq.b32 q, %5, %5;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%6], [%7], p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %8, %9, %4, [%6], [%7], q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %10, %11, %3, [%12], [%13], q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %14, %15, %4, [%12], [%13], q;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%16];\n\t}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(id0), "r"(id2), "r"(accumulate), "r"(sf), "r"(sf + 8), "l"(ad + 2), "l"(bd + 2),
+        "l"(ad + 4), "l"(bd + 4), "r"(sf + 4), "r"(sf + 12), "l"(ad + 6), "l"(bd + 6), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // mbar_wait by every lane of a warp with a warp-uniform verdict.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
                                                long long limit = kWaitCycles) {
@@ -137,31 +171,11 @@ __device__ __forceinline__ uint32_t idesc_mxf4(int M, int N) {
 // The MMA warp runs its loop with all 32 lanes (warp-uniform control flow, so every operand is
 // warp-uniform) and each tcgen05 instruction is issued by one lane chosen by elect.sync inside
 // the instruction's own asm block.
-__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
-            d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-        : "memory");
-}
-
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
-        "l"(sdesc)
         : "memory");
 }
 
@@ -341,21 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                 }
                 tc_fence_after();
                 const uint32_t sf = tmem + kSfBase + s * kSfCols;
-                tc_cp_sf(sf + 0, desc_sf(stage_sfa(s)));
-                tc_cp_sf(sf + 4, desc_sf(stage_sfa(s) + kAtom));
-                tc_cp_sf(sf + 8, desc_sf(stage_sfb(s)));
-                tc_cp_sf(sf + 12, desc_sf(stage_sfb(s) + kAtom));
-                const uint64_t adesc = desc_sw128(stage_a(s));
-                const uint64_t bdesc = desc_sw128(stage_b(s));
-#pragma unroll
-                for (int sub = 0; sub < 4; ++sub) {  // K = 64 per MMA
-                    const uint32_t sfid = (uint32_t)(sub & 1) * 2;
-                    const uint32_t id = idesc | (sfid << 29) | (sfid << 4);
-                    const uint32_t col = (uint32_t)(sub >> 1) * 4;
-                    mma_mxf4(d_tmem, adesc + 2 * sub, bdesc + 2 * sub, id, sf + col, sf + 8 + col,
-                             (kt > 0 || sub > 0) ? 1u : 0u);
-                }
-                tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+                stage_scales_to_tmem(sf, desc_sf(stage_sfa(s)), desc_sf(stage_sfa(s) + kAtom), desc_sf(stage_sfb(s)),
+                                     desc_sf(stage_sfb(s) + kAtom));
+                // the stage is free once these MMAs have read it
+                stage_mmas_commit(d_tmem, desc_sw128(stage_a(s)), desc_sw128(stage_b(s)), idesc,
+                                  idesc | (2u << 29) | (2u << 4), sf, kt > 0 ? 1u : 0u, &empty[s]);
             }
             if (!ok) break;
             tc_commit(&acc_full[buf]);
