@@ -230,19 +230,46 @@ cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float
 }
 
 // ------------------------------------------------------------------ tiled logits (any T)
-// CTA tile: 32 tokens x 32 experts, 16 warps as 4 (tokens) x 4 (experts), warp tile 8 x 8.
-// Lanes are the 32 partial sums of the fixed order; K is staged through shared memory in
-// chunks of 256 elements (64 groups of 4; lane c takes groups c and c + 32 of a chunk).
-constexpr int kLT = 32, kLE = 32, kLKC = 256;
+// Pure fp32 FMA work in the fixed order (lanes are the 32 partial sums).  CTA tile: 32 tokens x
+// 16 experts, 8 warps as 4 (tokens) x 2 (experts), warp tile 8 x 8 (64 accumulators per lane).
+// K is streamed through a 3-stage cp.async ring of 256-element chunks (64 groups of 4; lane c
+// takes groups c and c + 32 of a chunk, i.e. its elements in increasing order).  1024 CTAs of 256
+// threads for 4096 tokens x 128 experts: two resident per SM, about 7 per SM in all, so the last
+// wave is nearly full.
+constexpr int kLT = 32, kLE = 16, kLKC = 256, kLStages = 3, kLThreads = 256;
+constexpr int kLStageBytes = kLT * kLKC * 2 + kLE * kLKC * 4;  // bf16 x chunk + fp32 W_r chunk
 
-__global__ void __launch_bounds__(512)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+
+__global__ void __launch_bounds__(kLThreads, 2)
 route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ b,
                           int T, int d, int E, float* __restrict__ logits) {
-    __shared__ __align__(16) uint16_t xs[kLT][kLKC];
-    __shared__ __align__(16) float ws[kLE][kLKC];
+    extern __shared__ __align__(16) unsigned char lsm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * kLT, e0 = blockIdx.y * kLE;
-    const int wt = (warp >> 2) * 8, we = (warp & 3) * 8;
+    const int wt = (warp >> 1) * 8, we = (warp & 1) * 8;
+    auto xs = [&](int st) { return reinterpret_cast<uint16_t*>(lsm + (size_t)st * kLStageBytes); };
+    auto ws = [&](int st) { return reinterpret_cast<float*>(lsm + (size_t)st * kLStageBytes + kLT * kLKC * 2); };
+    const int nchunks = (d + kLKC - 1) / kLKC;
+    // stage chunk kc (16-byte pieces: x 32 rows x 32, W_r 16 rows x 64; zero-filled past T, E, d)
+    auto load_chunk = [&](int kc) {
+        const int st = kc % kLStages, k0 = kc * kLKC;
+        uint16_t* xd = xs(st);
+        float* wd = ws(st);
+        for (int i = tid; i < kLT * (kLKC / 8); i += kLThreads) {
+            const int r = i / (kLKC / 8), c = i % (kLKC / 8);
+            const bool ok = t0 + r < T && k0 + 8 * c < d;
+            cp_async16(xd + r * kLKC + 8 * c, ok ? x + (size_t)(t0 + r) * d + k0 + 8 * c : x, ok);
+        }
+        for (int i = tid; i < kLE * (kLKC / 4); i += kLThreads) {
+            const int r = i / (kLKC / 4), c = i % (kLKC / 4);
+            const bool ok = e0 + r < E && k0 + 4 * c < d;
+            cp_async16(wd + r * kLKC + 4 * c, ok ? W_r + (size_t)(e0 + r) * d + k0 + 4 * c : W_r, ok);
+        }
+    };
     float acc[8][8];
 #pragma unroll
     for (int a = 0; a < 8; ++a)
@@ -250,21 +277,19 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
         for (int c = 0; c < 8; ++c) acc[a][c] = 0.f;
 
     pdl_wait();
-    for (int k0 = 0; k0 < d; k0 += kLKC) {
-        __syncthreads();
-        for (int i = tid; i < kLT * kLKC / 8; i += blockDim.x) {  // 16-byte pieces of x
-            int r = i / (kLKC / 8), c = i % (kLKC / 8);
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t0 + r < T && k0 + 8 * c < d) v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * d + k0 + 8 * c);
-            *reinterpret_cast<uint4*>(&xs[r][8 * c]) = v;
-        }
-        for (int i = tid; i < kLE * kLKC / 4; i += blockDim.x) {
-            int r = i / (kLKC / 4), c = i % (kLKC / 4);
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e0 + r < E && k0 + 4 * c < d) v = *reinterpret_cast<const float4*>(W_r + (size_t)(e0 + r) * d + k0 + 4 * c);
-            *reinterpret_cast<float4*>(&ws[r][4 * c]) = v;
-        }
-        __syncthreads();
+#pragma unroll
+    for (int kc = 0; kc < kLStages - 1; ++kc) {
+        if (kc < nchunks) load_chunk(kc);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int kc = 0; kc < nchunks; ++kc) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kLStages - 2) : "memory");
+        __syncthreads();  // chunk kc is in; every warp is done with the stage refilled below
+        if (kc + kLStages - 1 < nchunks) load_chunk(kc + kLStages - 1);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        const uint16_t* xc = xs(kc % kLStages);
+        const float* wc = ws(kc % kLStages);
+        const int k0 = kc * kLKC;
 #pragma unroll
         for (int gi = 0; gi < 2; ++gi) {
             if (k0 + 128 * gi >= d) break;  // d % 128 == 0: a group of 32 lanes is all in or all out
@@ -272,7 +297,7 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
             float xv[8][4], wv[8][4];
 #pragma unroll
             for (int a = 0; a < 8; ++a) {
-                uint2 u = *reinterpret_cast<const uint2*>(&xs[wt + a][4 * g]);
+                const uint2 u = *reinterpret_cast<const uint2*>(xc + (wt + a) * kLKC + 4 * g);
                 xv[a][0] = bf16_bits_to_f32(u.x & 0xFFFF);
                 xv[a][1] = bf16_bits_to_f32(u.x >> 16);
                 xv[a][2] = bf16_bits_to_f32(u.y & 0xFFFF);
@@ -280,7 +305,7 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
             }
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                float4 f = *reinterpret_cast<const float4*>(&ws[we + c][4 * g]);
+                const float4 f = *reinterpret_cast<const float4*>(wc + (we + c) * kLKC + 4 * g);
                 wv[c][0] = f.x;
                 wv[c][1] = f.y;
                 wv[c][2] = f.z;
@@ -294,6 +319,7 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
                     for (int c = 0; c < 8; ++c) acc[a][c] = fmaf(xv[a][q], wv[c][q], acc[a][c]);
         }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
     for (int a = 0; a < 8; ++a)
 #pragma unroll
@@ -317,7 +343,8 @@ cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float
     if (T == 0) return cudaSuccess;
     void* args[] = {&x, &W_r, &b, &T, &d, &E, &logits};
     dim3 grid((T + kLT - 1) / kLT, (E + kLE - 1) / kLE);
-    return launch_kernel((const void*)route_logits_tiled_kernel, grid, dim3(512), 0, st, pdl, args);
+    return launch_kernel((const void*)route_logits_tiled_kernel, grid, dim3(kLThreads),
+                         (size_t)kLStages * kLStageBytes, st, pdl, args);
 }
 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl) {
