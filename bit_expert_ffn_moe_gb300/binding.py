@@ -27,8 +27,7 @@ MOE_ACT_MXFP4 = 1
 # every entry point declared in include/moe.h
 EXPORTED = (
     "moe_status_string", "moe_abi_version", "moe_last_cuda_error", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
-    "moe_mxfp4_scales_to_mma", "moe_mxfp4_scales_to_mma_paired", "moe_mxfp4_codes_to_mma",
-    "moe_mxfp4_codes_to_mma_paired", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
+    "moe_mxfp4_scales_to_mma", "moe_mxfp4_codes_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_layer_forward", "moe_synth_weights",
 )
@@ -45,8 +44,8 @@ class MoeError(RuntimeError):
 
 class moe_expert_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s", "gate_up_q_mma", "gate_up_s_mma",
-                 "down_q_mma", "down_s_mma")]
+                ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s", "gate_q_mma", "gate_s_mma",
+                 "up_q_mma", "up_s_mma", "down_q_mma", "down_s_mma")]
 
 
 _lib = None
@@ -63,9 +62,7 @@ _SIGS = {
     "moe_mxfp4_unpack": (I32, [P, P, I64, I64, P, P]),
     "moe_mxfp4_mma_scale_bytes": (SZ, [I64, I64]),
     "moe_mxfp4_scales_to_mma": (I32, [P, I64, I64, P, P]),
-    "moe_mxfp4_scales_to_mma_paired": (I32, [P, P, I64, I64, P, P]),
     "moe_mxfp4_codes_to_mma": (I32, [P, I64, I64, P, P]),
-    "moe_mxfp4_codes_to_mma_paired": (I32, [P, P, I64, I64, P, P]),
     "moe_workspace_size": (SZ, [I32, I32, I32, I32, I32, I32]),
     "moe_padded_rows": (I64, [I32, I32, I32]),
     "moe_workspace_init": (I32, [P, SZ, P]),
@@ -131,10 +128,10 @@ def status_string(status: int) -> str:
     return load().moe_status_string(int(status)).decode()
 
 
-def expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s, gate_up_q_mma=None, gate_up_s_mma=None,
-                          down_q_mma=None, down_s_mma=None) -> moe_expert_weights:
-    return moe_expert_weights(*[_p(t) for t in (gate_q, gate_s, up_q, up_s, down_q, down_s, gate_up_q_mma,
-                                                gate_up_s_mma, down_q_mma, down_s_mma)])
+def expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s, gate_q_mma=None, gate_s_mma=None,
+                          up_q_mma=None, up_s_mma=None, down_q_mma=None, down_s_mma=None) -> moe_expert_weights:
+    return moe_expert_weights(*[_p(t) for t in (gate_q, gate_s, up_q, up_s, down_q, down_s, gate_q_mma, gate_s_mma,
+                                                up_q_mma, up_s_mma, down_q_mma, down_s_mma)])
 
 
 # ------------------------------------------------------------------ entry points
@@ -159,18 +156,8 @@ def moe_mxfp4_scales_to_mma(s, rows, K, s_mma, stream=None):
     _check("moe_mxfp4_scales_to_mma", load().moe_mxfp4_scales_to_mma(_p(s), rows, K, _p(s_mma), _stream(stream)))
 
 
-def moe_mxfp4_scales_to_mma_paired(s_a, s_b, rows, K, s_mma, stream=None):
-    _check("moe_mxfp4_scales_to_mma_paired",
-           load().moe_mxfp4_scales_to_mma_paired(_p(s_a), _p(s_b), rows, K, _p(s_mma), _stream(stream)))
-
-
 def moe_mxfp4_codes_to_mma(q, rows, K, q_mma, stream=None):
     _check("moe_mxfp4_codes_to_mma", load().moe_mxfp4_codes_to_mma(_p(q), rows, K, _p(q_mma), _stream(stream)))
-
-
-def moe_mxfp4_codes_to_mma_paired(q_a, q_b, rows, K, q_mma, stream=None):
-    _check("moe_mxfp4_codes_to_mma_paired",
-           load().moe_mxfp4_codes_to_mma_paired(_p(q_a), _p(q_b), rows, K, _p(q_mma), _stream(stream)))
 
 
 def moe_workspace_size(T, d, E, k, I, fmt) -> int:

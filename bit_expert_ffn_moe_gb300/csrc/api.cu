@@ -8,7 +8,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -63,8 +63,9 @@ moe_status check_weights(const moe_expert_weights* W, moe_act_fmt fmt, bool need
     if (need_up) {
         if (!W->gate_q || !W->gate_s || !W->up_q || !W->up_s) return MOE_ERR_INVALID_ARG;
         if (!aligned(W->gate_q, 16) || !aligned(W->up_q, 16)) return MOE_ERR_INVALID_ARG;
-        if (fmt == MOE_ACT_MXFP4 && (!W->gate_up_q_mma || !W->gate_up_s_mma || !aligned(W->gate_up_q_mma, 16) ||
-                                     !aligned(W->gate_up_s_mma, 16)))
+        if (fmt == MOE_ACT_MXFP4 && (!W->gate_q_mma || !W->gate_s_mma || !W->up_q_mma || !W->up_s_mma ||
+                                     !aligned(W->gate_q_mma, 16) || !aligned(W->gate_s_mma, 16) ||
+                                     !aligned(W->up_q_mma, 16) || !aligned(W->up_s_mma, 16)))
             return MOE_ERR_INVALID_ARG;
     }
     if (need_down) {
@@ -141,28 +142,11 @@ moe_status moe_mxfp4_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, ui
     return from_cuda(launch_scales_to_mma(s, rows, K, s_mma, (cudaStream_t)stream));
 }
 
-moe_status moe_mxfp4_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
-                                          uint8_t* s_mma, moe_stream_t stream) {
-    if (rows <= 0 || K <= 0 || rows % 64 != 0 || K % 128 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (!s_a || !s_b || !s_mma) return MOE_ERR_INVALID_ARG;
-    MOE_TRY(check_device());
-    return from_cuda(launch_scales_to_mma_paired(s_a, s_b, rows, K, s_mma, (cudaStream_t)stream));
-}
-
 moe_status moe_mxfp4_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma, moe_stream_t stream) {
     if (rows <= 0 || K <= 0 || rows % 128 != 0 || K % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!q || !q_mma || !aligned(q, 16) || !aligned(q_mma, 16)) return MOE_ERR_INVALID_ARG;
     MOE_TRY(check_device());
-    return from_cuda(launch_codes_to_mma(q, nullptr, rows, K, false, q_mma, (cudaStream_t)stream));
-}
-
-moe_status moe_mxfp4_codes_to_mma_paired(const uint8_t* q_a, const uint8_t* q_b, int64_t rows, int64_t K,
-                                         uint8_t* q_mma, moe_stream_t stream) {
-    if (rows <= 0 || K <= 0 || rows % 64 != 0 || K % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (!q_a || !q_b || !q_mma || !aligned(q_a, 16) || !aligned(q_b, 16) || !aligned(q_mma, 16))
-        return MOE_ERR_INVALID_ARG;
-    MOE_TRY(check_device());
-    return from_cuda(launch_codes_to_mma(q_a, q_b, rows, K, true, q_mma, (cudaStream_t)stream));
+    return from_cuda(launch_codes_to_mma(q, rows, K, q_mma, (cudaStream_t)stream));
 }
 
 // ---------------------------------------------------------------- workspace

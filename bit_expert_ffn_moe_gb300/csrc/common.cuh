@@ -227,10 +227,7 @@ cudaError_t launch_synth(uint64_t seed, uint32_t tensor_id, uint32_t expert_firs
 cudaError_t launch_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w, cudaStream_t st);
 cudaError_t launch_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma, cudaStream_t st);
-cudaError_t launch_codes_to_mma(const uint8_t* q_a, const uint8_t* q_b, int64_t rows, int64_t K, bool paired,
-                                uint8_t* q_mma, cudaStream_t st);
-cudaError_t launch_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
-                                       uint8_t* s_mma, cudaStream_t st);
+cudaError_t launch_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma, cudaStream_t st);
 
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
                                 float* logits, cudaStream_t st, bool pdl);

@@ -59,39 +59,14 @@ __global__ void scales_to_mma_kernel(const uint8_t* __restrict__ s, int64_t rows
     }
 }
 
-// Paired layout: row block m of the virtual [2*rows][K] matrix = rows 64m..64m+63 of a, then
-// the same rows of b.  One thread per output byte.
-__global__ void scales_to_mma_paired_kernel(const uint8_t* __restrict__ sa, const uint8_t* __restrict__ sb,
-                                            int64_t rows, int64_t K, uint8_t* __restrict__ out) {
-    const int64_t cols = K / 32, total = 2 * rows * cols;
+// Code tiles: one thread per 16-byte chunk (one 32-element block) of the output.
+__global__ void codes_to_mma_kernel(const uint8_t* __restrict__ q, int64_t rows, int64_t K, uint8_t* __restrict__ out) {
+    const int64_t nb = K / 32;  // 16-byte chunks per row
+    const int64_t total = rows * nb;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t vr = i / cols, c = i % cols;  // row of the virtual paired matrix
-        const int64_t m = vr / 128, r = vr % 128;
-        const int64_t src_row = 64 * m + (r & 63);
-        const uint8_t* src = r < 64 ? sa : sb;
-        out[mma_scale_offset(vr, c, K)] = src[src_row * cols + c];
-    }
-}
-
-// Code tiles: one thread per 16-byte chunk (one 32-element block) of the output.  Unpaired: row
-// block R = rows 128R..128R+127 of q_a.  Paired: rows 64R..64R+63 of q_a, then of q_b.
-__global__ void codes_to_mma_kernel(const uint8_t* __restrict__ qa, const uint8_t* __restrict__ qb, int64_t rows,
-                                    int64_t K, int paired, uint8_t* __restrict__ out) {
-    const int64_t nb = K / 32;                           // 16-byte chunks per row
-    const int64_t out_rows = paired ? 2 * rows : rows;   // rows of the (virtual) tiled matrix
-    const int64_t total = out_rows * nb;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t vr = i / nb, blk = i % nb;
-        const uint8_t* src;
-        if (paired) {
-            const int64_t m = vr / 128, r = vr % 128;
-            src = (r < 64 ? qa : qb) + (64 * m + (r & 63)) * (K / 2);
-        } else {
-            src = qa + vr * (K / 2);
-        }
-        *reinterpret_cast<uint4*>(out + mma_tile_offset(vr, blk, K)) = reinterpret_cast<const uint4*>(src)[blk];
+        const int64_t r = i / nb, blk = i % nb;
+        *reinterpret_cast<uint4*>(out + mma_tile_offset(r, blk, K)) = reinterpret_cast<const uint4*>(q)[i];
     }
 }
 
@@ -122,19 +97,10 @@ cudaError_t launch_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint
     return cudaGetLastError();
 }
 
-cudaError_t launch_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
-                                       uint8_t* s_mma, cudaStream_t st) {
-    int64_t n = 2 * rows * (K / 32);
+cudaError_t launch_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma, cudaStream_t st) {
+    int64_t n = rows * (K / 32);
     if (n == 0) return cudaSuccess;
-    scales_to_mma_paired_kernel<<<grid_for(n, 256), 256, 0, st>>>(s_a, s_b, rows, K, s_mma);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_codes_to_mma(const uint8_t* q_a, const uint8_t* q_b, int64_t rows, int64_t K, bool paired,
-                                uint8_t* q_mma, cudaStream_t st) {
-    int64_t n = (paired ? 2 : 1) * rows * (K / 32);
-    if (n == 0) return cudaSuccess;
-    codes_to_mma_kernel<<<grid_for(n, 256), 256, 0, st>>>(q_a, q_b, rows, K, paired ? 1 : 0, q_mma);
+    codes_to_mma_kernel<<<grid_for(n, 256), 256, 0, st>>>(q, rows, K, q_mma);
     return cudaGetLastError();
 }
 

@@ -6,30 +6,35 @@
 // batch).  Expert weights and activations are both MXFP4 (DGX Spark news item, section 2: the
 // block-scaled 4-bit MXFP4 expert path), so the MMA consumes them without any dequantisation.
 //
-// Roles: the tokens of one expert are the MMA "A" operand (M = 128 padded token rows) and a
-// block of weight rows is "B" (N = 128).  D[m][n] = sum_k A[m][k] * B[n][k] lives in tensor
-// memory with lane m = token and column n = weight row, so an epilogue thread owns one token
-// row and one tcgen05.ld of 32 columns hands it a whole 32-element block of the output: the
-// SwiGLU result is requantised to MXFP4 with no cross-lane traffic, and y rows are written as
-// contiguous 64-byte pieces.
-//   up:   B = 64 gate rows followed by the same 64 up rows (paired tensor-core layouts), so D
-//         holds g in columns 0..63 and u in columns 64..127 of 64 consecutive intermediate rows.
-//   down: B = 128 rows of W_down (128 output features).
+// Roles: the tokens of one expert are the MMA "A" operand (M = 128 padded token rows) and 256
+// weight rows are "B" (N = 256).  D[m][n] = sum_k A[m][k] * B[n][k] lives in tensor memory with
+// lane m = token and column n = weight row, so an epilogue thread owns one token row and one
+// tcgen05.ld of 32 columns hands it a whole 32-element block of the output: the SwiGLU result is
+// requantised to MXFP4 with no cross-lane traffic, and y rows are written as contiguous 64-byte
+// pieces.
+//   up:   B = 128 gate rows followed by the same 128 up rows, so D holds g in columns 0..127 and
+//         u in columns 128..255 of 128 consecutive intermediate rows.
+//   down: B = 256 rows of W_down (256 output features).
+// Why N = 256: an MMA reads its operands from shared memory, which the copy engine also has to
+// fill, and at M = N = 128 that traffic (not the tensor math) bounds the K loop on GB300; N = 256
+// moves 25% fewer shared-memory bytes per flop and hides the scale copies behind the MMAs.  Its
+// 256 accumulator columns leave room for one accumulator buffer only (tensor memory holds 512
+// columns and the scale slots need the rest), so the MMAs wait while the epilogue drains it.
 // Tiles are (expert e, token tile j, weight block p) with p fastest: CTAs that run at the same
 // time share a token tile through L2 and walk the expert's weight blocks, each of which stays in
 // L2 while the expert's other token tiles use it.
 //
 // One persistent CTA per SM walks the tile list:
-//   warp 0    producer: per K step, four bulk copies (the copy engine) into a ring of stages --
-//             the 16 KB token tile, the 16 KB weight tile and their two 1 KB scale pieces.  All
+//   warp 0    producer: per K step, six bulk copies (the copy engine) into a ring of stages --
+//             the 16 KB token tile, two 16 KB weight tiles and their 1 KB scale pieces.  All
 //             operands are stored pre-arranged in the tensor-core layouts (code tiles already
 //             in the 128-byte swizzle, scale atoms), so every piece is one contiguous copy; on
 //             GB300 these run markedly faster than 2-D tensor boxes of 128-byte rows, from L2 as
 //             well as from HBM;
-//   warp 1    allocates tensor memory, copies each stage's scales into it (tcgen05.cp) and
-//             issues the MMAs from one thread; tcgen05.commit frees stages and publishes tiles;
-//   warps 2-5 epilogue, one tensor-memory lane quarter (32 token rows) each, on a ring of three
-//             accumulator buffers so that the MMAs of the next tiles overlap it.
+//   warp 1    allocates tensor memory; with all 32 lanes, copies each stage's scales into it
+//             (tcgen05.cp) and issues the MMAs (one elected lane); tcgen05.commit frees stages
+//             and publishes the accumulator;
+//   warps 2-5 epilogue, one tensor-memory lane quarter (32 token rows) each.
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
@@ -41,12 +46,13 @@ constexpr int kEpiWarps = 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, 4 epilogue warps
 constexpr int kTile = 128 * 128;                // 128 rows x 128 bytes (256 FP4 values)
 constexpr int kAtom = 512;                      // scale atom: 128 rows x 4 scales
-constexpr int kStages = 6;
-constexpr int kStageBytes = 2 * kTile + 4 * kAtom;  // A tile, B tile, 2 atoms of A scales, 2 of B
-constexpr int kAccBufs = 3;
-constexpr int kAccCols = 128;
-constexpr int kSfBase = kAccBufs * kAccCols;  // scale slots after the accumulators
-constexpr int kSfCols = 16;                   // per stage: A scales 8 columns, B scales 8
+constexpr int kStages = 4;
+// A tile, two B tiles (256 weight rows), 2 atoms of A scales, 2 + 2 of B scales
+constexpr int kStageBytes = 3 * kTile + 6 * kAtom;
+constexpr int kAccBufs = 1;
+constexpr int kAccCols = 256;
+constexpr int kSfBase = kAccBufs * kAccCols;  // scale slots after the accumulator
+constexpr int kSfCols = 24;                   // per stage: A scales 8 columns, B scales 16
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarBytes = 256;
 constexpr long long kWaitCycles = 4000000000LL;  // about two seconds at GB300 clocks
@@ -98,23 +104,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// One K step of 256 values: the four scale-atom copies of the stage into tensor memory, then the
+// One K step of 256 values: the six scale-atom copies of the stage into tensor memory, then the
 // four K = 64 MMAs and the commit that frees the stage, each group issued by one elected lane.
-__device__ __forceinline__ void stage_scales_to_tmem(uint32_t sf, uint64_t da0, uint64_t da1, uint64_t db0,
-                                                     uint64_t db1) {
+// Scale slot of a stage (24 columns from sf): A scales of K values 0..127 at sf, 128..255 at
+// sf + 4; B scales of K values 0..127 at sf + 8 (rows 0..127) and sf + 12 (rows 128..255), of
+// K values 128..255 at sf + 16 and sf + 20.
+__device__ __forceinline__ void stage_scales_to_tmem(uint32_t sf, uint64_t a0, uint64_t a1, uint64_t b00,
+                                                     uint64_t b10, uint64_t b01, uint64_t b11) {
     asm volatile(
         "{\n\t.reg .pred e;\n\t"
         "elect.sync _|e, 0xffffffff;\n\t"
         "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t"
         "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%2], %3;\n\t"
         "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%6], %7;\n\t}" ::"r"(sf),
-        "l"(da0), "r"(sf + 4), "l"(da1), "r"(sf + 8), "l"(db0), "r"(sf + 12), "l"(db1)
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%6], %7;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%8], %9;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%10], %11;\n\t}" ::"r"(sf),
+        "l"(a0), "r"(sf + 4), "l"(a1), "r"(sf + 8), "l"(b00), "r"(sf + 12), "l"(b10), "r"(sf + 16), "l"(b01),
+        "r"(sf + 20), "l"(b11)
         : "memory");
 }
 
-// MMAs of one stage: sub-steps 0..3 use A/B descriptors advanced by 32 bytes each, scale bytes
-// (sub & 1) * 2 of tensor-memory column (sub >> 1) * 4 (A at sf, B at sf + 8).
+// MMAs of one stage: sub-steps 0..3 use A/B descriptors advanced by 32 bytes each and scale bytes
+// (sub & 1) * 2 of the A/B scale columns of K values 0..127 (subs 0, 1) or 128..255 (subs 2, 3).
 __device__ __forceinline__ void stage_mmas_commit(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id0, uint32_t id2,
                                                   uint32_t sf, uint32_t accumulate, uint64_t* bar) {
     asm volatile(
@@ -128,7 +140,7 @@ __device__ __forceinline__ void stage_mmas_commit(uint32_t d, uint64_t ad, uint6
         "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %14, %15, %4, [%12], [%13], q;\n\t"
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%16];\n\t}" ::"r"(d),
         "l"(ad), "l"(bd), "r"(id0), "r"(id2), "r"(accumulate), "r"(sf), "r"(sf + 8), "l"(ad + 2), "l"(bd + 2),
-        "l"(ad + 4), "l"(bd + 4), "r"(sf + 4), "r"(sf + 12), "l"(ad + 6), "l"(bd + 6), "r"(smem_u32(bar))
+        "l"(ad + 4), "l"(bd + 4), "r"(sf + 4), "r"(sf + 16), "l"(ad + 6), "l"(bd + 6), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -195,13 +207,16 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 struct UmmaArgs {
     const uint8_t* qa;   // token-operand code tiles (padded rows)
     const uint8_t* sfa;  // token-operand scales (tensor-core layout over padded rows)
-    const uint8_t* qb;   // weight code tiles: paired gate/up (up) or down
-    const uint8_t* sfb;  // weight scales: paired gate/up layout (up) or down layout
+    const uint8_t* qb0;  // B rows 0..127: gate (up) or down code tiles
+    const uint8_t* sfb0;
+    const uint8_t* qb1;  // B rows 128..255: up (up) or down code tiles
+    const uint8_t* sfb1;
+    int b1_step;         // 128-row block of B rows 128..255 relative to rows 0..127: 0 (up), 1 (down)
     PlanView plan;
     const int32_t* offsets;
     int E;
     int K;       // contraction length: d (up) or I (down)
-    int NB;      // weight blocks per expert: I/64 (up) or d/128 (down)
+    int NB;      // weight blocks per expert: I/128 (up) or d/256 (down)
     int n_out;   // output row length: I (h, up) or d (y_perm, down)
     uint8_t* h;    // up: MXFP4 code tiles of [pad_rows][I]
     uint8_t* h_s;  // up: scales, tensor-core layout
@@ -218,7 +233,7 @@ struct SmemPlan {
 };
 
 struct Tile {
-    int e, j, p, n_valid, a_row, y_row, b_blk;
+    int e, j, p, n_valid, a_row, y_row, b_rb;
 };
 
 // Advance `e` (monotone over a CTA's tiles) to the expert owning tile t and fill in the tile.
@@ -233,7 +248,8 @@ __device__ __forceinline__ Tile decode_tile(int t, int& e, const SmemPlan& sp, c
     T.n_valid = min(kTokTile, sp.counts[e] - T.j * kTokTile);
     T.a_row = sp.pad_offsets[e] + T.j * kTokTile;
     T.y_row = sp.offsets[e] + T.j * kTokTile;
-    T.b_blk = e * a.NB + T.p;  // 128-row block of the (paired) weight layouts
+    // 128-row block of B rows 0..127 in the weight matrix ([E*I] rows up, [E*d] rows down)
+    T.b_rb = IS_UP ? e * a.NB + T.p : e * 2 * a.NB + 2 * T.p;
     return T;
 }
 
@@ -260,9 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     auto stage_a = [&](int s) { return smem + (size_t)s * kStageBytes; };
-    auto stage_b = [&](int s) { return smem + (size_t)s * kStageBytes + kTile; };
-    auto stage_sfa = [&](int s) { return smem + (size_t)s * kStageBytes + 2 * kTile; };
-    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + 2 * kTile + 2 * kAtom; };
+    auto stage_b = [&](int s) { return smem + (size_t)s * kStageBytes + kTile; };  // 256 rows
+    auto stage_sfa = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile; };
+    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile + 2 * kAtom; };  // 2 x 1 KB
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -307,10 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
             bool ok = true;
             for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
                 const Tile T = decode_tile<IS_UP>(t, e, sp, args);
+                const size_t rb1 = (size_t)T.b_rb + args.b1_step;
                 const uint8_t* qa = args.qa + (size_t)(T.a_row / 128) * KT * kTile;
-                const uint8_t* qb = args.qb + (size_t)T.b_blk * KT * kTile;
+                const uint8_t* qb0 = args.qb0 + (size_t)T.b_rb * KT * kTile;
+                const uint8_t* qb1 = args.qb1 + rb1 * KT * kTile;
                 const uint8_t* sfa = args.sfa + ((size_t)(T.a_row / 128) * atoms_per_rowblk) * kAtom;
-                const uint8_t* sfb = args.sfb + ((size_t)T.b_blk * atoms_per_rowblk) * kAtom;
+                const uint8_t* sfb0 = args.sfb0 + ((size_t)T.b_rb * atoms_per_rowblk) * kAtom;
+                const uint8_t* sfb1 = args.sfb1 + (rb1 * atoms_per_rowblk) * kAtom;
                 for (int kt = 0; kt < KT; ++kt, ++kiter) {
                     const int s = kiter % kStages;
                     const uint32_t ph = (kiter / kStages) & 1;
@@ -320,9 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                     }
                     mbar_arrive_expect_tx(&full[s], kStageBytes);
                     bulk_load(stage_a(s), qa + (size_t)kt * kTile, kTile, &full[s]);
-                    bulk_load(stage_b(s), qb + (size_t)kt * kTile, kTile, &full[s]);
+                    bulk_load(stage_b(s), qb0 + (size_t)kt * kTile, kTile, &full[s]);
+                    bulk_load(stage_b(s) + kTile, qb1 + (size_t)kt * kTile, kTile, &full[s]);
                     bulk_load(stage_sfa(s), sfa + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
-                    bulk_load(stage_sfb(s), sfb + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
+                    bulk_load(stage_sfb(s), sfb0 + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
+                    bulk_load(stage_sfb(s) + 2 * kAtom, sfb1 + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
                 }
             }
             if (*abort_flag) {
@@ -339,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
         // ---------------------------------------------------------- MMA issuer (whole warp)
         int kiter = 0, it = 0;
         bool ok = true;
-        const uint32_t idesc = idesc_mxf4(128, 128);
+        const uint32_t idesc = idesc_mxf4(128, 256);
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
             const int buf = it % kAccBufs;
             const uint32_t use = it / kAccBufs;
@@ -356,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                 tc_fence_after();
                 const uint32_t sf = tmem + kSfBase + s * kSfCols;
                 stage_scales_to_tmem(sf, desc_sf(stage_sfa(s)), desc_sf(stage_sfa(s) + kAtom), desc_sf(stage_sfb(s)),
-                                     desc_sf(stage_sfb(s) + kAtom));
+                                     desc_sf(stage_sfb(s) + 2 * kAtom), desc_sf(stage_sfb(s) + kAtom),
+                                     desc_sf(stage_sfb(s) + 3 * kAtom));
                 // the stage is free once these MMAs have read it
                 stage_mmas_commit(d_tmem, desc_sw128(stage_a(s)), desc_sw128(stage_b(s)), idesc,
                                   idesc | (2u << 29) | (2u << 4), sf, kt > 0 ? 1u : 0u, &empty[s]);
@@ -384,11 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
             if (IS_UP) {
                 const int I = args.n_out;
                 const size_t row = (size_t)T.a_row + m;  // every padded row is written (zeros there)
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
                     uint32_t g[32], u[32];
                     tmem_ld32(acc + 32 * c, g);
-                    tmem_ld32(acc + 64 + 32 * c, u);
+                    tmem_ld32(acc + 128 + 32 * c, u);
                     tmem_ld_wait();
                     float hv[32];
 #pragma unroll
@@ -398,15 +420,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                     }
                     uint4 codes;
                     const uint32_t sb = mx_block_encode(hv, codes);
-                    const int blk = 2 * T.p + c;  // 32-block of h along I
+                    const int blk = 4 * T.p + c;  // 32-block of h along I
                     *reinterpret_cast<uint4*>(args.h + mma_tile_offset((int64_t)row, blk, I)) = codes;
                     args.h_s[mma_scale_offset((int64_t)row, blk, I)] = (uint8_t)sb;
                 }
             } else {
                 const int d = args.n_out;
-                uint16_t* yrow = args.y_perm + ((size_t)T.y_row + m) * d + (size_t)T.p * 128;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                uint16_t* yrow = args.y_perm + ((size_t)T.y_row + m) * d + (size_t)T.p * 256;
+#pragma unroll 1
+                for (int c = 0; c < 8; ++c) {
                     uint32_t v[32];
                     tmem_ld32(acc + 32 * c, v);
                     tmem_ld_wait();
@@ -464,13 +486,16 @@ cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan
     UmmaArgs a = {};
     a.qa = xa;
     a.sfa = xa_s;
-    a.qb = W->gate_up_q_mma;
-    a.sfb = W->gate_up_s_mma;
+    a.qb0 = W->gate_q_mma;
+    a.sfb0 = W->gate_s_mma;
+    a.qb1 = W->up_q_mma;
+    a.sfb1 = W->up_s_mma;
+    a.b1_step = 0;
     a.plan = plan;
     a.offsets = offsets;
     a.E = E;
     a.K = d;
-    a.NB = I / 64;
+    a.NB = I / 128;
     a.n_out = I;
     a.h = h;
     a.h_s = h_s;
@@ -487,13 +512,16 @@ cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan
     UmmaArgs a = {};
     a.qa = h;
     a.sfa = h_s;
-    a.qb = W->down_q_mma;
-    a.sfb = W->down_s_mma;
+    a.qb0 = W->down_q_mma;
+    a.sfb0 = W->down_s_mma;
+    a.qb1 = W->down_q_mma;
+    a.sfb1 = W->down_s_mma;
+    a.b1_step = 1;
     a.plan = plan;
     a.offsets = offsets;
     a.E = E;
     a.K = I;
-    a.NB = d / 128;
+    a.NB = d / 256;
     a.n_out = d;
     a.y_perm = y_perm;
     a.status = status;

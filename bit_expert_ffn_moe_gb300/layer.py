@@ -43,14 +43,11 @@ class DeviceLayer:
         G, U, D = IN.TENSOR_GATE, IN.TENSOR_UP, IN.TENSOR_DOWN
         self.q_mma = {}
         if mma_layouts and d % 256 == 0 and I % 256 == 0:  # copies for the tensor-core (MXFP4) path
-            self.q_mma[G] = torch.empty(2 * E * I * d // 2, **u8)
-            B.moe_mxfp4_codes_to_mma_paired(self.q[G], self.q[U], E * I, d, self.q_mma[G])
-            self.s_mma[G] = torch.empty(B.moe_mxfp4_mma_scale_bytes(2 * E * I, d), **u8)
-            B.moe_mxfp4_scales_to_mma_paired(self.s[G], self.s[U], E * I, d, self.s_mma[G])
-            self.q_mma[D] = torch.empty(E * d * I // 2, **u8)
-            B.moe_mxfp4_codes_to_mma(self.q[D], E * d, I, self.q_mma[D])
-            self.s_mma[D] = torch.empty(B.moe_mxfp4_mma_scale_bytes(E * d, I), **u8)
-            B.moe_mxfp4_scales_to_mma(self.s[D], E * d, I, self.s_mma[D])
+            for tid, (rows, K) in shapes.items():
+                self.q_mma[tid] = torch.empty(E * rows * K // 2, **u8)
+                B.moe_mxfp4_codes_to_mma(self.q[tid], E * rows, K, self.q_mma[tid])
+                self.s_mma[tid] = torch.empty(B.moe_mxfp4_mma_scale_bytes(E * rows, K), **u8)
+                B.moe_mxfp4_scales_to_mma(self.s[tid], E * rows, K, self.s_mma[tid])
         W_r, b = IN.make_router(cfg)
         if layer != 0:  # independent router per layer copy
             rng = np.random.default_rng([cfg.seed, 77, layer])
@@ -59,8 +56,8 @@ class DeviceLayer:
         self.W_r = torch.from_numpy(W_r).to(self.device)
         self.b = torch.from_numpy(b).to(self.device)
         self.weights = B.expert_weights_struct(self.q[G], self.s[G], self.q[U], self.s[U], self.q[D], self.s[D],
-                                               self.q_mma.get(G), self.s_mma.get(G), self.q_mma.get(D),
-                                               self.s_mma.get(D))
+                                               self.q_mma.get(G), self.s_mma.get(G), self.q_mma.get(U),
+                                               self.s_mma.get(U), self.q_mma.get(D), self.s_mma.get(D))
 
     def weight_bytes_per_expert(self) -> int:
         cfg = self.cfg

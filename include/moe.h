@@ -67,13 +67,11 @@ typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1 } moe_act_fmt;
  *   gate_q/up_q [E][I][d/2], gate_s/up_s [E][I][d/32]   (gate and up: I rows of d)
  *   down_q      [E][d][I/2], down_s      [E][d][I/32]   (down: d rows of I)
  * The MXFP4 path reads copies re-laid out for the tensor cores (see "tensor-core layouts"):
- *   gate_up_q_mma  moe_mxfp4_codes_to_mma_paired(gate_q, up_q, E*I, d)
- *   gate_up_s_mma  moe_mxfp4_scales_to_mma_paired(gate_s, up_s, E*I, d)
- *                  (the gate and up rows of each 64-row block side by side: the MMA computes g
- *                  and u of 64 intermediate rows in one 128-row operand)
- *   down_q_mma     moe_mxfp4_codes_to_mma(down_q, E*d, I)
- *   down_s_mma     moe_mxfp4_scales_to_mma(down_s, E*d, I)
- * The BF16 path reads only the canonical tensors (the four copies may be NULL). */
+ *   gate_q_mma, up_q_mma   moe_mxfp4_codes_to_mma(gate_q or up_q, E*I, d)
+ *   gate_s_mma, up_s_mma   moe_mxfp4_scales_to_mma(gate_s or up_s, E*I, d)
+ *   down_q_mma             moe_mxfp4_codes_to_mma(down_q, E*d, I)
+ *   down_s_mma             moe_mxfp4_scales_to_mma(down_s, E*d, I)
+ * The BF16 path reads only the canonical tensors (the six copies may be NULL). */
 typedef struct moe_expert_weights {
     const uint8_t* gate_q;
     const uint8_t* gate_s;
@@ -81,8 +79,10 @@ typedef struct moe_expert_weights {
     const uint8_t* up_s;
     const uint8_t* down_q;
     const uint8_t* down_s;
-    const uint8_t* gate_up_q_mma;
-    const uint8_t* gate_up_s_mma;
+    const uint8_t* gate_q_mma;
+    const uint8_t* gate_s_mma;
+    const uint8_t* up_q_mma;
+    const uint8_t* up_s_mma;
     const uint8_t* down_q_mma;
     const uint8_t* down_s_mma;
 } moe_expert_weights;
@@ -123,10 +123,7 @@ moe_status moe_mxfp4_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, in
  *           as the canonical codes.
  *   scales  a grid of 512-byte atoms, atom (R, C) = rows 128R..128R+127 x scale columns
  *           4C..4C+3 at atom index R*(K/128) + C; inside an atom, row r and scale column c sit
- *           at byte (r%32)*16 + ((r/32)%4)*4 + (c%4).
- * Paired forms of two matrices a and b (the gate and up matrices, rows % 64 == 0): the layout of
- * the [2*rows][K] matrix whose 128-row block m holds rows 64m..64m+63 of a followed by rows
- * 64m..64m+63 of b. */
+ *           at byte (r%32)*16 + ((r/32)%4)*4 + (c%4). */
 
 /* Bytes of the tensor-core scale layout of a [rows][K] matrix (rows % 128 == 0, K % 128 == 0;
  * 0 otherwise). */
@@ -136,20 +133,10 @@ size_t moe_mxfp4_mma_scale_bytes(int64_t rows, int64_t K);
 moe_status moe_mxfp4_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma,
                                    moe_stream_t stream);
 
-/* Paired tensor-core scale layout of s_a and s_b ([rows][K/32] each; rows % 64 == 0,
- * K % 128 == 0); s_mma has moe_mxfp4_mma_scale_bytes(2*rows, K) bytes. */
-moe_status moe_mxfp4_scales_to_mma_paired(const uint8_t* s_a, const uint8_t* s_b, int64_t rows, int64_t K,
-                                          uint8_t* s_mma, moe_stream_t stream);
-
 /* Re-lay canonical codes q[rows][K/2] out into the tensor-core code tiles q_mma (rows*K/2 bytes;
  * rows % 128 == 0, K % 256 == 0). */
 moe_status moe_mxfp4_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma,
                                   moe_stream_t stream);
-
-/* Paired code tiles of q_a and q_b ([rows][K/2] each; rows % 64 == 0, K % 256 == 0); q_mma has
- * rows*K bytes. */
-moe_status moe_mxfp4_codes_to_mma_paired(const uint8_t* q_a, const uint8_t* q_b, int64_t rows, int64_t K,
-                                         uint8_t* q_mma, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- workspace */
 

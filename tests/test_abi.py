@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 3
+    assert B.moe_abi_version() == 4
     assert B.status_string(0) == "MOE_OK"
     assert B.status_string(5) == "MOE_ERR_TIMEOUT"
 

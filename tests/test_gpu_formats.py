@@ -73,28 +73,6 @@ def test_scales_to_mma_layout():
     np.testing.assert_array_equal(got, ref)
 
 
-def test_scales_to_mma_paired_layout():
-    rows, K = 192, 256  # three 64-row pairs, two atoms along K
-    rng = np.random.default_rng(4)
-    sa = rng.integers(0, 255, size=(rows, K // 32)).astype(np.uint8)
-    sb = rng.integers(0, 255, size=(rows, K // 32)).astype(np.uint8)
-    out = torch.empty(B.moe_mxfp4_mma_scale_bytes(2 * rows, K), dtype=torch.uint8, device="cuda")
-    B.moe_mxfp4_scales_to_mma_paired(torch.from_numpy(sa).cuda(), torch.from_numpy(sb).cuda(), rows, K, out)
-    got = out.cpu().numpy()
-    # documented layout: the plain layout of the [2*rows][K] matrix whose 128-row block m holds
-    # rows 64m..64m+63 of a, then the same rows of b
-    virt = np.empty((2 * rows, K // 32), dtype=np.uint8)
-    for m in range(rows // 64):
-        virt[128 * m:128 * m + 64] = sa[64 * m:64 * m + 64]
-        virt[128 * m + 64:128 * m + 128] = sb[64 * m:64 * m + 64]
-    ref = np.empty_like(got)
-    for r in range(2 * rows):
-        for c in range(K // 32):
-            atom = (r // 128) * (K // 128) + c // 4
-            ref[atom * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + c % 4] = virt[r, c]
-    np.testing.assert_array_equal(got, ref)
-
-
 def _tiles_reference(virt_codes, K):
     """Documented code tiles of a [rows][K/2] code matrix: tile (R, C) at index R*(K/256) + C,
     16-byte chunk j of row r inside it at r*128 + (j ^ (r % 8))*16."""
@@ -114,17 +92,3 @@ def test_codes_to_mma_tiles():
     out = torch.empty(rows * K // 2, dtype=torch.uint8, device="cuda")
     B.moe_mxfp4_codes_to_mma(torch.from_numpy(q).cuda(), rows, K, out)
     np.testing.assert_array_equal(out.cpu().numpy(), _tiles_reference(q, K))
-
-
-def test_codes_to_mma_tiles_paired():
-    rows, K = 192, 768
-    rng = np.random.default_rng(6)
-    qa = rng.integers(0, 256, size=(rows, K // 2)).astype(np.uint8)
-    qb = rng.integers(0, 256, size=(rows, K // 2)).astype(np.uint8)
-    out = torch.empty(rows * K, dtype=torch.uint8, device="cuda")
-    B.moe_mxfp4_codes_to_mma_paired(torch.from_numpy(qa).cuda(), torch.from_numpy(qb).cuda(), rows, K, out)
-    virt = np.empty((2 * rows, K // 2), dtype=np.uint8)
-    for m in range(rows // 64):
-        virt[128 * m:128 * m + 64] = qa[64 * m:64 * m + 64]
-        virt[128 * m + 64:128 * m + 128] = qb[64 * m:64 * m + 64]
-    np.testing.assert_array_equal(out.cpu().numpy(), _tiles_reference(virt, K))
