@@ -34,7 +34,8 @@
 //   warp 1    allocates tensor memory; with all 32 lanes, copies each stage's scales into it
 //             (tcgen05.cp) and issues the MMAs (one elected lane); tcgen05.commit frees stages
 //             and publishes the accumulator;
-//   warps 2-5 epilogue, one tensor-memory lane quarter (32 token rows) each.
+//   warps 2-9 epilogue: two warps per tensor-memory lane quarter (32 token rows), each taking
+//             half of the accumulator columns, so that it is drained (and the MMAs resume) soon.
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
@@ -42,8 +43,8 @@
 namespace moe {
 namespace {
 
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, 4 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, 8 epilogue warps
 constexpr int kTile = 128 * 128;                // 128 rows x 128 bytes (256 FP4 values)
 constexpr int kAtom = 512;                      // scale atom: 128 rows x 4 scales
 constexpr int kStages = 4;
@@ -392,7 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
         mbar_wait_warp(mma_done, 0, &never, nullptr, 100000000LL);
     } else {
         // ---------------------------------------------------------- epilogue
-        const int q = warp & 3;  // tensor-memory lane quarter this warp may access
+        const int q = warp & 3;                // tensor-memory lane quarter this warp may access
+        const int half = (warp - 2) / 4;       // half of the accumulator columns it drains
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const int m = 32 * q + lane;  // token row within the tile
         int it = 0, e = 0;
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                 const int I = args.n_out;
                 const size_t row = (size_t)T.a_row + m;  // every padded row is written (zeros there)
 #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 2 * half; c < 2 * half + 2; ++c) {
                     uint32_t g[32], u[32];
                     tmem_ld32(acc + 32 * c, g);
                     tmem_ld32(acc + 128 + 32 * c, u);
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                 const int d = args.n_out;
                 uint16_t* yrow = args.y_perm + ((size_t)T.y_row + m) * d + (size_t)T.p * 256;
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 4 * half; c < 4 * half + 4; ++c) {
                     uint32_t v[32];
                     tmem_ld32(acc + 32 * c, v);
                     tmem_ld_wait();
