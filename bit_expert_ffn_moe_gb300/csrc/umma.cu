@@ -204,6 +204,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 4 x 4 transpose of 16-byte pieces among the lanes of each aligned group of four: on entry lane
+// 4g + i holds pieces p[0..3] of row i of the group, on return p[j] = piece i of row j.  Two xor
+// stages (swap the off-diagonal 2 x 2 blocks, then the off-diagonal pieces inside each block).
+__device__ __forceinline__ void transpose4_pieces(uint4 (&p)[4], int lane) {
+    const bool i1 = (lane >> 1) & 1, i0 = lane & 1;
+#pragma unroll
+    for (int j0 = 0; j0 < 2; ++j0) {  // stage A: exchange pieces whose bit 1 differs from the lane's
+        uint4& lo = p[j0];
+        uint4& hi = p[2 | j0];
+        uint4 snd = i1 ? lo : hi;
+        uint4 rcv;
+        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, 2);
+        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, 2);
+        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, 2);
+        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, 2);
+        if (i1) lo = rcv; else hi = rcv;
+    }
+#pragma unroll
+    for (int j1 = 0; j1 < 2; ++j1) {  // stage B: exchange pieces whose bit 0 differs from the lane's
+        uint4& lo = p[2 * j1];
+        uint4& hi = p[2 * j1 + 1];
+        uint4 snd = i0 ? lo : hi;
+        uint4 rcv;
+        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, 1);
+        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, 1);
+        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, 1);
+        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, 1);
+        if (i0) lo = rcv; else hi = rcv;
+    }
+}
+
 // ------------------------------------------------------------------ kernel arguments / tiles
 struct UmmaArgs {
     const uint8_t* qa;   // token-operand code tiles (padded rows)
@@ -427,23 +458,35 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                     args.h_s[mma_scale_offset((int64_t)row, blk, I)] = (uint8_t)sb;
                 }
             } else {
+                // Each thread holds 32 columns (64 bytes) of its own token row; after a 4 x 4
+                // transpose of 16-byte pieces inside groups of four lanes, store j writes 64
+                // contiguous bytes of 8 rows (row 4g + j of each group) instead of 16 bytes of 32.
                 const int d = args.n_out;
-                uint16_t* yrow = args.y_perm + ((size_t)T.y_row + m) * d + (size_t)T.p * 256;
+                const int rbase = 32 * q + 4 * (lane >> 2), piece = lane & 3;
 #pragma unroll 1
                 for (int c = 4 * half; c < 4 * half + 4; ++c) {
                     uint32_t v[32];
                     tmem_ld32(acc + 32 * c, v);
                     tmem_ld_wait();
-                    if (m < T.n_valid) {
-                        uint32_t pk[16];
+                    uint4 pc[4];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                            pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+                    for (int a = 0; a < 4; ++a) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * a + 2 * i]),
+                                                                      __uint_as_float(v[8 * a + 2 * i + 1]));
+                            w4[i] = *reinterpret_cast<uint32_t*>(&b2);
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(yrow + 32 * c);
+                        pc[a] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    transpose4_pieces(pc, lane);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = rbase + j;  // token row within the tile
+                        if (r < T.n_valid)
+                            *reinterpret_cast<uint4*>(args.y_perm + ((size_t)T.y_row + r) * d + (size_t)T.p * 256 +
+                                                      32 * c + 8 * piece) = pc[j];
                     }
                 }
             }
