@@ -35,7 +35,8 @@
 //             (tcgen05.cp) and issues the MMAs (one elected lane); tcgen05.commit frees stages
 //             and publishes the accumulator;
 //   warps 2-9 epilogue: two warps per tensor-memory lane quarter (32 token rows), each taking
-//             half of the accumulator columns, so that it is drained (and the MMAs resume) soon.
+//             half of the accumulator columns into registers and freeing tensor memory at once,
+//             then converting and storing them while the next tile's MMAs run.
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
 #include "common.cuh"
@@ -436,46 +437,55 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
             if (!mbar_wait(&acc_full[buf], use & 1, abort_flag, args.status)) break;
             tc_fence_after();
             const uint32_t acc = tmem + lane_base + (uint32_t)(buf * kAccCols);
+            // Copy this warp's 128 accumulator columns to registers and free tensor memory at once,
+            // so that the next tile's MMAs run while these values are converted and stored.
+            uint32_t v[4][32];
+            if (IS_UP) {  // g and u of chunks 2*half, 2*half + 1
+                tmem_ld32(acc + 32 * (2 * half), v[0]);
+                tmem_ld32(acc + 32 * (2 * half + 1), v[1]);
+                tmem_ld32(acc + 128 + 32 * (2 * half), v[2]);
+                tmem_ld32(acc + 128 + 32 * (2 * half + 1), v[3]);
+            } else {  // chunks 4*half .. 4*half + 3
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(acc + 32 * (4 * half + c), v[c]);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
             if (IS_UP) {
                 const int I = args.n_out;
                 const size_t row = (size_t)T.a_row + m;  // every padded row is written (zeros there)
-#pragma unroll 1
-                for (int c = 2 * half; c < 2 * half + 2; ++c) {
-                    uint32_t g[32], u[32];
-                    tmem_ld32(acc + 32 * c, g);
-                    tmem_ld32(acc + 128 + 32 * c, u);
-                    tmem_ld_wait();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float gv = __uint_as_float(g[i]), uv = __uint_as_float(u[i]);
+                        const float gv = __uint_as_float(v[cc][i]), uv = __uint_as_float(v[2 + cc][i]);
                         hv[i] = __fdividef(gv, 1.f + __expf(-gv)) * uv;  // SiLU(g) * u
                     }
                     uint4 codes;
                     const uint32_t sb = mx_block_encode(hv, codes);
-                    const int blk = 4 * T.p + c;  // 32-block of h along I
+                    const int blk = 4 * T.p + 2 * half + cc;  // 32-block of h along I
                     *reinterpret_cast<uint4*>(args.h + mma_tile_offset((int64_t)row, blk, I)) = codes;
                     args.h_s[mma_scale_offset((int64_t)row, blk, I)] = (uint8_t)sb;
                 }
             } else {
-                // Each thread holds 32 columns (64 bytes) of its own token row; after a 4 x 4
-                // transpose of 16-byte pieces inside groups of four lanes, store j writes 64
+                // Each thread holds 32 columns (64 bytes) of its own token row per chunk; after a
+                // 4 x 4 transpose of 16-byte pieces inside groups of four lanes, store j writes 64
                 // contiguous bytes of 8 rows (row 4g + j of each group) instead of 16 bytes of 32.
                 const int d = args.n_out;
                 const int rbase = 32 * q + 4 * (lane >> 2), piece = lane & 3;
-#pragma unroll 1
-                for (int c = 4 * half; c < 4 * half + 4; ++c) {
-                    uint32_t v[32];
-                    tmem_ld32(acc + 32 * c, v);
-                    tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
                     uint4 pc[4];
 #pragma unroll
                     for (int a = 0; a < 4; ++a) {
                         uint32_t w4[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * a + 2 * i]),
-                                                                      __uint_as_float(v[8 * a + 2 * i + 1]));
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c][8 * a + 2 * i]),
+                                                                      __uint_as_float(v[c][8 * a + 2 * i + 1]));
                             w4[i] = *reinterpret_cast<uint32_t*>(&b2);
                         }
                         pc[a] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -486,13 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                         const int r = rbase + j;  // token row within the tile
                         if (r < T.n_valid)
                             *reinterpret_cast<uint4*>(args.y_perm + ((size_t)T.y_row + r) * d + (size_t)T.p * 256 +
-                                                      32 * c + 8 * piece) = pc[j];
+                                                      32 * (4 * half + c) + 8 * piece) = pc[j];
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
     }
 
