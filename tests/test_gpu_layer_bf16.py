@@ -15,11 +15,18 @@ pytestmark = pytest.mark.gpu
 _layers = {}
 
 
+# Shapes on the warp-ring GEMVs (d and I multiples of 512) with several tokens per expert.
+SMALL = {
+    "ring_t3": IN.small_config("ring_t3", T=3, d=1024, E=12, k=4, I=512, index=93),
+    "ring_t2": IN.small_config("ring_t2", T=2, d=2048, E=6, k=3, I=1536, index=94),
+}
+
+
 def get_layer(name):
     if name not in _layers:
         _layers.clear()
         torch.cuda.empty_cache()
-        _layers[name] = DeviceLayer(IN.CONFIGS[name])
+        _layers[name] = DeviceLayer(SMALL[name] if name in SMALL else IN.CONFIGS[name])
     return _layers[name]
 
 
@@ -29,7 +36,8 @@ def oracle_layer(layer, xb, act_fmt, tokens=None):
                        tokens=tokens)
 
 
-@pytest.mark.parametrize("name,calls", [("tiny", [0, 1]), ("decode", [0, 1, 2]), ("spec_verify", [0])])
+@pytest.mark.parametrize("name,calls", [("tiny", [0, 1]), ("decode", [0, 1, 2]), ("spec_verify", [0]),
+                                        ("ring_t3", [0, 1]), ("ring_t2", [0, 1])])
 def test_layer_matches_oracle(name, calls):
     layer = get_layer(name)
     cfg = layer.cfg
@@ -44,8 +52,9 @@ def test_layer_matches_oracle(name, calls):
     assert B.moe_get_device_status(ws) == B.MOE_OK
 
 
-def test_step_calls_equal_layer_call_and_oracle_h():
-    layer = get_layer("tiny")
+@pytest.mark.parametrize("name", ["tiny", "ring_t3"])
+def test_step_calls_equal_layer_call_and_oracle_h(name):
+    layer = get_layer(name)
     cfg = layer.cfg
     T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
     P = T * k
