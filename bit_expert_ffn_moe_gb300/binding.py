@@ -29,7 +29,7 @@ EXPORTED = (
     "moe_status_string", "moe_abi_version", "moe_last_cuda_error", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
     "moe_mxfp4_scales_to_mma", "moe_mxfp4_codes_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
-    "moe_layer_forward", "moe_synth_weights",
+    "moe_layer_forward", "moe_synth_weights", "moe_selftest_wait_timeout",
 )
 
 
@@ -75,6 +75,7 @@ _SIGS = {
     "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
     "moe_layer_forward": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, SZ, P]),
     "moe_synth_weights": (I32, [U64, U32, U32, U32, I64, I64, ctypes.c_float, P, P]),
+    "moe_selftest_wait_timeout": (I32, [P, SZ, I32, P]),
 }
 
 
@@ -231,3 +232,8 @@ def moe_layer_forward(x, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, y, i
 def moe_synth_weights(seed, tensor_id, expert_first, n_experts, rows, K, c, out, stream=None):
     _check("moe_synth_weights", load().moe_synth_weights(seed, tensor_id, expert_first, n_experts, rows, K,
                                                          float(c), _p(out), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(ws, limit_us, ws_bytes=None, stream=None):
+    n = ws.numel() * ws.element_size() if ws_bytes is None else ws_bytes
+    _check("moe_selftest_wait_timeout", load().moe_selftest_wait_timeout(_p(ws), n, int(limit_us), _stream(stream)))

@@ -233,6 +233,15 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
                              int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids,
                              float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* ---------------------------------------------------------------- failure-detection self-test
+ * Not part of the layer.  Every barrier wait in the library's kernels is bounded: when it runs out
+ * the kernel records MOE_ERR_TIMEOUT in the workspace status word and finishes, so a lost copy or
+ * signal is reported by moe_get_device_status instead of hanging the GPU.  This call runs that
+ * path on purpose: one kernel thread waits up to limit_us microseconds (1 .. 1000000) on an
+ * mbarrier phase that nothing completes, then records MOE_ERR_TIMEOUT and returns normally.  The
+ * CUDA context stays usable.  ws: an initialised workspace (only its control block is used). */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int limit_us, moe_stream_t stream);
+
 /* ---------------------------------------------------------------- synthetic inputs
  * Not part of the layer: the counter-based generator that benchmarks and tests use to create
  * expert weights on the device.  Element n (row-major) of expert `e`'s matrix [rows][K] is

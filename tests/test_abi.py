@@ -59,3 +59,10 @@ def test_library_is_built_for_sm103a_only():
     from bit_expert_ffn_moe_gb300 import _build
     assert "arch=compute_103a,code=sm_103a" in _build.NVCC_FLAGS
     assert os.path.exists(_build.LIB)
+
+
+def test_selftest_arguments_are_checked_on_the_host(lib):
+    # rejected before anything is launched (no GPU needed)
+    assert lib.moe_selftest_wait_timeout(None, 0, 10, None) == B.MOE_ERR_WORKSPACE
+    assert lib.moe_selftest_wait_timeout(256, 1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_selftest_wait_timeout(256, 1 << 20, 2000000, None) == B.MOE_ERR_INVALID_ARG
