@@ -188,6 +188,14 @@ moe_status moe_route(const uint16_t* x, const float* W_r, const float* b, int T,
     const WsLayout L = ws_layout(T, d, E, k, 32, MOE_ACT_BF16);
     MOE_TRY(check_ws(ws, ws_bytes, L));
     MOE_TRY(check_device());
+    if (route_decode_supported(T, d, E, k)) {  // few tokens: the one-launch router (its plan goes to ws)
+        return from_cuda(launch_route_decode(
+            x, W_r, b, T, d, E, k, reinterpret_cast<float*>(at(ws, L.logits)), ids, w,
+            reinterpret_cast<int32_t*>(at(ws, L.counts)), reinterpret_cast<int32_t*>(at(ws, L.offsets)),
+            reinterpret_cast<int32_t*>(at(ws, L.perm)), reinterpret_cast<int32_t*>(at(ws, L.inv)),
+            reinterpret_cast<float*>(at(ws, L.row_w)), plan_view(ws, L, E), reinterpret_cast<Ctrl*>(at(ws, L.ctrl)),
+            (cudaStream_t)stream, false));
+    }
     return run_route(x, W_r, b, T, d, E, k, ids, w, ws, L, (cudaStream_t)stream, false);
 }
 

@@ -453,34 +453,35 @@ __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks
 }
 
 // One thread per (padded row, 32-element block).
-__global__ void act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, int d, int E,
-                                  int64_t pad_rows, const int32_t* __restrict__ offsets,
-                                  const int32_t* __restrict__ perm_token, PlanView plan, uint8_t* __restrict__ xa,
-                                  uint8_t* __restrict__ xa_s) {
+// One warp per padded row: the row's expert comes from a binary search over the padded offsets
+// cached in shared memory; lanes copy consecutive 16-byte blocks of the token's quantised row
+// into the tensor-core code tiles (8 lanes fill one 128-byte line) and write its scale bytes.
+__global__ void __launch_bounds__(256)
+act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, int d, int E, int64_t pad_rows,
+                  const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_token, PlanView plan,
+                  uint8_t* __restrict__ xa, uint8_t* __restrict__ xa_s) {
+    extern __shared__ int32_t s_pad[];  // [E+1]
     pdl_wait();
-    const int nb = d / 32;
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_pad[i] = plan.pad_offsets[i];
+    __syncthreads();
+    const int nb = d / 32, lane = threadIdx.x & 31;
     const int64_t used = plan.scalars[2];
-    const int64_t total = used * nb;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const int64_t r = i / nb;
-        const int blk = (int)(i % nb);
-        // expert of padded row r: last e with pad_offsets[e] <= r
-        int lo = 0, hi = E;  // invariant pad_offsets[lo] <= r < pad_offsets[hi]
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < used; r += nwarps) {
+        int lo = 0, hi = E;  // expert of padded row r: last e with s_pad[e] <= r
         while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (plan.pad_offsets[mid] <= r) lo = mid; else hi = mid;
+            const int mid = (lo + hi) >> 1;
+            if (s_pad[mid] <= r) lo = mid; else hi = mid;
         }
-        const int64_t local = r - plan.pad_offsets[lo];
-        uint4 v = make_uint4(0, 0, 0, 0);
-        uint8_t sb = 0;
-        if (local < plan.counts[lo]) {
-            const int t = perm_token[offsets[lo] + local];
-            v = reinterpret_cast<const uint4*>(xq)[(size_t)t * nb + blk];
-            sb = xs[(size_t)t * nb + blk];
+        const int64_t local = r - s_pad[lo];
+        const bool real = local < plan.counts[lo];
+        const int t = real ? perm_token[offsets[lo] + local] : 0;
+        const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (d / 2));
+        for (int blk = lane; blk < nb; blk += 32) {
+            const uint4 v = real ? src[blk] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(xa + mma_tile_offset(r, blk, d)) = v;
+            xa_s[mma_scale_offset(r, blk, d)] = real ? xs[(size_t)t * nb + blk] : (uint8_t)0;
         }
-        *reinterpret_cast<uint4*>(xa + mma_tile_offset(r, blk, d)) = v;
-        xa_s[mma_scale_offset(r, blk, d)] = sb;
     }
     (void)pad_rows;
 }
@@ -497,12 +498,12 @@ cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int 
         cudaError_t err = launch_kernel((const void*)act_quant_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
         if (err != cudaSuccess) return err;
     }
-    int64_t tot = pad_rows * (d / 32);
-    if (tot == 0) return cudaSuccess;
-    int64_t blocks = (tot + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (pad_rows == 0) return cudaSuccess;
+    int64_t blocks = (pad_rows + 7) / 8;  // 8 warps (rows) per CTA
+    if (blocks > 152 * 8) blocks = 152 * 8;
     void* a2[] = {&xq, &xs, &d, &E, &pad_rows, &offsets, &perm_token, &plan, &xa, &xa_s};
-    return launch_kernel((const void*)act_gather_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a2);
+    return launch_kernel((const void*)act_gather_kernel, dim3((unsigned)blocks), dim3(256),
+                         sizeof(int32_t) * (size_t)(E + 1), st, pdl, a2);
 }
 
 }  // namespace moe
