@@ -313,16 +313,32 @@ def run_gpu(args, cfg, rank, world, local):
                    "l2": "inputs larger than L2: %d layer copies, %.1f GB of expert weights rotated"
                          % (len(layers), len(layers) * E * expert_bytes(d, I) / 1e9),
                    "cuda_graph": graph is not None, "parallelism": "replicas" if world > 1 else "single GPU"},
-        "layer_roofline": {"bound": "hbm", "algorithmic_bytes_per_step": layer_bytes,
-                           "achieved_GBps": round(layer_bytes / (ms_per_step / 1e3) / 1e9, 1),
-                           "peak_GBps": pk["hbm_gbs"], "frac": round(layer_bytes / (ms_per_step / 1e3) / bw, 4),
-                           "peak_source": pk["source"], "mean_active_experts": round(mean_active, 2)},
+        "layer_roofline": layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, world),
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": launches_per_step(fmt, T, d, E, k) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
     }
+    return out
+
+
+def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, world):
+    """Whole-layer fraction of the roofline the workload is quoted against: HBM bytes for the
+    decode path; for the prefill path the FP4 tensor peak (useful flops 6 P d I per step), with
+    the HBM fraction beside it."""
+    out = {"bound": "hbm", "algorithmic_bytes_per_step": layer_bytes,
+           "achieved_GBps": round(layer_bytes / (ms_per_step / 1e3) / 1e9, 1),
+           "peak_GBps": pk["hbm_gbs"], "frac": round(layer_bytes / (ms_per_step / 1e3) / bw, 4),
+           "peak_source": pk["source"], "mean_active_experts": round(mean_active, 2)}
+    if fmt != 0:
+        flops = 6.0 * cfg.T * cfg.k * cfg.d * cfg.I * world
+        peak_tf = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16 * world
+        achieved = flops / (ms_per_step / 1e3) / 1e12
+        out = {"bound": "tensor", "algorithmic_flops_per_step": flops, "achieved_TFLOPs": round(achieved, 1),
+               "peak_TFLOPs": round(peak_tf, 1), "frac": round(achieved / peak_tf, 4),
+               "peak_source": pk["source"] + " bf16 x %.0f (nominal FP4 : bf16 dense ratio)" % NOMINAL_FP4_OVER_BF16,
+               "hbm": out}
     return out
 
 
@@ -359,7 +375,7 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     active = []
     if fmt != B.MOE_ACT_BF16:
-        return None
+        return kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n)
     st = stream.cuda_stream
     with torch.cuda.stream(stream):
         for s in range(n + 3):
@@ -387,6 +403,64 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
             "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": per_launch, "avg_launch_us": round(avg_ms * 1e3, 3),
             "launches_timed": n, "peak_source": pk["source"] + " (HBM copy bandwidth)"}
+
+
+def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
+    """Prefill path: the tcgen05 gate/up kernel (umma_grouped_kernel<1>) timed with CUDA events
+    on its stream through the step API, against the dense FP4 tensor peak (the measured or
+    fallback bf16 peak times the nominal FP4 : bf16 ratio); its HBM rate is reported beside."""
+    import numpy as np
+    import torch
+
+    from bit_expert_ffn_moe_gb300 import binding as B
+    from bit_expert_ffn_moe_gb300.layer import make_workspace
+
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    P = T * k
+    R = B.moe_padded_rows(T, k, E)
+    ws = make_workspace(T, d, E, k, I, fmt, dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    ids, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts, offsets, perm, inv = torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(P, **i32), \
+        torch.empty(P, **i32)
+    xa, xa_s = torch.empty(R * d // 2, **u8), torch.empty(B.moe_mxfp4_mma_scale_bytes(R, d), **u8)
+    h, h_s = torch.empty(R * I // 2, **u8), torch.empty(B.moe_mxfp4_mma_scale_bytes(R, I), **u8)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    active = []
+    st = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for s in range(n + 3):
+            L = layers[s % len(layers)]
+            x = xs[s % xs.shape[0]]
+            B.moe_route(x, L.W_r, L.b, T, d, E, k, ids, w, ws, stream=st)
+            B.moe_permute(x, ids, T, d, E, k, fmt, counts, offsets, perm, inv, xa, xa_s, ws, stream=st)
+            if s >= 3:
+                evs[s - 3][0].record(stream)
+            B.moe_expert_up_swiglu(None, xa, xa_s, fmt, perm, offsets, T, d, E, k, I, L.weights, h, h_s, ws,
+                                   stream=st)
+            if s >= 3:
+                evs[s - 3][1].record(stream)
+                active.append(torch.count_nonzero(counts))
+    stream.synchronize()
+    if B.moe_get_device_status(ws) != B.MOE_OK:
+        raise RuntimeError("device-side error in the prefill roofline loop")
+    avg_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    n_act = float(np.mean([int(a.item()) for a in active]))
+    flops = 4.0 * P * d * I  # gate and up: 2 flops per weight per token row
+    achieved = flops / (avg_ms / 1e3) / 1e12
+    peak_tf = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+    hbm_bytes = n_act * up_bytes_per_expert(d, I) + P * (d * 17 // 32) + P * (I * 17 // 32)
+    traffic = ncu_traffic("umma_grouped_prefill.md", ["bit_expert_ffn_moe_gb300/csrc/umma.cu",
+                                                      "bit_expert_ffn_moe_gb300/csrc/common.cuh"])
+    return {"kernel": "umma_grouped_kernel<1> (tcgen05 kind::mxf4 gate/up + SwiGLU, prefill)", "bound": "tensor",
+            "achieved": round(achieved, 1), "peak": round(peak_tf, 1), "unit": "TFLOP/s",
+            "frac": round(achieved / peak_tf, 4), "traffic": traffic,
+            "algorithmic_flops_per_launch": flops, "avg_launch_us": round(avg_ms * 1e3, 3), "launches_timed": n,
+            "hbm_achieved_GBps": round(hbm_bytes / (avg_ms / 1e3) / 1e9, 1),
+            "hbm_frac": round(hbm_bytes / (avg_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+            "algorithmic_bytes_per_launch": hbm_bytes,
+            "peak_source": pk["source"] + " bf16 x %.0f (nominal FP4 : bf16 dense ratio)" % NOMINAL_FP4_OVER_BF16}
 
 
 def end_to_end(args, cfg, layers, xs_host, fmt, dev, stream):
