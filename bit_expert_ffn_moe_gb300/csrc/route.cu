@@ -244,6 +244,18 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
 
+// Two independent fp32 fmas (round to nearest each) on packed pairs: (a.x*b.x + c.x, a.y*b.y + c.y).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 __global__ void __launch_bounds__(kLThreads, 2)
 route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ b,
                           int T, int d, int E, float* __restrict__ logits) {
@@ -270,11 +282,13 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
             cp_async16(wd + r * kLKC + 4 * c, ok ? W_r + (size_t)(e0 + r) * d + k0 + 4 * c : W_r, ok);
         }
     };
-    float acc[8][8];
+    // acc[p][c] = partial sums of tokens wt + 2p (x) and wt + 2p + 1 (y) against expert we + c;
+    // each is the same sequential fma chain as a scalar accumulator, two per instruction.
+    float2 acc[4][8];
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int p = 0; p < 4; ++p)
 #pragma unroll
-        for (int c = 0; c < 8; ++c) acc[a][c] = 0.f;
+        for (int c = 0; c < 8; ++c) acc[p][c] = make_float2(0.f, 0.f);
 
     pdl_wait();
 #pragma unroll
@@ -294,15 +308,17 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
         for (int gi = 0; gi < 2; ++gi) {
             if (k0 + 128 * gi >= d) break;  // d % 128 == 0: a group of 32 lanes is all in or all out
             const int g = lane + 32 * gi;
-            float xv[8][4], wv[8][4];
+            float2 xv[4][4];  // [token pair][element of the group]
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                const uint2 u = *reinterpret_cast<const uint2*>(xc + (wt + a) * kLKC + 4 * g);
-                xv[a][0] = bf16_bits_to_f32(u.x & 0xFFFF);
-                xv[a][1] = bf16_bits_to_f32(u.x >> 16);
-                xv[a][2] = bf16_bits_to_f32(u.y & 0xFFFF);
-                xv[a][3] = bf16_bits_to_f32(u.y >> 16);
+            for (int p = 0; p < 4; ++p) {
+                const uint2 u0 = *reinterpret_cast<const uint2*>(xc + (wt + 2 * p) * kLKC + 4 * g);
+                const uint2 u1 = *reinterpret_cast<const uint2*>(xc + (wt + 2 * p + 1) * kLKC + 4 * g);
+                xv[p][0] = make_float2(bf16_bits_to_f32(u0.x & 0xFFFF), bf16_bits_to_f32(u1.x & 0xFFFF));
+                xv[p][1] = make_float2(bf16_bits_to_f32(u0.x >> 16), bf16_bits_to_f32(u1.x >> 16));
+                xv[p][2] = make_float2(bf16_bits_to_f32(u0.y & 0xFFFF), bf16_bits_to_f32(u1.y & 0xFFFF));
+                xv[p][3] = make_float2(bf16_bits_to_f32(u0.y >> 16), bf16_bits_to_f32(u1.y >> 16));
             }
+            float wv[8][4];
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 const float4 f = *reinterpret_cast<const float4*>(wc + (we + c) * kLKC + 4 * g);
@@ -314,9 +330,11 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int a = 0; a < 8; ++a)
+                for (int c = 0; c < 8; ++c) {
+                    const float2 wq = make_float2(wv[c][q], wv[c][q]);
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) acc[a][c] = fmaf(xv[a][q], wv[c][q], acc[a][c]);
+                    for (int p = 0; p < 4; ++p) acc[p][c] = fma2(xv[p][q], wq, acc[p][c]);
+                }
         }
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -324,7 +342,7 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
     for (int a = 0; a < 8; ++a)
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-            float s = warp_butterfly_sum(acc[a][c]);
+            float s = warp_butterfly_sum((a & 1) ? acc[a >> 1][c].y : acc[a >> 1][c].x);
             int t = t0 + wt + a, e = e0 + we + c;
             if (lane == ((a * 8 + c) & 31) && t < T && e < E) logits[(size_t)t * E + e] = s + (b ? b[e] : 0.f);
         }
