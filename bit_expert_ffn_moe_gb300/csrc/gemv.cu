@@ -510,7 +510,6 @@ gemv_down_kernel(const GemvArgs a) {
         __syncthreads();
     }
     const int nrows = s_cnt;
-    stage_rows_f16(a.act, s_row, nrows, a.K, hs, inv, smax);
 
     auto load_rows = [&](int e, uint4 (&wv)[RPW][BPL], uint32_t (&sv)[RPW][BPL]) {
 #pragma unroll
@@ -529,7 +528,8 @@ gemv_down_kernel(const GemvArgs a) {
     uint4 wcur[RPW][BPL], wnxt[RPW][BPL];
     uint32_t scur[RPW][BPL], snxt[RPW][BPL];
     int qs = 0;
-    if (nrows > 0) load_rows(s_exp[0], wcur, scur);
+    if (nrows > 0) load_rows(s_exp[0], wcur, scur);  // in flight while h is staged
+    stage_rows_f16(a.act, s_row, nrows, a.K, hs, inv, smax);
     while (qs < nrows) {
         const int e = s_exp[qs];
         int qe = qs + 1;
