@@ -362,8 +362,9 @@ gemv_up_cta_kernel(const GemvArgs a) {
     const CtaGeo geo = make_cta_geo(a.K);
     uint4* xs = reinterpret_cast<uint4*>(smem);                              // [Q][K/8]
     float* inv = reinterpret_cast<float*>(smem + (size_t)Q * a.K * 2);      // [Q]
-    float* red = inv + Q;                                                   // [8 warps][32]
-    int* rows = reinterpret_cast<int*>(red + 8 * 32);                       // [Q]
+    float* red = inv + Q;                                                   // [2][8 warps][32]
+    int* rows = reinterpret_cast<int*>(red + 2 * 8 * 32);                   // [Q]
+    unsigned* smax = reinterpret_cast<unsigned*>(rows + Q);                 // [Q]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = tid / geo.G, gl = tid % geo.G;
     const int wpg = geo.G / 32;  // warps per group
@@ -397,8 +398,7 @@ gemv_up_cta_kernel(const GemvArgs a) {
         __syncthreads();
         if (tid < nq) rows[tid] = a.perm_token[r0 + tc0 + tid];
         __syncthreads();
-        stage_rows_warp(a.act, rows, nq, a.K, xs, inv);
-        __syncthreads();
+        stage_rows_f16(a.act, rows, nq, a.K, xs, inv, smax);  // all warps; ends with a barrier
         for (int bi = 0; bi < nbatch; ++bi) {
             const bool more = bi + 1 < nbatch || tc0 + Q < n;
             if (more) {
@@ -408,7 +408,10 @@ gemv_up_cta_kernel(const GemvArgs a) {
             }
             float acc[V];
             batch_dots<BPT, Q>(xs, 0, nq, gl, geo, wcur, scur, acc);
-            red[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
+            // partial sums go to alternating halves of red, so one barrier per batch suffices: the
+            // leader warp finishes batch bi's features while the others compute batch bi + 1
+            float* rb = red + (bi & 1) * (8 * 32);
+            rb[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
             __syncthreads();
             if (gl < 32) {
                 // lane l holds value v = l >> (5 - log2 V); v = qq * kR + j
@@ -419,8 +422,8 @@ gemv_up_cta_kernel(const GemvArgs a) {
                     float g = 0.f, u = 0.f;
                     for (int w = 0; w < wpg; ++w) {
                         const int wi = (grp * wpg + w) * 32;
-                        g += red[wi + lane];
-                        u += red[wi + lane + kOut * (32 / V)];
+                        g += rb[wi + lane];
+                        u += rb[wi + lane + kOut * (32 / V)];
                     }
                     g *= inv[qq];
                     u *= inv[qq];
@@ -429,7 +432,6 @@ gemv_up_cta_kernel(const GemvArgs a) {
                     a.out[(size_t)(r0 + tc0 + qq) * a.M_exp + i] = f32_to_bf16_bits(hv);
                 }
             }
-            __syncthreads();
             if (more) {
 #pragma unroll
                 for (int j = 0; j < kR; ++j)
@@ -655,7 +657,7 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
         a.outs = outs;
         a.out = h;
         const int Q = T;
-        const size_t smem = (size_t)Q * d * 2 + sizeof(float) * (Q + 8 * 32) + sizeof(int) * Q;
+        const size_t smem = (size_t)Q * d * 2 + sizeof(float) * (Q + 2 * 8 * 32) + sizeof(int) * Q + sizeof(unsigned) * Q;
         void* args[] = {&a};
         const dim3 grid(I / outs, P < E ? P : E);
         const void* f;
