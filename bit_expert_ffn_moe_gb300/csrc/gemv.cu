@@ -446,6 +446,106 @@ gemv_up_cta_kernel(const GemvArgs a) {
     pdl_launch_dependents();
 }
 
+// ------------------------------------------------------------------ down (+ weighted sum), T <= 2
+// Same CTA-wide split of K as the gate/up kernel above.  A CTA owns RG * kR output features; row
+// group g takes features n0 + kR*g .. + kR - 1 and a batch is those kR rows of one active expert,
+// so batches walk the experts in ascending order, i.e. each token's slot order.  Every thread
+// owns one K-block of every row; the expert's h rows (at most Q) are staged once as prescaled f16.
+// FUSED: ys[t][f] accumulates w * bf16(expert output) batch after batch (the same lane updates a
+// given (t, f) in expert order); otherwise the bf16 outputs go to y_perm.
+template <int Q, bool FUSED>
+__global__ void __launch_bounds__(kThr, 2)
+gemv_down_cta_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int V = kR * Q;
+    const CtaGeo geo = make_cta_geo(a.K);
+    const int P = a.P, feats = geo.RG * kR;
+    uint4* hs = reinterpret_cast<uint4*>(smem);                              // [P][K/8]
+    float* inv = reinterpret_cast<float*>(smem + (size_t)P * a.K * 2);      // [P]
+    float* red = inv + P;                                                   // [2][8 warps][32]
+    float* ys = red + 2 * 8 * 32;                                           // [Q][feats]
+    int* rows = reinterpret_cast<int*>(ys + (size_t)Q * feats);             // [P]
+    unsigned* smax = reinterpret_cast<unsigned*>(rows + P);                 // [P]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int grp = tid / geo.G, gl = tid % geo.G;
+    const int wpg = geo.G / 32;
+    const size_t row_bytes = (size_t)a.K / 2;
+    const int n0 = blockIdx.x * feats + grp * kR;  // this group's first feature
+
+    pdl_wait();
+    const int n_act = a.plan.scalars[0];
+    auto load = [&](int u, uint4 (&wv)[kR], uint32_t (&sv)[kR]) {
+        const size_t g0 = (size_t)a.plan.active[u] * a.M_exp + n0;
+#pragma unroll
+        for (int j = 0; j < kR; ++j)
+            if (gl < geo.nb) {
+                wv[j] = ldg_stream(a.q0 + (g0 + j) * row_bytes + 16 * (size_t)gl);
+                sv[j] = __ldg(a.s0 + (g0 + j) * geo.nb + gl);
+            }
+    };
+    uint4 wcur[kR], wnxt[kR];
+    uint32_t scur[kR], snxt[kR];
+    if (n_act > 0) load(0, wcur, scur);  // in flight while h is staged
+    for (int i = tid; i < P; i += blockDim.x) rows[i] = i;
+    for (int i = tid; i < Q * feats; i += blockDim.x) ys[i] = 0.f;
+    __syncthreads();
+    stage_rows_f16(a.act, rows, P, a.K, hs, inv, smax);  // ends with a barrier
+
+    for (int u = 0; u < n_act; ++u) {
+        const int e = a.plan.active[u];
+        const int r0 = a.offsets[e], cnt = min(Q, a.offsets[e + 1] - r0);
+        if (u + 1 < n_act) load(u + 1, wnxt, snxt);
+        float acc[V];
+#pragma unroll
+        for (int v = 0; v < V; ++v) acc[v] = 0.f;
+        if (gl < geo.nb) {
+#pragma unroll
+            for (int qq = 0; qq < Q; ++qq) {
+                if (qq < cnt) {
+                    uint32_t x[16];
+                    load_x_block(hs, r0 + qq, geo.nb, gl, x);
+#pragma unroll
+                    for (int j = 0; j < kR; ++j)
+                        acc[qq * kR + j] = block_dot(wcur[j], x) * e8m0_to_f32(scur[j]);
+                }
+            }
+        }
+        float* rb = red + (u & 1) * (8 * 32);
+        rb[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
+        __syncthreads();
+        if (gl < 32) {
+            const int v = lane >> (5 - (V == 8 ? 3 : V == 16 ? 4 : 5));
+            const int qq = v / kR, j = v % kR;
+            const bool leader = (lane & ((32 / V) - 1)) == 0;
+            if (leader && qq < cnt) {
+                float o = 0.f;
+                for (int w = 0; w < wpg; ++w) o += rb[(grp * wpg + w) * 32 + lane];
+                const uint16_t ob = f32_to_bf16_bits(o * inv[r0 + qq]);
+                if (FUSED) {
+                    const int t = a.perm_token[r0 + qq];
+                    float& yv = ys[t * feats + grp * kR + j];
+                    yv = fmaf(a.row_w[r0 + qq], bf16_bits_to_f32(ob), yv);
+                } else {
+                    a.out[(size_t)(r0 + qq) * a.M_exp + n0 + j] = ob;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kR; ++j) {
+            wcur[j] = wnxt[j];
+            scur[j] = snxt[j];
+        }
+    }
+    if (FUSED) {
+        __syncthreads();
+        for (int i = tid; i < a.T * feats; i += blockDim.x) {
+            const int t = i / feats, f = i % feats;
+            a.out[(size_t)t * a.M_exp + blockIdx.x * feats + f] = f32_to_bf16_bits(ys[i]);
+        }
+    }
+    pdl_launch_dependents();
+}
+
 // ------------------------------------------------------------------ down (+ weighted sum)
 // Grid (d / outs, token chunks).  The CTA stages every permuted row whose token lies in its chunk
 // (rows are expert-major, so each active expert forms a consecutive segment).  Warp w owns rows
@@ -701,6 +801,32 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
                              const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
                              uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
+    const CtaGeo dgeo = make_cta_geo(I);
+    const int P = T * k;
+    const size_t cta_smem = (size_t)P * I * 2 + sizeof(float) * (P + 2 * 8 * 32 + (size_t)T * dgeo.RG * kR) +
+                            sizeof(int) * P + sizeof(unsigned) * P;
+    if (T <= 2 && dgeo.bpt == 1 && d % (dgeo.RG * kR) == 0 && cta_smem <= 100 * 1024) {
+        // one or two tokens: CTA-split of K (see gemv_down_cta_kernel)
+        GemvArgs a = {};
+        a.q0 = W->down_q;
+        a.s0 = W->down_s;
+        a.act = h;
+        a.perm_token = perm_token;
+        a.offsets = offsets;
+        a.plan = plan;
+        a.row_w = row_w;
+        a.T = T;
+        a.K = I;
+        a.M_exp = d;
+        a.P = P;
+        a.E = E;
+        a.out = y ? y : y_perm;
+        void* args[] = {&a};
+        const dim3 grid(d / (dgeo.RG * kR));
+        const void* f = T == 1 ? (y ? (const void*)gemv_down_cta_kernel<1, true> : (const void*)gemv_down_cta_kernel<1, false>)
+                               : (y ? (const void*)gemv_down_cta_kernel<2, true> : (const void*)gemv_down_cta_kernel<2, false>);
+        return launch_kernel(f, grid, dim3(kThr), cta_smem, st, pdl, args);
+    }
     const int bpl = bpl_for(I);
     const int outs = kWarps * down_rows_per_warp(bpl);
     if (bpl == 0 || d % outs != 0) return cudaErrorInvalidValue;
