@@ -156,19 +156,20 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(profile_name: str, kernel_sources):
+def ncu_traffic(profile_name: str, kernel_sources, workload: str):
     """dram bytes per launch recorded in profiles/<profile_name> for the kernel, or None when
-    the summary is missing or the kernel's sources changed since the capture."""
+    the summary is missing, was captured on another workload, or the kernel's sources changed
+    since the capture."""
     path = os.path.join(ROOT, "profiles", profile_name)
     if not os.path.exists(path):
         return None
     vals = {}
     with open(path) as f:
         for line in f:
-            if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch")):
+            if ":" in line and line.strip().startswith(("source_hash", "dram_bytes_per_launch", "workload")):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_hash") != source_hash(kernel_sources):
+    if vals.get("source_hash") != source_hash(kernel_sources) or vals.get("workload") != workload:
         return None
     try:
         return float(vals["dram_bytes_per_launch"])
@@ -397,7 +398,7 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
     avg_ms = float(np.mean(dur))
     achieved = per_launch / (avg_ms / 1e3) / 1e9
     traffic = ncu_traffic("gemv_up_decode.md", ["bit_expert_ffn_moe_gb300/csrc/gemv.cu",
-                                                "bit_expert_ffn_moe_gb300/csrc/common.cuh"])
+                                                "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
     return {"kernel": "gemv_up_kernel (gate/up + SwiGLU, decode)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
@@ -452,7 +453,7 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     peak_tf = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
     hbm_bytes = n_act * up_bytes_per_expert(d, I) + P * (d * 17 // 32) + P * (I * 17 // 32)
     traffic = ncu_traffic("umma_grouped_prefill.md", ["bit_expert_ffn_moe_gb300/csrc/umma.cu",
-                                                      "bit_expert_ffn_moe_gb300/csrc/common.cuh"])
+                                                      "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
     return {"kernel": "umma_grouped_kernel<1> (tcgen05 kind::mxf4 gate/up + SwiGLU, prefill)", "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(peak_tf, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak_tf, 4), "traffic": traffic,

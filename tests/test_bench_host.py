@@ -77,3 +77,11 @@ def test_replica_timing_takes_the_max_over_gloo_ranks():
     res = sorted(q.get(timeout=5) for _ in range(2))
     assert [r[0] for r in res] == [0, 1] and all(r[1] == 2 for r in res)
     assert all(r[3] == 11.0 for r in res)
+
+
+def test_recorded_traffic_only_for_its_workload_and_sources():
+    import bench
+    src = ["bit_expert_ffn_moe_gb300/csrc/umma.cu", "bit_expert_ffn_moe_gb300/csrc/common.cuh"]
+    assert bench.ncu_traffic("no_such_profile.md", src, "prefill") is None
+    assert bench.ncu_traffic("umma_grouped_prefill.md", src, "long_prefill") is None
+    assert bench.ncu_traffic("umma_grouped_prefill.md", src[:1], "prefill") is None  # other sources
