@@ -257,14 +257,14 @@ moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, c
     MOE_TRY(check_device());
     cudaStream_t st = (cudaStream_t)stream;
     PlanView plan = plan_view(ws, L, E);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
     if (fmt == MOE_ACT_BF16) {
         if (!perm_token) return MOE_ERR_INVALID_ARG;
         if (!gemv_supported(d, I)) return MOE_ERR_UNSUPPORTED_SHAPE;
         return from_cuda(launch_gemv_down(static_cast<const uint16_t*>(h), perm_token, offsets, plan, nullptr, T, d, E,
-                                          k, I, W, y_perm, nullptr, st, false));
+                                          k, I, W, y_perm, nullptr, &ctrl->status, st, false));
     }
     if (!h_s) return MOE_ERR_INVALID_ARG;
-    Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
     return from_cuda(launch_umma_down(static_cast<const uint8_t*>(h), h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W,
                                       y_perm, &ctrl->status, st, false));
 }
@@ -310,7 +310,7 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
         }
         uint16_t* h = reinterpret_cast<uint16_t*>(at(ws, L.h));
         MOE_CUDA(launch_gemv_up(x, perm, offsets, plan, T, d, E, k, I, W, h, st, true));
-        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, row_w, T, d, E, k, I, W, nullptr, y, st, true));
+        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, row_w, T, d, E, k, I, W, nullptr, y, &ctrl->status, st, true));
         return MOE_OK;
     }
     MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));

@@ -204,6 +204,57 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     return v;
 }
 
+// ------------------------------------------------------------------ mbarriers and bulk copies
+constexpr long long kWaitCycles = 4000000000LL;  // bound of a device-side wait: about two seconds at GB300 clocks
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.  Returns false when the CTA is
+// aborting (another role timed out) or this wait ran out (then it records the timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          long long limit = kWaitCycles) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (*abort_flag) return false;
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > limit) {
+            set_status(status, MOE_ERR_TIMEOUT);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding kernel's results / let the next
 // kernel start its prologue.  No-ops when the launch did not use the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -253,7 +304,7 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
 // y != nullptr: fused weighted sum into y [T][d] using row_w; otherwise bf16 y_perm [P][d].
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                              const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
-                             uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl);
+                             uint16_t* y_perm, uint16_t* y, int* status, cudaStream_t st, bool pdl);
 bool gemv_supported(int d, int I);
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                            uint16_t* y, cudaStream_t st, bool pdl);

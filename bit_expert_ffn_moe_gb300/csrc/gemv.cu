@@ -135,6 +135,7 @@ struct GemvArgs {
     int maxrows;   // down: staged rows per CTA (tch * k)
     int outs;      // up: output features per CTA; down: rows per CTA
     uint16_t* out; // up: h [P][I]; down: y_perm [P][d] or y [T][d]
+    int* status;   // device status word (first error wins)
 };
 
 // ------------------------------------------------------------------ gate/up + SwiGLU
@@ -447,72 +448,170 @@ gemv_up_cta_kernel(const GemvArgs a) {
 }
 
 // ------------------------------------------------------------------ down (+ weighted sum), T <= 2
-// Same CTA-wide split of K as the gate/up kernel above.  A CTA owns RG * kR output features; row
-// group g takes features n0 + kR*g .. + kR - 1 and a batch is those kR rows of one active expert,
-// so batches walk the experts in ascending order, i.e. each token's slot order.  Every thread
-// owns one K-block of every row; the expert's h rows (at most Q) are staged once as prescaled f16.
+// The same CTA-wide split of K as the gate/up kernel above, with the weights fed through a ring
+// of shared-memory stages by the copy engine.  A CTA owns feats = RG * kR output features and
+// walks the active experts in ascending order (each token's slot order); batch u is the feats
+// rows of expert active[u], whose codes (feats * K/2 bytes) and scales (feats * K/32 bytes) are
+// each one contiguous range: two bulk copies fill a stage, and kDownStages batches are in
+// flight.  Row group g takes rows kR*g .. kR*g + kR - 1 of the batch; thread gl of the group owns
+// K-block gl of each.
+// The batch's h rows (bf16, at most Q) are converted once per CTA, a batch ahead, into a double
+// buffer of f16 blocks: four threads share a 32-element block (8 elements each), scale it by a
+// power of two that puts the block maximum in [2^14, 2^15), and the block's partial sums are
+// scaled back by the inverse, an exact rescaling.
 // FUSED: ys[t][f] accumulates w * bf16(expert output) batch after batch (the same lane updates a
 // given (t, f) in expert order); otherwise the bf16 outputs go to y_perm.
+constexpr int kDownStages = 3;
+constexpr int kDownHUnits = 2;  // 8-element h pieces per thread and batch (Q * K/8 <= 2 * kThr)
+
+__host__ __device__ inline uint32_t down_stage_bytes(int K) {
+    const CtaGeo g = make_cta_geo(K);
+    return (uint32_t)(g.RG * kR) * (uint32_t)(K / 2 + K / 32);
+}
+
+template <int Q>
+__host__ __device__ inline size_t down_ring_smem(int K, int P) {
+    const CtaGeo g = make_cta_geo(K);
+    return (size_t)kDownStages * down_stage_bytes(K) + (size_t)2 * Q * K * 2 /* h blocks */ +
+           sizeof(float) * ((size_t)2 * Q * g.nb /* inverse scales */ + 2 * 8 * 32 + (size_t)Q * g.RG * kR) +
+           sizeof(uint64_t) * kDownStages + sizeof(int) * 3 * (size_t)P;
+}
+
 template <int Q, bool FUSED>
 __global__ void __launch_bounds__(kThr, 2)
-gemv_down_cta_kernel(const GemvArgs a) {
+gemv_down_ring_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int V = kR * Q;
     const CtaGeo geo = make_cta_geo(a.K);
-    const int P = a.P, feats = geo.RG * kR;
-    uint4* hs = reinterpret_cast<uint4*>(smem);                              // [P][K/8]
-    float* inv = reinterpret_cast<float*>(smem + (size_t)P * a.K * 2);      // [P]
-    float* red = inv + P;                                                   // [2][8 warps][32]
-    float* ys = red + 2 * 8 * 32;                                           // [Q][feats]
-    int* rows = reinterpret_cast<int*>(ys + (size_t)Q * feats);             // [P]
-    unsigned* smax = reinterpret_cast<unsigned*>(rows + P);                 // [P]
+    const int feats = geo.RG * kR, nb = geo.nb;
+    const uint32_t code_bytes = (uint32_t)feats * (a.K / 2), stage_bytes = code_bytes + (uint32_t)feats * (a.K / 32);
+    uint4* hb = reinterpret_cast<uint4*>(smem + (size_t)kDownStages * stage_bytes);  // [2][Q][4][nb] f16 blocks
+    float* hinv = reinterpret_cast<float*>(hb + (size_t)2 * Q * 4 * nb);               // [2][Q][nb]
+    float* red = hinv + 2 * Q * nb;                                                     // [2][8 warps][32]
+    float* ys = red + 2 * 8 * 32;                                                       // [Q][feats]
+    uint64_t* full = reinterpret_cast<uint64_t*>(ys + (size_t)Q * feats);              // [kDownStages]
+    int* sl_r0 = reinterpret_cast<int*>(full + kDownStages);                           // [P] first row of slot u
+    int* sl_cnt = sl_r0 + a.P;                                                          // [P] its rows (<= Q)
+    int* sl_e = sl_cnt + a.P;                                                           // [P] its expert
+    __shared__ int s_abort;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int grp = tid / geo.G, gl = tid % geo.G;
     const int wpg = geo.G / 32;
-    const size_t row_bytes = (size_t)a.K / 2;
-    const int n0 = blockIdx.x * feats + grp * kR;  // this group's first feature
+    const int f0 = blockIdx.x * feats;
+    const int K2 = a.K / 2;
+    const int hunits = Q * nb * 4;  // 8-element pieces of the batch's h rows
 
+    if (tid == 0) {
+        for (int s = 0; s < kDownStages; ++s) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_abort = 0;
+    }
+    for (int i = tid; i < Q * feats; i += blockDim.x) ys[i] = 0.f;
     pdl_wait();
     const int n_act = a.plan.scalars[0];
-    auto load = [&](int u, uint4 (&wv)[kR], uint32_t (&sv)[kR]) {
-        const size_t g0 = (size_t)a.plan.active[u] * a.M_exp + n0;
-#pragma unroll
-        for (int j = 0; j < kR; ++j)
-            if (gl < geo.nb) {
-                wv[j] = ldg_stream(a.q0 + (g0 + j) * row_bytes + 16 * (size_t)gl);
-                sv[j] = __ldg(a.s0 + (g0 + j) * geo.nb + gl);
-            }
-    };
-    uint4 wcur[kR], wnxt[kR];
-    uint32_t scur[kR], snxt[kR];
-    if (n_act > 0) load(0, wcur, scur);  // in flight while h is staged
-    for (int i = tid; i < P; i += blockDim.x) rows[i] = i;
-    for (int i = tid; i < Q * feats; i += blockDim.x) ys[i] = 0.f;
+    if (tid < n_act) {
+        const int e = a.plan.active[tid];
+        const int r0 = a.offsets[e];
+        sl_e[tid] = e;
+        sl_r0[tid] = r0;
+        sl_cnt[tid] = min(Q, a.offsets[e + 1] - r0);
+    }
     __syncthreads();
-    stage_rows_f16(a.act, rows, P, a.K, hs, inv, smax);  // ends with a barrier
 
+    auto stage = [&](int s) { return smem + (size_t)s * stage_bytes; };
+    auto issue = [&](int u) {  // thread 0: batch u into stage u % kDownStages
+        const int s = u % kDownStages;
+        const size_t R = (size_t)sl_e[u] * a.M_exp + f0;
+        mbar_arrive_expect_tx(&full[s], stage_bytes);
+        bulk_load(stage(s), a.q0 + R * K2, code_bytes, &full[s]);
+        bulk_load(stage(s) + code_bytes, a.s0 + R * (a.K / 32), stage_bytes - code_bytes, &full[s]);
+    };
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < min(n_act, kDownStages); ++issued) issue(issued);
+
+    // piece i = (qq, b, c): elements 8c .. 8c+7 of block b of h row qq of the batch
+    auto load_h = [&](int u, uint4 (&hv)[kDownHUnits]) {
+#pragma unroll
+        for (int m = 0; m < kDownHUnits; ++m) {
+            const int i = tid + m * kThr;
+            const int qq = i / (4 * nb), rem = i % (4 * nb);
+            hv[m] = (u < n_act && i < hunits && qq < sl_cnt[u])
+                        ? __ldcg(reinterpret_cast<const uint4*>(a.act + (size_t)(sl_r0[u] + qq) * a.K) + rem)
+                        : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    auto convert_h = [&](int u, const uint4 (&hv)[kDownHUnits], int buf) {
+#pragma unroll
+        for (int m = 0; m < kDownHUnits; ++m) {
+            const int i = tid + m * kThr;  // the four pieces of a block are adjacent lanes
+            const int qq = i / (4 * nb), rem = i % (4 * nb), b = rem >> 2, c = rem & 3;
+            const bool valid = u < n_act && i < hunits && qq < sl_cnt[u];
+            const uint32_t w[4] = {hv[m].x, hv[m].y, hv[m].z, hv[m].w};
+            uint32_t mx = 0;
+            if (valid)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) mx = max(mx, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+            if (m * kThr < hunits) {  // warp-uniform: whole warps hold valid pieces or none
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            }
+            if (valid) {
+                const int p = prescale_exp(mx);
+                const float up = __uint_as_float((uint32_t)(127 + p) << 23);
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __half2 h2 = __floats2half2_rn(bf16_bits_to_f32(w[j] & 0xFFFFu) * up,
+                                                         bf16_bits_to_f32(w[j] >> 16) * up);
+                    o[j] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                hb[(((size_t)buf * Q + qq) * 4 + c) * nb + b] = make_uint4(o[0], o[1], o[2], o[3]);
+                if (c == 0) hinv[((size_t)buf * Q + qq) * nb + b] = __uint_as_float((uint32_t)(127 - p) << 23);
+            }
+        }
+    };
+    uint4 hv[kDownHUnits];
+    load_h(0, hv);
+    convert_h(0, hv, 0);
+    __syncthreads();
+
+    bool ok = true;
     for (int u = 0; u < n_act; ++u) {
-        const int e = a.plan.active[u];
-        const int r0 = a.offsets[e], cnt = min(Q, a.offsets[e + 1] - r0);
-        if (u + 1 < n_act) load(u + 1, wnxt, snxt);
+        const int s = u % kDownStages, buf = u & 1;
+        const int r0 = sl_r0[u], cnt = sl_cnt[u];
+        load_h(u + 1, hv);  // converted after this batch's arithmetic
+        const bool arrived = mbar_wait(&full[s], (uint32_t)(u / kDownStages) & 1u, &s_abort, a.status);
         float acc[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) acc[v] = 0.f;
-        if (gl < geo.nb) {
+        if (gl < nb) {
+            const unsigned char* st = stage(s);
 #pragma unroll
             for (int qq = 0; qq < Q; ++qq) {
                 if (qq < cnt) {
                     uint32_t x[16];
-                    load_x_block(hs, r0 + qq, geo.nb, gl, x);
+                    load_x_block(hb + (size_t)buf * Q * 4 * nb, qq, nb, gl, x);
+                    const float inv = hinv[((size_t)buf * Q + qq) * nb + gl];
 #pragma unroll
-                    for (int j = 0; j < kR; ++j)
-                        acc[qq * kR + j] = block_dot(wcur[j], x) * e8m0_to_f32(scur[j]);
+                    for (int j = 0; j < kR; ++j) {
+                        const int row = grp * kR + j;
+                        const uint4 w = *reinterpret_cast<const uint4*>(st + (size_t)row * K2 + 16 * gl);
+                        const uint32_t sc = st[code_bytes + (size_t)row * nb + gl];
+                        acc[qq * kR + j] = block_dot(w, x) * e8m0_to_f32(sc) * inv;
+                    }
                 }
             }
         }
+        convert_h(u + 1, hv, buf ^ 1);
         float* rb = red + (u & 1) * (8 * 32);
         rb[warp * 32 + lane] = warp_transpose_reduce<V>(acc, lane);
-        __syncthreads();
+        ok = __syncthreads_and(arrived);  // stage s read, next h blocks and rb written; one verdict
+        if (!ok) break;
+        if (tid == 0 && issued < n_act) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(issued++);
+        }
         if (gl < 32) {
             const int v = lane >> (5 - (V == 8 ? 3 : V == 16 ? 4 : 5));
             const int qq = v / kR, j = v % kR;
@@ -520,27 +619,33 @@ gemv_down_cta_kernel(const GemvArgs a) {
             if (leader && qq < cnt) {
                 float o = 0.f;
                 for (int w = 0; w < wpg; ++w) o += rb[(grp * wpg + w) * 32 + lane];
-                const uint16_t ob = f32_to_bf16_bits(o * inv[r0 + qq]);
+                const uint16_t ob = f32_to_bf16_bits(o);
                 if (FUSED) {
                     const int t = a.perm_token[r0 + qq];
                     float& yv = ys[t * feats + grp * kR + j];
                     yv = fmaf(a.row_w[r0 + qq], bf16_bits_to_f32(ob), yv);
                 } else {
-                    a.out[(size_t)(r0 + qq) * a.M_exp + n0 + j] = ob;
+                    a.out[(size_t)(r0 + qq) * a.M_exp + f0 + grp * kR + j] = ob;
                 }
             }
         }
-#pragma unroll
-        for (int j = 0; j < kR; ++j) {
-            wcur[j] = wnxt[j];
-            scur[j] = snxt[j];
+    }
+    if (!ok) {
+        // a copy did not arrive in time: wait (bounded) for the last batch issued to each stage,
+        // so that no copy still writes into this CTA's shared memory, then leave
+        if (tid == 0) {
+            volatile int never = 0;
+            for (int u = max(0, issued - kDownStages); u < issued; ++u)
+                mbar_wait(&full[u % kDownStages], (uint32_t)(u / kDownStages) & 1u, &never, nullptr, kWaitCycles / 4);
         }
+        __syncthreads();
+        return;
     }
     if (FUSED) {
         __syncthreads();
         for (int i = tid; i < a.T * feats; i += blockDim.x) {
             const int t = i / feats, f = i % feats;
-            a.out[(size_t)t * a.M_exp + blockIdx.x * feats + f] = f32_to_bf16_bits(ys[i]);
+            a.out[(size_t)t * a.M_exp + f0 + f] = f32_to_bf16_bits(ys[i]);
         }
     }
     pdl_launch_dependents();
@@ -799,14 +904,16 @@ static const void* down_kernel(int bpl) {
 
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                              const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
-                             uint16_t* y_perm, uint16_t* y, cudaStream_t st, bool pdl) {
+                             uint16_t* y_perm, uint16_t* y, int* status, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
     const CtaGeo dgeo = make_cta_geo(I);
-    const int P = T * k;
-    const size_t cta_smem = (size_t)P * I * 2 + sizeof(float) * (P + 2 * 8 * 32 + (size_t)T * dgeo.RG * kR) +
-                            sizeof(int) * P + sizeof(unsigned) * P;
-    if (T <= 2 && dgeo.bpt == 1 && d % (dgeo.RG * kR) == 0 && cta_smem <= 100 * 1024) {
-        // one or two tokens: CTA-split of K (see gemv_down_cta_kernel)
+    const int P = T * k, feats = dgeo.RG * kR;
+    const size_t ring_smem = T == 1 ? down_ring_smem<1>(I, P) : down_ring_smem<2>(I, P);
+    const bool aligned16 = ((uintptr_t)W->down_q % 16 == 0) && ((uintptr_t)W->down_s % 16 == 0);
+    // two CTAs per SM: 2 x (ring_smem + 1 KB reserved) within the SM's 228 KB
+    if (T <= 2 && dgeo.bpt == 1 && d % feats == 0 && aligned16 && T * dgeo.nb * 4 <= kDownHUnits * kThr &&
+        ring_smem <= 113 * 1024) {
+        // one or two tokens: CTA-split of K, weights through the copy-engine ring
         GemvArgs a = {};
         a.q0 = W->down_q;
         a.s0 = W->down_s;
@@ -821,11 +928,12 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
         a.P = P;
         a.E = E;
         a.out = y ? y : y_perm;
+        a.status = status;
         void* args[] = {&a};
-        const dim3 grid(d / (dgeo.RG * kR));
-        const void* f = T == 1 ? (y ? (const void*)gemv_down_cta_kernel<1, true> : (const void*)gemv_down_cta_kernel<1, false>)
-                               : (y ? (const void*)gemv_down_cta_kernel<2, true> : (const void*)gemv_down_cta_kernel<2, false>);
-        return launch_kernel(f, grid, dim3(kThr), cta_smem, st, pdl, args);
+        const dim3 grid(d / feats);
+        const void* f = T == 1 ? (y ? (const void*)gemv_down_ring_kernel<1, true> : (const void*)gemv_down_ring_kernel<1, false>)
+                               : (y ? (const void*)gemv_down_ring_kernel<2, true> : (const void*)gemv_down_ring_kernel<2, false>);
+        return launch_kernel(f, grid, dim3(kThr), ring_smem, st, pdl, args);
     }
     const int bpl = bpl_for(I);
     const int outs = kWarps * down_rows_per_warp(bpl);

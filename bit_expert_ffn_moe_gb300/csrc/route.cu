@@ -23,56 +23,78 @@ __device__ __forceinline__ float warp_butterfly_sum(float p) {
     return p;
 }
 
-// One warp selects the top-k of logits[0..E) (ties -> lower id), sorts the set ascending and
-// writes ids[0..k) and the softmax weights w[0..k).
-__device__ void topk_softmax_warp(const float* logits, int E, int k, int32_t* ids, float* w) {
+// Order-preserving key of a logit: a larger float gives a larger unsigned key, +0 and -0 give the
+// same key, and no finite value or infinity maps to 0, which marks "no candidate".
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_logit(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// One warp selects the top-k of logits[0..E) (largest first; ties -> lower id), sorts the set by
+// ascending id and writes ids[0..k) and the softmax weights w[0..k); when cnt is given it also
+// counts each pick there (shared-memory histogram).  Lane l holds the keys of ids l + 32 i in
+// registers; a round takes the lane maxima (strict > over increasing i keeps the lower id), the
+// warp maximum of the keys and then the least id among the lanes holding it.
+template <int NV>
+__device__ __forceinline__ void topk_softmax_regs(const float* logits, int E, int k, int32_t* ids, float* w, int* cnt) {
     const int lane = threadIdx.x & 31;
-    uint32_t taken = 0;
-    int my_id = 0x7fffffff;
-    float my_logit = -FLT_MAX;
-    for (int r = 0; r < k; ++r) {
-        float best = -FLT_MAX;
-        int bid = 0x7fffffff;
-        for (int i = 0; lane + 32 * i < E; ++i) {
-            if ((taken >> i) & 1u) continue;
-            float v = logits[lane + 32 * i];
-            if (bid == 0x7fffffff || v > best) {  // increasing e within a lane: strict > keeps the lower id
-                best = v;
-                bid = lane + 32 * i;
-            }
-        }
+    uint32_t key[NV];
 #pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, best, m);
-            int oid = __shfl_xor_sync(0xffffffffu, bid, m);
-            if (oid != 0x7fffffff && (bid == 0x7fffffff || ov > best || (ov == best && oid < bid))) {
-                best = ov;
-                bid = oid;
+    for (int i = 0; i < NV; ++i) key[i] = lane + 32 * i < E ? logit_key(__ldcg(logits + lane + 32 * i)) : 0u;
+    int my_id = 0x7fffffff;
+    uint32_t my_key = 0, taken = 0;  // bit i: id lane + 32 i already chosen
+    for (int r = 0; r < k; ++r) {
+        uint32_t lb = 0;
+        int li = 0;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+            if (!((taken >> i) & 1u) && key[i] > lb) {
+                lb = key[i];
+                li = i;
             }
-        }
-        if ((bid & 31) == lane) taken |= 1u << (bid >> 5);
+        const uint32_t wb = __reduce_max_sync(0xffffffffu, lb);
+        const int id = __reduce_min_sync(0xffffffffu, (lb == wb) ? lane + 32 * li : 0x7fffffff);
+        if ((id & 31) == lane) taken |= 1u << (id >> 5);
         if (lane == r) {
-            my_id = bid;
-            my_logit = best;
+            my_id = id;
+            my_key = wb;
         }
     }
-    // rank of each chosen id among the k chosen (ids are distinct)
+    // ascending-id order of the chosen set
     int rank = 0;
     for (int s = 0; s < k; ++s) {
         int o = __shfl_sync(0xffffffffu, my_id, s);
         if (lane < k && o < my_id) ++rank;
     }
-    float m = __shfl_sync(0xffffffffu, my_logit, 0);  // the first pick is the largest logit
+    const float my_logit = key_logit(my_key);
+    const float m = __shfl_sync(0xffffffffu, my_logit, 0);  // the first pick is the largest logit
     float ex = lane < k ? expf(my_logit - m) : 0.f;
     float sum = warp_butterfly_sum(ex);
     if (lane < k) {
         ids[rank] = my_id;
         w[rank] = ex / sum;
+        if (cnt) atomicAdd(cnt + my_id, 1);
     }
 }
 
-// Warp 0 of a block: counts[E] -> offsets, padded offsets, token-tile prefix, active list.
-__device__ void build_plan_warp(const int32_t* counts_in, int E, int32_t* counts_out, int32_t* offsets, PlanView plan) {
+__device__ void topk_softmax_warp(const float* logits, int E, int k, int32_t* ids, float* w, int* cnt = nullptr) {
+    const int nv = (E + 31) / 32;
+    if (nv <= 1) topk_softmax_regs<1>(logits, E, k, ids, w, cnt);
+    else if (nv <= 2) topk_softmax_regs<2>(logits, E, k, ids, w, cnt);
+    else if (nv <= 4) topk_softmax_regs<4>(logits, E, k, ids, w, cnt);
+    else if (nv <= 8) topk_softmax_regs<8>(logits, E, k, ids, w, cnt);
+    else if (nv <= 16) topk_softmax_regs<16>(logits, E, k, ids, w, cnt);
+    else topk_softmax_regs<32>(logits, E, k, ids, w, cnt);
+}
+
+// Warp 0 of a block: counts[E] -> offsets, padded offsets, token-tile prefix, active list
+// (offsets also to shared memory when offsets_smem is given).
+__device__ void build_plan_warp(const int32_t* counts_in, int E, int32_t* counts_out, int32_t* offsets, PlanView plan,
+                                int32_t* offsets_smem = nullptr) {
     const int lane = threadIdx.x & 31;
     const int chunk = (E + 31) / 32;
     const int lo = min(E, lane * chunk), hi = min(E, lo + chunk);
@@ -102,6 +124,7 @@ __device__ void build_plan_warp(const int32_t* counts_in, int E, int32_t* counts
         if (counts_out) counts_out[e] = c;
         plan.counts[e] = c;
         offsets[e] = c_off;
+        if (offsets_smem) offsets_smem[e] = c_off;
         plan.pad_offsets[e] = p_off;
         plan.ttile_prefix[e] = t_off;
         if (c > 0) plan.active[a_off++] = e;
@@ -111,6 +134,7 @@ __device__ void build_plan_warp(const int32_t* counts_in, int E, int32_t* counts
     }
     if (lane == 31) {
         offsets[E] = x_cnt;
+        if (offsets_smem) offsets_smem[E] = x_cnt;
         plan.pad_offsets[E] = x_pad;
         plan.ttile_prefix[E] = x_tile;
         plan.scalars[0] = x_act;
@@ -121,14 +145,21 @@ __device__ void build_plan_warp(const int32_t* counts_in, int E, int32_t* counts
 
 // ------------------------------------------------------------------ decode route (small T)
 // Grid: one CTA per expert.  W_r[e] and x (T <= 8 rows) are staged in shared memory with
-// cp.async; warps compute the T logits of expert e.  The last CTA to finish (atomic ticket)
-// runs top-k for every token and the whole permutation, so a decode step needs one launch.
+// cp.async in kRouteChunks commit groups, so the dot products of chunk c overlap the copies of
+// the later chunks; warps compute the T logits of expert e.  The last CTA to finish (atomic
+// ticket) runs top-k for every token and the whole permutation, so a decode step needs one launch.
 constexpr int kRouteDecodeThreads = 128;
 constexpr int kRouteDecodeMaxT = 8;
+constexpr int kRouteChunks = 4;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __global__ void __launch_bounds__(kRouteDecodeThreads)
@@ -141,31 +172,75 @@ route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sizeof(float) * d);  // [T][d]
     __shared__ int s_last;
     __shared__ int s_cnt[kMaxE];
+    __shared__ int s_off[kMaxE + 1];
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     pdl_wait();
-    for (int i = tid; i < d / 4; i += blockDim.x) cp_async16(Ws + 4 * i, W_r + (size_t)e * d + 4 * i);
-    for (int i = tid; i < T * d / 8; i += blockDim.x) cp_async16(xs + 8 * i, x + 8 * (size_t)i);
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
+    // Chunk c holds the 4-element groups [c*Gc, (c+1)*Gc) of the row (clamped to d/4); Gc is a
+    // multiple of 32, so group g stays with lane g % 32 and the fixed summation order holds.
+    const int ng = d / 4;
+    const int Gc = ((ng + kRouteChunks - 1) / kRouteChunks + 31) / 32 * 32;
+#pragma unroll
+    for (int c = 0; c < kRouteChunks; ++c) {
+        const int lo = min(c * Gc, ng), hi = min(lo + Gc, ng);
+        for (int g = lo + tid; g < hi; g += blockDim.x) cp_async16(Ws + 4 * g, W_r + (size_t)e * d + 4 * g);
+        const int n8 = (hi - lo) / 2;  // 8-element pieces of a token row in this chunk
+        for (int i = tid; i < T * n8; i += blockDim.x) {
+            const int t = i / n8, p8 = lo / 2 + i % n8;
+            cp_async16(xs + (size_t)t * d + 8 * p8, x + (size_t)t * d + 8 * p8);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int i = tid; i < E; i += blockDim.x) s_cnt[i] = 0;
 
     const float bias = b ? b[e] : 0.f;
-    for (int t = warp; t < T; t += blockDim.x / 32) {
-        const uint16_t* xr = xs + (size_t)t * d;
-        float acc = 0.f;
-        for (int g = lane; g < d / 4; g += 32) {
-            float4 wv = *reinterpret_cast<const float4*>(Ws + 4 * g);
-            uint2 xv = *reinterpret_cast<const uint2*>(xr + 4 * g);
-            acc = fmaf(bf16_bits_to_f32(xv.x & 0xFFFF), wv.x, acc);
-            acc = fmaf(bf16_bits_to_f32(xv.x >> 16), wv.y, acc);
-            acc = fmaf(bf16_bits_to_f32(xv.y & 0xFFFF), wv.z, acc);
-            acc = fmaf(bf16_bits_to_f32(xv.y >> 16), wv.w, acc);
+    float acc = 0.f, acc2 = 0.f;  // partial sum `lane` of tokens `warp` and `warp + 4` (T <= 8)
+#pragma unroll
+    for (int c = 0; c < kRouteChunks; ++c) {
+        if (c == 0) cp_async_wait_group<kRouteChunks - 1>();
+        else if (c == 1) cp_async_wait_group<kRouteChunks - 2>();
+        else if (c == 2) cp_async_wait_group<kRouteChunks - 3>();
+        else cp_async_wait_group<0>();
+        __syncthreads();
+        const int lo = min(c * Gc, ng), hi = min(lo + Gc, ng);
+        if (warp < T) {
+            const uint16_t* xr = xs + (size_t)warp * d;
+            const int n = (hi - lo) / 32;  // groups of this lane in the chunk (hi - lo is a multiple of 32)
+#pragma unroll 4
+            for (int m = 0; m < n; ++m) {
+                const int g = lo + lane + 32 * m;
+                const float4 wv = *reinterpret_cast<const float4*>(Ws + 4 * g);
+                const uint2 xv = *reinterpret_cast<const uint2*>(xr + 4 * g);
+                acc = fmaf(bf16_bits_to_f32(xv.x & 0xFFFF), wv.x, acc);
+                acc = fmaf(bf16_bits_to_f32(xv.x >> 16), wv.y, acc);
+                acc = fmaf(bf16_bits_to_f32(xv.y & 0xFFFF), wv.z, acc);
+                acc = fmaf(bf16_bits_to_f32(xv.y >> 16), wv.w, acc);
+            }
+            if (warp + 4 < T) {
+                const uint16_t* xr2 = xs + (size_t)(warp + 4) * d;
+#pragma unroll 4
+                for (int m = 0; m < n; ++m) {
+                    const int g = lo + lane + 32 * m;
+                    const float4 wv = *reinterpret_cast<const float4*>(Ws + 4 * g);
+                    const uint2 xv = *reinterpret_cast<const uint2*>(xr2 + 4 * g);
+                    acc2 = fmaf(bf16_bits_to_f32(xv.x & 0xFFFF), wv.x, acc2);
+                    acc2 = fmaf(bf16_bits_to_f32(xv.x >> 16), wv.y, acc2);
+                    acc2 = fmaf(bf16_bits_to_f32(xv.y & 0xFFFF), wv.z, acc2);
+                    acc2 = fmaf(bf16_bits_to_f32(xv.y >> 16), wv.w, acc2);
+                }
+            }
         }
+    }
+    if (warp < T) {
         acc = warp_butterfly_sum(acc);
-        if (lane == 0) logits[(size_t)t * E + e] = acc + bias;
+        if (lane == 0) logits[(size_t)warp * E + e] = acc + bias;
+    }
+    if (warp + 4 < T) {
+        acc2 = warp_butterfly_sum(acc2);
+        if (lane == 0) logits[(size_t)(warp + 4) * E + e] = acc2 + bias;
     }
 
-    // ---- last CTA: top-k + permutation, working from shared memory
+    // ---- last CTA: top-k + permutation
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -179,51 +254,42 @@ route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_
 
     __shared__ int32_t s_ids[kRouteDecodeMaxT * kMaxK];
     __shared__ float s_w[kRouteDecodeMaxT * kMaxK];
-    float* sl = reinterpret_cast<float*>(smem);  // [T][E]; the staging area is free now
-    for (int i = tid; i < T * E; i += blockDim.x) sl[i] = __ldcg(logits + i);  // other CTAs' results
-    for (int i = tid; i < E; i += blockDim.x) s_cnt[i] = 0;
-    __syncthreads();
-    for (int t = warp; t < T; t += blockDim.x / 32)
-        topk_softmax_warp(sl + (size_t)t * E, E, k, s_ids + t * k, s_w + t * k);
+    for (int t = warp; t < T; t += blockDim.x / 32)  // other CTAs' logits, read from L2
+        topk_softmax_warp(logits + (size_t)t * E, E, k, s_ids + t * k, s_w + t * k, s_cnt);
     __syncthreads();
     const int P = T * k;
     for (int p = tid; p < P; p += blockDim.x) {
         ids[p] = s_ids[p];
         w[p] = s_w[p];
-        atomicAdd(&s_cnt[s_ids[p]], 1);
     }
-    __syncthreads();
-    if (warp == 0) build_plan_warp(s_cnt, E, counts, offsets, plan);
+    if (warp == 0) build_plan_warp(s_cnt, E, counts, offsets, plan, s_off);
     __syncthreads();
     for (int p = tid; p < P; p += blockDim.x) {
         const int t = p / k, ex = s_ids[p];
         int rank = 0;  // tokens before t that chose ex (each token picks an expert at most once)
         for (int t2 = 0; t2 < t; ++t2)
             for (int j = 0; j < k; ++j) rank += (s_ids[t2 * k + j] == ex);
-        const int r = offsets[ex] + rank;
+        const int r = s_off[ex] + rank;
         perm_token[r] = t;
         inv_pos[p] = r;
         row_w[r] = s_w[p];
     }
-    __threadfence();
     pdl_launch_dependents();
 }
 
-static size_t route_decode_smem(int T, int d, int E) {
-    const size_t staging = sizeof(float) * (size_t)d + sizeof(uint16_t) * (size_t)T * d;
-    const size_t logits = sizeof(float) * (size_t)T * E;
-    return staging > logits ? staging : logits;
+static size_t route_decode_smem(int T, int d) {
+    return sizeof(float) * (size_t)d + sizeof(uint16_t) * (size_t)T * d;  // W_r[e] and x staging
 }
 
 bool route_decode_supported(int T, int d, int E, int k) {
-    return T >= 1 && T <= kRouteDecodeMaxT && E <= kMaxE && k <= kMaxK && route_decode_smem(T, d, E) <= 200 * 1024;
+    return T >= 1 && T <= kRouteDecodeMaxT && E <= kMaxE && k <= kMaxK && route_decode_smem(T, d) <= 200 * 1024;
 }
 
 cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                 float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
                                 int32_t* perm_token, int32_t* inv_pos, float* row_w, PlanView plan, Ctrl* ctrl,
                                 cudaStream_t st, bool pdl) {
-    const size_t smem = route_decode_smem(T, d, E);
+    const size_t smem = route_decode_smem(T, d);
     void* args[] = {&x, &W_r, &b, &T, &d, &E, &k, &logits, &ids, &w, &counts, &offsets, &perm_token, &inv_pos,
                     &row_w, &plan, &ctrl};
     return launch_kernel((const void*)route_decode_kernel, dim3(E), dim3(kRouteDecodeThreads), smem, st, pdl, args);

@@ -57,7 +57,6 @@ constexpr int kSfBase = kAccBufs * kAccCols;  // scale slots after the accumulat
 constexpr int kSfCols = 24;                   // per stage: A scales 8 columns, B scales 16
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarBytes = 256;
-constexpr long long kWaitCycles = 4000000000LL;  // about two seconds at GB300 clocks
 static_assert(kSfBase + kStages * kSfCols <= (int)kTmemCols, "tensor memory budget");
 
 constexpr size_t smem_bytes(int E) {
@@ -65,47 +64,6 @@ constexpr size_t smem_bytes(int E) {
 }
 
 // ------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait for the phase with the given parity to complete.  Returns false when the CTA is
-// aborting (another role timed out) or this wait ran out (then it records the timeout).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                          long long limit = kWaitCycles) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (true) {
-        if (*abort_flag) return false;
-        if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > limit) {
-            set_status(status, MOE_ERR_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
 // One K step of 256 values: the six scale-atom copies of the stage into tensor memory, then the
 // four K = 64 MMAs and the commit that frees the stage, each group issued by one elected lane.
 // Scale slot of a stage (24 columns from sf): A scales of K values 0..127 at sf, 128..255 at
@@ -151,13 +109,6 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
                                                long long limit = kWaitCycles) {
     const bool ok = mbar_wait(bar, parity, abort_flag, status, limit);
     return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }

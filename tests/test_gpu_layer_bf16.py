@@ -15,10 +15,12 @@ pytestmark = pytest.mark.gpu
 _layers = {}
 
 
-# Shapes on the warp-ring GEMVs (d and I multiples of 512) with several tokens per expert.
+# Small shapes: ring_t3 on the warp-per-row GEMVs with several tokens per expert; ring_t2 and
+# ring_t1 on the CTA-split GEMVs (one or two tokens, down weights through the copy-engine ring).
 SMALL = {
     "ring_t3": IN.small_config("ring_t3", T=3, d=1024, E=12, k=4, I=512, index=93),
     "ring_t2": IN.small_config("ring_t2", T=2, d=2048, E=6, k=3, I=1536, index=94),
+    "ring_t1": IN.small_config("ring_t1", T=1, d=1024, E=16, k=4, I=1024, index=95),
 }
 
 
@@ -37,7 +39,7 @@ def oracle_layer(layer, xb, act_fmt, tokens=None):
 
 
 @pytest.mark.parametrize("name,calls", [("tiny", [0, 1]), ("decode", [0, 1, 2]), ("spec_verify", [0]),
-                                        ("ring_t3", [0, 1]), ("ring_t2", [0, 1])])
+                                        ("ring_t3", [0, 1]), ("ring_t2", [0, 1]), ("ring_t1", [0, 1, 2])])
 def test_layer_matches_oracle(name, calls):
     layer = get_layer(name)
     cfg = layer.cfg
@@ -52,7 +54,7 @@ def test_layer_matches_oracle(name, calls):
     assert B.moe_get_device_status(ws) == B.MOE_OK
 
 
-@pytest.mark.parametrize("name", ["tiny", "ring_t3"])
+@pytest.mark.parametrize("name", ["tiny", "ring_t3", "ring_t2", "ring_t1"])
 def test_step_calls_equal_layer_call_and_oracle_h(name):
     layer = get_layer(name)
     cfg = layer.cfg
