@@ -272,6 +272,7 @@ cudaError_t ensure_dyn_smem(const void* func, size_t bytes);
 // Launch with the programmatic-dependent-launch attribute when pdl is true.
 cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
                           void** args);
+int sm_count();  // SMs of the current device
 
 cudaError_t launch_synth(uint64_t seed, uint32_t tensor_id, uint32_t expert_first, uint32_t n_experts, int64_t rows,
                          int64_t K, float c, float* out, cudaStream_t st);

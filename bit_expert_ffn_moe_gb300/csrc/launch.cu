@@ -22,6 +22,13 @@ cudaError_t ensure_dyn_smem(const void* func, size_t bytes) {
     return err;
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
+}
+
 cudaError_t launch_kernel(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
                           void** args) {
     if (smem > 0) {  // static + dynamic shared memory may pass 48 KB even when smem alone does not

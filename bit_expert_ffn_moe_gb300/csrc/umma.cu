@@ -464,13 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
 }
 
 // ------------------------------------------------------------------ host side
-int sm_count() {
-    int dev = 0, n = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 148;
-}
-
 template <bool IS_UP>
 cudaError_t launch_grouped(const UmmaArgs& args, cudaStream_t st, bool pdl) {
     const void* f = (const void*)umma_grouped_kernel<IS_UP>;
