@@ -154,6 +154,9 @@ gemv_up_kernel(const GemvArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     pdl_wait();
+    // the next kernel (the down GEMV) may start now: before its own wait it only reads the routing
+    // plan, which the kernel before this one wrote, and the weights
+    pdl_launch_dependents();
     const int slot = blockIdx.y;
     if (slot >= a.plan.scalars[0]) return;
     const int e = a.plan.active[slot];
@@ -371,6 +374,9 @@ gemv_up_cta_kernel(const GemvArgs a) {
     const int wpg = geo.G / 32;  // warps per group
 
     pdl_wait();
+    // the next kernel (the down GEMV) may start now: before its own wait it only reads the routing
+    // plan, which the kernel before this one wrote, and the weights
+    pdl_launch_dependents();
     const int slot = blockIdx.y;
     if (slot >= a.plan.scalars[0]) return;
     const int e = a.plan.active[slot];
@@ -507,14 +513,16 @@ gemv_down_ring_kernel(const GemvArgs a) {
         s_abort = 0;
     }
     for (int i = tid; i < Q * feats; i += blockDim.x) ys[i] = 0.f;
-    pdl_wait();
-    const int n_act = a.plan.scalars[0];
+    // The routing plan comes from the kernel two launches back, which completed before the gate/up
+    // kernel passed its own wait and let this one start; it is read through L2 before this
+    // kernel's wait, and the first weight stages are issued, so only h waits for gate/up.
+    const int n_act = __ldcg(a.plan.scalars);
     if (tid < n_act) {
-        const int e = a.plan.active[tid];
-        const int r0 = a.offsets[e];
+        const int e = __ldcg(a.plan.active + tid);
+        const int r0 = __ldcg(a.offsets + e);
         sl_e[tid] = e;
         sl_r0[tid] = r0;
-        sl_cnt[tid] = min(Q, a.offsets[e + 1] - r0);
+        sl_cnt[tid] = min(Q, __ldcg(a.offsets + e + 1) - r0);
     }
     __syncthreads();
 
@@ -529,6 +537,7 @@ gemv_down_ring_kernel(const GemvArgs a) {
     int issued = 0;
     if (tid == 0)
         for (; issued < min(n_act, kDownStages); ++issued) issue(issued);
+    pdl_wait();
 
     // piece i = (qq, b, c): elements 8c .. 8c+7 of block b of h row qq of the batch
     auto load_h = [&](int u, uint4 (&hv)[kDownHUnits]) {
