@@ -40,6 +40,11 @@
  *       Expert outputs (y_perm) are rounded to fp32 then bf16, as the GPU stores them; the
  *       weighted sum is formed in fp64 over the k slots in slot order, rounded to fp32, then
  *       to bf16.
+ *   R8  expert output normalisation (optional; [MUSE] s.9 says each chosen expert's output is
+ *       normalised before the weighted sum, without naming the normalisation): RMSNorm over
+ *       the d output features of the expert's (bf16) output row, v / sqrt(mean(v^2) + eps),
+ *       eps = 1e-6 unless given, no learned scale; computed in fp64 and rounded to fp32, then
+ *       summed as in R7.
  * Accumulations inside the expert matrices are fp64 (closer to exact than the kernels).
  */
 #include <math.h>
@@ -387,6 +392,17 @@ void oracle_combine(const float* y_perm, const int32_t* rows, const float* w, in
                 acc += (double)w[(int64_t)t * k + j] * (double)y_perm[(int64_t)rows[(int64_t)t * k + j] * d + c];
             y[(int64_t)s * d + c] = round_to_bf16((float)acc);
         }
+    }
+}
+
+/* Expert output normalisation (R8): out[r] = y[r] / sqrt(mean_c y[r][c]^2 + eps), fp64, rounded
+ * to fp32.  An all-zero row stays zero. */
+void oracle_expert_norm(const float* y, int64_t rows, int d, double eps, float* out) {
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int c = 0; c < d; ++c) ss += (double)y[r * d + c] * (double)y[r * d + c];
+        double inv = 1.0 / sqrt(ss / d + eps);
+        for (int c = 0; c < d; ++c) out[r * d + c] = (float)((double)y[r * d + c] * inv);
     }
 }
 

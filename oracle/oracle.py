@@ -6,7 +6,7 @@ library and never imports it; inputs come from the seeded generators and are pas
 as numpy arrays.
 
 Each function follows one step of the layer as the sources state it (see the header of
-``moe_oracle.c`` for the citations and the readings R1-R7 taken where they are silent):
+``moe_oracle.c`` for the citations and the readings R1-R8 taken where they are silent):
 
 * ``router_logits``  -- Muse Spark Open explainer, section 8 (one FP32 matrix product)
 * ``topk_softmax``   -- section 8 (best k of E, a set) and section 9 (weights sum to 1)
@@ -14,6 +14,8 @@ Each function follows one step of the layer as the sources state it (see the hea
 * ``expert_ffn``     -- section 9 (gate / up / down) on MXFP4 weights (section 11, and the
                         DGX Spark news item, section 2)
 * ``combine``        -- section 9 (weighted sum over the chosen experts)
+* ``expert_norm``    -- section 9 (each chosen expert's output is normalised before the sum;
+                        reading R8: RMSNorm over d, no learned scale)
 """
 from __future__ import annotations
 
@@ -71,6 +73,7 @@ def _load():
         "oracle_activation_row": (None, [P, i32, i32, P, P, P]),
         "oracle_expert_ffn": (None, [P, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P, P]),
         "oracle_combine": (None, [P, P, P, i32, P, i32, i32, P]),
+        "oracle_expert_norm": (None, [P, i64, i32, ctypes.c_double, P]),
         "oracle_float_to_bf16_bits": (ctypes.c_uint16, [ctypes.c_float]),
         "oracle_bf16_bits_to_float": (ctypes.c_float, [ctypes.c_uint16]),
     }
@@ -233,13 +236,27 @@ def combine(y_perm: np.ndarray, rows: np.ndarray, w: np.ndarray, tokens: np.ndar
     return y
 
 
+EXPERT_NORM_EPS = 1e-6
+
+
+def expert_norm(y: np.ndarray, eps: float = EXPERT_NORM_EPS) -> np.ndarray:
+    """Each row divided by its RMS over the columns, sqrt(mean(v^2) + eps) (reading R8)."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    out = np.empty_like(y)
+    if y.size:
+        _load().oracle_expert_norm(_ptr(y), y.shape[0], y.shape[1], float(eps), _ptr(out))
+    return out
+
+
 # ------------------------------------------------------------------ the layer
 
 def moe_layer(x_bits: np.ndarray, W_r: np.ndarray, b: Optional[np.ndarray], k: int,
               expert_weights: Callable[[int], Dict[str, tuple]], act_fmt: int,
-              tokens: Optional[Sequence[int]] = None, want_intermediates: bool = False) -> Dict:
+              tokens: Optional[Sequence[int]] = None, want_intermediates: bool = False,
+              expert_norm_eps: Optional[float] = None) -> Dict:
     """The whole layer: routing and permutation for every token, expert outputs and the
-    weighted sum for ``tokens`` (all tokens when None).
+    weighted sum for ``tokens`` (all tokens when None).  With ``expert_norm_eps`` each expert
+    output row is normalised (``expert_norm``) before the weighted sum.
 
     ``expert_weights(e)`` returns {"gate": (q, s), "up": (q, s), "down": (q, s)} for expert e
     (MXFP4 packed by this oracle's own packer), so only the experts the sampled tokens
@@ -281,7 +298,8 @@ def moe_layer(x_bits: np.ndarray, W_r: np.ndarray, b: Optional[np.ndarray], k: i
     rows_full = np.zeros((T, k), dtype=np.int32)
     for (t, j), r in pair_rows.items():
         rows_full[t, j] = r
-    y = combine(y_perm_sel, rows_full, w, tok)
+    y_in = y_perm_sel if expert_norm_eps is None else expert_norm(y_perm_sel, expert_norm_eps)
+    y = combine(y_in, rows_full, w, tok)
     out = dict(logits=logits, ids=ids, w=w, counts=counts, offsets=offsets, perm_token=perm_token,
                inv_pos=inv_pos, tokens=tok, y=y)
     if want_intermediates:

@@ -374,3 +374,59 @@ def test_synth_c_and_numpy_definitions_agree():
     np.testing.assert_array_equal(a, b)
     key = IN._host().inputs_stream_key(77, 1, 3)
     assert key == int(IN.stream_key(77, 1, 3))
+
+
+# ------------------------------------------------------------------ expert output normalisation
+
+def test_expert_norm_closed_form_and_unit_rms():
+    """RMSNorm over the row: [3, 4] has mean square 12.5, so it becomes [3, 4] / sqrt(12.5 + eps);
+    random rows come out with unit RMS (to within eps / mean square); a zero row stays zero."""
+    eps = 1e-6
+    y = O.expert_norm(np.array([[3.0, 4.0]], np.float32), eps)
+    r = math.sqrt(12.5 + eps)
+    np.testing.assert_array_equal(y[0], np.array([3.0 / r, 4.0 / r], np.float32))
+    rng = np.random.default_rng(21)
+    rows = (rng.standard_normal((7, 300)) * rng.uniform(0.01, 50.0, (7, 1))).astype(np.float32)
+    out = O.expert_norm(rows, eps).astype(np.float64)
+    ms = np.mean(rows.astype(np.float64) ** 2, axis=1)
+    np.testing.assert_allclose(np.sqrt(np.mean(out ** 2, axis=1)), np.sqrt(ms / (ms + eps)), rtol=1e-6)
+    np.testing.assert_array_equal(O.expert_norm(np.zeros((2, 32), np.float32), eps), np.zeros((2, 32), np.float32))
+
+
+def test_expert_norm_removes_the_scale_of_each_expert():
+    """With the normalisation, multiplying one expert's down weights by 2 (every scale byte + 1,
+    an exact doubling of its bf16 outputs) leaves the layer output unchanged: bit for bit when
+    eps = 0 (every step is an exact power-of-two rescaling), within a bf16 step for eps = 1e-6;
+    without the normalisation the output changes."""
+    rng = np.random.default_rng(22)
+    d, I, E, k, T = 64, 64, 5, 2, 11
+    experts = [_rand_expert(rng, d, I) for _ in range(E)]
+    doubled = [list(x) for x in experts]
+    dq, ds = experts[3][2]
+    doubled[3][2] = (dq, (ds + 1).astype(np.uint8))
+    xb = IN.to_bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    W_r = rng.standard_normal((E, d)).astype(np.float32)
+
+    def run(ex, eps):
+        return O.moe_layer(xb, W_r, None, k, lambda e: {"gate": ex[e][0], "up": ex[e][1], "down": ex[e][2]},
+                           O.ACT_BF16, expert_norm_eps=eps)
+
+    assert 3 in run(experts, None)["ids"]
+    np.testing.assert_array_equal(run(experts, 0.0)["y"], run(doubled, 0.0)["y"])
+    np.testing.assert_allclose(run(experts, 1e-6)["y"], run(doubled, 1e-6)["y"], rtol=2 ** -7, atol=0)
+    assert not np.array_equal(run(experts, None)["y"], run(doubled, None)["y"])
+
+
+def test_expert_norm_with_identical_experts_is_the_normalised_expert_output():
+    """Identical experts and weights summing to one: y = RMSNorm(expert output) (numpy fp64)."""
+    rng = np.random.default_rng(23)
+    d, I, E, k, T = 64, 64, 4, 3, 6
+    wg, wu, wd = _rand_expert(rng, d, I)
+    xb = IN.to_bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    W_r = rng.standard_normal((E, d)).astype(np.float32)
+    res = O.moe_layer(xb, W_r, None, k, lambda e: {"gate": wg, "up": wu, "down": wd}, O.ACT_BF16,
+                      expert_norm_eps=1e-6)
+    a = O.activation_rows(xb, O.ACT_BF16)
+    v = O.expert_ffn(a, wg, wu, wd, O.ACT_BF16).astype(np.float64)
+    ref = v / np.sqrt(np.mean(v ** 2, axis=1, keepdims=True) + 1e-6)
+    np.testing.assert_allclose(res["y"], ref, rtol=2 ** -7, atol=1e-6)
