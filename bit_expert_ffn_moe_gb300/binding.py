@@ -29,7 +29,7 @@ EXPORTED = (
     "moe_status_string", "moe_abi_version", "moe_last_cuda_error", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
     "moe_mxfp4_scales_to_mma", "moe_mxfp4_codes_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
-    "moe_layer_forward", "moe_synth_weights", "moe_selftest_wait_timeout",
+    "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
 )
 
 
@@ -74,6 +74,8 @@ _SIGS = {
     "moe_expert_down": (I32, [P, P, I32, P, P, I32, I32, I32, I32, I32, WP, P, P, SZ, P]),
     "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
     "moe_layer_forward": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, SZ, P]),
+    "moe_combine_norm": (I32, [P, P, P, I32, I32, I32, ctypes.c_float, P, P]),
+    "moe_layer_forward_norm": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, ctypes.c_float, P, P, P, P, SZ, P]),
     "moe_synth_weights": (I32, [U64, U32, U32, U32, I64, I64, ctypes.c_float, P, P]),
     "moe_selftest_wait_timeout": (I32, [P, SZ, I32, P]),
 }
@@ -227,6 +229,18 @@ def moe_layer_forward(x, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, y, i
     _check("moe_layer_forward",
            load().moe_layer_forward(_p(x), _p(W_r), _p(b), T, d, E, k, I, ctypes.byref(W), fmt, _p(y), _p(ids),
                                     _p(w), _p(ws), _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_combine_norm(y_perm, inv_pos, w, T, k, d, eps, y, stream=None):
+    _check("moe_combine_norm", load().moe_combine_norm(_p(y_perm), _p(inv_pos), _p(w), T, k, d, float(eps), _p(y),
+                                                       _stream(stream)))
+
+
+def moe_layer_forward_norm(x, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, eps, y, ids, w, ws, ws_bytes=None,
+                           stream=None):
+    _check("moe_layer_forward_norm",
+           load().moe_layer_forward_norm(_p(x), _p(W_r), _p(b), T, d, E, k, I, ctypes.byref(W), fmt, float(eps), _p(y),
+                                         _p(ids), _p(w), _p(ws), _ws_bytes(ws, ws_bytes), _stream(stream)))
 
 
 def moe_synth_weights(seed, tensor_id, expert_first, n_experts, rows, K, c, out, stream=None):

@@ -8,7 +8,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kAbiVersion = 4;
+constexpr int kAbiVersion = 5;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -278,17 +278,28 @@ moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const flo
     return from_cuda(launch_combine(y_perm, inv_pos, w, T, k, d, y, (cudaStream_t)stream, false));
 }
 
-moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k, int I,
-                             const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids, float* w,
-                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+moe_status moe_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
+                            float eps, uint16_t* y, moe_stream_t stream) {
+    if (T < 0 || k <= 0 || k > kMaxK || d <= 0 || d % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!(eps > 0.f && eps <= 1.f)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y_perm || !inv_pos || !w || !y || !aligned(y_perm, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_combine_norm(y_perm, inv_pos, w, T, k, d, eps, y, (cudaStream_t)stream, false));
+}
+
+// The layer; norm: each expert output row is divided by its RMS over d before the weighted sum.
+static moe_status layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k, int I,
+                                const moe_expert_weights* W, moe_act_fmt fmt, bool norm, float eps, uint16_t* y,
+                                int32_t* ids, float* w, void* ws, size_t ws_bytes, cudaStream_t st) {
     MOE_TRY(check_shape(T, d, E, k, I, fmt));
+    if (norm && !(eps > 0.f && eps <= 1.f)) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     MOE_TRY(check_weights(W, fmt, true, true));
     if (!x || !W_r || !y || !aligned(x, 16) || !aligned(W_r, 16) || !aligned(y, 16)) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, d, E, k, I, fmt);
     MOE_TRY(check_ws(ws, ws_bytes, L));
     MOE_TRY(check_device());
-    cudaStream_t st = (cudaStream_t)stream;
     PlanView plan = plan_view(ws, L, E);
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
     int32_t* ids_b = ids ? ids : reinterpret_cast<int32_t*>(at(ws, L.ids));
@@ -310,7 +321,15 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
         }
         uint16_t* h = reinterpret_cast<uint16_t*>(at(ws, L.h));
         MOE_CUDA(launch_gemv_up(x, perm, offsets, plan, T, d, E, k, I, W, h, st, true));
-        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, row_w, T, d, E, k, I, W, nullptr, y, &ctrl->status, st, true));
+        if (!norm) {
+            MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, row_w, T, d, E, k, I, W, nullptr, y, &ctrl->status, st,
+                                      true));
+            return MOE_OK;
+        }
+        uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
+        MOE_CUDA(launch_gemv_down(h, perm, offsets, plan, nullptr, T, d, E, k, I, W, y_perm, nullptr, &ctrl->status,
+                                  st, true));
+        MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
         return MOE_OK;
     }
     MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
@@ -325,8 +344,21 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
     uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
     MOE_CUDA(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, h, h_s, &ctrl->status, st, true));
     MOE_CUDA(launch_umma_down(h, h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, y_perm, &ctrl->status, st, true));
-    MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
+    if (norm) MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
+    else MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
     return MOE_OK;
+}
+
+moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k, int I,
+                             const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids, float* w,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return layer_forward(x, W_r, b, T, d, E, k, I, W, fmt, false, 0.f, y, ids, w, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+moe_status moe_layer_forward_norm(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                                  int I, const moe_expert_weights* W, moe_act_fmt fmt, float eps, uint16_t* y,
+                                  int32_t* ids, float* w, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return layer_forward(x, W_r, b, T, d, E, k, I, W, fmt, true, eps, y, ids, w, ws, ws_bytes, (cudaStream_t)stream);
 }
 
 // ---------------------------------------------------------------- synthetic inputs

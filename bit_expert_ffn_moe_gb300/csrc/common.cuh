@@ -81,6 +81,7 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
         L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);
     } else {
         L.h = take(sizeof(uint16_t) * (size_t)P * I);
+        L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);  // expert outputs when they are normalised
     }
     L.total = off;
     return L;
@@ -309,6 +310,9 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
 bool gemv_supported(int d, int I);
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                            uint16_t* y, cudaStream_t st, bool pdl);
+// Weighted sum of the expert outputs, each first divided by its RMS over d (sqrt(mean + eps)).
+cudaError_t launch_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
+                                float eps, uint16_t* y, cudaStream_t st, bool pdl);
 
 cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets,
                            int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,

@@ -831,6 +831,65 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_
     pdl_launch_dependents();
 }
 
+// ------------------------------------------------------------------ weighted sum of normalised expert outputs
+// Muse Spark Open explainer, section 9: each chosen expert's output is normalised before the
+// router-weighted sum; the normalisation is RMSNorm over the d features (no learned scale).
+// One CTA per token.  Pass 1: the sum of squares of each slot row, per thread over its 8-feature
+// units in increasing order, then a warp butterfly, then the warps in order; the slot's factor
+// is w[t][j] / sqrt(ss / d + eps).  Pass 2: y = sum_j factor_j * y_perm[row_j], fp32 in slot order.
+__global__ void combine_norm_kernel(const uint16_t* __restrict__ y_perm, const int32_t* __restrict__ inv_pos,
+                                    const float* __restrict__ w, int T, int k, int d, float eps,
+                                    uint16_t* __restrict__ y) {
+    __shared__ float red[kMaxK][32];
+    __shared__ float factor[kMaxK];
+    pdl_wait();
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int units = d / 8;
+    for (int j = 0; j < k; ++j) {
+        const uint16_t* row = y_perm + (size_t)inv_pos[(size_t)t * k + j] * d;
+        float ss = 0.f;
+        for (int c = tid; c < units; c += blockDim.x) {
+            const uint4 u = *reinterpret_cast<const uint4*>(row + 8 * c);
+            const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                const float lo = bf16_bits_to_f32(v[m] & 0xFFFF), hi = bf16_bits_to_f32(v[m] >> 16);
+                ss = fmaf(lo, lo, ss);
+                ss = fmaf(hi, hi, ss);
+            }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) red[j][warp] = ss;
+    }
+    __syncthreads();
+    if (tid < k) {
+        float ss = 0.f;
+        for (int i = 0; i < nwarps; ++i) ss += red[tid][i];
+        factor[tid] = w[(size_t)t * k + tid] / sqrtf(ss / (float)d + eps);
+    }
+    __syncthreads();
+    for (int c = tid; c < units; c += blockDim.x) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j = 0; j < k; ++j) {
+            const float fj = factor[j];
+            const uint4 u = *reinterpret_cast<const uint4*>(y_perm + (size_t)inv_pos[(size_t)t * k + j] * d + 8 * c);
+            const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                acc[2 * m] = fmaf(fj, bf16_bits_to_f32(v[m] & 0xFFFF), acc[2 * m]);
+                acc[2 * m + 1] = fmaf(fj, bf16_bits_to_f32(v[m] >> 16), acc[2 * m + 1]);
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            o[m] = (uint32_t)f32_to_bf16_bits(acc[2 * m]) | ((uint32_t)f32_to_bf16_bits(acc[2 * m + 1]) << 16);
+        *reinterpret_cast<uint4*>(y + (size_t)t * d + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    pdl_launch_dependents();
+}
+
+
 // ------------------------------------------------------------------ launchers
 
 static int bpl_for(int K) {
@@ -976,6 +1035,15 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
     const dim3 grid(d / outs, (T + tch - 1) / tch);
     const void* f = y ? down_kernel<true>(bpl) : down_kernel<false>(bpl);
     return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
+}
+
+cudaError_t launch_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
+                                float eps, uint16_t* y, cudaStream_t st, bool pdl) {
+    if (T == 0) return cudaSuccess;
+    // few tokens (decode): wide CTAs so that one token's rows stream with many loads in flight
+    const int threads = T < 2 * sm_count() ? 1024 : 256;
+    void* args[] = {&y_perm, &inv_pos, &w, &T, &k, &d, &eps, &y};
+    return launch_kernel((const void*)combine_norm_kernel, dim3((unsigned)T), dim3(threads), 0, st, pdl, args);
 }
 
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,

@@ -74,8 +74,9 @@ def make_workspace(T: int, d: int, E: int, k: int, I: int, fmt: int, device="cud
 
 
 def layer_forward(layer: DeviceLayer, x: torch.Tensor, fmt: int, ws: Optional[torch.Tensor] = None,
-                  want_routing: bool = False, stream=None):
-    """y = MoE(x) for bf16 x [T][d] (as int16/uint16 bit patterns or torch.bfloat16)."""
+                  want_routing: bool = False, stream=None, expert_norm_eps: Optional[float] = None):
+    """y = MoE(x) for bf16 x [T][d] (as int16/uint16 bit patterns or torch.bfloat16); with
+    expert_norm_eps, each expert output is normalised before the weighted sum."""
     cfg = layer.cfg
     T = x.shape[0]
     if ws is None:
@@ -83,8 +84,12 @@ def layer_forward(layer: DeviceLayer, x: torch.Tensor, fmt: int, ws: Optional[to
     y = torch.empty((T, cfg.d), dtype=torch.bfloat16, device=x.device)
     ids = torch.empty((T, cfg.k), dtype=torch.int32, device=x.device) if want_routing else None
     w = torch.empty((T, cfg.k), dtype=torch.float32, device=x.device) if want_routing else None
-    B.moe_layer_forward(x, layer.W_r, layer.b, T, cfg.d, cfg.E, cfg.k, cfg.I, layer.weights, fmt, y, ids, w, ws,
-                        stream=stream)
+    if expert_norm_eps is None:
+        B.moe_layer_forward(x, layer.W_r, layer.b, T, cfg.d, cfg.E, cfg.k, cfg.I, layer.weights, fmt, y, ids, w, ws,
+                            stream=stream)
+    else:
+        B.moe_layer_forward_norm(x, layer.W_r, layer.b, T, cfg.d, cfg.E, cfg.k, cfg.I, layer.weights, fmt,
+                                 expert_norm_eps, y, ids, w, ws, stream=stream)
     if want_routing:
         return y, ids, w
     return y

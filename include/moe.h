@@ -225,6 +225,16 @@ moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, c
 moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                        uint16_t* y, moe_stream_t stream);
 
+/* Weighted sum of normalised expert outputs (Muse Spark Open explainer, section 9: each chosen
+ * expert's output is normalised before the router-weighted sum; the normalisation is not named
+ * there, and this library takes RMSNorm over the d features with no learned scale):
+ *   y[t] = sum_j w[t][j] * v_j / sqrt(mean_c(v_j[c]^2) + eps),  v_j = y_perm[inv_pos[t*k+j]],
+ * the mean over the d features of the bf16 row, the sum of squares and the weighted sum in
+ * fp32 (slot order j = 0..k-1), stored as bf16 [T][d].  Layouts as for moe_combine.
+ * eps in (0, 1] (MOE_ERR_INVALID_ARG otherwise); 1e-6 is the reading used by the tests. */
+moe_status moe_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
+                            float eps, uint16_t* y, moe_stream_t stream);
+
 /* The whole layer in one call: route -> permute -> up+SwiGLU -> down -> combine, all on
  * `stream`, with no host synchronisation.  y bf16 [T][d].  ids/w (optional, may be NULL)
  * receive the routing.  For MOE_ACT_BF16 the down GEMV and the weighted sum are fused (the
@@ -232,6 +242,14 @@ moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const flo
 moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                              int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids,
                              float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The layer with each expert's output normalised before the weighted sum (moe_combine_norm's
+ * definition; eps in (0, 1]).  Same arguments, workspace and stream rules as moe_layer_forward;
+ * the per-expert bf16 outputs go through the workspace (both formats), then the normalised
+ * weighted sum produces y. */
+moe_status moe_layer_forward_norm(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                                  int I, const moe_expert_weights* W, moe_act_fmt fmt, float eps, uint16_t* y,
+                                  int32_t* ids, float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- failure-detection self-test
  * Not part of the layer.  Every barrier wait in the library's kernels is bounded: when it runs out

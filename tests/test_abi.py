@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 4
+    assert B.moe_abi_version() == 5
     assert B.status_string(0) == "MOE_OK"
     assert B.status_string(5) == "MOE_ERR_TIMEOUT"
 
@@ -66,3 +66,15 @@ def test_selftest_arguments_are_checked_on_the_host(lib):
     assert lib.moe_selftest_wait_timeout(None, 0, 10, None) == B.MOE_ERR_WORKSPACE
     assert lib.moe_selftest_wait_timeout(256, 1 << 20, 0, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_selftest_wait_timeout(256, 1 << 20, 2000000, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_expert_norm_arguments_are_checked_on_the_host(lib):
+    # eps must lie in (0, 1]; shapes follow moe_combine; both are rejected before any launch
+    for eps in (0.0, -1e-6, 2.0, float("nan")):
+        assert lib.moe_combine_norm(256, 256, 256, 4, 2, 256, eps, 256, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine_norm(256, 256, 256, 4, 33, 256, 1e-6, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_combine_norm(256, 256, 256, 4, 2, 100, 1e-6, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_combine_norm(256, 256, 256, 0, 2, 256, 1e-6, 256, None) == B.MOE_OK
+    W = B.moe_expert_weights()
+    assert lib.moe_layer_forward_norm(256, 256, None, 4, 256, 8, 2, 512, W, B.MOE_ACT_BF16, 0.0, 256, None, None,
+                                      256, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
