@@ -241,9 +241,8 @@ def run_gpu(args, cfg, rank, world, local):
 
     def step(s, st, record_routing=True):
         L = layers[s % len(layers)]
-        B.moe_layer_forward(xs[s % n_x], L.W_r, L.b, T, d, E, k, I, L.weights, fmt, y,
-                            ids[s] if record_routing else None, wts[s] if record_routing else None, ws,
-                            stream=st.cuda_stream)
+        layer_call(B, args, xs[s % n_x], L, T, d, E, k, I, fmt, y, ids[s] if record_routing else None,
+                   wts[s] if record_routing else None, ws, st.cuda_stream)
 
     # warm-up (eager), then capture the K timed steps in one CUDA graph
     with torch.cuda.stream(stream):
@@ -309,7 +308,8 @@ def run_gpu(args, cfg, rank, world, local):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(fmt), "data": "synthetic",
-        "config": {"workload": cfg.note, "T": T, "d": d, "E": E, "k": k, "I": I, "act": args.fmt,
+        "config": {"workload": cfg.note + (" + per-expert RMSNorm before the weighted sum" if norm_eps(args) else ""),
+                   "T": T, "d": d, "E": E, "k": k, "I": I, "act": args.fmt, "expert_norm_eps": norm_eps(args),
                    "layer_copies_rotated": len(layers),
                    "l2": "inputs larger than L2: %d layer copies, %.1f GB of expert weights rotated"
                          % (len(layers), len(layers) * E * expert_bytes(d, I) / 1e9),
@@ -317,7 +317,7 @@ def run_gpu(args, cfg, rank, world, local):
         "layer_roofline": layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, world),
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(fmt, T, d, E, k) * args.steps,
+        "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
     }
@@ -347,11 +347,29 @@ def dtype_name(fmt):
     return "mxfp4 weights x bf16 activations, fp32 accumulate" if fmt == 0 else "mxfp4 x mxfp4, fp32 accumulate"
 
 
-def launches_per_step(fmt, T, d, E, k):
+EXPERT_NORM_EPS = 1e-6
+
+
+def norm_eps(args):
+    """eps of the per-expert output normalisation, or None when the layer runs without it."""
+    return EXPERT_NORM_EPS if getattr(args, "expert_norm", False) else None
+
+
+def layer_call(B, args, x, L, T, d, E, k, I, fmt, y, ids, w, ws, stream):
+    """One layer call through the C ABI (with the per-expert normalisation when asked for)."""
+    if norm_eps(args) is None:
+        B.moe_layer_forward(x, L.W_r, L.b, T, d, E, k, I, L.weights, fmt, y, ids, w, ws, stream=stream)
+    else:
+        B.moe_layer_forward_norm(x, L.W_r, L.b, T, d, E, k, I, L.weights, fmt, norm_eps(args), y, ids, w, ws,
+                                 stream=stream)
+
+
+def launches_per_step(fmt, T, d, E, k, expert_norm=False):
     # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
-    # gate/up, down+sum.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum
+    # gate/up, down+sum; with the expert normalisation the down GEMV and the (normalising) sum are
+    # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum
     if fmt == 0:
-        return 3 if T <= 8 else 7
+        return (3 if T <= 8 else 7) + (1 if expert_norm else 0)
     return 10
 
 
@@ -485,7 +503,7 @@ def end_to_end(args, cfg, layers, xs_host, fmt, dev, stream):
     def one(s):
         L = layers[s % len(layers)]
         x_dev.copy_(x_pin[s % x_pin.shape[0]], non_blocking=True)
-        B.moe_layer_forward(x_dev, L.W_r, L.b, T, d, E, k, I, L.weights, fmt, y_dev, None, None, ws, stream=st)
+        layer_call(B, args, x_dev, L, T, d, E, k, I, fmt, y_dev, None, None, ws, st)
         y_pin[s].copy_(y_dev, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -544,7 +562,7 @@ def oracle_sample(args, cfg, n_tokens):
                 weights(int(e))
         t0 = time.perf_counter()
         for xb in xs:
-            O.moe_layer(xb, W_r, b, cfg.k, weights, act)
+            O.moe_layer(xb, W_r, b, cfg.k, weights, act, expert_norm_eps=norm_eps(args))
         dt = time.perf_counter() - t0
         return dict(value=round(cfg.T * n_tokens / dt, 3), unit=UNIT, cores=threads, kind="oracle",
                     sample="%d layer calls of T=%d (full routing, all %d touched experts per call, fp64 oracle), "
@@ -559,7 +577,7 @@ def oracle_sample(args, cfg, n_tokens):
     for e in np.unique(ids[tokens]):
         weights(int(e))
     t0 = time.perf_counter()
-    O.moe_layer(xb[tokens], W_r, b, cfg.k, weights, act)
+    O.moe_layer(xb[tokens], W_r, b, cfg.k, weights, act, expert_norm_eps=norm_eps(args))
     t_exp = time.perf_counter() - t0
     per_tok = t_route / cfg.T + t_exp / len(tokens)
     return dict(value=round(1.0 / per_tok, 3), unit=UNIT, cores=threads, kind="oracle",
@@ -583,8 +601,9 @@ def run_reference(args, cfg, rank, world):
     out = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": n,
            "warmup": 1, "ms_per_step": round(1e3 * cfg.T / res["value"], 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-           "config": {"workload": cfg.note, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I,
-                      "act": args.fmt},
+           "config": {"workload": cfg.note + (" + per-expert RMSNorm before the weighted sum" if norm_eps(args) else ""),
+                      "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I, "act": args.fmt,
+                      "expert_norm_eps": norm_eps(args)},
            "impl": "reference",
            "cpu_baseline": {"value": res["value"], "unit": UNIT, "cores": res["cores"], "kind": "oracle",
                             "sample": res["sample"] + "; %d of the %d requested steps" % (n, args.steps)},
@@ -603,6 +622,8 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYER_COPIES)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--expert-norm", action="store_true",
+                    help="normalise each expert output (RMSNorm over d, eps 1e-6) before the weighted sum")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     args = ap.parse_args()

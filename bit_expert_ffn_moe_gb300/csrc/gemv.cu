@@ -803,7 +803,8 @@ gemv_down_kernel(const GemvArgs a) {
 }
 
 // ------------------------------------------------------------------ weighted sum (unfused)
-// One thread per (token, 8 consecutive features): y = sum_j w[t][j] * y_perm[inv_pos[t*k+j]].
+// One thread per (token, 8 consecutive features): y = sum_j w[t][j] * y_perm[inv_pos[t*k+j]]; a row
+// index outside [0, T k) is not read (that slot contributes nothing).
 __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_t* __restrict__ inv_pos,
                                const float* __restrict__ w, int T, int k, int d, uint16_t* __restrict__ y) {
     pdl_wait();
@@ -813,8 +814,10 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_
         const int t = (int)(i / per_row), c = (int)(i % per_row);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
+            const int r = inv_pos[(size_t)t * k + j];
+            if ((unsigned)r >= (unsigned)(T * k)) continue;  // not a row of y_perm: contributes nothing
             const float wj = w[(size_t)t * k + j];
-            const uint4 u = *reinterpret_cast<const uint4*>(y_perm + (size_t)inv_pos[(size_t)t * k + j] * d + 8 * c);
+            const uint4 u = *reinterpret_cast<const uint4*>(y_perm + (size_t)r * d + 8 * c);
             const uint32_t v[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -837,27 +840,35 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_
 // One CTA per token.  Pass 1: the sum of squares of each slot row, per thread over its 8-feature
 // units in increasing order, then a warp butterfly, then the warps in order; the slot's factor
 // is w[t][j] / sqrt(ss / d + eps).  Pass 2: y = sum_j factor_j * y_perm[row_j], fp32 in slot order.
-__global__ void combine_norm_kernel(const uint16_t* __restrict__ y_perm, const int32_t* __restrict__ inv_pos,
-                                    const float* __restrict__ w, int T, int k, int d, float eps,
-                                    uint16_t* __restrict__ y) {
+// A row index outside [0, T k) is not read: that slot contributes nothing.
+__global__ void __launch_bounds__(1024) combine_norm_kernel(const uint16_t* __restrict__ y_perm,
+                                                            const int32_t* __restrict__ inv_pos,
+                                                            const float* __restrict__ w, int T, int k, int d,
+                                                            float eps, uint16_t* __restrict__ y) {
     __shared__ float red[kMaxK][32];
     __shared__ float factor[kMaxK];
+    __shared__ int rows[kMaxK];
     pdl_wait();
     const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     const int units = d / 8;
+    if (tid < k) {
+        const int r = inv_pos[(size_t)t * k + tid];
+        rows[tid] = ((unsigned)r < (unsigned)(T * k)) ? r : -1;
+    }
+    __syncthreads();
     for (int j = 0; j < k; ++j) {
-        const uint16_t* row = y_perm + (size_t)inv_pos[(size_t)t * k + j] * d;
         float ss = 0.f;
-        for (int c = tid; c < units; c += blockDim.x) {
-            const uint4 u = *reinterpret_cast<const uint4*>(row + 8 * c);
-            const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+        if (rows[j] >= 0)
+            for (int c = tid; c < units; c += blockDim.x) {
+                const uint4 u = *reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * d + 8 * c);
+                const uint32_t v[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const float lo = bf16_bits_to_f32(v[m] & 0xFFFF), hi = bf16_bits_to_f32(v[m] >> 16);
-                ss = fmaf(lo, lo, ss);
-                ss = fmaf(hi, hi, ss);
+                for (int m = 0; m < 4; ++m) {
+                    const float lo = bf16_bits_to_f32(v[m] & 0xFFFF), hi = bf16_bits_to_f32(v[m] >> 16);
+                    ss = fmaf(lo, lo, ss);
+                    ss = fmaf(hi, hi, ss);
+                }
             }
-        }
         ss = warp_sum(ss);
         if (lane == 0) red[j][warp] = ss;
     }
@@ -865,14 +876,15 @@ __global__ void combine_norm_kernel(const uint16_t* __restrict__ y_perm, const i
     if (tid < k) {
         float ss = 0.f;
         for (int i = 0; i < nwarps; ++i) ss += red[tid][i];
-        factor[tid] = w[(size_t)t * k + tid] / sqrtf(ss / (float)d + eps);
+        factor[tid] = rows[tid] >= 0 ? w[(size_t)t * k + tid] / sqrtf(ss / (float)d + eps) : 0.f;
     }
     __syncthreads();
     for (int c = tid; c < units; c += blockDim.x) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j = 0; j < k; ++j) {
+            if (rows[j] < 0) continue;
             const float fj = factor[j];
-            const uint4 u = *reinterpret_cast<const uint4*>(y_perm + (size_t)inv_pos[(size_t)t * k + j] * d + 8 * c);
+            const uint4 u = *reinterpret_cast<const uint4*>(y_perm + (size_t)rows[j] * d + 8 * c);
             const uint32_t v[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
@@ -1040,7 +1052,7 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
 cudaError_t launch_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                                 float eps, uint16_t* y, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
-    // few tokens (decode): wide CTAs so that one token's rows stream with many loads in flight
+    // few tokens (decode): wide CTAs, so that one token's rows stream with many loads in flight
     const int threads = T < 2 * sm_count() ? 1024 : 256;
     void* args[] = {&y_perm, &inv_pos, &w, &T, &k, &d, &eps, &y};
     return launch_kernel((const void*)combine_norm_kernel, dim3((unsigned)T), dim3(threads), 0, st, pdl, args);

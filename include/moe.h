@@ -221,7 +221,9 @@ moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, c
                            uint16_t* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Weighted sum (section 9): y[t] = sum_j w[t][j] * y_perm[inv_pos[t*k+j]] accumulated in fp32
- * in slot order j = 0..k-1, stored as bf16 [T][d]. */
+ * in slot order j = 0..k-1, stored as bf16 [T][d].  inv_pos comes from moe_permute; an entry
+ * outside [0, T*k) is not read (that slot contributes nothing), so a bad index cannot make the
+ * kernel read outside y_perm. */
 moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                        uint16_t* y, moe_stream_t stream);
 
@@ -230,7 +232,8 @@ moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const flo
  * there, and this library takes RMSNorm over the d features with no learned scale):
  *   y[t] = sum_j w[t][j] * v_j / sqrt(mean_c(v_j[c]^2) + eps),  v_j = y_perm[inv_pos[t*k+j]],
  * the mean over the d features of the bf16 row, the sum of squares and the weighted sum in
- * fp32 (slot order j = 0..k-1), stored as bf16 [T][d].  Layouts as for moe_combine.
+ * fp32 (slot order j = 0..k-1), stored as bf16 [T][d].  Layouts and the inv_pos rule as for
+ * moe_combine.
  * eps in (0, 1] (MOE_ERR_INVALID_ARG otherwise); 1e-6 is the reading used by the tests. */
 moe_status moe_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                             float eps, uint16_t* y, moe_stream_t stream);
