@@ -439,9 +439,20 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, 
 
 // ------------------------------------------------------------------ permutation (any T)
 
-__global__ void count_kernel(const int32_t* __restrict__ ids, int P, int32_t* counts) {
+// Histogram of the chosen experts: each CTA counts its share of the pairs in shared memory, then
+// adds its nonzero counts to the global ones (few global atomics even when the load is skewed).
+__global__ void count_kernel(const int32_t* __restrict__ ids, int P, int E, int32_t* counts) {
+    __shared__ int hist[kMaxE];
     pdl_wait();
-    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) atomicAdd(&counts[ids[p]], 1);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < P; p += gridDim.x * blockDim.x) {
+        const int e = ids[p];
+        if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);  // an id outside [0, E) is not counted
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (hist[e] != 0) atomicAdd(&counts[e], hist[e]);
 }
 
 __global__ void plan_kernel(int E, int32_t* counts_out, int32_t* offsets, PlanView plan) {
@@ -493,9 +504,9 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
     if (err != cudaSuccess) return err;
     int P = T * k;
     if (P > 0) {
-        int blocks = (P + 255) / 256;
-        if (blocks > 1024) blocks = 1024;
-        void* a1[] = {&ids, &P, &plan.counts};
+        int blocks = (P + 1023) / 1024;  // about 1024 pairs per CTA
+        if (blocks > 256) blocks = 256;
+        void* a1[] = {&ids, &P, &E, &plan.counts};
         err = launch_kernel((const void*)count_kernel, dim3(blocks), dim3(256), 0, st, false, a1);
         if (err != cudaSuccess) return err;
     }
@@ -536,10 +547,10 @@ __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks
     }
 }
 
-// One thread per (padded row, 32-element block).
 // One warp per padded row: the row's expert comes from a binary search over the padded offsets
 // cached in shared memory; lanes copy consecutive 16-byte blocks of the token's quantised row
-// into the tensor-core code tiles (8 lanes fill one 128-byte line) and write its scale bytes.
+// into the tensor-core code tiles (8 lanes fill one 128-byte line), then its scale bytes four
+// at a time.
 __global__ void __launch_bounds__(256)
 act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, int d, int E, int64_t pad_rows,
                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_token, PlanView plan,
@@ -564,8 +575,11 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
         for (int blk = lane; blk < nb; blk += 32) {
             const uint4 v = real ? src[blk] : make_uint4(0, 0, 0, 0);
             *reinterpret_cast<uint4*>(xa + mma_tile_offset(r, blk, d)) = v;
-            xa_s[mma_scale_offset(r, blk, d)] = real ? xs[(size_t)t * nb + blk] : (uint8_t)0;
         }
+        // scales: blocks 4q .. 4q+3 of a row are 4 consecutive bytes of one scale atom (and of xs)
+        const uint32_t* srcs = reinterpret_cast<const uint32_t*>(xs + (size_t)t * nb);
+        for (int q = lane; q < nb / 4; q += 32)
+            *reinterpret_cast<uint32_t*>(xa_s + mma_scale_offset(r, 4 * q, d)) = real ? srcs[q] : 0u;
     }
     (void)pad_rows;
 }

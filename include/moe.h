@@ -189,6 +189,8 @@ moe_status moe_route_noalloc(const uint16_t* x, const float* W_r, const float* b
  *   offsets[E+1]   exclusive prefix sum of counts
  *   perm_token[P]  token of permuted row r (P = T*k)
  *   inv_pos[P]     permuted row of pair (t, j) at index t*k + j
+ * ids as moe_route returns them: each token's k ids distinct and in [0, E).  An id outside
+ * [0, E) is not counted and its pair gets no row (its inv_pos entry is not written).
  * For MOE_ACT_MXFP4 it also quantises every token row of x once and writes the activation
  * operand of the [moe_padded_rows][d] matrix of permuted rows in padded expert-grouped order
  * (expert e's rows start at a multiple of 128; padding rows are zero): xa in the tensor-core
