@@ -40,6 +40,11 @@
  *       Expert outputs (y_perm) are rounded to fp32 then bf16, as the GPU stores them; the
  *       weighted sum is formed in fp64 over the k slots in slot order, rounded to fp32, then
  *       to bf16.
+ *   R9  shared latent projections (optional; [MUSE] s.9: one matrix shared by the 8 experts
+ *       narrows the token from 8192 to 4096 before them and one widens the weighted sum back
+ *       to 8192): plain MXFP4 matrix products, out[n] = sum_c a[c] W[n][c], with the input row
+ *       in the activation format of R7 (bf16 values, or MXFP4-quantised), fp64 accumulation,
+ *       the output rounded to fp32 then bf16 like an expert output.
  *   R8  expert output normalisation (optional; [MUSE] s.9 says each chosen expert's output is
  *       normalised before the weighted sum, without naming the normalisation): RMSNorm over
  *       the d output features of the expert's (bf16) output row, v / sqrt(mean(v^2) + eps),
@@ -392,6 +397,26 @@ void oracle_combine(const float* y_perm, const int32_t* rows, const float* w, in
                 acc += (double)w[(int64_t)t * k + j] * (double)y_perm[(int64_t)rows[(int64_t)t * k + j] * d + c];
             y[(int64_t)s * d + c] = round_to_bf16((float)acc);
         }
+    }
+}
+
+/* Dense MXFP4 linear map (R9): out[r][n] = sum_c a[r][c] * W[n][c] for n_rows rows of the
+ * activation operand a [n_rows][K] (from oracle_activation_row), W MXFP4 [N][K]; fp64
+ * accumulation, rounded to fp32 then bf16. */
+void oracle_dense_linear(const float* a, int n_rows, int K, int N, const uint8_t* Wq, const uint8_t* Ws, float* out) {
+#pragma omp parallel
+    {
+        double* wrow = (double*)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(dynamic, 16)
+        for (int n = 0; n < N; ++n) {
+            weight_row(Wq, Ws, n, K, wrow);
+            for (int r = 0; r < n_rows; ++r) {
+                double acc = 0.0;
+                for (int c = 0; c < K; ++c) acc += (double)a[(int64_t)r * K + c] * wrow[c];
+                out[(int64_t)r * N + n] = round_to_bf16((float)acc);
+            }
+        }
+        free(wrow);
     }
 }
 

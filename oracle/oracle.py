@@ -6,7 +6,7 @@ library and never imports it; inputs come from the seeded generators and are pas
 as numpy arrays.
 
 Each function follows one step of the layer as the sources state it (see the header of
-``moe_oracle.c`` for the citations and the readings R1-R8 taken where they are silent):
+``moe_oracle.c`` for the citations and the readings R1-R9 taken where they are silent):
 
 * ``router_logits``  -- Muse Spark Open explainer, section 8 (one FP32 matrix product)
 * ``topk_softmax``   -- section 8 (best k of E, a set) and section 9 (weights sum to 1)
@@ -16,6 +16,7 @@ Each function follows one step of the layer as the sources state it (see the hea
 * ``combine``        -- section 9 (weighted sum over the chosen experts)
 * ``expert_norm``    -- section 9 (each chosen expert's output is normalised before the sum;
                         reading R8: RMSNorm over d, no learned scale)
+* ``dense_linear``   -- section 9 (the shared latent projections around the experts; reading R9)
 """
 from __future__ import annotations
 
@@ -74,6 +75,7 @@ def _load():
         "oracle_expert_ffn": (None, [P, i32, i32, i32, P, P, P, P, P, P, i32, P, P, P, P]),
         "oracle_combine": (None, [P, P, P, i32, P, i32, i32, P]),
         "oracle_expert_norm": (None, [P, i64, i32, ctypes.c_double, P]),
+        "oracle_dense_linear": (None, [P, i32, i32, i32, P, P, P]),
         "oracle_float_to_bf16_bits": (ctypes.c_uint16, [ctypes.c_float]),
         "oracle_bf16_bits_to_float": (ctypes.c_float, [ctypes.c_uint16]),
     }
@@ -237,6 +239,20 @@ def combine(y_perm: np.ndarray, rows: np.ndarray, w: np.ndarray, tokens: np.ndar
 
 
 EXPERT_NORM_EPS = 1e-6
+
+
+def dense_linear(x_bits: np.ndarray, W: tuple, act_fmt: int) -> np.ndarray:
+    """out = a(x) W^T for bf16 rows x [n][K] and W MXFP4 (q [N][K/2], s [N][K/32]) (reading R9):
+    a(x) the activation operand of R7, fp64 accumulation, rounded to fp32 then bf16."""
+    q, s = W
+    n, K = x_bits.shape
+    N = q.shape[0]
+    a = np.ascontiguousarray(activation_rows(x_bits, act_fmt), dtype=np.float32)
+    out = np.empty((n, N), dtype=np.float32)
+    if n:
+        _load().oracle_dense_linear(_ptr(a), n, K, N, _ptr(np.ascontiguousarray(q)), _ptr(np.ascontiguousarray(s)),
+                                    _ptr(out))
+    return out
 
 
 def expert_norm(y: np.ndarray, eps: float = EXPERT_NORM_EPS) -> np.ndarray:

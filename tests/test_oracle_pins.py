@@ -430,3 +430,47 @@ def test_expert_norm_with_identical_experts_is_the_normalised_expert_output():
     v = O.expert_ffn(a, wg, wu, wd, O.ACT_BF16).astype(np.float64)
     ref = v / np.sqrt(np.mean(v ** 2, axis=1, keepdims=True) + 1e-6)
     np.testing.assert_allclose(res["y"], ref, rtol=2 ** -7, atol=1e-6)
+
+
+# ------------------------------------------------------------------ shared latent projections
+
+def test_dense_linear_against_numpy_fp64():
+    """out = x W^T on the dequantised weights (numpy fp64, then bf16), bf16 activation values."""
+    rng = np.random.default_rng(31)
+    n, K, N = 5, 96, 64
+    W = O.mxfp4_pack((rng.standard_normal((N, K)) * 0.05).astype(np.float32))
+    xb = IN.to_bf16_bits(rng.standard_normal((n, K)).astype(np.float32))
+    out = O.dense_linear(xb, W, O.ACT_BF16)
+    ref = IN.bf16_bits_to_f32(xb).astype(np.float64) @ np_unpack(*W).T
+    ref_b = IN.bf16_bits_to_f32(IN.to_bf16_bits(ref.astype(np.float32)))
+    assert np.all(np.abs(out - ref_b) <= np.abs(ref_b) * 2.0 ** -7 + 1e-30)
+    np.testing.assert_allclose(out, ref, rtol=2 ** -7, atol=1e-6)
+
+
+def test_dense_linear_grid_case_is_exact_and_mxfp4_operand_is_used():
+    """W row n holds 1.5 in column 0 and 6 in column 1 (scale 2^0), zeros elsewhere: out[n] =
+    1.5 x0 + 6 x1 exactly.  With x0 = 0.3 the MXFP4 operand rounds x0 within its block (amax 1:
+    scale 2^-2, 0.3 / 0.25 = 1.2 -> 1, so 0.25), which the MXFP4 mode must show."""
+    K, N = 64, 32
+    Wf = np.zeros((N, K), np.float32)
+    Wf[:, 0], Wf[:, 1] = 1.5, 6.0
+    W = O.mxfp4_pack(Wf)
+    x = np.zeros((1, K), np.float32)
+    x[0, 0], x[0, 1] = 0.3, 1.0
+    xb = IN.to_bf16_bits(x)
+    x0 = float(IN.bf16_bits_to_f32(xb)[0, 0])
+    out_bf16 = O.dense_linear(xb, W, O.ACT_BF16)
+    want = IN.bf16_bits_to_f32(IN.to_bf16_bits(np.array([np.float32(1.5 * x0 + 6.0)])))[0]
+    assert np.all(out_bf16 == want)
+    out_mx = O.dense_linear(xb, W, O.ACT_MXFP4)
+    assert np.all(out_mx == np.float32(1.5 * 0.25 + 6.0))
+
+
+def test_dense_linear_scales_exactly_with_powers_of_two():
+    rng = np.random.default_rng(32)
+    n, K, N = 3, 128, 32
+    W = O.mxfp4_pack((rng.standard_normal((N, K)) * 0.05).astype(np.float32))
+    xf = rng.standard_normal((n, K)).astype(np.float32)
+    a = O.dense_linear(IN.to_bf16_bits(xf), W, O.ACT_BF16)
+    b = O.dense_linear(IN.to_bf16_bits(xf * np.float32(8.0)), W, O.ACT_BF16)
+    np.testing.assert_array_equal(b, a * np.float32(8.0))
