@@ -30,6 +30,7 @@ EXPORTED = (
     "moe_mxfp4_scales_to_mma", "moe_mxfp4_codes_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
+    "moe_dense_workspace_size", "moe_dense_linear",
 )
 
 
@@ -48,11 +49,16 @@ class moe_expert_weights(ctypes.Structure):
                  "up_q_mma", "up_s_mma", "down_q_mma", "down_s_mma")]
 
 
+class moe_mxfp4_matrix(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "s", "q_mma", "s_mma")]
+
+
 _lib = None
 P = ctypes.c_void_p
 I32, I64, U32, U64 = ctypes.c_int, ctypes.c_int64, ctypes.c_uint32, ctypes.c_uint64
 SZ = ctypes.c_size_t
 WP = ctypes.POINTER(moe_expert_weights)
+MP = ctypes.POINTER(moe_mxfp4_matrix)
 
 _SIGS = {
     "moe_status_string": (ctypes.c_char_p, [I32]),
@@ -75,6 +81,8 @@ _SIGS = {
     "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
     "moe_layer_forward": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, SZ, P]),
     "moe_combine_norm": (I32, [P, P, P, I32, I32, I32, ctypes.c_float, P, P]),
+    "moe_dense_workspace_size": (SZ, [I32, I32, I32, I32]),
+    "moe_dense_linear": (I32, [P, I32, I32, I32, MP, I32, P, P, SZ, P]),
     "moe_layer_forward_norm": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, ctypes.c_float, P, P, P, P, SZ, P]),
     "moe_synth_weights": (I32, [U64, U32, U32, U32, I64, I64, ctypes.c_float, P, P]),
     "moe_selftest_wait_timeout": (I32, [P, SZ, I32, P]),
@@ -135,6 +143,10 @@ def expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s, gate_q_mma
                           up_q_mma=None, up_s_mma=None, down_q_mma=None, down_s_mma=None) -> moe_expert_weights:
     return moe_expert_weights(*[_p(t) for t in (gate_q, gate_s, up_q, up_s, down_q, down_s, gate_q_mma, gate_s_mma,
                                                 up_q_mma, up_s_mma, down_q_mma, down_s_mma)])
+
+
+def mxfp4_matrix_struct(q, s, q_mma=None, s_mma=None) -> moe_mxfp4_matrix:
+    return moe_mxfp4_matrix(*[_p(t) for t in (q, s, q_mma, s_mma)])
 
 
 # ------------------------------------------------------------------ entry points
@@ -241,6 +253,15 @@ def moe_layer_forward_norm(x, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt,
     _check("moe_layer_forward_norm",
            load().moe_layer_forward_norm(_p(x), _p(W_r), _p(b), T, d, E, k, I, ctypes.byref(W), fmt, float(eps), _p(y),
                                          _p(ids), _p(w), _p(ws), _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_dense_workspace_size(T, K, N, fmt) -> int:
+    return int(load().moe_dense_workspace_size(T, K, N, fmt))
+
+
+def moe_dense_linear(x, T, K, N, W: moe_mxfp4_matrix, fmt, y, ws, ws_bytes=None, stream=None):
+    _check("moe_dense_linear", load().moe_dense_linear(_p(x), T, K, N, ctypes.byref(W), fmt, _p(y), _p(ws),
+                                                       _ws_bytes(ws, ws_bytes), _stream(stream)))
 
 
 def moe_synth_weights(seed, tensor_id, expert_first, n_experts, rows, K, c, out, stream=None):

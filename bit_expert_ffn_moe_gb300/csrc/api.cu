@@ -8,7 +8,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kAbiVersion = 5;
+constexpr int kAbiVersion = 6;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -359,6 +359,64 @@ moe_status moe_layer_forward_norm(const uint16_t* x, const float* W_r, const flo
                                   int I, const moe_expert_weights* W, moe_act_fmt fmt, float eps, uint16_t* y,
                                   int32_t* ids, float* w, void* ws, size_t ws_bytes, moe_stream_t stream) {
     return layer_forward(x, W_r, b, T, d, E, k, I, W, fmt, true, eps, y, ids, w, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+// ---------------------------------------------------------------- dense MXFP4 linear map
+
+static moe_status check_dense_shape(int T, int K, int N, moe_act_fmt fmt) {
+    if (T < 0 || K <= 0 || N <= 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (fmt == MOE_ACT_MXFP4) {
+        if (K % 256 != 0 || N % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    } else if (fmt == MOE_ACT_BF16) {
+        if (K % 128 != 0 || N % 128 != 0 || !gemv_supported(N, K)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    } else {
+        return MOE_ERR_INVALID_ARG;
+    }
+    return MOE_OK;
+}
+
+size_t moe_dense_workspace_size(int T, int K, int N, moe_act_fmt fmt) {
+    if (check_dense_shape(T, K, N, fmt) != MOE_OK) return 0;
+    return dense_layout(T, K, N, fmt).total;
+}
+
+moe_status moe_dense_linear(const uint16_t* x, int T, int K, int N, const moe_mxfp4_matrix* W, moe_act_fmt fmt,
+                            uint16_t* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_dense_shape(T, K, N, fmt));
+    if (T == 0) return MOE_OK;
+    if (!x || !y || !W || !W->q || !W->s || !aligned(x, 16) || !aligned(y, 16) || !aligned(W->q, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (fmt == MOE_ACT_MXFP4 && (!W->q_mma || !W->s_mma || !aligned(W->q_mma, 16) || !aligned(W->s_mma, 16)))
+        return MOE_ERR_INVALID_ARG;
+    const WsLayout L = dense_layout(T, K, N, fmt);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    MOE_TRY(check_device());
+    cudaStream_t st = (cudaStream_t)stream;
+    PlanView plan = plan_view(ws, L, 1);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
+    int32_t* offsets = reinterpret_cast<int32_t*>(at(ws, L.offsets));
+    int32_t* perm = reinterpret_cast<int32_t*>(at(ws, L.perm));
+    // the matrix as the down weights of one expert that holds every row
+    moe_expert_weights Wd = {};
+    Wd.down_q = W->q;
+    Wd.down_s = W->s;
+    Wd.down_q_mma = W->q_mma;
+    Wd.down_s_mma = W->s_mma;
+    MOE_CUDA(launch_dense_plan(T, plan, offsets, perm, st, false));
+    if (fmt == MOE_ACT_BF16) {
+        // launched after the plan kernel has completed: the down GEMV reads the plan before its
+        // own dependency wait, which needs the plan's writer two launches back
+        MOE_CUDA(launch_gemv_down(x, perm, offsets, plan, nullptr, T, N, 1, 1, K, &Wd, y, nullptr, &ctrl->status, st,
+                                  false));
+        return MOE_OK;
+    }
+    uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
+    uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
+    MOE_CUDA(launch_act_quant_gather(x, T, K, 1, 1, offsets, perm, plan, L.pad_rows,
+                                     reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
+                                     xa, xa_s, st, true));
+    MOE_CUDA(launch_umma_down(xa, xa_s, plan, offsets, T, N, 1, 1, K, L.pad_rows, &Wd, y, &ctrl->status, st, true));
+    return MOE_OK;
 }
 
 // ---------------------------------------------------------------- synthetic inputs

@@ -87,6 +87,33 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     return L;
 }
 
+// Workspace of the dense MXFP4 linear map (y = x W^T, x [T][K], W [N][K]), run as the down GEMM
+// of one expert holding every row: control block, one-expert plan, offsets, identity permutation
+// and, for MOE_ACT_MXFP4, the quantised rows and the padded operand tiles of width K.
+inline WsLayout dense_layout(int T, int K, int N, moe_act_fmt fmt) {
+    (void)N;
+    WsLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.ctrl = take(sizeof(Ctrl));
+    L.plan = take(sizeof(int32_t) * (size_t)(4 * 1 + 2 + 8));
+    L.offsets = take(sizeof(int32_t) * 2);
+    L.perm = take(sizeof(int32_t) * (size_t)T);
+    if (fmt == MOE_ACT_MXFP4) {
+        L.pad_rows = padded_rows(T, 1, 1);
+        L.xq = take((size_t)T * K / 2);
+        L.xs = take((size_t)T * K / 32);
+        L.xa = take((size_t)L.pad_rows * K / 2);
+        L.xa_s = take(mma_scale_bytes(L.pad_rows, K));
+    }
+    L.total = off;
+    return L;
+}
+
 inline PlanView plan_view(void* ws, const WsLayout& L, int E) {
     int32_t* p = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + L.plan);
     PlanView v;
@@ -304,12 +331,17 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,
                            cudaStream_t st, bool pdl);
 // y != nullptr: fused weighted sum into y [T][d] using row_w; otherwise bf16 y_perm [P][d].
+// pdl: the one/two-token kernel reads the plan (and offsets) before its dependency wait, so with
+// pdl = true the plan must come from a kernel that completed before the preceding kernel's own wait.
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                              const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,
                              uint16_t* y_perm, uint16_t* y, int* status, cudaStream_t st, bool pdl);
 bool gemv_supported(int d, int I);
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                            uint16_t* y, cudaStream_t st, bool pdl);
+// The plan of one expert holding rows 0..T-1 in order (a dense product as a grouped one).
+cudaError_t launch_dense_plan(int T, PlanView plan, int32_t* offsets, int32_t* perm_token, cudaStream_t st,
+                              bool pdl);
 // Weighted sum of the expert outputs, each first divided by its RMS over d (sqrt(mean + eps)).
 cudaError_t launch_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                                 float eps, uint16_t* y, cudaStream_t st, bool pdl);

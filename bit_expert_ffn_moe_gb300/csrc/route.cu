@@ -460,6 +460,28 @@ __global__ void plan_kernel(int E, int32_t* counts_out, int32_t* offsets, PlanVi
     if (threadIdx.x < 32) build_plan_warp(plan.counts, E, counts_out, offsets, plan);
 }
 
+// One expert (0) holding rows 0..T-1 in order: the plan a dense product runs with.
+__global__ void dense_plan_kernel(int T, PlanView plan, int32_t* offsets, int32_t* perm_token) {
+    pdl_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        const int tiles = (T + kTokTile - 1) / kTokTile;
+        const int used = (T + kPadRows - 1) / kPadRows * kPadRows;  // the expert's padded rows
+        plan.counts[0] = T;
+        plan.pad_offsets[0] = 0;
+        plan.pad_offsets[1] = used;
+        plan.ttile_prefix[0] = 0;
+        plan.ttile_prefix[1] = tiles;
+        plan.active[0] = 0;
+        plan.scalars[0] = T > 0 ? 1 : 0;
+        plan.scalars[1] = tiles;
+        plan.scalars[2] = used;
+        offsets[0] = 0;
+        offsets[1] = T;
+    }
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x) perm_token[i] = i;
+    pdl_launch_dependents();
+}
+
 // One CTA per expert: a stable block-wide compaction over the tokens that chose it.
 __global__ void __launch_bounds__(256)
 scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __restrict__ offsets, PlanView plan,
@@ -517,6 +539,15 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
     if (w == nullptr) row_w = nullptr;
     void* a3[] = {&ids, &T, &k, &offsets, &plan, &perm_token, &inv_pos, &w, &row_w};
     return launch_kernel((const void*)scatter_kernel, dim3(E), dim3(256), 0, st, pdl, a3);
+}
+
+cudaError_t launch_dense_plan(int T, PlanView plan, int32_t* offsets, int32_t* perm_token, cudaStream_t st,
+                              bool pdl) {
+    int blocks = (T + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 152) blocks = 152;
+    void* args[] = {&T, &plan, &offsets, &perm_token};
+    return launch_kernel((const void*)dense_plan_kernel, dim3(blocks), dim3(256), 0, st, pdl, args);
 }
 
 // ------------------------------------------------------------------ MXFP4 activation operand

@@ -92,7 +92,7 @@ typedef struct moe_expert_weights {
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status s);
 
-/* ABI version of this header (incremented on incompatible changes). */
+/* ABI version of this header (incremented on changes to the entry points). */
 int moe_abi_version(void);
 
 /* Description of the CUDA error behind the calling thread's last MOE_ERR_CUDA (static string). */
@@ -255,6 +255,29 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
 moe_status moe_layer_forward_norm(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                   int I, const moe_expert_weights* W, moe_act_fmt fmt, float eps, uint16_t* y,
                                   int32_t* ids, float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* ---------------------------------------------------------------- dense MXFP4 linear map
+ * The shared latent projections of Muse Spark Open explainer, section 9 (one matrix, shared by
+ * all experts, narrows each token from 8192 to 4096 features before the router and the experts;
+ * another widens the weighted sum back): y[t][n] = sum_c a(x[t])[c] * W[n][c] for x bf16 [T][K],
+ * W MXFP4 [N][K], y bf16 [T][N] (fp32 accumulation, rounded once to bf16).  a(x) is the
+ * activation operand of the format: MOE_ACT_BF16 uses the bf16 values (K % 128 == 0,
+ * N % 128 == 0, K <= 8192, N <= 8192); MOE_ACT_MXFP4 quantises each row's 32-element blocks
+ * like moe_permute does and runs the tcgen05 GEMM (K % 256 == 0, N % 256 == 0; W's
+ * tensor-core copies q_mma / s_mma required).  A latent layer is moe_dense_linear(W_in) ->
+ * moe_layer_forward with d = the latent width -> moe_dense_linear(W_out).
+ * ws: moe_dense_workspace_size(T, K, N, fmt) bytes, 256-byte aligned, initialised with
+ * moe_workspace_init; device-side timeouts are reported through it (moe_get_device_status). */
+typedef struct {
+    const uint8_t* q;     /* codes  [N][K/2] */
+    const uint8_t* s;     /* scales [N][K/32] */
+    const uint8_t* q_mma; /* tensor-core code tiles (moe_mxfp4_codes_to_mma), MOE_ACT_MXFP4 only */
+    const uint8_t* s_mma; /* tensor-core scale layout (moe_mxfp4_scales_to_mma), MOE_ACT_MXFP4 only */
+} moe_mxfp4_matrix;
+
+size_t moe_dense_workspace_size(int T, int K, int N, moe_act_fmt fmt);  /* 0 for an unsupported shape */
+moe_status moe_dense_linear(const uint16_t* x, int T, int K, int N, const moe_mxfp4_matrix* W, moe_act_fmt fmt,
+                            uint16_t* y, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* ---------------------------------------------------------------- failure-detection self-test
  * Not part of the layer.  Every barrier wait in the library's kernels is bounded: when it runs out

@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 5
+    assert B.moe_abi_version() == 6
     assert B.status_string(0) == "MOE_OK"
     assert B.status_string(5) == "MOE_ERR_TIMEOUT"
 
@@ -78,3 +78,15 @@ def test_expert_norm_arguments_are_checked_on_the_host(lib):
     W = B.moe_expert_weights()
     assert lib.moe_layer_forward_norm(256, 256, None, 4, 256, 8, 2, 512, W, B.MOE_ACT_BF16, 0.0, 256, None, None,
                                       256, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_dense_linear_shapes_and_arguments_are_checked_on_the_host(lib):
+    assert B.moe_dense_workspace_size(4, 8192, 4096, B.MOE_ACT_MXFP4) > B.moe_dense_workspace_size(4, 8192, 4096, 0)
+    assert B.moe_dense_workspace_size(4, 384, 256, B.MOE_ACT_MXFP4) == 0    # K % 256 on the MXFP4 path
+    assert B.moe_dense_workspace_size(4, 384, 256, B.MOE_ACT_BF16) > 0
+    assert B.moe_dense_workspace_size(4, 200, 256, B.MOE_ACT_BF16) == 0     # K % 128
+    assert B.moe_dense_workspace_size(4, 16384, 256, B.MOE_ACT_BF16) == 0   # K <= 8192 on the GEMV path
+    W = B.moe_mxfp4_matrix()
+    assert lib.moe_dense_linear(256, 4, 256, 256, W, B.MOE_ACT_BF16, 256, 256, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_dense_linear(256, 4, 200, 256, W, B.MOE_ACT_BF16, 256, 256, 1 << 20, None) == \
+        B.MOE_ERR_UNSUPPORTED_SHAPE
