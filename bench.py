@@ -224,25 +224,37 @@ def run_gpu(args, cfg, rank, world, local):
     init_dist(world, "nccl")
     B.load(build_if_missing=False)
     fmt = B.MOE_ACT_BF16 if args.fmt == "bf16" else B.MOE_ACT_MXFP4
-    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I  # d: the model width of x and y
+    cm = moe_cfg(args, cfg)  # the layer's configuration (its width dl = cm.d)
+    dl = cm.d
     n_calls = max(cfg.calls, 1)
 
-    layers = [DeviceLayer(cfg, device=dev, layer=i + 1000 * rank, mma_layouts=(fmt == B.MOE_ACT_MXFP4))
+    layers = [DeviceLayer(cm, device=dev, layer=i + 1000 * rank, mma_layouts=(fmt == B.MOE_ACT_MXFP4))
               for i in range(args.layers)]
+    lat = Latent(cfg, dl, fmt, dev, layers) if args.latent else None
     # all seeded inputs resident in HBM before timing
     xs_host = np.stack([IN.make_x(cfg, call=(c + rank * 100000) % (1 << 20)) for c in range(min(n_calls, 1000))])
     xs = torch.from_numpy(xs_host.view(np.int16).copy()).to(dev).view(torch.bfloat16)
     n_x = xs.shape[0]
-    ws = make_workspace(T, d, E, k, I, fmt, dev)
+    ws = make_workspace(T, dl, E, k, I, fmt, dev)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     ids = torch.empty((args.steps, T, k), dtype=torch.int32, device=dev)
     wts = torch.empty((args.steps, T, k), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(s, st, record_routing=True):
+    def call(s, x, y_out, ids_s, w_s, ws_l, st):
+        """One step: the layer, or narrow -> layer at the latent width -> widen."""
         L = layers[s % len(layers)]
-        layer_call(B, args, xs[s % n_x], L, T, d, E, k, I, fmt, y, ids[s] if record_routing else None,
-                   wts[s] if record_routing else None, ws, st.cuda_stream)
+        if lat is None:
+            layer_call(B, args, x, L, T, d, E, k, I, fmt, y_out, ids_s, w_s, ws_l, st)
+            return
+        lat.narrow(s, x, lat.xl, st)
+        layer_call(B, args, lat.xl, L, T, dl, E, k, I, fmt, lat.yl, ids_s, w_s, ws_l, st)
+        lat.widen(s, lat.yl, y_out, st)
+
+    def step(s, st, record_routing=True):
+        call(s, xs[s % n_x], y, ids[s] if record_routing else None, wts[s] if record_routing else None, ws,
+             st.cuda_stream)
 
     # warm-up (eager), then capture the K timed steps in one CUDA graph
     with torch.cuda.stream(stream):
@@ -279,6 +291,8 @@ def run_gpu(args, cfg, rank, world, local):
     ms_total = start.elapsed_time(end)
     ms_total = max_over_ranks(ms_total, world, dev)
     status = B.moe_get_device_status(ws, stream=stream.cuda_stream)
+    if status == B.MOE_OK and lat is not None:
+        status = lat.status(stream.cuda_stream)
     if status != B.MOE_OK:
         raise RuntimeError("device status after timed region: %s" % B.status_string(status))
     yf = y.float()
@@ -296,44 +310,55 @@ def run_gpu(args, cfg, rank, world, local):
     pk = peaks()
     bw = pk["hbm_gbs"] * 1e9
     mean_active = float(np.mean(n_active))
-    layer_bytes = layer_algorithmic_bytes(d, I, E, T, mean_active)
+    layer_bytes = layer_algorithmic_bytes(dl, I, E, T, mean_active)
+    if lat is not None:  # + the projections, x and y at the model width instead of dl
+        layer_bytes += lat.bytes_per_step() + 2 * T * (d - dl) * 2
 
     # ---- dominant kernel, timed alone with events on its own stream (same inputs, same layers)
-    roof = kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk)
+    xs_k = xs
+    if lat is not None:  # the gate/up kernel's inputs are the narrowed rows
+        xs_k = torch.empty((n_x, T, dl), dtype=torch.bfloat16, device=dev)
+        with torch.cuda.stream(stream):
+            for i in range(n_x):
+                lat.narrow(0, xs[i], xs_k[i], stream.cuda_stream)
+        stream.synchronize()
+    roof = kernel_roofline(args, cm, layers, xs_k, fmt, dev, stream, pk)
 
     # ---- end to end through the C ABI with host buffers
-    e2e = end_to_end(args, cfg, layers, xs_host, fmt, dev, stream)
+    e2e = end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call)
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(fmt), "data": "synthetic",
-        "config": {"workload": cfg.note + (" + per-expert RMSNorm before the weighted sum" if norm_eps(args) else ""),
+        "config": {"workload": workload_name(args, cfg),
                    "T": T, "d": d, "E": E, "k": k, "I": I, "act": args.fmt, "expert_norm_eps": norm_eps(args),
+                   "latent_width": dl if lat is not None else None,
                    "layer_copies_rotated": len(layers),
                    "l2": "inputs larger than L2: %d layer copies, %.1f GB of expert weights rotated"
-                         % (len(layers), len(layers) * E * expert_bytes(d, I) / 1e9),
+                         % (len(layers), len(layers) * E * expert_bytes(dl, I) / 1e9),
                    "cuda_graph": graph is not None, "parallelism": "replicas" if world > 1 else "single GPU"},
-        "layer_roofline": layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, world),
+        "layer_roofline": layer_roofline(fmt, cm, layer_bytes, ms_per_step, bw, pk, mean_active, world,
+                                         lat.flops_per_step() if lat is not None else 0.0),
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None) * args.steps,
+        "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None, lat is not None) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
     }
     return out
 
 
-def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, world):
+def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, world, extra_flops=0.0):
     """Whole-layer fraction of the roofline the workload is quoted against: HBM bytes for the
-    decode path; for the prefill path the FP4 tensor peak (useful flops 6 P d I per step), with
-    the HBM fraction beside it."""
+    decode path; for the prefill path the FP4 tensor peak (useful flops 6 P d I per step, plus
+    extra_flops of the latent projections), with the HBM fraction beside it."""
     out = {"bound": "hbm", "algorithmic_bytes_per_step": layer_bytes,
            "achieved_GBps": round(layer_bytes / (ms_per_step / 1e3) / 1e9, 1),
            "peak_GBps": pk["hbm_gbs"], "frac": round(layer_bytes / (ms_per_step / 1e3) / bw, 4),
            "peak_source": pk["source"], "mean_active_experts": round(mean_active, 2)}
     if fmt != 0:
-        flops = 6.0 * cfg.T * cfg.k * cfg.d * cfg.I * world
+        flops = (6.0 * cfg.T * cfg.k * cfg.d * cfg.I + extra_flops) * world
         peak_tf = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16 * world
         achieved = flops / (ms_per_step / 1e3) / 1e12
         out = {"bound": "tensor", "algorithmic_flops_per_step": flops, "achieved_TFLOPs": round(achieved, 1),
@@ -364,13 +389,79 @@ def layer_call(B, args, x, L, T, d, E, k, I, fmt, y, ids, w, ws, stream):
                                  stream=stream)
 
 
-def launches_per_step(fmt, T, d, E, k, expert_norm=False):
+TENSOR_W_IN, TENSOR_W_OUT = 10, 11  # generator streams of the shared latent projections
+
+
+def workload_name(args, cfg):
+    name = cfg.note
+    if getattr(args, "latent", 0):
+        name += " + shared latent projections %d -> %d -> %d" % (cfg.d, args.latent, cfg.d)
+    if norm_eps(args):
+        name += " + per-expert RMSNorm before the weighted sum"
+    return name
+
+
+def moe_cfg(args, cfg):
+    """The layer's own configuration: the workload's, or its latent width with --latent."""
+    import dataclasses
+    return dataclasses.replace(cfg, d=args.latent) if getattr(args, "latent", 0) else cfg
+
+
+class Latent:
+    """Shared latent projections around the layer (Muse Spark Open explainer, section 9): per layer
+    copy a narrowing matrix [dl][dm] and a widening matrix [dm][dl] (MXFP4), their workspaces and
+    the intermediate rows at the latent width."""
+
+    def __init__(self, cfg, dl, fmt, dev, layers):
+        import torch
+
+        from bit_expert_ffn_moe_gb300 import binding as B
+        from bit_expert_ffn_moe_gb300.layer import DeviceMatrix
+        self.B, self.fmt, self.T, self.dm, self.dl = B, fmt, cfg.T, cfg.d, dl
+        mma = fmt == B.MOE_ACT_MXFP4
+        self.win = [DeviceMatrix(dl, cfg.d, L.seed, TENSOR_W_IN, cfg.weight_std, mma, dev) for L in layers]
+        self.wout = [DeviceMatrix(cfg.d, dl, L.seed, TENSOR_W_OUT, cfg.weight_std, mma, dev) for L in layers]
+
+        def ws(K, N):
+            w = torch.empty(B.moe_dense_workspace_size(cfg.T, K, N, fmt), dtype=torch.uint8, device=dev)
+            B.moe_workspace_init(w)
+            return w
+        self.ws_in, self.ws_out = ws(cfg.d, dl), ws(dl, cfg.d)
+        self.xl = torch.empty((cfg.T, dl), dtype=torch.bfloat16, device=dev)
+        self.yl = torch.empty((cfg.T, dl), dtype=torch.bfloat16, device=dev)
+
+    def narrow(self, s, x, out, st):
+        self.B.moe_dense_linear(x, self.T, self.dm, self.dl, self.win[s % len(self.win)].struct, self.fmt, out,
+                                self.ws_in, stream=st)
+
+    def widen(self, s, yl, y, st):
+        self.B.moe_dense_linear(yl, self.T, self.dl, self.dm, self.wout[s % len(self.wout)].struct, self.fmt, y,
+                                self.ws_out, stream=st)
+
+    def bytes_per_step(self):
+        return 2.0 * self.dm * self.dl * 17 / 32
+
+    def flops_per_step(self):
+        return 4.0 * self.T * self.dm * self.dl
+
+    def status(self, st):
+        B = self.B
+        for w in (self.ws_in, self.ws_out):
+            v = B.moe_get_device_status(w, stream=st)
+            if v != B.MOE_OK:
+                return v
+        return B.MOE_OK
+
+
+def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False):
     # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
     # gate/up, down+sum; with the expert normalisation the down GEMV and the (normalising) sum are
-    # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum
+    # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum.
+    # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).
+    proj = (2 if fmt == 0 else 4) * 2 if latent else 0
     if fmt == 0:
-        return (3 if T <= 8 else 7) + (1 if expert_norm else 0)
-    return 10
+        return (3 if T <= 8 else 7) + (1 if expert_norm else 0) + proj
+    return 10 + proj
 
 
 def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
@@ -482,9 +573,9 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
             "peak_source": pk["source"] + " bf16 x %.0f (nominal FP4 : bf16 dense ratio)" % NOMINAL_FP4_OVER_BF16}
 
 
-def end_to_end(args, cfg, layers, xs_host, fmt, dev, stream):
+def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call):
     """Same metric through the C ABI with host buffers: per step, copy x from pinned host memory,
-    run the layer, copy y back; all inside the timed region."""
+    run the step (call), copy y back; all inside the timed region."""
     import numpy as np
     import torch
 
@@ -497,13 +588,12 @@ def end_to_end(args, cfg, layers, xs_host, fmt, dev, stream):
     y_pin = torch.empty((n, T, d), dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     y_dev = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-    ws = make_workspace(T, d, E, k, I, fmt, dev)
+    ws = make_workspace(T, cm.d, E, k, I, fmt, dev)
     st = stream.cuda_stream
 
     def one(s):
-        L = layers[s % len(layers)]
         x_dev.copy_(x_pin[s % x_pin.shape[0]], non_blocking=True)
-        layer_call(B, args, x_dev, L, T, d, E, k, I, fmt, y_dev, None, None, ws, st)
+        call(s, x_dev, y_dev, None, None, ws, st)
         y_pin[s].copy_(y_dev, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -528,19 +618,21 @@ def end_to_end(args, cfg, layers, xs_host, fmt, dev, stream):
 # ------------------------------------------------------------------ CPU oracle arm
 
 def oracle_sample(args, cfg, n_tokens):
-    """Time the CPU oracle (as it stands) on n_tokens decode tokens: routing, dequantisation of
-    the touched experts, expert GEMVs and the weighted sum.  Weight generation is untimed."""
+    """Time the CPU oracle (as it stands) on a bounded sample of the workload: routing,
+    dequantisation of the touched experts, expert GEMVs and the weighted sum (with --latent also
+    the two projections of the sampled tokens).  Weight generation is untimed."""
     import numpy as np
 
     from bit_expert_ffn_moe_gb300 import inputs as IN
     from oracle import oracle as O
 
     threads = len(os.sched_getaffinity(0))
+    cm = moe_cfg(args, cfg)
     layer_seed = cfg.seed + 7919 * 1
-    W_r, b = IN.make_router(cfg)
-    rng = np.random.default_rng([cfg.seed, 77, 1])
-    W_r = (rng.standard_normal(W_r.shape) / np.sqrt(cfg.d)).astype(np.float32)
-    shapes = IN.expert_matrix_shapes(cfg)
+    W_r, b = IN.make_router(cm)
+    rng = np.random.default_rng([cm.seed, 77, 1])
+    W_r = (rng.standard_normal(W_r.shape) / np.sqrt(cm.d)).astype(np.float32)
+    shapes = IN.expert_matrix_shapes(cm)
     cache = {}
 
     def weights(e):
@@ -553,6 +645,30 @@ def oracle_sample(args, cfg, n_tokens):
         return cache[e]
 
     act = O.ACT_BF16 if args.fmt == "bf16" else O.ACT_MXFP4
+    eps = norm_eps(args)
+    if getattr(args, "latent", 0):
+        win = O.mxfp4_pack(IN.synth_weights(layer_seed, TENSOR_W_IN, 0, cm.d, cfg.d, cfg.weight_std))
+        wout = O.mxfp4_pack(IN.synth_weights(layer_seed, TENSOR_W_OUT, 0, cfg.d, cm.d, cfg.weight_std))
+
+        def full(xb):  # narrow -> layer -> widen, on the sampled rows
+            xl = IN.to_bf16_bits(O.dense_linear(xb, win, act))
+            yl = O.moe_layer(xl, W_r, b, cfg.k, weights, act, expert_norm_eps=eps)["y"]
+            return O.dense_linear(IN.to_bf16_bits(yl), wout, act)
+
+        xs = [IN.make_x(cfg, call=c) for c in range(n_tokens)] if cfg.T <= 8 else \
+            [IN.make_x(cfg, call=0)[np.arange(0, cfg.T, max(1, cfg.T // n_tokens))[:n_tokens]]]
+        for xb in xs:  # pre-generate the touched experts (untimed: input generation)
+            xl = IN.to_bf16_bits(O.dense_linear(xb, win, act))
+            for e in np.unique(O.topk_softmax(O.router_logits(xl, W_r, b), cfg.k)[0]):
+                weights(int(e))
+        t0 = time.perf_counter()
+        for xb in xs:
+            full(xb)
+        dt = time.perf_counter() - t0
+        rows = sum(xb.shape[0] for xb in xs)
+        return dict(value=round(rows / dt, 3), unit=UNIT, cores=threads, kind="oracle",
+                    sample="%d token rows through narrow -> layer (routing of those rows) -> widen, fp64 oracle, "
+                           "weights pre-generated" % rows, seconds=round(dt, 2))
     if cfg.T <= 8:
         # decode sizes: whole layer calls
         xs = [IN.make_x(cfg, call=c) for c in range(n_tokens)]
@@ -562,7 +678,7 @@ def oracle_sample(args, cfg, n_tokens):
                 weights(int(e))
         t0 = time.perf_counter()
         for xb in xs:
-            O.moe_layer(xb, W_r, b, cfg.k, weights, act, expert_norm_eps=norm_eps(args))
+            O.moe_layer(xb, W_r, b, cfg.k, weights, act, expert_norm_eps=eps)
         dt = time.perf_counter() - t0
         return dict(value=round(cfg.T * n_tokens / dt, 3), unit=UNIT, cores=threads, kind="oracle",
                     sample="%d layer calls of T=%d (full routing, all %d touched experts per call, fp64 oracle), "
@@ -577,7 +693,7 @@ def oracle_sample(args, cfg, n_tokens):
     for e in np.unique(ids[tokens]):
         weights(int(e))
     t0 = time.perf_counter()
-    O.moe_layer(xb[tokens], W_r, b, cfg.k, weights, act, expert_norm_eps=norm_eps(args))
+    O.moe_layer(xb[tokens], W_r, b, cfg.k, weights, act, expert_norm_eps=eps)
     t_exp = time.perf_counter() - t0
     per_tok = t_route / cfg.T + t_exp / len(tokens)
     return dict(value=round(1.0 / per_tok, 3), unit=UNIT, cores=threads, kind="oracle",
@@ -601,9 +717,9 @@ def run_reference(args, cfg, rank, world):
     out = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": world, "steps": n,
            "warmup": 1, "ms_per_step": round(1e3 * cfg.T / res["value"], 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-           "config": {"workload": cfg.note + (" + per-expert RMSNorm before the weighted sum" if norm_eps(args) else ""),
+           "config": {"workload": workload_name(args, cfg),
                       "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I, "act": args.fmt,
-                      "expert_norm_eps": norm_eps(args)},
+                      "expert_norm_eps": norm_eps(args), "latent_width": args.latent or None},
            "impl": "reference",
            "cpu_baseline": {"value": res["value"], "unit": UNIT, "cores": res["cores"], "kind": "oracle",
                             "sample": res["sample"] + "; %d of the %d requested steps" % (n, args.steps)},
@@ -622,6 +738,9 @@ def main():
     ap.add_argument("--layers", type=int, default=N_LAYER_COPIES)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--latent", type=int, default=0,
+                    help="latent width: narrow x with a shared MXFP4 matrix before the router, run the layer "
+                         "at that width and widen the weighted sum back (0 = off)")
     ap.add_argument("--expert-norm", action="store_true",
                     help="normalise each expert output (RMSNorm over d, eps 1e-6) before the weighted sum")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)

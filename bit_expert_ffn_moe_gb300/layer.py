@@ -64,6 +64,31 @@ class DeviceLayer:
         return 3 * cfg.I * cfg.d // 2 + 3 * cfg.I * cfg.d // 32
 
 
+class DeviceMatrix:
+    """One synthetic MXFP4 matrix [rows][K] on ``device`` (the library's generator, matrix 0 of
+    ``tensor_id`` under ``seed``), with the tensor-core copies when ``mma``: the shared latent
+    projections of a latent layer."""
+
+    def __init__(self, rows: int, K: int, seed: int, tensor_id: int, std: float = 0.02, mma: bool = True,
+                 device="cuda"):
+        dev = torch.device(device)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        buf = torch.empty((rows, K), dtype=torch.float32, device=dev)
+        B.moe_synth_weights(seed, tensor_id, 0, 1, rows, K, float(IN.weight_scale(std)), buf)
+        self.q = torch.empty((rows, K // 2), **u8)
+        self.s = torch.empty((rows, K // 32), **u8)
+        B.moe_mxfp4_pack(buf, rows, K, self.q, self.s)
+        del buf
+        self.q_mma = self.s_mma = None
+        if mma:
+            self.q_mma = torch.empty(rows * K // 2, **u8)
+            self.s_mma = torch.empty(B.moe_mxfp4_mma_scale_bytes(rows, K), **u8)
+            B.moe_mxfp4_codes_to_mma(self.q, rows, K, self.q_mma)
+            B.moe_mxfp4_scales_to_mma(self.s, rows, K, self.s_mma)
+        self.rows, self.K = rows, K
+        self.struct = B.mxfp4_matrix_struct(self.q, self.s, self.q_mma, self.s_mma)
+
+
 def make_workspace(T: int, d: int, E: int, k: int, I: int, fmt: int, device="cuda") -> torch.Tensor:
     n = B.moe_workspace_size(T, d, E, k, I, fmt)
     if n == 0:
