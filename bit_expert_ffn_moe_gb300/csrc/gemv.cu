@@ -228,10 +228,11 @@ gemv_up_kernel(const GemvArgs a) {
 }
 
 
-// ------------------------------------------------------------------ gate/up + SwiGLU, T <= 2
-// For one or two tokens a CTA-wide split of K is faster than whole rows per warp: the weight
+// ------------------------------------------------------------------ gate/up + SwiGLU, T <= 4
+// For up to four tokens a CTA-wide split of K is faster than whole rows per warp: the weight
 // rows of a batch are prefetched into registers one batch ahead and every thread owns one
-// K-block, so the activations need no shared-memory traffic per row.
+// K-block, so the activations need no shared-memory traffic per row.  (The down GEMV takes the
+// same split for one or two tokens.)
 constexpr int kR = 8;  // weight rows per batch per row group
 
 // Sum V values over the 32 lanes of a warp; afterwards lane l holds the warp sum of value
@@ -356,7 +357,8 @@ __device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int 
 }
 
 // Grid (M_exp / outs, slots): slot u is the u-th active expert.  A batch gives each row group
-// kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens.
+// kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens; an
+// expert with more rows takes them Q at a time (its weights are read again per pass).
 template <int BPT, int Q>
 __global__ void __launch_bounds__(kThr)
 gemv_up_cta_kernel(const GemvArgs a) {
@@ -917,8 +919,8 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
     const int P = T * k;
     if (P == 0) return cudaSuccess;
     const int bpl = bpl_for(d);
-    if (T <= 2 && make_cta_geo(d).bpt <= 2) {
-        // one or two tokens: CTA-wide split of K (see gemv_up_cta_kernel)
+    if (T <= 4 && make_cta_geo(d).bpt <= 2) {
+        // up to four tokens: CTA-wide split of K (see gemv_up_cta_kernel), two token rows per pass
         const CtaGeo geo = make_cta_geo(d);
         const int unit = geo.RG * (kR / 2);
         if (I % unit != 0) return cudaErrorInvalidValue;
@@ -941,7 +943,7 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
         a.E = E;
         a.outs = outs;
         a.out = h;
-        const int Q = T;
+        const int Q = T < 2 ? T : 2;
         const size_t smem = (size_t)Q * d * 2 + sizeof(float) * (Q + 2 * 8 * 32) + sizeof(int) * Q + sizeof(unsigned) * Q;
         void* args[] = {&a};
         const dim3 grid(I / outs, P < E ? P : E);
