@@ -455,7 +455,7 @@ gemv_up_cta_kernel(const GemvArgs a) {
     pdl_launch_dependents();
 }
 
-// ------------------------------------------------------------------ down (+ weighted sum), T <= 2
+// ------------------------------------------------------------------ down (+ weighted sum), T <= 4
 // The same CTA-wide split of K as the gate/up kernel above, with the weights fed through a ring
 // of shared-memory stages by the copy engine.  A CTA owns feats = RG * kR output features and
 // walks the active experts in ascending order (each token's slot order); batch u is the feats
@@ -469,8 +469,11 @@ gemv_up_cta_kernel(const GemvArgs a) {
 // scaled back by the inverse, an exact rescaling.
 // FUSED: ys[t][f] accumulates w * bf16(expert output) batch after batch (the same lane updates a
 // given (t, f) in expert order); otherwise the bf16 outputs go to y_perm.
-constexpr int kDownStages = 3;
-constexpr int kDownHUnits = 2;  // 8-element h pieces per thread and batch (Q * K/8 <= 2 * kThr)
+// Q = 1: three stages; Q = 2, 4: two stages (the h rows take the third stage's shared memory,
+// so that two CTAs still fit an SM).  8-element h pieces per thread and batch: 2 for Q <= 2
+// (Q K/8 <= 2 kThr), Q for Q = 4.
+template <int Q> __host__ __device__ constexpr int down_stages() { return Q == 1 ? 3 : 2; }
+template <int Q> __host__ __device__ constexpr int down_hunits() { return Q <= 2 ? 2 : Q; }
 
 __host__ __device__ inline uint32_t down_stage_bytes(int K) {
     const CtaGeo g = make_cta_geo(K);
@@ -480,9 +483,9 @@ __host__ __device__ inline uint32_t down_stage_bytes(int K) {
 template <int Q>
 __host__ __device__ inline size_t down_ring_smem(int K, int P) {
     const CtaGeo g = make_cta_geo(K);
-    return (size_t)kDownStages * down_stage_bytes(K) + (size_t)2 * Q * K * 2 /* h blocks */ +
+    return (size_t)down_stages<Q>() * down_stage_bytes(K) + (size_t)2 * Q * K * 2 /* h blocks */ +
            sizeof(float) * ((size_t)2 * Q * g.nb /* inverse scales */ + 2 * 8 * 32 + (size_t)Q * g.RG * kR) +
-           sizeof(uint64_t) * kDownStages + sizeof(int) * 3 * (size_t)P;
+           sizeof(uint64_t) * down_stages<Q>() + sizeof(int) * 3 * (size_t)P;
 }
 
 template <int Q, bool FUSED>
@@ -490,6 +493,8 @@ __global__ void __launch_bounds__(kThr, 2)
 gemv_down_ring_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int V = kR * Q;
+    constexpr int kDownStages = down_stages<Q>();
+    constexpr int kDownHUnits = down_hunits<Q>();
     const CtaGeo geo = make_cta_geo(a.K);
     const int feats = geo.RG * kR, nb = geo.nb;
     const uint32_t code_bytes = (uint32_t)feats * (a.K / 2), stage_bytes = code_bytes + (uint32_t)feats * (a.K / 32);
@@ -990,12 +995,13 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
     if (T == 0) return cudaSuccess;
     const CtaGeo dgeo = make_cta_geo(I);
     const int P = T * k, feats = dgeo.RG * kR;
-    const size_t ring_smem = T == 1 ? down_ring_smem<1>(I, P) : down_ring_smem<2>(I, P);
+    const size_t ring_smem = T == 1 ? down_ring_smem<1>(I, P) : T == 2 ? down_ring_smem<2>(I, P) : down_ring_smem<4>(I, P);
     const bool aligned16 = ((uintptr_t)W->down_q % 16 == 0) && ((uintptr_t)W->down_s % 16 == 0);
     // two CTAs per SM: 2 x (ring_smem + 1 KB reserved) within the SM's 228 KB
-    if (T <= 2 && dgeo.bpt == 1 && d % feats == 0 && aligned16 && T * dgeo.nb * 4 <= kDownHUnits * kThr &&
+    const int hunits = T <= 2 ? down_hunits<2>() : down_hunits<4>();
+    if (T <= 4 && dgeo.bpt == 1 && d % feats == 0 && aligned16 && T * dgeo.nb * 4 <= hunits * kThr &&
         ring_smem <= 113 * 1024) {
-        // one or two tokens: CTA-split of K, weights through the copy-engine ring
+        // up to four tokens: CTA-split of K, weights through the copy-engine ring
         GemvArgs a = {};
         a.q0 = W->down_q;
         a.s0 = W->down_s;
@@ -1014,7 +1020,8 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
         void* args[] = {&a};
         const dim3 grid(d / feats);
         const void* f = T == 1 ? (y ? (const void*)gemv_down_ring_kernel<1, true> : (const void*)gemv_down_ring_kernel<1, false>)
-                               : (y ? (const void*)gemv_down_ring_kernel<2, true> : (const void*)gemv_down_ring_kernel<2, false>);
+                      : T == 2 ? (y ? (const void*)gemv_down_ring_kernel<2, true> : (const void*)gemv_down_ring_kernel<2, false>)
+                               : (y ? (const void*)gemv_down_ring_kernel<4, true> : (const void*)gemv_down_ring_kernel<4, false>);
         return launch_kernel(f, grid, dim3(kThr), ring_smem, st, pdl, args);
     }
     const int bpl = bpl_for(I);
