@@ -331,7 +331,7 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,
                            cudaStream_t st, bool pdl);
 // y != nullptr: fused weighted sum into y [T][d] using row_w; otherwise bf16 y_perm [P][d].
-// pdl: the one/two-token kernel reads the plan (and offsets) before its dependency wait, so with
+// pdl: the kernel for up to four tokens reads the plan (and offsets) before its dependency wait, so with
 // pdl = true the plan must come from a kernel that completed before the preceding kernel's own wait.
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                              const float* row_w, int T, int d, int E, int k, int I, const moe_expert_weights* W,

@@ -232,7 +232,7 @@ gemv_up_kernel(const GemvArgs a) {
 // For up to four tokens a CTA-wide split of K is faster than whole rows per warp: the weight
 // rows of a batch are prefetched into registers one batch ahead and every thread owns one
 // K-block, so the activations need no shared-memory traffic per row.  (The down GEMV takes the
-// same split for one or two tokens.)
+// same split, with its weights fed through a copy-engine ring.)
 constexpr int kR = 8;  // weight rows per batch per row group
 
 // Sum V values over the 32 lanes of a warp; afterwards lane l holds the warp sum of value
