@@ -85,3 +85,28 @@ def test_recorded_traffic_only_for_its_workload_and_sources():
     assert bench.ncu_traffic("no_such_profile.md", src, "prefill") is None
     assert bench.ncu_traffic("umma_grouped_prefill.md", src, "long_prefill") is None
     assert bench.ncu_traffic("umma_grouped_prefill.md", src[:1], "prefill") is None  # other sources
+
+
+def test_variant_options_name_the_workload_and_count_launches():
+    """--expert-norm and --latent change the layer the bench times: the workload name says so,
+    the layer runs at the latent width, and the launch count includes the extra kernels."""
+    import argparse
+
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    cfg = IN.CONFIGS["decode"]
+    plain = argparse.Namespace(expert_norm=False, latent=0)
+    both = argparse.Namespace(expert_norm=True, latent=4096)
+    assert bench.workload_name(plain, cfg) == cfg.note
+    name = bench.workload_name(both, cfg)
+    assert "8192 -> 4096 -> 8192" in name and "RMSNorm" in name
+    assert bench.moe_cfg(plain, cfg) is cfg
+    cm = bench.moe_cfg(both, cfg)
+    assert (cm.d, cm.E, cm.k, cm.I, cm.T) == (4096, cfg.E, cfg.k, cfg.I, cfg.T)
+    assert bench.norm_eps(plain) is None and bench.norm_eps(both) == 1e-6
+    # decode: fused router, gate/up, down+sum; + the normalising sum; + 2 x (plan + GEMV)
+    assert bench.launches_per_step(0, 1, 8192, 128, 8) == 3
+    assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True) == 4
+    assert bench.launches_per_step(0, 1, 8192, 128, 8, latent=True) == 7
+    # prefill: 10 layer kernels; + 2 x (plan, quantise, gather, GEMM)
+    assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 10
+    assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 18
