@@ -18,6 +18,8 @@
  *             compute path is the block-scaled 4-bit MXFP4 format.
  *   [OCP-MX] OCP Microscaling Formats (MX) v1.0 -- E2M1 element grid, E8M0 scale,
  *             shared exponent = floor(log2(amax)) - emax_elem (emax_elem = 2 for E2M1).
+ *   [OFP8]  OCP 8-bit Floating Point Specification (OFP8) v1.0 -- the E4M3 encoding (bias 7,
+ *             subnormals, S.1111.111 NaN, no infinity, largest finite 448).
  *
  * Readings taken where the sources are silent (each also listed in the design notes):
  *   R1  router reduction order: the sources only say "FP32".  Logits are formed from 32
@@ -50,6 +52,14 @@
  *       the d output features of the expert's (bf16) output row, v / sqrt(mean(v^2) + eps),
  *       eps = 1e-6 unless given, no learned scale; computed in fp64 and rounded to fp32, then
  *       summed as in R7.
+ *   R10 NVFP4 expert weights (optional; [MUSE] s.11 describes the weights as 4-bit values of
+ *       which 16 share a small scale, about 4.5 bits each, without giving the scale's format):
+ *       E2M1 codes as in MXFP4, one E4M3 scale [OFP8] per 16 consecutive elements of a row and
+ *       one fp32 global scale per matrix; value = E2M1 * E4M3 * global.  Quantiser, in fp32:
+ *       global = amax(matrix) / (6 * 448) (1 if that is 0); per block t = (amax(block) / global)
+ *       / 6, scale = nearest E4M3 to t (ties even, saturating at 448); D = scale * global;
+ *       each code = nearest E2M1 to |v| / D (ties even, saturating at 6), signed unless 0;
+ *       D = 0 gives zero codes.
  * Accumulations inside the expert matrices are fp64 (closer to exact than the kernels).
  */
 #include <math.h>
@@ -176,6 +186,116 @@ int oracle_mxfp4_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_
             w[r * K + i] = (float)(oracle_e2m1_value(code) * oracle_e8m0_value(sb));
         }
     }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ NVFP4 tensors  (R10) */
+
+/* E4M3 byte -> value [OFP8]: sign bit 7, exponent bits 6..3 with bias 7, mantissa bits 2..0;
+ * exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is no infinity. */
+double oracle_e4m3_value(int code) {
+    int e = (code >> 3) & 0xF, m = code & 7;
+    if (e == 15 && m == 7) return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp(8.0 + m, e - 10);
+    return (code & 0x80) ? -v : v;
+}
+
+/* Nearest non-negative finite E4M3 code to a >= 0: a search over the 127 codes 0x00..0x7E,
+ * ties to the even code, values beyond 448 saturating to 448 (R10). */
+int oracle_e4m3_encode_nonneg(double a) {
+    int best = 0;
+    double best_dist = fabs(a);
+    for (int c = 1; c <= 0x7E; ++c) {
+        double dist = fabs(a - oracle_e4m3_value(c));
+        if (dist < best_dist || (dist == best_dist && (c % 2) == 0)) {
+            best = c;
+            best_dist = dist;
+        }
+    }
+    return best;
+}
+
+/* Global scale of one NVFP4 matrix from its largest magnitude (R10): amax / (6 * 448) in fp32,
+ * so that the largest block scale lands at the top of the E4M3 range; 1 when that is 0. */
+float oracle_nvfp4_global_scale(float amax) {
+    float gs = amax / 2688.0f;
+    return gs == 0.0f ? 1.0f : gs;
+}
+
+/* Quantise one block of n values (16 in NVFP4) with the matrix's global scale gs (R10), every
+ * step in fp32 in this order: t = (amax / gs) / 6; scale byte = nearest E4M3 to t (ties even,
+ * saturating); D = value(scale byte) * gs; code of v = nearest E2M1 to |v| / D (ties even,
+ * saturating at 6), with the sign of v unless the magnitude code is 0; D = 0 gives zero codes. */
+void oracle_nv_block_quantize(const float* v, int n, float gs, uint8_t* codes, uint8_t* scale_byte) {
+    float amax = 0.0f;
+    for (int i = 0; i < n; ++i) {
+        float a = fabsf(v[i]);
+        if (a > amax) amax = a;
+    }
+    float t = (amax / gs) / 6.0f;
+    int sb = oracle_e4m3_encode_nonneg((double)t);
+    *scale_byte = (uint8_t)sb;
+    float D = (float)oracle_e4m3_value(sb) * gs;
+    for (int i = 0; i < n; ++i) {
+        if (D == 0.0f) {
+            codes[i] = 0;
+            continue;
+        }
+        float a = fabsf(v[i]) / D;
+        int c = oracle_e2m1_encode_magnitude((double)a);
+        if (c != 0 && v[i] < 0.0f) c |= 8;
+        codes[i] = (uint8_t)c;
+    }
+}
+
+/* Pack n_mats fp32 matrices [n_mats][rows][K] into NVFP4 (R10): codes q[n_mats*rows][K/2]
+ * (same nibble order as MXFP4), scales s[n_mats*rows][K/16] (one E4M3 byte per 16 consecutive
+ * elements of a row) and one fp32 global scale gs[m] per matrix.  Returns 0, or -1 when K is
+ * not a multiple of 16. */
+int oracle_nvfp4_pack(const float* w, int64_t n_mats, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, float* gs) {
+    if (K % 16 != 0) return -1;
+    int64_t nb = K / 16;
+    for (int64_t m = 0; m < n_mats; ++m) {
+        const float* wm = w + m * rows * K;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < rows * K; ++i) {
+            float a = fabsf(wm[i]);
+            if (a > amax) amax = a;
+        }
+        float g = oracle_nvfp4_global_scale(amax);
+        gs[m] = g;
+#pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            uint8_t codes[16];
+            int64_t row = m * rows + r;
+            for (int64_t b = 0; b < nb; ++b) {
+                oracle_nv_block_quantize(wm + r * K + b * 16, 16, g, codes, &s[row * nb + b]);
+                for (int i = 0; i < 8; ++i)
+                    q[row * (K / 2) + b * 8 + i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
+            }
+        }
+    }
+    return 0;
+}
+
+/* Dequantise NVFP4 matrices to fp64 (exact: code value * scale value has at most 6 significant
+ * bits, times the fp32 global scale at most 30).  Returns 0, or -1 if a scale byte is NaN. */
+int oracle_nvfp4_unpack(const uint8_t* q, const uint8_t* s, const float* gs, int64_t n_mats, int64_t rows, int64_t K,
+                        double* w) {
+    if (K % 16 != 0) return -1;
+    int64_t nb = K / 16;
+    int bad = 0;
+    for (int64_t m = 0; m < n_mats; ++m)
+        for (int64_t r = 0; r < rows; ++r) {
+            int64_t row = m * rows + r;
+            for (int64_t i = 0; i < K; ++i) {
+                uint8_t sb = s[row * nb + i / 16];
+                if ((sb & 0x7F) == 0x7F) bad = 1;
+                uint8_t byte = q[row * (K / 2) + i / 2];
+                int code = (i % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+                w[row * K + i] = oracle_e2m1_value(code) * oracle_e4m3_value(sb) * (double)gs[m];
+            }
+        }
     return bad ? -1 : 0;
 }
 
@@ -312,15 +432,38 @@ static void weight_row(const uint8_t* q, const uint8_t* s, int64_t row, int K, d
     }
 }
 
+/* One weight matrix of an expert: MXFP4 (q, s), or NVFP4 (q, s, gs) (R10). */
+#define W_MXFP4 0
+#define W_NVFP4 1
+typedef struct {
+    const uint8_t* q;
+    const uint8_t* s;
+    int fmt;
+    double gs;
+} wmat;
+
+/* Decode one weight row of either format into fp64 (exact in both). */
+static void wmat_row(const wmat* W, int64_t row, int K, double* out) {
+    if (W->fmt == W_MXFP4) {
+        weight_row(W->q, W->s, row, K, out);
+        return;
+    }
+    const uint8_t* qr = W->q + row * (K / 2);
+    const uint8_t* sr = W->s + row * (K / 16);
+    for (int i = 0; i < K; ++i) {
+        int code = (i % 2 == 0) ? (qr[i / 2] & 0xF) : (qr[i / 2] >> 4);
+        out[i] = oracle_e2m1_value(code) * oracle_e4m3_value(sr[i / 16]) * W->gs;
+    }
+}
+
 /* Expert FFN for n activation rows of one expert.
  *   a      [n][d]  activation operand values (from oracle_activation_row)
- *   W_g, W_u MXFP4 [I][d] (q, s);  W_d MXFP4 [d][I] (q, s)
+ *   W_g, W_u [I][d];  W_d [d][I]  (MXFP4 (q, s), or NVFP4 (q, s, global scale), R10)
  *   h_out  [n][I]  the down-GEMM operand after the R7 rounding (may be NULL)
  *   hq/hs  [n][I/2], [n][I/32]  MXFP4 codes/scales of h when act_fmt == ACT_MXFP4 (may be NULL)
  *   y_out  [n][d]  expert output rounded to fp32 then bf16 (R7)
  * g and u accumulate in fp64 and are rounded to fp32, as the kernels hold them in fp32. */
-void oracle_expert_ffn(const float* a, int n, int d, int I, const uint8_t* Wg_q, const uint8_t* Wg_s,
-                       const uint8_t* Wu_q, const uint8_t* Wu_s, const uint8_t* Wd_q, const uint8_t* Wd_s,
+static void expert_ffn(const float* a, int n, int d, int I, const wmat* Wg, const wmat* Wu, const wmat* Wd,
                        int act_fmt, float* h_out, uint8_t* hq, uint8_t* hs, float* y_out) {
     double* h = (double*)malloc(sizeof(double) * (size_t)n * I);
 #pragma omp parallel
@@ -329,8 +472,8 @@ void oracle_expert_ffn(const float* a, int n, int d, int I, const uint8_t* Wg_q,
         double* urow = (double*)malloc(sizeof(double) * (size_t)d);
 #pragma omp for schedule(dynamic, 16)
         for (int i = 0; i < I; ++i) {
-            weight_row(Wg_q, Wg_s, i, d, wrow);
-            weight_row(Wu_q, Wu_s, i, d, urow);
+            wmat_row(Wg, i, d, wrow);
+            wmat_row(Wu, i, d, urow);
             for (int r = 0; r < n; ++r) {
                 const float* ar = a + (int64_t)r * d;
                 double g = 0.0, u = 0.0;
@@ -369,7 +512,7 @@ void oracle_expert_ffn(const float* a, int n, int d, int I, const uint8_t* Wg_q,
         double* wrow = (double*)malloc(sizeof(double) * (size_t)I);
 #pragma omp for schedule(dynamic, 16)
         for (int c = 0; c < d; ++c) {
-            weight_row(Wd_q, Wd_s, c, I, wrow);
+            wmat_row(Wd, c, I, wrow);
             for (int r = 0; r < n; ++r) {
                 const double* hr = h + (int64_t)r * I;
                 double y = 0.0;
@@ -380,6 +523,23 @@ void oracle_expert_ffn(const float* a, int n, int d, int I, const uint8_t* Wg_q,
         free(wrow);
     }
     free(h);
+}
+
+void oracle_expert_ffn(const float* a, int n, int d, int I, const uint8_t* Wg_q, const uint8_t* Wg_s,
+                       const uint8_t* Wu_q, const uint8_t* Wu_s, const uint8_t* Wd_q, const uint8_t* Wd_s,
+                       int act_fmt, float* h_out, uint8_t* hq, uint8_t* hs, float* y_out) {
+    wmat g = {Wg_q, Wg_s, W_MXFP4, 1.0}, u = {Wu_q, Wu_s, W_MXFP4, 1.0}, dn = {Wd_q, Wd_s, W_MXFP4, 1.0};
+    expert_ffn(a, n, d, I, &g, &u, &dn, act_fmt, h_out, hq, hs, y_out);
+}
+
+/* The same expert with NVFP4 weights (R10): scales [rows][K/16] E4M3 and one global scale per
+ * matrix (gs_g, gs_u, gs_d). */
+void oracle_expert_ffn_nvfp4(const float* a, int n, int d, int I, const uint8_t* Wg_q, const uint8_t* Wg_s,
+                             const uint8_t* Wu_q, const uint8_t* Wu_s, const uint8_t* Wd_q, const uint8_t* Wd_s,
+                             float gs_g, float gs_u, float gs_d, int act_fmt, float* h_out, uint8_t* hq,
+                             uint8_t* hs, float* y_out) {
+    wmat g = {Wg_q, Wg_s, W_NVFP4, gs_g}, u = {Wu_q, Wu_s, W_NVFP4, gs_u}, dn = {Wd_q, Wd_s, W_NVFP4, gs_d};
+    expert_ffn(a, n, d, I, &g, &u, &dn, act_fmt, h_out, hq, hs, y_out);
 }
 
 /* ------------------------------------------------------------------ weighted sum  [MUSE] s.9 */

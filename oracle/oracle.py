@@ -17,6 +17,8 @@ Each function follows one step of the layer as the sources state it (see the hea
 * ``expert_norm``    -- section 9 (each chosen expert's output is normalised before the sum;
                         reading R8: RMSNorm over d, no learned scale)
 * ``dense_linear``   -- section 9 (the shared latent projections around the experts; reading R9)
+* ``nvfp4_pack``     -- section 11 (16 values share a small scale, about 4.5 bits each; reading
+                        R10: E4M3 block scales after OCP OFP8, one fp32 global scale per matrix)
 """
 from __future__ import annotations
 
@@ -76,6 +78,14 @@ def _load():
         "oracle_combine": (None, [P, P, P, i32, P, i32, i32, P]),
         "oracle_expert_norm": (None, [P, i64, i32, ctypes.c_double, P]),
         "oracle_dense_linear": (None, [P, i32, i32, i32, P, P, P]),
+        "oracle_e4m3_value": (ctypes.c_double, [i32]),
+        "oracle_e4m3_encode_nonneg": (i32, [ctypes.c_double]),
+        "oracle_nvfp4_global_scale": (ctypes.c_float, [ctypes.c_float]),
+        "oracle_nv_block_quantize": (None, [P, i32, ctypes.c_float, P, P]),
+        "oracle_nvfp4_pack": (i32, [P, i64, i64, i64, P, P, P]),
+        "oracle_nvfp4_unpack": (i32, [P, P, P, i64, i64, i64, P]),
+        "oracle_expert_ffn_nvfp4": (None, [P, i32, i32, i32, P, P, P, P, P, P, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_float, i32, P, P, P, P]),
         "oracle_float_to_bf16_bits": (ctypes.c_uint16, [ctypes.c_float]),
         "oracle_bf16_bits_to_float": (ctypes.c_float, [ctypes.c_uint16]),
     }
@@ -151,6 +161,64 @@ def mxfp4_unpack(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return w
 
 
+# ------------------------------------------------------------------ NVFP4 tensors (reading R10)
+
+def e4m3_value(code: int) -> float:
+    return _load().oracle_e4m3_value(int(code))
+
+
+def e4m3_encode(a: float) -> int:
+    """Nearest finite non-negative E4M3 code to a >= 0 (ties even, saturating at 448)."""
+    return _load().oracle_e4m3_encode_nonneg(float(a))
+
+
+def nvfp4_global_scale(amax: float) -> float:
+    return float(_load().oracle_nvfp4_global_scale(float(amax)))
+
+
+def nv_block_quantize(v: np.ndarray, gs: float):
+    """Quantise one block (fp32 values) with the global scale gs: (codes uint8[n], scale byte)."""
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    codes = np.zeros(v.shape[0], dtype=np.uint8)
+    sb = np.zeros(1, dtype=np.uint8)
+    _load().oracle_nv_block_quantize(_ptr(v), v.shape[0], float(gs), _ptr(codes), _ptr(sb))
+    return codes, int(sb[0])
+
+
+def nvfp4_pack(w: np.ndarray):
+    """fp32 [rows][K] (one matrix) or [n][rows][K] -> (q uint8 [.., rows, K/2],
+    s uint8 [.., rows, K/16], gs fp32 (a scalar array for one matrix, [n] otherwise))."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    one = w.ndim == 2
+    w3 = w[None] if one else w
+    n, rows, K = w3.shape
+    q = np.empty((n, rows, K // 2), dtype=np.uint8)
+    s = np.empty((n, rows, K // 16), dtype=np.uint8)
+    gs = np.empty(n, dtype=np.float32)
+    rc = _load().oracle_nvfp4_pack(_ptr(w3), n, rows, K, _ptr(q), _ptr(s), _ptr(gs))
+    if rc != 0:
+        raise ValueError("K must be a multiple of 16")
+    if one:
+        return q[0], s[0], np.float32(gs[0])
+    return q, s, gs
+
+
+def nvfp4_unpack(q: np.ndarray, s: np.ndarray, gs) -> np.ndarray:
+    """Exact fp64 values of one NVFP4 matrix (q [rows][K/2], s [rows][K/16], gs scalar) or of
+    n matrices (leading axis n, gs [n])."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    s = np.ascontiguousarray(s, dtype=np.uint8)
+    gs = np.ascontiguousarray(np.atleast_1d(np.asarray(gs, dtype=np.float32)))
+    one = q.ndim == 2
+    q3, s3 = (q[None], s[None]) if one else (q, s)
+    n, rows, K = q3.shape[0], q3.shape[1], q3.shape[2] * 2
+    w = np.empty((n, rows, K), dtype=np.float64)
+    rc = _load().oracle_nvfp4_unpack(_ptr(q3), _ptr(s3), _ptr(gs), n, rows, K, _ptr(w))
+    if rc != 0:
+        raise ValueError("NaN scale byte in NVFP4 tensor")
+    return w[0] if one else w
+
+
 # ------------------------------------------------------------------ router / permute
 
 def router_logits(x_bits: np.ndarray, W_r: np.ndarray, b: Optional[np.ndarray]) -> np.ndarray:
@@ -207,20 +275,26 @@ def activation_rows(x_bits: np.ndarray, act_fmt: int, want_codes: bool = False):
 
 
 def expert_ffn(a: np.ndarray, wg, wu, wd, act_fmt: int, want_h: bool = False):
-    """One expert on n activation rows.  wg/wu/wd are (q, s) MXFP4 pairs with
-    wg/wu of shape [I][d] and wd of shape [d][I].  Returns y [n][d] (bf16 values as fp32)
-    and optionally (h [n][I], hq, hs)."""
+    """One expert on n activation rows.  wg/wu/wd are MXFP4 pairs (q, s), or NVFP4 triples
+    (q, s, global scale) (reading R10), with wg/wu of shape [I][d] and wd of shape [d][I].
+    Returns y [n][d] (bf16 values as fp32) and optionally (h [n][I], hq, hs)."""
     a = np.ascontiguousarray(a, dtype=np.float32)
     n, d = a.shape
     I = wg[0].shape[0]
     assert wg[0].shape == (I, d // 2) and wu[0].shape == (I, d // 2) and wd[0].shape == (d, I // 2)
+    nv = len(wg) == 3
+    assert len(wu) == len(wg) and len(wd) == len(wg), "one weight format per expert"
     y = np.empty((n, d), dtype=np.float32)
     h = np.empty((n, I), dtype=np.float32) if want_h else None
     hq = np.zeros((n, I // 2), dtype=np.uint8) if want_h else None
     hs = np.zeros((n, I // 32), dtype=np.uint8) if want_h else None
-    ws = [np.ascontiguousarray(m, dtype=np.uint8) for pair in (wg, wu, wd) for m in pair]
-    _load().oracle_expert_ffn(_ptr(a), n, d, I, *[_ptr(m) for m in ws], act_fmt,
-                              _ptr(h), _ptr(hq), _ptr(hs), _ptr(y))
+    ws = [np.ascontiguousarray(m[i], dtype=np.uint8) for m in (wg, wu, wd) for i in (0, 1)]
+    if nv:
+        _load().oracle_expert_ffn_nvfp4(_ptr(a), n, d, I, *[_ptr(m) for m in ws], float(wg[2]), float(wu[2]),
+                                        float(wd[2]), act_fmt, _ptr(h), _ptr(hq), _ptr(hs), _ptr(y))
+    else:
+        _load().oracle_expert_ffn(_ptr(a), n, d, I, *[_ptr(m) for m in ws], act_fmt,
+                                  _ptr(h), _ptr(hq), _ptr(hs), _ptr(y))
     if want_h:
         return y, (h, hq, hs)
     return y
@@ -275,8 +349,8 @@ def moe_layer(x_bits: np.ndarray, W_r: np.ndarray, b: Optional[np.ndarray], k: i
     output row is normalised (``expert_norm``) before the weighted sum.
 
     ``expert_weights(e)`` returns {"gate": (q, s), "up": (q, s), "down": (q, s)} for expert e
-    (MXFP4 packed by this oracle's own packer), so only the experts the sampled tokens
-    touch need to exist on the host.
+    (MXFP4 packed by this oracle's own packer; (q, s, global scale) triples for NVFP4), so only
+    the experts the sampled tokens touch need to exist on the host.
     """
     T, d = x_bits.shape
     E = W_r.shape[0]
