@@ -39,7 +39,11 @@ N_LAYER_COPIES = 4
 # ------------------------------------------------------------------ byte / flop model
 # Per-expert sizes as the Muse Spark Open explainer models them (sections 10-13): an expert is
 # three matrices; reading it costs its packed bytes, computing one token costs 2 flops per
-# weight.  MXFP4 stores 4 bits per weight plus one byte per 32 weights (4.25 bits).
+# weight.  MXFP4 stores 4 bits per weight plus one byte per 32 weights (4.25 bits); NVFP4 one byte
+# per 16 weights (4.5 bits, the explainer's section 11 figure) plus a 4-byte global scale per matrix.
+
+WEIGHT_BITS = {"mxfp4": 4.25, "nvfp4": 4.5}
+GLOBAL_SCALE_BYTES = {"mxfp4": 0, "nvfp4": 4}
 
 def matrix_bytes(rows: int, K: int, bits_per_weight: float = 4.25) -> float:
     return rows * K * bits_per_weight / 8.0
@@ -49,8 +53,12 @@ def expert_bytes(d: int, I: int, bits_per_weight: float = 4.25) -> float:
     return 3 * matrix_bytes(I, d, bits_per_weight)
 
 
-def up_bytes_per_expert(d: int, I: int) -> float:
-    return 2 * matrix_bytes(I, d)
+def up_bytes_per_expert(d: int, I: int, wfmt: str = "mxfp4") -> float:
+    return 2 * (matrix_bytes(I, d, WEIGHT_BITS[wfmt]) + GLOBAL_SCALE_BYTES[wfmt])
+
+
+def expert_read_bytes(d: int, I: int, wfmt: str = "mxfp4") -> float:
+    return 3 * (matrix_bytes(I, d, WEIGHT_BITS[wfmt]) + GLOBAL_SCALE_BYTES[wfmt])
 
 
 def down_bytes_per_expert(d: int, I: int) -> float:
@@ -69,9 +77,9 @@ def crossover_tokens(read_us: float, compute_us_per_token: float) -> float:
     return read_us / compute_us_per_token
 
 
-def layer_algorithmic_bytes(d: int, I: int, E: int, T: int, n_active: float) -> float:
+def layer_algorithmic_bytes(d: int, I: int, E: int, T: int, n_active: float, wfmt: str = "mxfp4") -> float:
     """Touched experts + router weights and bias + x in + y out."""
-    return n_active * expert_bytes(d, I) + E * d * 4 + E * 4 + 2 * T * d * 2
+    return n_active * expert_read_bytes(d, I, wfmt) + E * d * 4 + E * 4 + 2 * T * d * 2
 
 
 # ------------------------------------------------------------------ environment helpers
@@ -229,8 +237,8 @@ def run_gpu(args, cfg, rank, world, local):
     dl = cm.d
     n_calls = max(cfg.calls, 1)
 
-    layers = [DeviceLayer(cm, device=dev, layer=i + 1000 * rank, mma_layouts=(fmt == B.MOE_ACT_MXFP4))
-              for i in range(args.layers)]
+    layers = [DeviceLayer(cm, device=dev, layer=i + 1000 * rank, mma_layouts=(fmt == B.MOE_ACT_MXFP4),
+                          wfmt=args.weights) for i in range(args.layers)]
     lat = Latent(cfg, dl, fmt, dev, layers) if args.latent else None
     # all seeded inputs resident in HBM before timing
     xs_host = np.stack([IN.make_x(cfg, call=(c + rank * 100000) % (1 << 20)) for c in range(min(n_calls, 1000))])
@@ -310,7 +318,7 @@ def run_gpu(args, cfg, rank, world, local):
     pk = peaks()
     bw = pk["hbm_gbs"] * 1e9
     mean_active = float(np.mean(n_active))
-    layer_bytes = layer_algorithmic_bytes(dl, I, E, T, mean_active)
+    layer_bytes = layer_algorithmic_bytes(dl, I, E, T, mean_active, args.weights)
     if lat is not None:  # + the projections, x and y at the model width instead of dl
         layer_bytes += lat.bytes_per_step() + 2 * T * (d - dl) * 2
 
@@ -330,13 +338,14 @@ def run_gpu(args, cfg, rank, world, local):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(fmt), "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(fmt, args.weights), "data": "synthetic",
         "config": {"workload": workload_name(args, cfg),
-                   "T": T, "d": d, "E": E, "k": k, "I": I, "act": args.fmt, "expert_norm_eps": norm_eps(args),
+                   "T": T, "d": d, "E": E, "k": k, "I": I, "act": args.fmt, "weights": args.weights,
+                   "expert_norm_eps": norm_eps(args),
                    "latent_width": dl if lat is not None else None,
                    "layer_copies_rotated": len(layers),
                    "l2": "inputs larger than L2: %d layer copies, %.1f GB of expert weights rotated"
-                         % (len(layers), len(layers) * E * expert_bytes(dl, I) / 1e9),
+                         % (len(layers), len(layers) * E * expert_read_bytes(dl, I, args.weights) / 1e9),
                    "cuda_graph": graph is not None, "parallelism": "replicas" if world > 1 else "single GPU"},
         "layer_roofline": layer_roofline(fmt, cm, layer_bytes, ms_per_step, bw, pk, mean_active, world,
                                          lat.flops_per_step() if lat is not None else 0.0),
@@ -368,8 +377,8 @@ def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, worl
     return out
 
 
-def dtype_name(fmt):
-    return "mxfp4 weights x bf16 activations, fp32 accumulate" if fmt == 0 else "mxfp4 x mxfp4, fp32 accumulate"
+def dtype_name(fmt, wfmt="mxfp4"):
+    return "%s weights x bf16 activations, fp32 accumulate" % wfmt if fmt == 0 else "mxfp4 x mxfp4, fp32 accumulate"
 
 
 EXPERT_NORM_EPS = 1e-6
@@ -398,6 +407,8 @@ def workload_name(args, cfg):
         name += " + shared latent projections %d -> %d -> %d" % (cfg.d, args.latent, cfg.d)
     if norm_eps(args):
         name += " + per-expert RMSNorm before the weighted sum"
+    if getattr(args, "weights", "mxfp4") == "nvfp4":
+        name += ", NVFP4 expert weights (E4M3 scale per 16 values, fp32 scale per matrix)"
     return name
 
 
@@ -503,11 +514,12 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
     stream.synchronize()
     dur = [a.elapsed_time(b) for a, b in evs]
     n_act = float(np.mean([int(a.item()) for a in active]))
-    per_launch = n_act * up_bytes_per_expert(d, I) + T * d * 2 + P * I * 2
+    per_launch = n_act * up_bytes_per_expert(d, I, args.weights) + T * d * 2 + P * I * 2
     avg_ms = float(np.mean(dur))
     achieved = per_launch / (avg_ms / 1e3) / 1e9
-    traffic = ncu_traffic("gemv_up_decode.md", ["bit_expert_ffn_moe_gb300/csrc/gemv.cu",
-                                                "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
+    profile = "gemv_up_decode.md" if args.weights == "mxfp4" else "gemv_up_decode_nvfp4.md"
+    traffic = ncu_traffic(profile, ["bit_expert_ffn_moe_gb300/csrc/gemv.cu",
+                                    "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
     return {"kernel": "gemv_up_kernel (gate/up + SwiGLU, decode)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
@@ -640,7 +652,8 @@ def oracle_sample(args, cfg, n_tokens):
             out = {}
             for name, tid in (("gate", IN.TENSOR_GATE), ("up", IN.TENSOR_UP), ("down", IN.TENSOR_DOWN)):
                 rows, K = shapes[tid]
-                out[name] = O.mxfp4_pack(IN.synth_weights(layer_seed, tid, e, rows, K, cfg.weight_std))
+                w = IN.synth_weights(layer_seed, tid, e, rows, K, cfg.weight_std)
+                out[name] = O.nvfp4_pack(w) if getattr(args, "weights", "mxfp4") == "nvfp4" else O.mxfp4_pack(w)
             cache[e] = out
         return cache[e]
 
@@ -719,7 +732,8 @@ def run_reference(args, cfg, rank, world):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
            "config": {"workload": workload_name(args, cfg),
                       "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I, "act": args.fmt,
-                      "expert_norm_eps": norm_eps(args), "latent_width": args.latent or None},
+                      "weights": args.weights, "expert_norm_eps": norm_eps(args),
+                      "latent_width": args.latent or None},
            "impl": "reference",
            "cpu_baseline": {"value": res["value"], "unit": UNIT, "cores": res["cores"], "kind": "oracle",
                             "sample": res["sample"] + "; %d of the %d requested steps" % (n, args.steps)},
@@ -743,6 +757,8 @@ def main():
                          "at that width and widen the weighted sum back (0 = off)")
     ap.add_argument("--expert-norm", action="store_true",
                     help="normalise each expert output (RMSNorm over d, eps 1e-6) before the weighted sum")
+    ap.add_argument("--weights", choices=["mxfp4", "nvfp4"], default="mxfp4",
+                    help="expert weight format (nvfp4: E4M3 scale per 16 values; bf16 activations only)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     args = ap.parse_args()
@@ -751,7 +767,9 @@ def main():
     from bit_expert_ffn_moe_gb300 import inputs as IN
     cfg = IN.CONFIGS[args.config]
     if args.fmt is None:
-        args.fmt = "bf16" if cfg.T <= 8 else "mxfp4"
+        args.fmt = "bf16" if cfg.T <= 8 or args.weights == "nvfp4" else "mxfp4"
+    if args.weights == "nvfp4" and args.fmt != "bf16":
+        ap.error("NVFP4 expert weights are read by the bf16-activation path only")
     rank, world, local = dist_env()
 
     if args.impl == "reference":

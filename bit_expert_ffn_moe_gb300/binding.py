@@ -24,13 +24,16 @@ MOE_ERR_DEVICE = 6
 MOE_ACT_BF16 = 0
 MOE_ACT_MXFP4 = 1
 
+MOE_W_MXFP4 = 0
+MOE_W_NVFP4 = 1
+
 # every entry point declared in include/moe.h
 EXPORTED = (
     "moe_status_string", "moe_abi_version", "moe_last_cuda_error", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
     "moe_mxfp4_scales_to_mma", "moe_mxfp4_codes_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
-    "moe_dense_workspace_size", "moe_dense_linear",
+    "moe_dense_workspace_size", "moe_dense_linear", "moe_nvfp4_pack", "moe_nvfp4_unpack",
 )
 
 
@@ -46,7 +49,8 @@ class MoeError(RuntimeError):
 class moe_expert_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s", "gate_q_mma", "gate_s_mma",
-                 "up_q_mma", "up_s_mma", "down_q_mma", "down_s_mma")]
+                 "up_q_mma", "up_s_mma", "down_q_mma", "down_s_mma")] + \
+               [("wfmt", ctypes.c_int32)] + [(n, ctypes.c_void_p) for n in ("gate_gs", "up_gs", "down_gs")]
 
 
 class moe_mxfp4_matrix(ctypes.Structure):
@@ -86,6 +90,8 @@ _SIGS = {
     "moe_layer_forward_norm": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, ctypes.c_float, P, P, P, P, SZ, P]),
     "moe_synth_weights": (I32, [U64, U32, U32, U32, I64, I64, ctypes.c_float, P, P]),
     "moe_selftest_wait_timeout": (I32, [P, SZ, I32, P]),
+    "moe_nvfp4_pack": (I32, [P, I64, I64, I64, P, P, P, P]),
+    "moe_nvfp4_unpack": (I32, [P, P, P, I64, I64, I64, P, P]),
 }
 
 
@@ -145,6 +151,15 @@ def expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s, gate_q_mma
                                                 up_q_mma, up_s_mma, down_q_mma, down_s_mma)])
 
 
+def nvfp4_expert_weights_struct(gate_q, gate_s, gate_gs, up_q, up_s, up_gs, down_q, down_s,
+                                down_gs) -> moe_expert_weights:
+    """NVFP4 expert weights: codes, E4M3 scales [.][K/16] and per-expert global scales [E]."""
+    W = expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s)
+    W.wfmt = MOE_W_NVFP4
+    W.gate_gs, W.up_gs, W.down_gs = _p(gate_gs), _p(up_gs), _p(down_gs)
+    return W
+
+
 def mxfp4_matrix_struct(q, s, q_mma=None, s_mma=None) -> moe_mxfp4_matrix:
     return moe_mxfp4_matrix(*[_p(t) for t in (q, s, q_mma, s_mma)])
 
@@ -161,6 +176,15 @@ def moe_mxfp4_pack(w, rows, K, q, s, stream=None):
 
 def moe_mxfp4_unpack(q, s, rows, K, w, stream=None):
     _check("moe_mxfp4_unpack", load().moe_mxfp4_unpack(_p(q), _p(s), rows, K, _p(w), _stream(stream)))
+
+
+def moe_nvfp4_pack(w, n_mats, rows, K, q, s, gs, stream=None):
+    _check("moe_nvfp4_pack", load().moe_nvfp4_pack(_p(w), n_mats, rows, K, _p(q), _p(s), _p(gs), _stream(stream)))
+
+
+def moe_nvfp4_unpack(q, s, gs, n_mats, rows, K, w, stream=None):
+    _check("moe_nvfp4_unpack", load().moe_nvfp4_unpack(_p(q), _p(s), _p(gs), n_mats, rows, K, _p(w),
+                                                       _stream(stream)))
 
 
 def moe_mxfp4_mma_scale_bytes(rows, K) -> int:

@@ -8,7 +8,7 @@ using namespace moe;
 
 namespace {
 
-constexpr int kAbiVersion = 6;
+constexpr int kAbiVersion = 7;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -60,6 +60,13 @@ moe_status check_ws(void* ws, size_t ws_bytes, const WsLayout& L) {
 
 moe_status check_weights(const moe_expert_weights* W, moe_act_fmt fmt, bool need_up, bool need_down) {
     if (W == nullptr) return MOE_ERR_INVALID_ARG;
+    if (W->wfmt != MOE_W_MXFP4 && W->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
+    if (W->wfmt == MOE_W_NVFP4) {  // the GEMV path only; E4M3 scale pairs are read as 16-bit words
+        if (fmt != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED_SHAPE;
+        if (need_up && (!W->gate_gs || !W->up_gs || !aligned(W->gate_s, 2) || !aligned(W->up_s, 2)))
+            return MOE_ERR_INVALID_ARG;
+        if (need_down && (!W->down_gs || !aligned(W->down_s, 2))) return MOE_ERR_INVALID_ARG;
+    }
     if (need_up) {
         if (!W->gate_q || !W->gate_s || !W->up_q || !W->up_s) return MOE_ERR_INVALID_ARG;
         if (!aligned(W->gate_q, 16) || !aligned(W->up_q, 16)) return MOE_ERR_INVALID_ARG;
@@ -128,6 +135,33 @@ moe_status moe_mxfp4_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, in
     if (!w || !q || !s || !aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
     MOE_TRY(check_device());
     return from_cuda(launch_unpack(q, s, rows, K, w, (cudaStream_t)stream));
+}
+
+// ---------------------------------------------------------------- NVFP4 helpers
+
+static moe_status check_nvfp4(const void* w, int64_t n_mats, int64_t rows, int64_t K, const void* q, const void* s,
+                              const void* gs) {
+    if (n_mats < 0 || n_mats > 65535 || rows < 0 || K <= 0 || K % 32 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (n_mats == 0) return MOE_OK;
+    if (!gs || !aligned(gs, 4)) return MOE_ERR_INVALID_ARG;
+    if (rows > 0 && (!w || !q || !s || !aligned(w, 16) || !aligned(q, 16) || !aligned(s, 2))) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status moe_nvfp4_pack(const float* w, int64_t n_mats, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, float* gs,
+                          moe_stream_t stream) {
+    MOE_TRY(check_nvfp4(w, n_mats, rows, K, q, s, gs));
+    if (n_mats == 0) return MOE_OK;
+    MOE_TRY(check_device());
+    return from_cuda(launch_nvfp4_pack(w, n_mats, rows, K, q, s, gs, (cudaStream_t)stream));
+}
+
+moe_status moe_nvfp4_unpack(const uint8_t* q, const uint8_t* s, const float* gs, int64_t n_mats, int64_t rows,
+                            int64_t K, float* w, moe_stream_t stream) {
+    MOE_TRY(check_nvfp4(w, n_mats, rows, K, q, s, gs));
+    if (n_mats == 0 || rows == 0) return MOE_OK;
+    MOE_TRY(check_device());
+    return from_cuda(launch_nvfp4_unpack(q, s, gs, n_mats, rows, K, w, (cudaStream_t)stream));
 }
 
 size_t moe_mxfp4_mma_scale_bytes(int64_t rows, int64_t K) {

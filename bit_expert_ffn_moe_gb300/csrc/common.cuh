@@ -180,6 +180,30 @@ __device__ __forceinline__ uint32_t e2m1x8_encode(const float* a) {
     return mag | (r & nonzero);
 }
 
+// Two E4M3 bytes (OCP OFP8: bias 7, subnormals, largest finite 448) -> their values as fp32; the
+// byte in bits 0..7 becomes .x.  Every E4M3 value is an f16 value, so the hardware conversion to
+// f16 pairs is exact.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t two) {
+    uint32_t h;
+    asm("{\n\t.reg .b16 p;\n\t"
+        "cvt.u16.u32 p, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, p;\n\t}"
+        : "=r"(h)
+        : "r"(two));
+    return h2_to_f2(h);
+}
+
+// fp32 t >= 0 -> the nearest E4M3 byte, ties to even, saturating at 448 (hardware conversion).
+__device__ __forceinline__ uint32_t f32_to_e4m3_sat(float t) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 p;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 p, %1, %1;\n\t"
+        "cvt.u32.u16 %0, p;\n\t}"
+        : "=r"(r)
+        : "f"(t));
+    return r & 0xFFu;  // both halves hold the same conversion
+}
+
 // Block exponent X = floor(log2(amax)) - 2 clamped to [-127, 127] (amax = 0 gives -127).
 // Returns the scale byte X + 127 and writes 2^-X (exact) to inv_scale.
 __device__ __forceinline__ uint32_t mx_scale_from_amax(float amax, float& inv_scale) {
@@ -307,6 +331,10 @@ cudaError_t launch_synth(uint64_t seed, uint32_t tensor_id, uint32_t expert_firs
 cudaError_t launch_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, uint8_t* s, cudaStream_t st);
 cudaError_t launch_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w, cudaStream_t st);
 cudaError_t launch_scales_to_mma(const uint8_t* s, int64_t rows, int64_t K, uint8_t* s_mma, cudaStream_t st);
+cudaError_t launch_nvfp4_pack(const float* w, int64_t n_mats, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
+                              float* gs, cudaStream_t st);
+cudaError_t launch_nvfp4_unpack(const uint8_t* q, const uint8_t* s, const float* gs, int64_t n_mats, int64_t rows,
+                                int64_t K, float* w, cudaStream_t st);
 cudaError_t launch_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma, cudaStream_t st);
 
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,

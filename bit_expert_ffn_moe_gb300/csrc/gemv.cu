@@ -1,4 +1,6 @@
-// gemv.cu -- decode-shape expert kernels (MOE_ACT_BF16): bf16 activations, MXFP4 weights.
+// gemv.cu -- decode-shape expert kernels (MOE_ACT_BF16): bf16 activations, MXFP4 or NVFP4
+// weights (template flag NV: two E4M3 scales per 32-element block and a global scale per matrix,
+// applied to each 16-element half-sum and to the finished dot product).
 //
 // At decode sizes every chosen expert sees one or a few tokens, so the expert matrices are read
 // once and used for very little arithmetic: the time is the weight read (Muse Spark Open
@@ -57,6 +59,33 @@ __device__ __forceinline__ float block_dot(const uint4& codes, const uint32_t (&
         a1 = dot2_f16(h[3], x[4 * m + 3], a1);
     }
     return a0 + a1;
+}
+
+// NVFP4: acc + the dot product of one 32-element block with 32 f16 activations, each 16-element
+// half scaled by its E4M3 scale (sc: elements 0..15 in bits 0..7, 16..31 in bits 8..15).
+__device__ __forceinline__ float block_dot_nv(const uint4& codes, const uint32_t (&x)[16], uint32_t sc, float acc) {
+    const uint32_t words[4] = {codes.x, codes.y, codes.z, codes.w};
+    float a[4] = {0.f, 0.f, 0.f, 0.f};  // a[0], a[1]: elements 0..15; a[2], a[3]: 16..31
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        uint32_t h[4];
+        e2m1x8_to_h2(words[m], h);
+        const int p = (m >> 1) * 2;
+        a[p] = dot2_f16(h[0], x[4 * m + 0], a[p]);
+        a[p + 1] = dot2_f16(h[1], x[4 * m + 1], a[p + 1]);
+        a[p] = dot2_f16(h[2], x[4 * m + 2], a[p]);
+        a[p + 1] = dot2_f16(h[3], x[4 * m + 3], a[p + 1]);
+    }
+    const float2 s = e4m3x2_to_f2(sc);
+    return fmaf(a[2] + a[3], s.y, fmaf(a[0] + a[1], s.x, acc));
+}
+
+// Scale word of one 32-element block (idx = row * K/32 + block): MXFP4 one E8M0 byte, NVFP4 the
+// block's two E4M3 bytes.
+template <bool NV>
+__device__ __forceinline__ uint32_t load_block_scale(const uint8_t* s, size_t idx) {
+    if constexpr (NV) return __ldg(reinterpret_cast<const unsigned short*>(s) + idx);
+    else return __ldg(s + idx);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -125,6 +154,8 @@ struct GemvArgs {
     const uint8_t* s0;
     const uint8_t* q1;  // up: up codes
     const uint8_t* s1;
+    const float* gs0;   // NVFP4: global scale per expert of q0 / q1
+    const float* gs1;
     const uint16_t* act;  // up: x [T][d]; down: h [P][I]
     const int32_t* perm_token;
     const int32_t* offsets;
@@ -142,7 +173,7 @@ struct GemvArgs {
 // Grid (I / outs, slots): slot u is the u-th active expert.  Warp w computes outputs
 // i = blockIdx.x * outs + w * kUpOutsPerWarp + o, reading gate row i and up row i (lane l owns
 // K-blocks l + 32 j, j < BPL) and the staged activation blocks of up to kQ tokens.
-template <int BPL>
+template <int BPL, bool NV>
 __global__ void __launch_bounds__(kThr, 2)
 gemv_up_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -171,8 +202,8 @@ gemv_up_kernel(const GemvArgs a) {
             if (b < nb) {
                 wg[j] = ldg_stream(a.q0 + grow * row_bytes + 16 * (size_t)b);
                 wu[j] = ldg_stream(a.q1 + grow * row_bytes + 16 * (size_t)b);
-                sg[j] = __ldg(a.s0 + grow * nb + b);
-                su[j] = __ldg(a.s1 + grow * nb + b);
+                sg[j] = load_block_scale<NV>(a.s0, grow * nb + b);
+                su[j] = load_block_scale<NV>(a.s1, grow * nb + b);
             }
         }
     };
@@ -204,8 +235,13 @@ gemv_up_kernel(const GemvArgs a) {
                         if (q < nq) {
                             uint32_t x[16];
                             load_x_block(xs, q, nb, b, x);
-                            g[q] = fmaf(block_dot(wg[j], x), fg, g[q]);
-                            u[q] = fmaf(block_dot(wu[j], x), fu, u[q]);
+                            if constexpr (NV) {
+                                g[q] = block_dot_nv(wg[j], x, sg[j], g[q]);
+                                u[q] = block_dot_nv(wu[j], x, su[j], u[q]);
+                            } else {
+                                g[q] = fmaf(block_dot(wg[j], x), fg, g[q]);
+                                u[q] = fmaf(block_dot(wu[j], x), fu, u[q]);
+                            }
                         }
                     }
                 }
@@ -215,7 +251,11 @@ gemv_up_kernel(const GemvArgs a) {
 #pragma unroll
             for (int q = 0; q < kQ; ++q) {
                 if (q < nq) {
-                    const float gs = warp_sum(g[q]) * inv[q], us = warp_sum(u[q]) * inv[q];
+                    float gs = warp_sum(g[q]) * inv[q], us = warp_sum(u[q]) * inv[q];
+                    if constexpr (NV) {
+                        gs *= __ldg(a.gs0 + e);
+                        us *= __ldg(a.gs1 + e);
+                    }
                     if (lane == q) {
                         const float hv = gs / (1.f + expf(-gs)) * us;  // SiLU(g) * u
                         a.out[(size_t)(r0 + tc0 + q) * a.M_exp + i0 + o] = f32_to_bf16_bits(hv);
@@ -314,7 +354,7 @@ __device__ void stage_rows_warp(const uint16_t* __restrict__ src, const int* row
 }
 
 // Weight rows of one batch into registers (rows[j] = global row index, or -1 to skip).
-template <int BPT>
+template <int BPT, bool NV>
 __device__ __forceinline__ void load_rows_cta(const uint8_t* const (&q)[kR], const uint8_t* const (&s)[kR],
                                           const size_t (&grow)[kR], int gl, const CtaGeo& geo, size_t row_bytes,
                                           uint4 (&wv)[kR][BPT], uint32_t (&sv)[kR][BPT]) {
@@ -325,14 +365,14 @@ __device__ __forceinline__ void load_rows_cta(const uint8_t* const (&q)[kR], con
             const int b = gl + c * geo.G;
             if (b < geo.nb) {
                 wv[j][c] = ldg_stream(q[j] + grow[j] * row_bytes + 16 * (size_t)b);
-                sv[j][c] = __ldg(s[j] + grow[j] * geo.nb + b);
+                sv[j][c] = load_block_scale<NV>(s[j], grow[j] * geo.nb + b);
             }
         }
 }
 
 // kR x Q partial dot products of the thread's blocks: acc[qq * kR + j] for staged row q0 + qq
 // (qq < nq) against weight row j.
-template <int BPT, int Q>
+template <int BPT, int Q, bool NV>
 __device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int gl, const CtaGeo& geo,
                                            const uint4 (&wv)[kR][BPT], const uint32_t (&sv)[kR][BPT],
                                            float (&acc)[kR * Q]) {
@@ -348,8 +388,12 @@ __device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int 
                     uint32_t x[16];
                     load_x_block(xs, q0 + qq, geo.nb, b, x);
 #pragma unroll
-                    for (int j = 0; j < kR; ++j)
-                        acc[qq * kR + j] = fmaf(block_dot(wv[j][c], x), e8m0_to_f32(sv[j][c]), acc[qq * kR + j]);
+                    for (int j = 0; j < kR; ++j) {
+                        if constexpr (NV)
+                            acc[qq * kR + j] = block_dot_nv(wv[j][c], x, sv[j][c], acc[qq * kR + j]);
+                        else
+                            acc[qq * kR + j] = fmaf(block_dot(wv[j][c], x), e8m0_to_f32(sv[j][c]), acc[qq * kR + j]);
+                    }
                 }
             }
         }
@@ -359,7 +403,7 @@ __device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int 
 // Grid (M_exp / outs, slots): slot u is the u-th active expert.  A batch gives each row group
 // kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens; an
 // expert with more rows takes them Q at a time (its weights are read again per pass).
-template <int BPT, int Q>
+template <int BPT, int Q, bool NV>
 __global__ void __launch_bounds__(kThr)
 gemv_up_cta_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -398,7 +442,7 @@ gemv_up_cta_kernel(const GemvArgs a) {
     {
         size_t g[kR];
         grows(0, g);
-        load_rows_cta<BPT>(qsel, ssel, g, gl, geo, row_bytes, wcur, scur);  // weights depend only on e
+        load_rows_cta<BPT, NV>(qsel, ssel, g, gl, geo, row_bytes, wcur, scur);  // weights depend only on e
     }
     const int r0 = a.offsets[e], n = a.offsets[e + 1] - r0;
 
@@ -413,10 +457,10 @@ gemv_up_cta_kernel(const GemvArgs a) {
             if (more) {
                 size_t g[kR];
                 grows(bi + 1 < nbatch ? bi + 1 : 0, g);
-                load_rows_cta<BPT>(qsel, ssel, g, gl, geo, row_bytes, wnxt, snxt);
+                load_rows_cta<BPT, NV>(qsel, ssel, g, gl, geo, row_bytes, wnxt, snxt);
             }
             float acc[V];
-            batch_dots<BPT, Q>(xs, 0, nq, gl, geo, wcur, scur, acc);
+            batch_dots<BPT, Q, NV>(xs, 0, nq, gl, geo, wcur, scur, acc);
             // partial sums go to alternating halves of red, so one barrier per batch suffices: the
             // leader warp finishes batch bi's features while the others compute batch bi + 1
             float* rb = red + (bi & 1) * (8 * 32);
@@ -436,6 +480,10 @@ gemv_up_cta_kernel(const GemvArgs a) {
                     }
                     g *= inv[qq];
                     u *= inv[qq];
+                    if constexpr (NV) {
+                        g *= __ldg(a.gs0 + e);
+                        u *= __ldg(a.gs1 + e);
+                    }
                     const float hv = g / (1.f + expf(-g)) * u;  // SiLU(g) * u
                     const int i = i_base + bi * kOut + j;
                     a.out[(size_t)(r0 + tc0 + qq) * a.M_exp + i] = f32_to_bf16_bits(hv);
@@ -469,35 +517,39 @@ gemv_up_cta_kernel(const GemvArgs a) {
 // scaled back by the inverse, an exact rescaling.
 // FUSED: ys[t][f] accumulates w * bf16(expert output) batch after batch (the same lane updates a
 // given (t, f) in expert order); otherwise the bf16 outputs go to y_perm.
-// Q = 1: three stages; Q = 2, 4: two stages (the h rows take the third stage's shared memory,
-// so that two CTAs still fit an SM).  8-element h pieces per thread and batch: 2 for Q <= 2
+// MXFP4, Q = 1: three stages; otherwise two (for Q = 2, 4 the h rows take the third stage's
+// shared memory, and the NVFP4 stages are larger by their second scale byte per block, so that
+// two CTAs still fit an SM).  8-element h pieces per thread and batch: 2 for Q <= 2
 // (Q K/8 <= 2 kThr), Q for Q = 4.
-template <int Q> __host__ __device__ constexpr int down_stages() { return Q == 1 ? 3 : 2; }
+template <int Q, bool NV> __host__ __device__ constexpr int down_stages() { return Q == 1 && !NV ? 3 : 2; }
 template <int Q> __host__ __device__ constexpr int down_hunits() { return Q <= 2 ? 2 : Q; }
 
-__host__ __device__ inline uint32_t down_stage_bytes(int K) {
+// Bytes of one stage: codes, then scales (one byte per 32-element block, two for NVFP4).
+__host__ __device__ inline uint32_t down_stage_bytes(int K, bool nv) {
     const CtaGeo g = make_cta_geo(K);
-    return (uint32_t)(g.RG * kR) * (uint32_t)(K / 2 + K / 32);
+    return (uint32_t)(g.RG * kR) * (uint32_t)(K / 2 + (K / 32) * (nv ? 2 : 1));
 }
 
-template <int Q>
+template <int Q, bool NV>
 __host__ __device__ inline size_t down_ring_smem(int K, int P) {
     const CtaGeo g = make_cta_geo(K);
-    return (size_t)down_stages<Q>() * down_stage_bytes(K) + (size_t)2 * Q * K * 2 /* h blocks */ +
+    return (size_t)down_stages<Q, NV>() * down_stage_bytes(K, NV) + (size_t)2 * Q * K * 2 /* h blocks */ +
            sizeof(float) * ((size_t)2 * Q * g.nb /* inverse scales */ + 2 * 8 * 32 + (size_t)Q * g.RG * kR) +
-           sizeof(uint64_t) * down_stages<Q>() + sizeof(int) * 3 * (size_t)P;
+           sizeof(uint64_t) * down_stages<Q, NV>() + sizeof(int) * 3 * (size_t)P;
 }
 
-template <int Q, bool FUSED>
+template <int Q, bool FUSED, bool NV>
 __global__ void __launch_bounds__(kThr, 2)
 gemv_down_ring_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int V = kR * Q;
-    constexpr int kDownStages = down_stages<Q>();
+    constexpr int kDownStages = down_stages<Q, NV>();
     constexpr int kDownHUnits = down_hunits<Q>();
+    constexpr uint32_t kScaleBytes = NV ? 2 : 1;  // per 32-element block
     const CtaGeo geo = make_cta_geo(a.K);
     const int feats = geo.RG * kR, nb = geo.nb;
-    const uint32_t code_bytes = (uint32_t)feats * (a.K / 2), stage_bytes = code_bytes + (uint32_t)feats * (a.K / 32);
+    const uint32_t code_bytes = (uint32_t)feats * (a.K / 2),
+                   stage_bytes = code_bytes + (uint32_t)feats * (a.K / 32) * kScaleBytes;
     uint4* hb = reinterpret_cast<uint4*>(smem + (size_t)kDownStages * stage_bytes);  // [2][Q][4][nb] f16 blocks
     float* hinv = reinterpret_cast<float*>(hb + (size_t)2 * Q * 4 * nb);               // [2][Q][nb]
     float* red = hinv + 2 * Q * nb;                                                     // [2][8 warps][32]
@@ -539,7 +591,7 @@ gemv_down_ring_kernel(const GemvArgs a) {
         const size_t R = (size_t)sl_e[u] * a.M_exp + f0;
         mbar_arrive_expect_tx(&full[s], stage_bytes);
         bulk_load(stage(s), a.q0 + R * K2, code_bytes, &full[s]);
-        bulk_load(stage(s) + code_bytes, a.s0 + R * (a.K / 32), stage_bytes - code_bytes, &full[s]);
+        bulk_load(stage(s) + code_bytes, a.s0 + R * (a.K / 32) * kScaleBytes, stage_bytes - code_bytes, &full[s]);
     };
     int issued = 0;
     if (tid == 0)
@@ -613,8 +665,13 @@ gemv_down_ring_kernel(const GemvArgs a) {
                     for (int j = 0; j < kR; ++j) {
                         const int row = grp * kR + j;
                         const uint4 w = *reinterpret_cast<const uint4*>(st + (size_t)row * K2 + 16 * gl);
-                        const uint32_t sc = st[code_bytes + (size_t)row * nb + gl];
-                        acc[qq * kR + j] = block_dot(w, x) * e8m0_to_f32(sc) * inv;
+                        if constexpr (NV) {
+                            const uint32_t sc = reinterpret_cast<const uint16_t*>(st + code_bytes)[(size_t)row * nb + gl];
+                            acc[qq * kR + j] = block_dot_nv(w, x, sc, 0.f) * inv;
+                        } else {
+                            const uint32_t sc = st[code_bytes + (size_t)row * nb + gl];
+                            acc[qq * kR + j] = block_dot(w, x) * e8m0_to_f32(sc) * inv;
+                        }
                     }
                 }
             }
@@ -635,6 +692,7 @@ gemv_down_ring_kernel(const GemvArgs a) {
             if (leader && qq < cnt) {
                 float o = 0.f;
                 for (int w = 0; w < wpg; ++w) o += rb[(grp * wpg + w) * 32 + lane];
+                if constexpr (NV) o *= __ldg(a.gs0 + sl_e[u]);
                 const uint16_t ob = f32_to_bf16_bits(o);
                 if (FUSED) {
                     const int t = a.perm_token[r0 + qq];
@@ -674,7 +732,7 @@ gemv_down_ring_kernel(const GemvArgs a) {
 // order, prefetching the next segment's weight rows.
 // FUSED: y[t] accumulates w * bf16(expert output) in that order, which is the slot order j of the
 // token (ids are ascending); otherwise the bf16 expert outputs go to y_perm.
-template <int BPL, bool FUSED>
+template <int BPL, bool FUSED, bool NV>
 __global__ void __launch_bounds__(kThr, 2)
 gemv_down_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -743,7 +801,7 @@ gemv_down_kernel(const GemvArgs a) {
                 const int b = lane + 32 * j;
                 if (b < nb) {
                     wv[rr][j] = ldg_stream(a.q0 + grow * row_bytes + 16 * (size_t)b);
-                    sv[rr][j] = __ldg(a.s0 + grow * nb + b);
+                    sv[rr][j] = load_block_scale<NV>(a.s0, grow * nb + b);
                 }
             }
         }
@@ -755,6 +813,7 @@ gemv_down_kernel(const GemvArgs a) {
     stage_rows_f16(a.act, s_row, nrows, a.K, hs, inv, smax);
     while (qs < nrows) {
         const int e = s_exp[qs];
+        const float gsd = NV ? __ldg(a.gs0 + e) : 1.f;  // NVFP4: the expert's global scale
         int qe = qs + 1;
         while (qe < nrows && s_exp[qe] == e) ++qe;
         const bool more = qe < nrows;
@@ -770,13 +829,18 @@ gemv_down_kernel(const GemvArgs a) {
                     uint32_t x[16];
                     load_x_block(hs, q, nb, b, x);
 #pragma unroll
-                    for (int rr = 0; rr < RPW; ++rr)
-                        acc[rr] = fmaf(block_dot(wcur[rr][j], x), e8m0_to_f32(scur[rr][j]), acc[rr]);
+                    for (int rr = 0; rr < RPW; ++rr) {
+                        if constexpr (NV)
+                            acc[rr] = block_dot_nv(wcur[rr][j], x, scur[rr][j], acc[rr]);
+                        else
+                            acc[rr] = fmaf(block_dot(wcur[rr][j], x), e8m0_to_f32(scur[rr][j]), acc[rr]);
+                    }
                 }
             }
 #pragma unroll
             for (int rr = 0; rr < RPW; ++rr) {
-                const float s = warp_sum(acc[rr]) * inv[q];
+                float s = warp_sum(acc[rr]) * inv[q];
+                if constexpr (NV) s *= gsd;
                 if (lane == rr) {
                     const uint16_t sb = f32_to_bf16_bits(s);
                     if (FUSED) {
@@ -918,12 +982,43 @@ static int bpl_for(int K) {
 
 bool gemv_supported(int d, int I) { return bpl_for(d) != 0 && bpl_for(I) != 0; }
 
+template <bool NV>
+static const void* up_cta_kernel(int bpt, int Q) {
+    if (bpt == 1) return Q == 1 ? (const void*)gemv_up_cta_kernel<1, 1, NV> : (const void*)gemv_up_cta_kernel<1, 2, NV>;
+    return Q == 1 ? (const void*)gemv_up_cta_kernel<2, 1, NV> : (const void*)gemv_up_cta_kernel<2, 2, NV>;
+}
+
+template <bool NV>
+static const void* up_warp_kernel(int bpl) {
+    return bpl == 1 ? (const void*)gemv_up_kernel<1, NV> : bpl == 2 ? (const void*)gemv_up_kernel<2, NV>
+         : bpl == 4 ? (const void*)gemv_up_kernel<4, NV> : (const void*)gemv_up_kernel<8, NV>;
+}
+
+template <bool F, bool NV>
+static const void* down_kernel(int bpl) {
+    return bpl == 1 ? (const void*)gemv_down_kernel<1, F, NV> : bpl == 2 ? (const void*)gemv_down_kernel<2, F, NV>
+         : bpl == 4 ? (const void*)gemv_down_kernel<4, F, NV> : (const void*)gemv_down_kernel<8, F, NV>;
+}
+
+template <bool NV>
+static const void* ring_kernel(int T, bool fused) {
+    if (T == 1) return fused ? (const void*)gemv_down_ring_kernel<1, true, NV> : (const void*)gemv_down_ring_kernel<1, false, NV>;
+    if (T == 2) return fused ? (const void*)gemv_down_ring_kernel<2, true, NV> : (const void*)gemv_down_ring_kernel<2, false, NV>;
+    return fused ? (const void*)gemv_down_ring_kernel<4, true, NV> : (const void*)gemv_down_ring_kernel<4, false, NV>;
+}
+
+template <bool NV>
+static size_t ring_smem(int T, int K, int P) {
+    return T == 1 ? down_ring_smem<1, NV>(K, P) : T == 2 ? down_ring_smem<2, NV>(K, P) : down_ring_smem<4, NV>(K, P);
+}
+
 cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,
                            cudaStream_t st, bool pdl) {
     const int P = T * k;
     if (P == 0) return cudaSuccess;
     const int bpl = bpl_for(d);
+    const bool nv = W->wfmt == MOE_W_NVFP4;
     if (T <= 4 && make_cta_geo(d).bpt <= 2) {
         // up to four tokens: CTA-wide split of K (see gemv_up_cta_kernel), two token rows per pass
         const CtaGeo geo = make_cta_geo(d);
@@ -937,6 +1032,8 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
         a.s0 = W->gate_s;
         a.q1 = W->up_q;
         a.s1 = W->up_s;
+        a.gs0 = W->gate_gs;
+        a.gs1 = W->up_gs;
         a.act = x;
         a.perm_token = perm_token;
         a.offsets = offsets;
@@ -952,9 +1049,7 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
         const size_t smem = (size_t)Q * d * 2 + sizeof(float) * (Q + 2 * 8 * 32) + sizeof(int) * Q + sizeof(unsigned) * Q;
         void* args[] = {&a};
         const dim3 grid(I / outs, P < E ? P : E);
-        const void* f;
-        if (geo.bpt == 1) f = Q == 1 ? (const void*)gemv_up_cta_kernel<1, 1> : (const void*)gemv_up_cta_kernel<1, 2>;
-        else f = Q == 1 ? (const void*)gemv_up_cta_kernel<2, 1> : (const void*)gemv_up_cta_kernel<2, 2>;
+        const void* f = nv ? up_cta_kernel<true>(geo.bpt, Q) : up_cta_kernel<false>(geo.bpt, Q);
         return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
     }
     const int outs = kWarps * kUpOutsPerWarp;
@@ -964,6 +1059,8 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
     a.s0 = W->gate_s;
     a.q1 = W->up_q;
     a.s1 = W->up_s;
+    a.gs0 = W->gate_gs;
+    a.gs1 = W->up_gs;
     a.act = x;
     a.perm_token = perm_token;
     a.offsets = offsets;
@@ -978,15 +1075,8 @@ cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const i
     const size_t smem = (size_t)kQ * d * 2 + sizeof(float) * kQ + sizeof(unsigned) * kQ + sizeof(int) * kQ;
     void* args[] = {&a};
     const dim3 grid(I / outs, P < E ? P : E);
-    const void* f = bpl == 1 ? (const void*)gemv_up_kernel<1> : bpl == 2 ? (const void*)gemv_up_kernel<2>
-                  : bpl == 4 ? (const void*)gemv_up_kernel<4> : (const void*)gemv_up_kernel<8>;
+    const void* f = nv ? up_warp_kernel<true>(bpl) : up_warp_kernel<false>(bpl);
     return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
-}
-
-template <bool F>
-static const void* down_kernel(int bpl) {
-    return bpl == 1 ? (const void*)gemv_down_kernel<1, F> : bpl == 2 ? (const void*)gemv_down_kernel<2, F>
-         : bpl == 4 ? (const void*)gemv_down_kernel<4, F> : (const void*)gemv_down_kernel<8, F>;
 }
 
 cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
@@ -995,16 +1085,18 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
     if (T == 0) return cudaSuccess;
     const CtaGeo dgeo = make_cta_geo(I);
     const int P = T * k, feats = dgeo.RG * kR;
-    const size_t ring_smem = T == 1 ? down_ring_smem<1>(I, P) : T == 2 ? down_ring_smem<2>(I, P) : down_ring_smem<4>(I, P);
+    const bool nv = W->wfmt == MOE_W_NVFP4;
+    const size_t ring_bytes = nv ? ring_smem<true>(T, I, P) : ring_smem<false>(T, I, P);
     const bool aligned16 = ((uintptr_t)W->down_q % 16 == 0) && ((uintptr_t)W->down_s % 16 == 0);
     // two CTAs per SM: 2 x (ring_smem + 1 KB reserved) within the SM's 228 KB
     const int hunits = T <= 2 ? down_hunits<2>() : down_hunits<4>();
     if (T <= 4 && dgeo.bpt == 1 && d % feats == 0 && aligned16 && T * dgeo.nb * 4 <= hunits * kThr &&
-        ring_smem <= 113 * 1024) {
+        ring_bytes <= 113 * 1024) {
         // up to four tokens: CTA-split of K, weights through the copy-engine ring
         GemvArgs a = {};
         a.q0 = W->down_q;
         a.s0 = W->down_s;
+        a.gs0 = W->down_gs;
         a.act = h;
         a.perm_token = perm_token;
         a.offsets = offsets;
@@ -1019,10 +1111,8 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
         a.status = status;
         void* args[] = {&a};
         const dim3 grid(d / feats);
-        const void* f = T == 1 ? (y ? (const void*)gemv_down_ring_kernel<1, true> : (const void*)gemv_down_ring_kernel<1, false>)
-                      : T == 2 ? (y ? (const void*)gemv_down_ring_kernel<2, true> : (const void*)gemv_down_ring_kernel<2, false>)
-                               : (y ? (const void*)gemv_down_ring_kernel<4, true> : (const void*)gemv_down_ring_kernel<4, false>);
-        return launch_kernel(f, grid, dim3(kThr), ring_smem, st, pdl, args);
+        const void* f = nv ? ring_kernel<true>(T, y != nullptr) : ring_kernel<false>(T, y != nullptr);
+        return launch_kernel(f, grid, dim3(kThr), ring_bytes, st, pdl, args);
     }
     const int bpl = bpl_for(I);
     const int outs = kWarps * down_rows_per_warp(bpl);
@@ -1035,6 +1125,7 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
     GemvArgs a = {};
     a.q0 = W->down_q;
     a.s0 = W->down_s;
+    a.gs0 = W->down_gs;
     a.act = h;
     a.perm_token = perm_token;
     a.offsets = offsets;
@@ -1054,7 +1145,8 @@ cudaError_t launch_gemv_down(const uint16_t* h, const int32_t* perm_token, const
                         sizeof(int) * 3 * mr + sizeof(float) * mr + sizeof(int) * (E + 1);
     void* args[] = {&a};
     const dim3 grid(d / outs, (T + tch - 1) / tch);
-    const void* f = y ? down_kernel<true>(bpl) : down_kernel<false>(bpl);
+    const void* f = nv ? (y ? down_kernel<true, true>(bpl) : down_kernel<false, true>(bpl))
+                       : (y ? down_kernel<true, false>(bpl) : down_kernel<false, false>(bpl));
     return launch_kernel(f, grid, dim3(kThr), smem, st, pdl, args);
 }
 

@@ -14,34 +14,46 @@ from . import inputs as IN
 
 class DeviceLayer:
     """One synthetic layer of workload ``cfg`` on ``device``.  ``layer`` selects an independent
-    copy (different weight seed), used to rotate layers so that L2 cannot carry experts."""
+    copy (different weight seed), used to rotate layers so that L2 cannot carry experts.
+    ``wfmt``: "mxfp4" (E8M0 scale per 32 values) or "nvfp4" (E4M3 scale per 16 values and a
+    global scale per expert matrix; read by the bf16-activation path only)."""
 
     def __init__(self, cfg: IN.Config, device="cuda", layer: int = 0, mma_layouts: bool = True,
-                 chunk_bytes: int = 1 << 30):
+                 chunk_bytes: int = 1 << 30, wfmt: str = "mxfp4"):
+        assert wfmt in ("mxfp4", "nvfp4")
         self.cfg = cfg
+        self.wfmt = wfmt
+        nv = wfmt == "nvfp4"
         self.device = torch.device(device)
         self.seed = cfg.seed + 7919 * layer
         E, I, d = cfg.E, cfg.I, cfg.d
         u8 = dict(dtype=torch.uint8, device=self.device)
         self.q = {}
         self.s = {}
+        self.gs = {}
         self.s_mma = {}
         shapes = IN.expert_matrix_shapes(cfg)
         c = float(IN.weight_scale(cfg.weight_std))
         for tid, (rows, K) in shapes.items():
             q = torch.empty((E, rows, K // 2), **u8)
-            s = torch.empty((E, rows, K // 32), **u8)
+            s = torch.empty((E, rows, K // (16 if nv else 32)), **u8)
+            gs = torch.empty(E, dtype=torch.float32, device=self.device) if nv else None
             per = rows * K * 4
             n_chunk = max(1, min(E, chunk_bytes // per))
             buf = torch.empty((n_chunk, rows, K), dtype=torch.float32, device=self.device)
             for e0 in range(0, E, n_chunk):
                 n = min(n_chunk, E - e0)
                 B.moe_synth_weights(self.seed, tid, e0, n, rows, K, c, buf)
-                B.moe_mxfp4_pack(buf, n * rows, K, q[e0:e0 + n], s[e0:e0 + n])
+                if nv:
+                    B.moe_nvfp4_pack(buf, n, rows, K, q[e0:e0 + n], s[e0:e0 + n], gs[e0:e0 + n])
+                else:
+                    B.moe_mxfp4_pack(buf, n * rows, K, q[e0:e0 + n], s[e0:e0 + n])
             del buf
-            self.q[tid], self.s[tid] = q, s
+            self.q[tid], self.s[tid], self.gs[tid] = q, s, gs
         G, U, D = IN.TENSOR_GATE, IN.TENSOR_UP, IN.TENSOR_DOWN
         self.q_mma = {}
+        if nv:
+            mma_layouts = False
         if mma_layouts and d % 256 == 0 and I % 256 == 0:  # copies for the tensor-core (MXFP4) path
             for tid, (rows, K) in shapes.items():
                 self.q_mma[tid] = torch.empty(E * rows * K // 2, **u8)
@@ -55,12 +67,19 @@ class DeviceLayer:
         self.W_r_host, self.b_host = W_r, b
         self.W_r = torch.from_numpy(W_r).to(self.device)
         self.b = torch.from_numpy(b).to(self.device)
-        self.weights = B.expert_weights_struct(self.q[G], self.s[G], self.q[U], self.s[U], self.q[D], self.s[D],
-                                               self.q_mma.get(G), self.s_mma.get(G), self.q_mma.get(U),
-                                               self.s_mma.get(U), self.q_mma.get(D), self.s_mma.get(D))
+        if nv:
+            self.weights = B.nvfp4_expert_weights_struct(self.q[G], self.s[G], self.gs[G], self.q[U], self.s[U],
+                                                         self.gs[U], self.q[D], self.s[D], self.gs[D])
+        else:
+            self.weights = B.expert_weights_struct(self.q[G], self.s[G], self.q[U], self.s[U], self.q[D], self.s[D],
+                                                   self.q_mma.get(G), self.s_mma.get(G), self.q_mma.get(U),
+                                                   self.s_mma.get(U), self.q_mma.get(D), self.s_mma.get(D))
 
     def weight_bytes_per_expert(self) -> int:
+        """Bytes of one expert's three matrices as the expert kernels read them."""
         cfg = self.cfg
+        if self.wfmt == "nvfp4":
+            return 3 * cfg.I * cfg.d // 2 + 3 * cfg.I * cfg.d // 16 + 3 * 4
         return 3 * cfg.I * cfg.d // 2 + 3 * cfg.I * cfg.d // 32
 
 

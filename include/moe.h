@@ -27,7 +27,8 @@
  *   - Inputs are assumed finite.
  *   - Shape rules (MOE_ERR_UNSUPPORTED_SHAPE otherwise): 1 <= k <= min(E, 32); E <= 1024;
  *     T >= 0; MOE_ACT_BF16: d % 128 == 0 and I % 32 == 0; MOE_ACT_MXFP4: d % 256 == 0 and
- *     I % 256 == 0 (whole 256-value MMA tiles along both contractions).
+ *     I % 256 == 0 (whole 256-value MMA tiles along both contractions).  NVFP4 expert weights
+ *     (moe_weight_fmt) are read by the MOE_ACT_BF16 path only.
  *
  * MXFP4 tensor layout ("canonical"): a [rows][K] matrix is stored as codes q[rows][K/2]
  * (element 2i in the low nibble of byte i, element 2i+1 in the high nibble; bit 3 of a code
@@ -63,6 +64,15 @@ typedef enum moe_status {
  *                    packer); tcgen05 block-scaled MMA (kind::mxf4) grouped GEMMs. */
 typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1 } moe_act_fmt;
 
+/* Format of the expert weight matrices (moe_expert_weights.wfmt).
+ *   MOE_W_MXFP4 -- the canonical MXFP4 layout above.
+ *   MOE_W_NVFP4 -- 4-bit values of which 16 share a small scale, about 4.5 bits each (Muse
+ *                  Spark Open explainer, section 11): the same E2M1 codes q[rows][K/2], one
+ *                  E4M3 scale (OCP OFP8: bias 7, largest finite 448) per 16 consecutive
+ *                  elements of a row, s[rows][K/16], and one fp32 global scale per matrix;
+ *                  value = E2M1 * E4M3 * global.  Read by the MOE_ACT_BF16 path only. */
+typedef enum moe_weight_fmt { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1 } moe_weight_fmt;
+
 /* Expert weights of one layer (all device pointers, canonical MXFP4 layout):
  *   gate_q/up_q [E][I][d/2], gate_s/up_s [E][I][d/32]   (gate and up: I rows of d)
  *   down_q      [E][d][I/2], down_s      [E][d][I/32]   (down: d rows of I)
@@ -71,7 +81,11 @@ typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1 } moe_act_fmt;
  *   gate_s_mma, up_s_mma   moe_mxfp4_scales_to_mma(gate_s or up_s, E*I, d)
  *   down_q_mma             moe_mxfp4_codes_to_mma(down_q, E*d, I)
  *   down_s_mma             moe_mxfp4_scales_to_mma(down_s, E*d, I)
- * The BF16 path reads only the canonical tensors (the six copies may be NULL). */
+ * The BF16 path reads only the canonical tensors (the six copies may be NULL).
+ * With wfmt = MOE_W_NVFP4 the scale tensors are E4M3 [E][I][d/16] (gate, up) and [E][d][I/16]
+ * (down), 2-byte aligned, and gate_gs / up_gs / down_gs hold the global scale of each expert's
+ * matrix ([E] fp32 each); the tensor-core copies are not used.  A zero-initialised struct is
+ * MXFP4 (MOE_ERR_INVALID_ARG for any other wfmt). */
 typedef struct moe_expert_weights {
     const uint8_t* gate_q;
     const uint8_t* gate_s;
@@ -85,6 +99,10 @@ typedef struct moe_expert_weights {
     const uint8_t* up_s_mma;
     const uint8_t* down_q_mma;
     const uint8_t* down_s_mma;
+    int32_t wfmt;         /* moe_weight_fmt */
+    const float* gate_gs; /* MOE_W_NVFP4 only: [E] */
+    const float* up_gs;
+    const float* down_gs;
 } moe_expert_weights;
 
 /* ---------------------------------------------------------------- library */
@@ -113,6 +131,27 @@ moe_status moe_mxfp4_pack(const float* w, int64_t rows, int64_t K, uint8_t* q, u
 /* Dequantise q, s back to fp32 w[rows][K] (exact). */
 moe_status moe_mxfp4_unpack(const uint8_t* q, const uint8_t* s, int64_t rows, int64_t K, float* w,
                             moe_stream_t stream);
+
+/* ---------------------------------------------------------------- NVFP4 helpers
+ * Quantisation rule of the NVFP4 weight format, every step in fp32 with round-to-nearest-even:
+ *   global = (largest |w| of the matrix) / 2688 (= 6 * 448), or 1 when that is 0;
+ *   for each 16-element block: t = (largest |v| of the block / global) / 6; scale byte = t
+ *   rounded to the nearest E4M3 value (ties to even, saturating at 448); D = E4M3 value *
+ *   global; each element is |v| / D rounded to the nearest E2M1 magnitude (ties to the even
+ *   code, saturating at 6), with the sign of v unless it rounds to 0 (stored as +0); D = 0
+ *   gives zero codes. */
+
+/* Pack n_mats fp32 matrices w[n_mats][rows][K] into q[n_mats*rows][K/2], s[n_mats*rows][K/16]
+ * and the global scales gs[n_mats] (gs is also the scratch of the per-matrix maximum while the
+ * call runs).  K % 32 == 0, rows >= 0, 0 <= n_mats <= 65535; w and q 16-byte aligned, s 2-byte
+ * aligned, gs 4-byte aligned. */
+moe_status moe_nvfp4_pack(const float* w, int64_t n_mats, int64_t rows, int64_t K, uint8_t* q, uint8_t* s,
+                          float* gs, moe_stream_t stream);
+
+/* Dequantise to fp32: w = (E2M1 value * E4M3 value) * gs[matrix], the exact product of the first
+ * two rounded once.  Same shapes and alignment as moe_nvfp4_pack. */
+moe_status moe_nvfp4_unpack(const uint8_t* q, const uint8_t* s, const float* gs, int64_t n_mats, int64_t rows,
+                            int64_t K, float* w, moe_stream_t stream);
 
 /* Tensor-core layouts of a [rows][K] MXFP4 matrix (rows % 128 == 0, K % 256 == 0), read by the
  * block-scaled MMA path with one contiguous copy per operand tile:

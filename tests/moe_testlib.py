@@ -35,6 +35,25 @@ def oracle_expert_weights(cfg: IN.Config, seed: int):
     return get
 
 
+@functools.lru_cache(maxsize=512)
+def oracle_matrix_nv(seed: int, tensor_id: int, expert: int, rows: int, K: int, std: float):
+    """One expert matrix packed by the oracle's NVFP4 packer: (q, s, global scale)."""
+    w = IN.synth_weights(seed, tensor_id, expert, rows, K, std)
+    return O.nvfp4_pack(w)
+
+
+def oracle_expert_weights_nv(cfg: IN.Config, seed: int):
+    shapes = IN.expert_matrix_shapes(cfg)
+
+    def get(e):
+        out = {}
+        for name, tid in (("gate", IN.TENSOR_GATE), ("up", IN.TENSOR_UP), ("down", IN.TENSOR_DOWN)):
+            rows, K = shapes[tid]
+            out[name] = oracle_matrix_nv(seed, tid, e, rows, K, cfg.weight_std)
+        return out
+    return get
+
+
 def check_outputs(y_gpu: np.ndarray, y_ref: np.ndarray, what: str = "y"):
     y_gpu = np.asarray(y_gpu, dtype=np.float64)
     y_ref = np.asarray(y_ref, dtype=np.float64)

@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 6
+    assert B.moe_abi_version() == 7
     assert B.status_string(0) == "MOE_OK"
     assert B.status_string(5) == "MOE_ERR_TIMEOUT"
 
@@ -90,3 +90,25 @@ def test_dense_linear_shapes_and_arguments_are_checked_on_the_host(lib):
     assert lib.moe_dense_linear(256, 4, 256, 256, W, B.MOE_ACT_BF16, 256, 256, 1 << 20, None) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_dense_linear(256, 4, 200, 256, W, B.MOE_ACT_BF16, 256, 256, 1 << 20, None) == \
         B.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+def test_nvfp4_arguments_are_checked_on_the_host(lib):
+    # pack / unpack: K % 32, at most 65535 matrices, pointers and alignment; n_mats == 0 is a no-op
+    assert lib.moe_nvfp4_pack(256, 1, 4, 48, 256, 256, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_nvfp4_pack(256, 70000, 4, 64, 256, 256, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_nvfp4_pack(256, 1, 4, 64, 256, 256, None, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_nvfp4_pack(256, 1, 4, 64, 256, 257, 256, None) == B.MOE_ERR_INVALID_ARG  # s 2-byte aligned
+    assert lib.moe_nvfp4_pack(None, 0, 4, 64, None, None, None, None) == B.MOE_OK
+    assert lib.moe_nvfp4_unpack(256, 256, 256, 1, 4, 40, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    # NVFP4 expert weights: the bf16-activation path only, global scales required, known formats
+    W = B.nvfp4_expert_weights_struct(256, 256, 256, 256, 256, 256, 256, 256, 256)
+    args = (256, 256, None, 4, 256, 8, 2, 512)
+    tail = (256, None, None, 256, 1 << 30, None)
+    assert lib.moe_layer_forward(*args, W, B.MOE_ACT_MXFP4, *tail) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    W.down_gs = None
+    assert lib.moe_layer_forward(*args, W, B.MOE_ACT_BF16, *tail) == B.MOE_ERR_INVALID_ARG
+    W.down_gs = 256
+    W.up_s = 257
+    assert lib.moe_layer_forward(*args, W, B.MOE_ACT_BF16, *tail) == B.MOE_ERR_INVALID_ARG
+    W.wfmt = 7
+    assert lib.moe_layer_forward(*args, W, B.MOE_ACT_BF16, *tail) == B.MOE_ERR_INVALID_ARG

@@ -110,3 +110,22 @@ def test_variant_options_name_the_workload_and_count_launches():
     # prefill: 10 layer kernels; + 2 x (plan, quantise, gather, GEMM)
     assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 10
     assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 18
+
+
+def test_nvfp4_weight_option_changes_the_byte_model_and_the_names():
+    """--weights nvfp4: 4.5 bits per weight (one E4M3 byte per 16 values) plus a 4-byte global
+    scale per matrix; the workload and dtype name the format."""
+    import argparse
+
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    cfg = IN.CONFIGS["decode"]
+    d, I = cfg.d, cfg.I
+    assert bench.expert_read_bytes(d, I) == bench.expert_bytes(d, I) == 3 * (I * d // 2 + I * d // 32)
+    assert bench.expert_read_bytes(d, I, "nvfp4") == 3 * (I * d // 2 + I * d // 16 + 4)
+    assert bench.up_bytes_per_expert(d, I, "nvfp4") == 2 * (I * d // 2 + I * d // 16 + 4)
+    mx = bench.layer_algorithmic_bytes(d, I, cfg.E, 1, 8)
+    nv = bench.layer_algorithmic_bytes(d, I, cfg.E, 1, 8, "nvfp4")
+    assert nv - mx == 8 * 3 * (I * d // 32 + 4)
+    args = argparse.Namespace(expert_norm=False, latent=0, weights="nvfp4")
+    assert "NVFP4" in bench.workload_name(args, cfg)
+    assert bench.dtype_name(0, "nvfp4").startswith("nvfp4 weights x bf16")
