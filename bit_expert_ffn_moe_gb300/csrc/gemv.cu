@@ -81,11 +81,19 @@ __device__ __forceinline__ float block_dot_nv(const uint4& codes, const uint32_t
 }
 
 // Scale word of one 32-element block (idx = row * K/32 + block): MXFP4 one E8M0 byte, NVFP4 the
-// block's two E4M3 bytes.
+// block's two E4M3 bytes.  The NVFP4 pair is read like the weight codes (a streaming load issued
+// where it is written, so that a batch's scales stay in flight with its codes).
 template <bool NV>
 __device__ __forceinline__ uint32_t load_block_scale(const uint8_t* s, size_t idx) {
-    if constexpr (NV) return __ldg(reinterpret_cast<const unsigned short*>(s) + idx);
-    else return __ldg(s + idx);
+    if constexpr (NV) {
+        uint32_t v;
+        asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];"
+                     : "=r"(v)
+                     : "l"(reinterpret_cast<const unsigned short*>(s) + idx));
+        return v;
+    } else {
+        return __ldg(s + idx);
+    }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -193,6 +201,7 @@ gemv_up_kernel(const GemvArgs a) {
     const int e = a.plan.active[slot];
     const size_t row_bytes = (size_t)a.K / 2;
     const int i0 = blockIdx.x * a.outs + warp * kUpOutsPerWarp;
+    const float gsg = NV ? __ldg(a.gs0 + e) : 1.f, gsu = NV ? __ldg(a.gs1 + e) : 1.f;  // NVFP4 global scales
 
     auto load_out = [&](int i, uint4 (&wg)[BPL], uint4 (&wu)[BPL], uint32_t (&sg)[BPL], uint32_t (&su)[BPL]) {
         const size_t grow = (size_t)e * a.M_exp + i;
@@ -253,8 +262,8 @@ gemv_up_kernel(const GemvArgs a) {
                 if (q < nq) {
                     float gs = warp_sum(g[q]) * inv[q], us = warp_sum(u[q]) * inv[q];
                     if constexpr (NV) {
-                        gs *= __ldg(a.gs0 + e);
-                        us *= __ldg(a.gs1 + e);
+                        gs *= gsg;
+                        us *= gsu;
                     }
                     if (lane == q) {
                         const float hv = gs / (1.f + expf(-gs)) * us;  // SiLU(g) * u
@@ -403,8 +412,10 @@ __device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int 
 // Grid (M_exp / outs, slots): slot u is the u-th active expert.  A batch gives each row group
 // kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens; an
 // expert with more rows takes them Q at a time (its weights are read again per pass).
+// NVFP4 with one block per thread and two token rows: bounded to two CTAs per SM (without the
+// bound its registers allow one).
 template <int BPT, int Q, bool NV>
-__global__ void __launch_bounds__(kThr)
+__global__ void __launch_bounds__(kThr, (NV && BPT == 1 && Q == 2) ? 2 : 0)
 gemv_up_cta_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int kOut = kR / 2;
@@ -427,6 +438,7 @@ gemv_up_cta_kernel(const GemvArgs a) {
     if (slot >= a.plan.scalars[0]) return;
     const int e = a.plan.active[slot];
     const size_t row_bytes = (size_t)a.K / 2;
+    const float gsg = NV ? __ldg(a.gs0 + e) : 1.f, gsu = NV ? __ldg(a.gs1 + e) : 1.f;  // NVFP4 global scales
     const int outs_per_group = a.outs / geo.RG;
     const int nbatch = outs_per_group / kOut;
     const int i_base = blockIdx.x * a.outs + grp * outs_per_group;
@@ -481,8 +493,8 @@ gemv_up_cta_kernel(const GemvArgs a) {
                     g *= inv[qq];
                     u *= inv[qq];
                     if constexpr (NV) {
-                        g *= __ldg(a.gs0 + e);
-                        u *= __ldg(a.gs1 + e);
+                        g *= gsg;
+                        u *= gsu;
                     }
                     const float hv = g / (1.f + expf(-g)) * u;  // SiLU(g) * u
                     const int i = i_base + bi * kOut + j;
