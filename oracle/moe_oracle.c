@@ -60,6 +60,14 @@
  *       / 6, scale = nearest E4M3 to t (ties even, saturating at 448); D = scale * global;
  *       each code = nearest E2M1 to |v| / D (ties even, saturating at 6), signed unless 0;
  *       D = 0 gives zero codes.
+ *   R11 MXFP8 activations (optional, ACT_MXFP8; [SPARK] s.2 names the baseline configuration
+ *       "4-bit weights, 8-bit activations" without the 8-bit format): the MX format of the same
+ *       family as the MXFP4 path [OCP-MX], E4M3 elements [OFP8] with one E8M0 scale per 32:
+ *       X = floor(log2(amax)) - 8 (8 = exponent of E4M3's largest normal, 448 = 1.75 * 2^8),
+ *       clamped to [-127, 127]; each element is |v| / 2^X rounded to the nearest E4M3 value
+ *       (ties even, saturating at 448), signed unless its magnitude code is 0; an all-zero block
+ *       gets scale byte 0.  x rows and the fp32 h rows are quantised this way (as R7 does with
+ *       MXFP4); the weights stay MXFP4 (or NVFP4).
  * Accumulations inside the expert matrices are fp64 (closer to exact than the kernels).
  */
 #include <math.h>
@@ -70,6 +78,7 @@
 #define ACT_BF16 0
 #define ACT_MXFP4 1
 #define ACT_EXACT 2
+#define ACT_MXFP8 3
 
 /* ------------------------------------------------------------------ scalar formats */
 
@@ -299,6 +308,33 @@ int oracle_nvfp4_unpack(const uint8_t* q, const uint8_t* s, const float* gs, int
     return bad ? -1 : 0;
 }
 
+/* ------------------------------------------------------------------ MXFP8 blocks  (R11) */
+
+/* Quantise one block of n values to E4M3 codes (sign in bit 7) with one shared E8M0 scale. */
+void oracle_mx8_block_quantize(const double* v, int n, uint8_t* codes, uint8_t* scale_byte) {
+    double amax = 0.0;
+    for (int i = 0; i < n; ++i) {
+        double a = fabs(v[i]);
+        if (a > amax) amax = a;
+    }
+    if (amax == 0.0) {
+        *scale_byte = 0;
+        for (int i = 0; i < n; ++i) codes[i] = 0;
+        return;
+    }
+    int ex;
+    (void)frexp(amax, &ex); /* floor(log2(amax)) = ex - 1 */
+    int X = (ex - 1) - 8;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+    *scale_byte = (uint8_t)(X + 127);
+    for (int i = 0; i < n; ++i) {
+        int c = oracle_e4m3_encode_nonneg(ldexp(fabs(v[i]), -X));
+        if (c != 0 && v[i] < 0.0) c |= 0x80;
+        codes[i] = (uint8_t)c;
+    }
+}
+
 /* ------------------------------------------------------------------ router  [MUSE] s.8 */
 
 /* logits[t][e] = b[e] + sum_i x[t][i] * W_r[e][i] with the R1 reduction order.
@@ -402,14 +438,26 @@ int oracle_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int
 
 /* The activation operand of one token row as the GEMMs see it (fp32 values).
  * ACT_MXFP4: quantise each 32-block (R6) and return the dequantised values, plus the codes
- * and scales if q / s are non-NULL (q: [d/2] packed like weights, s: [d/32]). */
+ * and scales if q / s are non-NULL (q: [d/2] packed like weights, s: [d/32]).
+ * ACT_MXFP8: the same with the R11 rule (q: [d] E4M3 code bytes, s: [d/32]). */
 void oracle_activation_row(const uint16_t* x_row, int d, int act_fmt, float* out, uint8_t* q, uint8_t* s) {
+    double v[32];
+    uint8_t codes[32], sb;
+    if (act_fmt == ACT_MXFP8) { /* R11: one E4M3 code byte per element */
+        for (int b = 0; b < d / 32; ++b) {
+            for (int i = 0; i < 32; ++i) v[i] = (double)bf16_bits_to_float(x_row[b * 32 + i]);
+            oracle_mx8_block_quantize(v, 32, codes, &sb);
+            for (int i = 0; i < 32; ++i) out[b * 32 + i] = (float)(oracle_e4m3_value(codes[i]) * oracle_e8m0_value(sb));
+            if (q)
+                for (int i = 0; i < 32; ++i) q[b * 32 + i] = codes[i];
+            if (s) s[b] = sb;
+        }
+        return;
+    }
     if (act_fmt != ACT_MXFP4) {
         for (int i = 0; i < d; ++i) out[i] = bf16_bits_to_float(x_row[i]);
         return;
     }
-    double v[32];
-    uint8_t codes[32], sb;
     for (int b = 0; b < d / 32; ++b) {
         for (int i = 0; i < 32; ++i) v[i] = (double)bf16_bits_to_float(x_row[b * 32 + i]);
         oracle_mx_block_quantize(v, 32, codes, &sb);
@@ -460,7 +508,8 @@ static void wmat_row(const wmat* W, int64_t row, int K, double* out) {
  *   a      [n][d]  activation operand values (from oracle_activation_row)
  *   W_g, W_u [I][d];  W_d [d][I]  (MXFP4 (q, s), or NVFP4 (q, s, global scale), R10)
  *   h_out  [n][I]  the down-GEMM operand after the R7 rounding (may be NULL)
- *   hq/hs  [n][I/2], [n][I/32]  MXFP4 codes/scales of h when act_fmt == ACT_MXFP4 (may be NULL)
+ *   hq/hs  [n][I/2], [n][I/32]  MXFP4 codes/scales of h when act_fmt == ACT_MXFP4; [n][I] E4M3
+ *          codes and [n][I/32] scales when act_fmt == ACT_MXFP8 (may be NULL)
  *   y_out  [n][d]  expert output rounded to fp32 then bf16 (R7)
  * g and u accumulate in fp64 and are rounded to fp32, as the kernels hold them in fp32. */
 static void expert_ffn(const float* a, int n, int d, int I, const wmat* Wg, const wmat* Wu, const wmat* Wd,
@@ -501,6 +550,17 @@ static void expert_ffn(const float* a, int n, int d, int I, const wmat* Wg, cons
                 if (hq)
                     for (int i = 0; i < 16; ++i)
                         hq[(int64_t)r * (I / 2) + b * 16 + i] = (uint8_t)(codes[2 * i] | (codes[2 * i + 1] << 4));
+                if (hs) hs[(int64_t)r * (I / 32) + b] = sb;
+            }
+        } else if (act_fmt == ACT_MXFP8) { /* R11 */
+            double v[32];
+            uint8_t codes[32], sb;
+            for (int b = 0; b < I / 32; ++b) {
+                for (int i = 0; i < 32; ++i) v[i] = (double)(float)hr[b * 32 + i];
+                oracle_mx8_block_quantize(v, 32, codes, &sb);
+                for (int i = 0; i < 32; ++i) hr[b * 32 + i] = oracle_e4m3_value(codes[i]) * oracle_e8m0_value(sb);
+                if (hq)
+                    for (int i = 0; i < 32; ++i) hq[(int64_t)r * I + b * 32 + i] = codes[i];
                 if (hs) hs[(int64_t)r * (I / 32) + b] = sb;
             }
         }

@@ -38,6 +38,7 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_%s.so" % platform.machine())
 ACT_BF16 = 0
 ACT_MXFP4 = 1
 ACT_EXACT = 2
+ACT_MXFP8 = 3   # reading R11: E4M3 elements, one E8M0 scale per 32 (x and h)
 
 _lib = None
 
@@ -79,6 +80,7 @@ def _load():
         "oracle_expert_norm": (None, [P, i64, i32, ctypes.c_double, P]),
         "oracle_dense_linear": (None, [P, i32, i32, i32, P, P, P]),
         "oracle_e4m3_value": (ctypes.c_double, [i32]),
+        "oracle_mx8_block_quantize": (None, [P, i32, P, P]),
         "oracle_e4m3_encode_nonneg": (i32, [ctypes.c_double]),
         "oracle_nvfp4_global_scale": (ctypes.c_float, [ctypes.c_float]),
         "oracle_nv_block_quantize": (None, [P, i32, ctypes.c_float, P, P]),
@@ -159,6 +161,15 @@ def mxfp4_unpack(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     if rc != 0:
         raise ValueError("NaN scale byte (0xFF) in MXFP4 tensor")
     return w
+
+
+def mx8_block_quantize(v: np.ndarray):
+    """MXFP8 (reading R11) of one block: (E4M3 code bytes uint8[n], E8M0 scale byte)."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    codes = np.zeros(v.shape[0], dtype=np.uint8)
+    sb = np.zeros(1, dtype=np.uint8)
+    _load().oracle_mx8_block_quantize(_ptr(v), v.shape[0], _ptr(codes), _ptr(sb))
+    return codes, int(sb[0])
 
 
 # ------------------------------------------------------------------ NVFP4 tensors (reading R10)
@@ -259,11 +270,11 @@ def permute(ids: np.ndarray, E: int):
 
 def activation_rows(x_bits: np.ndarray, act_fmt: int, want_codes: bool = False):
     """Activation operand values of token rows (fp32 [n][d]); with want_codes also the
-    MXFP4 codes/scales (only meaningful for ACT_MXFP4)."""
+    codes/scales (ACT_MXFP4: packed nibbles [n][d/2]; ACT_MXFP8: E4M3 bytes [n][d])."""
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     n, d = x_bits.shape
     out = np.empty((n, d), dtype=np.float32)
-    q = np.zeros((n, d // 2), dtype=np.uint8) if want_codes else None
+    q = np.zeros((n, d if act_fmt == ACT_MXFP8 else d // 2), dtype=np.uint8) if want_codes else None
     s = np.zeros((n, d // 32), dtype=np.uint8) if want_codes else None
     lib = _load()
     for r in range(n):
@@ -286,7 +297,7 @@ def expert_ffn(a: np.ndarray, wg, wu, wd, act_fmt: int, want_h: bool = False):
     assert len(wu) == len(wg) and len(wd) == len(wg), "one weight format per expert"
     y = np.empty((n, d), dtype=np.float32)
     h = np.empty((n, I), dtype=np.float32) if want_h else None
-    hq = np.zeros((n, I // 2), dtype=np.uint8) if want_h else None
+    hq = np.zeros((n, I if act_fmt == ACT_MXFP8 else I // 2), dtype=np.uint8) if want_h else None
     hs = np.zeros((n, I // 32), dtype=np.uint8) if want_h else None
     ws = [np.ascontiguousarray(m[i], dtype=np.uint8) for m in (wg, wu, wd) for i in (0, 1)]
     if nv:
