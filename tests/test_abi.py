@@ -112,3 +112,56 @@ def test_nvfp4_arguments_are_checked_on_the_host(lib):
     assert lib.moe_layer_forward(*args, W, B.MOE_ACT_BF16, *tail) == B.MOE_ERR_INVALID_ARG
     W.wfmt = 7
     assert lib.moe_layer_forward(*args, W, B.MOE_ACT_BF16, *tail) == B.MOE_ERR_INVALID_ARG
+
+
+def _c_struct_fields(name):
+    """(field, C type) pairs of `typedef struct ... { ... } name;` in include/moe.h."""
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    m = re.search(r"typedef struct\s*\w*\s*\{([^}]*)\}\s*" + name + r"\s*;", src)
+    assert m, name
+    out = []
+    for decl in m.group(1).split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        typ, _, rest = decl.rpartition(" ")
+        for field in rest.split(","):
+            out.append((field.strip().lstrip("*"), typ + ("*" if field.strip().startswith("*") else "")))
+    return out
+
+
+@pytest.mark.parametrize("name", ["moe_expert_weights", "moe_mxfp4_matrix"])
+def test_ctypes_structs_mirror_the_header(name):
+    import ctypes
+    fields = _c_struct_fields(name)
+    cls = getattr(B, name)
+    assert [f for f, _ in fields] == [f for f, _ in cls._fields_]
+    for (f, ctype), (_, pytype) in zip(fields, cls._fields_):
+        if ctype.endswith("*"):
+            assert pytype is ctypes.c_void_p, f
+        else:
+            assert ctype == "int32_t" and pytype is ctypes.c_int32, f
+    # the C layout of these fields on an LP64 ABI: pointers 8-byte aligned
+    assert ctypes.sizeof(cls) % 8 == 0
+
+
+@pytest.mark.parametrize("name", ["moe_expert_weights", "moe_mxfp4_matrix"])
+def test_ctypes_struct_offsets_equal_the_c_compilers(name, tmp_path):
+    import ctypes
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    cls = getattr(B, name)
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe.h"', "int main(void) {",
+             '  printf("%%zu\\n", sizeof(%s));' % name]
+    lines += ['  printf("%%zu\\n", offsetof(%s, %s));' % (name, f) for f, _ in cls._fields_]
+    lines += ["  return 0;", "}"]
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(c), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()]
+    assert got[0] == ctypes.sizeof(cls)
+    assert got[1:] == [getattr(cls, f).offset for f, _ in cls._fields_]
