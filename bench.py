@@ -335,6 +335,17 @@ def run_gpu(args, cfg, rank, world, local):
     # ---- end to end through the C ABI with host buffers
     e2e = end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call)
 
+    # ---- the oracle sample's rows through the same layer copy (checked in main)
+    parity_y = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        parity_y = []
+        with torch.cuda.stream(stream):
+            for xb, rows in parity_inputs(cfg, args.cpu_sample_tokens):
+                x = torch.from_numpy(xb.view(np.int16).copy()).to(dev).view(torch.bfloat16)
+                call(sample_layer_index(args), x, y, None, None, ws, stream.cuda_stream)
+                yh = y.float().cpu().numpy()
+                parity_y.append(yh if rows is None else yh[rows])
+
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
@@ -354,6 +365,7 @@ def run_gpu(args, cfg, rank, world, local):
         "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None, lat is not None) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
+        "_parity_y": parity_y,
     }
     return out
 
@@ -629,10 +641,68 @@ def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call):
 
 # ------------------------------------------------------------------ CPU oracle arm
 
-def oracle_sample(args, cfg, n_tokens):
+# Output tolerance of the layer (the parity tests' bar): relative Frobenius error and max abs
+# error over the RMS of the oracle output, over the checked tokens.
+PARITY_REL_FRO, PARITY_MAX_ABS_RMS = 5e-3, 3e-2
+
+
+def sample_layer_index(args):
+    """The layer copy the oracle sample and the bench's parity gate use."""
+    return 1 if getattr(args, "layers", 2) > 1 else 0
+
+
+def parity_inputs(cfg, n_tokens):
+    """The inputs of the oracle sample: (bf16 bits x [T][d], checked rows or None for all).
+    Decode sizes: n_tokens whole layer calls; prefill sizes: one call, n_tokens spread rows."""
+    import numpy as np
+
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    if cfg.T <= 8:
+        return [(IN.make_x(cfg, call=c), None) for c in range(n_tokens)]
+    return [(IN.make_x(cfg, call=0), np.arange(0, cfg.T, max(1, cfg.T // n_tokens))[:n_tokens])]
+
+
+def parity_gate(gpu_ys, oracle_ys):
+    """Compare the GPU's outputs of the sampled tokens with the oracle's; refuse to record a
+    timing whose output is wrong."""
+    import numpy as np
+    g = np.concatenate([np.asarray(y, dtype=np.float64).reshape(-1, np.shape(y)[-1]) for y in gpu_ys])
+    o = np.concatenate([np.asarray(y, dtype=np.float64).reshape(-1, np.shape(y)[-1]) for y in oracle_ys])
+    if g.shape != o.shape:
+        raise RuntimeError("refusing to record: parity sample shapes differ %s vs %s" % (g.shape, o.shape))
+    ref = np.linalg.norm(o)
+    rms = np.sqrt(np.mean(o ** 2))
+    rel = float(np.linalg.norm(g - o) / ref) if ref > 0 else float("inf")
+    mx = float(np.max(np.abs(g - o)) / rms) if rms > 0 else float("inf")
+    ok = bool(np.all(np.isfinite(g)) and rel <= PARITY_REL_FRO and mx <= PARITY_MAX_ABS_RMS)
+    out = {"rows_checked": int(g.shape[0]), "rel_fro": rel, "max_abs_over_rms": mx,
+           "tolerance": {"rel_fro": PARITY_REL_FRO, "max_abs_over_rms": PARITY_MAX_ABS_RMS}, "ok": ok}
+    if not ok:
+        raise RuntimeError("refusing to record: output differs from the oracle: %s" % json.dumps(out))
+    return out
+
+
+def oracle_sample(args, cfg, n_tokens, threads=None):
     """Time the CPU oracle (as it stands) on a bounded sample of the workload: routing,
     dequantisation of the touched experts, expert GEMVs and the weighted sum (with --latent also
-    the two projections of the sampled tokens).  Weight generation is untimed."""
+    the two projections of the sampled tokens).  Weight generation is untimed.  threads: OpenMP
+    threads for this sample (default: all host cores).  The result's "ys" holds the outputs of
+    the rows that parity_inputs() names."""
+    import numpy as np
+
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    from oracle import oracle as O
+
+    O.set_threads(threads or len(os.sched_getaffinity(0)))
+    try:
+        res = _oracle_sample(args, cfg, n_tokens)
+        res["cores"] = O.max_threads()
+    finally:
+        O.set_threads(len(os.sched_getaffinity(0)))
+    return res
+
+
+def _oracle_sample(args, cfg, n_tokens):
     import numpy as np
 
     from bit_expert_ffn_moe_gb300 import inputs as IN
@@ -640,10 +710,12 @@ def oracle_sample(args, cfg, n_tokens):
 
     threads = len(os.sched_getaffinity(0))
     cm = moe_cfg(args, cfg)
-    layer_seed = cfg.seed + 7919 * 1
+    li = sample_layer_index(args)
+    layer_seed = cfg.seed + 7919 * li
     W_r, b = IN.make_router(cm)
-    rng = np.random.default_rng([cm.seed, 77, 1])
-    W_r = (rng.standard_normal(W_r.shape) / np.sqrt(cm.d)).astype(np.float32)
+    if li != 0:  # the router of that layer copy
+        rng = np.random.default_rng([cm.seed, 77, li])
+        W_r = (rng.standard_normal(W_r.shape) / np.sqrt(cm.d)).astype(np.float32)
     shapes = IN.expert_matrix_shapes(cm)
     cache = {}
 
@@ -668,51 +740,47 @@ def oracle_sample(args, cfg, n_tokens):
             yl = O.moe_layer(xl, W_r, b, cfg.k, weights, act, expert_norm_eps=eps)["y"]
             return O.dense_linear(IN.to_bf16_bits(yl), wout, act)
 
-        xs = [IN.make_x(cfg, call=c) for c in range(n_tokens)] if cfg.T <= 8 else \
-            [IN.make_x(cfg, call=0)[np.arange(0, cfg.T, max(1, cfg.T // n_tokens))[:n_tokens]]]
+        xs = [xb if rows is None else xb[rows] for xb, rows in parity_inputs(cfg, n_tokens)]
         for xb in xs:  # pre-generate the touched experts (untimed: input generation)
             xl = IN.to_bf16_bits(O.dense_linear(xb, win, act))
             for e in np.unique(O.topk_softmax(O.router_logits(xl, W_r, b), cfg.k)[0]):
                 weights(int(e))
         t0 = time.perf_counter()
-        for xb in xs:
-            full(xb)
+        ys = [full(xb) for xb in xs]
         dt = time.perf_counter() - t0
         rows = sum(xb.shape[0] for xb in xs)
         return dict(value=round(rows / dt, 3), unit=UNIT, cores=threads, kind="oracle",
                     sample="%d token rows through narrow -> layer (routing of those rows) -> widen, fp64 oracle, "
-                           "weights pre-generated" % rows, seconds=round(dt, 2))
+                           "weights pre-generated" % rows, seconds=round(dt, 2), ys=ys)
     if cfg.T <= 8:
         # decode sizes: whole layer calls
-        xs = [IN.make_x(cfg, call=c) for c in range(n_tokens)]
+        xs = [xb for xb, _ in parity_inputs(cfg, n_tokens)]
         for xb in xs:  # pre-generate the experts the sample touches (untimed: input generation)
             ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
             for e in np.unique(ids):
                 weights(int(e))
         t0 = time.perf_counter()
-        for xb in xs:
-            O.moe_layer(xb, W_r, b, cfg.k, weights, act, expert_norm_eps=eps)
+        ys = [O.moe_layer(xb, W_r, b, cfg.k, weights, act, expert_norm_eps=eps)["y"] for xb in xs]
         dt = time.perf_counter() - t0
         return dict(value=round(cfg.T * n_tokens / dt, 3), unit=UNIT, cores=threads, kind="oracle",
                     sample="%d layer calls of T=%d (full routing, all %d touched experts per call, fp64 oracle), "
-                           "weights pre-generated" % (n_tokens, cfg.T, cfg.k), seconds=round(dt, 2))
+                           "weights pre-generated" % (n_tokens, cfg.T, cfg.k), seconds=round(dt, 2), ys=ys)
     # prefill sizes: routing of the whole chunk, expert work for a token sample; per-token cost =
     # routing time / T + expert time / sample size
-    xb = IN.make_x(cfg, call=0)
-    tokens = np.arange(0, cfg.T, max(1, cfg.T // n_tokens))[:n_tokens]
+    (xb, tokens), = parity_inputs(cfg, n_tokens)
     t0 = time.perf_counter()
     ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
     t_route = time.perf_counter() - t0
     for e in np.unique(ids[tokens]):
         weights(int(e))
     t0 = time.perf_counter()
-    O.moe_layer(xb[tokens], W_r, b, cfg.k, weights, act, expert_norm_eps=eps)
+    y_tok = O.moe_layer(xb[tokens], W_r, b, cfg.k, weights, act, expert_norm_eps=eps)["y"]
     t_exp = time.perf_counter() - t0
     per_tok = t_route / cfg.T + t_exp / len(tokens)
     return dict(value=round(1.0 / per_tok, 3), unit=UNIT, cores=threads, kind="oracle",
                 sample="routing of all %d tokens (%.2f s) + expert FFNs and sum for %d sampled tokens (%.2f s), "
                        "fp64 oracle, weights pre-generated; tokens/s = 1 / (route/T + experts/sample)"
-                       % (cfg.T, t_route, len(tokens), t_exp), seconds=round(t_route + t_exp, 2))
+                       % (cfg.T, t_route, len(tokens), t_exp), seconds=round(t_route + t_exp, 2), ys=[y_tok])
 
 
 def run_reference(args, cfg, rank, world):
@@ -780,9 +848,14 @@ def main():
 
     os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
     out = run_gpu(args, cfg, rank, world, local)
+    parity_y = out.pop("_parity_y", None)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         res = oracle_sample(args, cfg, args.cpu_sample_tokens)
         out["cpu_baseline"] = {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        one = oracle_sample(args, cfg, 1, threads=1)
+        out["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "cores", "sample")}
+        # the same rows on the GPU (layer copy sample_layer_index) against the oracle
+        out["parity"] = parity_gate(parity_y, res["ys"])
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

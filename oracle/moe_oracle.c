@@ -74,11 +74,31 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ACT_BF16 0
 #define ACT_MXFP4 1
 #define ACT_EXACT 2
 #define ACT_MXFP8 3
+
+/* Threads of the OpenMP loops for later calls (the environment is read only once). */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------ scalar formats */
 

@@ -88,6 +88,8 @@ def _load():
         "oracle_nvfp4_unpack": (i32, [P, P, P, i64, i64, i64, P]),
         "oracle_expert_ffn_nvfp4": (None, [P, i32, i32, i32, P, P, P, P, P, P, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_float, i32, P, P, P, P]),
+        "oracle_set_threads": (None, [i32]),
+        "oracle_max_threads": (i32, []),
         "oracle_float_to_bf16_bits": (ctypes.c_uint16, [ctypes.c_float]),
         "oracle_bf16_bits_to_float": (ctypes.c_float, [ctypes.c_uint16]),
     }
@@ -107,8 +109,12 @@ def _ptr(a: Optional[np.ndarray]):
 
 
 def set_threads(n: int) -> None:
-    """Thread count used by the OpenMP loops (applies to later calls)."""
-    os.environ["OMP_NUM_THREADS"] = str(int(n))
+    """Thread count of the OpenMP loops for later calls."""
+    _load().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
 
 
 # ------------------------------------------------------------------ scalar formats

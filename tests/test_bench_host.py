@@ -129,3 +129,51 @@ def test_nvfp4_weight_option_changes_the_byte_model_and_the_names():
     args = argparse.Namespace(expert_norm=False, latent=0, weights="nvfp4")
     assert "NVFP4" in bench.workload_name(args, cfg)
     assert bench.dtype_name(0, "nvfp4").startswith("nvfp4 weights x bf16")
+
+
+def test_parity_gate_accepts_the_oracle_and_refuses_a_wrong_output():
+    import numpy as np
+    rng = np.random.default_rng(0)
+    ys = [rng.standard_normal((1, 64)).astype(np.float32) for _ in range(3)]
+    res = bench.parity_gate(ys, ys)
+    assert res["ok"] and res["rows_checked"] == 3 and res["rel_fro"] == 0.0
+    bad = [y.copy() for y in ys]
+    bad[1][0, 5] += 1.0  # one wrong element
+    with pytest.raises(RuntimeError, match="refusing to record"):
+        bench.parity_gate(bad, ys)
+    with pytest.raises(RuntimeError, match="refusing to record"):
+        bench.parity_gate([np.zeros((1, 64))] * 3, ys)  # an all-zero output
+    with pytest.raises(RuntimeError, match="refusing to record"):
+        bench.parity_gate(ys[:2], ys)
+
+
+@pytest.mark.parametrize("T,weights,norm", [(2, "mxfp4", False), (16, "mxfp4", True), (2, "nvfp4", False)])
+def test_oracle_sample_outputs_are_the_parity_rows(T, weights, norm):
+    """The oracle sample returns, row for row, the outputs of the inputs parity_inputs() names,
+    computed with the sampled layer copy's weights; threads=1 runs on one thread."""
+    import argparse
+
+    import numpy as np
+
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    from oracle import oracle as O
+    cfg = IN.small_config("sample_T%d" % T, T=T, d=256, E=8, k=2, I=256, index=150 + T)
+    args = argparse.Namespace(fmt="bf16", weights=weights, latent=0, expert_norm=norm, layers=4)
+    res = bench.oracle_sample(args, cfg, 3, threads=1)
+    assert res["cores"] == 1
+    inputs = bench.parity_inputs(cfg, 3)
+    li = bench.sample_layer_index(args)
+    assert li == 1
+    W_r, b = IN.make_router(cfg)
+    W_r = (np.random.default_rng([cfg.seed, 77, li]).standard_normal(W_r.shape) / np.sqrt(cfg.d)).astype(np.float32)
+    pack = O.nvfp4_pack if weights == "nvfp4" else O.mxfp4_pack
+
+    def wts(e):
+        return {n: pack(IN.synth_weights(cfg.seed + 7919 * li, t, e, *IN.expert_matrix_shapes(cfg)[t], cfg.weight_std))
+                for n, t in (("gate", IN.TENSOR_GATE), ("up", IN.TENSOR_UP), ("down", IN.TENSOR_DOWN))}
+    assert len(res["ys"]) == len(inputs)
+    for (xb, rows), y in zip(inputs, res["ys"]):
+        ref = O.moe_layer(xb, W_r, b, cfg.k, wts, O.ACT_BF16,
+                          expert_norm_eps=bench.EXPERT_NORM_EPS if norm else None)["y"]
+        np.testing.assert_array_equal(y, ref if rows is None else ref[rows])
+    assert O.max_threads() == len(__import__("os").sched_getaffinity(0))  # restored
