@@ -688,9 +688,6 @@ def oracle_sample(args, cfg, n_tokens, threads=None):
     the two projections of the sampled tokens).  Weight generation is untimed.  threads: OpenMP
     threads for this sample (default: all host cores).  The result's "ys" holds the outputs of
     the rows that parity_inputs() names."""
-    import numpy as np
-
-    from bit_expert_ffn_moe_gb300 import inputs as IN
     from oracle import oracle as O
 
     O.set_threads(threads or len(os.sched_getaffinity(0)))
@@ -708,7 +705,7 @@ def _oracle_sample(args, cfg, n_tokens):
     from bit_expert_ffn_moe_gb300 import inputs as IN
     from oracle import oracle as O
 
-    threads = len(os.sched_getaffinity(0))
+    threads = O.max_threads()
     cm = moe_cfg(args, cfg)
     li = sample_layer_index(args)
     layer_seed = cfg.seed + 7919 * li
