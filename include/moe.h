@@ -110,7 +110,9 @@ typedef struct moe_expert_weights {
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(moe_status s);
 
-/* ABI version of this header (incremented on changes to the entry points). */
+/* ABI version of this header (incremented on changes to the entry points or their structs);
+ * moe_abi_version() returns the library's, which a caller compares with MOE_ABI_VERSION. */
+#define MOE_ABI_VERSION 7
 int moe_abi_version(void);
 
 /* Description of the CUDA error behind the calling thread's last MOE_ERR_CUDA (static string). */
