@@ -336,15 +336,18 @@ def run_gpu(args, cfg, rank, world, local):
     e2e = end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call)
 
     # ---- the oracle sample's rows through the same layer copy (checked in main)
-    parity_y = None
+    parity_y = parity_ids = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        parity_y = []
+        parity_y, parity_ids = [], []
+        ids_p = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w_p = torch.empty((T, k), dtype=torch.float32, device=dev)
         with torch.cuda.stream(stream):
             for xb, rows in parity_inputs(cfg, args.cpu_sample_tokens):
                 x = torch.from_numpy(xb.view(np.int16).copy()).to(dev).view(torch.bfloat16)
-                call(sample_layer_index(args), x, y, None, None, ws, stream.cuda_stream)
+                call(sample_layer_index(args), x, y, ids_p, w_p, ws, stream.cuda_stream)
                 yh = y.float().cpu().numpy()
                 parity_y.append(yh if rows is None else yh[rows])
+                parity_ids.append(ids_p.cpu().numpy().copy())
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -366,6 +369,7 @@ def run_gpu(args, cfg, rank, world, local):
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
         "_parity_y": parity_y,
+        "_parity_ids": parity_ids,
     }
     return out
 
@@ -381,10 +385,21 @@ def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, worl
     if fmt != 0:
         flops = (6.0 * cfg.T * cfg.k * cfg.d * cfg.I + extra_flops) * world
         peak_tf = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16 * world
+        peak_sus = pk["bf16_tflops_sustained"] * NOMINAL_FP4_OVER_BF16 * world
         achieved = flops / (ms_per_step / 1e3) / 1e12
+        # the read-vs-compute roofline of the step: whichever of the weight read and the FP4 math
+        # takes longer bounds it
+        t_bytes = layer_bytes * world / bw
+        t_flops = flops / (peak_tf * 1e12)
+        t_roof = max(t_bytes, t_flops)
         out = {"bound": "tensor", "algorithmic_flops_per_step": flops, "achieved_TFLOPs": round(achieved, 1),
                "peak_TFLOPs": round(peak_tf, 1), "frac": round(achieved / peak_tf, 4),
-               "peak_source": pk["source"] + " bf16 x %.0f (nominal FP4 : bf16 dense ratio)" % NOMINAL_FP4_OVER_BF16,
+               "peak_source": pk["source"] + " bf16 burst x %.0f (nominal FP4 : bf16 dense ratio)"
+                              % NOMINAL_FP4_OVER_BF16,
+               "frac_of_sustained_peak": round(achieved / peak_sus, 4), "sustained_peak_TFLOPs": round(peak_sus, 1),
+               "max_roofline": {"t_bytes_us": round(t_bytes * 1e6, 2), "t_flops_us": round(t_flops * 1e6, 2),
+                                "bound": "hbm" if t_bytes >= t_flops else "tensor",
+                                "frac": round(t_roof / (ms_per_step / 1e3), 4)},
                "hbm": out}
     return out
 
@@ -533,6 +548,8 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
     traffic = ncu_traffic(profile, ["bit_expert_ffn_moe_gb300/csrc/gemv.cu",
                                     "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
     return {"kernel": "gemv_up_kernel (gate/up + SwiGLU, decode)", "bound": "hbm",
+            "timing": "each launch bracketed by events through the step API (eager; inside the timed graph the "
+                      "launch overlaps its neighbours through programmatic dependent launch)",
             "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": per_launch, "avg_launch_us": round(avg_ms * 1e3, 3),
@@ -609,7 +626,7 @@ def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call):
     T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
     n = min(args.steps, 500)
     x_pin = torch.from_numpy(xs_host[:n].view(np.int16).copy()).view(torch.bfloat16).pin_memory()
-    y_pin = torch.empty((n, T, d), dtype=torch.bfloat16).pin_memory()
+    y_pin = torch.empty((min(n, 4), T, d), dtype=torch.bfloat16).pin_memory()  # a ring of host outputs
     x_dev = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     y_dev = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
     ws = make_workspace(T, cm.d, E, k, I, fmt, dev)
@@ -618,7 +635,7 @@ def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call):
     def one(s):
         x_dev.copy_(x_pin[s % x_pin.shape[0]], non_blocking=True)
         call(s, x_dev, y_dev, None, None, ws, st)
-        y_pin[s].copy_(y_dev, non_blocking=True)
+        y_pin[s % y_pin.shape[0]].copy_(y_dev, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for s in range(3):
@@ -653,19 +670,31 @@ def sample_layer_index(args):
 
 def parity_inputs(cfg, n_tokens):
     """The inputs of the oracle sample: (bf16 bits x [T][d], checked rows or None for all).
-    Decode sizes: n_tokens whole layer calls; prefill sizes: one call, n_tokens spread rows."""
+    Decode sizes: n_tokens whole layer calls; prefill sizes: one call (chunk 0) and the workload's
+    seeded token sample (256 tokens of the prefill chunk, 512 of a long-prefill chunk), or n_tokens
+    evenly spread rows when the workload names no sample."""
     import numpy as np
 
     from bit_expert_ffn_moe_gb300 import inputs as IN
     if cfg.T <= 8:
         return [(IN.make_x(cfg, call=c), None) for c in range(n_tokens)]
+    if cfg.sample_tokens:
+        return [(IN.make_x(cfg, call=0), IN.sample_tokens(cfg, cfg.T))]
     return [(IN.make_x(cfg, call=0), np.arange(0, cfg.T, max(1, cfg.T // n_tokens))[:n_tokens])]
 
 
-def parity_gate(gpu_ys, oracle_ys):
-    """Compare the GPU's outputs of the sampled tokens with the oracle's; refuse to record a
-    timing whose output is wrong."""
+def parity_gate(gpu_ys, oracle_ys, gpu_ids=None, oracle_ids=None):
+    """Compare the GPU's outputs of the sampled tokens with the oracle's (and its routing of every
+    token of those calls, which must be identical); refuse to record a timing whose output or
+    routing is wrong."""
     import numpy as np
+    routing = None
+    if gpu_ids is not None and oracle_ids is not None:
+        gi = [np.asarray(a) for a in gpu_ids]
+        oi = [np.asarray(a) for a in oracle_ids]
+        routing = bool(len(gi) == len(oi) and all(a.shape == b.shape and np.array_equal(a, b) for a, b in zip(gi, oi)))
+        if not routing:
+            raise RuntimeError("refusing to record: routing differs from the oracle")
     g = np.concatenate([np.asarray(y, dtype=np.float64).reshape(-1, np.shape(y)[-1]) for y in gpu_ys])
     o = np.concatenate([np.asarray(y, dtype=np.float64).reshape(-1, np.shape(y)[-1]) for y in oracle_ys])
     if g.shape != o.shape:
@@ -677,6 +706,9 @@ def parity_gate(gpu_ys, oracle_ys):
     ok = bool(np.all(np.isfinite(g)) and rel <= PARITY_REL_FRO and mx <= PARITY_MAX_ABS_RMS)
     out = {"rows_checked": int(g.shape[0]), "rel_fro": rel, "max_abs_over_rms": mx,
            "tolerance": {"rel_fro": PARITY_REL_FRO, "max_abs_over_rms": PARITY_MAX_ABS_RMS}, "ok": ok}
+    if routing is not None:
+        out["routing_bit_exact"] = routing
+        out["tokens_routed"] = int(sum(np.asarray(a).shape[0] for a in gpu_ids))
     if not ok:
         raise RuntimeError("refusing to record: output differs from the oracle: %s" % json.dumps(out))
     return out
@@ -748,7 +780,7 @@ def _oracle_sample(args, cfg, n_tokens):
         rows = sum(xb.shape[0] for xb in xs)
         return dict(value=round(rows / dt, 3), unit=UNIT, cores=threads, kind="oracle",
                     sample="%d token rows through narrow -> layer (routing of those rows) -> widen, fp64 oracle, "
-                           "weights pre-generated" % rows, seconds=round(dt, 2), ys=ys)
+                           "weights pre-generated" % rows, seconds=round(dt, 2), ys=ys, ids=None)
     if cfg.T <= 8:
         # decode sizes: whole layer calls
         xs = [xb for xb, _ in parity_inputs(cfg, n_tokens)]
@@ -756,12 +788,18 @@ def _oracle_sample(args, cfg, n_tokens):
             ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
             for e in np.unique(ids):
                 weights(int(e))
+        touched, routed = [], []
+        for xb in xs:
+            ids, _ = O.topk_softmax(O.router_logits(xb, W_r, b), cfg.k)
+            touched.append(len(np.unique(ids)))
+            routed.append(ids)
         t0 = time.perf_counter()
         ys = [O.moe_layer(xb, W_r, b, cfg.k, weights, act, expert_norm_eps=eps)["y"] for xb in xs]
         dt = time.perf_counter() - t0
         return dict(value=round(cfg.T * n_tokens / dt, 3), unit=UNIT, cores=threads, kind="oracle",
-                    sample="%d layer calls of T=%d (full routing, all %d touched experts per call, fp64 oracle), "
-                           "weights pre-generated" % (n_tokens, cfg.T, cfg.k), seconds=round(dt, 2), ys=ys)
+                    sample="%d layer calls of T=%d (full routing, every touched expert: %.1f per call on average, "
+                           "fp64 oracle), weights pre-generated" % (n_tokens, cfg.T, float(np.mean(touched))),
+                    seconds=round(dt, 2), ys=ys, ids=routed)
     # prefill sizes: routing of the whole chunk, expert work for a token sample; per-token cost =
     # routing time / T + expert time / sample size
     (xb, tokens), = parity_inputs(cfg, n_tokens)
@@ -777,7 +815,8 @@ def _oracle_sample(args, cfg, n_tokens):
     return dict(value=round(1.0 / per_tok, 3), unit=UNIT, cores=threads, kind="oracle",
                 sample="routing of all %d tokens (%.2f s) + expert FFNs and sum for %d sampled tokens (%.2f s), "
                        "fp64 oracle, weights pre-generated; tokens/s = 1 / (route/T + experts/sample)"
-                       % (cfg.T, t_route, len(tokens), t_exp), seconds=round(t_route + t_exp, 2), ys=[y_tok])
+                       % (cfg.T, t_route, len(tokens), t_exp), seconds=round(t_route + t_exp, 2), ys=[y_tok],
+                ids=[ids])
 
 
 def run_reference(args, cfg, rank, world):
@@ -806,6 +845,40 @@ def run_reference(args, cfg, rank, world):
     return out
 
 
+PREFILL_LAYER_COPIES = 2  # a prefill step reads ~3.4 GB of expert weights: far more than L2 already
+SUB_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config", "layer_roofline", "roofline",
+            "e2e", "gpu_launches", "clocks", "wall_s_timed", "cpu_baseline", "parity")
+
+
+def extra_workloads(args):
+    """Workloads timed after the headline one in the same run: the prefill chunk and one chunk of
+    the long prefill, when the headline is the plain decode workload (no variant options)."""
+    if args.extra == "none":
+        return []
+    if args.extra != "auto":
+        return [n for n in args.extra.split(",") if n]
+    plain = (args.config == "decode" and not args.latent and not args.expert_norm and args.weights == "mxfp4"
+             and args.fmt == "bf16")
+    return ["prefill", "long_prefill"] if plain else []
+
+
+def run_workload(args, cfg, rank, world, local):
+    """One workload: the GPU timing, then (rank 0, one GPU) the oracle sample, its time as the
+    CPU baseline and the parity gate of the same rows (and routing) through the GPU layer."""
+    out = run_gpu(args, cfg, rank, world, local)
+    parity_y = out.pop("_parity_y", None)
+    parity_ids = out.pop("_parity_ids", None)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = oracle_sample(args, cfg, args.cpu_sample_tokens)
+        out["cpu_baseline"] = {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        if cfg.T <= 8:  # a one-thread sample of the same kind (prefill sizes: tens of seconds, skipped)
+            one = oracle_sample(args, cfg, 1, threads=1)
+            out["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "cores", "sample")}
+        # the same rows on the GPU (layer copy sample_layer_index) against the oracle
+        out["parity"] = parity_gate(parity_y, res["ys"], parity_ids, res["ids"])
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -813,6 +886,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="decode")
+    ap.add_argument("--extra", default="auto",
+                    help="workloads timed after the headline one ('auto': prefill and one long-prefill chunk "
+                         "when the headline is the plain decode workload; 'none'; or a comma list)")
     ap.add_argument("--fmt", choices=["bf16", "mxfp4"], default=None)
     ap.add_argument("--layers", type=int, default=N_LAYER_COPIES)
     ap.add_argument("--no-graph", action="store_true")
@@ -844,15 +920,19 @@ def main():
         return
 
     os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
-    out = run_gpu(args, cfg, rank, world, local)
-    parity_y = out.pop("_parity_y", None)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res = oracle_sample(args, cfg, args.cpu_sample_tokens)
-        out["cpu_baseline"] = {k: res[k] for k in ("value", "unit", "cores", "kind", "sample")}
-        one = oracle_sample(args, cfg, 1, threads=1)
-        out["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "cores", "sample")}
-        # the same rows on the GPU (layer copy sample_layer_index) against the oracle
-        out["parity"] = parity_gate(parity_y, res["ys"])
+    out = run_workload(args, cfg, rank, world, local)
+    # With the default workload the same process also times the prefill chunk and one chunk of the
+    # long prefill (the other half of the metric: the FP4 tensor roofline), each in a sub-object.
+    for name in extra_workloads(args):
+        import gc
+
+        import torch
+        gc.collect()
+        torch.cuda.empty_cache()
+        sub_args = argparse.Namespace(**vars(args))
+        sub_args.config, sub_args.fmt, sub_args.layers = name, "mxfp4", PREFILL_LAYER_COPIES
+        sub = run_workload(sub_args, IN.CONFIGS[name], rank, world, local)
+        out[name] = {k: sub[k] for k in SUB_KEYS if k in sub}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -33,7 +33,7 @@ EXPORTED = (
     "moe_mxfp4_scales_to_mma", "moe_mxfp4_codes_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
-    "moe_dense_workspace_size", "moe_dense_linear", "moe_nvfp4_pack", "moe_nvfp4_unpack",
+    "moe_dense_workspace_size", "moe_dense_linear", "moe_nvfp4_pack", "moe_nvfp4_unpack", "moe_workspace_routing",
 )
 
 
@@ -92,6 +92,8 @@ _SIGS = {
     "moe_selftest_wait_timeout": (I32, [P, SZ, I32, P]),
     "moe_nvfp4_pack": (I32, [P, I64, I64, I64, P, P, P, P]),
     "moe_nvfp4_unpack": (I32, [P, P, P, I64, I64, I64, P, P]),
+    "moe_workspace_routing": (I32, [P, SZ, I32, I32, I32, I32, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P),
+                                    ctypes.POINTER(P), ctypes.POINTER(P)]),
 }
 
 
@@ -227,6 +229,15 @@ def _ws_bytes(ws, ws_bytes):
 def moe_route(x, W_r, b, T, d, E, k, ids, w, ws, ws_bytes=None, stream=None):
     _check("moe_route", load().moe_route(_p(x), _p(W_r), _p(b), T, d, E, k, _p(ids), _p(w), _p(ws),
                                          _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_workspace_routing(ws, T, d, E, k, I, fmt, ws_bytes=None):
+    """Device addresses (ints) of counts, offsets, perm_token and inv_pos inside a layer workspace."""
+    ptrs = [P() for _ in range(4)]
+    _check("moe_workspace_routing",
+           load().moe_workspace_routing(_p(ws), _ws_bytes(ws, ws_bytes), T, d, E, k, I, fmt,
+                                        *[ctypes.byref(q) for q in ptrs]))
+    return tuple(int(q.value) for q in ptrs)
 
 
 def moe_route_noalloc(x, W_r, b, T, d, E, k, ids, w, stream=None):

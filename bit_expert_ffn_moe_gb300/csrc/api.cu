@@ -6,11 +6,7 @@
 
 using namespace moe;
 
-namespace {
-
-constexpr int kAbiVersion = 7;
-
-bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+namespace moe {
 
 // The kernels are compiled for sm_103a only; refuse other devices before launching.
 moe_status check_device() {
@@ -35,13 +31,6 @@ moe_status from_cuda(cudaError_t e) {
     return MOE_ERR_CUDA;
 }
 
-#define MOE_TRY(expr)                               \
-    do {                                            \
-        moe_status _s = (expr);                     \
-        if (_s != MOE_OK) return _s;                \
-    } while (0)
-#define MOE_CUDA(expr) MOE_TRY(from_cuda(expr))
-
 moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     if (T < 0 || d <= 0 || E <= 0 || k <= 0 || I <= 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
@@ -51,6 +40,21 @@ moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     if ((int64_t)T * k > (int64_t)1 << 30 || (int64_t)T * d > ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
+
+}  // namespace moe
+
+namespace {
+
+constexpr int kAbiVersion = 8;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+#define MOE_TRY(expr)                               \
+    do {                                            \
+        moe_status _s = (expr);                     \
+        if (_s != MOE_OK) return _s;                \
+    } while (0)
+#define MOE_CUDA(expr) MOE_TRY(from_cuda(expr))
 
 moe_status check_ws(void* ws, size_t ws_bytes, const WsLayout& L) {
     if (ws == nullptr || !aligned(ws, 256)) return MOE_ERR_WORKSPACE;
@@ -213,6 +217,20 @@ moe_status moe_get_device_status(void* ws, moe_stream_t stream, moe_status* out)
 }
 
 // ---------------------------------------------------------------- layer steps
+
+moe_status moe_workspace_routing(void* ws, size_t ws_bytes, int T, int d, int E, int k, int I, moe_act_fmt fmt,
+                                 int32_t** counts, int32_t** offsets, int32_t** perm_token, int32_t** inv_pos) {
+    MOE_TRY(check_shape(T, d, E, k, I, fmt));
+    if (!counts || !offsets || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, I, fmt);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    *counts = reinterpret_cast<int32_t*>(at(ws, L.counts));
+    *offsets = reinterpret_cast<int32_t*>(at(ws, L.offsets));
+    *perm_token = reinterpret_cast<int32_t*>(at(ws, L.perm));
+    *inv_pos = reinterpret_cast<int32_t*>(at(ws, L.inv));
+    return MOE_OK;
+}
+
 
 moe_status moe_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k, int32_t* ids,
                      float* w, void* ws, size_t ws_bytes, moe_stream_t stream) {

@@ -314,6 +314,14 @@ __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepc
 
 }  // namespace moe
 
+// ------------------------------------------------------------------ host-side checks (api.cu)
+namespace moe {
+moe_status check_device();                 // MOE_ERR_DEVICE unless the current device is sm_103
+moe_status from_cuda(cudaError_t e);       // MOE_ERR_CUDA (recorded for moe_last_cuda_error) or MOE_OK
+// Shape rules of the layer entry points (MOE_ERR_UNSUPPORTED_SHAPE / MOE_ERR_INVALID_ARG).
+moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt);
+}  // namespace moe
+
 // ------------------------------------------------------------------ host-side launch entry points
 // (one per kernel family; defined in the .cu files, called by api.cu)
 namespace moe {

@@ -112,7 +112,7 @@ const char* moe_status_string(moe_status s);
 
 /* ABI version of this header (incremented on changes to the entry points or their structs);
  * moe_abi_version() returns the library's, which a caller compares with MOE_ABI_VERSION. */
-#define MOE_ABI_VERSION 7
+#define MOE_ABI_VERSION 8
 int moe_abi_version(void);
 
 /* Description of the CUDA error behind the calling thread's last MOE_ERR_CUDA (static string). */
@@ -196,6 +196,18 @@ moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
  * *out is MOE_OK or the first device-side error (MOE_ERR_TIMEOUT) recorded since the last
  * call. */
 moe_status moe_get_device_status(void* ws, moe_stream_t stream, moe_status* out);
+
+/* Device pointers to the routing buffers inside a layer workspace (ws of ws_bytes bytes, laid out
+ * for T, d, E, k, I, fmt as moe_workspace_size sizes it): counts[E], offsets[E+1],
+ * perm_token[T*k] and inv_pos[T*k] with the meaning moe_permute gives them (Muse Spark Open
+ * explainer, section 12: pairs gathered per expert).  moe_layer_forward and
+ * moe_layer_forward_norm write them on every call (on the MOE_ACT_BF16 path with up to eight
+ * tokens the one-launch router builds them itself); moe_route on up to eight tokens writes them
+ * too.  They hold the last such call's permutation until the next call on ws; reading them is the
+ * caller's business (after the call's stream work is done).  No device work, no allocation.
+ * MOE_ERR_WORKSPACE when ws is null, misaligned or smaller than the layout. */
+moe_status moe_workspace_routing(void* ws, size_t ws_bytes, int T, int d, int E, int k, int I, moe_act_fmt fmt,
+                                 int32_t** counts, int32_t** offsets, int32_t** perm_token, int32_t** inv_pos);
 
 /* ---------------------------------------------------------------- layer steps */
 

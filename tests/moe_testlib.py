@@ -82,3 +82,28 @@ def bf16_tensor_to_f32(t) -> np.ndarray:
 def bits_to_device(bits: np.ndarray, device="cuda"):
     import torch
     return torch.from_numpy(bits.view(np.int16).copy()).to(device).view(torch.bfloat16)
+
+
+def workspace_routing(ws, T, d, E, k, I, fmt):
+    """counts, offsets, perm_token, inv_pos as the last layer call left them in its workspace."""
+    import torch
+
+    from bit_expert_ffn_moe_gb300 import binding as B
+    torch.cuda.synchronize()
+    ptrs = B.moe_workspace_routing(ws, T, d, E, k, I, fmt)
+    base = ws.data_ptr()
+    out = []
+    for p, n in zip(ptrs, (E, E + 1, T * k, T * k)):
+        off = p - base
+        assert 0 <= off and off % 4 == 0 and off + 4 * n <= ws.numel()
+        out.append(ws[off:off + 4 * n].view(torch.int32).cpu().numpy().copy())
+    return out
+
+
+def check_permutation(routing, ref):
+    """Bit-exact counts, offsets, perm_token and inv_pos against the oracle's permutation."""
+    counts, offsets, perm, inv = routing
+    np.testing.assert_array_equal(counts, ref["counts"])
+    np.testing.assert_array_equal(offsets, ref["offsets"])
+    np.testing.assert_array_equal(perm, ref["perm_token"])
+    np.testing.assert_array_equal(inv, ref["inv_pos"])

@@ -7,7 +7,8 @@ import torch
 from bit_expert_ffn_moe_gb300 import binding as B
 from bit_expert_ffn_moe_gb300 import inputs as IN
 from bit_expert_ffn_moe_gb300.layer import DeviceLayer, layer_forward, make_workspace
-from moe_testlib import bf16_tensor_to_f32, bits_to_device, check_outputs, check_weights, oracle_expert_weights
+from moe_testlib import (bf16_tensor_to_f32, bits_to_device, check_outputs, check_permutation, check_weights,
+                         oracle_expert_weights, workspace_routing)
 from oracle import oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -50,6 +51,8 @@ def test_layer_matches_oracle(name, calls):
         ref = oracle_layer(layer, xb, O.ACT_BF16)
         np.testing.assert_array_equal(ids.cpu().numpy(), ref["ids"])
         check_weights(w.cpu().numpy(), ref["w"])
+        # the permutation the layer call built in its workspace (the one-launch router for T <= 8)
+        check_permutation(workspace_routing(ws, cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16), ref)
         check_outputs(bf16_tensor_to_f32(y), ref["y"], "%s call %d" % (name, call))
     assert B.moe_get_device_status(ws) == B.MOE_OK
 
