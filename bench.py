@@ -237,7 +237,7 @@ def run_gpu(args, cfg, rank, world, local):
     dl = cm.d
     n_calls = max(cfg.calls, 1)
 
-    layers = [DeviceLayer(cm, device=dev, layer=i + 1000 * rank, mma_layouts=(fmt == B.MOE_ACT_MXFP4),
+    layers = [DeviceLayer(cm, device=dev, layer=i + 1000 * rank, mma_layouts=(args.weights == "mxfp4"),
                           wfmt=args.weights) for i in range(args.layers)]
     lat = Latent(cfg, dl, fmt, dev, layers) if args.latent else None
     # all seeded inputs resident in HBM before timing

@@ -16,12 +16,24 @@ constexpr int kPadRows = 128;   // expert row groups of the MXFP4 path start at 
 constexpr int kTokTile = 128;   // token tile (MMA N) of the tcgen05 grouped GEMMs
 
 // ------------------------------------------------------------------ workspace layout
-// Control block (first 256 bytes): status word, decode-route ticket.
+// Control block (first 4 KB, zeroed by moe_workspace_init): status word, decode-route ticket, and
+// the counters of the tensor-core decode kernel (decode_mma.cu): its tile claims and finished
+// CTAs, per active slot the epilogue arrivals that publish the slot's h operand, per 256-feature
+// block the arrivals of the down tiles (the last computes the block's weighted sum).  Every counter
+// is back at zero when a call completes (after a device-side timeout, initialise the workspace
+// again).
+constexpr int kDecTickets = 64;
+constexpr int kDecSlots = 512;
 struct Ctrl {
     int status;
     unsigned route_ticket;
-    int pad[62];
+    unsigned dec_tile;
+    unsigned dec_done;
+    unsigned dec_ticket[kDecTickets];
+    unsigned dec_ready[kDecSlots];
+    int pad[444];
 };
+static_assert(sizeof(Ctrl) == 4096, "control block size");
 
 // Per-call plan written by the permutation and read by the expert kernels (int32 words).
 struct PlanView {
@@ -35,8 +47,14 @@ struct PlanView {
 struct WsLayout {
     size_t ctrl = 0, logits = 0, plan = 0, ids = 0, w = 0, counts = 0, offsets = 0, perm = 0, inv = 0, row_w = 0,
            xq = 0, xs = 0, xa = 0, xa_s = 0, h = 0, h_s = 0, y_perm = 0, total = 0;
+    size_t dxa = 0, dxa_s = 0, dha = 0, dha_s = 0;  // decode on the tensor cores: x and h pieces
     int64_t pad_rows = 0;
 };
+
+// Decode on the tensor cores (decode_mma.cu): at most 16 tokens, whose activation rows are fed to
+// the block-scaled FP4 MMAs as 8 MXFP4 pieces each (rows of one 128-row operand tile).
+constexpr int kMmaDecodeMaxT = 16;
+inline bool mma_decode_shape(int T, int d, int I) { return T >= 1 && T <= kMmaDecodeMaxT && d % 256 == 0 && I % 256 == 0; }
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -81,7 +99,14 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
         L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);
     } else {
         L.h = take(sizeof(uint16_t) * (size_t)P * I);
-        L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);  // expert outputs when they are normalised
+        L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);  // expert outputs (normalised layer, tensor-core decode)
+        if (mma_decode_shape(T, d, I)) {
+            const size_t slots = (size_t)(P < E ? P : E);
+            L.dxa = take((size_t)128 * d / 2);
+            L.dxa_s = take(mma_scale_bytes(128, d));
+            L.dha = take(slots * 128 * I / 2);
+            L.dha_s = take(slots * mma_scale_bytes(128, I));
+        }
     }
     L.total = off;
     return L;
@@ -248,6 +273,11 @@ __host__ __device__ __forceinline__ size_t mma_tile_offset(int64_t row, int64_t 
     return (size_t)tile * 16384 + (size_t)(r * 128 + (((blk % 8) ^ (r % 8)) * 16));
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (no completion signal; p and bytes multiples of 16).
+__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -381,6 +411,21 @@ cudaError_t launch_dense_plan(int T, PlanView plan, int32_t* offsets, int32_t* p
 // Weighted sum of the expert outputs, each first divided by its RMS over d (sqrt(mean + eps)).
 cudaError_t launch_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d,
                                 float eps, uint16_t* y, cudaStream_t st, bool pdl);
+
+// Decode on the tensor cores (decode_mma.cu), MXFP4 weights with their tensor-core copies.
+bool mma_decode_supported(int T, int d, int E, int k, int I, const moe_expert_weights* W);
+// x bf16 [T][d] -> 8 MXFP4 pieces per row: rows 8t + p of a [128][d] operand tile (code tiles xa,
+// scale atoms xa_s).  Reads x before its dependency wait (the preceding kernel must have passed its
+// own wait before letting this one start).
+cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl);
+// Both expert GEMMs in one persistent launch: gate/up tiles, then down tiles (each waits for its
+// slot's h operand), expert outputs to y_perm; with y != nullptr (T <= 4, d <= 64 * 256) the weighted
+// sum y[t] = sum_j w[t][j] y_perm[inv_pos[t k + j]] (fp32, slot order, then bf16) is fused too.
+cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, PlanView plan,
+                              const int32_t* offsets, const int32_t* perm_token, int T, int d, int E, int k, int I,
+                              const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos, const float* w,
+                              uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl);
+bool mma_decode_fused_sum(int T, int d);
 
 cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets,
                            int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,

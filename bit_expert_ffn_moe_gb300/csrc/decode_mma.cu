@@ -1,0 +1,705 @@
+// decode_mma.cu -- the expert GEMMs of small batches (up to 16 tokens) with bf16 activations on
+// the block-scaled FP4 tensor cores (tcgen05, kind::mxf4).
+//
+// At decode sizes every chosen expert sees one or a few tokens and the layer time is the read of
+// the 4-bit expert weights (Muse Spark Open explainer, section 13: at one token per expert the
+// weight read dominates; DGX Spark news item, section 1: batch-1 generation is bound by weight
+// reads).  The tensor cores consume the MXFP4 weights as they are stored, so no CUDA-core work is
+// spent per weight: the copy engine streams 16 KB weight tiles into shared memory and one thread
+// issues the MMAs.  What remains is to hand the tensor cores the bf16 activations.
+//
+// Activation pieces.  A bf16 row (x, or the bf16 SwiGLU output h) is written as the exact sum of
+// kPieces MXFP4 rows plus a residual: piece p is the block-scaled E2M1 rounding of what the
+// earlier pieces left over, r_0 = v, q_p = E2M1(r_p / 2^X_p) * 2^X_p, r_{p+1} = r_p - q_p, with
+// the block exponent X_p = floor(log2 max|r_p|) - 2, raised by one when the maximum would
+// saturate (so that every element lies within the grid, |r_p| / 2^X_p <= 6).  Rounding to the
+// nearest grid value keeps q_p within a factor of two of r_p, so r_p - q_p is exact in fp32, and
+// each piece shrinks the block's largest residual at least threefold (typically about eightfold):
+// after eight pieces it lies below 2^-12 of the block maximum in the worst case and near 2^-24
+// for normal data, far under the bf16 rounding of the layer's outputs.  The MMA of a piece row
+// with a weight row is exact in its products and accumulates in fp32, so the piece rows of a
+// token sum to its dot products.  A token t's pieces are rows 8t .. 8t+7 of the MMA's A operand
+// (M = 128 rows: up to 16 tokens); the epilogue adds the eight lanes of each token.
+//
+// Kernels (one persistent CTA per SM, the same roles as the grouped prefill GEMMs in umma.cu:
+// a producer warp issuing bulk copies into a 4-stage ring, an MMA warp, 8 epilogue warps):
+//   up:   tile (active slot u, block p of 128 intermediate rows): A = the token pieces (one
+//         128-row tile for every expert), B = 128 gate rows followed by the 128 up rows of the
+//         expert, K = d.  Epilogue: per token of the expert, g and u summed over its piece lanes,
+//         h = SiLU(g) * u rounded to bf16, and h's own pieces written as the A operand of the down
+//         GEMM (slot u's 128-row tile, row 8j + p for the expert's j-th token).
+//   down: tile (active slot u, block p of 256 output features): A = slot u's h pieces, B = 256 rows
+//         of W_down, K = I.  Epilogue: per token of the expert, the sum over its piece lanes
+//         rounded to bf16, stored as that permuted row of y_perm (the weighted sum follows).
+// Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
+// waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
+#include "tcgen05.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPieces = 8;
+constexpr int kDecMaxT = 128 / kPieces;  // tokens whose piece rows fill one 128-row tile
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kTile = kStageTileBytes;
+constexpr int kAtom = kScaleAtomBytes;
+constexpr int kStages = 4;
+constexpr int kStageBytes = 3 * kTile + 6 * kAtom;
+constexpr int kAccCols = 256;
+constexpr int kSfBase = kAccCols;
+constexpr int kSfCols = 24;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBarBytes = 512;
+static_assert(kSfBase + kStages * kSfCols <= (int)kTmemCols, "tensor memory budget");
+
+__host__ __device__ constexpr size_t dec_smem_bytes(int E) {
+    return (size_t)kStages * kStageBytes + 1024 + kBarBytes + sizeof(int32_t) * (size_t)(2 * E + 2 + kMaxE);
+}
+
+// ------------------------------------------------------------------ activation pieces
+// Block exponent of a residual block: floor(log2 amax) - 2, plus one when amax > 6 * 2^X, clamped
+// to [-127, 127]; amax = 0 gives -127.  Writes 2^-X (exact) to inv.
+__device__ __forceinline__ int piece_exponent(float amax, float& inv) {
+    const int ef = (int)((__float_as_uint(amax) >> 23) & 0xFF);  // biased exponent; 0 for 0
+    int X = ef - 127 - 2;
+    if (ef != 0 && amax > __uint_as_float((uint32_t)(X + 127 + 2) << 23) * 1.5f) ++X;  // amax > 6 * 2^X
+    X = max(-127, min(127, X));
+    inv = __uint_as_float((uint32_t)(127 - X) << 23);
+    return X;
+}
+
+// Exact values of eight E2M1 codes (one 32-bit word, element 0 in the low nibble).
+__device__ __forceinline__ void e2m1x8_values(uint32_t word, float (&v)[8]) {
+    uint32_t h[4];
+    e2m1x8_to_h2(word, h);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = h2_to_f2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+
+// One piece of eight elements of a block whose maximum residual is amax: the E2M1 codes of
+// r / 2^X (returned) and r -= their values * 2^X (exact).  Returns the scale byte in sbyte.
+__device__ __forceinline__ uint32_t piece8(float (&r)[8], float amax, uint32_t& sbyte) {
+    float inv;
+    const int X = piece_exponent(amax, inv);
+    sbyte = (uint32_t)(X + 127);
+    float s[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = r[i] * inv;
+    const uint32_t codes = e2m1x8_encode(s);
+    float q[8];
+    e2m1x8_values(codes, q);
+    const float scale = __uint_as_float((uint32_t)(X + 127) << 23);  // 2^X (X >= -126 here or q = 0)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) r[i] -= q[i] * (X == -127 ? __uint_as_float(0x00400000u) : scale);
+    return codes;
+}
+
+// Four elements: two E2M1 bytes (element 0 in the low nibble), r -= their values * 2^X.
+__device__ __forceinline__ uint32_t piece4(float (&r)[4], float amax, uint32_t& sbyte) {
+    float inv;
+    const int X = piece_exponent(amax, inv);
+    sbyte = (uint32_t)(X + 127);
+    float s8[8] = {r[0] * inv, r[1] * inv, r[2] * inv, r[3] * inv, 0.f, 0.f, 0.f, 0.f};
+    const uint32_t codes = e2m1x8_encode(s8) & 0xFFFFu;
+    float q[8];
+    e2m1x8_values(codes, q);
+    const float scale = X == -127 ? __uint_as_float(0x00400000u) : __uint_as_float((uint32_t)(X + 127) << 23);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] -= q[i] * scale;
+    return codes;
+}
+
+__device__ __forceinline__ float absmax8(const float (&r)[8]) {
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(r[i]));
+    return m;
+}
+
+// x pieces: one thread per (token, 32-element block); rows 8t + p of the [128][d] A tile.
+__global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restrict__ x, int T, int d, uint8_t* xa,
+                                                       uint8_t* xa_s) {
+    const int nb = d / 32;
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < T * nb) {
+        const int t = i / nb, b = i % nb;
+        float r[4][8];
+        const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + 32 * b);
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint4 u = src[g];
+            const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                r[g][2 * m] = bf16_bits_to_f32(w[m] & 0xFFFFu);
+                r[g][2 * m + 1] = bf16_bits_to_f32(w[m] >> 16);
+            }
+        }
+#pragma unroll 1
+        for (int p = 0; p < kPieces; ++p) {
+            const float amax = fmaxf(fmaxf(absmax8(r[0]), absmax8(r[1])), fmaxf(absmax8(r[2]), absmax8(r[3])));
+            uint32_t sb = 0;
+            uint4 c;
+            c.x = piece8(r[0], amax, sb);
+            c.y = piece8(r[1], amax, sb);
+            c.z = piece8(r[2], amax, sb);
+            c.w = piece8(r[3], amax, sb);
+            const int row = 8 * t + p;
+            *reinterpret_cast<uint4*>(xa + mma_tile_offset(row, b, d)) = c;
+            xa_s[mma_scale_offset(row, b, d)] = (uint8_t)sb;
+        }
+    }
+    // the next kernel's dependency wait covers this kernel's predecessors too
+    pdl_wait();
+}
+
+// ------------------------------------------------------------------ the GEMMs
+struct DecArgs {
+    const uint8_t* xa;    // token pieces: one 128-row A tile of width d (code tiles, scale atoms)
+    const uint8_t* xa_s;
+    uint8_t* ha;          // h pieces: one 128-row A tile of width I per active slot (written by the
+    uint8_t* ha_s;        //   gate/up epilogue, read by the down tiles of that slot)
+    const uint8_t* gq;    // weights, tensor-core layouts: gate / up [E*I][d], down [E*d][I]
+    const uint8_t* gs;
+    const uint8_t* uq;
+    const uint8_t* us;
+    const uint8_t* dq;
+    const uint8_t* ds;
+    PlanView plan;
+    const int32_t* offsets;     // [E+1] permuted-row offsets of the experts
+    const int32_t* perm_token;  // [T*k]
+    int T, E, k, d, I;
+    uint16_t* y_perm;           // bf16 [T*k][d]
+    const int32_t* inv_pos;     // fused weighted sum: [T*k] permuted row of each slot
+    const float* w;             //   [T*k] gate weights
+    uint16_t* y;                //   bf16 [T][d], or null (the sum is a separate launch)
+    Ctrl* ctrl;
+};
+
+// Sum of the accumulator words of one 32-column tensor-memory load over the eight lanes of a lane
+// group (lane bits 0-2), in place: afterwards lane l of the group holds, as fp32 bit patterns in v[0..4), the sums of columns 4 (l & 7) .. 4 (l & 7) + 3.
+template <int HALF, int MASK>
+__device__ __forceinline__ void group8_stage(uint32_t (&v)[32], int lane) {
+    const bool upper = (lane & MASK) != 0;
+#pragma unroll
+    for (int i = 0; i < HALF; ++i) {
+        const float send = __uint_as_float(upper ? v[i] : v[i + HALF]);
+        const float recv = __shfl_xor_sync(0xffffffffu, send, MASK);
+        v[i] = __float_as_uint(__uint_as_float(upper ? v[i + HALF] : v[i]) + recv);
+    }
+}
+
+__device__ __forceinline__ void group8_reduce32(uint32_t (&v)[32], int lane) {
+    group8_stage<16, 4>(v, lane);
+    group8_stage<8, 2>(v, lane);
+    group8_stage<4, 1>(v, lane);
+}
+
+// One epilogue warp's arrival for 256-feature block p after its y_perm rows of a down tile are
+// stored; the last of the 8 x n_act arrivals (every epilogue warp of every tile of the block)
+// computes y[t][256p .. 256p + 255] = sum_j w[t][j] * y_perm[inv_pos[t k + j]] in fp32 in slot
+// order, rounds it to bf16 and resets the ticket.  A slot whose row lies outside [0, T k)
+// contributes nothing.
+__device__ __forceinline__ void fused_sum(const DecArgs& a, int p, int n_act, int lane) {
+    __threadfence();  // this lane's y_perm stores before the arrival
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0) last = atomicAdd(&a.ctrl->dec_ticket[p], 1u) == (unsigned)(8 * n_act - 1);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    const int P = a.T * a.k, d = a.d;
+    const int f = 256 * p + 8 * lane;  // this lane's 8 features
+    for (int t = 0; t < a.T; ++t) {
+        // lane j holds slot j's row and weight (k <= 32), broadcast below: two dependent loads per
+        // token instead of two per slot
+        const int rj = lane < a.k ? __ldcg(a.inv_pos + (size_t)t * a.k + lane) : -1;
+        const float wl = lane < a.k ? __ldcg(a.w + (size_t)t * a.k + lane) : 0.f;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int j0 = 0; j0 < a.k; j0 += 8) {
+            uint4 u[8];
+            float wj[8];
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int r = __shfl_sync(0xffffffffu, rj, (j0 + jj) & 31);
+                wj[jj] = __shfl_sync(0xffffffffu, wl, (j0 + jj) & 31);
+                const bool ok = j0 + jj < a.k && (unsigned)r < (unsigned)P;
+                u[jj] = ok ? __ldcg(reinterpret_cast<const uint4*>(a.y_perm + (size_t)r * d + f)) : make_uint4(0, 0, 0, 0);
+                if (!ok) wj[jj] = 0.f;
+            }
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {  // slot order
+                const uint32_t v[4] = {u[jj].x, u[jj].y, u[jj].z, u[jj].w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    acc[2 * m] = fmaf(wj[jj], bf16_bits_to_f32(v[m] & 0xFFFFu), acc[2 * m]);
+                    acc[2 * m + 1] = fmaf(wj[jj], bf16_bits_to_f32(v[m] >> 16), acc[2 * m + 1]);
+                }
+            }
+        }
+        uint32_t o[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            o[m] = (uint32_t)f32_to_bf16_bits(acc[2 * m]) | ((uint32_t)f32_to_bf16_bits(acc[2 * m + 1]) << 16);
+        *reinterpret_cast<uint4*>(a.y + (size_t)t * d + f) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) a.ctrl->dec_ticket[p] = 0u;  // ready for the next call
+}
+
+// A tile of the decode layer: gate/up (slot u, block p of 128 intermediate rows; K = d) or down
+// (slot u, block p of 256 output features; K = I).
+struct DecTile {
+    bool up;
+    int u, p, e, KT;
+    size_t a_rb, rb0, rb1;  // 128-row blocks: A operand, B rows 0..127, B rows 128..255
+    const uint8_t *aq, *as, *bq0, *bs0, *bq1, *bs1;
+};
+
+__device__ __forceinline__ DecTile dec_tile(int t, const DecArgs& a, const int32_t* s_act, int n_up) {
+    DecTile D;
+    const int nbu = a.I / 128, nbd = a.d / 256;
+    D.up = t < n_up;
+    const int l = D.up ? t : t - n_up, nb = D.up ? nbu : nbd;
+    D.u = l / nb;
+    D.p = l % nb;
+    D.e = s_act[D.u];
+    D.KT = (D.up ? a.d : a.I) / 256;
+    if (D.up) {
+        D.a_rb = 0;
+        D.rb0 = D.rb1 = (size_t)D.e * nbu + D.p;
+        D.aq = a.xa;
+        D.as = a.xa_s;
+        D.bq0 = a.gq;
+        D.bs0 = a.gs;
+        D.bq1 = a.uq;
+        D.bs1 = a.us;
+    } else {
+        D.a_rb = D.u;
+        D.rb0 = (size_t)D.e * 2 * nbd + 2 * D.p;
+        D.rb1 = D.rb0 + 1;
+        D.aq = a.ha;
+        D.as = a.ha_s;
+        D.bq0 = D.bq1 = a.dq;
+        D.bs0 = D.bs1 = a.ds;
+    }
+    return D;
+}
+
+// Chunk c of a gate/up tile's columns (one MX block of h, 32 features): lane pl of the token's
+// group gets features 4pl .. 4pl+3, forms h and writes its part of the block's 8 pieces.
+__device__ __forceinline__ void up_chunk(const DecArgs& args, const DecTile& D, uint32_t (&gv)[32], uint32_t (&uv)[32],
+                                         int half, int c, int lane, int j, size_t row0) {
+    const int pl = lane & 7;
+    group8_reduce32(gv, lane);
+    group8_reduce32(uv, lane);
+    float r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float g = __uint_as_float(gv[i]), u = __uint_as_float(uv[i]);
+        const float hv = __fdividef(g, 1.f + __expf(-g)) * u;  // SiLU(g) * u
+        r[i] = bf16_bits_to_f32(f32_to_bf16_bits(hv));      // h as bf16
+    }
+    const int blk = 4 * D.p + 2 * half + c;
+#pragma unroll 1
+    for (int pc = 0; pc < kPieces; ++pc) {
+        float amax = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        uint32_t sb;
+        const uint32_t codes = piece4(r, amax, sb);
+        if (j >= 0) {
+            const size_t row = row0 + pc;
+            *reinterpret_cast<uint16_t*>(args.ha + mma_tile_offset((int64_t)row, blk, args.I) + 2 * pl) =
+                (uint16_t)codes;
+            if (pl == 0) args.ha_s[mma_scale_offset((int64_t)row, blk, args.I)] = (uint8_t)sb;
+        }
+    }
+}
+
+// Chunk c of a down tile's columns: lane pl of row group grp gets columns 4pl .. 4pl+3, stores them
+// as bf16 into that permuted row of y_perm.
+__device__ __forceinline__ void down_chunk(const DecArgs& args, const DecTile& D, uint32_t (&v)[32], int half, int c,
+                                           int lane, int grp, int r0, int cnt) {
+    const int pl = lane & 7;
+    group8_reduce32(v, lane);
+    if (grp < cnt) {
+        const uint32_t o0 = (uint32_t)f32_to_bf16_bits(__uint_as_float(v[0])) |
+                            ((uint32_t)f32_to_bf16_bits(__uint_as_float(v[1])) << 16);
+        const uint32_t o1 = (uint32_t)f32_to_bf16_bits(__uint_as_float(v[2])) |
+                            ((uint32_t)f32_to_bf16_bits(__uint_as_float(v[3])) << 16);
+        uint16_t* dst = args.y_perm + (size_t)(r0 + grp) * args.d + (size_t)D.p * 256 + 128 * half + 32 * c + 4 * pl;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(o0, o1);
+    }
+}
+
+// Gate/up tile epilogue of one warp (lane quarter rows, half of the columns): per token of the
+// expert, g and u summed over its 8 piece lanes, h = SiLU(g) * u rounded to bf16, and h's pieces
+// written as the slot's down-GEMM operand; then the warp's arrival publishes them.
+__device__ __forceinline__ void epilogue_up(const DecArgs& args, const DecTile& D, uint32_t acc, int half, int grp,
+                                            int lane, int r0, int cnt, const int32_t* s_perm, uint64_t* acc_empty,
+                                            Ctrl* ctrl) {
+    const bool live = 4 * (grp >> 2) < args.T;  // this warp's token groups include a real token
+    if (live) {
+        int j = -1;  // the expert's row index of token grp, or -1 when it did not choose it
+        if (grp < args.T)
+            for (int i = 0; i < cnt; ++i)
+                if (s_perm[r0 + i] == grp) j = i;
+        const size_t row0 = (size_t)D.u * 128 + 8 * (size_t)(j < 0 ? 0 : j);
+        // one chunk (g and u of 32 features) at a time; the accumulator is released after the last load
+        uint32_t gv[32], uv[32];
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+            tmem_ld32(acc + 32 * (2 * half + c), gv);
+            tmem_ld32(acc + 128 + 32 * (2 * half + c), uv);
+            tmem_ld_wait();
+            if (c == 1) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            }
+            up_chunk(args, D, gv, uv, half, c, lane, j, row0);
+        }
+    } else {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+    }
+    // publish: this warp's share of the slot's h pieces is in place (every warp arrives)
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(&ctrl->dec_ready[D.u], 1u);
+}
+
+// Down tile epilogue of one warp: per row of the expert, the sum over its 8 piece lanes rounded to
+// bf16 and stored as that permuted row of y_perm; then (fused weighted sum) the warp's arrival.
+__device__ __forceinline__ void epilogue_down(const DecArgs& args, const DecTile& D, uint32_t acc, int half, int grp,
+                                              int lane, int r0, int cnt, int n_act, uint64_t* acc_empty) {
+    const bool live = 4 * (grp >> 2) < cnt;
+    if (live) {
+        uint32_t v[32];
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            tmem_ld32(acc + 32 * (4 * half + c), v);
+            tmem_ld_wait();
+            if (c == 3) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            }
+            down_chunk(args, D, v, half, c, lane, grp, r0, cnt);
+        }
+    } else {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+    }
+    if (args.y != nullptr) fused_sum(args, D.p, n_act, lane);
+}
+
+constexpr int kTileQ = 8;  // tile-id queue from the claiming producer to the other roles
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// One persistent CTA per SM.  Roles: warp 0 claims tiles (a global counter: every gate/up tile,
+// then every down tile) and streams their weight tiles and scales into the ring; warp 10 streams
+// the A operand (the token pieces, or the slot's h pieces once all gate/up tiles of that slot have
+// published them); warp 1 copies scales to tensor memory and issues the MMAs; warps 2-9 drain the
+// accumulator.  The down tiles' weights stream while their h is still being produced.
+__global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(const DecArgs args) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full_b = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+    uint64_t* full_a = full_b + kStages;
+    uint64_t* empty = full_a + kStages;
+    uint64_t* tq_full = empty + kStages;
+    uint64_t* tq_empty = tq_full + kTileQ;
+    uint64_t* acc_full = tq_empty + kTileQ;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* mma_done = acc_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    int* s_tq = const_cast<int*>(abort_flag) + 1;                                           // [kTileQ]
+    int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + kBarBytes);  // [E+1]
+    int32_t* s_act = s_off + (args.E + 1);                                                  // [E]
+    int32_t* s_perm = s_act + args.E;                                                       // [T*k]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Ctrl* ctrl = args.ctrl;
+    int* status = &ctrl->status;
+
+    auto stage_a = [&](int s) { return smem + (size_t)s * kStageBytes; };
+    auto stage_b = [&](int s) { return smem + (size_t)s * kStageBytes + kTile; };
+    auto stage_sfa = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile; };
+    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile + 2 * kAtom; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full_b[s], 1);
+            mbar_init(&full_a[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int q = 0; q < kTileQ; ++q) {
+            mbar_init(&tq_full[q], 1);
+            mbar_init(&tq_empty[q], 2 + kEpiWarps);  // A producer, MMA warp, epilogue warps
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kEpiWarps);
+        mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+
+    pdl_wait();  // routing plan and token pieces come from the preceding kernels
+    const int n_act = args.plan.scalars[0];
+    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
+        s_off[i] = args.offsets[i];
+        if (i < args.E) s_act[i] = args.plan.active[i];
+    }
+    __syncthreads();
+    const int n_pairs = s_off[args.E];
+    for (int i = threadIdx.x; i < n_pairs; i += blockDim.x) s_perm[i] = args.perm_token[i];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int nbu = args.I / 128;
+    const int n_up = n_act * nbu, n_tiles = n_up + n_act * (args.d / 256);
+
+    // next tile id from the queue (every role but the claiming producer); -1 ends the loop
+    auto next_tile = [&](int q, bool arrive) -> int {
+        if (!mbar_wait(&tq_full[q % kTileQ], (uint32_t)(q / kTileQ) & 1u, abort_flag, status)) return -1;
+        const int t = s_tq[q % kTileQ];
+        if (arrive) mbar_arrive(&tq_empty[q % kTileQ]);
+        return t;
+    };
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- tile claims + weight copies
+        if (lane == 0) {
+            int kiter = 0;
+            for (int q = 0;; ++q) {
+                if (!mbar_wait(&tq_empty[q % kTileQ], ((uint32_t)(q / kTileQ) & 1u) ^ 1u, abort_flag, status)) break;
+                // the first tile of every CTA is its own index; later ones are claimed from the
+                // counter, which starts past them
+                const unsigned c = q == 0 ? blockIdx.x : gridDim.x + atomicAdd(&ctrl->dec_tile, 1u);
+                const int t = c < (unsigned)n_tiles ? (int)c : -1;
+                s_tq[q % kTileQ] = t;
+                mbar_arrive(&tq_full[q % kTileQ]);
+                if (t < 0) break;
+                const DecTile D = dec_tile(t, args, s_act, n_up);
+                const int apr = D.KT * 2;  // scale atoms per 128-row block
+                bool ok = true;
+                for (int kt = 0; kt < D.KT; ++kt, ++kiter) {
+                    const int s = kiter % kStages;
+                    if (!mbar_wait(&empty[s], ((uint32_t)(kiter / kStages) & 1u) ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_b[s], 2 * kTile + 4 * kAtom);
+                    bulk_load(stage_b(s), D.bq0 + (D.rb0 * D.KT + kt) * kTile, kTile, &full_b[s]);
+                    bulk_load(stage_b(s) + kTile, D.bq1 + (D.rb1 * D.KT + kt) * kTile, kTile, &full_b[s]);
+                    bulk_load(stage_sfb(s), D.bs0 + (D.rb0 * apr + 2 * kt) * kAtom, 2 * kAtom, &full_b[s]);
+                    bulk_load(stage_sfb(s) + 2 * kAtom, D.bs1 + (D.rb1 * apr + 2 * kt) * kAtom, 2 * kAtom, &full_b[s]);
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {  // let the copies already issued land before shared memory is released
+                volatile int never = 0;
+                for (int i = 0; i < kStages && i < kiter; ++i) {
+                    const int it = kiter - 1 - i;
+                    mbar_wait(&full_b[it % kStages], (it / kStages) & 1, &never, nullptr, 100000000LL);
+                }
+            }
+        }
+    } else if (warp == kThreads / 32) {
+        // ---------------------------------------------------------- A operand copies
+        if (lane == 0) {
+            int kiter = 0;
+            for (int q = 0;; ++q) {
+                const int t = next_tile(q, true);
+                if (t < 0) break;
+                const DecTile D = dec_tile(t, args, s_act, n_up);
+                const int cnt = s_off[D.e + 1] - s_off[D.e];
+                const int rows = 8 * (D.up ? args.T : cnt);
+                const uint32_t a_bytes = (uint32_t)(rows < 128 ? rows : 128) * 128;
+                bool ok = true;
+                if (!D.up) {
+                    // the slot's h pieces: every epilogue warp of every gate/up tile of the slot arrives
+                    const unsigned need = (unsigned)(kEpiWarps * nbu);
+                    const long long t0 = clock64();
+                    while (ld_acquire_u32(&ctrl->dec_ready[D.u]) < need) {
+                        if (*abort_flag || clock64() - t0 > kWaitCycles) {
+                            set_status(status, MOE_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    asm volatile("fence.proxy.async.global;" ::: "memory");  // generic stores -> bulk copies
+                }
+                for (int kt = 0; kt < D.KT && ok; ++kt, ++kiter) {
+                    const int s = kiter % kStages;
+                    if (!mbar_wait(&empty[s], ((uint32_t)(kiter / kStages) & 1u) ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full_a[s], a_bytes + 2 * kAtom);
+                    bulk_load(stage_a(s), D.aq + (D.a_rb * D.KT + kt) * kTile, a_bytes, &full_a[s]);
+                    bulk_load(stage_sfa(s), D.as + (D.a_rb * D.KT * 2 + 2 * kt) * kAtom, 2 * kAtom, &full_a[s]);
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                volatile int never = 0;
+                for (int i = 0; i < kStages && i < kiter; ++i) {
+                    const int it = kiter - 1 - i;
+                    mbar_wait(&full_a[it % kStages], (it / kStages) & 1, &never, nullptr, 100000000LL);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer (whole warp)
+        int kiter = 0, it = 0;
+        const uint32_t idesc = idesc_mxf4(128, 256);
+        for (int q = 0;; ++q, ++it) {
+            int t = next_tile(q, false);
+            if (lane == 0 && t >= 0) mbar_arrive(&tq_empty[q % kTileQ]);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t < 0) break;
+            const DecTile D = dec_tile(t, args, s_act, n_up);
+            if (!mbar_wait_warp(acc_empty, (it & 1) ^ 1, abort_flag, status)) break;
+            tc_fence_after();
+            bool ok = true;
+            for (int kt = 0; kt < D.KT; ++kt, ++kiter) {
+                const int s = kiter % kStages;
+                const uint32_t ph = (kiter / kStages) & 1;
+                if (!mbar_wait_warp(&full_b[s], ph, abort_flag, status) ||
+                    !mbar_wait_warp(&full_a[s], ph, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sf = tmem + kSfBase + s * kSfCols;
+                stage_scales_to_tmem(sf, desc_sf(stage_sfa(s)), desc_sf(stage_sfa(s) + kAtom), desc_sf(stage_sfb(s)),
+                                     desc_sf(stage_sfb(s) + 2 * kAtom), desc_sf(stage_sfb(s) + kAtom),
+                                     desc_sf(stage_sfb(s) + 3 * kAtom));
+                stage_mmas_commit(tmem, desc_sw128(stage_a(s)), desc_sw128(stage_b(s)), idesc,
+                                  idesc | (2u << 29) | (2u << 4), sf, kt > 0 ? 1u : 0u, &empty[s]);
+            }
+            if (!ok) break;
+            tc_commit(acc_full);
+        }
+        tc_commit(mma_done);
+        volatile int never = 0;
+        mbar_wait_warp(mma_done, 0, &never, nullptr, 100000000LL);
+    } else {
+        // ---------------------------------------------------------- epilogue (warps 2-9)
+        const int q4 = warp & 3;          // tensor-memory lane quarter: rows 32q4 .. 32q4 + 31
+        const int half = (warp - 2) / 4;  // half of the accumulator columns
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+        const int grp = 4 * q4 + (lane >> 3);  // 8-row group: token grp (gate/up) or the expert's row grp (down)
+        int it = 0;
+        for (int q = 0;; ++q, ++it) {
+            int t = next_tile(q, false);
+            if (lane == 0 && t >= 0) mbar_arrive(&tq_empty[q % kTileQ]);
+            t = __shfl_sync(0xffffffffu, t, 0);
+            if (t < 0) break;
+            const DecTile D = dec_tile(t, args, s_act, n_up);
+            const int r0 = s_off[D.e], cnt = s_off[D.e + 1] - r0;
+            if (!mbar_wait(acc_full, it & 1, abort_flag, status)) break;
+            tc_fence_after();
+            if (D.up)
+                epilogue_up(args, D, tmem + lane_base, half, grp, lane, r0, cnt, s_perm, acc_empty, ctrl);
+            else
+                epilogue_down(args, D, tmem + lane_base, half, grp, lane, r0, cnt, n_act, acc_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    if (threadIdx.x == 0 && !(*abort_flag)) {
+        // the last CTA out resets the claim counter and the slots' arrival counts for the next call
+        __threadfence();
+        if (atomicAdd(&ctrl->dec_done, 1u) == gridDim.x - 1) {
+            for (int u = 0; u < n_act; ++u) ctrl->dec_ready[u] = 0u;
+            ctrl->dec_tile = 0u;
+            __threadfence();
+            ctrl->dec_done = 0u;
+        }
+    }
+    pdl_launch_dependents();
+}
+
+}  // namespace
+
+static_assert(kDecMaxT == kMmaDecodeMaxT, "decode tile geometry");
+
+bool mma_decode_supported(int T, int d, int E, int k, int I, const moe_expert_weights* W) {
+    return mma_decode_shape(T, d, I) && (T * k < E ? T * k : E) <= kDecSlots && W->wfmt == MOE_W_MXFP4 &&
+           W->gate_q_mma && W->gate_s_mma && W->up_q_mma && W->up_s_mma && W->down_q_mma && W->down_s_mma;
+}
+
+bool mma_decode_fused_sum(int T, int d) { return T <= 4 && d / 256 <= kDecTickets; }
+
+cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl) {
+    const int n = T * (d / 32);
+    void* args[] = {&x, &T, &d, &xa, &xa_s};
+    return launch_kernel((const void*)x_pieces_kernel, dim3((n + 255) / 256), dim3(256), 0, st, pdl, args);
+}
+
+cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, PlanView plan,
+                              const int32_t* offsets, const int32_t* perm_token, int T, int d, int E, int k, int I,
+                              const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos, const float* w,
+                              uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl) {
+    DecArgs a = {};
+    a.xa = xa;
+    a.xa_s = xa_s;
+    a.ha = ha;
+    a.ha_s = ha_s;
+    a.gq = W->gate_q_mma;
+    a.gs = W->gate_s_mma;
+    a.uq = W->up_q_mma;
+    a.us = W->up_s_mma;
+    a.dq = W->down_q_mma;
+    a.ds = W->down_s_mma;
+    a.plan = plan;
+    a.offsets = offsets;
+    a.perm_token = perm_token;
+    a.T = T;
+    a.E = E;
+    a.k = k;
+    a.d = d;
+    a.I = I;
+    a.y_perm = y_perm;
+    a.inv_pos = inv_pos;
+    a.w = w;
+    a.y = (y != nullptr && mma_decode_fused_sum(T, d)) ? y : nullptr;
+    a.ctrl = ctrl;
+    void* kargs[] = {&a};
+    return launch_kernel((const void*)umma_decode_layer_kernel, dim3(sm_count()), dim3(kThreads + 32),
+                         dec_smem_bytes(E), st, pdl, kargs);
+}
+
+}  // namespace moe

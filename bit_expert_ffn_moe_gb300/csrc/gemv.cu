@@ -412,10 +412,10 @@ __device__ __forceinline__ void batch_dots(const uint4* xs, int q0, int nq, int 
 // Grid (M_exp / outs, slots): slot u is the u-th active expert.  A batch gives each row group
 // kR/2 output features i (gate row i and up row i), for up to Q of the expert's tokens; an
 // expert with more rows takes them Q at a time (its weights are read again per pass).
-// NVFP4 with one block per thread and two token rows: bounded to two CTAs per SM (without the
-// bound its registers allow one).
+// One block per thread: bounded to two CTAs per SM (128 registers; the two-row instantiations
+// would otherwise take more and fit one CTA per SM).
 template <int BPT, int Q, bool NV>
-__global__ void __launch_bounds__(kThr, (NV && BPT == 1 && Q == 2) ? 2 : 0)
+__global__ void __launch_bounds__(kThr, BPT == 1 ? 2 : 0)
 gemv_up_cta_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int kOut = kR / 2;

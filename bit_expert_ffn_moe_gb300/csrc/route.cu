@@ -176,6 +176,8 @@ route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     pdl_wait();
+    // the next kernel may start now: what it reads before its own dependency wait (x) is ready
+    pdl_launch_dependents();
     // Chunk c holds the 4-element groups [c*Gc, (c+1)*Gc) of the row (clamped to d/4); Gc is a
     // multiple of 32, so group g stays with lane g % 32 and the fixed summation order holds.
     const int ng = d / 4;

@@ -39,7 +39,7 @@
 //             then converting and storing them while the next tile's MMAs run.
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
-#include "common.cuh"
+#include "tcgen05.cuh"
 
 namespace moe {
 namespace {
@@ -61,130 +61,6 @@ static_assert(kSfBase + kStages * kSfCols <= (int)kTmemCols, "tensor memory budg
 
 constexpr size_t smem_bytes(int E) {
     return (size_t)kStages * kStageBytes + 1024 /* alignment */ + kBarBytes + (size_t)4 * (E + 1) * sizeof(int32_t);
-}
-
-// ------------------------------------------------------------------ PTX wrappers
-// One K step of 256 values: the six scale-atom copies of the stage into tensor memory, then the
-// four K = 64 MMAs and the commit that frees the stage, each group issued by one elected lane.
-// Scale slot of a stage (24 columns from sf): A scales of K values 0..127 at sf, 128..255 at
-// sf + 4; B scales of K values 0..127 at sf + 8 (rows 0..127) and sf + 12 (rows 128..255), of
-// K values 128..255 at sf + 16 and sf + 20.
-__device__ __forceinline__ void stage_scales_to_tmem(uint32_t sf, uint64_t a0, uint64_t a1, uint64_t b00,
-                                                     uint64_t b10, uint64_t b01, uint64_t b11) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%2], %3;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%6], %7;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%8], %9;\n\t"
-        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%10], %11;\n\t}" ::"r"(sf),
-        "l"(a0), "r"(sf + 4), "l"(a1), "r"(sf + 8), "l"(b00), "r"(sf + 12), "l"(b10), "r"(sf + 16), "l"(b01),
-        "r"(sf + 20), "l"(b11)
-        : "memory");
-}
-
-// MMAs of one stage: sub-steps 0..3 use A/B descriptors advanced by 32 bytes each and scale bytes
-// (sub & 1) * 2 of the A/B scale columns of K values 0..127 (subs 0, 1) or 128..255 (subs 2, 3).
-__device__ __forceinline__ void stage_mmas_commit(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id0, uint32_t id2,
-                                                  uint32_t sf, uint32_t accumulate, uint64_t* bar) {
-    asm volatile(
-        "{\n\t.reg .pred e, p, q;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "setp.ne.b32 p, %5, 0;\n\t"
-        "setp.eq.b32 q, %5, %5;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%6], [%7], p;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %8, %9, %4, [%6], [%7], q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %10, %11, %3, [%12], [%13], q;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %14, %15, %4, [%12], [%13], q;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%16];\n\t}" ::"r"(d),
-        "l"(ad), "l"(bd), "r"(id0), "r"(id2), "r"(accumulate), "r"(sf), "r"(sf + 8), "l"(ad + 2), "l"(bd + 2),
-        "l"(ad + 4), "l"(bd + 4), "r"(sf + 4), "r"(sf + 16), "l"(ad + 6), "l"(bd + 6), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// mbar_wait by every lane of a warp with a warp-uniform verdict.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                               long long limit = kWaitCycles) {
-    const bool ok = mbar_wait(bar, parity, abort_flag, status, limit);
-    return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor: K-major operand tile with 128-byte swizzle; 8-row groups of
-// 8 x 128 bytes lie 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_sw128(const void* p) {
-    const uint64_t a = smem_u32(p);
-    return ((a >> 4) & 0x3FFFull) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
-}
-// Descriptor of one 512-byte scale atom: 32 rows x 16 bytes, no swizzle (8-row core matrices
-// of 128 contiguous bytes).
-__device__ __forceinline__ uint64_t desc_sf(const void* p) {
-    const uint64_t a = smem_u32(p);
-    return ((a >> 4) & 0x3FFFull) | (1ull << 16) | ((uint64_t)(128 >> 4) << 32) | (1ull << 46);
-}
-
-// Instruction descriptor of kind::mxf4 with block scaling: A and B E2M1 (format code 1), K-major,
-// UE8M0 scales, D fp32, shape M x N; the scale-factor byte selectors are added per MMA.
-__device__ __forceinline__ uint32_t idesc_mxf4(int M, int N) {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
-}
-
-// The MMA warp runs its loop with all 32 lanes (warp-uniform control flow, so every operand is
-// warp-uniform) and each tcgen05 instruction is issued by one lane chosen by elect.sync inside
-// the instruction's own asm block.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// 4 x 4 transpose of 16-byte pieces among the lanes of each aligned group of four: on entry lane
-// 4g + i holds pieces p[0..3] of row i of the group, on return p[j] = piece i of row j.  Two xor
-// stages (swap the off-diagonal 2 x 2 blocks, then the off-diagonal pieces inside each block).
-__device__ __forceinline__ void transpose4_pieces(uint4 (&p)[4], int lane) {
-    const bool i1 = (lane >> 1) & 1, i0 = lane & 1;
-#pragma unroll
-    for (int j0 = 0; j0 < 2; ++j0) {  // stage A: exchange pieces whose bit 1 differs from the lane's
-        uint4& lo = p[j0];
-        uint4& hi = p[2 | j0];
-        uint4 snd = i1 ? lo : hi;
-        uint4 rcv;
-        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, 2);
-        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, 2);
-        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, 2);
-        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, 2);
-        if (i1) lo = rcv; else hi = rcv;
-    }
-#pragma unroll
-    for (int j1 = 0; j1 < 2; ++j1) {  // stage B: exchange pieces whose bit 0 differs from the lane's
-        uint4& lo = p[2 * j1];
-        uint4& hi = p[2 * j1 + 1];
-        uint4 snd = i0 ? lo : hi;
-        uint4 rcv;
-        rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, 1);
-        rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, 1);
-        rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, 1);
-        rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, 1);
-        if (i0) lo = rcv; else hi = rcv;
-    }
 }
 
 // ------------------------------------------------------------------ kernel arguments / tiles

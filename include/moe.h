@@ -189,7 +189,9 @@ size_t moe_workspace_size(int T, int d, int E, int k, int I, moe_act_fmt fmt);
  * expert's rows start at a multiple of 128.  An upper bound that depends on sizes only. */
 int64_t moe_padded_rows(int T, int k, int E);
 
-/* Zero the workspace control block (status word, counters).  Call once per workspace. */
+/* Zero the workspace control block (status word, counters; the first 4 KB).  Call once per
+ * workspace, and again after moe_get_device_status reported MOE_ERR_TIMEOUT (a call that timed
+ * out may leave its counters set). */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Synchronise `stream`, copy the device status word of `ws` to *out and clear it.
@@ -295,8 +297,19 @@ moe_status moe_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, cons
 
 /* The whole layer in one call: route -> permute -> up+SwiGLU -> down -> combine, all on
  * `stream`, with no host synchronisation.  y bf16 [T][d].  ids/w (optional, may be NULL)
- * receive the routing.  For MOE_ACT_BF16 the down GEMV and the weighted sum are fused (the
- * per-expert outputs are rounded to bf16 before weighting, exactly as y_perm would be). */
+ * receive the routing.  The per-expert outputs are rounded to bf16 before the weighted sum,
+ * exactly as y_perm would be.  MOE_ACT_BF16 takes one of two kernel paths:
+ *   - 1 <= T <= 16, d % 256 == 0, I % 256 == 0 and MXFP4 weights carrying their tensor-core
+ *     copies (the *_mma fields): the expert GEMMs run on the block-scaled FP4 tensor cores in one
+ *     persistent launch.  Each bf16 activation row (x, and the bf16 SwiGLU output h) is fed as
+ *     the exact sum of 8 MXFP4 rows plus a residual: piece p rounds what pieces 0..p-1 left over
+ *     onto the E2M1 grid with its own power-of-two block scale, so the residual after 8 pieces
+ *     is below 2^-12 of each 32-element block's maximum (about 2^-24 for normal data); products
+ *     are exact and accumulate in fp32.  For T <= 4 the weighted sum is fused as well.
+ *   - otherwise (NVFP4 weights, no tensor-core copies, other shapes): CUDA-core GEMVs with
+ *     exact products (bf16 activations, fp32 accumulation), down GEMV and weighted sum fused.
+ * The step entry points (moe_expert_up_swiglu, moe_expert_down with MOE_ACT_BF16) run the
+ * GEMVs. */
 moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                              int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids,
                              float* w, void* ws, size_t ws_bytes, moe_stream_t stream);

@@ -1,5 +1,7 @@
-"""GPU parity of the decode-shape path (MOE_ACT_BF16): the whole layer against the oracle, and the
-step-by-step entry points against the fused layer call."""
+"""GPU parity of the decode-shape path (MOE_ACT_BF16): the whole layer against the oracle on both
+of its kernel paths (tensor-core GEMMs on activation pieces when the weights carry their
+tensor-core copies, CUDA-core GEMVs otherwise), and the step-by-step entry points (the GEMVs)
+against the fused layer call on the GEMV path."""
 import numpy as np
 import pytest
 import torch
@@ -25,12 +27,15 @@ SMALL = {
 }
 
 
-def get_layer(name):
-    if name not in _layers:
+def get_layer(name, mma=True):
+    """mma: with the tensor-core weight copies (the layer call then runs the tensor-core GEMMs for
+    up to 16 tokens); without them every bf16-path call runs the GEMVs."""
+    key = (name, mma)
+    if key not in _layers:
         _layers.clear()
         torch.cuda.empty_cache()
-        _layers[name] = DeviceLayer(SMALL[name] if name in SMALL else IN.CONFIGS[name])
-    return _layers[name]
+        _layers[key] = DeviceLayer(SMALL[name] if name in SMALL else IN.CONFIGS[name], mma_layouts=mma)
+    return _layers[key]
 
 
 def oracle_layer(layer, xb, act_fmt, tokens=None):
@@ -39,10 +44,11 @@ def oracle_layer(layer, xb, act_fmt, tokens=None):
                        tokens=tokens)
 
 
+@pytest.mark.parametrize("mma", [True, False])
 @pytest.mark.parametrize("name,calls", [("tiny", [0, 1]), ("decode", [0, 1, 2]), ("spec_verify", [0]),
                                         ("ring_t3", [0, 1]), ("ring_t2", [0, 1]), ("ring_t1", [0, 1, 2])])
-def test_layer_matches_oracle(name, calls):
-    layer = get_layer(name)
+def test_layer_matches_oracle(name, calls, mma):
+    layer = get_layer(name, mma)
     cfg = layer.cfg
     ws = make_workspace(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
     for call in calls:
@@ -59,7 +65,7 @@ def test_layer_matches_oracle(name, calls):
 
 @pytest.mark.parametrize("name", ["tiny", "ring_t3", "ring_t2", "ring_t1"])
 def test_step_calls_equal_layer_call_and_oracle_h(name):
-    layer = get_layer(name)
+    layer = get_layer(name, mma=False)  # the step calls and the layer call both on the GEMVs
     cfg = layer.cfg
     T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
     P = T * k

@@ -1,6 +1,7 @@
 """GPU parity of the bf16-activation path with more than four tokens at the full decode widths:
 the warp-per-row GEMVs whose lanes own 8 (d = 8192), 4 (d = 4096) or 2 (I = 2048 and 1536)
-32-element blocks of a row, for MXFP4 and NVFP4 expert weights, every token against the oracle
+32-element blocks of a row, for MXFP4 and NVFP4 expert weights, and the tensor-core decode GEMMs
+(MXFP4 weights with their tensor-core copies, up to 16 tokens), every token against the oracle
 (Muse Spark Open explainer, section 9: gate, up and down per expert, weighted sum; section 11:
 4-bit block-scaled weights), with the layer call's permutation bit-exact (section 12)."""
 import numpy as np
@@ -22,19 +23,24 @@ MID = IN.small_config("wide_4096", T=8, d=4096, E=64, k=8, I=1536, index=72, zip
 _layers = {}
 
 
-def get_layer(cfg, wfmt):
-    key = (cfg.name, wfmt)
+def get_layer(cfg, wfmt, mma):
+    key = (cfg.name, wfmt, mma)
     if key not in _layers:
         _layers.clear()
         torch.cuda.empty_cache()
-        _layers[key] = DeviceLayer(cfg, mma_layouts=False, wfmt=wfmt)
+        _layers[key] = DeviceLayer(cfg, mma_layouts=mma, wfmt=wfmt)
     return _layers[key]
 
 
-@pytest.mark.parametrize("wfmt", ["mxfp4", "nvfp4"])
+# (weight format, tensor-core weight copies): MXFP4 on the GEMVs, MXFP4 on the tensor-core decode
+# GEMMs (up to 16 tokens), NVFP4 (GEMVs only)
+PATHS = [("mxfp4", False), ("mxfp4", True), ("nvfp4", False)]
+
+
 @pytest.mark.parametrize("cfg,T", [(WIDE, 5), (WIDE, 8), (WIDE, 16), (MID, 8), (MID, 7)])
-def test_wide_rows_match_oracle(wfmt, cfg, T):
-    layer = get_layer(cfg, wfmt)
+@pytest.mark.parametrize("wfmt,mma", PATHS)
+def test_wide_rows_match_oracle(wfmt, mma, cfg, T):
+    layer = get_layer(cfg, wfmt, mma)
     d, E, k, I = cfg.d, cfg.E, cfg.k, cfg.I
     xb = IN.make_x(cfg, call=T)[:T]
     ws = make_workspace(T, d, E, k, I, B.MOE_ACT_BF16)
