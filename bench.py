@@ -365,7 +365,9 @@ def run_gpu(args, cfg, rank, world, local):
                                          lat.flops_per_step() if lat is not None else 0.0),
         "roofline": roof,
         "e2e": e2e,
-        "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None, lat is not None) * args.steps,
+        "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None, lat is not None,
+                                          fmt == B.MOE_ACT_BF16 and args.weights == "mxfp4"
+                                          and B.moe_decode_pieces_bytes(T, dl, 0) > 0 and I % 256 == 0) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
         "_parity_y": parity_y,
@@ -491,13 +493,15 @@ class Latent:
         return B.MOE_OK
 
 
-def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False):
+def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_decode=False):
     # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
     # gate/up, down+sum; with the expert normalisation the down GEMV and the (normalising) sum are
     # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum.
     # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).
     proj = (2 if fmt == 0 else 4) * 2 if latent else 0
     if fmt == 0:
+        if mma_decode:  # route (+ permute), token pieces, the fused expert kernel (+ separate sum)
+            return (1 if T <= 8 else 5) + 2 + (0 if (T <= 4 and not expert_norm) else 1) + proj
         return (3 if T <= 8 else 7) + (1 if expert_norm else 0) + proj
     return 10 + proj
 
@@ -524,6 +528,8 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
     active = []
     if fmt != B.MOE_ACT_BF16:
         return kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n)
+    if args.weights == "mxfp4" and B.moe_decode_pieces_bytes(T, d, 0) > 0 and I % 256 == 0:
+        return kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n)
     st = stream.cuda_stream
     with torch.cuda.stream(stream):
         for s in range(n + 3):
@@ -554,6 +560,66 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
             "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
             "algorithmic_bytes_per_launch": per_launch, "avg_launch_us": round(avg_ms * 1e3, 3),
             "launches_timed": n, "peak_source": pk["source"] + " (HBM copy bandwidth)"}
+
+
+def kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n):
+    """bf16 decode path on the tensor cores: the fused expert kernel (umma_decode_layer_kernel: gate/up
+    + SwiGLU + down, and the weighted sum for up to four tokens) timed with CUDA events on its stream
+    through moe_expert_ffn_decode, after moe_route and moe_permute (which writes the token pieces).
+    Algorithmic bytes per launch: every touched expert's gate, up and down weights, plus y."""
+    import numpy as np
+    import torch
+
+    from bit_expert_ffn_moe_gb300 import binding as B
+    from bit_expert_ffn_moe_gb300.layer import make_workspace
+
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    P = T * k
+    fmt = B.MOE_ACT_BF16
+    ws = make_workspace(T, d, E, k, I, fmt, dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    u8 = dict(dtype=torch.uint8, device=dev)
+    ids, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts, offsets, perm, inv = torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(P, **i32), \
+        torch.empty(P, **i32)
+    xa = torch.empty(B.moe_decode_pieces_bytes(T, d, 0), **u8)
+    xa_s = torch.empty(B.moe_decode_pieces_bytes(T, d, 1), **u8)
+    y_perm = torch.empty((P, d), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if T <= 4 else None
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    active = []
+    st = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        for s in range(n + 3):
+            L = layers[s % len(layers)]
+            x = xs[s % xs.shape[0]]
+            B.moe_route(x, L.W_r, L.b, T, d, E, k, ids, w, ws, stream=st)
+            B.moe_permute(x, ids, T, d, E, k, fmt, counts, offsets, perm, inv, xa, xa_s, ws, stream=st)
+            if s >= 3:
+                evs[s - 3][0].record(stream)
+            B.moe_expert_ffn_decode(xa, xa_s, perm, offsets, inv, w, T, d, E, k, I, L.weights, y_perm, y, ws,
+                                    stream=st)
+            if s >= 3:
+                evs[s - 3][1].record(stream)
+                active.append(torch.count_nonzero(counts))
+    stream.synchronize()
+    if B.moe_get_device_status(ws) != B.MOE_OK:
+        raise RuntimeError("device-side error in the decode roofline loop")
+    avg_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    n_act = float(np.mean([int(a.item()) for a in active]))
+    per_launch = n_act * expert_read_bytes(d, I, "mxfp4") + T * d * 2
+    achieved = per_launch / (avg_ms / 1e3) / 1e9
+    traffic = ncu_traffic("umma_decode_layer.md", ["bit_expert_ffn_moe_gb300/csrc/decode_mma.cu",
+                                                   "bit_expert_ffn_moe_gb300/csrc/tcgen05.cuh",
+                                                   "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
+    return {"kernel": "umma_decode_layer_kernel (tcgen05 kind::mxf4 gate/up + SwiGLU + down%s, decode)"
+                      % (" + weighted sum" if y is not None else ""),
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / pk["hbm_gbs"], 4), "traffic": traffic,
+            "algorithmic_bytes_per_launch": per_launch, "avg_launch_us": round(avg_ms * 1e3, 3),
+            "launches_timed": n, "peak_source": pk["source"] + " (HBM copy bandwidth)",
+            "timing": "each launch bracketed by events through the step API (eager; in the timed graph the "
+                      "launch also overlaps its predecessors through programmatic dependent launch)"}
 
 
 def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):

@@ -34,6 +34,7 @@ EXPORTED = (
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
     "moe_dense_workspace_size", "moe_dense_linear", "moe_nvfp4_pack", "moe_nvfp4_unpack", "moe_workspace_routing",
+    "moe_decode_pieces_bytes", "moe_expert_ffn_decode",
 )
 
 
@@ -92,6 +93,8 @@ _SIGS = {
     "moe_selftest_wait_timeout": (I32, [P, SZ, I32, P]),
     "moe_nvfp4_pack": (I32, [P, I64, I64, I64, P, P, P, P]),
     "moe_nvfp4_unpack": (I32, [P, P, P, I64, I64, I64, P, P]),
+    "moe_decode_pieces_bytes": (SZ, [I32, I32, I32]),
+    "moe_expert_ffn_decode": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, WP, P, P, P, SZ, P]),
     "moe_workspace_routing": (I32, [P, SZ, I32, I32, I32, I32, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P),
                                     ctypes.POINTER(P), ctypes.POINTER(P)]),
 }
@@ -229,6 +232,18 @@ def _ws_bytes(ws, ws_bytes):
 def moe_route(x, W_r, b, T, d, E, k, ids, w, ws, ws_bytes=None, stream=None):
     _check("moe_route", load().moe_route(_p(x), _p(W_r), _p(b), T, d, E, k, _p(ids), _p(w), _p(ws),
                                          _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_decode_pieces_bytes(T, d, scales):
+    return load().moe_decode_pieces_bytes(T, d, int(scales))
+
+
+def moe_expert_ffn_decode(xa, xa_s, perm_token, offsets, inv_pos, w, T, d, E, k, I, W: moe_expert_weights, y_perm, y,
+                          ws, ws_bytes=None, stream=None):
+    _check("moe_expert_ffn_decode",
+           load().moe_expert_ffn_decode(_p(xa), _p(xa_s), _p(perm_token), _p(offsets), _p(inv_pos), _p(w), T, d, E, k,
+                                        I, ctypes.byref(W), _p(y_perm), _p(y), _p(ws), _ws_bytes(ws, ws_bytes),
+                                        _stream(stream)))
 
 
 def moe_workspace_routing(ws, T, d, E, k, I, fmt, ws_bytes=None):

@@ -45,7 +45,7 @@ moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
 
 namespace {
 
-constexpr int kAbiVersion = 8;
+constexpr int kAbiVersion = 9;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -264,12 +264,45 @@ moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int 
     MOE_TRY(check_device());
     cudaStream_t st = (cudaStream_t)stream;
     PlanView plan = plan_view(ws, L, E);
+    const bool pieces = fmt == MOE_ACT_BF16 && xa != nullptr && xa_s != nullptr;
+    if (pieces && (!mma_decode_shape(T, d, 256) || !x || !aligned(x, 16) || !aligned(xa, 16)))
+        return T == 0 ? MOE_OK : MOE_ERR_UNSUPPORTED_SHAPE;
     MOE_CUDA(launch_permute(ids, T, E, k, counts, offsets, perm_token, inv_pos, plan, st, false));
     if (fmt == MOE_ACT_MXFP4)
         MOE_CUDA(launch_act_quant_gather(x, T, d, E, k, offsets, perm_token, plan, L.pad_rows,
                                          reinterpret_cast<uint8_t*>(at(ws, L.xq)),
                                          reinterpret_cast<uint8_t*>(at(ws, L.xs)), xa, xa_s, st, true));
+    else if (pieces && T > 0)
+        MOE_CUDA(launch_x_pieces(x, T, d, xa, xa_s, st, false));
     return MOE_OK;
+}
+
+size_t moe_decode_pieces_bytes(int T, int d, int scales) {
+    if (!mma_decode_shape(T, d, 256)) return 0;
+    return scales ? mma_scale_bytes(128, d) : (size_t)128 * d / 2;
+}
+
+moe_status moe_expert_ffn_decode(const uint8_t* xa, const uint8_t* xa_s, const int32_t* perm_token,
+                                 const int32_t* offsets, const int32_t* inv_pos, const float* w, int T, int d, int E,
+                                 int k, int I, const moe_expert_weights* W, uint16_t* y_perm, uint16_t* y, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_shape(T, d, E, k, I, MOE_ACT_BF16));
+    if (T == 0) return MOE_OK;
+    MOE_TRY(check_weights(W, MOE_ACT_BF16, true, true));
+    if (!mma_decode_supported(T, d, E, k, I, W)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (y != nullptr && !mma_decode_fused_sum(T, d)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!xa || !xa_s || !perm_token || !offsets || !y_perm || !aligned(xa, 16) || !aligned(y_perm, 16))
+        return MOE_ERR_INVALID_ARG;
+    if (y != nullptr && (!inv_pos || !w || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, I, MOE_ACT_BF16);
+    MOE_TRY(check_ws(ws, ws_bytes, L));
+    MOE_TRY(check_device());
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
+    return from_cuda(launch_mma_decode(xa, xa_s, reinterpret_cast<uint8_t*>(at(ws, L.dha)),
+                                       reinterpret_cast<uint8_t*>(at(ws, L.dha_s)),
+                                       reinterpret_cast<float*>(at(ws, L.dpart)), plan_view(ws, L, E), offsets,
+                                       perm_token, T, d, E, k, I, W, y_perm, inv_pos, w, y, ctrl,
+                                       (cudaStream_t)stream, false));
 }
 
 moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint8_t* xa_s, moe_act_fmt fmt,
@@ -379,8 +412,8 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
         uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
         MOE_CUDA(launch_x_pieces(x, T, d, dxa, dxa_s, st, true));
         const bool fused = !norm && mma_decode_fused_sum(T, d);
-        MOE_CUDA(launch_mma_decode(dxa, dxa_s, dha, dha_s, plan, offsets, perm, T, d, E, k, I, W, y_perm, inv, w_b,
-                                   fused ? y : nullptr, ctrl, st, true));
+        MOE_CUDA(launch_mma_decode(dxa, dxa_s, dha, dha_s, reinterpret_cast<float*>(at(ws, L.dpart)), plan, offsets,
+                                   perm, T, d, E, k, I, W, y_perm, inv, w_b, fused ? y : nullptr, ctrl, st, true));
         if (norm) MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
         else if (!fused) MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
         return MOE_OK;

@@ -24,6 +24,7 @@ constexpr int kTokTile = 128;   // token tile (MMA N) of the tcgen05 grouped GEM
 // again).
 constexpr int kDecTickets = 64;
 constexpr int kDecSlots = 512;
+constexpr int kDecSplitCounters = 1024;  // (slot, block) arrival counters of split gate/up tiles
 struct Ctrl {
     int status;
     unsigned route_ticket;
@@ -31,9 +32,10 @@ struct Ctrl {
     unsigned dec_done;
     unsigned dec_ticket[kDecTickets];
     unsigned dec_ready[kDecSlots];
+    unsigned dec_split[kDecSplitCounters];
     int pad[444];
 };
-static_assert(sizeof(Ctrl) == 4096, "control block size");
+static_assert(sizeof(Ctrl) == 8192, "control block size");
 
 // Per-call plan written by the permutation and read by the expert kernels (int32 words).
 struct PlanView {
@@ -48,6 +50,7 @@ struct WsLayout {
     size_t ctrl = 0, logits = 0, plan = 0, ids = 0, w = 0, counts = 0, offsets = 0, perm = 0, inv = 0, row_w = 0,
            xq = 0, xs = 0, xa = 0, xa_s = 0, h = 0, h_s = 0, y_perm = 0, total = 0;
     size_t dxa = 0, dxa_s = 0, dha = 0, dha_s = 0;  // decode on the tensor cores: x and h pieces
+    size_t dpart = 0;                                // its split gate/up tiles' fp32 partial sums
     int64_t pad_rows = 0;
 };
 
@@ -55,6 +58,21 @@ struct WsLayout {
 // the block-scaled FP4 MMAs as 8 MXFP4 pieces each (rows of one 128-row operand tile).
 constexpr int kMmaDecodeMaxT = 16;
 inline bool mma_decode_shape(int T, int d, int I) { return T >= 1 && T <= kMmaDecodeMaxT && d % 256 == 0 && I % 256 == 0; }
+// K splits of a gate/up tile (1 = whole tiles): with one or two tokens there are too few gate/up
+// tiles to occupy every SM, so each tile's K range is split into parts of at least 8 K steps
+// whose fp32 partial sums are added by the last part to finish.
+inline int mma_decode_ksplit(int T, int d) {
+    const int kt = d / 256;
+    if (T > 2) return 1;
+    int ks = 1;
+    while (ks < 8 && kt % (2 * ks) == 0 && kt / (2 * ks) >= 8) ks *= 2;
+    return ks;
+}
+// bytes of those partial sums: per token row of the layer, per 128-row block, per part, 128 g + 128 u
+inline size_t mma_decode_part_bytes(int T, int d, int k, int I) {
+    const int ks = mma_decode_ksplit(T, d);
+    return ks > 1 ? (size_t)T * k * (I / 128) * ks * 256 * sizeof(float) : 0;
+}
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -106,6 +124,7 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
             L.dxa_s = take(mma_scale_bytes(128, d));
             L.dha = take(slots * 128 * I / 2);
             L.dha_s = take(slots * mma_scale_bytes(128, I));
+            L.dpart = take(mma_decode_part_bytes(T, d, k, I));
         }
     }
     L.total = off;
@@ -421,10 +440,10 @@ cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, uint8_t* xa, uint8_
 // Both expert GEMMs in one persistent launch: gate/up tiles, then down tiles (each waits for its
 // slot's h operand), expert outputs to y_perm; with y != nullptr (T <= 4, d <= 64 * 256) the weighted
 // sum y[t] = sum_j w[t][j] y_perm[inv_pos[t k + j]] (fp32, slot order, then bf16) is fused too.
-cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, PlanView plan,
-                              const int32_t* offsets, const int32_t* perm_token, int T, int d, int E, int k, int I,
-                              const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos, const float* w,
-                              uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl);
+cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, float* part,
+                              PlanView plan, const int32_t* offsets, const int32_t* perm_token, int T, int d, int E,
+                              int k, int I, const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos,
+                              const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl);
 bool mma_decode_fused_sum(int T, int d);
 
 cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets,

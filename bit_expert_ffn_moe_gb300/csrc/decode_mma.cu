@@ -124,6 +124,9 @@ __device__ __forceinline__ float absmax8(const float (&r)[8]) {
 // x pieces: one thread per (token, 32-element block); rows 8t + p of the [128][d] A tile.
 __global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restrict__ x, int T, int d, uint8_t* xa,
                                                        uint8_t* xa_s) {
+    // the next kernel (the expert GEMMs) may start its set-up now; it waits for this kernel, and so
+    // for the routing, before it reads anything either produced
+    pdl_launch_dependents();
     const int nb = d / 32;
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < T * nb) {
@@ -179,6 +182,8 @@ struct DecArgs {
     const float* w;             //   [T*k] gate weights
     uint16_t* y;                //   bf16 [T][d], or null (the sum is a separate launch)
     Ctrl* ctrl;
+    float* part;                // split gate/up tiles: fp32 partial sums [T*k][I/128][ks][256]
+    int ks;                     // K parts per gate/up tile (1: whole tiles)
 };
 
 // Sum of the accumulator words of one 32-column tensor-memory load over the eight lanes of a lane
@@ -251,11 +256,14 @@ __device__ __forceinline__ void fused_sum(const DecArgs& a, int p, int n_act, in
     if (lane == 0) a.ctrl->dec_ticket[p] = 0u;  // ready for the next call
 }
 
-// A tile of the decode layer: gate/up (slot u, block p of 128 intermediate rows; K = d) or down
-// (slot u, block p of 256 output features; K = I).
+// A tile of the decode layer: gate/up (slot u, block p of 128 intermediate rows, K part ks of
+// args.ks; K = d) or down (slot u, block p of 256 output features; K = I).
 struct DecTile {
     bool up;
-    int u, p, e, KT;
+    int u, p, ks, e;
+    int KT;    // K steps of this tile
+    int KTT;   // K tiles of a whole row of the operands
+    int kbase; // first K tile of this tile
     size_t a_rb, rb0, rb1;  // 128-row blocks: A operand, B rows 0..127, B rows 128..255
     const uint8_t *aq, *as, *bq0, *bs0, *bq1, *bs1;
 };
@@ -264,11 +272,23 @@ __device__ __forceinline__ DecTile dec_tile(int t, const DecArgs& a, const int32
     DecTile D;
     const int nbu = a.I / 128, nbd = a.d / 256;
     D.up = t < n_up;
-    const int l = D.up ? t : t - n_up, nb = D.up ? nbu : nbd;
-    D.u = l / nb;
-    D.p = l % nb;
+    if (D.up) {
+        D.u = t / (nbu * a.ks);
+        const int rem = t % (nbu * a.ks);
+        D.p = rem / a.ks;
+        D.ks = rem % a.ks;
+        D.KTT = a.d / 256;
+        D.KT = D.KTT / a.ks;
+        D.kbase = D.ks * D.KT;
+    } else {
+        const int l = t - n_up;
+        D.u = l / nbd;
+        D.p = l % nbd;
+        D.ks = 0;
+        D.KTT = D.KT = a.I / 256;
+        D.kbase = 0;
+    }
     D.e = s_act[D.u];
-    D.KT = (D.up ? a.d : a.I) / 256;
     if (D.up) {
         D.a_rb = 0;
         D.rb0 = D.rb1 = (size_t)D.e * nbu + D.p;
@@ -290,21 +310,12 @@ __device__ __forceinline__ DecTile dec_tile(int t, const DecArgs& a, const int32
     return D;
 }
 
-// Chunk c of a gate/up tile's columns (one MX block of h, 32 features): lane pl of the token's
-// group gets features 4pl .. 4pl+3, forms h and writes its part of the block's 8 pieces.
-__device__ __forceinline__ void up_chunk(const DecArgs& args, const DecTile& D, uint32_t (&gv)[32], uint32_t (&uv)[32],
-                                         int half, int c, int lane, int j, size_t row0) {
+// The 8 pieces of four bf16 h values per lane: lanes of one 8-lane group hold one MX block of h
+// (features 4 (lane & 7) .. + 3 of the block); written to rows row0 .. row0 + 7, block blk of the
+// slot's down-GEMM operand (nothing is written when store is false).
+__device__ __forceinline__ void h_pieces(const DecArgs& args, float (&r)[4], int lane, int blk, size_t row0,
+                                         bool store) {
     const int pl = lane & 7;
-    group8_reduce32(gv, lane);
-    group8_reduce32(uv, lane);
-    float r[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float g = __uint_as_float(gv[i]), u = __uint_as_float(uv[i]);
-        const float hv = __fdividef(g, 1.f + __expf(-g)) * u;  // SiLU(g) * u
-        r[i] = bf16_bits_to_f32(f32_to_bf16_bits(hv));      // h as bf16
-    }
-    const int blk = 4 * D.p + 2 * half + c;
 #pragma unroll 1
     for (int pc = 0; pc < kPieces; ++pc) {
         float amax = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
@@ -313,12 +324,62 @@ __device__ __forceinline__ void up_chunk(const DecArgs& args, const DecTile& D, 
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
         uint32_t sb;
         const uint32_t codes = piece4(r, amax, sb);
-        if (j >= 0) {
+        if (store) {
             const size_t row = row0 + pc;
             *reinterpret_cast<uint16_t*>(args.ha + mma_tile_offset((int64_t)row, blk, args.I) + 2 * pl) =
                 (uint16_t)codes;
             if (pl == 0) args.ha_s[mma_scale_offset((int64_t)row, blk, args.I)] = (uint8_t)sb;
         }
+    }
+}
+
+__device__ __forceinline__ float swiglu_bf16(float g, float u) {
+    const float hv = __fdividef(g, 1.f + __expf(-g)) * u;  // SiLU(g) * u
+    return bf16_bits_to_f32(f32_to_bf16_bits(hv));      // h as bf16
+}
+
+// Chunk c of a gate/up tile's columns (32 features = one MX block of h): lane pl of the token's
+// group gets features 4pl .. 4pl+3.  Whole tiles: form h and write its pieces.  Split tiles:
+// store this part's fp32 sums of g and u for the last part to add.
+__device__ __forceinline__ void up_chunk(const DecArgs& args, const DecTile& D, uint32_t (&gv)[32], uint32_t (&uv)[32],
+                                         int half, int c, int lane, int j, int r0, size_t row0) {
+    group8_reduce32(gv, lane);
+    group8_reduce32(uv, lane);
+    const int f = 64 * half + 32 * c + 4 * (lane & 7);  // feature within the tile's 128
+    if (args.ks > 1) {
+        if (j >= 0) {
+            float* dst = args.part + (((size_t)(r0 + j) * (args.I / 128) + D.p) * args.ks + D.ks) * 256;
+            *reinterpret_cast<float4*>(dst + f) = make_float4(__uint_as_float(gv[0]), __uint_as_float(gv[1]),
+                                                              __uint_as_float(gv[2]), __uint_as_float(gv[3]));
+            *reinterpret_cast<float4*>(dst + 128 + f) = make_float4(__uint_as_float(uv[0]), __uint_as_float(uv[1]),
+                                                                    __uint_as_float(uv[2]), __uint_as_float(uv[3]));
+        }
+        return;
+    }
+    float r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = swiglu_bf16(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
+    h_pieces(args, r, lane, 4 * D.p + 2 * half + c, row0, j >= 0);
+}
+
+// Split gate/up tiles: the last of the 8 x ks warp arrivals of (slot u, block p) adds the ks partial
+// sums of each of the expert's tokens in part order, forms h and writes its pieces; lane group
+// lane >> 3 takes MX block (lane >> 3) of the block's 128 features.
+__device__ __forceinline__ void up_finish_split(const DecArgs& args, const DecTile& D, int lane, int r0, int cnt) {
+    const int nbu = args.I / 128, g8 = lane >> 3, f = 32 * g8 + 4 * (lane & 7);
+    for (int j = 0; j < cnt; ++j) {
+        const float* src = args.part + ((size_t)(r0 + j) * nbu + D.p) * args.ks * 256;
+        float g[4] = {0.f, 0.f, 0.f, 0.f}, u[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q = 0; q < args.ks; ++q) {
+            const float4 gq = __ldcg(reinterpret_cast<const float4*>(src + (size_t)q * 256 + f));
+            const float4 uq = __ldcg(reinterpret_cast<const float4*>(src + (size_t)q * 256 + 128 + f));
+            g[0] += gq.x; g[1] += gq.y; g[2] += gq.z; g[3] += gq.w;
+            u[0] += uq.x; u[1] += uq.y; u[2] += uq.z; u[3] += uq.w;
+        }
+        float r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r[i] = swiglu_bf16(g[i], u[i]);
+        h_pieces(args, r, lane, 4 * D.p + g8, (size_t)D.u * 128 + 8 * (size_t)j, true);
     }
 }
 
@@ -363,14 +424,27 @@ __device__ __forceinline__ void epilogue_up(const DecArgs& args, const DecTile& 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(acc_empty);
             }
-            up_chunk(args, D, gv, uv, half, c, lane, j, row0);
+            up_chunk(args, D, gv, uv, half, c, lane, j, r0, row0);
         }
     } else {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty);
     }
-    // publish: this warp's share of the slot's h pieces is in place (every warp arrives)
+    if (args.ks > 1) {
+        // this warp's partial sums are stored; the last of the tile's 8 x ks warp arrivals finishes it
+        __threadfence();
+        __syncwarp();
+        unsigned* counter = &ctrl->dec_split[D.u * (args.I / 128) + D.p];
+        unsigned last = 0;
+        if (lane == 0) last = atomicAdd(counter, 1u) == (unsigned)(kEpiWarps * args.ks - 1);
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (!last) return;
+        __threadfence();
+        up_finish_split(args, D, lane, r0, cnt);
+        if (lane == 0) *counter = 0u;  // ready for the next call
+    }
+    // publish: h pieces in place (whole tiles: every warp's share; split tiles: the block)
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __threadfence();
     __syncwarp();
@@ -465,22 +539,20 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
-    pdl_wait();  // routing plan and token pieces come from the preceding kernels
+    pdl_wait();  // the routing plan and the token pieces come from the preceding kernels
     const int n_act = args.plan.scalars[0];
     for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
         s_off[i] = args.offsets[i];
         if (i < args.E) s_act[i] = args.plan.active[i];
     }
-    __syncthreads();
-    const int n_pairs = s_off[args.E];
-    for (int i = threadIdx.x; i < n_pairs; i += blockDim.x) s_perm[i] = args.perm_token[i];
+    for (int i = threadIdx.x; i < args.T * args.k; i += blockDim.x) s_perm[i] = args.perm_token[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     const int nbu = args.I / 128;
-    const int n_up = n_act * nbu, n_tiles = n_up + n_act * (args.d / 256);
+    const int n_up = n_act * nbu * args.ks, n_tiles = n_up + n_act * (args.d / 256);
 
     // next tile id from the queue (every role but the claiming producer); -1 ends the loop
     auto next_tile = [&](int q, bool arrive) -> int {
@@ -504,17 +576,19 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
                 mbar_arrive(&tq_full[q % kTileQ]);
                 if (t < 0) break;
                 const DecTile D = dec_tile(t, args, s_act, n_up);
-                const int apr = D.KT * 2;  // scale atoms per 128-row block
+                const int apr = D.KTT * 2;  // scale atoms per 128-row block
+                const int kt0 = t % D.KT;   // concurrent tiles start at different K steps
                 bool ok = true;
-                for (int kt = 0; kt < D.KT; ++kt, ++kiter) {
+                for (int kk = 0; kk < D.KT; ++kk, ++kiter) {
                     const int s = kiter % kStages;
+                    const int kt = D.kbase + (kk + kt0 < D.KT ? kk + kt0 : kk + kt0 - D.KT);
                     if (!mbar_wait(&empty[s], ((uint32_t)(kiter / kStages) & 1u) ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&full_b[s], 2 * kTile + 4 * kAtom);
-                    bulk_load(stage_b(s), D.bq0 + (D.rb0 * D.KT + kt) * kTile, kTile, &full_b[s]);
-                    bulk_load(stage_b(s) + kTile, D.bq1 + (D.rb1 * D.KT + kt) * kTile, kTile, &full_b[s]);
+                    bulk_load(stage_b(s), D.bq0 + (D.rb0 * D.KTT + kt) * kTile, kTile, &full_b[s]);
+                    bulk_load(stage_b(s) + kTile, D.bq1 + (D.rb1 * D.KTT + kt) * kTile, kTile, &full_b[s]);
                     bulk_load(stage_sfb(s), D.bs0 + (D.rb0 * apr + 2 * kt) * kAtom, 2 * kAtom, &full_b[s]);
                     bulk_load(stage_sfb(s) + 2 * kAtom, D.bs1 + (D.rb1 * apr + 2 * kt) * kAtom, 2 * kAtom, &full_b[s]);
                 }
@@ -539,10 +613,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
                 const int cnt = s_off[D.e + 1] - s_off[D.e];
                 const int rows = 8 * (D.up ? args.T : cnt);
                 const uint32_t a_bytes = (uint32_t)(rows < 128 ? rows : 128) * 128;
+                const int kt0 = t % D.KT;
                 bool ok = true;
                 if (!D.up) {
-                    // the slot's h pieces: every epilogue warp of every gate/up tile of the slot arrives
-                    const unsigned need = (unsigned)(kEpiWarps * nbu);
+                    // the slot's h pieces: published by every epilogue warp of every gate/up tile of the
+                    // slot (whole tiles), or once per 128-row block (split tiles)
+                    const unsigned need = (unsigned)(args.ks > 1 ? nbu : kEpiWarps * nbu);
                     const long long t0 = clock64();
                     while (ld_acquire_u32(&ctrl->dec_ready[D.u]) < need) {
                         if (*abort_flag || clock64() - t0 > kWaitCycles) {
@@ -555,15 +631,16 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
                     }
                     asm volatile("fence.proxy.async.global;" ::: "memory");  // generic stores -> bulk copies
                 }
-                for (int kt = 0; kt < D.KT && ok; ++kt, ++kiter) {
+                for (int kk = 0; kk < D.KT && ok; ++kk, ++kiter) {
                     const int s = kiter % kStages;
+                    const int kt = D.kbase + (kk + kt0 < D.KT ? kk + kt0 : kk + kt0 - D.KT);
                     if (!mbar_wait(&empty[s], ((uint32_t)(kiter / kStages) & 1u) ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     mbar_arrive_expect_tx(&full_a[s], a_bytes + 2 * kAtom);
-                    bulk_load(stage_a(s), D.aq + (D.a_rb * D.KT + kt) * kTile, a_bytes, &full_a[s]);
-                    bulk_load(stage_sfa(s), D.as + (D.a_rb * D.KT * 2 + 2 * kt) * kAtom, 2 * kAtom, &full_a[s]);
+                    bulk_load(stage_a(s), D.aq + (D.a_rb * D.KTT + kt) * kTile, a_bytes, &full_a[s]);
+                    bulk_load(stage_sfa(s), D.as + (D.a_rb * D.KTT * 2 + 2 * kt) * kAtom, 2 * kAtom, &full_a[s]);
                 }
                 if (!ok) break;
             }
@@ -669,11 +746,14 @@ cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, uint8_t* xa, uint8_
     return launch_kernel((const void*)x_pieces_kernel, dim3((n + 255) / 256), dim3(256), 0, st, pdl, args);
 }
 
-cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, PlanView plan,
-                              const int32_t* offsets, const int32_t* perm_token, int T, int d, int E, int k, int I,
-                              const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos, const float* w,
-                              uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl) {
+cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, float* part,
+                              PlanView plan, const int32_t* offsets, const int32_t* perm_token, int T, int d, int E,
+                              int k, int I, const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos,
+                              const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl) {
     DecArgs a = {};
+    const int slots = T * k < E ? T * k : E;
+    a.ks = slots * (I / 128) <= kDecSplitCounters ? mma_decode_ksplit(T, d) : 1;
+    a.part = part;
     a.xa = xa;
     a.xa_s = xa_s;
     a.ha = ha;

@@ -175,17 +175,25 @@ route_decode_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_
     __shared__ int s_off[kMaxE + 1];
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    pdl_wait();
-    // the next kernel may start now: what it reads before its own dependency wait (x) is ready
-    pdl_launch_dependents();
     // Chunk c holds the 4-element groups [c*Gc, (c+1)*Gc) of the row (clamped to d/4); Gc is a
     // multiple of 32, so group g stays with lane g % 32 and the fixed summation order holds.
     const int ng = d / 4;
     const int Gc = ((ng + kRouteChunks - 1) / kRouteChunks + 31) / 32 * 32;
+    // the router weights do not depend on the preceding kernel: their copies start before its wait
+    // (commit groups 0 .. kRouteChunks-1), the token rows after it (groups kRouteChunks ..); chunk c
+    // is complete once at most kRouteChunks - 1 - c groups are pending
 #pragma unroll
     for (int c = 0; c < kRouteChunks; ++c) {
         const int lo = min(c * Gc, ng), hi = min(lo + Gc, ng);
         for (int g = lo + tid; g < hi; g += blockDim.x) cp_async16(Ws + 4 * g, W_r + (size_t)e * d + 4 * g);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    pdl_wait();
+    // the next kernel may start now: what it reads before its own dependency wait (x) is ready
+    pdl_launch_dependents();
+#pragma unroll
+    for (int c = 0; c < kRouteChunks; ++c) {
+        const int lo = min(c * Gc, ng), hi = min(lo + Gc, ng);
         const int n8 = (hi - lo) / 2;  // 8-element pieces of a token row in this chunk
         for (int i = tid; i < T * n8; i += blockDim.x) {
             const int t = i / n8, p8 = lo / 2 + i % n8;

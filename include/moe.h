@@ -112,7 +112,7 @@ const char* moe_status_string(moe_status s);
 
 /* ABI version of this header (incremented on changes to the entry points or their structs);
  * moe_abi_version() returns the library's, which a caller compares with MOE_ABI_VERSION. */
-#define MOE_ABI_VERSION 8
+#define MOE_ABI_VERSION 9
 int moe_abi_version(void);
 
 /* Description of the CUDA error behind the calling thread's last MOE_ERR_CUDA (static string). */
@@ -251,8 +251,12 @@ moe_status moe_route_noalloc(const uint16_t* x, const float* W_r, const float* b
  * (expert e's rows start at a multiple of 128; padding rows are zero): xa in the tensor-core
  * code tiles (moe_padded_rows*d/2 bytes) and xa_s in the tensor-core scale layout
  * (moe_mxfp4_mma_scale_bytes(moe_padded_rows, d) bytes).  For MOE_ACT_BF16, xa and xa_s are
- * unused (may be NULL).  Writes the per-expert plan (padded offsets, tile table) into ws for
- * the expert calls that follow. */
+ * unused (may be NULL), except that when both are given (1 <= T <= 16, d % 256 == 0; buffers of
+ * moe_decode_pieces_bytes(T, d, 0) and (T, d, 1) bytes, 16-byte aligned) the call also writes
+ * the activation operand of moe_expert_ffn_decode: each token row as 8 MXFP4 pieces (see
+ * moe_layer_forward), rows 8t .. 8t+7 of a 128-row tensor-core tile (codes in xa, scales in
+ * xa_s; the other rows are not written).  Writes the per-expert plan (padded offsets, tile table)
+ * into ws for the expert calls that follow. */
 moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int E, int k, moe_act_fmt fmt,
                        int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_pos,
                        uint8_t* xa, uint8_t* xa_s, void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -276,6 +280,24 @@ moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint
 moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, const int32_t* perm_token,
                            const int32_t* offsets, int T, int d, int E, int k, int I, const moe_expert_weights* W,
                            uint16_t* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Bytes of the pieces operand moe_permute writes for moe_expert_ffn_decode: scales = 0 the codes,
+ * scales = 1 the scale atoms.  0 when 1 <= T <= 16 and d % 256 == 0 do not hold. */
+size_t moe_decode_pieces_bytes(int T, int d, int scales);
+
+/* Both expert GEMMs of a small batch on the block-scaled FP4 tensor cores, in one persistent
+ * launch (the kernels moe_layer_forward runs for MOE_ACT_BF16 with MXFP4 weights carrying their
+ * tensor-core copies): gate/up with SwiGLU (section 9) on the token pieces xa / xa_s from
+ * moe_permute, h rounded to bf16 and fed to the down GEMM as its own 8 pieces, the expert
+ * outputs rounded to bf16 into y_perm [T*k][d] (compact permuted order).  With y != NULL
+ * (T <= 4) the weighted sum of moe_combine is fused and written to y bf16 [T][d] (inv_pos and w
+ * as moe_combine takes them).  Needs the plan that moe_permute wrote into ws (laid out for the
+ * same T, d, E, k, I with MOE_ACT_BF16).  1 <= T <= 16, d % 256 == 0, I % 256 == 0 and MXFP4
+ * weights with their tensor-core copies (MOE_ERR_UNSUPPORTED_SHAPE otherwise). */
+moe_status moe_expert_ffn_decode(const uint8_t* xa, const uint8_t* xa_s, const int32_t* perm_token,
+                                 const int32_t* offsets, const int32_t* inv_pos, const float* w, int T, int d,
+                                 int E, int k, int I, const moe_expert_weights* W, uint16_t* y_perm, uint16_t* y,
+                                 void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Weighted sum (section 9): y[t] = sum_j w[t][j] * y_perm[inv_pos[t*k+j]] accumulated in fp32
  * in slot order j = 0..k-1, stored as bf16 [T][d].  inv_pos comes from moe_permute; an entry

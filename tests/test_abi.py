@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 8
+    assert B.moe_abi_version() == 9
     header = open(os.path.join(ROOT, "include", "moe.h")).read()
     assert int(re.search(r"#define MOE_ABI_VERSION (\d+)", header).group(1)) == B.moe_abi_version()
     assert B.status_string(0) == "MOE_OK"

@@ -127,3 +127,43 @@ def test_bad_arguments_are_rejected():
         B.moe_layer_forward(x, layer.W_r, layer.b, 4, cfg.d, cfg.E, cfg.E + 1, cfg.I, layer.weights,
                             B.MOE_ACT_BF16, y, None, None, ws)
     assert e.value.status == B.MOE_ERR_UNSUPPORTED_SHAPE
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "spec_verify", "ring_t3", "ring_t2"])
+def test_tensor_core_step_calls_equal_layer_call(name):
+    """moe_route -> moe_permute (with the pieces operand) -> moe_expert_ffn_decode (-> moe_combine
+    beyond four tokens) gives the layer call's output bit for bit, and the expert outputs match the
+    oracle's intermediates."""
+    layer = get_layer(name, mma=True)
+    cfg = layer.cfg
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    P = T * k
+    xb = IN.make_x(cfg, call=4)
+    x = bits_to_device(xb)
+    ws = make_workspace(T, d, E, k, I, B.MOE_ACT_BF16)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    ids, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device="cuda")
+    counts, offsets, perm, inv = (torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(P, **i32),
+                                  torch.empty(P, **i32))
+    xa = torch.empty(B.moe_decode_pieces_bytes(T, d, 0), **u8)
+    xa_s = torch.empty(B.moe_decode_pieces_bytes(T, d, 1), **u8)
+    y_perm = torch.empty((P, d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    B.moe_route(x, layer.W_r, layer.b, T, d, E, k, ids, w, ws)
+    B.moe_permute(x, ids, T, d, E, k, B.MOE_ACT_BF16, counts, offsets, perm, inv, xa, xa_s, ws)
+    fused = T <= 4
+    B.moe_expert_ffn_decode(xa, xa_s, perm, offsets, inv, w, T, d, E, k, I, layer.weights, y_perm,
+                            y if fused else None, ws)
+    if not fused:
+        B.moe_combine(y_perm, inv, w, T, k, d, y)
+    y_layer = layer_forward(layer, x, B.MOE_ACT_BF16)
+    torch.cuda.synchronize()
+    assert B.moe_get_device_status(ws) == B.MOE_OK
+    assert torch.equal(y.view(torch.int16), y_layer.view(torch.int16))
+    ref = O.moe_layer(xb, layer.W_r_host, layer.b_host, k, oracle_expert_weights(cfg, layer.seed), O.ACT_BF16,
+                      want_intermediates=True)
+    rows = inv.cpu().numpy()
+    yp_ref = np.stack([ref["y_perm"][(t, j)] for t in range(T) for j in range(k)])
+    check_outputs(bf16_tensor_to_f32(y_perm)[rows], yp_ref, "y_perm")
+    check_outputs(bf16_tensor_to_f32(y), ref["y"], "y")
