@@ -966,6 +966,9 @@ def main():
                     help="normalise each expert output (RMSNorm over d, eps 1e-6) before the weighted sum")
     ap.add_argument("--weights", choices=["mxfp4", "nvfp4"], default="mxfp4",
                     help="expert weight format (nvfp4: E4M3 scale per 16 values; bf16 activations only)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="number of experts E (0 = the workload's); profiling captures use a smaller E so that "
+                         "few GB stay resident (per-expert shapes, T and k unchanged)")
     ap.add_argument("--cpu-sample-tokens", type=int, default=4)
     ap.add_argument("--ref-budget", type=float, default=90.0)
     args = ap.parse_args()
@@ -973,6 +976,9 @@ def main():
 
     from bit_expert_ffn_moe_gb300 import inputs as IN
     cfg = IN.CONFIGS[args.config]
+    if args.experts:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, E=args.experts, note=cfg.note + " (E=%d for profiling)" % args.experts)
     if args.fmt is None:
         args.fmt = "bf16" if cfg.T <= 8 or args.weights == "nvfp4" else "mxfp4"
     if args.weights == "nvfp4" and args.fmt != "bf16":
