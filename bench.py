@@ -565,7 +565,7 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
 def kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n):
     """bf16 decode path on the tensor cores: the fused expert kernel (umma_decode_layer_kernel: gate/up
     + SwiGLU + down, and the weighted sum for up to four tokens) timed with CUDA events on its stream
-    through moe_expert_ffn_decode, after moe_route and moe_permute (which writes the token pieces).
+    through moe_expert_ffn_decode, after moe_route, moe_permute and moe_decode_pieces (the token pieces).
     Algorithmic bytes per launch: every touched expert's gate, up and down weights, plus y."""
     import numpy as np
     import torch
@@ -594,10 +594,11 @@ def kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n):
             L = layers[s % len(layers)]
             x = xs[s % xs.shape[0]]
             B.moe_route(x, L.W_r, L.b, T, d, E, k, ids, w, ws, stream=st)
-            B.moe_permute(x, ids, T, d, E, k, fmt, counts, offsets, perm, inv, xa, xa_s, ws, stream=st)
+            B.moe_permute(x, ids, T, d, E, k, fmt, counts, offsets, perm, inv, None, None, ws, stream=st)
+            B.moe_decode_pieces(x, T, d, fmt, xa, xa_s, stream=st)
             if s >= 3:
                 evs[s - 3][0].record(stream)
-            B.moe_expert_ffn_decode(xa, xa_s, perm, offsets, inv, w, T, d, E, k, I, L.weights, y_perm, y, ws,
+            B.moe_expert_ffn_decode(xa, xa_s, fmt, perm, offsets, inv, w, T, d, E, k, I, L.weights, y_perm, y, ws,
                                     stream=st)
             if s >= 3:
                 evs[s - 3][1].record(stream)

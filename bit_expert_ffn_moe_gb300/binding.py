@@ -23,6 +23,7 @@ MOE_ERR_DEVICE = 6
 
 MOE_ACT_BF16 = 0
 MOE_ACT_MXFP4 = 1
+MOE_ACT_MXFP8 = 2
 
 MOE_W_MXFP4 = 0
 MOE_W_NVFP4 = 1
@@ -34,7 +35,7 @@ EXPORTED = (
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
     "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
     "moe_dense_workspace_size", "moe_dense_linear", "moe_nvfp4_pack", "moe_nvfp4_unpack", "moe_workspace_routing",
-    "moe_decode_pieces_bytes", "moe_expert_ffn_decode",
+    "moe_decode_pieces_bytes", "moe_decode_pieces", "moe_expert_ffn_decode",
 )
 
 
@@ -94,7 +95,8 @@ _SIGS = {
     "moe_nvfp4_pack": (I32, [P, I64, I64, I64, P, P, P, P]),
     "moe_nvfp4_unpack": (I32, [P, P, P, I64, I64, I64, P, P]),
     "moe_decode_pieces_bytes": (SZ, [I32, I32, I32]),
-    "moe_expert_ffn_decode": (I32, [P, P, P, P, P, P, I32, I32, I32, I32, I32, WP, P, P, P, SZ, P]),
+    "moe_decode_pieces": (I32, [P, I32, I32, I32, P, P, P]),
+    "moe_expert_ffn_decode": (I32, [P, P, I32, P, P, P, P, I32, I32, I32, I32, I32, WP, P, P, P, SZ, P]),
     "moe_workspace_routing": (I32, [P, SZ, I32, I32, I32, I32, I32, I32, ctypes.POINTER(P), ctypes.POINTER(P),
                                     ctypes.POINTER(P), ctypes.POINTER(P)]),
 }
@@ -238,11 +240,15 @@ def moe_decode_pieces_bytes(T, d, scales):
     return load().moe_decode_pieces_bytes(T, d, int(scales))
 
 
-def moe_expert_ffn_decode(xa, xa_s, perm_token, offsets, inv_pos, w, T, d, E, k, I, W: moe_expert_weights, y_perm, y,
-                          ws, ws_bytes=None, stream=None):
+def moe_decode_pieces(x, T, d, fmt, xa, xa_s, stream=None):
+    _check("moe_decode_pieces", load().moe_decode_pieces(_p(x), T, d, fmt, _p(xa), _p(xa_s), _stream(stream)))
+
+
+def moe_expert_ffn_decode(xa, xa_s, fmt, perm_token, offsets, inv_pos, w, T, d, E, k, I, W: moe_expert_weights, y_perm,
+                          y, ws, ws_bytes=None, stream=None):
     _check("moe_expert_ffn_decode",
-           load().moe_expert_ffn_decode(_p(xa), _p(xa_s), _p(perm_token), _p(offsets), _p(inv_pos), _p(w), T, d, E, k,
-                                        I, ctypes.byref(W), _p(y_perm), _p(y), _p(ws), _ws_bytes(ws, ws_bytes),
+           load().moe_expert_ffn_decode(_p(xa), _p(xa_s), fmt, _p(perm_token), _p(offsets), _p(inv_pos), _p(w), T, d,
+                                        E, k, I, ctypes.byref(W), _p(y_perm), _p(y), _p(ws), _ws_bytes(ws, ws_bytes),
                                         _stream(stream)))
 
 

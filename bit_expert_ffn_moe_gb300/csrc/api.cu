@@ -33,10 +33,10 @@ moe_status from_cuda(cudaError_t e) {
 
 moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     if (T < 0 || d <= 0 || E <= 0 || k <= 0 || I <= 0) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_MXFP4 && fmt != MOE_ACT_MXFP8) return MOE_ERR_INVALID_ARG;
     if (E > kMaxE || k > kMaxK || k > E) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (d % (fmt == MOE_ACT_MXFP4 ? 256 : 128) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (I % (fmt == MOE_ACT_MXFP4 ? 256 : 32) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (d % (fmt == MOE_ACT_BF16 ? 128 : 256) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (I % (fmt == MOE_ACT_BF16 ? 32 : 256) != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)T * k > (int64_t)1 << 30 || (int64_t)T * d > ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
@@ -45,7 +45,7 @@ moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
 
 namespace {
 
-constexpr int kAbiVersion = 9;
+constexpr int kAbiVersion = 10;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -71,18 +71,20 @@ moe_status check_weights(const moe_expert_weights* W, moe_act_fmt fmt, bool need
             return MOE_ERR_INVALID_ARG;
         if (need_down && (!W->down_gs || !aligned(W->down_s, 2))) return MOE_ERR_INVALID_ARG;
     }
+    // MOE_ACT_MXFP8 reads the canonical codes through tensor maps (32-byte aligned) as well as the
+    // tensor-core copies
+    const size_t q_align = fmt == MOE_ACT_MXFP8 ? 32 : 16;
+    const bool mma = fmt != MOE_ACT_BF16;
     if (need_up) {
         if (!W->gate_q || !W->gate_s || !W->up_q || !W->up_s) return MOE_ERR_INVALID_ARG;
-        if (!aligned(W->gate_q, 16) || !aligned(W->up_q, 16)) return MOE_ERR_INVALID_ARG;
-        if (fmt == MOE_ACT_MXFP4 && (!W->gate_q_mma || !W->gate_s_mma || !W->up_q_mma || !W->up_s_mma ||
-                                     !aligned(W->gate_q_mma, 16) || !aligned(W->gate_s_mma, 16) ||
-                                     !aligned(W->up_q_mma, 16) || !aligned(W->up_s_mma, 16)))
+        if (!aligned(W->gate_q, q_align) || !aligned(W->up_q, q_align)) return MOE_ERR_INVALID_ARG;
+        if (mma && (!W->gate_q_mma || !W->gate_s_mma || !W->up_q_mma || !W->up_s_mma || !aligned(W->gate_q_mma, 16) ||
+                    !aligned(W->gate_s_mma, 16) || !aligned(W->up_q_mma, 16) || !aligned(W->up_s_mma, 16)))
             return MOE_ERR_INVALID_ARG;
     }
     if (need_down) {
-        if (!W->down_q || !W->down_s || !aligned(W->down_q, 16)) return MOE_ERR_INVALID_ARG;
-        if (fmt == MOE_ACT_MXFP4 && (!W->down_q_mma || !W->down_s_mma || !aligned(W->down_q_mma, 16) ||
-                                     !aligned(W->down_s_mma, 16)))
+        if (!W->down_q || !W->down_s || !aligned(W->down_q, q_align)) return MOE_ERR_INVALID_ARG;
+        if (mma && (!W->down_q_mma || !W->down_s_mma || !aligned(W->down_q_mma, 16) || !aligned(W->down_s_mma, 16)))
             return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;
@@ -255,25 +257,23 @@ moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int 
                        int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_pos, uint8_t* xa,
                        uint8_t* xa_s, void* ws, size_t ws_bytes, moe_stream_t stream) {
     // the buffers this call uses do not depend on I: check against the smallest valid I
-    const int I_min = fmt == MOE_ACT_MXFP4 ? 256 : 32;
+    const int I_min = fmt == MOE_ACT_BF16 ? 32 : 256;
     MOE_TRY(check_shape(T, d, E, k, I_min, fmt));
     if (!ids || !counts || !offsets || !perm_token || !inv_pos) return MOE_ERR_INVALID_ARG;
-    if (fmt == MOE_ACT_MXFP4 && (!x || !xa || !xa_s || !aligned(x, 16) || !aligned(xa, 16))) return MOE_ERR_INVALID_ARG;
+    // the token operand of the prefill GEMMs (MXFP4 / MXFP8), unless both buffers are NULL
+    const bool operand = fmt != MOE_ACT_BF16 && (xa != nullptr || xa_s != nullptr);
+    if (operand && (!x || !xa || !xa_s || !aligned(x, 16) || !aligned(xa, 16))) return MOE_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, d, E, k, I_min, fmt);
     MOE_TRY(check_ws(ws, ws_bytes, L));
     MOE_TRY(check_device());
     cudaStream_t st = (cudaStream_t)stream;
     PlanView plan = plan_view(ws, L, E);
-    const bool pieces = fmt == MOE_ACT_BF16 && xa != nullptr && xa_s != nullptr;
-    if (pieces && (!mma_decode_shape(T, d, 256) || !x || !aligned(x, 16) || !aligned(xa, 16)))
-        return T == 0 ? MOE_OK : MOE_ERR_UNSUPPORTED_SHAPE;
     MOE_CUDA(launch_permute(ids, T, E, k, counts, offsets, perm_token, inv_pos, plan, st, false));
-    if (fmt == MOE_ACT_MXFP4)
+    if (operand)
         MOE_CUDA(launch_act_quant_gather(x, T, d, E, k, offsets, perm_token, plan, L.pad_rows,
                                          reinterpret_cast<uint8_t*>(at(ws, L.xq)),
-                                         reinterpret_cast<uint8_t*>(at(ws, L.xs)), xa, xa_s, st, true));
-    else if (pieces && T > 0)
-        MOE_CUDA(launch_x_pieces(x, T, d, xa, xa_s, st, false));
+                                         reinterpret_cast<uint8_t*>(at(ws, L.xs)), xa, xa_s, fmt == MOE_ACT_MXFP8, st,
+                                         true));
     return MOE_OK;
 }
 
@@ -282,26 +282,37 @@ size_t moe_decode_pieces_bytes(int T, int d, int scales) {
     return scales ? mma_scale_bytes(128, d) : (size_t)128 * d / 2;
 }
 
-moe_status moe_expert_ffn_decode(const uint8_t* xa, const uint8_t* xa_s, const int32_t* perm_token,
+moe_status moe_decode_pieces(const uint16_t* x, int T, int d, moe_act_fmt fmt, uint8_t* xa, uint8_t* xa_s,
+                             moe_stream_t stream) {
+    if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_MXFP8) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return d > 0 && d % 256 == 0 ? MOE_OK : MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!mma_decode_shape(T, d, 256)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!x || !xa || !xa_s || !aligned(x, 16) || !aligned(xa, 16)) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_device());
+    return from_cuda(launch_x_pieces(x, T, d, fmt == MOE_ACT_MXFP8, xa, xa_s, (cudaStream_t)stream, false));
+}
+
+moe_status moe_expert_ffn_decode(const uint8_t* xa, const uint8_t* xa_s, moe_act_fmt fmt, const int32_t* perm_token,
                                  const int32_t* offsets, const int32_t* inv_pos, const float* w, int T, int d, int E,
                                  int k, int I, const moe_expert_weights* W, uint16_t* y_perm, uint16_t* y, void* ws,
                                  size_t ws_bytes, moe_stream_t stream) {
-    MOE_TRY(check_shape(T, d, E, k, I, MOE_ACT_BF16));
+    if (fmt != MOE_ACT_BF16 && fmt != MOE_ACT_MXFP8) return MOE_ERR_INVALID_ARG;
+    MOE_TRY(check_shape(T, d, E, k, I, fmt));
     if (T == 0) return MOE_OK;
-    MOE_TRY(check_weights(W, MOE_ACT_BF16, true, true));
+    MOE_TRY(check_weights(W, fmt, true, true));
     if (!mma_decode_supported(T, d, E, k, I, W)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (y != nullptr && !mma_decode_fused_sum(T, d)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!xa || !xa_s || !perm_token || !offsets || !y_perm || !aligned(xa, 16) || !aligned(y_perm, 16))
         return MOE_ERR_INVALID_ARG;
     if (y != nullptr && (!inv_pos || !w || !aligned(y, 16))) return MOE_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(T, d, E, k, I, MOE_ACT_BF16);
+    const WsLayout L = ws_layout(T, d, E, k, I, fmt);
     MOE_TRY(check_ws(ws, ws_bytes, L));
     MOE_TRY(check_device());
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
     return from_cuda(launch_mma_decode(xa, xa_s, reinterpret_cast<uint8_t*>(at(ws, L.dha)),
                                        reinterpret_cast<uint8_t*>(at(ws, L.dha_s)),
                                        reinterpret_cast<float*>(at(ws, L.dpart)), plan_view(ws, L, E), offsets,
-                                       perm_token, T, d, E, k, I, W, y_perm, inv_pos, w, y, ctrl,
+                                       perm_token, T, d, E, k, I, W, fmt == MOE_ACT_MXFP8, y_perm, inv_pos, w, y, ctrl,
                                        (cudaStream_t)stream, false));
 }
 
@@ -326,8 +337,8 @@ moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint
     }
     if (!xa || !xa_s || !h_s || !aligned(xa, 16) || !aligned(h, 16)) return MOE_ERR_INVALID_ARG;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
-    return from_cuda(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, static_cast<uint8_t*>(h),
-                                    h_s, &ctrl->status, st, false));
+    return from_cuda(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fmt == MOE_ACT_MXFP8,
+                                    static_cast<uint8_t*>(h), h_s, &ctrl->status, st, false));
 }
 
 moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, const int32_t* perm_token,
@@ -351,7 +362,7 @@ moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, c
     }
     if (!h_s) return MOE_ERR_INVALID_ARG;
     return from_cuda(launch_umma_down(static_cast<const uint8_t*>(h), h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W,
-                                      y_perm, &ctrl->status, st, false));
+                                      fmt == MOE_ACT_MXFP8, y_perm, &ctrl->status, st, false));
 }
 
 moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d, uint16_t* y,
@@ -395,9 +406,10 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
     int32_t* inv = reinterpret_cast<int32_t*>(at(ws, L.inv));
     float* row_w = reinterpret_cast<float*>(at(ws, L.row_w));
 
-    if (fmt == MOE_ACT_BF16 && mma_decode_supported(T, d, E, k, I, W)) {
+    if (fmt != MOE_ACT_MXFP4 && mma_decode_supported(T, d, E, k, I, W)) {
         // few tokens, MXFP4 weights with their tensor-core copies: the expert GEMMs on the tensor
-        // cores, each activation row fed as 8 MXFP4 pieces (decode_mma.cu)
+        // cores, each activation row (bf16, or its MXFP8 values) fed as 8 MXFP4 pieces (decode_mma.cu)
+        const bool mx8 = fmt == MOE_ACT_MXFP8;
         if (route_decode_supported(T, d, E, k)) {
             MOE_CUDA(launch_route_decode(x, W_r, b, T, d, E, k, reinterpret_cast<float*>(at(ws, L.logits)), ids_b, w_b,
                                          counts, offsets, perm, inv, row_w, plan, ctrl, st, true));
@@ -410,10 +422,11 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
         uint8_t* dha = reinterpret_cast<uint8_t*>(at(ws, L.dha));
         uint8_t* dha_s = reinterpret_cast<uint8_t*>(at(ws, L.dha_s));
         uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
-        MOE_CUDA(launch_x_pieces(x, T, d, dxa, dxa_s, st, true));
+        MOE_CUDA(launch_x_pieces(x, T, d, mx8, dxa, dxa_s, st, true));
         const bool fused = !norm && mma_decode_fused_sum(T, d);
         MOE_CUDA(launch_mma_decode(dxa, dxa_s, dha, dha_s, reinterpret_cast<float*>(at(ws, L.dpart)), plan, offsets,
-                                   perm, T, d, E, k, I, W, y_perm, inv, w_b, fused ? y : nullptr, ctrl, st, true));
+                                   perm, T, d, E, k, I, W, mx8, y_perm, inv, w_b, fused ? y : nullptr, ctrl, st,
+                                   true));
         if (norm) MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
         else if (!fused) MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
         return MOE_OK;
@@ -444,14 +457,17 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
     MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
     uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
     uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
+    const bool fp8 = fmt == MOE_ACT_MXFP8;
     MOE_CUDA(launch_act_quant_gather(x, T, d, E, k, offsets, perm, plan, L.pad_rows,
                                      reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
-                                     xa, xa_s, st, true));
+                                     xa, xa_s, fp8, st, true));
     uint8_t* h = reinterpret_cast<uint8_t*>(at(ws, L.h));
     uint8_t* h_s = reinterpret_cast<uint8_t*>(at(ws, L.h_s));
     uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
-    MOE_CUDA(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, h, h_s, &ctrl->status, st, true));
-    MOE_CUDA(launch_umma_down(h, h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, y_perm, &ctrl->status, st, true));
+    MOE_CUDA(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fp8, h, h_s, &ctrl->status, st,
+                            true));
+    MOE_CUDA(launch_umma_down(h, h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fp8, y_perm, &ctrl->status, st,
+                              true));
     if (norm) MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
     else MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
     return MOE_OK;
@@ -473,7 +489,7 @@ moe_status moe_layer_forward_norm(const uint16_t* x, const float* W_r, const flo
 
 static moe_status check_dense_shape(int T, int K, int N, moe_act_fmt fmt) {
     if (T < 0 || K <= 0 || N <= 0) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (fmt == MOE_ACT_MXFP4) {
+    if (fmt == MOE_ACT_MXFP4 || fmt == MOE_ACT_MXFP8) {
         if (K % 256 != 0 || N % 256 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     } else if (fmt == MOE_ACT_BF16) {
         if (K % 128 != 0 || N % 128 != 0 || !gemv_supported(N, K)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -496,6 +512,7 @@ moe_status moe_dense_linear(const uint16_t* x, int T, int K, int N, const moe_mx
         return MOE_ERR_INVALID_ARG;
     if (fmt == MOE_ACT_MXFP4 && (!W->q_mma || !W->s_mma || !aligned(W->q_mma, 16) || !aligned(W->s_mma, 16)))
         return MOE_ERR_INVALID_ARG;
+    if (fmt == MOE_ACT_MXFP8 && (!W->s_mma || !aligned(W->q, 32) || !aligned(W->s_mma, 16))) return MOE_ERR_INVALID_ARG;
     const WsLayout L = dense_layout(T, K, N, fmt);
     MOE_TRY(check_ws(ws, ws_bytes, L));
     MOE_TRY(check_device());
@@ -520,10 +537,12 @@ moe_status moe_dense_linear(const uint16_t* x, int T, int K, int N, const moe_mx
     }
     uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
     uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
+    const bool fp8 = fmt == MOE_ACT_MXFP8;
     MOE_CUDA(launch_act_quant_gather(x, T, K, 1, 1, offsets, perm, plan, L.pad_rows,
                                      reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
-                                     xa, xa_s, st, true));
-    MOE_CUDA(launch_umma_down(xa, xa_s, plan, offsets, T, N, 1, 1, K, L.pad_rows, &Wd, y, &ctrl->status, st, true));
+                                     xa, xa_s, fp8, st, true));
+    MOE_CUDA(launch_umma_down(xa, xa_s, plan, offsets, T, N, 1, 1, K, L.pad_rows, &Wd, fp8, y, &ctrl->status, st,
+                              true));
     return MOE_OK;
 }
 

@@ -106,26 +106,27 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     L.perm = take(sizeof(int32_t) * (size_t)P);
     L.inv = take(sizeof(int32_t) * (size_t)P);
     L.row_w = take(sizeof(float) * (size_t)P);
-    if (fmt == MOE_ACT_MXFP4) {
+    if (fmt == MOE_ACT_MXFP4 || fmt == MOE_ACT_MXFP8) {
+        const size_t per_byte = fmt == MOE_ACT_MXFP4 ? 2 : 1;  // values per code byte
         L.pad_rows = padded_rows(T, k, E);
-        L.xq = take((size_t)T * d / 2);
+        L.xq = take((size_t)T * d / per_byte);
         L.xs = take((size_t)T * d / 32);
-        L.xa = take((size_t)L.pad_rows * d / 2);
+        L.xa = take((size_t)L.pad_rows * d / per_byte);
         L.xa_s = take(mma_scale_bytes(L.pad_rows, d));
-        L.h = take((size_t)L.pad_rows * I / 2);
+        L.h = take((size_t)L.pad_rows * I / per_byte);
         L.h_s = take(mma_scale_bytes(L.pad_rows, I));
         L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);
     } else {
         L.h = take(sizeof(uint16_t) * (size_t)P * I);
         L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);  // expert outputs (normalised layer, tensor-core decode)
-        if (mma_decode_shape(T, d, I)) {
-            const size_t slots = (size_t)(P < E ? P : E);
-            L.dxa = take((size_t)128 * d / 2);
-            L.dxa_s = take(mma_scale_bytes(128, d));
-            L.dha = take(slots * 128 * I / 2);
-            L.dha_s = take(slots * mma_scale_bytes(128, I));
-            L.dpart = take(mma_decode_part_bytes(T, d, k, I));
-        }
+    }
+    if (fmt != MOE_ACT_MXFP4 && mma_decode_shape(T, d, I)) {  // decode on the tensor cores (bf16, MXFP8)
+        const size_t slots = (size_t)(P < E ? P : E);
+        L.dxa = take((size_t)128 * d / 2);
+        L.dxa_s = take(mma_scale_bytes(128, d));
+        L.dha = take(slots * 128 * I / 2);
+        L.dha_s = take(slots * mma_scale_bytes(128, I));
+        L.dpart = take(mma_decode_part_bytes(T, d, k, I));
     }
     L.total = off;
     return L;
@@ -133,7 +134,7 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
 
 // Workspace of the dense MXFP4 linear map (y = x W^T, x [T][K], W [N][K]), run as the down GEMM
 // of one expert holding every row: control block, one-expert plan, offsets, identity permutation
-// and, for MOE_ACT_MXFP4, the quantised rows and the padded operand tiles of width K.
+// and, for MOE_ACT_MXFP4 / MXFP8, the quantised rows and the padded operand tiles of width K.
 inline WsLayout dense_layout(int T, int K, int N, moe_act_fmt fmt) {
     (void)N;
     WsLayout L;
@@ -147,11 +148,12 @@ inline WsLayout dense_layout(int T, int K, int N, moe_act_fmt fmt) {
     L.plan = take(sizeof(int32_t) * (size_t)(4 * 1 + 2 + 8));
     L.offsets = take(sizeof(int32_t) * 2);
     L.perm = take(sizeof(int32_t) * (size_t)T);
-    if (fmt == MOE_ACT_MXFP4) {
+    if (fmt == MOE_ACT_MXFP4 || fmt == MOE_ACT_MXFP8) {
+        const size_t per_byte = fmt == MOE_ACT_MXFP4 ? 2 : 1;  // values per code byte
         L.pad_rows = padded_rows(T, 1, 1);
-        L.xq = take((size_t)T * K / 2);
+        L.xq = take((size_t)T * K / per_byte);
         L.xs = take((size_t)T * K / 32);
-        L.xa = take((size_t)L.pad_rows * K / 2);
+        L.xa = take((size_t)L.pad_rows * K / per_byte);
         L.xa_s = take(mma_scale_bytes(L.pad_rows, K));
     }
     L.total = off;
@@ -258,6 +260,60 @@ __device__ __forceinline__ uint32_t mx_scale_from_amax(float amax, float& inv_sc
     return (uint32_t)(X + 127);
 }
 
+// ------------------------------------------------------------------ MXFP8 (E4M3 elements)
+// Block exponent of the 8-bit MX format: X = floor(log2(amax)) - 8 (8 = the exponent of E4M3's
+// largest normal, 448 = 1.75 * 2^8) clamped to [-127, 127]; amax = 0 or below 2^-126 gives -127.
+// Returns the scale byte X + 127 and writes 2^-X (exact) to inv_scale.
+__device__ __forceinline__ uint32_t mx8_scale_from_amax(float amax, float& inv_scale) {
+    int X = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127 - 8;
+    if (X < -127) X = -127;
+    inv_scale = __uint_as_float((uint32_t)(127 - X) << 23);
+    return (uint32_t)(X + 127);
+}
+
+// Four values already divided by the block scale -> four E4M3 bytes (element 0 in bits 0..7):
+// nearest E4M3 value, ties to even, saturating at 448 (the hardware conversion), with the sign
+// of the value unless its magnitude rounds to zero (a zero is stored as +0).
+__device__ __forceinline__ uint32_t e4m3x4_encode(float a0, float a1, float a2, float a3) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    const uint32_t mag = r & 0x7F7F7F7Fu;
+    const uint32_t nonzero = (mag + 0x7F7F7F7Fu) & 0x80808080u;  // bit 7 of a byte: magnitude != 0
+    return mag | (r & nonzero);
+}
+
+// A whole 32-element block in MXFP8: returns the scale byte and writes the 32 code bytes (element
+// i in byte i % 16 of c[i / 16]).
+__device__ __forceinline__ uint32_t mx8_block_encode(const float (&v)[32], uint4 (&c)[2]) {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float inv;
+    const uint32_t sb = mx8_scale_from_amax(amax, inv);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = e4m3x4_encode(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
+    c[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    c[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    return sb;
+}
+
+// Four values of a block rounded in place to their MXFP8 values (E4M3 value * 2^X, exact in fp32)
+// given the block's 2^-X and 2^X.
+__device__ __forceinline__ void mx8_round4(float (&v)[4], float inv, float scale) {
+    const uint32_t c = e4m3x4_encode(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+    const float2 lo = e4m3x2_to_f2(c & 0xFFFFu), hi = e4m3x2_to_f2(c >> 16);
+    v[0] = lo.x * scale;
+    v[1] = lo.y * scale;
+    v[2] = hi.x * scale;
+    v[3] = hi.y * scale;
+}
+
 // A whole 32-element block: returns the scale byte and writes the 16 bytes of codes
 // (v is overwritten with v / 2^X).
 __device__ __forceinline__ uint32_t mx_block_encode(float (&v)[32], uint4& codes) {
@@ -290,6 +346,15 @@ __host__ __device__ __forceinline__ size_t mma_tile_offset(int64_t row, int64_t 
     const int64_t tile = (row / 128) * (K / 256) + blk / 8;
     const int64_t r = row % 128;
     return (size_t)tile * 16384 + (size_t)(r * 128 + (((blk % 8) ^ (r % 8)) * 16));
+}
+
+// Byte offset of the 16-byte chunk c (elements 16c .. 16c+15) of a row in the tensor-core tiles of
+// an E4M3 matrix with K values (bytes) per row: tiles of 128 rows x 128 values (16384 bytes) at
+// tile index (row/128)*(K/128) + c/8, chunk c%8 of row r stored at r*128 + ((c%8) ^ (r%8))*16.
+__host__ __device__ __forceinline__ size_t mma8_tile_offset(int64_t row, int64_t c, int64_t K) {
+    const int64_t tile = (row / 128) * (K / 128) + c / 8;
+    const int64_t r = row % 128;
+    return (size_t)tile * 16384 + (size_t)(r * 128 + (((c % 8) ^ (r % 8)) * 16));
 }
 
 // Bulk prefetch of [p, p + bytes) into L2 (no completion signal; p and bytes multiples of 16).
@@ -408,9 +473,11 @@ bool route_decode_supported(int T, int d, int E, int k);
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl,
                            const float* w = nullptr, float* row_w = nullptr);
+// The token operand of the prefill GEMMs: each row of x quantised once (xq, xs), then gathered into
+// padded expert-grouped tensor-core tiles (xa, xa_s).  fp8: MXFP8 (E4M3 bytes), else MXFP4.
 cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
                                     const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
-                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl);
+                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl);
 
 cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,
@@ -434,23 +501,28 @@ cudaError_t launch_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, 
 // Decode on the tensor cores (decode_mma.cu), MXFP4 weights with their tensor-core copies.
 bool mma_decode_supported(int T, int d, int E, int k, int I, const moe_expert_weights* W);
 // x bf16 [T][d] -> 8 MXFP4 pieces per row: rows 8t + p of a [128][d] operand tile (code tiles xa,
-// scale atoms xa_s).  Reads x before its dependency wait (the preceding kernel must have passed its
-// own wait before letting this one start).
-cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl);
+// scale atoms xa_s); mx8: of the row's MXFP8 values.  Reads x before its dependency wait (the
+// preceding kernel must have passed its own wait before letting this one start).
+cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, bool mx8, uint8_t* xa, uint8_t* xa_s, cudaStream_t st,
+                            bool pdl);
 // Both expert GEMMs in one persistent launch: gate/up tiles, then down tiles (each waits for its
 // slot's h operand), expert outputs to y_perm; with y != nullptr (T <= 4, d <= 64 * 256) the weighted
 // sum y[t] = sum_j w[t][j] y_perm[inv_pos[t k + j]] (fp32, slot order, then bf16) is fused too.
+// mx8: h is rounded to MXFP8 (else bf16) before its pieces are formed.
 cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, float* part,
                               PlanView plan, const int32_t* offsets, const int32_t* perm_token, int T, int d, int E,
-                              int k, int I, const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos,
-                              const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl);
+                              int k, int I, const moe_expert_weights* W, bool mx8, uint16_t* y_perm,
+                              const int32_t* inv_pos, const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st,
+                              bool pdl);
 bool mma_decode_fused_sum(int T, int d);
 
+// Grouped prefill GEMMs (umma.cu).  fp8: MXFP8 token operand and h (kind::mxf8f6f4, the weights
+// read from their canonical codes through tensor maps); else MXFP4 (kind::mxf4, tensor-core tiles).
 cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets,
                            int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,
-                           uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st, bool pdl);
+                           bool fp8, uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st, bool pdl);
 cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan, const int32_t* offsets,
                              int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,
-                             uint16_t* y_perm, int* status, cudaStream_t st, bool pdl);
+                             bool fp8, uint16_t* y_perm, int* status, cudaStream_t st, bool pdl);
 }  // namespace moe
 

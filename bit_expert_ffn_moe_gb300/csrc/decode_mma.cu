@@ -1,5 +1,5 @@
-// decode_mma.cu -- the expert GEMMs of small batches (up to 16 tokens) with bf16 activations on
-// the block-scaled FP4 tensor cores (tcgen05, kind::mxf4).
+// decode_mma.cu -- the expert GEMMs of small batches (up to 16 tokens) with bf16 or MXFP8
+// activations on the block-scaled FP4 tensor cores (tcgen05, kind::mxf4).
 //
 // At decode sizes every chosen expert sees one or a few tokens and the layer time is the read of
 // the 4-bit expert weights (Muse Spark Open explainer, section 13: at one token per expert the
@@ -20,6 +20,13 @@
 // with a weight row is exact in its products and accumulates in fp32, so the piece rows of a
 // token sum to its dot products.  A token t's pieces are rows 8t .. 8t+7 of the MMA's A operand
 // (M = 128 rows: up to 16 tokens); the epilogue adds the eight lanes of each token.
+//
+// 8-bit activations (MXFP8: E4M3 elements with one E8M0 scale per 32, the 4-bit-weight /
+// 8-bit-activation configuration of the DGX Spark news item, section 2): x and h are first rounded
+// to their MXFP8 values, then split into pieces in the same way, so the GEMMs see the 8-bit operand
+// to within the same residual.  At these sizes the tensor-core rate is irrelevant (the weight read
+// bounds the layer), and pieces keep the weight tiles packed: a kind::mxf8f6f4 MMA would need its
+// FP4 operand widened to one byte per value in shared memory, halving the weight bytes in flight.
 //
 // Kernels (one persistent CTA per SM, the same roles as the grouped prefill GEMMs in umma.cu:
 // a producer warp issuing bulk copies into a 4-stage ring, an MMA warp, 8 epilogue warps):
@@ -121,9 +128,11 @@ __device__ __forceinline__ float absmax8(const float (&r)[8]) {
     return m;
 }
 
-// x pieces: one thread per (token, 32-element block); rows 8t + p of the [128][d] A tile.
-__global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restrict__ x, int T, int d, uint8_t* xa,
-                                                       uint8_t* xa_s) {
+// x pieces: one thread per (token, 32-element block); rows 8t + p of the [128][d] A tile.  mx8: the
+// block is first rounded to its MXFP8 values (E4M3 elements, one power-of-two scale), so the pieces
+// sum to the 8-bit activation operand instead of the bf16 row.
+__global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restrict__ x, int T, int d, int mx8,
+                                                       uint8_t* xa, uint8_t* xa_s) {
     // the next kernel (the expert GEMMs) may start its set-up now; it waits for this kernel, and so
     // for the routing, before it reads anything either produced
     pdl_launch_dependents();
@@ -141,6 +150,22 @@ __global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restric
             for (int m = 0; m < 4; ++m) {
                 r[g][2 * m] = bf16_bits_to_f32(w[m] & 0xFFFFu);
                 r[g][2 * m + 1] = bf16_bits_to_f32(w[m] >> 16);
+            }
+        }
+        if (mx8) {
+            const float amax = fmaxf(fmaxf(absmax8(r[0]), absmax8(r[1])), fmaxf(absmax8(r[2]), absmax8(r[3])));
+            float inv;
+            const float scale = e8m0_to_f32(mx8_scale_from_amax(amax, inv));
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                float q0[4] = {r[g][0], r[g][1], r[g][2], r[g][3]}, q1[4] = {r[g][4], r[g][5], r[g][6], r[g][7]};
+                mx8_round4(q0, inv, scale);
+                mx8_round4(q1, inv, scale);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    r[g][i] = q0[i];
+                    r[g][4 + i] = q1[i];
+                }
             }
         }
 #pragma unroll 1
@@ -184,6 +209,7 @@ struct DecArgs {
     Ctrl* ctrl;
     float* part;                // split gate/up tiles: fp32 partial sums [T*k][I/128][ks][256]
     int ks;                     // K parts per gate/up tile (1: whole tiles)
+    int mx8;                    // h rounded to MXFP8 (else bf16) before its pieces are formed
 };
 
 // Sum of the accumulator words of one 32-column tensor-memory load over the eight lanes of a lane
@@ -333,9 +359,24 @@ __device__ __forceinline__ void h_pieces(const DecArgs& args, float (&r)[4], int
     }
 }
 
-__device__ __forceinline__ float swiglu_bf16(float g, float u) {
-    const float hv = __fdividef(g, 1.f + __expf(-g)) * u;  // SiLU(g) * u
-    return bf16_bits_to_f32(f32_to_bf16_bits(hv));      // h as bf16
+// h = SiLU(g) * u of four features, rounded to the down GEMM's operand format: bf16, or (mx8) the
+// MXFP8 value of its 32-element block, which the 8 lanes of the lane group hold together.
+__device__ __forceinline__ void swiglu_round(const DecArgs& args, const float (&g)[4], const float (&u)[4],
+                                             float (&r)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __fdividef(g[i], 1.f + __expf(-g[i])) * u[i];
+    if (!args.mx8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r[i] = bf16_bits_to_f32(f32_to_bf16_bits(r[i]));
+        return;
+    }
+    float amax = fmaxf(fmaxf(fabsf(r[0]), fabsf(r[1])), fmaxf(fabsf(r[2]), fabsf(r[3])));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    float inv;
+    const float scale = e8m0_to_f32(mx8_scale_from_amax(amax, inv));
+    mx8_round4(r, inv, scale);
 }
 
 // Chunk c of a gate/up tile's columns (32 features = one MX block of h): lane pl of the token's
@@ -356,9 +397,10 @@ __device__ __forceinline__ void up_chunk(const DecArgs& args, const DecTile& D, 
         }
         return;
     }
+    const float g[4] = {__uint_as_float(gv[0]), __uint_as_float(gv[1]), __uint_as_float(gv[2]), __uint_as_float(gv[3])};
+    const float u[4] = {__uint_as_float(uv[0]), __uint_as_float(uv[1]), __uint_as_float(uv[2]), __uint_as_float(uv[3])};
     float r[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r[i] = swiglu_bf16(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
+    swiglu_round(args, g, u, r);
     h_pieces(args, r, lane, 4 * D.p + 2 * half + c, row0, j >= 0);
 }
 
@@ -377,8 +419,7 @@ __device__ __forceinline__ void up_finish_split(const DecArgs& args, const DecTi
             u[0] += uq.x; u[1] += uq.y; u[2] += uq.z; u[3] += uq.w;
         }
         float r[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) r[i] = swiglu_bf16(g[i], u[i]);
+        swiglu_round(args, g, u, r);
         h_pieces(args, r, lane, 4 * D.p + g8, (size_t)D.u * 128 + 8 * (size_t)j, true);
     }
 }
@@ -740,17 +781,21 @@ bool mma_decode_supported(int T, int d, int E, int k, int I, const moe_expert_we
 
 bool mma_decode_fused_sum(int T, int d) { return T <= 4 && d / 256 <= kDecTickets; }
 
-cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl) {
+cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, bool mx8, uint8_t* xa, uint8_t* xa_s, cudaStream_t st,
+                            bool pdl) {
     const int n = T * (d / 32);
-    void* args[] = {&x, &T, &d, &xa, &xa_s};
+    int m8 = mx8 ? 1 : 0;
+    void* args[] = {&x, &T, &d, &m8, &xa, &xa_s};
     return launch_kernel((const void*)x_pieces_kernel, dim3((n + 255) / 256), dim3(256), 0, st, pdl, args);
 }
 
 cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, float* part,
                               PlanView plan, const int32_t* offsets, const int32_t* perm_token, int T, int d, int E,
-                              int k, int I, const moe_expert_weights* W, uint16_t* y_perm, const int32_t* inv_pos,
-                              const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st, bool pdl) {
+                              int k, int I, const moe_expert_weights* W, bool mx8, uint16_t* y_perm,
+                              const int32_t* inv_pos, const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st,
+                              bool pdl) {
     DecArgs a = {};
+    a.mx8 = mx8 ? 1 : 0;
     const int slots = T * k < E ? T * k : E;
     a.ks = slots * (I / 128) <= kDecSplitCounters ? mma_decode_ksplit(T, d) : 1;
     a.part = part;

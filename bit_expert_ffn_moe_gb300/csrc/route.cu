@@ -560,10 +560,13 @@ cudaError_t launch_dense_plan(int T, PlanView plan, int32_t* offsets, int32_t* p
     return launch_kernel((const void*)dense_plan_kernel, dim3(blocks), dim3(256), 0, st, pdl, args);
 }
 
-// ------------------------------------------------------------------ MXFP4 activation operand
+// ------------------------------------------------------------------ MX activation operand
 // Quantise each token row once (one thread per 32-element block), then gather the rows into
-// padded expert-grouped order with the scales in the tensor-core layout.
+// padded expert-grouped order with the scales in the tensor-core layout.  FP8: MXFP8 (32 E4M3
+// bytes per block, tiles of 128 values per 128-byte line), else MXFP4 (16 bytes of E2M1 codes per
+// block, 256 values per line).
 
+template <bool FP8>
 __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ xq,
                                  uint8_t* __restrict__ xs) {
     pdl_wait();
@@ -581,17 +584,26 @@ __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks
                 v[8 * i + 2 * m + 1] = bf16_bits_to_f32(ww[m] >> 16);
             }
         }
-        uint4 codes;
-        const uint32_t sb = mx_block_encode(v, codes);
-        reinterpret_cast<uint4*>(xq)[blk] = codes;
-        xs[blk] = (uint8_t)sb;
+        if (FP8) {
+            uint4 c[2];
+            const uint32_t sb = mx8_block_encode(v, c);
+            reinterpret_cast<uint4*>(xq)[2 * blk] = c[0];
+            reinterpret_cast<uint4*>(xq)[2 * blk + 1] = c[1];
+            xs[blk] = (uint8_t)sb;
+        } else {
+            uint4 codes;
+            const uint32_t sb = mx_block_encode(v, codes);
+            reinterpret_cast<uint4*>(xq)[blk] = codes;
+            xs[blk] = (uint8_t)sb;
+        }
     }
 }
 
 // One warp per padded row: the row's expert comes from a binary search over the padded offsets
-// cached in shared memory; lanes copy consecutive 16-byte blocks of the token's quantised row
+// cached in shared memory; lanes copy consecutive 16-byte chunks of the token's quantised row
 // into the tensor-core code tiles (8 lanes fill one 128-byte line), then its scale bytes four
 // at a time.
+template <bool FP8>
 __global__ void __launch_bounds__(256)
 act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, int d, int E, int64_t pad_rows,
                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_token, PlanView plan,
@@ -601,6 +613,7 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
     for (int i = threadIdx.x; i <= E; i += blockDim.x) s_pad[i] = plan.pad_offsets[i];
     __syncthreads();
     const int nb = d / 32, lane = threadIdx.x & 31;
+    const int nc = FP8 ? d / 16 : d / 32;  // 16-byte chunks of a quantised row
     const int64_t used = plan.scalars[2];
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
     for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < used; r += nwarps) {
@@ -612,10 +625,10 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
         const int64_t local = r - s_pad[lo];
         const bool real = local < plan.counts[lo];
         const int t = real ? perm_token[offsets[lo] + local] : 0;
-        const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (d / 2));
-        for (int blk = lane; blk < nb; blk += 32) {
-            const uint4 v = real ? src[blk] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(xa + mma_tile_offset(r, blk, d)) = v;
+        const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (size_t)nc * 16);
+        for (int c = lane; c < nc; c += 32) {
+            const uint4 v = real ? src[c] : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(xa + (FP8 ? mma8_tile_offset(r, c, d) : mma_tile_offset(r, c, d))) = v;
         }
         // scales: blocks 4q .. 4q+3 of a row are 4 consecutive bytes of one scale atom (and of xs)
         const uint32_t* srcs = reinterpret_cast<const uint32_t*>(xs + (size_t)t * nb);
@@ -627,22 +640,23 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
 
 cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
                                     const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
-                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, cudaStream_t st, bool pdl) {
+                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl) {
     (void)k;
     int64_t nb = (int64_t)T * (d / 32);
     if (nb > 0) {
         int64_t blocks = (nb + 255) / 256;
         if (blocks > 152 * 16) blocks = 152 * 16;
         void* a1[] = {&x, &nb, &xq, &xs};
-        cudaError_t err = launch_kernel((const void*)act_quant_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
+        const void* f = fp8 ? (const void*)act_quant_kernel<true> : (const void*)act_quant_kernel<false>;
+        cudaError_t err = launch_kernel(f, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
         if (err != cudaSuccess) return err;
     }
     if (pad_rows == 0) return cudaSuccess;
     int64_t blocks = (pad_rows + 7) / 8;  // 8 warps (rows) per CTA
     if (blocks > 152 * 8) blocks = 152 * 8;
     void* a2[] = {&xq, &xs, &d, &E, &pad_rows, &offsets, &perm_token, &plan, &xa, &xa_s};
-    return launch_kernel((const void*)act_gather_kernel, dim3((unsigned)blocks), dim3(256),
-                         sizeof(int32_t) * (size_t)(E + 1), st, pdl, a2);
+    const void* g = fp8 ? (const void*)act_gather_kernel<true> : (const void*)act_gather_kernel<false>;
+    return launch_kernel(g, dim3((unsigned)blocks), dim3(256), sizeof(int32_t) * (size_t)(E + 1), st, pdl, a2);
 }
 
 }  // namespace moe

@@ -1,7 +1,8 @@
 // tcgen05.cuh -- PTX wrappers of the 5th-generation tensor cores (sm_103a) shared by the grouped
-// expert GEMMs: tensor-memory scale copies, block-scaled FP4 MMAs (kind::mxf4, E2M1 operands with
-// one E8M0 scale per 32 elements), shared-memory and instruction descriptors, tensor-memory loads
-// and the commit / fence instructions.  The bit fields are the ones the PTX ISA defines.
+// expert GEMMs: tensor-memory scale copies, block-scaled MMAs (kind::mxf4: E2M1 operands;
+// kind::mxf8f6f4: E4M3 tokens x E2M1 weights; one E8M0 scale per 32 elements in both),
+// shared-memory and instruction descriptors, tensor-map copies, tensor-memory loads and the
+// commit / fence instructions.  The bit fields are the ones the PTX ISA defines.
 #pragma once
 
 #include "common.cuh"
@@ -51,6 +52,41 @@ __device__ __forceinline__ void stage_mmas_commit(uint32_t d, uint64_t ad, uint6
         : "memory");
 }
 
+// 8-bit operands (kind::mxf8f6f4, one E8M0 scale per 32 values, K = 32 per MMA): one K step of 128
+// values.  Scale slot: A scales at sf (4 columns), B scales of rows 0..127 at sf + 4 and of rows
+// 128..255 at sf + 8.
+__device__ __forceinline__ void stage_scales8_to_tmem(uint32_t sf, uint64_t a, uint64_t b0, uint64_t b1) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%2], %3;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t}" ::"r"(sf),
+        "l"(a), "r"(sf + 4), "l"(b0), "r"(sf + 8), "l"(b1)
+        : "memory");
+}
+
+// The four K = 32 MMAs of an 8-bit stage: sub-step i reads the operands 32 bytes further along
+// each row and scale byte i of the A and B scale columns (selectors in instruction-descriptor
+// bits 29-30 and 4-5), then the commit that frees the stage.
+__device__ __forceinline__ void stage_mmas8_commit(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sf,
+                                                   uint32_t accumulate, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, q;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %7, %8, %9, [%5], [%6], q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %10, %11, %12, [%5], [%6], q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %13, %14, %15, [%5], [%6], q;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%16];\n\t}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(sf), "r"(sf + 4), "l"(ad + 2), "l"(bd + 2),
+        "r"(idesc | (1u << 29) | (1u << 4)), "l"(ad + 4), "l"(bd + 4), "r"(idesc | (2u << 29) | (2u << 4)),
+        "l"(ad + 6), "l"(bd + 6), "r"(idesc | (3u << 29) | (3u << 4)), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // mbar_wait by every lane of a warp with a warp-uniform verdict.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
                                                long long limit = kWaitCycles) {
@@ -78,6 +114,23 @@ __device__ __forceinline__ uint64_t desc_sf(const void* p) {
 // UE8M0 scales, D fp32, shape M x N; the scale-factor byte selectors are added per MMA.
 __device__ __forceinline__ uint32_t idesc_mxf4(int M, int N) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A E4M3 (format code 0), B E2M1
+// (format code 5, read from the widened shared-memory layout: 16 values in 8 bytes, then 8 empty
+// bytes), K-major, UE8M0 scales, D fp32, shape M x N; scale byte selectors added per MMA.
+__device__ __forceinline__ uint32_t idesc_mxf8_e4m3_e2m1(int M, int N) {
+    return (0u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+
+// 2-D tensor-map copy of one box into shared memory, completing on an mbarrier (x: innermost
+// coordinate in elements, y: row).
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
 }
 
 // The MMA warp runs its loop with all 32 lanes (warp-uniform control flow, so every operand is

@@ -39,6 +39,10 @@
 //             then converting and storing them while the next tile's MMAs run.
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
+#include <cuda.h>
+
+#include <mutex>
+
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -49,8 +53,13 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, 8 epi
 constexpr int kTile = 128 * 128;                // 128 rows x 128 bytes (256 FP4 values)
 constexpr int kAtom = 512;                      // scale atom: 128 rows x 4 scales
 constexpr int kStages = 4;
-// A tile, two B tiles (256 weight rows), 2 atoms of A scales, 2 + 2 of B scales
+// A tile, two B tiles (256 weight rows), 2 atoms of A scales, 2 + 2 of B scales (MXFP4: 256 values
+// of K per stage); MXFP8 stages hold 128 values of K: the same three tiles (E4M3 tokens, the FP4
+// weights widened to one byte per value) and one scale atom each
 constexpr int kStageBytes = 3 * kTile + 6 * kAtom;
+static_assert(3 * kTile + 3 * kAtom <= kStageBytes, "an MXFP8 stage fits the stage ring");
+// bytes an MXFP8 stage's copies signal: a widened weight box counts its packed global bytes (8 KB)
+constexpr int kStageTx8 = kTile + 2 * (kTile / 2) + 3 * kAtom;
 constexpr int kAccBufs = 1;
 constexpr int kAccCols = 256;
 constexpr int kSfBase = kAccBufs * kAccCols;  // scale slots after the accumulator
@@ -65,6 +74,8 @@ constexpr size_t smem_bytes(int E) {
 
 // ------------------------------------------------------------------ kernel arguments / tiles
 struct UmmaArgs {
+    CUtensorMap tmap_b0;  // MXFP8: B rows 0..127 / 128..255 read from the canonical weight codes
+    CUtensorMap tmap_b1;
     const uint8_t* qa;   // token-operand code tiles (padded rows)
     const uint8_t* sfa;  // token-operand scales (tensor-core layout over padded rows)
     const uint8_t* qb0;  // B rows 0..127: gate (up) or down code tiles
@@ -78,7 +89,7 @@ struct UmmaArgs {
     int K;       // contraction length: d (up) or I (down)
     int NB;      // weight blocks per expert: I/128 (up) or d/256 (down)
     int n_out;   // output row length: I (h, up) or d (y_perm, down)
-    uint8_t* h;    // up: MXFP4 code tiles of [pad_rows][I]
+    uint8_t* h;    // up: MXFP4 (MXFP8) code tiles of [pad_rows][I]
     uint8_t* h_s;  // up: scales, tensor-core layout
     uint16_t* y_perm;  // down: bf16 [P][d]
     int* status;
@@ -114,8 +125,8 @@ __device__ __forceinline__ Tile decode_tile(int t, int& e, const SmemPlan& sp, c
 }
 
 // ------------------------------------------------------------------ the kernel
-template <bool IS_UP>
-__global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArgs args) {
+template <bool IS_UP, bool FP8>
+__global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_constant__ UmmaArgs args) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -173,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
     const uint32_t tmem = *tmem_slot;
 
     const int n_tiles = args.plan.scalars[1] * args.NB;
-    const int KT = args.K / 256;  // K steps of 256 FP4 values (128 bytes per row)
+    const int KT = args.K / (FP8 ? 128 : 256);  // K steps: 128 bytes of every operand row
     const int atoms_per_rowblk = args.K / 128;
 
     if (warp == 0) {
@@ -196,6 +207,18 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                     if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, args.status)) {
                         ok = false;
                         break;
+                    }
+                    if (FP8) {
+                        // the weight boxes come widened from the canonical codes through the tensor
+                        // maps (128 values x 128 rows, 16 KB each in shared memory)
+                        mbar_arrive_expect_tx(&full[s], kStageTx8);
+                        bulk_load(stage_a(s), qa + (size_t)kt * kTile, kTile, &full[s]);
+                        tma_load_2d(stage_b(s), &args.tmap_b0, 128 * kt, 128 * T.b_rb, &full[s]);
+                        tma_load_2d(stage_b(s) + kTile, &args.tmap_b1, 128 * kt, 128 * (int)rb1, &full[s]);
+                        bulk_load(stage_sfa(s), sfa + (size_t)kt * kAtom, kAtom, &full[s]);
+                        bulk_load(stage_sfb(s), sfb0 + (size_t)kt * kAtom, kAtom, &full[s]);
+                        bulk_load(stage_sfb(s) + kAtom, sfb1 + (size_t)kt * kAtom, kAtom, &full[s]);
+                        continue;
                     }
                     mbar_arrive_expect_tx(&full[s], kStageBytes);
                     bulk_load(stage_a(s), qa + (size_t)kt * kTile, kTile, &full[s]);
@@ -220,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
         // ---------------------------------------------------------- MMA issuer (whole warp)
         int kiter = 0, it = 0;
         bool ok = true;
-        const uint32_t idesc = idesc_mxf4(128, 256);
+        const uint32_t idesc = FP8 ? idesc_mxf8_e4m3_e2m1(128, 256) : idesc_mxf4(128, 256);
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
             const int buf = it % kAccBufs;
             const uint32_t use = it / kAccBufs;
@@ -236,10 +259,16 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                 }
                 tc_fence_after();
                 const uint32_t sf = tmem + kSfBase + s * kSfCols;
+                // the stage is free once these MMAs have read it
+                if (FP8) {
+                    stage_scales8_to_tmem(sf, desc_sf(stage_sfa(s)), desc_sf(stage_sfb(s)), desc_sf(stage_sfb(s) + kAtom));
+                    stage_mmas8_commit(d_tmem, desc_sw128(stage_a(s)), desc_sw128(stage_b(s)), idesc, sf,
+                                       kt > 0 ? 1u : 0u, &empty[s]);
+                    continue;
+                }
                 stage_scales_to_tmem(sf, desc_sf(stage_sfa(s)), desc_sf(stage_sfa(s) + kAtom), desc_sf(stage_sfb(s)),
                                      desc_sf(stage_sfb(s) + 2 * kAtom), desc_sf(stage_sfb(s) + kAtom),
                                      desc_sf(stage_sfb(s) + 3 * kAtom));
-                // the stage is free once these MMAs have read it
                 stage_mmas_commit(d_tmem, desc_sw128(stage_a(s)), desc_sw128(stage_b(s)), idesc,
                                   idesc | (2u << 29) | (2u << 4), sf, kt > 0 ? 1u : 0u, &empty[s]);
             }
@@ -291,10 +320,18 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
                         const float gv = __uint_as_float(v[cc][i]), uv = __uint_as_float(v[2 + cc][i]);
                         hv[i] = __fdividef(gv, 1.f + __expf(-gv)) * uv;  // SiLU(g) * u
                     }
-                    uint4 codes;
-                    const uint32_t sb = mx_block_encode(hv, codes);
                     const int blk = 4 * T.p + 2 * half + cc;  // 32-block of h along I
-                    *reinterpret_cast<uint4*>(args.h + mma_tile_offset((int64_t)row, blk, I)) = codes;
+                    uint32_t sb;
+                    if (FP8) {
+                        uint4 c8[2];
+                        sb = mx8_block_encode(hv, c8);
+                        *reinterpret_cast<uint4*>(args.h + mma8_tile_offset((int64_t)row, 2 * blk, I)) = c8[0];
+                        *reinterpret_cast<uint4*>(args.h + mma8_tile_offset((int64_t)row, 2 * blk + 1, I)) = c8[1];
+                    } else {
+                        uint4 codes;
+                        sb = mx_block_encode(hv, codes);
+                        *reinterpret_cast<uint4*>(args.h + mma_tile_offset((int64_t)row, blk, I)) = codes;
+                    }
                     args.h_s[mma_scale_offset((int64_t)row, blk, I)] = (uint8_t)sb;
                 }
             } else {
@@ -340,18 +377,55 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const UmmaArg
 }
 
 // ------------------------------------------------------------------ host side
-template <bool IS_UP>
+template <bool IS_UP, bool FP8>
 cudaError_t launch_grouped(const UmmaArgs& args, cudaStream_t st, bool pdl) {
-    const void* f = (const void*)umma_grouped_kernel<IS_UP>;
+    const void* f = (const void*)umma_grouped_kernel<IS_UP, FP8>;
     void* kargs[] = {const_cast<UmmaArgs*>(&args)};
     return launch_kernel(f, dim3(sm_count()), dim3(kThreads), smem_bytes(args.E), st, pdl, kargs);
+}
+
+typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, taken through the runtime's entry-point query (no link-time
+// dependency on the driver library); null when unavailable.
+encode_tiled_fn tensor_map_encoder() {
+    static encode_tiled_fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<encode_tiled_fn>(f);
+    });
+    return fn;
+}
+
+// Tensor map of a canonical MXFP4 code matrix q[rows][K/2] read in boxes of 128 values x 128 rows,
+// each 4-bit value given a byte's place in shared memory (16 values in 8 bytes, then 8 empty
+// bytes: the FP4 operand layout of kind::mxf8f6f4) with the 128-byte swizzle.  q must be 32-byte
+// aligned and K a multiple of 128.
+cudaError_t fp4_widening_map(CUtensorMap* m, const uint8_t* q, int64_t rows, int64_t K) {
+    encode_tiled_fn enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(K / 2)};
+    const cuuint32_t box[2] = {128, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<uint8_t*>(q), dims, strides, box,
+                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets, int T,
-                           int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W, uint8_t* h,
-                           uint8_t* h_s, int* status, cudaStream_t st, bool pdl) {
+                           int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W, bool fp8,
+                           uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st, bool pdl) {
     (void)T;
     (void)k;
     if (pad_rows == 0) return cudaSuccess;
@@ -372,11 +446,14 @@ cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan
     a.h = h;
     a.h_s = h_s;
     a.status = status;
-    return launch_grouped<true>(a, st, pdl);
+    if (!fp8) return launch_grouped<true, false>(a, st, pdl);
+    cudaError_t err = fp4_widening_map(&a.tmap_b0, W->gate_q, (int64_t)E * I, d);
+    if (err == cudaSuccess) err = fp4_widening_map(&a.tmap_b1, W->up_q, (int64_t)E * I, d);
+    return err == cudaSuccess ? launch_grouped<true, true>(a, st, pdl) : err;
 }
 
 cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan, const int32_t* offsets, int T,
-                             int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,
+                             int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W, bool fp8,
                              uint16_t* y_perm, int* status, cudaStream_t st, bool pdl) {
     (void)T;
     (void)k;
@@ -397,7 +474,10 @@ cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan
     a.n_out = d;
     a.y_perm = y_perm;
     a.status = status;
-    return launch_grouped<false>(a, st, pdl);
+    if (!fp8) return launch_grouped<false, false>(a, st, pdl);
+    cudaError_t err = fp4_widening_map(&a.tmap_b0, W->down_q, (int64_t)E * d, I);
+    if (err == cudaSuccess) a.tmap_b1 = a.tmap_b0;
+    return err == cudaSuccess ? launch_grouped<false, true>(a, st, pdl) : err;
 }
 
 }  // namespace moe

@@ -26,9 +26,9 @@
  *     MOE_ERR_TIMEOUT in the workspace and return; moe_get_device_status reads that word.
  *   - Inputs are assumed finite.
  *   - Shape rules (MOE_ERR_UNSUPPORTED_SHAPE otherwise): 1 <= k <= min(E, 32); E <= 1024;
- *     T >= 0; MOE_ACT_BF16: d % 128 == 0 and I % 32 == 0; MOE_ACT_MXFP4: d % 256 == 0 and
- *     I % 256 == 0 (whole 256-value MMA tiles along both contractions).  NVFP4 expert weights
- *     (moe_weight_fmt) are read by the MOE_ACT_BF16 path only.
+ *     T >= 0; MOE_ACT_BF16: d % 128 == 0 and I % 32 == 0; MOE_ACT_MXFP4 and MOE_ACT_MXFP8:
+ *     d % 256 == 0 and I % 256 == 0 (whole 256-value MMA tiles along both contractions).  NVFP4
+ *     expert weights (moe_weight_fmt) are read by the MOE_ACT_BF16 path only.
  *
  * MXFP4 tensor layout ("canonical"): a [rows][K] matrix is stored as codes q[rows][K/2]
  * (element 2i in the low nibble of byte i, element 2i+1 in the high nibble; bit 3 of a code
@@ -58,11 +58,21 @@ typedef enum moe_status {
 } moe_status;
 
 /* Activation format of the expert GEMM operands.
- *   MOE_ACT_BF16  -- decode-style path: x is used as bf16, the gate/up output h is stored as
- *                    bf16; CUDA-core GEMV kernels with 128-bit weight loads (best for T <= 4).
+ *   MOE_ACT_BF16  -- decode-style path: x is used as bf16, the gate/up output h is rounded to
+ *                    bf16 (see moe_layer_forward for its two kernel paths).
  *   MOE_ACT_MXFP4 -- prefill path: x and h are quantised to MXFP4 (same rule as the weight
- *                    packer); tcgen05 block-scaled MMA (kind::mxf4) grouped GEMMs. */
-typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1 } moe_act_fmt;
+ *                    packer); tcgen05 block-scaled MMA (kind::mxf4) grouped GEMMs.
+ *   MOE_ACT_MXFP8 -- 4-bit weights with 8-bit activations (the baseline configuration of the
+ *                    DGX Spark news item, section 2): x and h are quantised to MXFP8, E4M3
+ *                    elements (OCP OFP8: bias 7, subnormals, largest finite 448) with one E8M0
+ *                    scale per 32 consecutive elements: X = floor(log2(max |v|)) - 8 clamped to
+ *                    [-127, 127], scale byte X + 127, each element |v| / 2^X rounded to the
+ *                    nearest E4M3 value (ties to even, saturating at 448) with the sign of v
+ *                    unless it rounds to zero (stored as +0); an all-zero block gets scale byte 0.
+ *                    Needs MXFP4 weights with their tensor-core copies; up to 16 tokens run the
+ *                    decode kernels of MOE_ACT_BF16 on the operands' MXFP8 values, more run
+ *                    kind::mxf8f6f4 grouped GEMMs (E4M3 tokens x E2M1 weights). */
+typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1, MOE_ACT_MXFP8 = 2 } moe_act_fmt;
 
 /* Format of the expert weight matrices (moe_expert_weights.wfmt).
  *   MOE_W_MXFP4 -- the canonical MXFP4 layout above.
@@ -112,7 +122,7 @@ const char* moe_status_string(moe_status s);
 
 /* ABI version of this header (incremented on changes to the entry points or their structs);
  * moe_abi_version() returns the library's, which a caller compares with MOE_ABI_VERSION. */
-#define MOE_ABI_VERSION 9
+#define MOE_ABI_VERSION 10
 int moe_abi_version(void);
 
 /* Description of the CUDA error behind the calling thread's last MOE_ERR_CUDA (static string). */
@@ -185,11 +195,11 @@ moe_status moe_mxfp4_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uin
  * sizes.  Returns 0 when the shape is unsupported. */
 size_t moe_workspace_size(int T, int d, int E, int k, int I, moe_act_fmt fmt);
 
-/* Rows of the padded, expert-grouped activation buffers of the MXFP4 path (xa, h): every
+/* Rows of the padded, expert-grouped activation buffers of the MXFP4 / MXFP8 paths (xa, h): every
  * expert's rows start at a multiple of 128.  An upper bound that depends on sizes only. */
 int64_t moe_padded_rows(int T, int k, int E);
 
-/* Zero the workspace control block (status word, counters; the first 4 KB).  Call once per
+/* Zero the workspace control block (status word, counters; the first 8 KB).  Call once per
  * workspace, and again after moe_get_device_status reported MOE_ERR_TIMEOUT (a call that timed
  * out may leave its counters set). */
 moe_status moe_workspace_init(void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -246,17 +256,16 @@ moe_status moe_route_noalloc(const uint16_t* x, const float* W_r, const float* b
  *   inv_pos[P]     permuted row of pair (t, j) at index t*k + j
  * ids as moe_route returns them: each token's k ids distinct and in [0, E).  An id outside
  * [0, E) is not counted and its pair gets no row (its inv_pos entry is not written).
- * For MOE_ACT_MXFP4 it also quantises every token row of x once and writes the activation
- * operand of the [moe_padded_rows][d] matrix of permuted rows in padded expert-grouped order
- * (expert e's rows start at a multiple of 128; padding rows are zero): xa in the tensor-core
- * code tiles (moe_padded_rows*d/2 bytes) and xa_s in the tensor-core scale layout
- * (moe_mxfp4_mma_scale_bytes(moe_padded_rows, d) bytes).  For MOE_ACT_BF16, xa and xa_s are
- * unused (may be NULL), except that when both are given (1 <= T <= 16, d % 256 == 0; buffers of
- * moe_decode_pieces_bytes(T, d, 0) and (T, d, 1) bytes, 16-byte aligned) the call also writes
- * the activation operand of moe_expert_ffn_decode: each token row as 8 MXFP4 pieces (see
- * moe_layer_forward), rows 8t .. 8t+7 of a 128-row tensor-core tile (codes in xa, scales in
- * xa_s; the other rows are not written).  Writes the per-expert plan (padded offsets, tile table)
- * into ws for the expert calls that follow. */
+ * For MOE_ACT_MXFP4 and MOE_ACT_MXFP8, unless xa and xa_s are both NULL, it also quantises every
+ * token row of x once and writes the activation operand of the [moe_padded_rows][d] matrix of
+ * permuted rows in padded expert-grouped order (expert e's rows start at a multiple of 128;
+ * padding rows are zero): xa in the tensor-core code tiles and xa_s in the tensor-core scale
+ * layout (moe_mxfp4_mma_scale_bytes(moe_padded_rows, d) bytes).  MXFP4 code tiles are those of
+ * the weights (moe_padded_rows*d/2 bytes); MXFP8 code tiles (moe_padded_rows*d bytes) hold 128
+ * rows x 128 E4M3 bytes each, tile (R, C) at index R*(d/128) + C, the 16-byte chunk j of row r
+ * at byte r*128 + (j XOR (r%8))*16.  For MOE_ACT_BF16, xa and xa_s are unused (may be NULL).
+ * Writes the per-expert plan (padded offsets, tile table) into ws for the expert calls that
+ * follow. */
 moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int E, int k, moe_act_fmt fmt,
                        int32_t* counts, int32_t* offsets, int32_t* perm_token, int32_t* inv_pos,
                        uint8_t* xa, uint8_t* xa_s, void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -265,9 +274,12 @@ moe_status moe_permute(const uint16_t* x, const int32_t* ids, int T, int d, int 
  * for every permuted row, grouped by expert.  Needs the plan that moe_permute wrote into ws.
  *   MOE_ACT_BF16:  reads x bf16 [T][d] through perm_token; writes h bf16 [P][I] (row r =
  *                  permuted row r), h_s unused.
- *   MOE_ACT_MXFP4: reads xa / xa_s; writes the [moe_padded_rows][I] matrix h in the same padded
- *                  order as MXFP4: codes in the tensor-core code tiles (moe_padded_rows*I/2
- *                  bytes), scales in the tensor-core scale layout (padding rows are zero). */
+ *   MOE_ACT_MXFP4 / MOE_ACT_MXFP8: reads xa / xa_s; writes the [moe_padded_rows][I] matrix h,
+ *                  quantised to the same format, in the same padded order: codes in the
+ *                  tensor-core code tiles of the format (moe_padded_rows*I/2 bytes for MXFP4,
+ *                  moe_padded_rows*I for MXFP8), scales in the tensor-core scale layout (padding
+ *                  rows are zero).  MOE_ACT_MXFP8 reads the weight codes gate_q / up_q (32-byte
+ *                  aligned) and the scale copies gate_s_mma / up_s_mma. */
 moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint8_t* xa_s, moe_act_fmt fmt,
                                 const int32_t* perm_token, const int32_t* offsets, int T, int d, int E, int k,
                                 int I, const moe_expert_weights* W, void* h, uint8_t* h_s, void* ws,
@@ -281,20 +293,30 @@ moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, c
                            const int32_t* offsets, int T, int d, int E, int k, int I, const moe_expert_weights* W,
                            uint16_t* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Bytes of the pieces operand moe_permute writes for moe_expert_ffn_decode: scales = 0 the codes,
- * scales = 1 the scale atoms.  0 when 1 <= T <= 16 and d % 256 == 0 do not hold. */
+/* Bytes of the pieces operand of moe_decode_pieces: scales = 0 the codes, scales = 1 the scale
+ * atoms.  0 when 1 <= T <= 16 and d % 256 == 0 do not hold. */
 size_t moe_decode_pieces_bytes(int T, int d, int scales);
 
+/* The token operand of moe_expert_ffn_decode: each row of x bf16 [T][d] (fmt MOE_ACT_BF16), or
+ * its MXFP8 values (fmt MOE_ACT_MXFP8, the rule of moe_act_fmt), written as 8 MXFP4 pieces (see
+ * moe_layer_forward), rows 8t .. 8t+7 of a 128-row tensor-core tile: codes in xa, scales in xa_s
+ * (moe_decode_pieces_bytes(T, d, 0) and (T, d, 1) bytes, xa and x 16-byte aligned; the other
+ * rows are not written).  1 <= T <= 16 (T = 0 does nothing) and d % 256 == 0
+ * (MOE_ERR_UNSUPPORTED_SHAPE otherwise).  No workspace. */
+moe_status moe_decode_pieces(const uint16_t* x, int T, int d, moe_act_fmt fmt, uint8_t* xa, uint8_t* xa_s,
+                             moe_stream_t stream);
+
 /* Both expert GEMMs of a small batch on the block-scaled FP4 tensor cores, in one persistent
- * launch (the kernels moe_layer_forward runs for MOE_ACT_BF16 with MXFP4 weights carrying their
- * tensor-core copies): gate/up with SwiGLU (section 9) on the token pieces xa / xa_s from
- * moe_permute, h rounded to bf16 and fed to the down GEMM as its own 8 pieces, the expert
- * outputs rounded to bf16 into y_perm [T*k][d] (compact permuted order).  With y != NULL
- * (T <= 4) the weighted sum of moe_combine is fused and written to y bf16 [T][d] (inv_pos and w
- * as moe_combine takes them).  Needs the plan that moe_permute wrote into ws (laid out for the
- * same T, d, E, k, I with MOE_ACT_BF16).  1 <= T <= 16, d % 256 == 0, I % 256 == 0 and MXFP4
- * weights with their tensor-core copies (MOE_ERR_UNSUPPORTED_SHAPE otherwise). */
-moe_status moe_expert_ffn_decode(const uint8_t* xa, const uint8_t* xa_s, const int32_t* perm_token,
+ * launch (the kernels moe_layer_forward runs for MOE_ACT_BF16 and MOE_ACT_MXFP8 with MXFP4
+ * weights carrying their tensor-core copies): gate/up with SwiGLU (section 9) on the token
+ * pieces xa / xa_s from moe_decode_pieces (same fmt), h rounded to bf16 (MOE_ACT_BF16) or to
+ * MXFP8 (MOE_ACT_MXFP8) and fed to the down GEMM as its own 8 pieces, the expert outputs rounded
+ * to bf16 into y_perm [T*k][d] (compact permuted order).  With y != NULL (T <= 4) the weighted
+ * sum of moe_combine is fused and written to y bf16 [T][d] (inv_pos and w as moe_combine takes
+ * them).  Needs the plan that moe_permute wrote into ws (laid out for the same T, d, E, k, I and
+ * fmt).  1 <= T <= 16, d % 256 == 0, I % 256 == 0 and MXFP4 weights with their tensor-core
+ * copies (MOE_ERR_UNSUPPORTED_SHAPE otherwise). */
+moe_status moe_expert_ffn_decode(const uint8_t* xa, const uint8_t* xa_s, moe_act_fmt fmt, const int32_t* perm_token,
                                  const int32_t* offsets, const int32_t* inv_pos, const float* w, int T, int d,
                                  int E, int k, int I, const moe_expert_weights* W, uint16_t* y_perm, uint16_t* y,
                                  void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -331,7 +353,8 @@ moe_status moe_combine_norm(const uint16_t* y_perm, const int32_t* inv_pos, cons
  *   - otherwise (NVFP4 weights, no tensor-core copies, other shapes): CUDA-core GEMVs with
  *     exact products (bf16 activations, fp32 accumulation), down GEMV and weighted sum fused.
  * The step entry points (moe_expert_up_swiglu, moe_expert_down with MOE_ACT_BF16) run the
- * GEMVs. */
+ * GEMVs.  MOE_ACT_MXFP8 runs the first path on the MXFP8 values of x and h for up to 16 tokens,
+ * and the kind::mxf8f6f4 grouped GEMMs beyond (moe_expert_up_swiglu, moe_expert_down). */
 moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                              int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids,
                              float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -350,9 +373,9 @@ moe_status moe_layer_forward_norm(const uint16_t* x, const float* W_r, const flo
  * another widens the weighted sum back): y[t][n] = sum_c a(x[t])[c] * W[n][c] for x bf16 [T][K],
  * W MXFP4 [N][K], y bf16 [T][N] (fp32 accumulation, rounded once to bf16).  a(x) is the
  * activation operand of the format: MOE_ACT_BF16 uses the bf16 values (K % 128 == 0,
- * N % 128 == 0, K <= 8192, N <= 8192); MOE_ACT_MXFP4 quantises each row's 32-element blocks
- * like moe_permute does and runs the tcgen05 GEMM (K % 256 == 0, N % 256 == 0; W's
- * tensor-core copies q_mma / s_mma required).  A latent layer is moe_dense_linear(W_in) ->
+ * N % 128 == 0, K <= 8192, N <= 8192); MOE_ACT_MXFP4 and MOE_ACT_MXFP8 quantise each row's
+ * 32-element blocks like moe_permute does and run the tcgen05 GEMM (K % 256 == 0, N % 256 == 0;
+ * MXFP4: W's tensor-core copies q_mma / s_mma required; MXFP8: s_mma and q 32-byte aligned).  A latent layer is moe_dense_linear(W_in) ->
  * moe_layer_forward with d = the latent width -> moe_dense_linear(W_out).
  * ws: moe_dense_workspace_size(T, K, N, fmt) bytes, 256-byte aligned, initialised with
  * moe_workspace_init; device-side timeouts are reported through it (moe_get_device_status). */

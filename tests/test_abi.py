@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 9
+    assert B.moe_abi_version() == 10
     header = open(os.path.join(ROOT, "include", "moe.h")).read()
     assert int(re.search(r"#define MOE_ABI_VERSION (\d+)", header).group(1)) == B.moe_abi_version()
     assert B.status_string(0) == "MOE_OK"
@@ -55,12 +55,34 @@ def test_size_helpers():
     assert B.moe_workspace_size(16, 256, 8, 2, 384, B.MOE_ACT_MXFP4) == 0
     assert B.moe_workspace_size(16, 384, 8, 2, 512, B.MOE_ACT_MXFP4) == 0  # d % 256 on the MXFP4 path
     assert B.moe_workspace_size(16, 384, 8, 2, 384, B.MOE_ACT_BF16) > 0
+    # MXFP8: the MXFP4 shape rules, one byte per value in the operand buffers
+    assert B.moe_workspace_size(16, 256, 8, 2, 512, B.MOE_ACT_MXFP8) > B.moe_workspace_size(16, 256, 8, 2, 512, 1)
+    assert B.moe_workspace_size(16, 384, 8, 2, 512, B.MOE_ACT_MXFP8) == 0
+    assert B.moe_workspace_size(16, 256, 8, 2, 384, B.MOE_ACT_MXFP8) == 0
+    assert B.moe_workspace_size(16, 256, 8, 2, 512, 3) == 0      # unknown format
+    # decode pieces: up to 16 tokens, d % 256
+    assert B.moe_decode_pieces_bytes(16, 8192, 0) == 128 * 8192 // 2
+    assert B.moe_decode_pieces_bytes(16, 8192, 1) == 64 * 512
+    assert B.moe_decode_pieces_bytes(17, 8192, 0) == 0
+    assert B.moe_decode_pieces_bytes(4, 384, 0) == 0
 
 
 def test_library_is_built_for_sm103a_only():
     from bit_expert_ffn_moe_gb300 import _build
     assert "arch=compute_103a,code=sm_103a" in _build.NVCC_FLAGS
     assert os.path.exists(_build.LIB)
+
+
+def test_decode_pieces_arguments_are_checked_on_the_host(lib):
+    # format and shape rules are checked before anything is launched
+    assert lib.moe_decode_pieces(256, 4, 8192, B.MOE_ACT_MXFP4, 256, 256, None) == B.MOE_ERR_INVALID_ARG
+    assert lib.moe_decode_pieces(256, 17, 8192, B.MOE_ACT_BF16, 256, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_decode_pieces(256, 4, 384, B.MOE_ACT_MXFP8, 256, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_decode_pieces(256, 0, 8192, B.MOE_ACT_MXFP8, None, None, None) == B.MOE_OK
+    assert lib.moe_decode_pieces(None, 4, 8192, B.MOE_ACT_MXFP8, 256, 256, None) == B.MOE_ERR_INVALID_ARG
+    W = B.moe_expert_weights()
+    assert lib.moe_expert_ffn_decode(256, 256, B.MOE_ACT_MXFP4, 256, 256, 256, 256, 4, 8192, 128, 8, 2048, W, 256, None,
+                                     256, 1 << 30, None) == B.MOE_ERR_INVALID_ARG
 
 
 def test_selftest_arguments_are_checked_on_the_host(lib):
@@ -85,6 +107,8 @@ def test_expert_norm_arguments_are_checked_on_the_host(lib):
 def test_dense_linear_shapes_and_arguments_are_checked_on_the_host(lib):
     assert B.moe_dense_workspace_size(4, 8192, 4096, B.MOE_ACT_MXFP4) > B.moe_dense_workspace_size(4, 8192, 4096, 0)
     assert B.moe_dense_workspace_size(4, 384, 256, B.MOE_ACT_MXFP4) == 0    # K % 256 on the MXFP4 path
+    assert B.moe_dense_workspace_size(4, 8192, 4096, B.MOE_ACT_MXFP8) > B.moe_dense_workspace_size(4, 8192, 4096, 1)
+    assert B.moe_dense_workspace_size(4, 384, 256, B.MOE_ACT_MXFP8) == 0
     assert B.moe_dense_workspace_size(4, 384, 256, B.MOE_ACT_BF16) > 0
     assert B.moe_dense_workspace_size(4, 200, 256, B.MOE_ACT_BF16) == 0     # K % 128
     assert B.moe_dense_workspace_size(4, 16384, 256, B.MOE_ACT_BF16) == 0   # K <= 8192 on the GEMV path

@@ -31,9 +31,13 @@ def device_matrix(q, s, with_mma):
     return B.mxfp4_matrix_struct(qd, sd, q_mma, s_mma), keep
 
 
+ACT = {"bf16": B.MOE_ACT_BF16, "mxfp4": B.MOE_ACT_MXFP4, "mxfp8": B.MOE_ACT_MXFP8}
+OACT = {"bf16": O.ACT_BF16, "mxfp4": O.ACT_MXFP4, "mxfp8": O.ACT_MXFP8}
+
+
 def gpu_dense(xb, W, N, fmt):
     T, K = xb.shape
-    act = B.MOE_ACT_BF16 if fmt == "bf16" else B.MOE_ACT_MXFP4
+    act = ACT[fmt]
     ws = torch.empty(B.moe_dense_workspace_size(T, K, N, act), dtype=torch.uint8, device="cuda")
     B.moe_workspace_init(ws)
     y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
@@ -50,6 +54,9 @@ DENSE_CASES = [
     (50, 256, 512, "mxfp4", None),      # one ragged token tile
     (300, 512, 256, "mxfp4", None),     # two full tiles and a ragged one
     (4096, 8192, 4096, "mxfp4", 48),    # prefill-sized, sampled rows
+    (50, 256, 512, "mxfp8", None),      # kind::mxf8f6f4: one ragged token tile
+    (300, 512, 256, "mxfp8", None),
+    (4096, 8192, 4096, "mxfp8", 48),
 ]
 
 
@@ -57,12 +64,12 @@ DENSE_CASES = [
 def test_dense_linear_matches_oracle(T, K, N, fmt, n_check):
     seed = 5000 + T + K + N
     q, s = oracle_matrix(seed, TENSOR_W_IN, 0, N, K, 0.02)
-    W, _keep = device_matrix(q, s, fmt == "mxfp4")
+    W, _keep = device_matrix(q, s, fmt != "bf16")
     rng = np.random.default_rng(seed)
     xb = IN.to_bf16_bits(rng.standard_normal((T, K)).astype(np.float32))
     y = bf16_tensor_to_f32(gpu_dense(xb, W, N, fmt))
     rows = np.arange(T) if n_check is None else np.sort(rng.choice(T, n_check, replace=False))
-    ref = O.dense_linear(xb[rows], (q, s), O.ACT_BF16 if fmt == "bf16" else O.ACT_MXFP4)
+    ref = O.dense_linear(xb[rows], (q, s), OACT[fmt])
     check_outputs(y[rows], ref, "dense %dx%dx%d %s" % (T, K, N, fmt))
 
 

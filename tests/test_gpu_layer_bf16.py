@@ -131,7 +131,7 @@ def test_bad_arguments_are_rejected():
 
 @pytest.mark.parametrize("name", ["tiny", "decode", "spec_verify", "ring_t3", "ring_t2"])
 def test_tensor_core_step_calls_equal_layer_call(name):
-    """moe_route -> moe_permute (with the pieces operand) -> moe_expert_ffn_decode (-> moe_combine
+    """moe_route -> moe_permute -> moe_decode_pieces -> moe_expert_ffn_decode (-> moe_combine
     beyond four tokens) gives the layer call's output bit for bit, and the expert outputs match the
     oracle's intermediates."""
     layer = get_layer(name, mma=True)
@@ -151,9 +151,10 @@ def test_tensor_core_step_calls_equal_layer_call(name):
     y_perm = torch.empty((P, d), dtype=torch.bfloat16, device="cuda")
     y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
     B.moe_route(x, layer.W_r, layer.b, T, d, E, k, ids, w, ws)
-    B.moe_permute(x, ids, T, d, E, k, B.MOE_ACT_BF16, counts, offsets, perm, inv, xa, xa_s, ws)
+    B.moe_permute(x, ids, T, d, E, k, B.MOE_ACT_BF16, counts, offsets, perm, inv, None, None, ws)
+    B.moe_decode_pieces(x, T, d, B.MOE_ACT_BF16, xa, xa_s)
     fused = T <= 4
-    B.moe_expert_ffn_decode(xa, xa_s, perm, offsets, inv, w, T, d, E, k, I, layer.weights, y_perm,
+    B.moe_expert_ffn_decode(xa, xa_s, B.MOE_ACT_BF16, perm, offsets, inv, w, T, d, E, k, I, layer.weights, y_perm,
                             y if fused else None, ws)
     if not fused:
         B.moe_combine(y_perm, inv, w, T, k, d, y)
