@@ -33,6 +33,18 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense FP4 : dense bf16 nominal ratio on GB300 (6x)
+NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25   # dense FP8 (kind::mxf8f6f4) : dense bf16 (2x)
+ACT_FMTS = {"bf16": 0, "mxfp4": 1, "mxfp8": 2}  # moe_act_fmt values
+
+
+def grouped_gemm_path(fmt: int, T: int) -> bool:
+    """Whether the layer runs the tensor-bound grouped prefill GEMMs (MXFP4 always; MXFP8 beyond 16
+    tokens, below which it runs the decode kernels)."""
+    return fmt == 1 or (fmt == 2 and T > 16)
+
+
+def tensor_peak_ratio(fmt: int) -> float:
+    return NOMINAL_FP8_OVER_BF16 if fmt == 2 else NOMINAL_FP4_OVER_BF16
 N_LAYER_COPIES = 4
 
 
@@ -231,7 +243,7 @@ def run_gpu(args, cfg, rank, world, local):
     dev = torch.device("cuda", local)
     init_dist(world, "nccl")
     B.load(build_if_missing=False)
-    fmt = B.MOE_ACT_BF16 if args.fmt == "bf16" else B.MOE_ACT_MXFP4
+    fmt = ACT_FMTS[args.fmt]
     T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I  # d: the model width of x and y
     cm = moe_cfg(args, cfg)  # the layer's configuration (its width dl = cm.d)
     dl = cm.d
@@ -366,7 +378,7 @@ def run_gpu(args, cfg, rank, world, local):
         "roofline": roof,
         "e2e": e2e,
         "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None, lat is not None,
-                                          fmt == B.MOE_ACT_BF16 and args.weights == "mxfp4"
+                                          fmt != B.MOE_ACT_MXFP4 and args.weights == "mxfp4"
                                           and B.moe_decode_pieces_bytes(T, dl, 0) > 0 and I % 256 == 0) * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
@@ -378,16 +390,17 @@ def run_gpu(args, cfg, rank, world, local):
 
 def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, world, extra_flops=0.0):
     """Whole-layer fraction of the roofline the workload is quoted against: HBM bytes for the
-    decode path; for the prefill path the FP4 tensor peak (useful flops 6 P d I per step, plus
-    extra_flops of the latent projections), with the HBM fraction beside it."""
+    decode path; for the prefill path the FP4 (MXFP8 activations: FP8) tensor peak (useful flops
+    6 P d I per step, plus extra_flops of the latent projections), with the HBM fraction beside it."""
     out = {"bound": "hbm", "algorithmic_bytes_per_step": layer_bytes,
            "achieved_GBps": round(layer_bytes / (ms_per_step / 1e3) / 1e9, 1),
            "peak_GBps": pk["hbm_gbs"], "frac": round(layer_bytes / (ms_per_step / 1e3) / bw, 4),
            "peak_source": pk["source"], "mean_active_experts": round(mean_active, 2)}
-    if fmt != 0:
+    if grouped_gemm_path(fmt, cfg.T):
+        ratio = tensor_peak_ratio(fmt)
         flops = (6.0 * cfg.T * cfg.k * cfg.d * cfg.I + extra_flops) * world
-        peak_tf = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16 * world
-        peak_sus = pk["bf16_tflops_sustained"] * NOMINAL_FP4_OVER_BF16 * world
+        peak_tf = pk["bf16_tflops"] * ratio * world
+        peak_sus = pk["bf16_tflops_sustained"] * ratio * world
         achieved = flops / (ms_per_step / 1e3) / 1e12
         # the read-vs-compute roofline of the step: whichever of the weight read and the FP4 math
         # takes longer bounds it
@@ -396,8 +409,8 @@ def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, worl
         t_roof = max(t_bytes, t_flops)
         out = {"bound": "tensor", "algorithmic_flops_per_step": flops, "achieved_TFLOPs": round(achieved, 1),
                "peak_TFLOPs": round(peak_tf, 1), "frac": round(achieved / peak_tf, 4),
-               "peak_source": pk["source"] + " bf16 burst x %.0f (nominal FP4 : bf16 dense ratio)"
-                              % NOMINAL_FP4_OVER_BF16,
+               "peak_source": pk["source"] + " bf16 burst x %.0f (nominal %s : bf16 dense ratio)"
+                              % (ratio, "FP8" if fmt == 2 else "FP4"),
                "frac_of_sustained_peak": round(achieved / peak_sus, 4), "sustained_peak_TFLOPs": round(peak_sus, 1),
                "max_roofline": {"t_bytes_us": round(t_bytes * 1e6, 2), "t_flops_us": round(t_flops * 1e6, 2),
                                 "bound": "hbm" if t_bytes >= t_flops else "tensor",
@@ -407,7 +420,9 @@ def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, worl
 
 
 def dtype_name(fmt, wfmt="mxfp4"):
-    return "%s weights x bf16 activations, fp32 accumulate" % wfmt if fmt == 0 else "mxfp4 x mxfp4, fp32 accumulate"
+    if fmt == 0:
+        return "%s weights x bf16 activations, fp32 accumulate" % wfmt
+    return "mxfp4 x mxfp8 (E4M3), fp32 accumulate" if fmt == 2 else "mxfp4 x mxfp4, fp32 accumulate"
 
 
 EXPERT_NORM_EPS = 1e-6
@@ -458,7 +473,7 @@ class Latent:
         from bit_expert_ffn_moe_gb300 import binding as B
         from bit_expert_ffn_moe_gb300.layer import DeviceMatrix
         self.B, self.fmt, self.T, self.dm, self.dl = B, fmt, cfg.T, cfg.d, dl
-        mma = fmt == B.MOE_ACT_MXFP4
+        mma = fmt != B.MOE_ACT_BF16
         self.win = [DeviceMatrix(dl, cfg.d, L.seed, TENSOR_W_IN, cfg.weight_std, mma, dev) for L in layers]
         self.wout = [DeviceMatrix(cfg.d, dl, L.seed, TENSOR_W_OUT, cfg.weight_std, mma, dev) for L in layers]
 
@@ -499,7 +514,7 @@ def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_deco
     # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum.
     # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).
     proj = (2 if fmt == 0 else 4) * 2 if latent else 0
-    if fmt == 0:
+    if fmt == 0 or (fmt == 2 and mma_decode):
         if mma_decode:  # route (+ permute), token pieces, the fused expert kernel (+ separate sum)
             return (1 if T <= 8 else 5) + 2 + (0 if (T <= 4 and not expert_norm) else 1) + proj
         return (3 if T <= 8 else 7) + (1 if expert_norm else 0) + proj
@@ -526,10 +541,10 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
     n = min(args.steps, 200)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     active = []
-    if fmt != B.MOE_ACT_BF16:
+    if grouped_gemm_path(fmt, T):
         return kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n)
     if args.weights == "mxfp4" and B.moe_decode_pieces_bytes(T, d, 0) > 0 and I % 256 == 0:
-        return kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n)
+        return kernel_roofline_decode_mma(args, cfg, layers, xs, fmt, dev, stream, pk, n)
     st = stream.cuda_stream
     with torch.cuda.stream(stream):
         for s in range(n + 3):
@@ -562,7 +577,7 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
             "launches_timed": n, "peak_source": pk["source"] + " (HBM copy bandwidth)"}
 
 
-def kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n):
+def kernel_roofline_decode_mma(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     """bf16 decode path on the tensor cores: the fused expert kernel (umma_decode_layer_kernel: gate/up
     + SwiGLU + down, and the weighted sum for up to four tokens) timed with CUDA events on its stream
     through moe_expert_ffn_decode, after moe_route, moe_permute and moe_decode_pieces (the token pieces).
@@ -575,7 +590,6 @@ def kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n):
 
     T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
     P = T * k
-    fmt = B.MOE_ACT_BF16
     ws = make_workspace(T, d, E, k, I, fmt, dev)
     i32 = dict(dtype=torch.int32, device=dev)
     u8 = dict(dtype=torch.uint8, device=dev)
@@ -624,9 +638,9 @@ def kernel_roofline_decode_mma(args, cfg, layers, xs, dev, stream, pk, n):
 
 
 def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
-    """Prefill path: the tcgen05 gate/up kernel (umma_grouped_kernel<1>) timed with CUDA events
-    on its stream through the step API, against the dense FP4 tensor peak (the measured or
-    fallback bf16 peak times the nominal FP4 : bf16 ratio); its HBM rate is reported beside."""
+    """Prefill path: the tcgen05 gate/up kernel (umma_grouped_kernel<1, fp8>) timed with CUDA events
+    on its stream through the step API, against the dense FP4 (MXFP8 activations: FP8) tensor peak
+    (the measured or fallback bf16 peak times the nominal ratio); its HBM rate is reported beside."""
     import numpy as np
     import torch
 
@@ -642,8 +656,9 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     ids, w = torch.empty((T, k), **i32), torch.empty((T, k), dtype=torch.float32, device=dev)
     counts, offsets, perm, inv = torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(P, **i32), \
         torch.empty(P, **i32)
-    xa, xa_s = torch.empty(R * d // 2, **u8), torch.empty(B.moe_mxfp4_mma_scale_bytes(R, d), **u8)
-    h, h_s = torch.empty(R * I // 2, **u8), torch.empty(B.moe_mxfp4_mma_scale_bytes(R, I), **u8)
+    per_byte = 1 if fmt == 2 else 2  # values per code byte of the token operand and h
+    xa, xa_s = torch.empty(R * d // per_byte, **u8), torch.empty(B.moe_mxfp4_mma_scale_bytes(R, d), **u8)
+    h, h_s = torch.empty(R * I // per_byte, **u8), torch.empty(B.moe_mxfp4_mma_scale_bytes(R, I), **u8)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     active = []
     st = stream.cuda_stream
@@ -667,18 +682,24 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     n_act = float(np.mean([int(a.item()) for a in active]))
     flops = 4.0 * P * d * I  # gate and up: 2 flops per weight per token row
     achieved = flops / (avg_ms / 1e3) / 1e12
-    peak_tf = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
-    hbm_bytes = n_act * up_bytes_per_expert(d, I) + P * (d * 17 // 32) + P * (I * 17 // 32)
-    traffic = ncu_traffic("umma_grouped_prefill.md", ["bit_expert_ffn_moe_gb300/csrc/umma.cu",
-                                                      "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
-    return {"kernel": "umma_grouped_kernel<1> (tcgen05 kind::mxf4 gate/up + SwiGLU, prefill)", "bound": "tensor",
+    ratio = tensor_peak_ratio(fmt)
+    peak_tf = pk["bf16_tflops"] * ratio
+    act_bytes = 33 / 32 if fmt == 2 else 17 / 32  # per value: codes + scale of the token operand / h
+    hbm_bytes = n_act * up_bytes_per_expert(d, I) + P * d * act_bytes + P * I * act_bytes
+    fp8 = fmt == 2
+    traffic = ncu_traffic("umma_grouped_prefill_mxfp8.md" if fp8 else "umma_grouped_prefill.md",
+                          ["bit_expert_ffn_moe_gb300/csrc/umma.cu", "bit_expert_ffn_moe_gb300/csrc/common.cuh"],
+                          cfg.name)
+    return {"kernel": "umma_grouped_kernel<1, %d> (tcgen05 %s gate/up + SwiGLU, prefill)"
+                      % (int(fp8), "kind::mxf8f6f4" if fp8 else "kind::mxf4"), "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(peak_tf, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak_tf, 4), "traffic": traffic,
             "algorithmic_flops_per_launch": flops, "avg_launch_us": round(avg_ms * 1e3, 3), "launches_timed": n,
             "hbm_achieved_GBps": round(hbm_bytes / (avg_ms / 1e3) / 1e9, 1),
             "hbm_frac": round(hbm_bytes / (avg_ms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
             "algorithmic_bytes_per_launch": hbm_bytes,
-            "peak_source": pk["source"] + " bf16 x %.0f (nominal FP4 : bf16 dense ratio)" % NOMINAL_FP4_OVER_BF16}
+            "peak_source": pk["source"] + " bf16 x %.0f (nominal %s : bf16 dense ratio)"
+                           % (ratio, "FP8" if fp8 else "FP4")}
 
 
 def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call):
@@ -825,7 +846,7 @@ def _oracle_sample(args, cfg, n_tokens):
             cache[e] = out
         return cache[e]
 
-    act = O.ACT_BF16 if args.fmt == "bf16" else O.ACT_MXFP4
+    act = {"bf16": O.ACT_BF16, "mxfp4": O.ACT_MXFP4, "mxfp8": O.ACT_MXFP8}[args.fmt]
     eps = norm_eps(args)
     if getattr(args, "latent", 0):
         win = O.mxfp4_pack(IN.synth_weights(layer_seed, TENSOR_W_IN, 0, cm.d, cfg.d, cfg.weight_std))
@@ -917,16 +938,22 @@ SUB_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config"
             "e2e", "gpu_launches", "clocks", "wall_s_timed", "cpu_baseline", "parity")
 
 
+# extra workload name -> (configuration, activation format)
+EXTRA_WORKLOADS = {"prefill": ("prefill", "mxfp4"), "long_prefill": ("long_prefill", "mxfp4"),
+                   "prefill_mxfp8": ("prefill", "mxfp8")}
+
+
 def extra_workloads(args):
-    """Workloads timed after the headline one in the same run: the prefill chunk and one chunk of
-    the long prefill, when the headline is the plain decode workload (no variant options)."""
+    """Workloads timed after the headline one in the same run: the prefill chunk, one chunk of the
+    long prefill, and the prefill chunk with 8-bit activations, when the headline is the plain
+    decode workload (no variant options)."""
     if args.extra == "none":
         return []
     if args.extra != "auto":
         return [n for n in args.extra.split(",") if n]
     plain = (args.config == "decode" and not args.latent and not args.expert_norm and args.weights == "mxfp4"
              and args.fmt == "bf16")
-    return ["prefill", "long_prefill"] if plain else []
+    return ["prefill", "long_prefill", "prefill_mxfp8"] if plain else []
 
 
 def run_workload(args, cfg, rank, world, local):
@@ -956,7 +983,7 @@ def main():
     ap.add_argument("--extra", default="auto",
                     help="workloads timed after the headline one ('auto': prefill and one long-prefill chunk "
                          "when the headline is the plain decode workload; 'none'; or a comma list)")
-    ap.add_argument("--fmt", choices=["bf16", "mxfp4"], default=None)
+    ap.add_argument("--fmt", choices=["bf16", "mxfp4", "mxfp8"], default=None)
     ap.add_argument("--layers", type=int, default=N_LAYER_COPIES)
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -995,7 +1022,8 @@ def main():
     os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
     out = run_workload(args, cfg, rank, world, local)
     # With the default workload the same process also times the prefill chunk and one chunk of the
-    # long prefill (the other half of the metric: the FP4 tensor roofline), each in a sub-object.
+    # long prefill (the other half of the metric: the FP4 tensor roofline) and the prefill chunk with
+    # MXFP8 activations (the FP8 tensor roofline), each in a sub-object.
     for name in extra_workloads(args):
         import gc
 
@@ -1003,8 +1031,9 @@ def main():
         gc.collect()
         torch.cuda.empty_cache()
         sub_args = argparse.Namespace(**vars(args))
-        sub_args.config, sub_args.fmt, sub_args.layers = name, "mxfp4", PREFILL_LAYER_COPIES
-        sub = run_workload(sub_args, IN.CONFIGS[name], rank, world, local)
+        conf, act = EXTRA_WORKLOADS[name]
+        sub_args.config, sub_args.fmt, sub_args.layers = conf, act, PREFILL_LAYER_COPIES
+        sub = run_workload(sub_args, IN.CONFIGS[conf], rank, world, local)
         out[name] = {k: sub[k] for k in SUB_KEYS if k in sub}
     if rank == 0:
         print(json.dumps(out), flush=True)

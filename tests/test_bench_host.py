@@ -182,3 +182,21 @@ def test_oracle_sample_outputs_are_the_parity_rows(T, weights, norm):
                           expert_norm_eps=bench.EXPERT_NORM_EPS if norm else None)["y"]
         np.testing.assert_array_equal(y, ref if rows is None else ref[rows])
     assert O.max_threads() == len(__import__("os").sched_getaffinity(0))  # restored
+
+
+def test_default_line_times_the_prefill_workloads_in_both_activation_formats():
+    import argparse
+    a = argparse.Namespace(extra="auto", config="decode", latent=0, expert_norm=False, weights="mxfp4", fmt="bf16")
+    names = bench.extra_workloads(a)
+    assert names == ["prefill", "long_prefill", "prefill_mxfp8"]
+    assert [bench.EXTRA_WORKLOADS[n] for n in names] == [("prefill", "mxfp4"), ("long_prefill", "mxfp4"),
+                                                          ("prefill", "mxfp8")]
+    a.fmt = "mxfp8"  # a variant headline times nothing else
+    assert bench.extra_workloads(a) == []
+    # the prefill roofline is the FP4 tensor peak for MXFP4 activations, FP8 for MXFP8 beyond 16
+    # tokens; MXFP8 up to 16 tokens runs the decode kernels (HBM-bound)
+    assert bench.grouped_gemm_path(1, 1) and bench.grouped_gemm_path(2, 17) and not bench.grouped_gemm_path(2, 16)
+    assert bench.tensor_peak_ratio(1) == 6.0 and bench.tensor_peak_ratio(2) == 2.0
+    assert bench.launches_per_step(2, 1, 8192, 128, 8, mma_decode=True) == bench.launches_per_step(
+        0, 1, 8192, 128, 8, mma_decode=True)
+    assert bench.launches_per_step(2, 4096, 8192, 128, 8) == 10
