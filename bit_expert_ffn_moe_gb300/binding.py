@@ -159,9 +159,12 @@ def expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s, gate_q_mma
 
 
 def nvfp4_expert_weights_struct(gate_q, gate_s, gate_gs, up_q, up_s, up_gs, down_q, down_s,
-                                down_gs) -> moe_expert_weights:
-    """NVFP4 expert weights: codes, E4M3 scales [.][K/16] and per-expert global scales [E]."""
-    W = expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s)
+                                down_gs, gate_q_mma=None, gate_s_mma=None, up_q_mma=None, up_s_mma=None,
+                                down_q_mma=None, down_s_mma=None) -> moe_expert_weights:
+    """NVFP4 expert weights: codes, E4M3 scales [.][K/16] and per-expert global scales [E], with the
+    tensor-core copies (code tiles; the scales laid out as for a matrix of width 2K) when given."""
+    W = expert_weights_struct(gate_q, gate_s, up_q, up_s, down_q, down_s, gate_q_mma, gate_s_mma, up_q_mma,
+                              up_s_mma, down_q_mma, down_s_mma)
     W.wfmt = MOE_W_NVFP4
     W.gate_gs, W.up_gs, W.down_gs = _p(gate_gs), _p(up_gs), _p(down_gs)
     return W

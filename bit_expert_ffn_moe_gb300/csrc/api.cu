@@ -65,8 +65,8 @@ moe_status check_ws(void* ws, size_t ws_bytes, const WsLayout& L) {
 moe_status check_weights(const moe_expert_weights* W, moe_act_fmt fmt, bool need_up, bool need_down) {
     if (W == nullptr) return MOE_ERR_INVALID_ARG;
     if (W->wfmt != MOE_W_MXFP4 && W->wfmt != MOE_W_NVFP4) return MOE_ERR_INVALID_ARG;
-    if (W->wfmt == MOE_W_NVFP4) {  // the GEMV path only; E4M3 scale pairs are read as 16-bit words
-        if (fmt != MOE_ACT_BF16) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (W->wfmt == MOE_W_NVFP4) {  // the GEMVs (E4M3 scale pairs read as 16-bit words) or kind::mxf4nvf4
+        if (fmt == MOE_ACT_MXFP8) return MOE_ERR_UNSUPPORTED_SHAPE;
         if (need_up && (!W->gate_gs || !W->up_gs || !aligned(W->gate_s, 2) || !aligned(W->up_s, 2)))
             return MOE_ERR_INVALID_ARG;
         if (need_down && (!W->down_gs || !aligned(W->down_s, 2))) return MOE_ERR_INVALID_ARG;
@@ -337,8 +337,16 @@ moe_status moe_expert_up_swiglu(const uint16_t* x, const uint8_t* xa, const uint
     }
     if (!xa || !xa_s || !h_s || !aligned(xa, 16) || !aligned(h, 16)) return MOE_ERR_INVALID_ARG;
     Ctrl* ctrl = reinterpret_cast<Ctrl*>(at(ws, L.ctrl));
+    if (W->wfmt == MOE_W_NVFP4) {  // the token operand's scales as UE4M3 per 16 (workspace)
+        if (!umma_nv_supported(E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        uint8_t* s16 = reinterpret_cast<uint8_t*>(at(ws, L.xa_s16));
+        float* rf = reinterpret_cast<float*>(at(ws, L.xrf));
+        MOE_CUDA(launch_nv_operand_scales(xa_s, plan.scalars + 2, L.pad_rows, d, s16, rf, st, false));
+        return from_cuda(launch_umma_up(xa, s16, plan, offsets, T, d, E, k, I, L.pad_rows, W, false, rf,
+                                        static_cast<uint8_t*>(h), h_s, &ctrl->status, st, true));
+    }
     return from_cuda(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fmt == MOE_ACT_MXFP8,
-                                    static_cast<uint8_t*>(h), h_s, &ctrl->status, st, false));
+                                    nullptr, static_cast<uint8_t*>(h), h_s, &ctrl->status, st, false));
 }
 
 moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, const int32_t* perm_token,
@@ -361,8 +369,16 @@ moe_status moe_expert_down(const void* h, const uint8_t* h_s, moe_act_fmt fmt, c
                                           k, I, W, y_perm, nullptr, &ctrl->status, st, false));
     }
     if (!h_s) return MOE_ERR_INVALID_ARG;
+    if (W->wfmt == MOE_W_NVFP4) {  // h's scales as UE4M3 per 16 (workspace)
+        if (!umma_nv_supported(E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+        uint8_t* s16 = reinterpret_cast<uint8_t*>(at(ws, L.h_s16));
+        float* rf = reinterpret_cast<float*>(at(ws, L.hrf));
+        MOE_CUDA(launch_nv_operand_scales(h_s, plan.scalars + 2, L.pad_rows, I, s16, rf, st, false));
+        return from_cuda(launch_umma_down(static_cast<const uint8_t*>(h), s16, plan, offsets, T, d, E, k, I,
+                                          L.pad_rows, W, false, rf, y_perm, &ctrl->status, st, true));
+    }
     return from_cuda(launch_umma_down(static_cast<const uint8_t*>(h), h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W,
-                                      fmt == MOE_ACT_MXFP8, y_perm, &ctrl->status, st, false));
+                                      fmt == MOE_ACT_MXFP8, nullptr, y_perm, &ctrl->status, st, false));
 }
 
 moe_status moe_combine(const uint16_t* y_perm, const int32_t* inv_pos, const float* w, int T, int k, int d, uint16_t* y,
@@ -458,16 +474,34 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
     uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
     uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
     const bool fp8 = fmt == MOE_ACT_MXFP8;
+    const bool nv = W->wfmt == MOE_W_NVFP4;  // kind::mxf4nvf4: operand scales as UE4M3 per 16
+    if (nv && !umma_nv_supported(E)) return MOE_ERR_UNSUPPORTED_SHAPE;
     MOE_CUDA(launch_act_quant_gather(x, T, d, E, k, offsets, perm, plan, L.pad_rows,
                                      reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
                                      xa, xa_s, fp8, st, true));
     uint8_t* h = reinterpret_cast<uint8_t*>(at(ws, L.h));
     uint8_t* h_s = reinterpret_cast<uint8_t*>(at(ws, L.h_s));
     uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
-    MOE_CUDA(launch_umma_up(xa, xa_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fp8, h, h_s, &ctrl->status, st,
-                            true));
-    MOE_CUDA(launch_umma_down(h, h_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fp8, y_perm, &ctrl->status, st,
-                              true));
+    const uint8_t* up_s = xa_s;
+    const uint8_t* down_s = h_s;
+    float* xrf = nullptr;
+    float* hrf = nullptr;
+    if (nv) {
+        uint8_t* xa_s16 = reinterpret_cast<uint8_t*>(at(ws, L.xa_s16));
+        xrf = reinterpret_cast<float*>(at(ws, L.xrf));
+        MOE_CUDA(launch_nv_operand_scales(xa_s, plan.scalars + 2, L.pad_rows, d, xa_s16, xrf, st, true));
+        up_s = xa_s16;
+    }
+    MOE_CUDA(launch_umma_up(xa, up_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fp8, xrf, h, h_s, &ctrl->status,
+                            st, true));
+    if (nv) {
+        uint8_t* h_s16 = reinterpret_cast<uint8_t*>(at(ws, L.h_s16));
+        hrf = reinterpret_cast<float*>(at(ws, L.hrf));
+        MOE_CUDA(launch_nv_operand_scales(h_s, plan.scalars + 2, L.pad_rows, I, h_s16, hrf, st, true));
+        down_s = h_s16;
+    }
+    MOE_CUDA(launch_umma_down(h, down_s, plan, offsets, T, d, E, k, I, L.pad_rows, W, fp8, hrf, y_perm,
+                              &ctrl->status, st, true));
     if (norm) MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
     else MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
     return MOE_OK;
@@ -541,8 +575,8 @@ moe_status moe_dense_linear(const uint16_t* x, int T, int K, int N, const moe_mx
     MOE_CUDA(launch_act_quant_gather(x, T, K, 1, 1, offsets, perm, plan, L.pad_rows,
                                      reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
                                      xa, xa_s, fp8, st, true));
-    MOE_CUDA(launch_umma_down(xa, xa_s, plan, offsets, T, N, 1, 1, K, L.pad_rows, &Wd, fp8, y, &ctrl->status, st,
-                              true));
+    MOE_CUDA(launch_umma_down(xa, xa_s, plan, offsets, T, N, 1, 1, K, L.pad_rows, &Wd, fp8, nullptr, y,
+                              &ctrl->status, st, true));
     return MOE_OK;
 }
 

@@ -51,6 +51,7 @@ struct WsLayout {
            xq = 0, xs = 0, xa = 0, xa_s = 0, h = 0, h_s = 0, y_perm = 0, total = 0;
     size_t dxa = 0, dxa_s = 0, dha = 0, dha_s = 0;  // decode on the tensor cores: x and h pieces
     size_t dpart = 0;                                // its split gate/up tiles' fp32 partial sums
+    size_t xa_s16 = 0, h_s16 = 0, xrf = 0, hrf = 0;  // NVFP4 weights: operand scales per 16, row factors
     int64_t pad_rows = 0;
 };
 
@@ -116,6 +117,12 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
         L.h = take((size_t)L.pad_rows * I / per_byte);
         L.h_s = take(mma_scale_bytes(L.pad_rows, I));
         L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);
+        if (fmt == MOE_ACT_MXFP4) {  // NVFP4 weights on the tensor cores
+            L.xa_s16 = take(mma_scale_bytes(L.pad_rows, 2 * (int64_t)d));
+            L.h_s16 = take(mma_scale_bytes(L.pad_rows, 2 * (int64_t)I));
+            L.xrf = take(sizeof(float) * (size_t)L.pad_rows);
+            L.hrf = take(sizeof(float) * (size_t)L.pad_rows);
+        }
     } else {
         L.h = take(sizeof(uint16_t) * (size_t)P * I);
         L.y_perm = take(sizeof(uint16_t) * (size_t)P * d);  // expert outputs (normalised layer, tensor-core decode)
@@ -518,11 +525,20 @@ bool mma_decode_fused_sum(int T, int d);
 
 // Grouped prefill GEMMs (umma.cu).  fp8: MXFP8 token operand and h (kind::mxf8f6f4, the weights
 // read from their canonical codes through tensor maps); else MXFP4 (kind::mxf4, tensor-core tiles).
+// NVFP4 weights (W->wfmt) with MXFP4 operands: kind::mxf4nvf4; xa_s / h_s are then the operands'
+// UE4M3 scales and rf their row factors (launch_nv_operand_scales).
 cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets,
                            int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,
-                           bool fp8, uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st, bool pdl);
+                           bool fp8, const float* rf, uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st,
+                           bool pdl);
 cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan, const int32_t* offsets,
                              int T, int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W,
-                             bool fp8, uint16_t* y_perm, int* status, cudaStream_t st, bool pdl);
+                             bool fp8, const float* rf, uint16_t* y_perm, int* status, cudaStream_t st, bool pdl);
+// Whether the kind::mxf4nvf4 GEMMs fit shared memory for E experts.
+bool umma_nv_supported(int E);
+// E8M0 scales of an MXFP4 operand (tensor-core layout of width K, rows_used[0] padded rows) as
+// UE4M3 scales per 16 values (layout of width 2K) and one power-of-two factor per row (nvfp4.cu).
+cudaError_t launch_nv_operand_scales(const uint8_t* s32, const int32_t* rows_used, int64_t pad_rows, int K,
+                                     uint8_t* s16, float* rf, cudaStream_t st, bool pdl);
 }  // namespace moe
 

@@ -112,6 +112,48 @@ __global__ void nv_unpack_kernel(const uint8_t* __restrict__ q, const uint8_t* _
     }
 }
 
+// ------------------------------------------------------------------ MXFP4 rows against NVFP4 weights
+// The tensor cores take NVFP4 weights (kind::mxf4nvf4) only with both operands' scales in UE4M3, one
+// per 16 values.  An MXFP4 operand row keeps its codes; each 32-element block's scale 2^X_b becomes
+// the UE4M3 power of two 2^(X_b - F) on both of its 16-element halves, with one factor 2^F per row,
+// F = max_b X_b - 8, that the GEMM epilogue multiplies back in.  UE4M3 holds the powers of two
+// 2^-9 .. 2^8, so this is exact for every block within 17 binades of the row's largest; a block
+// further below (whose values are below 2^-15 of the row's largest block scale) gets scale 0.
+// One warp per padded row; s32 and s16 in the tensor-core scale layout of width K and 2K.
+__global__ void __launch_bounds__(256) nv_operand_scales_kernel(const uint8_t* __restrict__ s32,
+                                                                const int32_t* __restrict__ rows_used, int K,
+                                                                uint8_t* __restrict__ s16, float* __restrict__ rf) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t used = *rows_used;
+    const int nb = K / 32, lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < used; r += nwarps) {
+        int smax = 0;  // largest scale byte (X + 127) of the row
+        for (int b = lane; b < nb; b += 32) smax = max(smax, (int)s32[mma_scale_offset(r, b, K)]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) smax = max(smax, __shfl_xor_sync(0xffffffffu, smax, o));
+        const int F = smax - 127 - 8;
+        for (int b = lane; b < nb; b += 32) {
+            const int e = (int)s32[mma_scale_offset(r, b, K)] - 127 - F;  // <= 8
+            // UE4M3 of 2^e: normal for e >= -6 (exponent field e + 7), subnormal 2^-7 .. 2^-9
+            const uint32_t u = e >= -6 ? (uint32_t)(e + 7) << 3 : e >= -9 ? 1u << (e + 9) : 0u;
+            *reinterpret_cast<uint16_t*>(s16 + mma_scale_offset(r, 2 * b, 2 * K)) = (uint16_t)(u | (u << 8));
+        }
+        if (lane == 0)  // 2^F, F in [-135, 119]: subnormal below 2^-126
+            rf[r] = F >= -126 ? __uint_as_float((uint32_t)(F + 127) << 23) : __uint_as_float(1u << (F + 149));
+    }
+}
+
+cudaError_t launch_nv_operand_scales(const uint8_t* s32, const int32_t* rows_used, int64_t pad_rows, int K,
+                                     uint8_t* s16, float* rf, cudaStream_t st, bool pdl) {
+    if (pad_rows == 0) return cudaSuccess;
+    int64_t blocks = (pad_rows + 7) / 8;  // 8 warps (rows) per CTA
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    void* args[] = {&s32, &rows_used, &K, &s16, &rf};
+    return launch_kernel((const void*)nv_operand_scales_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, args);
+}
+
 static unsigned nv_grid(int64_t n, int threads) {
     int64_t b = (n + threads - 1) / threads;
     if (b > 152 * 64) b = 152 * 64;

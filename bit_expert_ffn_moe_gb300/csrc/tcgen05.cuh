@@ -1,6 +1,7 @@
 // tcgen05.cuh -- PTX wrappers of the 5th-generation tensor cores (sm_103a) shared by the grouped
 // expert GEMMs: tensor-memory scale copies, block-scaled MMAs (kind::mxf4: E2M1 operands;
-// kind::mxf8f6f4: E4M3 tokens x E2M1 weights; one E8M0 scale per 32 elements in both),
+// kind::mxf8f6f4: E4M3 tokens x E2M1 weights; one E8M0 scale per 32 elements in both;
+// kind::mxf4nvf4: E2M1 operands with one UE4M3 scale per 16 elements),
 // shared-memory and instruction descriptors, tensor-map copies, tensor-memory loads and the
 // commit / fence instructions.  The bit fields are the ones the PTX ISA defines.
 #pragma once
@@ -87,6 +88,54 @@ __device__ __forceinline__ void stage_mmas8_commit(uint32_t d, uint64_t ad, uint
         : "memory");
 }
 
+// 4-bit operands with 16-element UE4M3 scales (kind::mxf4nvf4, scale_vec::4X, K = 64 per MMA): one
+// K step of 256 values takes four scale atoms per 128 rows (each atom: 4 scales of every row, one
+// MMA's K range).  Scale slot (48 columns from sf): A atom i at sf + 4i, B atoms of K range i at
+// sf + 16 + 8i (rows 0..127) and sf + 20 + 8i (rows 128..255).  a, b0, b1: the stage's first
+// atoms (A, B rows 0..127, B rows 128..255), each followed by its next three.
+__device__ __forceinline__ void stage_scales_nv_to_tmem(uint32_t sf, uint64_t a, uint64_t b0, uint64_t b1) {
+    // a descriptor's start address field counts 16-byte units: one 512-byte atom is 32
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%2], %3;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%4], %5;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%6], %7;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%8], %9;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%10], %11;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%12], %13;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%14], %15;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%16], %17;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%18], %19;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%20], %21;\n\t"
+        "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%22], %23;\n\t}" ::"r"(sf),
+        "l"(a), "r"(sf + 4), "l"(a + 32), "r"(sf + 8), "l"(a + 64), "r"(sf + 12), "l"(a + 96), "r"(sf + 16),
+        "l"(b0), "r"(sf + 20), "l"(b1), "r"(sf + 24), "l"(b0 + 32), "r"(sf + 28), "l"(b1 + 32), "r"(sf + 32),
+        "l"(b0 + 64), "r"(sf + 36), "l"(b1 + 64), "r"(sf + 40), "l"(b0 + 96), "r"(sf + 44), "l"(b1 + 96)
+        : "memory");
+}
+
+// The four K = 64 MMAs of a stage with 16-element UE4M3 scales (scale byte selectors 0: an MMA
+// reads all four bytes of its scale columns), then the commit that frees the stage.
+__device__ __forceinline__ void stage_mmas_nv_commit(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sf,
+                                                     uint32_t accumulate, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, q;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "setp.eq.b32 q, %4, %4;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %7, %8, %3, [%9], [%10], q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %11, %12, %3, [%13], [%14], q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %15, %16, %3, [%17], [%18], q;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n\t}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(sf), "r"(sf + 16), "l"(ad + 2), "l"(bd + 2), "r"(sf + 4),
+        "r"(sf + 24), "l"(ad + 4), "l"(bd + 4), "r"(sf + 8), "r"(sf + 32), "l"(ad + 6), "l"(bd + 6), "r"(sf + 12),
+        "r"(sf + 40), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // mbar_wait by every lane of a warp with a warp-uniform verdict.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* status,
                                                long long limit = kWaitCycles) {
@@ -114,6 +163,12 @@ __device__ __forceinline__ uint64_t desc_sf(const void* p) {
 // UE8M0 scales, D fp32, shape M x N; the scale-factor byte selectors are added per MMA.
 __device__ __forceinline__ uint32_t idesc_mxf4(int M, int N) {
     return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Instruction descriptor of kind::mxf4nvf4 with 16-element block scaling: A and B E2M1 (format
+// code 1), K-major, UE4M3 scales (bit 23 clear), D fp32, shape M x N.
+__device__ __forceinline__ uint32_t idesc_mxf4nvf4_ue4m3(int M, int N) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: A E4M3 (format code 0), B E2M1

@@ -53,24 +53,37 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer warp, MMA warp, 8 epi
 constexpr int kTile = 128 * 128;                // 128 rows x 128 bytes (256 FP4 values)
 constexpr int kAtom = 512;                      // scale atom: 128 rows x 4 scales
 constexpr int kStages = 4;
-// A tile, two B tiles (256 weight rows), 2 atoms of A scales, 2 + 2 of B scales (MXFP4: 256 values
-// of K per stage); MXFP8 stages hold 128 values of K: the same three tiles (E4M3 tokens, the FP4
-// weights widened to one byte per value) and one scale atom each
-constexpr int kStageBytes = 3 * kTile + 6 * kAtom;
-static_assert(3 * kTile + 3 * kAtom <= kStageBytes, "an MXFP8 stage fits the stage ring");
+// MMA kinds of the grouped GEMMs: MXFP4 tokens x MXFP4 weights (kind::mxf4), MXFP8 tokens x MXFP4
+// weights (kind::mxf8f6f4), MXFP4 tokens x NVFP4 weights (kind::mxf4nvf4, 16-element UE4M3 scales)
+constexpr int kMxf4 = 0, kMxf8 = 1, kNvf4 = 2;
+// Bytes of a stage: the A tile, two B tiles (256 weight rows) and the scale atoms -- kind::mxf4:
+// 256 values of K, 2 atoms of A scales and 2 + 2 of B scales; kind::mxf8f6f4: 128 values of K (E4M3
+// tokens, the FP4 weights widened to one byte per value), one atom each (A's in a 2-atom slot, so
+// that every stage starts on the 1024-byte boundary the 128-byte swizzle needs); kind::mxf4nvf4:
+// 256 values of K with 16-element scales, 4 atoms of A scales and 4 + 4 of B scales.
+template <int KIND>
+__host__ __device__ constexpr int stage_bytes() { return 3 * kTile + (KIND == kMxf8 ? 4 : KIND == kNvf4 ? 12 : 6) * kAtom; }
+static_assert(stage_bytes<kMxf4>() % 1024 == 0 && stage_bytes<kMxf8>() % 1024 == 0 &&
+                  stage_bytes<kNvf4>() % 1024 == 0,
+              "stages start on 1024-byte boundaries");
 // bytes an MXFP8 stage's copies signal: a widened weight box counts its packed global bytes (8 KB)
 constexpr int kStageTx8 = kTile + 2 * (kTile / 2) + 3 * kAtom;
 constexpr int kAccBufs = 1;
 constexpr int kAccCols = 256;
 constexpr int kSfBase = kAccBufs * kAccCols;  // scale slots after the accumulator
-constexpr int kSfCols = 24;                   // per stage: A scales 8 columns, B scales 16
+// tensor-memory scale columns per stage: A 8 + B 16 (A 16 + B 32 for 16-element scales)
+template <int KIND>
+__host__ __device__ constexpr int sf_cols() { return KIND == kNvf4 ? 48 : 24; }
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarBytes = 256;
-static_assert(kSfBase + kStages * kSfCols <= (int)kTmemCols, "tensor memory budget");
+static_assert(kSfBase + kStages * sf_cols<kNvf4>() <= (int)kTmemCols, "tensor memory budget");
 
+template <int KIND>
 constexpr size_t smem_bytes(int E) {
-    return (size_t)kStages * kStageBytes + 1024 /* alignment */ + kBarBytes + (size_t)4 * (E + 1) * sizeof(int32_t);
+    return (size_t)kStages * stage_bytes<KIND>() + 1024 /* alignment */ + kBarBytes +
+           (size_t)4 * (E + 1) * sizeof(int32_t);
 }
+constexpr size_t kMaxSmem = 232448;  // 227 KB per CTA
 
 // ------------------------------------------------------------------ kernel arguments / tiles
 struct UmmaArgs {
@@ -93,6 +106,11 @@ struct UmmaArgs {
     uint8_t* h_s;  // up: scales, tensor-core layout
     uint16_t* y_perm;  // down: bf16 [P][d]
     int* status;
+    // NVFP4 weights: per padded A row the power-of-two factor its UE4M3 scales leave out, and the
+    // weight matrices' global scales per expert (B rows 0..127 / 128..255)
+    const float* rf;
+    const float* gs0;
+    const float* gs1;
 };
 
 // Plan copied to shared memory once per CTA.
@@ -125,8 +143,11 @@ __device__ __forceinline__ Tile decode_tile(int t, int& e, const SmemPlan& sp, c
 }
 
 // ------------------------------------------------------------------ the kernel
-template <bool IS_UP, bool FP8>
+template <bool IS_UP, int KIND>
 __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_constant__ UmmaArgs args) {
+    constexpr bool FP8 = KIND == kMxf8, NV = KIND == kNvf4;
+    constexpr int kStageBytes = stage_bytes<KIND>();
+    constexpr int kSfCols = sf_cols<KIND>();
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -149,7 +170,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
     auto stage_a = [&](int s) { return smem + (size_t)s * kStageBytes; };
     auto stage_b = [&](int s) { return smem + (size_t)s * kStageBytes + kTile; };  // 256 rows
     auto stage_sfa = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile; };
-    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile + 2 * kAtom; };  // 2 x 1 KB
+    // B scales: rows 0..127, then rows 128..255 (each 2 atoms; 1 for 8-bit tokens, after A's 2-atom
+    // slot; 4 with 16-element scales)
+    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile + (NV ? 4 : 2) * kAtom; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -185,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
 
     const int n_tiles = args.plan.scalars[1] * args.NB;
     const int KT = args.K / (FP8 ? 128 : 256);  // K steps: 128 bytes of every operand row
-    const int atoms_per_rowblk = args.K / 128;
+    const int atoms_per_rowblk = args.K / (NV ? 64 : 128);
 
     if (warp == 0) {
         // ---------------------------------------------------------- copy producer
@@ -220,13 +243,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
                         bulk_load(stage_sfb(s) + kAtom, sfb1 + (size_t)kt * kAtom, kAtom, &full[s]);
                         continue;
                     }
+                    constexpr int kStageAtoms = NV ? 4 : 2;  // scale atoms per operand block per K step
                     mbar_arrive_expect_tx(&full[s], kStageBytes);
                     bulk_load(stage_a(s), qa + (size_t)kt * kTile, kTile, &full[s]);
                     bulk_load(stage_b(s), qb0 + (size_t)kt * kTile, kTile, &full[s]);
                     bulk_load(stage_b(s) + kTile, qb1 + (size_t)kt * kTile, kTile, &full[s]);
-                    bulk_load(stage_sfa(s), sfa + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
-                    bulk_load(stage_sfb(s), sfb0 + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
-                    bulk_load(stage_sfb(s) + 2 * kAtom, sfb1 + (size_t)kt * 2 * kAtom, 2 * kAtom, &full[s]);
+                    bulk_load(stage_sfa(s), sfa + (size_t)kt * kStageAtoms * kAtom, kStageAtoms * kAtom, &full[s]);
+                    bulk_load(stage_sfb(s), sfb0 + (size_t)kt * kStageAtoms * kAtom, kStageAtoms * kAtom, &full[s]);
+                    bulk_load(stage_sfb(s) + kStageAtoms * kAtom, sfb1 + (size_t)kt * kStageAtoms * kAtom,
+                              kStageAtoms * kAtom, &full[s]);
                 }
             }
             if (*abort_flag) {
@@ -243,7 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
         // ---------------------------------------------------------- MMA issuer (whole warp)
         int kiter = 0, it = 0;
         bool ok = true;
-        const uint32_t idesc = FP8 ? idesc_mxf8_e4m3_e2m1(128, 256) : idesc_mxf4(128, 256);
+        const uint32_t idesc = FP8 ? idesc_mxf8_e4m3_e2m1(128, 256)
+                                   : NV ? idesc_mxf4nvf4_ue4m3(128, 256) : idesc_mxf4(128, 256);
         for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
             const int buf = it % kAccBufs;
             const uint32_t use = it / kAccBufs;
@@ -260,6 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
                 tc_fence_after();
                 const uint32_t sf = tmem + kSfBase + s * kSfCols;
                 // the stage is free once these MMAs have read it
+                if (NV) {
+                    stage_scales_nv_to_tmem(sf, desc_sf(stage_sfa(s)), desc_sf(stage_sfb(s)),
+                                            desc_sf(stage_sfb(s) + 4 * kAtom));
+                    stage_mmas_nv_commit(d_tmem, desc_sw128(stage_a(s)), desc_sw128(stage_b(s)), idesc, sf,
+                                         kt > 0 ? 1u : 0u, &empty[s]);
+                    continue;
+                }
                 if (FP8) {
                     stage_scales8_to_tmem(sf, desc_sf(stage_sfa(s)), desc_sf(stage_sfb(s)), desc_sf(stage_sfb(s) + kAtom));
                     stage_mmas8_commit(d_tmem, desc_sw128(stage_a(s)), desc_sw128(stage_b(s)), idesc, sf,
@@ -309,6 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            // NVFP4 weights: the accumulators miss the A row's power-of-two factor and the weight
+            // matrices' global scales
+            float f0 = 1.f, f1 = 1.f;
+            if (NV) {
+                const float r = __ldg(args.rf + T.a_row + m);
+                f0 = r * __ldg(args.gs0 + T.e);
+                f1 = r * __ldg(args.gs1 + T.e);
+            }
             if (IS_UP) {
                 const int I = args.n_out;
                 const size_t row = (size_t)T.a_row + m;  // every padded row is written (zeros there)
@@ -317,7 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
                     float hv[32];
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float gv = __uint_as_float(v[cc][i]), uv = __uint_as_float(v[2 + cc][i]);
+                        float gv = __uint_as_float(v[cc][i]), uv = __uint_as_float(v[2 + cc][i]);
+                        if (NV) {
+                            gv *= f0;
+                            uv *= f1;
+                        }
                         hv[i] = __fdividef(gv, 1.f + __expf(-gv)) * uv;  // SiLU(g) * u
                     }
                     const int blk = 4 * T.p + 2 * half + cc;  // 32-block of h along I
@@ -348,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
                         uint32_t w4[4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c][8 * a + 2 * i]),
-                                                                      __uint_as_float(v[c][8 * a + 2 * i + 1]));
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c][8 * a + 2 * i]) * f0,
+                                                                      __uint_as_float(v[c][8 * a + 2 * i + 1]) * f0);
                             w4[i] = *reinterpret_cast<uint32_t*>(&b2);
                         }
                         pc[a] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
@@ -377,11 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_grouped_kernel(const __grid_
 }
 
 // ------------------------------------------------------------------ host side
-template <bool IS_UP, bool FP8>
+template <bool IS_UP, int KIND>
 cudaError_t launch_grouped(const UmmaArgs& args, cudaStream_t st, bool pdl) {
-    const void* f = (const void*)umma_grouped_kernel<IS_UP, FP8>;
+    const void* f = (const void*)umma_grouped_kernel<IS_UP, KIND>;
     void* kargs[] = {const_cast<UmmaArgs*>(&args)};
-    return launch_kernel(f, dim3(sm_count()), dim3(kThreads), smem_bytes(args.E), st, pdl, kargs);
+    return launch_kernel(f, dim3(sm_count()), dim3(kThreads), smem_bytes<KIND>(args.E), st, pdl, kargs);
 }
 
 typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -423,9 +468,11 @@ cudaError_t fp4_widening_map(CUtensorMap* m, const uint8_t* q, int64_t rows, int
 
 }  // namespace
 
+bool umma_nv_supported(int E) { return smem_bytes<kNvf4>(E) <= kMaxSmem; }
+
 cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan, const int32_t* offsets, int T,
                            int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W, bool fp8,
-                           uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st, bool pdl) {
+                           const float* rf, uint8_t* h, uint8_t* h_s, int* status, cudaStream_t st, bool pdl) {
     (void)T;
     (void)k;
     if (pad_rows == 0) return cudaSuccess;
@@ -446,15 +493,21 @@ cudaError_t launch_umma_up(const uint8_t* xa, const uint8_t* xa_s, PlanView plan
     a.h = h;
     a.h_s = h_s;
     a.status = status;
-    if (!fp8) return launch_grouped<true, false>(a, st, pdl);
+    if (W->wfmt == MOE_W_NVFP4) {
+        a.rf = rf;
+        a.gs0 = W->gate_gs;
+        a.gs1 = W->up_gs;
+        return launch_grouped<true, kNvf4>(a, st, pdl);
+    }
+    if (!fp8) return launch_grouped<true, kMxf4>(a, st, pdl);
     cudaError_t err = fp4_widening_map(&a.tmap_b0, W->gate_q, (int64_t)E * I, d);
     if (err == cudaSuccess) err = fp4_widening_map(&a.tmap_b1, W->up_q, (int64_t)E * I, d);
-    return err == cudaSuccess ? launch_grouped<true, true>(a, st, pdl) : err;
+    return err == cudaSuccess ? launch_grouped<true, kMxf8>(a, st, pdl) : err;
 }
 
 cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan, const int32_t* offsets, int T,
                              int d, int E, int k, int I, int64_t pad_rows, const moe_expert_weights* W, bool fp8,
-                             uint16_t* y_perm, int* status, cudaStream_t st, bool pdl) {
+                             const float* rf, uint16_t* y_perm, int* status, cudaStream_t st, bool pdl) {
     (void)T;
     (void)k;
     if (pad_rows == 0) return cudaSuccess;
@@ -474,10 +527,15 @@ cudaError_t launch_umma_down(const uint8_t* h, const uint8_t* h_s, PlanView plan
     a.n_out = d;
     a.y_perm = y_perm;
     a.status = status;
-    if (!fp8) return launch_grouped<false, false>(a, st, pdl);
+    if (W->wfmt == MOE_W_NVFP4) {
+        a.rf = rf;
+        a.gs0 = a.gs1 = W->down_gs;
+        return launch_grouped<false, kNvf4>(a, st, pdl);
+    }
+    if (!fp8) return launch_grouped<false, kMxf4>(a, st, pdl);
     cudaError_t err = fp4_widening_map(&a.tmap_b0, W->down_q, (int64_t)E * d, I);
     if (err == cudaSuccess) a.tmap_b1 = a.tmap_b0;
-    return err == cudaSuccess ? launch_grouped<false, true>(a, st, pdl) : err;
+    return err == cudaSuccess ? launch_grouped<false, kMxf8>(a, st, pdl) : err;
 }
 
 }  // namespace moe

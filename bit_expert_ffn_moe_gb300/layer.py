@@ -16,7 +16,8 @@ class DeviceLayer:
     """One synthetic layer of workload ``cfg`` on ``device``.  ``layer`` selects an independent
     copy (different weight seed), used to rotate layers so that L2 cannot carry experts.
     ``wfmt``: "mxfp4" (E8M0 scale per 32 values) or "nvfp4" (E4M3 scale per 16 values and a
-    global scale per expert matrix; read by the bf16-activation path only)."""
+    global scale per expert matrix; read by the bf16-activation GEMVs and, with its tensor-core
+    copies, by the MXFP4-activation grouped GEMMs (kind::mxf4nvf4))."""
 
     def __init__(self, cfg: IN.Config, device="cuda", layer: int = 0, mma_layouts: bool = True,
                  chunk_bytes: int = 1 << 30, wfmt: str = "mxfp4"):
@@ -52,14 +53,14 @@ class DeviceLayer:
             self.q[tid], self.s[tid], self.gs[tid] = q, s, gs
         G, U, D = IN.TENSOR_GATE, IN.TENSOR_UP, IN.TENSOR_DOWN
         self.q_mma = {}
-        if nv:
-            mma_layouts = False
-        if mma_layouts and d % 256 == 0 and I % 256 == 0:  # copies for the tensor-core (MXFP4) path
+        if mma_layouts and d % 256 == 0 and I % 256 == 0:  # copies for the tensor-core paths
             for tid, (rows, K) in shapes.items():
                 self.q_mma[tid] = torch.empty(E * rows * K // 2, **u8)
                 B.moe_mxfp4_codes_to_mma(self.q[tid], E * rows, K, self.q_mma[tid])
-                self.s_mma[tid] = torch.empty(B.moe_mxfp4_mma_scale_bytes(E * rows, K), **u8)
-                B.moe_mxfp4_scales_to_mma(self.s[tid], E * rows, K, self.s_mma[tid])
+                # NVFP4: 16-element scales [rows][K/16] lay out like the scales of a width-2K matrix
+                Ks = 2 * K if nv else K
+                self.s_mma[tid] = torch.empty(B.moe_mxfp4_mma_scale_bytes(E * rows, Ks), **u8)
+                B.moe_mxfp4_scales_to_mma(self.s[tid], E * rows, Ks, self.s_mma[tid])
         W_r, b = IN.make_router(cfg)
         if layer != 0:  # independent router per layer copy
             rng = np.random.default_rng([cfg.seed, 77, layer])
@@ -69,7 +70,9 @@ class DeviceLayer:
         self.b = torch.from_numpy(b).to(self.device)
         if nv:
             self.weights = B.nvfp4_expert_weights_struct(self.q[G], self.s[G], self.gs[G], self.q[U], self.s[U],
-                                                         self.gs[U], self.q[D], self.s[D], self.gs[D])
+                                                         self.gs[U], self.q[D], self.s[D], self.gs[D],
+                                                         self.q_mma.get(G), self.s_mma.get(G), self.q_mma.get(U),
+                                                         self.s_mma.get(U), self.q_mma.get(D), self.s_mma.get(D))
         else:
             self.weights = B.expert_weights_struct(self.q[G], self.s[G], self.q[U], self.s[U], self.q[D], self.s[D],
                                                    self.q_mma.get(G), self.s_mma.get(G), self.q_mma.get(U),

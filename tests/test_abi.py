@@ -126,11 +126,13 @@ def test_nvfp4_arguments_are_checked_on_the_host(lib):
     assert lib.moe_nvfp4_pack(256, 1, 4, 64, 256, 257, 256, None) == B.MOE_ERR_INVALID_ARG  # s 2-byte aligned
     assert lib.moe_nvfp4_pack(None, 0, 4, 64, None, None, None, None) == B.MOE_OK
     assert lib.moe_nvfp4_unpack(256, 256, 256, 1, 4, 40, 256, None) == B.MOE_ERR_UNSUPPORTED_SHAPE
-    # NVFP4 expert weights: the bf16-activation path only, global scales required, known formats
+    # NVFP4 expert weights: the bf16-activation GEMVs, or MXFP4 activations on the tensor cores
+    # with the weights' tensor-core copies; not MXFP8; global scales required; known formats
     W = B.nvfp4_expert_weights_struct(256, 256, 256, 256, 256, 256, 256, 256, 256)
     args = (256, 256, None, 4, 256, 8, 2, 512)
     tail = (256, None, None, 256, 1 << 30, None)
-    assert lib.moe_layer_forward(*args, W, B.MOE_ACT_MXFP4, *tail) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_layer_forward(*args, W, B.MOE_ACT_MXFP8, *tail) == B.MOE_ERR_UNSUPPORTED_SHAPE
+    assert lib.moe_layer_forward(*args, W, B.MOE_ACT_MXFP4, *tail) == B.MOE_ERR_INVALID_ARG  # no copies
     W.down_gs = None
     assert lib.moe_layer_forward(*args, W, B.MOE_ACT_BF16, *tail) == B.MOE_ERR_INVALID_ARG
     W.down_gs = 256
