@@ -249,8 +249,10 @@ def run_gpu(args, cfg, rank, world, local):
     dl = cm.d
     n_calls = max(cfg.calls, 1)
 
-    layers = [DeviceLayer(cm, device=dev, layer=i + 1000 * rank, mma_layouts=(args.weights == "mxfp4"),
-                          wfmt=args.weights) for i in range(args.layers)]
+    # tensor-core weight copies: every MXFP4 path; NVFP4 weights use theirs with MXFP4 activations
+    layers = [DeviceLayer(cm, device=dev, layer=i + 1000 * rank,
+                          mma_layouts=(args.weights == "mxfp4" or args.fmt == "mxfp4"), wfmt=args.weights)
+              for i in range(args.layers)]
     lat = Latent(cfg, dl, fmt, dev, layers) if args.latent else None
     # all seeded inputs resident in HBM before timing
     xs_host = np.stack([IN.make_x(cfg, call=(c + rank * 100000) % (1 << 20)) for c in range(min(n_calls, 1000))])
@@ -379,7 +381,8 @@ def run_gpu(args, cfg, rank, world, local):
         "e2e": e2e,
         "gpu_launches": launches_per_step(fmt, T, d, E, k, norm_eps(args) is not None, lat is not None,
                                           fmt != B.MOE_ACT_MXFP4 and args.weights == "mxfp4"
-                                          and B.moe_decode_pieces_bytes(T, dl, 0) > 0 and I % 256 == 0) * args.steps,
+                                          and B.moe_decode_pieces_bytes(T, dl, 0) > 0 and I % 256 == 0,
+                                          fmt == B.MOE_ACT_MXFP4 and args.weights == "nvfp4") * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed": round(t_wall, 4),
         "_parity_y": parity_y,
@@ -422,7 +425,7 @@ def layer_roofline(fmt, cfg, layer_bytes, ms_per_step, bw, pk, mean_active, worl
 def dtype_name(fmt, wfmt="mxfp4"):
     if fmt == 0:
         return "%s weights x bf16 activations, fp32 accumulate" % wfmt
-    return "mxfp4 x mxfp8 (E4M3), fp32 accumulate" if fmt == 2 else "mxfp4 x mxfp4, fp32 accumulate"
+    return "mxfp4 x mxfp8 (E4M3), fp32 accumulate" if fmt == 2 else "%s x mxfp4, fp32 accumulate" % wfmt
 
 
 EXPERT_NORM_EPS = 1e-6
@@ -508,7 +511,7 @@ class Latent:
         return B.MOE_OK
 
 
-def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_decode=False):
+def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_decode=False, nv_grouped=False):
     # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
     # gate/up, down+sum; with the expert normalisation the down GEMV and the (normalising) sum are
     # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum.
@@ -518,7 +521,7 @@ def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_deco
         if mma_decode:  # route (+ permute), token pieces, the fused expert kernel (+ separate sum)
             return (1 if T <= 8 else 5) + 2 + (0 if (T <= 4 and not expert_norm) else 1) + proj
         return (3 if T <= 8 else 7) + (1 if expert_norm else 0) + proj
-    return 10 + proj
+    return 10 + (2 if nv_grouped else 0) + proj  # NVFP4 weights: + the two operand-scale conversions
 
 
 def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
@@ -685,13 +688,16 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     ratio = tensor_peak_ratio(fmt)
     peak_tf = pk["bf16_tflops"] * ratio
     act_bytes = 33 / 32 if fmt == 2 else 17 / 32  # per value: codes + scale of the token operand / h
-    hbm_bytes = n_act * up_bytes_per_expert(d, I) + P * d * act_bytes + P * I * act_bytes
+    hbm_bytes = n_act * up_bytes_per_expert(d, I, args.weights) + P * d * act_bytes + P * I * act_bytes
     fp8 = fmt == 2
-    traffic = ncu_traffic("umma_grouped_prefill_mxfp8.md" if fp8 else "umma_grouped_prefill.md",
-                          ["bit_expert_ffn_moe_gb300/csrc/umma.cu", "bit_expert_ffn_moe_gb300/csrc/common.cuh"],
+    nv = args.weights == "nvfp4"
+    kind = 2 if nv else int(fp8)
+    profile = "umma_grouped_prefill_mxfp8.md" if fp8 else ("umma_grouped_prefill_nvfp4.md" if nv
+                                                           else "umma_grouped_prefill.md")
+    traffic = ncu_traffic(profile, ["bit_expert_ffn_moe_gb300/csrc/umma.cu", "bit_expert_ffn_moe_gb300/csrc/common.cuh"],
                           cfg.name)
     return {"kernel": "umma_grouped_kernel<1, %d> (tcgen05 %s gate/up + SwiGLU, prefill)"
-                      % (int(fp8), "kind::mxf8f6f4" if fp8 else "kind::mxf4"), "bound": "tensor",
+                      % (kind, ["kind::mxf4", "kind::mxf8f6f4", "kind::mxf4nvf4"][kind]), "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(peak_tf, 1), "unit": "TFLOP/s",
             "frac": round(achieved / peak_tf, 4), "traffic": traffic,
             "algorithmic_flops_per_launch": flops, "avg_launch_us": round(avg_ms * 1e3, 3), "launches_timed": n,
@@ -1009,8 +1015,8 @@ def main():
         cfg = dataclasses.replace(cfg, E=args.experts, note=cfg.note + " (E=%d for profiling)" % args.experts)
     if args.fmt is None:
         args.fmt = "bf16" if cfg.T <= 8 or args.weights == "nvfp4" else "mxfp4"
-    if args.weights == "nvfp4" and args.fmt != "bf16":
-        ap.error("NVFP4 expert weights are read by the bf16-activation path only")
+    if args.weights == "nvfp4" and args.fmt == "mxfp8":
+        ap.error("NVFP4 expert weights are read by the bf16 and MXFP4 activation paths")
     rank, world, local = dist_env()
 
     if args.impl == "reference":

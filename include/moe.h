@@ -28,7 +28,7 @@
  *   - Shape rules (MOE_ERR_UNSUPPORTED_SHAPE otherwise): 1 <= k <= min(E, 32); E <= 1024;
  *     T >= 0; MOE_ACT_BF16: d % 128 == 0 and I % 32 == 0; MOE_ACT_MXFP4 and MOE_ACT_MXFP8:
  *     d % 256 == 0 and I % 256 == 0 (whole 256-value MMA tiles along both contractions).  NVFP4
- *     expert weights (moe_weight_fmt) are read by the MOE_ACT_BF16 path only.
+ *     expert weights (moe_weight_fmt) are read by MOE_ACT_BF16 and MOE_ACT_MXFP4 (not MXFP8).
  *
  * MXFP4 tensor layout ("canonical"): a [rows][K] matrix is stored as codes q[rows][K/2]
  * (element 2i in the low nibble of byte i, element 2i+1 in the high nibble; bit 3 of a code
@@ -80,7 +80,15 @@ typedef enum moe_act_fmt { MOE_ACT_BF16 = 0, MOE_ACT_MXFP4 = 1, MOE_ACT_MXFP8 = 
  *                  Spark Open explainer, section 11): the same E2M1 codes q[rows][K/2], one
  *                  E4M3 scale (OCP OFP8: bias 7, largest finite 448) per 16 consecutive
  *                  elements of a row, s[rows][K/16], and one fp32 global scale per matrix;
- *                  value = E2M1 * E4M3 * global.  Read by the MOE_ACT_BF16 path only. */
+ *                  value = E2M1 * E4M3 * global.  Read by the MOE_ACT_BF16 GEMVs and, with
+ *                  their tensor-core copies (codes: moe_mxfp4_codes_to_mma; scales:
+ *                  moe_mxfp4_scales_to_mma of s read as a [rows][2K] matrix's E8M0 scales, i.e.
+ *                  rows x K/16 bytes), by the MOE_ACT_MXFP4 grouped GEMMs (tcgen05
+ *                  kind::mxf4nvf4).  There the MXFP4 operands' block scales 2^X are carried as
+ *                  UE4M3 powers of two per 16 values relative to one power-of-two factor per row
+ *                  (2^(largest X of the row - 8)), which is exact for every block within 17
+ *                  binades of the row's largest; a block further below is dropped (its values
+ *                  are under 2^-15 of the row's largest block scale). */
 typedef enum moe_weight_fmt { MOE_W_MXFP4 = 0, MOE_W_NVFP4 = 1 } moe_weight_fmt;
 
 /* Expert weights of one layer (all device pointers, canonical MXFP4 layout):
