@@ -518,8 +518,12 @@ def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_deco
     # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).
     proj = (2 if fmt == 0 else 4) * 2 if latent else 0
     if fmt == 0 or (fmt == 2 and mma_decode):
-        if mma_decode:  # route (+ permute), token pieces, the fused expert kernel (+ separate sum)
-            return (1 if T <= 8 else 5) + 2 + (0 if (T <= 4 and not expert_norm) else 1) + proj
+        if mma_decode:
+            # up to 8 tokens (E <= 152): one launch that routes, builds the token pieces and runs both
+            # GEMMs; beyond: route + permute, token pieces, the expert kernel; + a separate sum when
+            # the weighted sum is not fused (more than four tokens, or normalised expert outputs)
+            sep_sum = 0 if (T <= 4 and not expert_norm) else 1
+            return (1 if (T <= 8 and E <= 152) else 5 + 1 + 1) + sep_sum + proj
         return (3 if T <= 8 else 7) + (1 if expert_norm else 0) + proj
     return 10 + (2 if nv_grouped else 0) + proj  # NVFP4 weights: + the two operand-scale conversions
 

@@ -426,6 +426,22 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
         // few tokens, MXFP4 weights with their tensor-core copies: the expert GEMMs on the tensor
         // cores, each activation row (bf16, or its MXFP8 values) fed as 8 MXFP4 pieces (decode_mma.cu)
         const bool mx8 = fmt == MOE_ACT_MXFP8;
+        uint8_t* dxa = reinterpret_cast<uint8_t*>(at(ws, L.dxa));
+        uint8_t* dxa_s = reinterpret_cast<uint8_t*>(at(ws, L.dxa_s));
+        uint8_t* dha = reinterpret_cast<uint8_t*>(at(ws, L.dha));
+        uint8_t* dha_s = reinterpret_cast<uint8_t*>(at(ws, L.dha_s));
+        uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
+        const bool fused = !norm && mma_decode_fused_sum(T, d);
+        if (mma_decode_route_supported(T, d, E, k)) {
+            // one launch: the kernel routes its tokens and builds their pieces itself
+            const DecRoute r = {x, W_r, b, reinterpret_cast<float*>(at(ws, L.logits)), ids_b, w_b, counts, row_w};
+            MOE_CUDA(launch_mma_decode(dxa, dxa_s, dha, dha_s, reinterpret_cast<float*>(at(ws, L.dpart)), plan,
+                                       offsets, perm, T, d, E, k, I, W, mx8, y_perm, inv, w_b, fused ? y : nullptr,
+                                       ctrl, st, true, &r));
+            if (norm) MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
+            else if (!fused) MOE_CUDA(launch_combine(y_perm, inv, w_b, T, k, d, y, st, true));
+            return MOE_OK;
+        }
         if (route_decode_supported(T, d, E, k)) {
             MOE_CUDA(launch_route_decode(x, W_r, b, T, d, E, k, reinterpret_cast<float*>(at(ws, L.logits)), ids_b, w_b,
                                          counts, offsets, perm, inv, row_w, plan, ctrl, st, true));
@@ -433,13 +449,7 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
             MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
             MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true, w_b, row_w));
         }
-        uint8_t* dxa = reinterpret_cast<uint8_t*>(at(ws, L.dxa));
-        uint8_t* dxa_s = reinterpret_cast<uint8_t*>(at(ws, L.dxa_s));
-        uint8_t* dha = reinterpret_cast<uint8_t*>(at(ws, L.dha));
-        uint8_t* dha_s = reinterpret_cast<uint8_t*>(at(ws, L.dha_s));
-        uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));
         MOE_CUDA(launch_x_pieces(x, T, d, mx8, dxa, dxa_s, st, true));
-        const bool fused = !norm && mma_decode_fused_sum(T, d);
         MOE_CUDA(launch_mma_decode(dxa, dxa_s, dha, dha_s, reinterpret_cast<float*>(at(ws, L.dpart)), plan, offsets,
                                    perm, T, d, E, k, I, W, mx8, y_perm, inv, w_b, fused ? y : nullptr, ctrl, st,
                                    true));

@@ -428,6 +428,24 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
+// L2 policy for data read once per call: evicted first, so that a stream larger than L2 does not
+// push out what later calls reuse (the code of the kernels, router weights, control counters).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_load with an L2 cache policy (l2_policy_evict_first).
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding kernel's results / let the next
 // kernel start its prologue.  No-ops when the launch did not use the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -516,11 +534,26 @@ cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, bool mx8, uint8_t* 
 // slot's h operand), expert outputs to y_perm; with y != nullptr (T <= 4, d <= 64 * 256) the weighted
 // sum y[t] = sum_j w[t][j] y_perm[inv_pos[t k + j]] (fp32, slot order, then bf16) is fused too.
 // mx8: h is rounded to MXFP8 (else bf16) before its pieces are formed.
+// route != nullptr (mma_decode_route_supported): the launch also routes -- it computes the logits,
+// the token pieces (into xa / xa_s), the top-k and the plan itself and writes ids, w, counts,
+// offsets, perm_token, inv_pos, row_w and the plan like the one-launch router; otherwise all of them
+// come from the preceding kernels.
+struct DecRoute {
+    const uint16_t* x;
+    const float* W_r;
+    const float* b;
+    float* logits;
+    int32_t* ids;
+    float* w;
+    int32_t* counts;
+    float* row_w;
+};
+bool mma_decode_route_supported(int T, int d, int E, int k);
 cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* ha, uint8_t* ha_s, float* part,
                               PlanView plan, const int32_t* offsets, const int32_t* perm_token, int T, int d, int E,
                               int k, int I, const moe_expert_weights* W, bool mx8, uint16_t* y_perm,
                               const int32_t* inv_pos, const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st,
-                              bool pdl);
+                              bool pdl, const DecRoute* route = nullptr);
 bool mma_decode_fused_sum(int T, int d);
 
 // Grouped prefill GEMMs (umma.cu).  fp8: MXFP8 token operand and h (kind::mxf8f6f4, the weights

@@ -40,6 +40,7 @@
 //         rounded to bf16, stored as that permuted row of y_perm (the weighted sum follows).
 // Every barrier wait is bounded: on expiry the CTA records MOE_ERR_TIMEOUT, stops issuing work,
 // waits (bounded) for its own copies and MMAs, frees tensor memory and exits.
+#include "route_common.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -51,18 +52,37 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTile = kStageTileBytes;
 constexpr int kAtom = kScaleAtomBytes;
-constexpr int kStages = 4;
-constexpr int kStageBytes = 3 * kTile + 6 * kAtom;
+// Stage ring: every stage holds the A rows that carry data (8 piece rows per token: 1 KB of the
+// 128-row tile per token, in its own 1024-byte-aligned region), the two 16 KB weight tiles and the
+// six scale atoms; up to kMaxStages stages.  The MMA still reads 128 A rows: the rows past the
+// live ones lie in the next region and only reach accumulator lanes that no epilogue reads.
+// (Six stages for one token -- 50% more weight bytes in flight per SM -- measured slower on GB300:
+// 60.5 against 57.3 us per decode step; five for four tokens: 138.5 against 137.4 us.)
+constexpr int kMaxStages = 4;
+constexpr int kSmemBudget = 232448;  // 227 KB per CTA
+__host__ __device__ constexpr int dec_a_region(int T) { return 1024 * (T < kDecMaxT ? T : kDecMaxT); }
+__host__ __device__ constexpr int dec_stage_bytes(int T) { return dec_a_region(T) + 2 * kTile + 6 * kAtom; }
 constexpr int kAccCols = 256;
 constexpr int kSfBase = kAccCols;
 constexpr int kSfCols = 24;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBarBytes = 512;
-static_assert(kSfBase + kStages * kSfCols <= (int)kTmemCols, "tensor memory budget");
+static_assert(kSfBase + kMaxStages * kSfCols <= (int)kTmemCols, "tensor memory budget");
 
-__host__ __device__ constexpr size_t dec_smem_bytes(int E) {
-    return (size_t)kStages * kStageBytes + 1024 + kBarBytes + sizeof(int32_t) * (size_t)(2 * E + 2 + kMaxE);
+// Shared memory besides the ring: alignment slack, barriers, and the plan as every CTA holds it
+// (offsets [E+1], active experts [E], pick counts [E], and per slot the token of each permuted row,
+// the permuted row of each slot, the gate weight of each slot and the picked expert).
+__host__ __device__ constexpr size_t dec_fixed_smem(int E, int P) {
+    return 1024 + kBarBytes + sizeof(int32_t) * (size_t)(3 * E + 1 + 4 * P);
 }
+// stages of the ring for T tokens, E experts and k picks per token (0: does not fit)
+__host__ __device__ constexpr int dec_stages(int T, int E, int k) {
+    return (int)(((size_t)kSmemBudget - dec_fixed_smem(E, T * k)) / (size_t)dec_stage_bytes(T)) < kMaxStages
+               ? (int)(((size_t)kSmemBudget - dec_fixed_smem(E, T * k)) / (size_t)dec_stage_bytes(T))
+               : kMaxStages;
+}
+static_assert(dec_stages(kDecMaxT, kMaxE, kMaxK) >= 3, "the largest stages fit three deep");
+static_assert(dec_stage_bytes(1) % 1024 == 0 && dec_stage_bytes(kDecMaxT) % 1024 == 0, "stage alignment");
 
 // ------------------------------------------------------------------ activation pieces
 // Block exponent of a residual block: floor(log2 amax) - 2, plus one when amax > 6 * 2^X, clamped
@@ -128,17 +148,13 @@ __device__ __forceinline__ float absmax8(const float (&r)[8]) {
     return m;
 }
 
-// x pieces: one thread per (token, 32-element block); rows 8t + p of the [128][d] A tile.  mx8: the
-// block is first rounded to its MXFP8 values (E4M3 elements, one power-of-two scale), so the pieces
-// sum to the 8-bit activation operand instead of the bf16 row.
-__global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restrict__ x, int T, int d, int mx8,
-                                                       uint8_t* xa, uint8_t* xa_s) {
-    // the next kernel (the expert GEMMs) may start its set-up now; it waits for this kernel, and so
-    // for the routing, before it reads anything either produced
-    pdl_launch_dependents();
+// The pieces of item i = (token t, 32-element block b) of x: rows 8t + p of the [128][d] A tile.
+// mx8: the block is first rounded to its MXFP8 values (E4M3 elements, one power-of-two scale), so
+// the pieces sum to the 8-bit activation operand instead of the bf16 row.
+__device__ __forceinline__ void x_pieces_item(const uint16_t* __restrict__ x, int i, int d, int mx8, uint8_t* xa,
+                                              uint8_t* xa_s) {
     const int nb = d / 32;
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i < T * nb) {
+    {
         const int t = i / nb, b = i % nb;
         float r[4][8];
         const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * d + 32 * b);
@@ -162,9 +178,9 @@ __global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restric
                 mx8_round4(q0, inv, scale);
                 mx8_round4(q1, inv, scale);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    r[g][i] = q0[i];
-                    r[g][4 + i] = q1[i];
+                for (int m = 0; m < 4; ++m) {
+                    r[g][m] = q0[m];
+                    r[g][4 + m] = q1[m];
                 }
             }
         }
@@ -182,6 +198,16 @@ __global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restric
             xa_s[mma_scale_offset(row, b, d)] = (uint8_t)sb;
         }
     }
+}
+
+// x pieces: one thread per (token, 32-element block).
+__global__ void __launch_bounds__(256) x_pieces_kernel(const uint16_t* __restrict__ x, int T, int d, int mx8,
+                                                       uint8_t* xa, uint8_t* xa_s) {
+    // the next kernel (the expert GEMMs) may start its set-up now; it waits for this kernel, and so
+    // for the routing, before it reads anything either produced
+    pdl_launch_dependents();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < T * (d / 32)) x_pieces_item(x, i, d, mx8, xa, xa_s);
     // the next kernel's dependency wait covers this kernel's predecessors too
     pdl_wait();
 }
@@ -210,7 +236,29 @@ struct DecArgs {
     float* part;                // split gate/up tiles: fp32 partial sums [T*k][I/128][ks][256]
     int ks;                     // K parts per gate/up tile (1: whole tiles)
     int mx8;                    // h rounded to MXFP8 (else bf16) before its pieces are formed
+    int nst;                    // stages of the ring (dec_stages)
+    // Routing inside the kernel (route != 0; up to kRouteMaxT tokens, E at most the grid): every CTA
+    // computes the logits of its expert and a share of the token pieces, and after one grid-wide
+    // arrival every CTA takes the top-k and builds the plan itself; CTA 0 writes the routing
+    // outputs (ids, w, the permutation and the plan, as the one-launch router does).  Otherwise the
+    // plan, offsets, perm_token, inv_pos, w and the token pieces come from the preceding kernels.
+    int route;
+    const uint16_t* x;          // bf16 [T][d]
+    const float* W_r;           // fp32 [E][d]
+    const float* bias;          // fp32 [E] or null
+    float* logits;              // [T][E] (workspace)
+    int32_t* ids_out;           // [T*k]
+    float* w_out;               // [T*k]
+    int32_t* counts_out;        // [E]
+    int32_t* offsets_out;       // [E+1] (= offsets)
+    int32_t* perm_out;          // [T*k] (= perm_token)
+    int32_t* inv_out;           // [T*k] (= inv_pos)
+    float* row_w_out;           // [T*k]
+    uint8_t* xa_w;              // the token pieces this launch writes (= xa, xa_s)
+    uint8_t* xa_s_w;
 };
+
+constexpr int kRouteMaxT = 8;   // tokens the in-kernel routing takes (one warp per token)
 
 // Sum of the accumulator words of one 32-column tensor-memory load over the eight lanes of a lane
 // group (lane bits 0-2), in place: afterwards lane l of the group holds, as fp32 bit patterns in v[0..4), the sums of columns 4 (l & 7) .. 4 (l & 7) + 3.
@@ -236,7 +284,8 @@ __device__ __forceinline__ void group8_reduce32(uint32_t (&v)[32], int lane) {
 // computes y[t][256p .. 256p + 255] = sum_j w[t][j] * y_perm[inv_pos[t k + j]] in fp32 in slot
 // order, rounds it to bf16 and resets the ticket.  A slot whose row lies outside [0, T k)
 // contributes nothing.
-__device__ __forceinline__ void fused_sum(const DecArgs& a, int p, int n_act, int lane) {
+__device__ __forceinline__ void fused_sum(const DecArgs& a, int p, int n_act, int lane, const int32_t* s_inv,
+                                          const float* s_w) {
     __threadfence();  // this lane's y_perm stores before the arrival
     __syncwarp();
     unsigned last = 0;
@@ -249,8 +298,8 @@ __device__ __forceinline__ void fused_sum(const DecArgs& a, int p, int n_act, in
     for (int t = 0; t < a.T; ++t) {
         // lane j holds slot j's row and weight (k <= 32), broadcast below: two dependent loads per
         // token instead of two per slot
-        const int rj = lane < a.k ? __ldcg(a.inv_pos + (size_t)t * a.k + lane) : -1;
-        const float wl = lane < a.k ? __ldcg(a.w + (size_t)t * a.k + lane) : 0.f;
+        const int rj = lane < a.k ? s_inv[t * a.k + lane] : -1;
+        const float wl = lane < a.k ? s_w[t * a.k + lane] : 0.f;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int j0 = 0; j0 < a.k; j0 += 8) {
             uint4 u[8];
@@ -495,7 +544,8 @@ __device__ __forceinline__ void epilogue_up(const DecArgs& args, const DecTile& 
 // Down tile epilogue of one warp: per row of the expert, the sum over its 8 piece lanes rounded to
 // bf16 and stored as that permuted row of y_perm; then (fused weighted sum) the warp's arrival.
 __device__ __forceinline__ void epilogue_down(const DecArgs& args, const DecTile& D, uint32_t acc, int half, int grp,
-                                              int lane, int r0, int cnt, int n_act, uint64_t* acc_empty) {
+                                              int lane, int r0, int cnt, int n_act, uint64_t* acc_empty,
+                                              const int32_t* s_inv, const float* s_w) {
     const bool live = 4 * (grp >> 2) < cnt;
     if (live) {
         uint32_t v[32];
@@ -515,7 +565,7 @@ __device__ __forceinline__ void epilogue_down(const DecArgs& args, const DecTile
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty);
     }
-    if (args.y != nullptr) fused_sum(args, D.p, n_act, lane);
+    if (args.y != nullptr) fused_sum(args, D.p, n_act, lane, s_inv, s_w);
 }
 
 constexpr int kTileQ = 8;  // tile-id queue from the claiming producer to the other roles
@@ -534,10 +584,12 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned* p) {
 __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(const DecArgs args) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int kStages = args.nst;
+    const int kStageBytes = dec_stage_bytes(args.T), kAReg = dec_a_region(args.T);
     uint64_t* full_b = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* full_a = full_b + kStages;
-    uint64_t* empty = full_a + kStages;
-    uint64_t* tq_full = empty + kStages;
+    uint64_t* full_a = full_b + kMaxStages;
+    uint64_t* empty = full_a + kMaxStages;
+    uint64_t* tq_full = empty + kMaxStages;
     uint64_t* tq_empty = tq_full + kTileQ;
     uint64_t* acc_full = tq_empty + kTileQ;
     uint64_t* acc_empty = acc_full + 1;
@@ -545,17 +597,23 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* s_tq = const_cast<int*>(abort_flag) + 1;                                           // [kTileQ]
+    const int P = args.T * args.k;
     int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + kBarBytes);  // [E+1]
     int32_t* s_act = s_off + (args.E + 1);                                                  // [E]
-    int32_t* s_perm = s_act + args.E;                                                       // [T*k]
+    int32_t* s_cnt = s_act + args.E;                                                        // [E]
+    int32_t* s_perm = s_cnt + args.E;                                                       // [P]
+    int32_t* s_inv = s_perm + P;                                                            // [P]
+    float* s_w = reinterpret_cast<float*>(s_inv + P);                                       // [P]
+    int32_t* s_ids = reinterpret_cast<int32_t*>(s_w + P);                                   // [P]
+    __shared__ int s_nact;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Ctrl* ctrl = args.ctrl;
     int* status = &ctrl->status;
 
     auto stage_a = [&](int s) { return smem + (size_t)s * kStageBytes; };
-    auto stage_b = [&](int s) { return smem + (size_t)s * kStageBytes + kTile; };
-    auto stage_sfa = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile; };
-    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + 3 * kTile + 2 * kAtom; };
+    auto stage_b = [&](int s) { return smem + (size_t)s * kStageBytes + kAReg; };
+    auto stage_sfa = [&](int s) { return smem + (size_t)s * kStageBytes + kAReg + 2 * kTile; };
+    auto stage_sfb = [&](int s) { return smem + (size_t)s * kStageBytes + kAReg + 2 * kTile + 2 * kAtom; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -580,17 +638,117 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
 
-    pdl_wait();  // the routing plan and the token pieces come from the preceding kernels
-    const int n_act = args.plan.scalars[0];
-    for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
-        s_off[i] = args.offsets[i];
-        if (i < args.E) s_act[i] = args.plan.active[i];
+    if (args.route) {
+        // ---- routing inside the kernel; the ring's memory stages the router rows meanwhile
+        float* Ws = reinterpret_cast<float*>(smem);                                     // [d]
+        uint16_t* xs = reinterpret_cast<uint16_t*>(smem + sizeof(float) * (size_t)args.d);  // [T][d]
+        const int E = args.E, d = args.d, T = args.T, k = args.k;
+        if ((int)blockIdx.x < E) route_stage_w(args.W_r, blockIdx.x, d, Ws);  // independent of earlier kernels
+        for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
+        pdl_wait();
+        if ((int)blockIdx.x < E) route_stage_x(args.x, T, d, xs);
+        // this CTA's share of the token pieces (items spread over the CTAs first, then the threads),
+        // while the router rows are in flight
+        for (int i = blockIdx.x + gridDim.x * threadIdx.x; i < T * (d / 32); i += gridDim.x * blockDim.x)
+            x_pieces_item(args.x, i, d, args.mx8, args.xa_w, args.xa_s_w);
+        if ((int)blockIdx.x < E) {  // the logits of expert blockIdx.x (E <= the grid)
+            const float2 acc = route_dot_staged(Ws, xs + (size_t)(warp < T ? warp : 0) * d, nullptr, d, warp < T);
+            if (warp < T && lane == 0)
+                args.logits[(size_t)warp * E + blockIdx.x] = acc.x + (args.bias ? args.bias[blockIdx.x] : 0.f);
+        }
+        // one arrival per CTA; every CTA waits for all of them (bounded)
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(&ctrl->route_ticket, 1u);
+            const long long t0 = clock64();
+            while (ld_acquire_u32(&ctrl->route_ticket) < gridDim.x) {
+                if (clock64() - t0 > kWaitCycles) {
+                    set_status(status, MOE_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __syncthreads();
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // others' piece stores -> this CTA's bulk copies
+        if (!*abort_flag) {
+            // all T x E logits into shared memory at once (the staging area is free now), then the
+            // top-k and softmax per token (warp t), the picks counted in s_cnt
+            float* s_logits = Ws;
+            for (int i = threadIdx.x; i < T * E; i += blockDim.x) s_logits[i] = __ldcg(args.logits + i);
+            __syncthreads();
+            if (warp < T) topk_softmax_warp<true>(s_logits + (size_t)warp * E, E, k, s_ids + warp * k, s_w + warp * k, s_cnt);
+            __syncthreads();
+            if (warp == 0) {  // offsets and the active list (and, in CTA 0, the workspace plan)
+                if (blockIdx.x == 0) build_plan_warp(s_cnt, E, args.counts_out, args.offsets_out, args.plan, s_off);
+                const int chunk = (E + 31) / 32, lo = min(E, lane * chunk), hi = min(E, lo + chunk);
+                int c_sum = 0, a_sum = 0;
+                for (int e = lo; e < hi; ++e) {
+                    c_sum += s_cnt[e];
+                    a_sum += s_cnt[e] > 0;
+                }
+                int c_inc = c_sum, a_inc = a_sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int cu = __shfl_up_sync(0xffffffffu, c_inc, o), au = __shfl_up_sync(0xffffffffu, a_inc, o);
+                    if (lane >= o) {
+                        c_inc += cu;
+                        a_inc += au;
+                    }
+                }
+                int c_off = c_inc - c_sum, a_off = a_inc - a_sum;
+                for (int e = lo; e < hi; ++e) {
+                    s_off[e] = c_off;
+                    c_off += s_cnt[e];
+                    if (s_cnt[e] > 0) s_act[a_off++] = e;
+                }
+                if (lane == 31) {
+                    s_off[E] = c_inc;
+                    s_nact = a_inc;
+                }
+            }
+            __syncthreads();
+            for (int p = threadIdx.x; p < P; p += blockDim.x) {  // rows ordered by (expert, token, slot)
+                const int t = p / k, ex = s_ids[p];
+                int rank = 0;  // tokens before t that chose ex (a token picks an expert at most once)
+                for (int t2 = 0; t2 < t; ++t2)
+                    for (int j = 0; j < k; ++j) rank += (s_ids[t2 * k + j] == ex);
+                const int r = s_off[ex] + rank;
+                s_perm[r] = t;
+                s_inv[p] = r;
+                if (blockIdx.x == 0) {
+                    args.ids_out[p] = ex;
+                    args.w_out[p] = s_w[p];
+                    args.perm_out[r] = t;
+                    args.inv_out[p] = r;
+                    args.row_w_out[r] = s_w[p];
+                }
+            }
+        } else if (threadIdx.x == 0) {
+            s_nact = 0;  // timed out: no tiles, straight to the teardown
+        }
+    } else {
+        pdl_wait();  // the routing plan and the token pieces come from the preceding kernels
+        if (threadIdx.x == 0) s_nact = args.plan.scalars[0];
+        for (int i = threadIdx.x; i <= args.E; i += blockDim.x) {
+            s_off[i] = args.offsets[i];
+            if (i < args.E) s_act[i] = args.plan.active[i];
+        }
+        for (int i = threadIdx.x; i < P; i += blockDim.x) {
+            s_perm[i] = args.perm_token[i];
+            if (args.y != nullptr) {
+                s_inv[i] = args.inv_pos[i];
+                s_w[i] = args.w[i];
+            }
+        }
     }
-    for (int i = threadIdx.x; i < args.T * args.k; i += blockDim.x) s_perm[i] = args.perm_token[i];
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int n_act = s_nact;
 
     const int nbu = args.I / 128;
     const int n_up = n_act * nbu * args.ks, n_tiles = n_up + n_act * (args.d / 256);
@@ -607,6 +765,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
         // ---------------------------------------------------------- tile claims + weight copies
         if (lane == 0) {
             int kiter = 0;
+            const uint64_t l2_stream = l2_policy_evict_first();
             for (int q = 0;; ++q) {
                 if (!mbar_wait(&tq_empty[q % kTileQ], ((uint32_t)(q / kTileQ) & 1u) ^ 1u, abort_flag, status)) break;
                 // the first tile of every CTA is its own index; later ones are claimed from the
@@ -628,10 +787,14 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
                         break;
                     }
                     mbar_arrive_expect_tx(&full_b[s], 2 * kTile + 4 * kAtom);
-                    bulk_load(stage_b(s), D.bq0 + (D.rb0 * D.KTT + kt) * kTile, kTile, &full_b[s]);
-                    bulk_load(stage_b(s) + kTile, D.bq1 + (D.rb1 * D.KTT + kt) * kTile, kTile, &full_b[s]);
-                    bulk_load(stage_sfb(s), D.bs0 + (D.rb0 * apr + 2 * kt) * kAtom, 2 * kAtom, &full_b[s]);
-                    bulk_load(stage_sfb(s) + 2 * kAtom, D.bs1 + (D.rb1 * apr + 2 * kt) * kAtom, 2 * kAtom, &full_b[s]);
+                    // the weights are read once per call: evict them first from L2
+                    bulk_load_hint(stage_b(s), D.bq0 + (D.rb0 * D.KTT + kt) * kTile, kTile, &full_b[s], l2_stream);
+                    bulk_load_hint(stage_b(s) + kTile, D.bq1 + (D.rb1 * D.KTT + kt) * kTile, kTile, &full_b[s],
+                                   l2_stream);
+                    bulk_load_hint(stage_sfb(s), D.bs0 + (D.rb0 * apr + 2 * kt) * kAtom, 2 * kAtom, &full_b[s],
+                                   l2_stream);
+                    bulk_load_hint(stage_sfb(s) + 2 * kAtom, D.bs1 + (D.rb1 * apr + 2 * kt) * kAtom, 2 * kAtom,
+                                   &full_b[s], l2_stream);
                 }
                 if (!ok) break;
             }
@@ -656,22 +819,25 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
                 const uint32_t a_bytes = (uint32_t)(rows < 128 ? rows : 128) * 128;
                 const int kt0 = t % D.KT;
                 bool ok = true;
-                if (!D.up) {
-                    // the slot's h pieces: published by every epilogue warp of every gate/up tile of the
-                    // slot (whole tiles), or once per 128-row block (split tiles)
-                    const unsigned need = (unsigned)(args.ks > 1 ? nbu : kEpiWarps * nbu);
+                // Down tiles wait for the slot's h pieces, published by every epilogue warp of a whole
+                // gate/up tile or once per 128-row block by a split tile's last part.  (Waiting per
+                // block, just before the K step that reads it, was measured slower: each acquiring
+                // poll costs a round trip under full load.)
+                auto wait_ready = [&](const unsigned* ctr, unsigned need) {
                     const long long t0 = clock64();
-                    while (ld_acquire_u32(&ctrl->dec_ready[D.u]) < need) {
+                    while (ld_acquire_u32(ctr) < need) {
                         if (*abort_flag || clock64() - t0 > kWaitCycles) {
                             set_status(status, MOE_ERR_TIMEOUT);
                             *abort_flag = 1;
-                            ok = false;
-                            break;
+                            return false;
                         }
                         __nanosleep(64);
                     }
                     asm volatile("fence.proxy.async.global;" ::: "memory");  // generic stores -> bulk copies
-                }
+                    return true;
+                };
+                const unsigned per_block = (unsigned)(args.ks > 1 ? 1 : kEpiWarps);
+                if (!D.up) ok = wait_ready(&ctrl->dec_ready[D.u], per_block * nbu);
                 for (int kk = 0; kk < D.KT && ok; ++kk, ++kiter) {
                     const int s = kiter % kStages;
                     const int kt = D.kbase + (kk + kt0 < D.KT ? kk + kt0 : kk + kt0 - D.KT);
@@ -747,7 +913,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
             if (D.up)
                 epilogue_up(args, D, tmem + lane_base, half, grp, lane, r0, cnt, s_perm, acc_empty, ctrl);
             else
-                epilogue_down(args, D, tmem + lane_base, half, grp, lane, r0, cnt, n_act, acc_empty);
+                epilogue_down(args, D, tmem + lane_base, half, grp, lane, r0, cnt, n_act, acc_empty, s_inv, s_w);
         }
     }
 
@@ -763,6 +929,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) umma_decode_layer_kernel(con
         if (atomicAdd(&ctrl->dec_done, 1u) == gridDim.x - 1) {
             for (int u = 0; u < n_act; ++u) ctrl->dec_ready[u] = 0u;
             ctrl->dec_tile = 0u;
+            if (args.route) ctrl->route_ticket = 0u;
             __threadfence();
             ctrl->dec_done = 0u;
         }
@@ -781,6 +948,12 @@ bool mma_decode_supported(int T, int d, int E, int k, int I, const moe_expert_we
 
 bool mma_decode_fused_sum(int T, int d) { return T <= 4 && d / 256 <= kDecTickets; }
 
+bool mma_decode_route_supported(int T, int d, int E, int k) {
+    const int nst = dec_stages(T, E, k);
+    return T >= 1 && T <= kRouteMaxT && E <= sm_count() &&
+           sizeof(float) * (size_t)d + sizeof(uint16_t) * (size_t)T * d <= (size_t)nst * dec_stage_bytes(T);
+}
+
 cudaError_t launch_x_pieces(const uint16_t* x, int T, int d, bool mx8, uint8_t* xa, uint8_t* xa_s, cudaStream_t st,
                             bool pdl) {
     const int n = T * (d / 32);
@@ -793,9 +966,25 @@ cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* h
                               PlanView plan, const int32_t* offsets, const int32_t* perm_token, int T, int d, int E,
                               int k, int I, const moe_expert_weights* W, bool mx8, uint16_t* y_perm,
                               const int32_t* inv_pos, const float* w, uint16_t* y, Ctrl* ctrl, cudaStream_t st,
-                              bool pdl) {
+                              bool pdl, const DecRoute* route) {
     DecArgs a = {};
     a.mx8 = mx8 ? 1 : 0;
+    if (route != nullptr) {
+        a.route = 1;
+        a.x = route->x;
+        a.W_r = route->W_r;
+        a.bias = route->b;
+        a.logits = route->logits;
+        a.ids_out = route->ids;
+        a.w_out = route->w;
+        a.counts_out = route->counts;
+        a.row_w_out = route->row_w;
+        a.offsets_out = const_cast<int32_t*>(offsets);
+        a.perm_out = const_cast<int32_t*>(perm_token);
+        a.inv_out = const_cast<int32_t*>(inv_pos);
+        a.xa_w = const_cast<uint8_t*>(xa);
+        a.xa_s_w = const_cast<uint8_t*>(xa_s);
+    }
     const int slots = T * k < E ? T * k : E;
     a.ks = slots * (I / 128) <= kDecSplitCounters ? mma_decode_ksplit(T, d) : 1;
     a.part = part;
@@ -822,9 +1011,10 @@ cudaError_t launch_mma_decode(const uint8_t* xa, const uint8_t* xa_s, uint8_t* h
     a.w = w;
     a.y = (y != nullptr && mma_decode_fused_sum(T, d)) ? y : nullptr;
     a.ctrl = ctrl;
+    a.nst = dec_stages(T, E, k);
     void* kargs[] = {&a};
     return launch_kernel((const void*)umma_decode_layer_kernel, dim3(sm_count()), dim3(kThreads + 32),
-                         dec_smem_bytes(E), st, pdl, kargs);
+                         dec_fixed_smem(E, T * k) + (size_t)a.nst * dec_stage_bytes(T), st, pdl, kargs);
 }
 
 }  // namespace moe

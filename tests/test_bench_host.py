@@ -109,10 +109,12 @@ def test_variant_options_name_the_workload_and_count_launches():
     assert bench.launches_per_step(0, 1, 8192, 128, 8, latent=True) == 7
     # prefill: 10 layer kernels; + 2 x (plan, quantise, gather, GEMM)
     # tensor-core decode: route, token pieces, the fused expert kernel (its sum fused up to 4 tokens)
-    assert bench.launches_per_step(0, 1, 8192, 128, 8, mma_decode=True) == 3
-    assert bench.launches_per_step(0, 4, 8192, 128, 8, mma_decode=True) == 3
+    # up to eight tokens: the expert kernel routes its own tokens (one launch; + the normalising sum)
+    assert bench.launches_per_step(0, 1, 8192, 128, 8, mma_decode=True) == 1
+    assert bench.launches_per_step(0, 4, 8192, 128, 8, mma_decode=True) == 1
+    assert bench.launches_per_step(0, 8, 8192, 128, 8, mma_decode=True) == 2
     assert bench.launches_per_step(0, 16, 8192, 128, 8, mma_decode=True) == 8
-    assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True, mma_decode=True) == 4
+    assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True, mma_decode=True) == 2
     assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 10
     assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 18
 
