@@ -16,7 +16,7 @@ constexpr int kPadRows = 128;   // expert row groups of the MXFP4 path start at 
 constexpr int kTokTile = 128;   // token tile (MMA N) of the tcgen05 grouped GEMMs
 
 // ------------------------------------------------------------------ workspace layout
-// Control block (first 4 KB, zeroed by moe_workspace_init): status word, decode-route ticket, and
+// Control block (first 8 KB, zeroed by moe_workspace_init): status word, decode-route ticket, and
 // the counters of the tensor-core decode kernel (decode_mma.cu): its tile claims and finished
 // CTAs, per active slot the epilogue arrivals that publish the slot's h operand, per 256-feature
 // block the arrivals of the down tiles (the last computes the block's weighted sum).  Every counter
@@ -63,7 +63,9 @@ inline bool mma_decode_shape(int T, int d, int I) { return T >= 1 && T <= kMmaDe
 // tiles to occupy every SM, so each tile's K range is split into two parts of at least 8 K steps
 // whose fp32 partial sums are added by the part that finishes last.  (Measured at one token,
 // d = 8192: 54.6 us per step with whole tiles, 51.1 with two parts, 53.8 with four -- more parts
-// fill the SMs but lengthen the partial-sum hand-off that the down tiles wait for.)
+// fill the SMs but lengthen the partial-sum hand-off that the down tiles wait for; half tiles of
+// 64 gate + 64 up rows with the full K range, which need no partial sums, took 60.1 us: their
+// 16 KB weight stages halve the bytes in flight per SM.)
 inline int mma_decode_ksplit(int T, int d) {
     const int kt = d / 256;
     if (T > 2) return 1;
