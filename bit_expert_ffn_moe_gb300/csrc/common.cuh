@@ -64,8 +64,10 @@ inline bool mma_decode_shape(int T, int d, int I) { return T >= 1 && T <= kMmaDe
 // whose fp32 partial sums are added by the part that finishes last.  (Measured at one token,
 // d = 8192: 54.6 us per step with whole tiles, 51.1 with two parts, 53.8 with four -- more parts
 // fill the SMs but lengthen the partial-sum hand-off that the down tiles wait for; half tiles of
-// 64 gate + 64 up rows with the full K range, which need no partial sums, took 60.1 us: their
-// 16 KB weight stages halve the bytes in flight per SM.)
+// 64 gate + 64 up rows with the full K range, which need no partial sums, took 60.1 us with 16 KB
+// weight stages and 54.0 us with two K steps per stage (twice the MMAs and scale copies per weight
+// byte); the two parts on the two CTAs of a cluster, partial sums exchanged through distributed
+// shared memory, took 56.9 us: pair claims keep both CTAs in step and lose the dynamic balance.)
 inline int mma_decode_ksplit(int T, int d) {
     const int kt = d / 256;
     if (T > 2) return 1;
