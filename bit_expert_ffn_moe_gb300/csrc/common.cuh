@@ -67,7 +67,8 @@ inline bool mma_decode_shape(int T, int d, int I) { return T >= 1 && T <= kMmaDe
 // 64 gate + 64 up rows with the full K range, which need no partial sums, took 60.1 us with 16 KB
 // weight stages and 54.0 us with two K steps per stage (twice the MMAs and scale copies per weight
 // byte); the two parts on the two CTAs of a cluster, partial sums exchanged through distributed
-// shared memory, took 56.9 us: pair claims keep both CTAs in step and lose the dynamic balance.)
+// shared memory, took 56.9 us, also when only the gate/up tiles are claimed in pairs and the down
+// tiles alone (57.1 us; the same code with the pairing switched off: 51.8 us).)
 inline int mma_decode_ksplit(int T, int d) {
     const int kt = d / 256;
     if (T > 2) return 1;
