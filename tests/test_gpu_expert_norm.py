@@ -23,20 +23,25 @@ CASES = [
     (IN.CONFIGS["decode"], "bf16", [0], None),
     (IN.CONFIGS["tiny"], "mxfp4", [0, 1], None),
     (IN.CONFIGS["prefill"], "mxfp4", [0], 64),
+    # 8-bit activations: the decode kernels (one token) and the kind::mxf8f6f4 GEMMs (200 tokens)
+    (IN.small_config("norm_mx8_t1", T=1, d=1024, E=16, k=4, I=1024, index=122), "mxfp8", [0], None),
+    (IN.small_config("norm_mx8_pf", T=200, d=512, E=8, k=2, I=768, index=123), "mxfp8", [0], None),
 ]
+ACT = {"bf16": (B.MOE_ACT_BF16, O.ACT_BF16), "mxfp4": (B.MOE_ACT_MXFP4, O.ACT_MXFP4),
+       "mxfp8": (B.MOE_ACT_MXFP8, O.ACT_MXFP8)}
 
 
 @pytest.mark.parametrize("cfg,fmt,calls,n_sample", CASES, ids=[c[0].name + "-" + c[1] for c in CASES])
 def test_normalised_layer_matches_oracle(cfg, fmt, calls, n_sample):
     layer = DeviceLayer(cfg)
-    act = B.MOE_ACT_BF16 if fmt == "bf16" else B.MOE_ACT_MXFP4
+    act, oact = ACT[fmt]
     ws = make_workspace(cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, act)
     for call in calls:
         xb = IN.make_x(cfg, call=call)
         y, ids, w = layer_forward(layer, bits_to_device(xb), act, ws=ws, want_routing=True, expert_norm_eps=EPS)
         tokens = None if n_sample is None else IN.sample_tokens(cfg, n_sample)
-        ref = O.moe_layer(xb, layer.W_r_host, layer.b_host, cfg.k, oracle_expert_weights(cfg, layer.seed),
-                          O.ACT_BF16 if fmt == "bf16" else O.ACT_MXFP4, tokens=tokens, expert_norm_eps=EPS)
+        ref = O.moe_layer(xb, layer.W_r_host, layer.b_host, cfg.k, oracle_expert_weights(cfg, layer.seed), oact,
+                          tokens=tokens, expert_norm_eps=EPS)
         np.testing.assert_array_equal(ids.cpu().numpy(), ref["ids"])
         check_weights(w.cpu().numpy(), ref["w"])
         yg = bf16_tensor_to_f32(y)

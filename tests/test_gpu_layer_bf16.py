@@ -24,6 +24,9 @@ SMALL = {
     "ring_t3": IN.small_config("ring_t3", T=3, d=1024, E=12, k=4, I=512, index=93),
     "ring_t2": IN.small_config("ring_t2", T=2, d=2048, E=6, k=3, I=1536, index=94),
     "ring_t1": IN.small_config("ring_t1", T=1, d=1024, E=16, k=4, I=1024, index=95),
+    # more experts than SMs: the decode kernel takes the plan from the router launches instead of
+    # routing its tokens itself
+    "many_e": IN.small_config("many_e", T=2, d=1024, E=200, k=4, I=512, index=96),
 }
 
 
@@ -46,7 +49,8 @@ def oracle_layer(layer, xb, act_fmt, tokens=None):
 
 @pytest.mark.parametrize("mma", [True, False])
 @pytest.mark.parametrize("name,calls", [("tiny", [0, 1]), ("decode", [0, 1, 2]), ("spec_verify", [0]),
-                                        ("ring_t3", [0, 1]), ("ring_t2", [0, 1]), ("ring_t1", [0, 1, 2])])
+                                        ("ring_t3", [0, 1]), ("ring_t2", [0, 1]), ("ring_t1", [0, 1, 2]),
+                                        ("many_e", [0, 1])])
 def test_layer_matches_oracle(name, calls, mma):
     layer = get_layer(name, mma)
     cfg = layer.cfg

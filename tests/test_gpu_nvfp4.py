@@ -240,6 +240,16 @@ def test_nvfp4_tensor_core_step_calls_equal_layer_call_and_oracle_h():
     check_outputs(bf16_tensor_to_f32(y), ref["y"], "y")
 
 
+def test_nvfp4_tensor_core_layer_with_normalised_expert_outputs():
+    layer = get_nv_mx_layer("nv_mx_prefill")
+    cfg = layer.cfg
+    xb = IN.make_x(cfg, call=3)
+    y = layer_forward(layer, bits_to_device(xb), B.MOE_ACT_MXFP4, expert_norm_eps=O.EXPERT_NORM_EPS)
+    ref = O.moe_layer(xb, layer.W_r_host, layer.b_host, cfg.k, oracle_expert_weights_nv(cfg, layer.seed),
+                      O.ACT_MXFP4, expert_norm_eps=O.EXPERT_NORM_EPS)
+    check_outputs(bf16_tensor_to_f32(y), ref["y"], "nvfp4 x mxfp4 normalised")
+
+
 def test_nvfp4_weights_are_refused_where_no_kernel_takes_them():
     layer = get_layer("nv_tiny")
     cfg = layer.cfg
