@@ -369,11 +369,6 @@ __host__ __device__ __forceinline__ size_t mma8_tile_offset(int64_t row, int64_t
     return (size_t)tile * 16384 + (size_t)(r * 128 + (((c % 8) ^ (r % 8)) * 16));
 }
 
-// Bulk prefetch of [p, p + bytes) into L2 (no completion signal; p and bytes multiples of 16).
-__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
