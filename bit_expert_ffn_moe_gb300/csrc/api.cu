@@ -96,7 +96,20 @@ char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                      int32_t* ids, float* w, void* ws, const WsLayout& L, cudaStream_t st, bool pdl) {
     float* logits = reinterpret_cast<float*>(at(ws, L.logits));
-    MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
+    cudaError_t e = cudaErrorNotSupported;
+    if (L.rs_list) {  // many tokens: tensor-core screen, fixed-order logits of the candidates only
+        const RouterScreenBufs rb = {reinterpret_cast<uint8_t*>(at(ws, L.rs_bhi)),
+                                     reinterpret_cast<uint8_t*>(at(ws, L.rs_blo)),
+                                     reinterpret_cast<float*>(at(ws, L.rs_wn2)),
+                                     reinterpret_cast<float*>(at(ws, L.rs_part)),
+                                     reinterpret_cast<float*>(at(ws, L.rs_xn2)),
+                                     reinterpret_cast<int32_t*>(at(ws, L.rs_cnt)),
+                                     reinterpret_cast<int32_t*>(at(ws, L.rs_list))};
+        e = launch_router_screen(x, W_r, b, T, d, E, k, rb, logits, &reinterpret_cast<Ctrl*>(at(ws, L.ctrl))->status,
+                                 st, pdl);
+        if (e != cudaErrorNotSupported) MOE_CUDA(e);
+    }
+    if (e == cudaErrorNotSupported) MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
     MOE_CUDA(launch_topk(logits, T, E, k, ids, w, st, true));
     return MOE_OK;
 }

@@ -52,6 +52,7 @@ struct WsLayout {
     size_t dxa = 0, dxa_s = 0, dha = 0, dha_s = 0;  // decode on the tensor cores: x and h pieces
     size_t dpart = 0;                                // its split gate/up tiles' fp32 partial sums
     size_t xa_s16 = 0, h_s16 = 0, xrf = 0, hrf = 0;  // NVFP4 weights: operand scales per 16, row factors
+    size_t rs_bhi = 0, rs_blo = 0, rs_wn2 = 0, rs_part = 0, rs_xn2 = 0, rs_cnt = 0, rs_list = 0;  // screened router
     int64_t pad_rows = 0;
 };
 
@@ -81,6 +82,25 @@ inline size_t mma_decode_part_bytes(int T, int d, int k, int I) {
 }
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Router of many tokens (route_screen.cu): tensor-core screen of the logits with a certified bound,
+// fixed-order logits for the candidates only.  S = K splits of the screen (0: the dense fixed-order
+// kernel routes this shape).
+struct RouterScreenSizes {
+    int S;
+    size_t b_bytes, wn2_bytes, part_bytes, xn2_bytes, cnt_bytes, list_bytes;
+};
+struct RouterScreenBufs {
+    uint8_t* bhi;   // bf16 high parts of W_r, tensor-core tiles [E_pad/128][d/64]
+    uint8_t* blo;   // bf16 low parts
+    float* wn2;     // [4][E] shares of ||w_e||^2 (quarters of the row)
+    float* part;    // [S][T][E_pad] screened values per K split
+    float* xn2;     // [S][T] ||x_t||^2 per K split
+    int32_t* cnt;   // [E] candidates per expert
+    int32_t* list;  // [E][T] candidate tokens of each expert
+};
+int router_screen_splits(int T, int d, int E);
+RouterScreenSizes router_screen_sizes(int T, int d, int E);
 
 inline int64_t padded_rows(int T, int k, int E) {
     int64_t P = (int64_t)T * k;
@@ -112,6 +132,16 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
     L.perm = take(sizeof(int32_t) * (size_t)P);
     L.inv = take(sizeof(int32_t) * (size_t)P);
     L.row_w = take(sizeof(float) * (size_t)P);
+    const RouterScreenSizes rs = router_screen_sizes(T, d, E);
+    if (rs.S) {
+        L.rs_bhi = take(rs.b_bytes);
+        L.rs_blo = take(rs.b_bytes);
+        L.rs_wn2 = take(rs.wn2_bytes);
+        L.rs_part = take(rs.part_bytes);
+        L.rs_xn2 = take(rs.xn2_bytes);
+        L.rs_cnt = take(rs.cnt_bytes);
+        L.rs_list = take(rs.list_bytes);
+    }
     if (fmt == MOE_ACT_MXFP4 || fmt == MOE_ACT_MXFP8) {
         const size_t per_byte = fmt == MOE_ACT_MXFP4 ? 2 : 1;  // values per code byte
         L.pad_rows = padded_rows(T, k, E);
@@ -487,6 +517,11 @@ cudaError_t launch_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
                                 float* logits, cudaStream_t st, bool pdl);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl);
+// The screened router's logits (route_screen.cu): exact fixed-order values for every candidate, -inf
+// for the experts the screen ruled out.  cudaErrorNotSupported when the shape or the operands'
+// alignment does not allow it or the tensor-map encoder is missing (route with the dense kernel).
+cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                                 const RouterScreenBufs& rb, float* logits, int* status, cudaStream_t st, bool pdl);
 // Decode route: logits, then the last CTA runs top-k and the whole permutation (small T).
 cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                 float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,

@@ -6,6 +6,8 @@
 // commit / fence instructions.  The bit fields are the ones the PTX ISA defines.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -178,6 +180,32 @@ __device__ __forceinline__ uint32_t idesc_mxf8_e4m3_e2m1(int M, int N) {
     return (0u << 7) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor of kind::f16 with bf16 A and B (format code 1), K-major, D fp32 (format
+// code 1), shape M x N, no sparsity, negation or saturation.
+__device__ __forceinline__ uint32_t idesc_f16_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// One stage of 64 bf16 values of K: the four K = 16 MMAs (descriptors advanced by 32 bytes each);
+// `accumulate` = 0 makes the first one overwrite the accumulator.  Then the commit that frees the
+// stage.
+__device__ __forceinline__ void stage_mmas_bf16_commit(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc,
+                                                       uint32_t accumulate, uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e, p, q;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %3, 0;\n\t"
+        "setp.eq.b32 q, %3, %3;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %6, %4, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %8, %4, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %10, %4, q;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(accumulate), "r"(idesc), "l"(ad + 2), "l"(bd + 2), "l"(ad + 4), "l"(bd + 4), "l"(ad + 6),
+        "l"(bd + 6), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // 2-D tensor-map copy of one box into shared memory, completing on an mbarrier (x: innermost
 // coordinate in elements, y: row).
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
@@ -241,5 +269,13 @@ __device__ __forceinline__ void transpose4_pieces(uint4 (&p)[4], int lane) {
         if (i0) lo = rcv; else hi = rcv;
     }
 }
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), taken through the runtime's entry-point
+// query so that the library needs no link-time dependency on the driver library; null when
+// unavailable.
+typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+encode_tiled_fn tensor_map_encoder();
 
 }  // namespace moe

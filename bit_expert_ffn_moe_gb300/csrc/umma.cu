@@ -429,26 +429,6 @@ cudaError_t launch_grouped(const UmmaArgs& args, cudaStream_t st, bool pdl) {
     return launch_kernel(f, dim3(sm_count()), dim3(kThreads), smem_bytes<KIND>(args.E), st, pdl, kargs);
 }
 
-typedef CUresult (*encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// The driver's tensor-map encoder, taken through the runtime's entry-point query (no link-time
-// dependency on the driver library); null when unavailable.
-encode_tiled_fn tensor_map_encoder() {
-    static encode_tiled_fn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult r;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &r) ==
-                cudaSuccess &&
-            r == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<encode_tiled_fn>(f);
-    });
-    return fn;
-}
-
 // Tensor map of a canonical MXFP4 code matrix q[rows][K/2] read in boxes of 128 values x 128 rows,
 // each 4-bit value given a byte's place in shared memory (16 values in 8 bytes, then 8 empty
 // bytes: the FP4 operand layout of kind::mxf8f6f4) with the 128-byte swizzle.  q must be 32-byte
@@ -467,6 +447,21 @@ cudaError_t fp4_widening_map(CUtensorMap* m, const uint8_t* q, int64_t rows, int
 }
 
 }  // namespace
+
+// The driver's tensor-map encoder, taken through the runtime's entry-point query.
+encode_tiled_fn tensor_map_encoder() {
+    static encode_tiled_fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult r;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess &&
+            r == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<encode_tiled_fn>(f);
+    });
+    return fn;
+}
 
 bool umma_nv_supported(int E) { return smem_bytes<kNvf4>(E) <= kMaxSmem; }
 

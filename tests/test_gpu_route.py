@@ -48,7 +48,7 @@ def test_route_matches_oracle(name):
     check_weights(w, w_o)
 
 
-@pytest.mark.parametrize("T", [64, 5])  # tiled router and one-launch router (small T)
+@pytest.mark.parametrize("T", [64, 5, 600])  # dense router, one-launch router, screened router
 def test_route_ties_and_zero_rows(T):
     d, E, k = 256, 16, 4
     rng = np.random.default_rng(5)
@@ -63,6 +63,28 @@ def test_route_ties_and_zero_rows(T):
     np.testing.assert_array_equal(ids, ids_o)
     check_weights(w, w_o)
     np.testing.assert_array_equal(ids[0], np.arange(k))
+
+
+@pytest.mark.parametrize("E,k,T,d", [(32, 6, 1024, 1024), (300, 8, 700, 512)])
+def test_screened_route_near_ties(E, k, T, d):
+    """Pairs of router rows that differ by a relative 2^-22 (and exact duplicates) give logits closer
+    than any bound the tensor-core screen can certify, at the k-th boundary of many tokens: those
+    experts must reach the fixed-order logits and be decided there, bit for bit as in the oracle."""
+    rng = np.random.default_rng(11)
+    base = rng.standard_normal((E // 2, d)) / np.sqrt(d)
+    W_r = np.empty((E, d), np.float32)
+    W_r[0::2] = base
+    W_r[1::2] = base * (1.0 + 2.0 ** -22)
+    W_r[5] = W_r[4]                                  # an exact tie
+    b = np.repeat(rng.standard_normal(E // 2) * 0.5, 2).astype(np.float32)  # equal bias within a pair
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    x[3] = 0.0
+    x[17] *= 30.0                                    # a large row
+    xb = IN.to_bf16_bits(x)
+    ids, w, _ = gpu_route(xb, W_r, b, k)
+    ids_o, w_o = O.topk_softmax(O.router_logits(xb, W_r, b), k)
+    np.testing.assert_array_equal(ids, ids_o)
+    check_weights(w, w_o)
 
 
 @pytest.mark.parametrize("name", ["tiny", "prefill", "ragged"])
