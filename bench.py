@@ -511,12 +511,20 @@ class Latent:
         return B.MOE_OK
 
 
+def screened_route(T, d, E):
+    """Whether the library routes T tokens with the tensor-core screen (router split, screen,
+    candidates, exact logits, top-k: five launches instead of the dense logits + top-k)."""
+    return T >= 256 and d % 128 == 0 and d <= 32768 and E <= 1024
+
+
 def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_decode=False, nv_grouped=False):
     # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
     # gate/up, down+sum; with the expert normalisation the down GEMV and the (normalising) sum are
     # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum.
-    # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).
+    # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).  Many
+    # tokens: the screened router adds three launches to the route.
     proj = (2 if fmt == 0 else 4) * 2 if latent else 0
+    proj += 3 if screened_route(T, d, E) else 0
     if fmt == 0 or (fmt == 2 and mma_decode):
         if mma_decode:
             # up to 8 tokens (E <= 152): one launch that routes, builds the token pieces and runs both

@@ -299,8 +299,25 @@ __global__ void __launch_bounds__(512) router_cand_kernel(const float* __restric
     __shared__ int lcnt[kMaxE];
     __shared__ uint32_t mask[kCandTok][NV];  // candidate bits of each token: bit l of word i = expert l + 32 i
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ uint32_t s_wm, s_bm;  // bit patterns of non-negative floats order like the values
+    __shared__ int s_fin;
     pdl_wait();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) lcnt[e] = 0;
+    if (threadIdx.x == 0) {
+        s_wm = 0u;
+        s_bm = 0u;
+        s_fin = 1;
+    }
+    __syncthreads();
+    // max ||w_e||^2 and max |b_e| over the experts (the same for every token)
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        lcnt[e] = 0;
+        float w2 = 0.f;
+        for (int q = 0; q < kSplitParts; ++q) w2 += __ldcg(wn2 + (size_t)q * E + e);
+        const float be = b ? __ldg(b + e) : 0.f;
+        if (!isfinite(w2) || !isfinite(be)) s_fin = 0;
+        atomicMax(&s_wm, __float_as_uint(w2));
+        atomicMax(&s_bm, __float_as_uint(fabsf(be)));
+    }
     __syncthreads();
     for (int u = 0; u < kCandTok / 16; ++u) {
         const int tl = warp + 16 * u, t = blockIdx.x * kCandTok + tl;
@@ -308,48 +325,47 @@ __global__ void __launch_bounds__(512) router_cand_kernel(const float* __restric
             if (lane < NV) mask[tl][lane] = 0u;
             continue;
         }
-        // every load of a K split is issued before the sums that wait for them
-        float av[NV], we[NV];
+        // the loads of up to four K splits are issued before the sums that wait for them (in split order)
+        float av[NV];
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int e = lane + 32 * i;
             av[i] = e < E ? __ldcg(part + (size_t)t * E_pad + e) : 0.f;
-            we[i] = 0.f;
         }
         float nx2 = __ldcg(xn2 + t);
-        for (int sp = 1; sp < S; ++sp) {
-            float pv[NV];
+        constexpr int kB = NV <= 8 ? 4 : 1;
+        for (int sp0 = 1; sp0 < S; sp0 += kB) {
+            float pv[kB][NV], xv[kB];
 #pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int e = lane + 32 * i;
-                pv[i] = e < E ? __ldcg(part + ((size_t)sp * T + t) * E_pad + e) : 0.f;
+            for (int q = 0; q < kB; ++q) {
+                const int sp = sp0 + q;
+                xv[q] = 0.f;
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    const int e = lane + 32 * i;
+                    pv[q][i] = sp < S && e < E ? __ldcg(part + ((size_t)sp * T + t) * E_pad + e) : 0.f;
+                }
+                if (sp < S) xv[q] = __ldcg(xn2 + (size_t)sp * T + t);
             }
-            nx2 += __ldcg(xn2 + (size_t)sp * T + t);
 #pragma unroll
-            for (int i = 0; i < NV; ++i) av[i] += pv[i];
+            for (int q = 0; q < kB; ++q)
+                if (sp0 + q < S) {
+#pragma unroll
+                    for (int i = 0; i < NV; ++i) av[i] += pv[q][i];
+                    nx2 += xv[q];
+                }
         }
-        for (int q = 0; q < kSplitParts; ++q)
-#pragma unroll
-            for (int i = 0; i < NV; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E) we[i] += __ldcg(wn2 + (size_t)q * E + e);
-            }
-        bool fin = true;
-        uint32_t wm = 0, bm = 0;  // bit patterns of non-negative floats order like the values
+        bool fin = s_fin != 0;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
             const int e = lane + 32 * i;
             if (e < E) {
-                const float be = b ? __ldg(b + e) : 0.f;
-                av[i] = av[i] + be;
-                fin = fin && isfinite(av[i]) && isfinite(we[i]);
-                wm = max(wm, __float_as_uint(we[i]));
-                bm = max(bm, __float_as_uint(fabsf(be)));
+                av[i] = av[i] + (b ? __ldg(b + e) : 0.f);
+                fin = fin && isfinite(av[i]);
             }
         }
         fin = __all_sync(0xffffffffu, fin);
-        const float wmax2 = __uint_as_float(__reduce_max_sync(0xffffffffu, wm));
-        const float bmax = __uint_as_float(__reduce_max_sync(0xffffffffu, bm));
+        const float wmax2 = __uint_as_float(s_wm), bmax = __uint_as_float(s_bm);
         // the fp32 sums of squares carry a relative error below (terms) 2^-24
         const float infl = 1.f + (float)(d + S + 8) * 0x1p-23f;
         const float nx = __fsqrt_ru(__fmul_ru(nx2, infl));
