@@ -105,11 +105,14 @@ moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T,
                                      reinterpret_cast<float*>(at(ws, L.rs_xn2)),
                                      reinterpret_cast<int32_t*>(at(ws, L.rs_cnt)),
                                      reinterpret_cast<int32_t*>(at(ws, L.rs_list))};
-        e = launch_router_screen(x, W_r, b, T, d, E, k, rb, logits, &reinterpret_cast<Ctrl*>(at(ws, L.ctrl))->status,
-                                 st, pdl);
-        if (e != cudaErrorNotSupported) MOE_CUDA(e);
+        e = launch_router_screen(x, W_r, b, T, d, E, k, rb, logits, ids, w,
+                                 &reinterpret_cast<Ctrl*>(at(ws, L.ctrl))->status, st, pdl);
+        if (e != cudaErrorNotSupported) {
+            MOE_CUDA(e);
+            return MOE_OK;
+        }
     }
-    if (e == cudaErrorNotSupported) MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
+    MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
     MOE_CUDA(launch_topk(logits, T, E, k, ids, w, st, true));
     return MOE_OK;
 }

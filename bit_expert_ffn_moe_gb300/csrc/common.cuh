@@ -517,11 +517,13 @@ cudaError_t launch_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
                                 float* logits, cudaStream_t st, bool pdl);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl);
-// The screened router's logits (route_screen.cu): exact fixed-order values for every candidate, -inf
-// for the experts the screen ruled out.  cudaErrorNotSupported when the shape or the operands'
-// alignment does not allow it or the tensor-map encoder is missing (route with the dense kernel).
+// The screened router (route_screen.cu): logits (exact fixed-order values for every candidate, -inf
+// for the experts the screen ruled out), then launch_topk's ids and w.
+// cudaErrorNotSupported when the shape or the operands' alignment does not allow it or the
+// tensor-map encoder is missing (route with the dense kernel).
 cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
-                                 const RouterScreenBufs& rb, float* logits, int* status, cudaStream_t st, bool pdl);
+                                 const RouterScreenBufs& rb, float* logits, int32_t* ids, float* w, int* status,
+                                 cudaStream_t st, bool pdl);
 // Decode route: logits, then the last CTA runs top-k and the whole permutation (small T).
 cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                 float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,

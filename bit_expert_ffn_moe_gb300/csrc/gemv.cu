@@ -896,16 +896,28 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int t = (int)(i / per_row), c = (int)(i % per_row);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int j = 0; j < k; ++j) {
-            const int r = inv_pos[(size_t)t * k + j];
-            if ((unsigned)r >= (unsigned)(T * k)) continue;  // not a row of y_perm: contributes nothing
-            const float wj = w[(size_t)t * k + j];
-            const uint4 u = *reinterpret_cast<const uint4*>(y_perm + (size_t)r * d + 8 * c);
-            const uint32_t v[4] = {u.x, u.y, u.z, u.w};
+        // up to 8 slots at a time: their rows' loads are issued before the sums (in slot order)
+        for (int j0 = 0; j0 < k; j0 += 8) {
+            uint4 u[8];
+            float wj[8];
+            bool ok[8];
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                acc[2 * m] = fmaf(wj, bf16_bits_to_f32(v[m] & 0xFFFF), acc[2 * m]);
-                acc[2 * m + 1] = fmaf(wj, bf16_bits_to_f32(v[m] >> 16), acc[2 * m + 1]);
+            for (int q = 0; q < 8; ++q) {
+                const int j = j0 + q;
+                const int r = j < k ? __ldg(inv_pos + (size_t)t * k + j) : -1;
+                ok[q] = (unsigned)r < (unsigned)(T * k);  // else not a row of y_perm: contributes nothing
+                wj[q] = ok[q] ? __ldg(w + (size_t)t * k + j) : 0.f;
+                u[q] = ok[q] ? *reinterpret_cast<const uint4*>(y_perm + (size_t)r * d + 8 * c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (!ok[q]) continue;
+                const uint32_t v[4] = {u[q].x, u[q].y, u[q].z, u[q].w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    acc[2 * m] = fmaf(wj[q], bf16_bits_to_f32(v[m] & 0xFFFF), acc[2 * m]);
+                    acc[2 * m + 1] = fmaf(wj[q], bf16_bits_to_f32(v[m] >> 16), acc[2 * m + 1]);
+                }
             }
         }
         uint32_t o[4];

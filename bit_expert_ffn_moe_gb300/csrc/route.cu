@@ -281,31 +281,44 @@ __global__ void dense_plan_kernel(int T, PlanView plan, int32_t* offsets, int32_
     pdl_launch_dependents();
 }
 
-// One CTA per expert: a stable block-wide compaction over the tokens that chose it.
-__global__ void __launch_bounds__(256)
+// One CTA per expert: a stable block-wide compaction over the tokens that chose it, 1024 tokens
+// per pass (their ids read as 16-byte vectors when k % 4 == 0).
+__global__ void __launch_bounds__(1024)
 scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __restrict__ offsets, PlanView plan,
                int32_t* perm_token, int32_t* inv_pos, const float* __restrict__ w, float* row_w) {
-    __shared__ int warp_tot[8];
+    __shared__ int warp_tot[32];
     pdl_wait();
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (plan.counts[e] == 0) return;
     int running = offsets[e];
-    for (int t0 = 0; t0 < T; t0 += 256) {
+    const bool vec = (k & 3) == 0;
+    for (int t0 = 0; t0 < T; t0 += 1024) {
         const int t = t0 + tid;
         int j_found = -1;
-        if (t < T)
-            for (int j = 0; j < k; ++j) {
-                int v = ids[(size_t)t * k + j];
-                if (v == e) j_found = j;
+        if (t < T) {
+            if (vec) {
+                const int4* p = reinterpret_cast<const int4*>(ids + (size_t)t * k);
+                for (int q = 0; q < k / 4; ++q) {
+                    const int4 v = __ldg(p + q);
+                    if (v.x == e) j_found = 4 * q;
+                    if (v.y == e) j_found = 4 * q + 1;
+                    if (v.z == e) j_found = 4 * q + 2;
+                    if (v.w == e) j_found = 4 * q + 3;
+                }
+            } else {
+                for (int j = 0; j < k; ++j)
+                    if (__ldg(ids + (size_t)t * k + j) == e) j_found = j;
             }
+        }
         const unsigned bal = __ballot_sync(0xffffffffu, j_found >= 0);
         const int before = __popc(bal & ((1u << lane) - 1u));
         if (lane == 0) warp_tot[warp] = __popc(bal);
         __syncthreads();
         int wbase = 0, tot = 0;
-        for (int q = 0; q < 8; ++q) {
-            if (q < warp) wbase += warp_tot[q];
-            tot += warp_tot[q];
+        for (int q = 0; q < 32; ++q) {
+            const int n = warp_tot[q];
+            if (q < warp) wbase += n;
+            tot += n;
         }
         if (j_found >= 0) {
             const int r = running + wbase + before;
@@ -337,7 +350,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
     if (P == 0) return cudaSuccess;
     if (w == nullptr) row_w = nullptr;
     void* a3[] = {&ids, &T, &k, &offsets, &plan, &perm_token, &inv_pos, &w, &row_w};
-    return launch_kernel((const void*)scatter_kernel, dim3(E), dim3(256), 0, st, pdl, a3);
+    return launch_kernel((const void*)scatter_kernel, dim3(E), dim3(1024), 0, st, pdl, a3);
 }
 
 cudaError_t launch_dense_plan(int T, PlanView plan, int32_t* offsets, int32_t* perm_token, cudaStream_t st,
@@ -415,9 +428,20 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
         const bool real = local < plan.counts[lo];
         const int t = real ? perm_token[offsets[lo] + local] : 0;
         const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (size_t)nc * 16);
-        for (int c = lane; c < nc; c += 32) {
-            const uint4 v = real ? src[c] : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(xa + (FP8 ? mma8_tile_offset(r, c, d) : mma_tile_offset(r, c, d))) = v;
+        constexpr int kGB = 8;  // a lane's loads of up to 8 chunks are issued before its stores
+        for (int c0 = lane; c0 < nc; c0 += 32 * kGB) {
+            uint4 v[kGB];
+#pragma unroll
+            for (int u = 0; u < kGB; ++u) {
+                const int c = c0 + 32 * u;
+                v[u] = real && c < nc ? src[c] : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kGB; ++u) {
+                const int c = c0 + 32 * u;
+                if (c < nc)
+                    *reinterpret_cast<uint4*>(xa + (FP8 ? mma8_tile_offset(r, c, d) : mma_tile_offset(r, c, d))) = v[u];
+            }
         }
         // scales: blocks 4q .. 4q+3 of a row are 4 consecutive bytes of one scale atom (and of xs)
         const uint32_t* srcs = reinterpret_cast<const uint32_t*>(xs + (size_t)t * nb);

@@ -575,7 +575,8 @@ RouterScreenSizes router_screen_sizes(int T, int d, int E) {
 }
 
 cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
-                                 const RouterScreenBufs& rb, float* logits, int* status, cudaStream_t st, bool pdl) {
+                                 const RouterScreenBufs& rb, float* logits, int32_t* ids, float* w, int* status,
+                                 cudaStream_t st, bool pdl) {
     const int S = router_screen_splits(T, d, E);
     if (!S || ((uintptr_t)x & 15) || ((uintptr_t)W_r & 15)) return cudaErrorNotSupported;
     const int E_pad = (E + 127) / 128 * 128, KB = d / 64;
@@ -628,8 +629,10 @@ cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const floa
         void* args[] = {&x, &W_r, &b, &T, &d, &E, (void*)&rb.cnt, (void*)&rb.list, &logits};
         err = launch_kernel((const void*)router_exact_kernel, dim3(2 * sm_count()), dim3(kXThreads), smem, st, true,
                             args);
+        if (err != cudaSuccess) return err;
     }
-    return err;
+    // 5. top-k + softmax
+    return launch_topk(logits, T, E, k, ids, w, st, true);
 }
 
 }  // namespace moe
