@@ -495,16 +495,18 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
         MOE_CUDA(launch_combine_norm(y_perm, inv, w_b, T, k, d, eps, y, st, true));
         return MOE_OK;
     }
-    MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
-    MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
     uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
     uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
+    uint8_t* xq = reinterpret_cast<uint8_t*>(at(ws, L.xq));
+    uint8_t* xs = reinterpret_cast<uint8_t*>(at(ws, L.xs));
     const bool fp8 = fmt == MOE_ACT_MXFP8;
     const bool nv = W->wfmt == MOE_W_NVFP4;  // kind::mxf4nvf4: operand scales as UE4M3 per 16
     if (nv && !umma_nv_supported(E)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    MOE_CUDA(launch_act_quant_gather(x, T, d, E, k, offsets, perm, plan, L.pad_rows,
-                                     reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
-                                     xa, xa_s, fp8, st, true));
+    // the token rows are quantised first: that pass leaves x in L2 for the router's reads of it
+    MOE_CUDA(launch_act_quant(x, T, d, xq, xs, fp8, st, true));
+    MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
+    MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
+    MOE_CUDA(launch_act_gather(xq, xs, d, E, offsets, perm, plan, L.pad_rows, xa, xa_s, fp8, st, true));
     uint8_t* h = reinterpret_cast<uint8_t*>(at(ws, L.h));
     uint8_t* h_s = reinterpret_cast<uint8_t*>(at(ws, L.h_s));
     uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));

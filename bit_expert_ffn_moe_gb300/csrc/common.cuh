@@ -540,6 +540,13 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
 cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
                                     const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
                                     uint8_t* xs, uint8_t* xa, uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl);
+// The two halves of it: each row of x quantised once (reads x only, so it may run before the
+// router), then the gather into the padded tiles (after the permutation).
+cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8_t* xs, bool fp8, cudaStream_t st,
+                             bool pdl);
+cudaError_t launch_act_gather(const uint8_t* xq, const uint8_t* xs, int d, int E, const int32_t* offsets,
+                              const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xa, uint8_t* xa_s,
+                              bool fp8, cudaStream_t st, bool pdl);
 
 cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,

@@ -451,25 +451,35 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
     (void)pad_rows;
 }
 
-cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
-                                    const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
-                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl) {
-    (void)k;
+cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8_t* xs, bool fp8, cudaStream_t st,
+                             bool pdl) {
     int64_t nb = (int64_t)T * (d / 32);
-    if (nb > 0) {
-        int64_t blocks = (nb + 255) / 256;
-        if (blocks > 152 * 16) blocks = 152 * 16;
-        void* a1[] = {&x, &nb, &xq, &xs};
-        const void* f = fp8 ? (const void*)act_quant_kernel<true> : (const void*)act_quant_kernel<false>;
-        cudaError_t err = launch_kernel(f, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
-        if (err != cudaSuccess) return err;
-    }
+    if (nb <= 0) return cudaSuccess;
+    int64_t blocks = (nb + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    void* a1[] = {&x, &nb, &xq, &xs};
+    const void* f = fp8 ? (const void*)act_quant_kernel<true> : (const void*)act_quant_kernel<false>;
+    return launch_kernel(f, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
+}
+
+cudaError_t launch_act_gather(const uint8_t* xq, const uint8_t* xs, int d, int E, const int32_t* offsets,
+                              const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xa, uint8_t* xa_s,
+                              bool fp8, cudaStream_t st, bool pdl) {
     if (pad_rows == 0) return cudaSuccess;
     int64_t blocks = (pad_rows + 7) / 8;  // 8 warps (rows) per CTA
     if (blocks > 152 * 8) blocks = 152 * 8;
     void* a2[] = {&xq, &xs, &d, &E, &pad_rows, &offsets, &perm_token, &plan, &xa, &xa_s};
     const void* g = fp8 ? (const void*)act_gather_kernel<true> : (const void*)act_gather_kernel<false>;
     return launch_kernel(g, dim3((unsigned)blocks), dim3(256), sizeof(int32_t) * (size_t)(E + 1), st, pdl, a2);
+}
+
+cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int k, const int32_t* offsets,
+                                    const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
+                                    uint8_t* xs, uint8_t* xa, uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl) {
+    (void)k;
+    cudaError_t err = launch_act_quant(x, T, d, xq, xs, fp8, st, pdl);
+    if (err != cudaSuccess) return err;
+    return launch_act_gather(xq, xs, d, E, offsets, perm_token, plan, pad_rows, xa, xa_s, fp8, st, pdl);
 }
 
 }  // namespace moe
