@@ -168,6 +168,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# the sources each profiled kernel is compiled from (a summary's counters hold while their hash matches)
+DECODE_KERNEL_SOURCES = ["bit_expert_ffn_moe_gb300/csrc/decode_mma.cu", "bit_expert_ffn_moe_gb300/csrc/tcgen05.cuh",
+                         "bit_expert_ffn_moe_gb300/csrc/common.cuh", "bit_expert_ffn_moe_gb300/csrc/route_common.cuh"]
+GROUPED_KERNEL_SOURCES = ["bit_expert_ffn_moe_gb300/csrc/umma.cu", "bit_expert_ffn_moe_gb300/csrc/tcgen05.cuh",
+                          "bit_expert_ffn_moe_gb300/csrc/common.cuh"]
+
+
 def source_hash(paths):
     h = hashlib.sha256()
     for p in paths:
@@ -639,9 +646,7 @@ def kernel_roofline_decode_mma(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     n_act = float(np.mean([int(a.item()) for a in active]))
     per_launch = n_act * expert_read_bytes(d, I, "mxfp4") + T * d * 2
     achieved = per_launch / (avg_ms / 1e3) / 1e9
-    traffic = ncu_traffic("umma_decode_layer.md", ["bit_expert_ffn_moe_gb300/csrc/decode_mma.cu",
-                                                   "bit_expert_ffn_moe_gb300/csrc/tcgen05.cuh",
-                                                   "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
+    traffic = ncu_traffic("umma_decode_layer.md", DECODE_KERNEL_SOURCES, cfg.name)
     return {"kernel": "umma_decode_layer_kernel (tcgen05 kind::mxf4 gate/up + SwiGLU + down%s, decode)"
                       % (" + weighted sum" if y is not None else ""),
             "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -706,8 +711,7 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     kind = 2 if nv else int(fp8)
     profile = "umma_grouped_prefill_mxfp8.md" if fp8 else ("umma_grouped_prefill_nvfp4.md" if nv
                                                            else "umma_grouped_prefill.md")
-    traffic = ncu_traffic(profile, ["bit_expert_ffn_moe_gb300/csrc/umma.cu", "bit_expert_ffn_moe_gb300/csrc/common.cuh"],
-                          cfg.name)
+    traffic = ncu_traffic(profile, GROUPED_KERNEL_SOURCES, cfg.name)
     return {"kernel": "umma_grouped_kernel<1, %d> (tcgen05 %s gate/up + SwiGLU, prefill)"
                       % (kind, ["kind::mxf4", "kind::mxf8f6f4", "kind::mxf4nvf4"][kind]), "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(peak_tf, 1), "unit": "TFLOP/s",
