@@ -711,6 +711,8 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     kind = 2 if nv else int(fp8)
     profile = "umma_grouped_prefill_mxfp8.md" if fp8 else ("umma_grouped_prefill_nvfp4.md" if nv
                                                            else "umma_grouped_prefill.md")
+    if cfg.name != "prefill":  # another workload's capture (e.g. umma_grouped_long_prefill.md)
+        profile = profile.replace("umma_grouped_prefill", "umma_grouped_" + cfg.name)
     traffic = ncu_traffic(profile, GROUPED_KERNEL_SOURCES, cfg.name)
     return {"kernel": "umma_grouped_kernel<1, %d> (tcgen05 %s gate/up + SwiGLU, prefill)"
                       % (kind, ["kind::mxf4", "kind::mxf8f6f4", "kind::mxf4nvf4"][kind]), "bound": "tensor",
