@@ -33,7 +33,7 @@ EXPORTED = (
     "moe_status_string", "moe_abi_version", "moe_last_cuda_error", "moe_mxfp4_pack", "moe_mxfp4_unpack", "moe_mxfp4_mma_scale_bytes",
     "moe_mxfp4_scales_to_mma", "moe_mxfp4_codes_to_mma", "moe_workspace_size", "moe_padded_rows", "moe_workspace_init",
     "moe_get_device_status", "moe_route", "moe_route_noalloc", "moe_permute", "moe_expert_up_swiglu", "moe_expert_down", "moe_combine",
-    "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
+    "moe_combine_norm", "moe_layer_forward", "moe_layer_forward_host", "moe_layer_forward_norm", "moe_synth_weights", "moe_selftest_wait_timeout",
     "moe_dense_workspace_size", "moe_dense_linear", "moe_nvfp4_pack", "moe_nvfp4_unpack", "moe_workspace_routing",
     "moe_decode_pieces_bytes", "moe_decode_pieces", "moe_expert_ffn_decode",
 )
@@ -86,6 +86,7 @@ _SIGS = {
     "moe_expert_down": (I32, [P, P, I32, P, P, I32, I32, I32, I32, I32, WP, P, P, SZ, P]),
     "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
     "moe_layer_forward": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, SZ, P]),
+    "moe_layer_forward_host": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, P, P, SZ, P]),
     "moe_combine_norm": (I32, [P, P, P, I32, I32, I32, ctypes.c_float, P, P]),
     "moe_dense_workspace_size": (SZ, [I32, I32, I32, I32]),
     "moe_dense_linear": (I32, [P, I32, I32, I32, MP, I32, P, P, SZ, P]),
@@ -300,6 +301,16 @@ def moe_layer_forward(x, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, y, i
     _check("moe_layer_forward",
            load().moe_layer_forward(_p(x), _p(W_r), _p(b), T, d, E, k, I, ctypes.byref(W), fmt, _p(y), _p(ids),
                                     _p(w), _p(ws), _ws_bytes(ws, ws_bytes), _stream(stream)))
+
+
+def moe_layer_forward_host(x_host, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, y_host, ids, w, x_dev, y_dev,
+                           ws, ws_bytes=None, stream=None):
+    """x_host / y_host: host tensors (pinned for asynchronous copies) or int addresses; x_dev / y_dev:
+    the device staging buffers."""
+    _check("moe_layer_forward_host",
+           load().moe_layer_forward_host(_p(x_host), _p(W_r), _p(b), T, d, E, k, I, ctypes.byref(W), fmt, _p(y_host),
+                                         _p(ids), _p(w), _p(x_dev), _p(y_dev), _p(ws), _ws_bytes(ws, ws_bytes),
+                                         _stream(stream)))
 
 
 def moe_combine_norm(y_perm, inv_pos, w, T, k, d, eps, y, stream=None):

@@ -45,7 +45,7 @@ moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
 
 namespace {
 
-constexpr int kAbiVersion = 10;
+constexpr int kAbiVersion = 11;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -539,6 +539,22 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
                              const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids, float* w,
                              void* ws, size_t ws_bytes, moe_stream_t stream) {
     return layer_forward(x, W_r, b, T, d, E, k, I, W, fmt, false, 0.f, y, ids, w, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+moe_status moe_layer_forward_host(const uint16_t* x_host, const float* W_r, const float* b, int T, int d, int E,
+                                  int k, int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y_host,
+                                  int32_t* ids, float* w, uint16_t* x_dev, uint16_t* y_dev, void* ws,
+                                  size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_shape(T, d, E, k, I, fmt));
+    if (T == 0) return MOE_OK;
+    if (!x_host || !y_host || !x_dev || !y_dev || !aligned(x_dev, 16) || !aligned(y_dev, 16) || x_dev == y_dev)
+        return MOE_ERR_INVALID_ARG;
+    const cudaStream_t st = (cudaStream_t)stream;
+    const size_t bytes = sizeof(uint16_t) * (size_t)T * (size_t)d;
+    MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st));
+    MOE_TRY(layer_forward(x_dev, W_r, b, T, d, E, k, I, W, fmt, false, 0.f, y_dev, ids, w, ws, ws_bytes, st));
+    MOE_CUDA(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st));
+    return MOE_OK;
 }
 
 moe_status moe_layer_forward_norm(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,

@@ -1,0 +1,44 @@
+"""GPU: the host-buffer layer call (moe_layer_forward_host) copies x in, runs the same layer and copies
+y out -- its y, ids and w equal moe_layer_forward's bit for bit (decode on the tensor cores, the
+MXFP4-activation prefill path), and y against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from bit_expert_ffn_moe_gb300 import binding as B
+from bit_expert_ffn_moe_gb300 import inputs as IN
+from bit_expert_ffn_moe_gb300.layer import DeviceLayer, layer_forward, make_workspace
+from moe_testlib import bf16_tensor_to_f32, bits_to_device, check_outputs, oracle_expert_weights
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,fmt,ofmt", [("tiny", B.MOE_ACT_BF16, O.ACT_BF16),
+                                           ("decode", B.MOE_ACT_BF16, O.ACT_BF16),
+                                           ("mx300", B.MOE_ACT_MXFP4, O.ACT_MXFP4)])
+def test_host_buffer_layer_equals_device_layer(name, fmt, ofmt):
+    cfg = (IN.small_config("mx300", T=300, d=512, E=12, k=3, I=512, index=97) if name == "mx300"
+           else IN.CONFIGS[name])
+    layer = DeviceLayer(cfg)
+    T, d = cfg.T, cfg.d
+    ws = make_workspace(T, d, cfg.E, cfg.k, cfg.I, fmt)
+    xb = IN.make_x(cfg, call=1)
+    y_ref, ids_ref, w_ref = layer_forward(layer, bits_to_device(xb), fmt, ws=ws, want_routing=True)
+
+    x_host = torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    y_host = torch.zeros((T, d), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    y_dev = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    ids = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, cfg.k), dtype=torch.float32, device="cuda")
+    B.moe_layer_forward_host(x_host, layer.W_r, layer.b, T, d, cfg.E, cfg.k, cfg.I, layer.weights, fmt, y_host, ids,
+                             w, x_dev, y_dev, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host.view(torch.int16), y_ref.cpu().view(torch.int16))
+    assert torch.equal(ids.cpu(), ids_ref.cpu())
+    assert torch.equal(w.cpu(), w_ref.cpu())
+    tokens = np.arange(min(T, 16))
+    y_o = O.moe_layer(xb, layer.W_r_host, layer.b_host, cfg.k, oracle_expert_weights(cfg, layer.seed), ofmt,
+                      tokens=tokens)
+    check_outputs(bf16_tensor_to_f32(y_host[tokens]), y_o["y"])
