@@ -18,6 +18,12 @@ CASES = {
     "prefill": IN.CONFIGS["prefill"],
     "long_prefill_chunk": IN.CONFIGS["long_prefill"],
     "ragged": IN.small_config("ragged", T=333, d=384, E=40, k=5, I=256, zipf_s=1.3),
+    # the screened router at its shape edges: the largest E and k (eight expert tiles, 32 experts
+    # per lane in the candidate kernel), two K steps in all, and the largest d (64 K splits)
+    "screen_e1024_k32": IN.small_config("screen_e1024_k32", T=300, d=256, E=1024, k=32, I=256, index=81),
+    "screen_e1000_k17_d128": IN.small_config("screen_e1000_k17_d128", T=512, d=128, E=1000, k=17, I=256,
+                                             zipf_s=1.1, index=82),
+    "screen_t256_d16384": IN.small_config("screen_t256_d16384", T=256, d=16384, E=64, k=4, I=256, index=83),
 }
 
 
