@@ -104,7 +104,8 @@ moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T,
                                      reinterpret_cast<float*>(at(ws, L.rs_part)),
                                      reinterpret_cast<float*>(at(ws, L.rs_xn2)),
                                      reinterpret_cast<int32_t*>(at(ws, L.rs_cnt)),
-                                     reinterpret_cast<int32_t*>(at(ws, L.rs_list))};
+                                     reinterpret_cast<int32_t*>(at(ws, L.rs_list)),
+                                     reinterpret_cast<uint32_t*>(at(ws, L.rs_stat))};
         e = launch_router_screen(x, W_r, b, T, d, E, k, rb, logits, ids, w,
                                  &reinterpret_cast<Ctrl*>(at(ws, L.ctrl))->status, st, pdl);
         if (e != cudaErrorNotSupported) {

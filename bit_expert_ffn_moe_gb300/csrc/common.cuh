@@ -53,6 +53,7 @@ struct WsLayout {
     size_t dpart = 0;                                // its split gate/up tiles' fp32 partial sums
     size_t xa_s16 = 0, h_s16 = 0, xrf = 0, hrf = 0;  // NVFP4 weights: operand scales per 16, row factors
     size_t rs_bhi = 0, rs_blo = 0, rs_wn2 = 0, rs_part = 0, rs_xn2 = 0, rs_cnt = 0, rs_list = 0;  // screened router
+    size_t rs_stat = 0;
     int64_t pad_rows = 0;
 };
 
@@ -88,7 +89,7 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 // kernel routes this shape).
 struct RouterScreenSizes {
     int S;
-    size_t b_bytes, wn2_bytes, part_bytes, xn2_bytes, cnt_bytes, list_bytes;
+    size_t b_bytes, wn2_bytes, part_bytes, xn2_bytes, cnt_bytes, list_bytes, stat_bytes;
 };
 struct RouterScreenBufs {
     uint8_t* bhi;   // bf16 high parts of W_r, tensor-core tiles [E_pad/128][d/64]
@@ -98,6 +99,7 @@ struct RouterScreenBufs {
     float* xn2;     // [S][T] ||x_t||^2 per K split
     int32_t* cnt;   // [E] candidates per expert
     int32_t* list;  // [E][T] candidate tokens of each expert
+    uint32_t* stat; // [4] max ||w_e||^2, max |b_e| (bit patterns), all finite (1 / 0)
 };
 int router_screen_splits(int T, int d, int E);
 RouterScreenSizes router_screen_sizes(int T, int d, int E);
@@ -141,6 +143,7 @@ inline WsLayout ws_layout(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
         L.rs_xn2 = take(rs.xn2_bytes);
         L.rs_cnt = take(rs.cnt_bytes);
         L.rs_list = take(rs.list_bytes);
+        L.rs_stat = take(rs.stat_bytes);
     }
     if (fmt == MOE_ACT_MXFP4 || fmt == MOE_ACT_MXFP8) {
         const size_t per_byte = fmt == MOE_ACT_MXFP4 ? 2 : 1;  // values per code byte

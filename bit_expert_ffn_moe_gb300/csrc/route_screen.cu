@@ -126,7 +126,10 @@ struct ScreenArgs {
     const uint8_t* blo;
     float* part;  // [S][T][E_pad] screened partial values of each K split
     float* xn2;   // [S][T] partial ||x_t||^2 of each K split
-    int T, E_pad, KB, kb_per;  // KB = d / 64 stages in all, kb_per of them per K split
+    const float* wn2;  // [4][E] shares of ||w_e||^2, and the bias: CTA (0, 0, 0) writes their maxima to stat
+    const float* b;
+    uint32_t* stat;    // max ||w_e||^2, max |b_e| (bit patterns), 1 when all are finite
+    int T, E, E_pad, KB, kb_per;  // KB = d / 64 stages in all, kb_per of them per K split
     int* status;
 };
 
@@ -214,6 +217,27 @@ __global__ void __launch_bounds__(kScrThreads, 1) router_screen_kernel(const __g
     } else {
         const int q = warp & 3;  // tensor-memory lane quarter
         const int m = 32 * q + lane;
+        if (warp == 2 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+            // the maxima the candidate bounds use, the same for every token
+            uint32_t wm = 0, bm = 0;  // bit patterns of non-negative floats order like the values
+            bool fin = true;
+            for (int e = lane; e < a.E; e += 32) {
+                float w2 = 0.f;
+                for (int p4 = 0; p4 < kSplitParts; ++p4) w2 += __ldcg(a.wn2 + (size_t)p4 * a.E + e);
+                const float be = a.b ? __ldg(a.b + e) : 0.f;
+                fin = fin && isfinite(w2) && isfinite(be);
+                wm = max(wm, __float_as_uint(w2));
+                bm = max(bm, __float_as_uint(fabsf(be)));
+            }
+            wm = __reduce_max_sync(0xffffffffu, wm);
+            bm = __reduce_max_sync(0xffffffffu, bm);
+            fin = __all_sync(0xffffffffu, fin);
+            if (lane == 0) {
+                a.stat[0] = wm;
+                a.stat[1] = bm;
+                a.stat[2] = fin ? 1u : 0u;
+            }
+        }
         float s2 = 0.f;
         bool ok = true;
         for (int i = 0; i < nk; ++i) {
@@ -289,35 +313,26 @@ __global__ void __launch_bounds__(kScrThreads, 1) router_screen_kernel(const __g
 // are counted per expert in shared memory first, so that each CTA adds to an expert's global count
 // once (the load is skewed: a popular expert is a candidate of most tokens), then written to the
 // experts' lists.  C: the relative bound factor (host side), tiny: sqrt(d) 2^-124.
-constexpr int kCandTok = 16;  // one token per warp
+constexpr int kCandTok = 32;  // two tokens per warp
 template <int NV>
-__global__ void __launch_bounds__(512) router_cand_kernel(const float* __restrict__ part, const float* __restrict__ xn2,
+__global__ void __launch_bounds__(512, 2) router_cand_kernel(const float* __restrict__ part, const float* __restrict__ xn2,
                                                           int S, int T, int d, int E, int E_pad, int k,
-                                                          const float* __restrict__ b, const float* __restrict__ wn2,
-                                                          float C, float tiny, float* __restrict__ logits,
-                                                          int32_t* __restrict__ cnt, int32_t* __restrict__ list) {
+                                                          const float* __restrict__ b,
+                                                          const uint32_t* __restrict__ stat, float C, float tiny,
+                                                          float* __restrict__ logits, int32_t* __restrict__ cnt,
+                                                          int32_t* __restrict__ list) {
     __shared__ int lcnt[kMaxE];
     __shared__ uint32_t mask[kCandTok][NV];  // candidate bits of each token: bit l of word i = expert l + 32 i
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __shared__ uint32_t s_wm, s_bm;  // bit patterns of non-negative floats order like the values
     __shared__ int s_fin;
     pdl_wait();
-    if (threadIdx.x == 0) {
-        s_wm = 0u;
-        s_bm = 0u;
-        s_fin = 1;
+    if (threadIdx.x == 0) {  // max ||w_e||^2 and max |b_e| over the experts (the screen kernel's)
+        s_wm = __ldcg(stat);
+        s_bm = __ldcg(stat + 1);
+        s_fin = (int)__ldcg(stat + 2);
     }
-    __syncthreads();
-    // max ||w_e||^2 and max |b_e| over the experts (the same for every token)
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        lcnt[e] = 0;
-        float w2 = 0.f;
-        for (int q = 0; q < kSplitParts; ++q) w2 += __ldcg(wn2 + (size_t)q * E + e);
-        const float be = b ? __ldg(b + e) : 0.f;
-        if (!isfinite(w2) || !isfinite(be)) s_fin = 0;
-        atomicMax(&s_wm, __float_as_uint(w2));
-        atomicMax(&s_bm, __float_as_uint(fabsf(be)));
-    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x) lcnt[e] = 0;
     __syncthreads();
     for (int u = 0; u < kCandTok / 16; ++u) {
         const int tl = warp + 16 * u, t = blockIdx.x * kCandTok + tl;
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(512) router_cand_kernel(const float* __restric
             av[i] = e < E ? __ldcg(part + (size_t)t * E_pad + e) : 0.f;
         }
         float nx2 = __ldcg(xn2 + t);
-        constexpr int kB = NV <= 8 ? 4 : 1;
+        constexpr int kB = NV <= 4 ? 4 : NV <= 8 ? 2 : 1;
         for (int sp0 = 1; sp0 < S; sp0 += kB) {
             float pv[kB][NV], xv[kB];
 #pragma unroll
@@ -571,6 +586,7 @@ RouterScreenSizes router_screen_sizes(int T, int d, int E) {
     z.xn2_bytes = sizeof(float) * z.S * (size_t)T;
     z.cnt_bytes = sizeof(int32_t) * E;
     z.list_bytes = sizeof(int32_t) * (size_t)E * T;
+    z.stat_bytes = 16;
     return z;
 }
 
@@ -594,6 +610,10 @@ cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const floa
     a.blo = rb.blo;
     a.part = rb.part;
     a.xn2 = rb.xn2;
+    a.wn2 = rb.wn2;
+    a.b = b;
+    a.stat = rb.stat;
+    a.E = E;
     a.T = T;
     a.E_pad = E_pad;
     a.KB = KB;
@@ -619,7 +639,7 @@ cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const floa
                         : E_pad <= 512 ? (const void*)router_cand_kernel<16>
                                        : (const void*)router_cand_kernel<32>;
         void* args[] = {(void*)&rb.part, (void*)&rb.xn2, (void*)&S, &T, &d, &E, (void*)&E_pad, &k, &b,
-                        (void*)&rb.wn2, &C, &tiny, &logits, (void*)&rb.cnt, (void*)&rb.list};
+                        (void*)&rb.stat, &C, &tiny, &logits, (void*)&rb.cnt, (void*)&rb.list};
         err = launch_kernel(f, dim3((T + kCandTok - 1) / kCandTok), dim3(512), 0, st, true, args);
         if (err != cudaSuccess) return err;
     }
