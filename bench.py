@@ -527,7 +527,7 @@ class Latent:
 def screened_route(T, d, E):
     """Whether the library routes T tokens with the tensor-core screen (router split, screen,
     candidates, exact logits, top-k: five launches instead of the dense logits + top-k)."""
-    return T >= 256 and d % 128 == 0 and d <= 32768 and E <= 1024
+    return T >= 256 and d % 128 == 0 and d <= 32768 and E <= 1024 and T * E <= (1 << 25)
 
 
 def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_decode=False, nv_grouped=False):

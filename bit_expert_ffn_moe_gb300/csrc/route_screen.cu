@@ -567,7 +567,9 @@ cudaError_t x_tensor_map(CUtensorMap* m, const uint16_t* x, int T, int d) {
 }  // namespace
 
 int router_screen_splits(int T, int d, int E) {
-    if (T < kScrMinT || d % 128 != 0 || d > kScrMaxD || E > kMaxE) return 0;
+    // the candidate lists and the screened values take 4 T E bytes each (and the values once per K
+    // split): beyond 2^25 token-expert pairs the dense kernel routes, with no such buffers
+    if (T < kScrMinT || d % 128 != 0 || d > kScrMaxD || E > kMaxE || (int64_t)T * E > ((int64_t)1 << 25)) return 0;
     const int KB = d / 64;
     const int tiles = ((T + 127) / 128) * ((E + 127) / 128);
     int S = 1;

@@ -112,6 +112,7 @@ def test_variant_options_name_the_workload_and_count_launches():
     # up to eight tokens: the expert kernel routes its own tokens (one launch; + the normalising sum)
     assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 13          # screened router: + 3
     assert bench.launches_per_step(1, 200, 8192, 128, 8) == 10           # dense router below 256 tokens
+    assert bench.launches_per_step(1, 65536, 8192, 1024, 8) == 10        # and beyond 2^25 token-expert pairs
     assert bench.launches_per_step(0, 1, 8192, 128, 8, mma_decode=True) == 1
     assert bench.launches_per_step(0, 4, 8192, 128, 8, mma_decode=True) == 1
     assert bench.launches_per_step(0, 8, 8192, 128, 8, mma_decode=True) == 2
