@@ -507,7 +507,7 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
     MOE_CUDA(launch_act_quant(x, T, d, xq, xs, fp8, st, true));
     MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
     MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
-    MOE_CUDA(launch_act_gather(xq, xs, d, E, offsets, perm, plan, L.pad_rows, xa, xa_s, fp8, st, true));
+    MOE_CUDA(launch_act_gather(xq, xs, d, E, offsets, perm, plan, L.pad_rows, xa, xa_s, fp8, st, true, false));
     uint8_t* h = reinterpret_cast<uint8_t*>(at(ws, L.h));
     uint8_t* h_s = reinterpret_cast<uint8_t*>(at(ws, L.h_s));
     uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));

@@ -544,12 +544,15 @@ cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int 
                                     const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xq,
                                     uint8_t* xs, uint8_t* xa, uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl);
 // The two halves of it: each row of x quantised once (reads x only, so it may run before the
-// router), then the gather into the padded tiles (after the permutation).
+// router), then the gather into the padded tiles (after the permutation).  zero_pad = false leaves
+// each expert's padding rows unwritten: the expert GEMMs' rows are independent and padding rows'
+// results are never stored, so the layer call skips those writes (a fifth of the gather's bytes at
+// the prefill workload); the step call moe_permute writes them as zeros.
 cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8_t* xs, bool fp8, cudaStream_t st,
                              bool pdl);
 cudaError_t launch_act_gather(const uint8_t* xq, const uint8_t* xs, int d, int E, const int32_t* offsets,
                               const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xa, uint8_t* xa_s,
-                              bool fp8, cudaStream_t st, bool pdl);
+                              bool fp8, cudaStream_t st, bool pdl, bool zero_pad = true);
 
 cudaError_t launch_gemv_up(const uint16_t* x, const int32_t* perm_token, const int32_t* offsets, PlanView plan,
                            int T, int d, int E, int k, int I, const moe_expert_weights* W, uint16_t* h,

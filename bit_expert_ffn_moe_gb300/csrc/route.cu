@@ -409,7 +409,7 @@ template <bool FP8>
 __global__ void __launch_bounds__(256)
 act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, int d, int E, int64_t pad_rows,
                   const int32_t* __restrict__ offsets, const int32_t* __restrict__ perm_token, PlanView plan,
-                  uint8_t* __restrict__ xa, uint8_t* __restrict__ xa_s) {
+                  uint8_t* __restrict__ xa, uint8_t* __restrict__ xa_s, int zero_pad) {
     extern __shared__ int32_t s_pad[];  // [E+1]
     pdl_wait();
     for (int i = threadIdx.x; i <= E; i += blockDim.x) s_pad[i] = plan.pad_offsets[i];
@@ -426,6 +426,7 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
         }
         const int64_t local = r - s_pad[lo];
         const bool real = local < plan.counts[lo];
+        if (!real && !zero_pad) continue;  // the caller leaves padding rows as they are
         const int t = real ? perm_token[offsets[lo] + local] : 0;
         const uint4* src = reinterpret_cast<const uint4*>(xq + (size_t)t * (size_t)nc * 16);
         constexpr int kGB = 8;  // a lane's loads of up to 8 chunks are issued before its stores
@@ -464,11 +465,12 @@ cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8
 
 cudaError_t launch_act_gather(const uint8_t* xq, const uint8_t* xs, int d, int E, const int32_t* offsets,
                               const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xa, uint8_t* xa_s,
-                              bool fp8, cudaStream_t st, bool pdl) {
+                              bool fp8, cudaStream_t st, bool pdl, bool zero_pad) {
     if (pad_rows == 0) return cudaSuccess;
     int64_t blocks = (pad_rows + 7) / 8;  // 8 warps (rows) per CTA
     if (blocks > 152 * 8) blocks = 152 * 8;
-    void* a2[] = {&xq, &xs, &d, &E, &pad_rows, &offsets, &perm_token, &plan, &xa, &xa_s};
+    int zp = zero_pad ? 1 : 0;
+    void* a2[] = {&xq, &xs, &d, &E, &pad_rows, &offsets, &perm_token, &plan, &xa, &xa_s, &zp};
     const void* g = fp8 ? (const void*)act_gather_kernel<true> : (const void*)act_gather_kernel<false>;
     return launch_kernel(g, dim3((unsigned)blocks), dim3(256), sizeof(int32_t) * (size_t)(E + 1), st, pdl, a2);
 }
