@@ -238,7 +238,11 @@ moe_status moe_workspace_routing(void* ws, size_t ws_bytes, int T, int d, int E,
  * ids[t][k] is that set in ascending expert order and w[t][k] the softmax of the selected
  * logits (section 9: the weights sum to 1).
  *   x bf16 [T][d]; W_r fp32 [E][d]; b fp32 [E] or NULL (= 0); ids int32 [T][k]; w fp32 [T][k].
- * Uses ws for the T*E logits. */
+ * Uses ws for the T*E logits.  From 256 tokens on (d at most 32768, T*E at most 2^25, x and W_r
+ * 16-byte aligned) the logits are first screened on the tensor cores (bf16 parts of W_r, fp32
+ * accumulation) with a bound on the screen's error, and the fixed-order logits above are then
+ * computed only for the experts that can still be among a token's k largest; every other
+ * expert's logit is left as -inf in ws.  ids and w are the same as with every logit computed. */
 moe_status moe_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                      int32_t* ids, float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
