@@ -14,6 +14,7 @@ collective); the step time is the maximum over ranks.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -356,10 +357,18 @@ def run_gpu(args, cfg, rank, world, local):
     # ---- end to end through the C ABI with host buffers
     host_call = None
     if lat is None and norm_eps(args) is None:
-        def host_call(s, x_host, y_host, x_dev, y_dev, ws_l, st):
-            L = layers[s % len(layers)]
-            B.moe_layer_forward_host(x_host, L.W_r, L.b, T, d, E, k, I, L.weights, fmt, y_host, None, None, x_dev,
-                                     y_dev, ws_l, stream=st)
+        fn = B.load().moe_layer_forward_host
+        # per layer copy: its router pointers and weight struct, marshalled once (the loop then only
+        # passes integers to the C entry point)
+        lay_args = [(L.W_r.data_ptr(), None if L.b is None else L.b.data_ptr(), ctypes.byref(L.weights))
+                    for L in layers]
+
+        def host_call(s, x_host, y_host, x_dev, y_dev, ws_l, st, cst):
+            wr, bb, wp = lay_args[s % len(lay_args)]
+            status = fn(x_host, wr, bb, T, d, E, k, I, wp, fmt, y_host, None, None, x_dev, y_dev, ws_l[0], ws_l[1],
+                        st, cst[0], cst[1])
+            if status != B.MOE_OK:
+                raise B.MoeError("moe_layer_forward_host", status)
     e2e = end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call, host_call)
 
     # ---- the oracle sample's rows through the same layer copy (checked in main)
@@ -783,17 +792,26 @@ def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call, host_call=None):
                 ev_out[b].record(cs)
 
     if host_call is not None and T * d * 2 <= (1 << 20):
+        xh = [x_pin[i].data_ptr() for i in range(x_pin.shape[0])]
+        yh = [y_pin[i].data_ptr() for i in range(y_pin.shape[0])]
+        xd = [t.data_ptr() for t in x_dev]
+        yd = [t.data_ptr() for t in y_dev]
+        ws_a = (ws.data_ptr(), ws.numel() * ws.element_size())
+        cs_out = torch.cuda.Stream(device=dev)  # copies out (cs: copies in)
+        cst = (cs.cuda_stream, cs_out.cuda_stream)
+
         def run(steps):
             for s in range(steps):
-                host_call(s, x_pin[s % x_pin.shape[0]], y_pin[s % y_pin.shape[0]], x_dev[0], y_dev[0], ws, st)
-        note = ("moe_layer_forward_host per step (eager, no graph): pinned H2D of x, the layer, D2H of y, "
-                "one C-ABI call")
-        start_stream = stream
+                host_call(s, xh[s % len(xh)], yh[s % len(yh)], xd[s % 2], yd[s % 2], ws_a, st, cst)
+        note = ("moe_layer_forward_host per step (eager, no graph, one C-ABI call): pinned H2D of x, the layer, "
+                "D2H of y; the copies on two copy streams (in, out) with two alternating staging pairs, so they "
+                "overlap the neighbouring steps' layers")
+        start_stream, end_stream = cs, cs_out
     else:
         note = ("eager C-ABI calls per step (no graph); every step's pinned H2D of x and D2H of y inside the "
                 "timed region, on a copy stream with double-buffered device x and y, so step s + 1's input and "
                 "step s's output move while step s computes")
-        start_stream = cs
+        start_stream = end_stream = cs
     run(3)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -801,7 +819,7 @@ def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call, host_call=None):
     start.record(start_stream)
     stream.wait_event(start)
     run(n)
-    end.record(start_stream)  # after the last read-back (on the copy stream it waited for the last layer call)
+    end.record(end_stream)  # after the last read-back (on a copy stream, which waited for the last layer call)
     end.synchronize()
     wall = time.perf_counter() - t0
     ms = start.elapsed_time(end)

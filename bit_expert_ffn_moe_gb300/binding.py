@@ -86,7 +86,7 @@ _SIGS = {
     "moe_expert_down": (I32, [P, P, I32, P, P, I32, I32, I32, I32, I32, WP, P, P, SZ, P]),
     "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
     "moe_layer_forward": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, SZ, P]),
-    "moe_layer_forward_host": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, P, P, SZ, P]),
+    "moe_layer_forward_host": (I32, [P, P, P, I32, I32, I32, I32, I32, WP, I32, P, P, P, P, P, P, SZ, P, P, P]),
     "moe_combine_norm": (I32, [P, P, P, I32, I32, I32, ctypes.c_float, P, P]),
     "moe_dense_workspace_size": (SZ, [I32, I32, I32, I32]),
     "moe_dense_linear": (I32, [P, I32, I32, I32, MP, I32, P, P, SZ, P]),
@@ -304,13 +304,16 @@ def moe_layer_forward(x, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, y, i
 
 
 def moe_layer_forward_host(x_host, W_r, b, T, d, E, k, I, W: moe_expert_weights, fmt, y_host, ids, w, x_dev, y_dev,
-                           ws, ws_bytes=None, stream=None):
+                           ws, ws_bytes=None, stream=None, in_stream=None, out_stream=None):
     """x_host / y_host: host tensors (pinned for asynchronous copies) or int addresses; x_dev / y_dev:
-    the device staging buffers."""
+    the device staging buffers; in_stream / out_stream (optional, both or neither): the streams of
+    the copy in and the copy out."""
+    ins = None if in_stream is None else _stream(in_stream)
+    outs = None if out_stream is None else _stream(out_stream)
     _check("moe_layer_forward_host",
            load().moe_layer_forward_host(_p(x_host), _p(W_r), _p(b), T, d, E, k, I, ctypes.byref(W), fmt, _p(y_host),
                                          _p(ids), _p(w), _p(x_dev), _p(y_dev), _p(ws), _ws_bytes(ws, ws_bytes),
-                                         _stream(stream)))
+                                         _stream(stream), ins, outs))
 
 
 def moe_combine_norm(y_perm, inv_pos, w, T, k, d, eps, y, stream=None):

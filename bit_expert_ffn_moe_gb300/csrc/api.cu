@@ -2,6 +2,10 @@
 // carving and the launch sequence of each layer step.  No entry point allocates device memory.
 #include <stdio.h>
 
+#include <mutex>
+#include <utility>
+#include <vector>
+
 #include "common.cuh"
 
 using namespace moe;
@@ -45,7 +49,7 @@ moe_status check_shape(int T, int d, int E, int k, int I, moe_act_fmt fmt) {
 
 namespace {
 
-constexpr int kAbiVersion = 11;
+constexpr int kAbiVersion = 13;
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -116,6 +120,42 @@ moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T,
     MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
     MOE_CUDA(launch_topk(logits, T, E, k, ids, w, st, true));
     return MOE_OK;
+}
+
+// Events of a host-buffer call's staging buffer (moe_layer_forward_host with copy streams): "ready"
+// (its input copy landed, or the layer wrote it), "consumed" (the last layer that read it is done),
+// "drained" (the last copy out of it is done).  Created on first use of a buffer address, kept for
+// the process (a small table: beyond 64 buffers the oldest entries are released -- destroying an
+// event whose work is pending is deferred by the runtime, so no pending wait is affected).
+struct StagingEvents {
+    cudaEvent_t ready = nullptr, consumed = nullptr, drained = nullptr;
+    bool consumed_recorded = false, drained_recorded = false;
+};
+
+StagingEvents* staging_events(const void* buf) {
+    static std::mutex mu;
+    static std::vector<std::pair<const void*, StagingEvents*>> table;
+    std::lock_guard<std::mutex> lock(mu);
+    for (auto& e : table)
+        if (e.first == buf) return e.second;
+    if (table.size() >= 64) {
+        for (auto& e : table) {
+            cudaEventDestroy(e.second->ready);
+            cudaEventDestroy(e.second->consumed);
+            cudaEventDestroy(e.second->drained);
+            delete e.second;
+        }
+        table.clear();
+    }
+    StagingEvents* ev = new StagingEvents();
+    if (cudaEventCreateWithFlags(&ev->ready, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev->consumed, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ev->drained, cudaEventDisableTiming) != cudaSuccess) {
+        delete ev;
+        return nullptr;
+    }
+    table.emplace_back(buf, ev);
+    return ev;
 }
 
 }  // namespace
@@ -545,16 +585,37 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
 moe_status moe_layer_forward_host(const uint16_t* x_host, const float* W_r, const float* b, int T, int d, int E,
                                   int k, int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y_host,
                                   int32_t* ids, float* w, uint16_t* x_dev, uint16_t* y_dev, void* ws,
-                                  size_t ws_bytes, moe_stream_t stream) {
+                                  size_t ws_bytes, moe_stream_t stream, moe_stream_t in_stream,
+                                  moe_stream_t out_stream) {
     MOE_TRY(check_shape(T, d, E, k, I, fmt));
     if (T == 0) return MOE_OK;
     if (!x_host || !y_host || !x_dev || !y_dev || !aligned(x_dev, 16) || !aligned(y_dev, 16) || x_dev == y_dev)
         return MOE_ERR_INVALID_ARG;
     const cudaStream_t st = (cudaStream_t)stream;
     const size_t bytes = sizeof(uint16_t) * (size_t)T * (size_t)d;
-    MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st));
+    if (!in_stream || !out_stream) {
+        MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st));
+        MOE_TRY(layer_forward(x_dev, W_r, b, T, d, E, k, I, W, fmt, false, 0.f, y_dev, ids, w, ws, ws_bytes, st));
+        MOE_CUDA(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st));
+        return MOE_OK;
+    }
+    const cudaStream_t is = (cudaStream_t)in_stream, os = (cudaStream_t)out_stream;
+    StagingEvents* ex = staging_events(x_dev);
+    StagingEvents* ey = staging_events(y_dev);
+    if (!ex || !ey) return MOE_ERR_CUDA;
+    if (ex->consumed_recorded) MOE_CUDA(cudaStreamWaitEvent(is, ex->consumed, 0));  // the last layer read x_dev
+    MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, is));
+    MOE_CUDA(cudaEventRecord(ex->ready, is));
+    MOE_CUDA(cudaStreamWaitEvent(st, ex->ready, 0));
+    if (ey->drained_recorded) MOE_CUDA(cudaStreamWaitEvent(st, ey->drained, 0));  // the last copy out of y_dev
     MOE_TRY(layer_forward(x_dev, W_r, b, T, d, E, k, I, W, fmt, false, 0.f, y_dev, ids, w, ws, ws_bytes, st));
-    MOE_CUDA(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st));
+    MOE_CUDA(cudaEventRecord(ex->consumed, st));
+    ex->consumed_recorded = true;
+    MOE_CUDA(cudaEventRecord(ey->ready, st));  // y_dev written
+    MOE_CUDA(cudaStreamWaitEvent(os, ey->ready, 0));
+    MOE_CUDA(cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, os));
+    MOE_CUDA(cudaEventRecord(ey->drained, os));
+    ey->drained_recorded = true;
     return MOE_OK;
 }
 

@@ -130,7 +130,7 @@ const char* moe_status_string(moe_status s);
 
 /* ABI version of this header (incremented on changes to the entry points or their structs);
  * moe_abi_version() returns the library's, which a caller compares with MOE_ABI_VERSION. */
-#define MOE_ABI_VERSION 11
+#define MOE_ABI_VERSION 13
 int moe_abi_version(void);
 
 /* Description of the CUDA error behind the calling thread's last MOE_ERR_CUDA (static string). */
@@ -371,19 +371,29 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
                              int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y, int32_t* ids,
                              float* w, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* moe_layer_forward with the activations in host memory: enqueues on `stream` the copy of x_host
- * (bf16 [T][d]) into the device buffer x_dev, the layer (x_dev -> y_dev, both bf16 [T][d] device
- * buffers of the caller, 16-byte aligned, not overlapping each other or the workspace) and the
- * copy of y_dev back to y_host, and returns without waiting: y_host holds the result once the
- * stream has passed that point (for example after cudaStreamSynchronize).  x_host and y_host
- * should be page-locked (pinned) for the copies to be asynchronous; pageable memory works, with
- * copies that are synchronous with respect to the host.  The other arguments, the shape rules,
- * the workspace and the errors are moe_layer_forward's; MOE_ERR_INVALID_ARG also for a null
- * host or staging pointer.  A copy that fails to enqueue returns MOE_ERR_CUDA. */
+/* moe_layer_forward with the activations in host memory: the copy of x_host (bf16 [T][d]) into the
+ * device buffer x_dev, the layer (x_dev -> y_dev, both bf16 [T][d] device buffers of the caller,
+ * 16-byte aligned, not overlapping each other or the workspace) and the copy of y_dev back to
+ * y_host, all enqueued, without waiting.
+ *   in_stream or out_stream NULL: everything in order on `stream`; y_host holds the result once
+ *     `stream` has passed that point (for example after cudaStreamSynchronize(stream)).
+ *   both given: the copy in runs on in_stream, the layer on `stream`, the copy out on out_stream,
+ *     so that a caller alternating two (x_dev, y_dev) pairs over consecutive calls has the copies
+ *     of one call overlap the layers of its neighbours (one stream per direction: a copy in never
+ *     queues behind a copy out, which waits for its layer).  The library orders the streams with
+ *     events it keeps per staging buffer (created on first use, reused): the copy into x_dev waits
+ *     for the last layer that read x_dev, the layer waits for its input copy and for the last copy
+ *     out of y_dev, the copy out waits for the layer.  y_host holds the result once out_stream has
+ *     passed that point.  Calls on the same workspace must share `stream`.
+ * x_host and y_host should be page-locked (pinned) for the copies to be asynchronous; pageable
+ * memory works, with copies that are synchronous with respect to the host.  The other arguments,
+ * the shape rules, the workspace and the errors are moe_layer_forward's; MOE_ERR_INVALID_ARG also
+ * for a null host or staging pointer.  A copy or event call that fails returns MOE_ERR_CUDA. */
 moe_status moe_layer_forward_host(const uint16_t* x_host, const float* W_r, const float* b, int T, int d, int E,
                                   int k, int I, const moe_expert_weights* W, moe_act_fmt fmt, uint16_t* y_host,
                                   int32_t* ids, float* w, uint16_t* x_dev, uint16_t* y_dev, void* ws,
-                                  size_t ws_bytes, moe_stream_t stream);
+                                  size_t ws_bytes, moe_stream_t stream, moe_stream_t in_stream,
+                                  moe_stream_t out_stream);
 
 /* The layer with each expert's output normalised before the weighted sum (moe_combine_norm's
  * definition; eps in (0, 1]).  Same arguments, workspace and stream rules as moe_layer_forward;

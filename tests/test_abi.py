@@ -30,7 +30,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert B.moe_abi_version() == 11
+    assert B.moe_abi_version() == 13
     header = open(os.path.join(ROOT, "include", "moe.h")).read()
     assert int(re.search(r"#define MOE_ABI_VERSION (\d+)", header).group(1)) == B.moe_abi_version()
     assert B.status_string(0) == "MOE_OK"
@@ -109,7 +109,7 @@ def test_host_buffer_layer_arguments_are_checked_on_the_host(lib):
     # rules are refused before any copy or launch; T = 0 is a no-op
     W = B.moe_expert_weights()
     args = lambda xh, yh, xd, yd, T=4, d=256: (xh, 256, None, T, d, 8, 2, 512, W, B.MOE_ACT_BF16, yh, None, None,
-                                               xd, yd, 256, 1 << 30, None)
+                                               xd, yd, 256, 1 << 30, None, None, None)
     assert lib.moe_layer_forward_host(*args(None, 4096, 8192, 16384)) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_layer_forward_host(*args(4096, None, 8192, 16384)) == B.MOE_ERR_INVALID_ARG
     assert lib.moe_layer_forward_host(*args(4096, 4096, None, 16384)) == B.MOE_ERR_INVALID_ARG

@@ -1,6 +1,7 @@
 """GPU: the host-buffer layer call (moe_layer_forward_host) copies x in, runs the same layer and copies
 y out -- its y, ids and w equal moe_layer_forward's bit for bit (decode on the tensor cores, the
-MXFP4-activation prefill path), and y against the oracle."""
+MXFP4-activation prefill path), and y against the oracle; with copy streams and two alternating
+staging pairs, consecutive calls on different inputs give each call's own result."""
 import numpy as np
 import pytest
 import torch
@@ -42,3 +43,27 @@ def test_host_buffer_layer_equals_device_layer(name, fmt, ofmt):
     y_o = O.moe_layer(xb, layer.W_r_host, layer.b_host, cfg.k, oracle_expert_weights(cfg, layer.seed), ofmt,
                       tokens=tokens)
     check_outputs(bf16_tensor_to_f32(y_host[tokens]), y_o["y"])
+
+
+@pytest.mark.parametrize("name", ["decode", "tiny"])
+def test_host_buffer_layer_with_copy_streams(name):
+    cfg = IN.CONFIGS[name]
+    layer = DeviceLayer(cfg)
+    T, d = cfg.T, cfg.d
+    ws = make_workspace(T, d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
+    calls = 5
+    xbs = [IN.make_x(cfg, call=c) for c in range(calls)]
+    refs = [layer_forward(layer, bits_to_device(xb), B.MOE_ACT_BF16, ws=ws).cpu() for xb in xbs]
+    x_host = [torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).pin_memory() for xb in xbs]
+    y_host = [torch.zeros((T, d), dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
+    x_dev = [torch.empty((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    y_dev = [torch.empty((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    st, ins, outs = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for c in range(calls):
+        B.moe_layer_forward_host(x_host[c], layer.W_r, layer.b, T, d, cfg.E, cfg.k, cfg.I, layer.weights,
+                                 B.MOE_ACT_BF16, y_host[c], None, None, x_dev[c % 2], y_dev[c % 2], ws, stream=st,
+                                 in_stream=ins, out_stream=outs)
+    outs.synchronize()
+    st.synchronize()
+    for c in range(calls):
+        assert torch.equal(y_host[c].view(torch.int16), refs[c].view(torch.int16)), "call %d" % c
