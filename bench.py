@@ -661,7 +661,8 @@ def kernel_roofline_decode_mma(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     n_act = float(np.mean([int(a.item()) for a in active]))
     per_launch = n_act * expert_read_bytes(d, I, "mxfp4") + T * d * 2
     achieved = per_launch / (avg_ms / 1e3) / 1e9
-    traffic = ncu_traffic("umma_decode_layer.md", DECODE_KERNEL_SOURCES, cfg.name)
+    profile = "umma_decode_layer.md" if cfg.name == "decode" else "umma_decode_layer_%s.md" % cfg.name
+    traffic = ncu_traffic(profile, DECODE_KERNEL_SOURCES, cfg.name)
     return {"kernel": "umma_decode_layer_kernel (tcgen05 kind::mxf4 gate/up + SwiGLU + down%s, decode)"
                       % (" + weighted sum" if y is not None else ""),
             "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -1023,21 +1024,21 @@ SUB_KEYS = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "config"
 
 
 # extra workload name -> (configuration, activation format)
-EXTRA_WORKLOADS = {"prefill": ("prefill", "mxfp4"), "long_prefill": ("long_prefill", "mxfp4"),
-                   "prefill_mxfp8": ("prefill", "mxfp8")}
+EXTRA_WORKLOADS = {"spec_verify": ("spec_verify", "bf16"), "prefill": ("prefill", "mxfp4"),
+                   "long_prefill": ("long_prefill", "mxfp4"), "prefill_mxfp8": ("prefill", "mxfp8")}
 
 
 def extra_workloads(args):
-    """Workloads timed after the headline one in the same run: the prefill chunk, one chunk of the
-    long prefill, and the prefill chunk with 8-bit activations, when the headline is the plain
-    decode workload (no variant options)."""
+    """Workloads timed after the headline one in the same run: speculative verification (four
+    tokens), the prefill chunk, one chunk of the long prefill, and the prefill chunk with 8-bit
+    activations, when the headline is the plain decode workload (no variant options)."""
     if args.extra == "none":
         return []
     if args.extra != "auto":
         return [n for n in args.extra.split(",") if n]
     plain = (args.config == "decode" and not args.latent and not args.expert_norm and args.weights == "mxfp4"
              and args.fmt == "bf16")
-    return ["prefill", "long_prefill", "prefill_mxfp8"] if plain else []
+    return ["spec_verify", "prefill", "long_prefill", "prefill_mxfp8"] if plain else []
 
 
 def run_workload(args, cfg, rank, world, local):
@@ -1105,9 +1106,10 @@ def main():
 
     os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
     out = run_workload(args, cfg, rank, world, local)
-    # With the default workload the same process also times the prefill chunk and one chunk of the
-    # long prefill (the other half of the metric: the FP4 tensor roofline) and the prefill chunk with
-    # MXFP8 activations (the FP8 tensor roofline), each in a sub-object.
+    # With the default workload the same process also times speculative verification (the HBM
+    # roofline at four tokens), the prefill chunk and one chunk of the long prefill (the other half
+    # of the metric: the FP4 tensor roofline) and the prefill chunk with MXFP8 activations (the FP8
+    # tensor roofline), each in a sub-object.
     for name in extra_workloads(args):
         import gc
 

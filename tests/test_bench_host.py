@@ -189,13 +189,13 @@ def test_oracle_sample_outputs_are_the_parity_rows(T, weights, norm):
     assert O.max_threads() == len(__import__("os").sched_getaffinity(0))  # restored
 
 
-def test_default_line_times_the_prefill_workloads_in_both_activation_formats():
+def test_default_line_times_verify_and_the_prefill_workloads_in_both_activation_formats():
     import argparse
     a = argparse.Namespace(extra="auto", config="decode", latent=0, expert_norm=False, weights="mxfp4", fmt="bf16")
     names = bench.extra_workloads(a)
-    assert names == ["prefill", "long_prefill", "prefill_mxfp8"]
-    assert [bench.EXTRA_WORKLOADS[n] for n in names] == [("prefill", "mxfp4"), ("long_prefill", "mxfp4"),
-                                                          ("prefill", "mxfp8")]
+    assert names == ["spec_verify", "prefill", "long_prefill", "prefill_mxfp8"]
+    assert [bench.EXTRA_WORKLOADS[n] for n in names] == [("spec_verify", "bf16"), ("prefill", "mxfp4"),
+                                                          ("long_prefill", "mxfp4"), ("prefill", "mxfp8")]
     a.fmt = "mxfp8"  # a variant headline times nothing else
     assert bench.extra_workloads(a) == []
     # the prefill roofline is the FP4 tensor peak for MXFP4 activations, FP8 for MXFP8 beyond 16
