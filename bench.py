@@ -542,7 +542,8 @@ def screened_route(T, d, E):
 def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_decode=False, nv_grouped=False):
     # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
     # gate/up, down+sum; with the expert normalisation the down GEMV and the (normalising) sum are
-    # separate launches.  MXFP4: logits, top-k, count, plan, scatter, quantise, gather, up, down, sum.
+    # separate launches.  MXFP4: quantise, logits, top-k (which also counts the picks per expert), the
+    # permutation (offsets, plan and rows in one launch), gather, up, down, sum.
     # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).  Many
     # tokens: the screened router adds three launches to the route.
     proj = (2 if fmt == 0 else 4) * 2 if latent else 0
@@ -555,7 +556,7 @@ def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_deco
             sep_sum = 0 if (T <= 4 and not expert_norm) else 1
             return (1 if (T <= 8 and E <= 152) else 5 + 1 + 1) + sep_sum + proj
         return (3 if T <= 8 else 7) + (1 if expert_norm else 0) + proj
-    return 10 + (2 if nv_grouped else 0) + proj  # NVFP4 weights: + the two operand-scale conversions
+    return 8 + (2 if nv_grouped else 0) + proj  # NVFP4 weights: + the two operand-scale conversions
 
 
 def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):

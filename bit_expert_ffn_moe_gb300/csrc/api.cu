@@ -98,7 +98,8 @@ char* at(void* ws, size_t off) { return static_cast<char*>(ws) + off; }
 
 // route (+ permutation when fused) into the given buffers
 moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
-                     int32_t* ids, float* w, void* ws, const WsLayout& L, cudaStream_t st, bool pdl) {
+                     int32_t* ids, float* w, void* ws, const WsLayout& L, cudaStream_t st, bool pdl,
+                     int32_t* counts = nullptr) {
     float* logits = reinterpret_cast<float*>(at(ws, L.logits));
     cudaError_t e = cudaErrorNotSupported;
     if (L.rs_list) {  // many tokens: tensor-core screen, fixed-order logits of the candidates only
@@ -111,14 +112,14 @@ moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T,
                                      reinterpret_cast<int32_t*>(at(ws, L.rs_list)),
                                      reinterpret_cast<uint32_t*>(at(ws, L.rs_stat))};
         e = launch_router_screen(x, W_r, b, T, d, E, k, rb, logits, ids, w,
-                                 &reinterpret_cast<Ctrl*>(at(ws, L.ctrl))->status, st, pdl);
+                                 &reinterpret_cast<Ctrl*>(at(ws, L.ctrl))->status, st, pdl, counts);
         if (e != cudaErrorNotSupported) {
             MOE_CUDA(e);
             return MOE_OK;
         }
     }
     MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
-    MOE_CUDA(launch_topk(logits, T, E, k, ids, w, st, true));
+    MOE_CUDA(launch_topk(logits, T, E, k, ids, w, st, true, counts));
     return MOE_OK;
 }
 
@@ -544,9 +545,10 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
     const bool nv = W->wfmt == MOE_W_NVFP4;  // kind::mxf4nvf4: operand scales as UE4M3 per 16
     if (nv && !umma_nv_supported(E)) return MOE_ERR_UNSUPPORTED_SHAPE;
     // the token rows are quantised first: that pass leaves x in L2 for the router's reads of it
-    MOE_CUDA(launch_act_quant(x, T, d, xq, xs, fp8, st, true));
-    MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
-    MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
+    // (it also zeroes the expert counts, which the router's top-k then fills)
+    MOE_CUDA(launch_act_quant(x, T, d, xq, xs, fp8, st, true, plan.counts, E));
+    MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true, plan.counts));
+    MOE_CUDA(launch_permute_counted(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
     MOE_CUDA(launch_act_gather(xq, xs, d, E, offsets, perm, plan, L.pad_rows, xa, xa_s, fp8, st, true, false));
     uint8_t* h = reinterpret_cast<uint8_t*>(at(ws, L.h));
     uint8_t* h_s = reinterpret_cast<uint8_t*>(at(ws, L.h_s));

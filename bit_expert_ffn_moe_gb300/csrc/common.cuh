@@ -519,14 +519,16 @@ cudaError_t launch_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8
 
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
                                 float* logits, cudaStream_t st, bool pdl);
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl);
+// counts (optional): the picks also counted per expert into counts[E], which the caller has zeroed.
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl,
+                        int32_t* counts = nullptr);
 // The screened router (route_screen.cu): logits (exact fixed-order values for every candidate, -inf
 // for the experts the screen ruled out), then launch_topk's ids and w.
 // cudaErrorNotSupported when the shape or the operands' alignment does not allow it or the
 // tensor-map encoder is missing (route with the dense kernel).
 cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                  const RouterScreenBufs& rb, float* logits, int32_t* ids, float* w, int* status,
-                                 cudaStream_t st, bool pdl);
+                                 cudaStream_t st, bool pdl, int32_t* counts = nullptr);
 // Decode route: logits, then the last CTA runs top-k and the whole permutation (small T).
 cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                 float* logits, int32_t* ids, float* w, int32_t* counts, int32_t* offsets,
@@ -534,6 +536,11 @@ cudaError_t launch_route_decode(const uint16_t* x, const float* W_r, const float
                                 cudaStream_t st, bool pdl);
 bool route_decode_supported(int T, int d, int E, int k);
 
+// The permutation from counts a counting top-k left in plan.counts (one launch: offsets, plan,
+// permuted rows); the other arguments as launch_permute's.
+cudaError_t launch_permute_counted(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                                   int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl,
+                                   const float* w = nullptr, float* row_w = nullptr);
 // row_w (optional, with w): gate weight of each permuted row, row_w[inv_pos[t*k+j]] = w[t][j].
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
                            int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl,
@@ -549,7 +556,7 @@ cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int 
 // results are never stored, so the layer call skips those writes (a fifth of the gather's bytes at
 // the prefill workload); the step call moe_permute writes them as zeros.
 cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8_t* xs, bool fp8, cudaStream_t st,
-                             bool pdl);
+                             bool pdl, int32_t* zero_counts = nullptr, int E = 0);
 cudaError_t launch_act_gather(const uint8_t* xq, const uint8_t* xs, int d, int E, const int32_t* offsets,
                               const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xa, uint8_t* xa_s,
                               bool fp8, cudaStream_t st, bool pdl, bool zero_pad = true);

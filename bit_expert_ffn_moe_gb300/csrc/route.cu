@@ -214,10 +214,24 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
     pdl_launch_dependents();
 }
 
-__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w) {
+// counts != nullptr: the picks are also counted per expert (a shared-memory histogram per CTA, then
+// one global add per expert and CTA); the caller has zeroed counts.
+__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w,
+                            int32_t* counts) {
+    __shared__ int hist[kMaxE];
     pdl_wait();
+    if (counts) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+        __syncthreads();
+    }
     const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (t < T) topk_softmax_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k);
+    if (t < T)
+        topk_softmax_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k, counts ? hist : nullptr);
+    if (counts) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            if (hist[e] != 0) atomicAdd(counts + e, hist[e]);
+    }
     pdl_launch_dependents();
 }
 
@@ -230,9 +244,10 @@ cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float
                          (size_t)kLStages * kLStageBytes, st, pdl, args);
 }
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl) {
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl,
+                        int32_t* counts) {
     if (T == 0) return cudaSuccess;
-    void* args[] = {&logits, &T, &E, &k, &ids, &w};
+    void* args[] = {&logits, &T, &E, &k, &ids, &w, &counts};
     return launch_kernel((const void*)topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pdl, args);
 }
 
@@ -281,8 +296,29 @@ __global__ void dense_plan_kernel(int T, PlanView plan, int32_t* offsets, int32_
     pdl_launch_dependents();
 }
 
-// One CTA per expert: a stable block-wide compaction over the tokens that chose it, 1024 tokens
-// per pass (their ids read as 16-byte vectors when k % 4 == 0).
+// One CTA per expert: a stable block-wide compaction over the tokens that chose it, 2048 tokens
+// per pass (each thread's ids of two tokens loaded at once, as 16-byte vectors when k % 4 == 0),
+// compacted in token order: the first 1024 tokens of the pass, then the next 1024.
+__device__ __forceinline__ int find_slot(const int32_t* __restrict__ ids, int t, int T, int k, int e) {
+    int j_found = -1;
+    if (t < T) {
+        if ((k & 3) == 0) {
+            const int4* p = reinterpret_cast<const int4*>(ids + (size_t)t * k);
+            for (int q = 0; q < k / 4; ++q) {
+                const int4 v = __ldg(p + q);
+                if (v.x == e) j_found = 4 * q;
+                if (v.y == e) j_found = 4 * q + 1;
+                if (v.z == e) j_found = 4 * q + 2;
+                if (v.w == e) j_found = 4 * q + 3;
+            }
+        } else {
+            for (int j = 0; j < k; ++j)
+                if (__ldg(ids + (size_t)t * k + j) == e) j_found = j;
+        }
+    }
+    return j_found;
+}
+
 __global__ void __launch_bounds__(1024)
 scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __restrict__ offsets, PlanView plan,
                int32_t* perm_token, int32_t* inv_pos, const float* __restrict__ w, float* row_w) {
@@ -291,44 +327,93 @@ scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __r
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (plan.counts[e] == 0) return;
     int running = offsets[e];
-    const bool vec = (k & 3) == 0;
-    for (int t0 = 0; t0 < T; t0 += 1024) {
-        const int t = t0 + tid;
-        int j_found = -1;
-        if (t < T) {
-            if (vec) {
-                const int4* p = reinterpret_cast<const int4*>(ids + (size_t)t * k);
-                for (int q = 0; q < k / 4; ++q) {
-                    const int4 v = __ldg(p + q);
-                    if (v.x == e) j_found = 4 * q;
-                    if (v.y == e) j_found = 4 * q + 1;
-                    if (v.z == e) j_found = 4 * q + 2;
-                    if (v.w == e) j_found = 4 * q + 3;
-                }
-            } else {
-                for (int j = 0; j < k; ++j)
-                    if (__ldg(ids + (size_t)t * k + j) == e) j_found = j;
+    for (int t0 = 0; t0 < T; t0 += 2048) {
+        const int ta = t0 + tid, tb = t0 + 1024 + tid;
+        const int ja = find_slot(ids, ta, T, k, e), jb = find_slot(ids, tb, T, k, e);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = h ? tb : ta, j_found = h ? jb : ja;
+            const unsigned bal = __ballot_sync(0xffffffffu, j_found >= 0);
+            const int before = __popc(bal & ((1u << lane) - 1u));
+            if (lane == 0) warp_tot[warp] = __popc(bal);
+            __syncthreads();
+            int wbase = 0, tot = 0;
+            for (int q = 0; q < 32; ++q) {
+                const int n = warp_tot[q];
+                if (q < warp) wbase += n;
+                tot += n;
             }
+            if (j_found >= 0) {
+                const int r = running + wbase + before;
+                perm_token[r] = t;
+                inv_pos[(size_t)t * k + j_found] = r;
+                if (row_w) row_w[r] = w[(size_t)t * k + j_found];
+            }
+            running += tot;
+            __syncthreads();
         }
-        const unsigned bal = __ballot_sync(0xffffffffu, j_found >= 0);
-        const int before = __popc(bal & ((1u << lane) - 1u));
-        if (lane == 0) warp_tot[warp] = __popc(bal);
-        __syncthreads();
-        int wbase = 0, tot = 0;
-        for (int q = 0; q < 32; ++q) {
-            const int n = warp_tot[q];
-            if (q < warp) wbase += n;
-            tot += n;
-        }
-        if (j_found >= 0) {
-            const int r = running + wbase + before;
-            perm_token[r] = t;
-            inv_pos[(size_t)t * k + j_found] = r;
-            if (row_w) row_w[r] = w[(size_t)t * k + j_found];
-        }
-        running += tot;
-        __syncthreads();
     }
+}
+
+// The permutation when the top-k has already counted the picks into plan.counts: CTA e takes its
+// expert's offset from the counts of the experts before it, CTA 0 also writes the whole plan
+// (counts, offsets, padded offsets, tile prefix, active list), and every CTA scatters as above.
+__global__ void __launch_bounds__(1024)
+scatter_plan_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int32_t* counts_out, int32_t* offsets,
+                    PlanView plan, int32_t* perm_token, int32_t* inv_pos, const float* __restrict__ w,
+                    float* row_w) {
+    __shared__ int warp_tot[32];
+    __shared__ int s_base;
+    pdl_wait();
+    const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (e == 0 && warp == 0) build_plan_warp(plan.counts, E, counts_out, offsets, plan);
+    int v = tid < e ? __ldcg(plan.counts + tid) : 0;  // E <= 1024 = blockDim.x
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) warp_tot[warp] = v;
+    __syncthreads();
+    if (tid == 0) {
+        int b = 0;
+        for (int q = 0; q < 32; ++q) b += warp_tot[q];
+        s_base = b;
+    }
+    __syncthreads();
+    if (__ldcg(plan.counts + e) == 0) return;  // block-uniform
+    int running = s_base;
+    for (int t0 = 0; t0 < T; t0 += 2048) {
+        const int ta = t0 + tid, tb = t0 + 1024 + tid;
+        const int ja = find_slot(ids, ta, T, k, e), jb = find_slot(ids, tb, T, k, e);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int t = h ? tb : ta, j_found = h ? jb : ja;
+            const unsigned bal = __ballot_sync(0xffffffffu, j_found >= 0);
+            const int before = __popc(bal & ((1u << lane) - 1u));
+            if (lane == 0) warp_tot[warp] = __popc(bal);
+            __syncthreads();
+            int wbase = 0, tot = 0;
+            for (int q = 0; q < 32; ++q) {
+                const int n = warp_tot[q];
+                if (q < warp) wbase += n;
+                tot += n;
+            }
+            if (j_found >= 0) {
+                const int r = running + wbase + before;
+                perm_token[r] = t;
+                inv_pos[(size_t)t * k + j_found] = r;
+                if (row_w) row_w[r] = w[(size_t)t * k + j_found];
+            }
+            running += tot;
+            __syncthreads();
+        }
+    }
+}
+
+cudaError_t launch_permute_counted(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                                   int32_t* perm_token, int32_t* inv_pos, PlanView plan, cudaStream_t st, bool pdl,
+                                   const float* w, float* row_w) {
+    if (w == nullptr) row_w = nullptr;
+    void* args[] = {&ids, &T, &k, &E, &counts, &offsets, &plan, &perm_token, &inv_pos, &w, &row_w};
+    return launch_kernel((const void*)scatter_plan_kernel, dim3(E), dim3(1024), 0, st, pdl, args);
 }
 
 cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
@@ -370,8 +455,10 @@ cudaError_t launch_dense_plan(int T, PlanView plan, int32_t* offsets, int32_t* p
 
 template <bool FP8>
 __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ xq,
-                                 uint8_t* __restrict__ xs) {
+                                 uint8_t* __restrict__ xs, int32_t* __restrict__ zero_counts, int zE) {
     pdl_wait();
+    if (zero_counts && blockIdx.x == 0)  // the permutation's counts, which the top-k adds to next
+        for (int e = threadIdx.x; e < zE; e += blockDim.x) zero_counts[e] = 0;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblocks; blk += stride) {
         const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
@@ -453,12 +540,12 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
 }
 
 cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8_t* xs, bool fp8, cudaStream_t st,
-                             bool pdl) {
+                             bool pdl, int32_t* zero_counts, int E) {
     int64_t nb = (int64_t)T * (d / 32);
     if (nb <= 0) return cudaSuccess;
     int64_t blocks = (nb + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    void* a1[] = {&x, &nb, &xq, &xs};
+    void* a1[] = {&x, &nb, &xq, &xs, &zero_counts, &E};
     const void* f = fp8 ? (const void*)act_quant_kernel<true> : (const void*)act_quant_kernel<false>;
     return launch_kernel(f, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
 }

@@ -599,7 +599,7 @@ RouterScreenSizes router_screen_sizes(int T, int d, int E) {
 
 cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                  const RouterScreenBufs& rb, float* logits, int32_t* ids, float* w, int* status,
-                                 cudaStream_t st, bool pdl) {
+                                 cudaStream_t st, bool pdl, int32_t* counts) {
     const int S = router_screen_splits(T, d, E);
     if (!S || ((uintptr_t)x & 15) || ((uintptr_t)W_r & 15)) return cudaErrorNotSupported;
     const int E_pad = (E + 127) / 128 * 128, KB = d / 64;
@@ -660,7 +660,7 @@ cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const floa
         if (err != cudaSuccess) return err;
     }
     // 5. top-k + softmax
-    return launch_topk(logits, T, E, k, ids, w, st, true);
+    return launch_topk(logits, T, E, k, ids, w, st, true, counts);
 }
 
 }  // namespace moe
