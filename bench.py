@@ -540,22 +540,24 @@ def screened_route(T, d, E):
 
 
 def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_decode=False, nv_grouped=False):
-    # BF16: fused route+permute, gate/up, down+sum; else logits, top-k, count, plan, scatter,
-    # gate/up, down+sum; with the expert normalisation the down GEMV and the (normalising) sum are
-    # separate launches.  MXFP4: quantise, logits, top-k (which also counts the picks per expert), the
-    # permutation (offsets, plan and rows in one launch), gather, up, down, sum.
-    # Each latent projection: plan + GEMV (BF16) or plan + quantise + gather + GEMM (MXFP4).  Many
-    # tokens: the screened router adds three launches to the route.
+    # Route + permutation: up to 8 tokens one launch (the decode router, or the expert kernel itself);
+    # beyond, logits, top-k (which also counts the picks per expert) and the permutation (offsets,
+    # plan and rows in one launch); the screened router (many tokens) adds three launches.
+    # BF16 GEMVs: route (+ permutation), gate/up, down+sum; with the expert normalisation the down
+    # GEMV and the (normalising) sum are separate launches.  MXFP4 (any T): quantise, logits, top-k,
+    # permutation, gather, up, down, sum.  Each latent projection: plan + GEMV (BF16) or plan + quantise + gather +
+    # GEMM (MXFP4).
     proj = (2 if fmt == 0 else 4) * 2 if latent else 0
     proj += 3 if screened_route(T, d, E) else 0
+    route = 1 if T <= 8 else 3
     if fmt == 0 or (fmt == 2 and mma_decode):
         if mma_decode:
             # up to 8 tokens (E <= 152): one launch that routes, builds the token pieces and runs both
-            # GEMMs; beyond: route + permute, token pieces, the expert kernel; + a separate sum when
+            # GEMMs; else route + permutation, token pieces, the expert kernel; + a separate sum when
             # the weighted sum is not fused (more than four tokens, or normalised expert outputs)
             sep_sum = 0 if (T <= 4 and not expert_norm) else 1
-            return (1 if (T <= 8 and E <= 152) else 5 + 1 + 1) + sep_sum + proj
-        return (3 if T <= 8 else 7) + (1 if expert_norm else 0) + proj
+            return (1 if (T <= 8 and E <= 152) else route + 2) + sep_sum + proj
+        return route + 2 + (1 if expert_norm else 0) + proj
     return 8 + (2 if nv_grouped else 0) + proj  # NVFP4 weights: + the two operand-scale conversions
 
 

@@ -123,6 +123,17 @@ moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T,
     return MOE_OK;
 }
 
+// route + permutation of the layer call: the top-k counts the picks per expert into plan.counts
+// (zeroed first), then one launch builds offsets, plan and the permuted rows (with row weights)
+moe_status route_counted(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
+                         int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                         float* row_w, const PlanView& plan, void* ws, const WsLayout& L, cudaStream_t st) {
+    MOE_CUDA(cudaMemsetAsync(plan.counts, 0, sizeof(int32_t) * (size_t)E, st));
+    MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids, w, ws, L, st, true, plan.counts));
+    MOE_CUDA(launch_permute_counted(ids, T, E, k, counts, offsets, perm, inv, plan, st, true, w, row_w));
+    return MOE_OK;
+}
+
 // Events of a host-buffer call's staging buffer (moe_layer_forward_host with copy streams): "ready"
 // (its input copy landed, or the layer wrote it), "consumed" (the last layer that read it is done),
 // "drained" (the last copy out of it is done).  Created on first use of a buffer address, kept for
@@ -504,8 +515,8 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
             MOE_CUDA(launch_route_decode(x, W_r, b, T, d, E, k, reinterpret_cast<float*>(at(ws, L.logits)), ids_b, w_b,
                                          counts, offsets, perm, inv, row_w, plan, ctrl, st, true));
         } else {
-            MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
-            MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true, w_b, row_w));
+            MOE_TRY(route_counted(x, W_r, b, T, d, E, k, ids_b, w_b, counts, offsets, perm, inv, row_w, plan, ws, L,
+                                  st));
         }
         MOE_CUDA(launch_x_pieces(x, T, d, mx8, dxa, dxa_s, st, true));
         MOE_CUDA(launch_mma_decode(dxa, dxa_s, dha, dha_s, reinterpret_cast<float*>(at(ws, L.dpart)), plan, offsets,
@@ -521,8 +532,8 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
             MOE_CUDA(launch_route_decode(x, W_r, b, T, d, E, k, reinterpret_cast<float*>(at(ws, L.logits)), ids_b, w_b,
                                          counts, offsets, perm, inv, row_w, plan, ctrl, st, true));
         } else {
-            MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true));
-            MOE_CUDA(launch_permute(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true, w_b, row_w));
+            MOE_TRY(route_counted(x, W_r, b, T, d, E, k, ids_b, w_b, counts, offsets, perm, inv, row_w, plan, ws, L,
+                                  st));
         }
         uint16_t* h = reinterpret_cast<uint16_t*>(at(ws, L.h));
         MOE_CUDA(launch_gemv_up(x, perm, offsets, plan, T, d, E, k, I, W, h, st, true));

@@ -117,7 +117,9 @@ def test_variant_options_name_the_workload_and_count_launches():
     assert bench.launches_per_step(0, 1, 8192, 128, 8, mma_decode=True) == 1
     assert bench.launches_per_step(0, 4, 8192, 128, 8, mma_decode=True) == 1
     assert bench.launches_per_step(0, 8, 8192, 128, 8, mma_decode=True) == 2
-    assert bench.launches_per_step(0, 16, 8192, 128, 8, mma_decode=True) == 8
+    assert bench.launches_per_step(0, 16, 8192, 128, 8, mma_decode=True) == 6   # logits, top-k, permutation,
+    assert bench.launches_per_step(0, 8, 8192, 200, 8, mma_decode=True) == 4    # pieces, experts, sum
+    assert bench.launches_per_step(0, 16, 8192, 128, 8) == 5                     # BF16 GEMVs beyond 8 tokens
     assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True, mma_decode=True) == 2
     assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 11
     assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 19
