@@ -544,8 +544,8 @@ def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_deco
     # beyond, logits, top-k (which also counts the picks per expert) and the permutation (offsets,
     # plan and rows in one launch); the screened router (many tokens) adds three launches.
     # BF16 GEMVs: route (+ permutation), gate/up, down+sum; with the expert normalisation the down
-    # GEMV and the (normalising) sum are separate launches.  MXFP4 (any T): quantise, logits, top-k,
-    # permutation, gather, up, down, sum.  Each latent projection: plan + GEMV (BF16) or plan + quantise + gather +
+    # GEMV and the (normalising) sum are separate launches.  MXFP4 (any T): logits, top-k,
+    # permutation, the operand rows (quantised and written to their padded rows), up, down, sum.  Each latent projection: plan + GEMV (BF16) or plan + quantise + gather +
     # GEMM (MXFP4).
     proj = (2 if fmt == 0 else 4) * 2 if latent else 0
     proj += 3 if screened_route(T, d, E) else 0
@@ -558,7 +558,7 @@ def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_deco
             sep_sum = 0 if (T <= 4 and not expert_norm) else 1
             return (1 if (T <= 8 and E <= 152) else route + 2) + sep_sum + proj
         return route + 2 + (1 if expert_norm else 0) + proj
-    return 8 + (2 if nv_grouped else 0) + proj  # NVFP4 weights: + the two operand-scale conversions
+    return 7 + (2 if nv_grouped else 0) + proj  # NVFP4 weights: + the two operand-scale conversions
 
 
 def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):

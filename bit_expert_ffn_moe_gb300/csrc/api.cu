@@ -118,17 +118,17 @@ moe_status run_route(const uint16_t* x, const float* W_r, const float* b, int T,
             return MOE_OK;
         }
     }
-    MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl));
+    MOE_CUDA(launch_route_logits(x, W_r, b, T, d, E, logits, st, pdl, counts));
     MOE_CUDA(launch_topk(logits, T, E, k, ids, w, st, true, counts));
     return MOE_OK;
 }
 
 // route + permutation of the layer call: the top-k counts the picks per expert into plan.counts
-// (zeroed first), then one launch builds offsets, plan and the permuted rows (with row weights)
+// (zeroed by the route's first launch), then one launch builds offsets, plan and the permuted rows
+// (with row weights)
 moe_status route_counted(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                          int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
                          float* row_w, const PlanView& plan, void* ws, const WsLayout& L, cudaStream_t st) {
-    MOE_CUDA(cudaMemsetAsync(plan.counts, 0, sizeof(int32_t) * (size_t)E, st));
     MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids, w, ws, L, st, true, plan.counts));
     MOE_CUDA(launch_permute_counted(ids, T, E, k, counts, offsets, perm, inv, plan, st, true, w, row_w));
     return MOE_OK;
@@ -550,17 +550,14 @@ static moe_status layer_forward(const uint16_t* x, const float* W_r, const float
     }
     uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
     uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
-    uint8_t* xq = reinterpret_cast<uint8_t*>(at(ws, L.xq));
-    uint8_t* xs = reinterpret_cast<uint8_t*>(at(ws, L.xs));
     const bool fp8 = fmt == MOE_ACT_MXFP8;
     const bool nv = W->wfmt == MOE_W_NVFP4;  // kind::mxf4nvf4: operand scales as UE4M3 per 16
     if (nv && !umma_nv_supported(E)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    // the token rows are quantised first: that pass leaves x in L2 for the router's reads of it
-    // (it also zeroes the expert counts, which the router's top-k then fills)
-    MOE_CUDA(launch_act_quant(x, T, d, xq, xs, fp8, st, true, plan.counts, E));
+    // route (its first launch zeroes the pick counts, its top-k fills them), the permutation in one
+    // launch, then each token row quantised once and written to its k padded operand rows
     MOE_TRY(run_route(x, W_r, b, T, d, E, k, ids_b, w_b, ws, L, st, true, plan.counts));
     MOE_CUDA(launch_permute_counted(ids_b, T, E, k, counts, offsets, perm, inv, plan, st, true));
-    MOE_CUDA(launch_act_gather(xq, xs, d, E, offsets, perm, plan, L.pad_rows, xa, xa_s, fp8, st, true, false));
+    MOE_CUDA(launch_act_quant_scatter(x, T, d, k, ids_b, inv, offsets, plan, xa, xa_s, fp8, st, true));
     uint8_t* h = reinterpret_cast<uint8_t*>(at(ws, L.h));
     uint8_t* h_s = reinterpret_cast<uint8_t*>(at(ws, L.h_s));
     uint16_t* y_perm = reinterpret_cast<uint16_t*>(at(ws, L.y_perm));

@@ -517,8 +517,9 @@ cudaError_t launch_nvfp4_unpack(const uint8_t* q, const uint8_t* s, const float*
                                 int64_t K, float* w, cudaStream_t st);
 cudaError_t launch_codes_to_mma(const uint8_t* q, int64_t rows, int64_t K, uint8_t* q_mma, cudaStream_t st);
 
+// zero_counts (optional): counts[E] zeroed for the counting top-k that follows.
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
-                                float* logits, cudaStream_t st, bool pdl);
+                                float* logits, cudaStream_t st, bool pdl, int32_t* zero_counts = nullptr);
 // counts (optional): the picks also counted per expert into counts[E], which the caller has zeroed.
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w, cudaStream_t st, bool pdl,
                         int32_t* counts = nullptr);
@@ -526,6 +527,7 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, 
 // for the experts the screen ruled out), then launch_topk's ids and w.
 // cudaErrorNotSupported when the shape or the operands' alignment does not allow it or the
 // tensor-map encoder is missing (route with the dense kernel).
+// counts (optional): zeroed by the route's first launch, then the picks counted per expert.
 cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E, int k,
                                  const RouterScreenBufs& rb, float* logits, int32_t* ids, float* w, int* status,
                                  cudaStream_t st, bool pdl, int32_t* counts = nullptr);
@@ -556,7 +558,12 @@ cudaError_t launch_act_quant_gather(const uint16_t* x, int T, int d, int E, int 
 // results are never stored, so the layer call skips those writes (a fifth of the gather's bytes at
 // the prefill workload); the step call moe_permute writes them as zeros.
 cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8_t* xs, bool fp8, cudaStream_t st,
-                             bool pdl, int32_t* zero_counts = nullptr, int E = 0);
+                             bool pdl);
+// Quantise each token row once and write it straight to the padded rows of its k picks (the
+// permutation of ids / inv_pos / offsets / plan already built); padding rows are left as they are.
+cudaError_t launch_act_quant_scatter(const uint16_t* x, int T, int d, int k, const int32_t* ids,
+                                     const int32_t* inv_pos, const int32_t* offsets, PlanView plan, uint8_t* xa,
+                                     uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl);
 cudaError_t launch_act_gather(const uint8_t* xq, const uint8_t* xs, int d, int E, const int32_t* offsets,
                               const int32_t* perm_token, PlanView plan, int64_t pad_rows, uint8_t* xa, uint8_t* xa_s,
                               bool fp8, cudaStream_t st, bool pdl, bool zero_pad = true);

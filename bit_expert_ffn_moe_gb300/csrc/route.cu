@@ -123,7 +123,7 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, bool vali
 
 __global__ void __launch_bounds__(kLThreads, 2)
 route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restrict__ W_r, const float* __restrict__ b,
-                          int T, int d, int E, float* __restrict__ logits) {
+                          int T, int d, int E, float* __restrict__ logits, int32_t* __restrict__ zero_counts) {
     extern __shared__ __align__(16) unsigned char lsm[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * kLT, e0 = blockIdx.y * kLE;
@@ -156,6 +156,8 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
         for (int c = 0; c < 8; ++c) acc[p][c] = make_float2(0.f, 0.f);
 
     pdl_wait();
+    if (zero_counts && blockIdx.x == 0 && blockIdx.y == 0)  // the pick counts the top-k adds to next
+        for (int e = tid; e < E; e += kLThreads) zero_counts[e] = 0;
 #pragma unroll
     for (int kc = 0; kc < kLStages - 1; ++kc) {
         if (kc < nchunks) load_chunk(kc);
@@ -236,9 +238,9 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
 }
 
 cudaError_t launch_route_logits(const uint16_t* x, const float* W_r, const float* b, int T, int d, int E,
-                                float* logits, cudaStream_t st, bool pdl) {
+                                float* logits, cudaStream_t st, bool pdl, int32_t* zero_counts) {
     if (T == 0) return cudaSuccess;
-    void* args[] = {&x, &W_r, &b, &T, &d, &E, &logits};
+    void* args[] = {&x, &W_r, &b, &T, &d, &E, &logits, &zero_counts};
     dim3 grid((T + kLT - 1) / kLT, (E + kLE - 1) / kLE);
     return launch_kernel((const void*)route_logits_tiled_kernel, grid, dim3(kLThreads),
                          (size_t)kLStages * kLStageBytes, st, pdl, args);
@@ -455,10 +457,8 @@ cudaError_t launch_dense_plan(int T, PlanView plan, int32_t* offsets, int32_t* p
 
 template <bool FP8>
 __global__ void act_quant_kernel(const uint16_t* __restrict__ x, int64_t nblocks, uint8_t* __restrict__ xq,
-                                 uint8_t* __restrict__ xs, int32_t* __restrict__ zero_counts, int zE) {
+                                 uint8_t* __restrict__ xs) {
     pdl_wait();
-    if (zero_counts && blockIdx.x == 0)  // the permutation's counts, which the top-k adds to next
-        for (int e = threadIdx.x; e < zE; e += blockDim.x) zero_counts[e] = 0;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; blk < nblocks; blk += stride) {
         const uint4* src = reinterpret_cast<const uint4*>(x + blk * 32);
@@ -539,13 +539,87 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
     (void)pad_rows;
 }
 
+// The layer call's operand in one pass, once the permutation is known: warp w of the grid takes
+// token t = w; lane j < k first finds the padded row of pick j (its expert's padded start + its row
+// within the expert), then lane l encodes the blocks l, l + 32, ... of the token row (as
+// act_quant_kernel) and writes each block's codes to all k rows; the scale bytes of four
+// consecutive blocks (four neighbouring lanes) go out as one 4-byte store per row.  Padding rows
+// are left as they are.
+template <bool FP8>
+__global__ void __launch_bounds__(256)
+act_quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int d, int k, const int32_t* __restrict__ ids,
+                         const int32_t* __restrict__ inv_pos, const int32_t* __restrict__ offsets, PlanView plan,
+                         uint8_t* __restrict__ xa, uint8_t* __restrict__ xa_s) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31, nb = d / 32;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+        int my_row = 0;
+        if (lane < k) {
+            const int e = __ldg(ids + t * k + lane);
+            my_row = __ldg(plan.pad_offsets + e) + (__ldg(inv_pos + t * k + lane) - __ldg(offsets + e));
+        }
+        const uint16_t* xrow = x + t * d;
+        for (int b0 = 0; b0 < nb; b0 += 32) {  // warp-uniform: the shuffles below need every lane
+            const int blk = b0 + lane;
+            uint32_t sb = 0;
+            uint4 c[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            if (blk < nb) {
+                const uint4* src = reinterpret_cast<const uint4*>(xrow + (size_t)blk * 32);
+                uint4 u[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) u[i] = __ldg(src + i);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t ww[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        v[8 * i + 2 * m] = bf16_bits_to_f32(ww[m] & 0xFFFF);
+                        v[8 * i + 2 * m + 1] = bf16_bits_to_f32(ww[m] >> 16);
+                    }
+                }
+                sb = FP8 ? mx8_block_encode(v, c) : mx_block_encode(v, c[0]);
+            }
+            const int q0 = lane & ~3;
+            const uint32_t s4 = (__shfl_sync(0xffffffffu, sb, q0) & 0xFF) |
+                                ((__shfl_sync(0xffffffffu, sb, q0 + 1) & 0xFF) << 8) |
+                                ((__shfl_sync(0xffffffffu, sb, q0 + 2) & 0xFF) << 16) |
+                                ((__shfl_sync(0xffffffffu, sb, q0 + 3) & 0xFF) << 24);
+            for (int j = 0; j < k; ++j) {
+                const int64_t r = __shfl_sync(0xffffffffu, my_row, j);
+                if (blk < nb) {
+                    if (FP8) {
+                        *reinterpret_cast<uint4*>(xa + mma8_tile_offset(r, 2 * blk, d)) = c[0];
+                        *reinterpret_cast<uint4*>(xa + mma8_tile_offset(r, 2 * blk + 1, d)) = c[1];
+                    } else {
+                        *reinterpret_cast<uint4*>(xa + mma_tile_offset(r, blk, d)) = c[0];
+                    }
+                    if ((lane & 3) == 0) *reinterpret_cast<uint32_t*>(xa_s + mma_scale_offset(r, blk, d)) = s4;
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_act_quant_scatter(const uint16_t* x, int T, int d, int k, const int32_t* ids,
+                                     const int32_t* inv_pos, const int32_t* offsets, PlanView plan, uint8_t* xa,
+                                     uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl) {
+    if (T == 0) return cudaSuccess;
+    int64_t blocks = ((int64_t)T + 7) / 8;  // 8 warps (tokens) per CTA
+    if (blocks > 152 * 8) blocks = 152 * 8;
+    void* args[] = {&x, &T, &d, &k, &ids, &inv_pos, &offsets, &plan, &xa, &xa_s};
+    const void* f = fp8 ? (const void*)act_quant_scatter_kernel<true> : (const void*)act_quant_scatter_kernel<false>;
+    return launch_kernel(f, dim3((unsigned)blocks), dim3(256), 0, st, pdl, args);
+}
+
 cudaError_t launch_act_quant(const uint16_t* x, int T, int d, uint8_t* xq, uint8_t* xs, bool fp8, cudaStream_t st,
-                             bool pdl, int32_t* zero_counts, int E) {
+                             bool pdl) {
     int64_t nb = (int64_t)T * (d / 32);
     if (nb <= 0) return cudaSuccess;
     int64_t blocks = (nb + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    void* a1[] = {&x, &nb, &xq, &xs, &zero_counts, &E};
+    void* a1[] = {&x, &nb, &xq, &xs};
     const void* f = fp8 ? (const void*)act_quant_kernel<true> : (const void*)act_quant_kernel<false>;
     return launch_kernel(f, dim3((unsigned)blocks), dim3(256), 0, st, pdl, a1);
 }

@@ -69,10 +69,11 @@ constexpr int kXBatch = 8;            // x loads in flight per lane and token
 // CTA (e, part) writes a quarter of row e of the hi and lo operand matrices ([E_pad][d] bf16, in
 // 128 x 64 tiles with the 128-byte swizzle: 16-byte chunk j of row r at chunk position j ^ (r % 8));
 // rows past E are zero.  Also that quarter's share of ||w_e||^2 (wn2 [kSplitParts][E]) and the
-// reset of the expert's candidate count.
+// reset of the expert's candidate count (and of its pick count, when the top-k counts picks).
 __global__ void __launch_bounds__(256) router_split_kernel(const float* __restrict__ W_r, int E, int d,
                                                            uint8_t* __restrict__ bhi, uint8_t* __restrict__ blo,
-                                                           float* __restrict__ wn2, int32_t* __restrict__ cnt) {
+                                                           float* __restrict__ wn2, int32_t* __restrict__ cnt,
+                                                           int32_t* __restrict__ counts) {
     __shared__ float red[8];
     pdl_wait();
     const int e = blockIdx.x, KB = d / 64, rb = e / 128, r = e % 128;
@@ -114,7 +115,10 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
         float t = 0.f;
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
         wn2[(size_t)blockIdx.y * E + e] = t;
-        if (blockIdx.y == 0) cnt[e] = 0;
+        if (blockIdx.y == 0) {
+            cnt[e] = 0;
+            if (counts) counts[e] = 0;  // the per-expert pick counts the top-k adds to
+        }
     }
     pdl_launch_dependents();
 }
@@ -608,7 +612,7 @@ cudaError_t launch_router_screen(const uint16_t* x, const float* W_r, const floa
     if (err != cudaSuccess) return err;
     // 1. split
     {
-        void* args[] = {&W_r, &E, &d, (void*)&rb.bhi, (void*)&rb.blo, (void*)&rb.wn2, (void*)&rb.cnt};
+        void* args[] = {&W_r, &E, &d, (void*)&rb.bhi, (void*)&rb.blo, (void*)&rb.wn2, (void*)&rb.cnt, &counts};
         err = launch_kernel((const void*)router_split_kernel, dim3(E_pad, kSplitParts), dim3(256), 0, st, pdl, args);
         if (err != cudaSuccess) return err;
     }

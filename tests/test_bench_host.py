@@ -107,13 +107,13 @@ def test_variant_options_name_the_workload_and_count_launches():
     assert bench.launches_per_step(0, 1, 8192, 128, 8) == 3
     assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True) == 4
     assert bench.launches_per_step(0, 1, 8192, 128, 8, latent=True) == 7
-    # prefill: 8 layer kernels (quantise, logits, counting top-k, permutation, gather, up, down, sum);
+    # prefill: 7 layer kernels (logits, counting top-k, permutation, operand rows, up, down, sum);
     # + 2 x (plan, quantise, gather, GEMM)
     # tensor-core decode: route, token pieces, the fused expert kernel (its sum fused up to 4 tokens)
     # up to eight tokens: the expert kernel routes its own tokens (one launch; + the normalising sum)
-    assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 11          # screened router: + 3
-    assert bench.launches_per_step(1, 200, 8192, 128, 8) == 8            # dense router below 256 tokens
-    assert bench.launches_per_step(1, 65536, 8192, 1024, 8) == 8         # and beyond 2^25 token-expert pairs
+    assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 10          # screened router: + 3
+    assert bench.launches_per_step(1, 200, 8192, 128, 8) == 7            # dense router below 256 tokens
+    assert bench.launches_per_step(1, 65536, 8192, 1024, 8) == 7         # and beyond 2^25 token-expert pairs
     assert bench.launches_per_step(0, 1, 8192, 128, 8, mma_decode=True) == 1
     assert bench.launches_per_step(0, 4, 8192, 128, 8, mma_decode=True) == 1
     assert bench.launches_per_step(0, 8, 8192, 128, 8, mma_decode=True) == 2
@@ -121,8 +121,8 @@ def test_variant_options_name_the_workload_and_count_launches():
     assert bench.launches_per_step(0, 8, 8192, 200, 8, mma_decode=True) == 4    # pieces, experts, sum
     assert bench.launches_per_step(0, 16, 8192, 128, 8) == 5                     # BF16 GEMVs beyond 8 tokens
     assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True, mma_decode=True) == 2
-    assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 11
-    assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 19
+    assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 10
+    assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 18
 
 
 def test_nvfp4_weight_option_changes_the_byte_model_and_the_names():
@@ -207,4 +207,4 @@ def test_default_line_times_verify_and_the_prefill_workloads_in_both_activation_
     assert bench.tensor_peak_ratio(1) == 6.0 and bench.tensor_peak_ratio(2) == 2.0
     assert bench.launches_per_step(2, 1, 8192, 128, 8, mma_decode=True) == bench.launches_per_step(
         0, 1, 8192, 128, 8, mma_decode=True)
-    assert bench.launches_per_step(2, 4096, 8192, 128, 8) == 11
+    assert bench.launches_per_step(2, 4096, 8192, 128, 8) == 10
