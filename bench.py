@@ -747,11 +747,12 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
 
 def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call, host_call=None):
     """Same metric through the C ABI with host buffers: every step copies its x from pinned host
-    memory and its y back to pinned host memory inside the timed region.  Small activations (up to
-    1 MB per step, the decode shapes) go through the host-buffer layer call (moe_layer_forward_host:
-    copy in, layer, copy out, one C call per step).  Larger ones run the copies on a second stream
-    with double-buffered device x and y, so the copy of step s + 1's input and of step s's output
-    overlap step s's layer call, as a pipelined host loop would run them."""
+    memory and its y back to pinned host memory inside the timed region.  The plain layer goes
+    through the host-buffer layer call (moe_layer_forward_host: copy in, layer, copy out, one C
+    call per step, the copies on an input and an output copy stream with two alternating staging
+    pairs).  The options without a host-buffer entry point (expert normalisation, latent
+    projections) run the copies on a second stream with double-buffered device x and y, so the
+    copy of step s + 1's input and of step s's output overlap step s's layer call."""
     import numpy as np
     import torch
 
@@ -795,7 +796,7 @@ def end_to_end(args, cfg, cm, xs_host, fmt, dev, stream, call, host_call=None):
                 y_pin[s % y_pin.shape[0]].copy_(y_dev[b], non_blocking=True)
                 ev_out[b].record(cs)
 
-    if host_call is not None and T * d * 2 <= (1 << 20):
+    if host_call is not None:
         xh = [x_pin[i].data_ptr() for i in range(x_pin.shape[0])]
         yh = [y_pin[i].data_ptr() for i in range(y_pin.shape[0])]
         xd = [t.data_ptr() for t in x_dev]

@@ -539,9 +539,10 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
     (void)pad_rows;
 }
 
-// The layer call's operand in one pass, once the permutation is known: warp w of the grid takes
-// token t = w; lane j < k first finds the padded row of pick j (its expert's padded start + its row
-// within the expert), then lane l encodes the blocks l, l + 32, ... of the token row (as
+// The layer call's operand in one pass, once the permutation is known.  Work item = (token t, a
+// segment of 64 of its 32-element blocks); lane j < k first finds the padded row of pick j (its
+// expert's padded start + its row within the expert), then lane l loads the blocks
+// seg + l and seg + 32 + l of the token row (both before any store), encodes them (as
 // act_quant_kernel) and writes each block's codes to all k rows; the scale bytes of four
 // consecutive blocks (four neighbouring lanes) go out as one 4-byte store per row.  Padding rows
 // are left as they are.
@@ -551,36 +552,40 @@ act_quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int d, int k, co
                          const int32_t* __restrict__ inv_pos, const int32_t* __restrict__ offsets, PlanView plan,
                          uint8_t* __restrict__ xa, uint8_t* __restrict__ xa_s) {
     pdl_wait();
-    const int lane = threadIdx.x & 31, nb = d / 32;
+    const int lane = threadIdx.x & 31, nb = d / 32, nseg = (nb + 63) / 64;
+    const int64_t items = (int64_t)T * nseg;
     const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x / 32);
-    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); t < T; t += nwarps) {
+    for (int64_t it = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); it < items; it += nwarps) {
+        const int64_t t = it / nseg;
+        const int b0 = (int)(it % nseg) * 64;
         int my_row = 0;
         if (lane < k) {
             const int e = __ldg(ids + t * k + lane);
             my_row = __ldg(plan.pad_offsets + e) + (__ldg(inv_pos + t * k + lane) - __ldg(offsets + e));
         }
-        const uint16_t* xrow = x + t * d;
-        for (int b0 = 0; b0 < nb; b0 += 32) {  // warp-uniform: the shuffles below need every lane
-            const int blk = b0 + lane;
-            uint32_t sb = 0;
-            uint4 c[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
-            if (blk < nb) {
-                const uint4* src = reinterpret_cast<const uint4*>(xrow + (size_t)blk * 32);
-                uint4 u[4];
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * d);  // 4 chunks of 16 bytes per block
+        uint4 u[2][4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) u[i] = __ldg(src + i);
-                float v[32];
+        for (int h = 0; h < 2; ++h) {
+            const int blk = b0 + 32 * h + lane;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t ww[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+            for (int i = 0; i < 4; ++i) u[h][i] = blk < nb ? __ldg(src + (size_t)blk * 4 + i) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        v[8 * i + 2 * m] = bf16_bits_to_f32(ww[m] & 0xFFFF);
-                        v[8 * i + 2 * m + 1] = bf16_bits_to_f32(ww[m] >> 16);
-                    }
+        for (int h = 0; h < 2; ++h) {  // warp-uniform: the shuffles below need every lane
+            const int blk = b0 + 32 * h + lane;
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t ww[4] = {u[h][i].x, u[h][i].y, u[h][i].z, u[h][i].w};
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    v[8 * i + 2 * m] = bf16_bits_to_f32(ww[m] & 0xFFFF);
+                    v[8 * i + 2 * m + 1] = bf16_bits_to_f32(ww[m] >> 16);
                 }
-                sb = FP8 ? mx8_block_encode(v, c) : mx_block_encode(v, c[0]);
             }
+            uint4 c[2];
+            const uint32_t sb = FP8 ? mx8_block_encode(v, c) : mx_block_encode(v, c[0]);
             const int q0 = lane & ~3;
             const uint32_t s4 = (__shfl_sync(0xffffffffu, sb, q0) & 0xFF) |
                                 ((__shfl_sync(0xffffffffu, sb, q0 + 1) & 0xFF) << 8) |
@@ -606,7 +611,8 @@ cudaError_t launch_act_quant_scatter(const uint16_t* x, int T, int d, int k, con
                                      const int32_t* inv_pos, const int32_t* offsets, PlanView plan, uint8_t* xa,
                                      uint8_t* xa_s, bool fp8, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
-    int64_t blocks = ((int64_t)T + 7) / 8;  // 8 warps (tokens) per CTA
+    const int64_t items = (int64_t)T * ((d / 32 + 63) / 64);
+    int64_t blocks = (items + 7) / 8;  // 8 warps (work items) per CTA
     if (blocks > 152 * 8) blocks = 152 * 8;
     void* args[] = {&x, &T, &d, &k, &ids, &inv_pos, &offsets, &plan, &xa, &xa_s};
     const void* f = fp8 ? (const void*)act_quant_scatter_kernel<true> : (const void*)act_quant_scatter_kernel<false>;

@@ -45,15 +45,17 @@ def test_host_buffer_layer_equals_device_layer(name, fmt, ofmt):
     check_outputs(bf16_tensor_to_f32(y_host[tokens]), y_o["y"])
 
 
-@pytest.mark.parametrize("name", ["decode", "tiny"])
-def test_host_buffer_layer_with_copy_streams(name):
-    cfg = IN.CONFIGS[name]
+@pytest.mark.parametrize("name,fmt", [("decode", B.MOE_ACT_BF16), ("tiny", B.MOE_ACT_BF16),
+                                      ("mx300", B.MOE_ACT_MXFP4)])
+def test_host_buffer_layer_with_copy_streams(name, fmt):
+    cfg = (IN.small_config("mx300", T=300, d=512, E=12, k=3, I=512, index=97) if name == "mx300"
+           else IN.CONFIGS[name])
     layer = DeviceLayer(cfg)
     T, d = cfg.T, cfg.d
-    ws = make_workspace(T, d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
+    ws = make_workspace(T, d, cfg.E, cfg.k, cfg.I, fmt)
     calls = 5
     xbs = [IN.make_x(cfg, call=c) for c in range(calls)]
-    refs = [layer_forward(layer, bits_to_device(xb), B.MOE_ACT_BF16, ws=ws).cpu() for xb in xbs]
+    refs = [layer_forward(layer, bits_to_device(xb), fmt, ws=ws).cpu() for xb in xbs]
     x_host = [torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).pin_memory() for xb in xbs]
     y_host = [torch.zeros((T, d), dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
     x_dev = [torch.empty((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
@@ -61,7 +63,7 @@ def test_host_buffer_layer_with_copy_streams(name):
     st, ins, outs = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     for c in range(calls):
         B.moe_layer_forward_host(x_host[c], layer.W_r, layer.b, T, d, cfg.E, cfg.k, cfg.I, layer.weights,
-                                 B.MOE_ACT_BF16, y_host[c], None, None, x_dev[c % 2], y_dev[c % 2], ws, stream=st,
+                                 fmt, y_host[c], None, None, x_dev[c % 2], y_dev[c % 2], ws, stream=st,
                                  in_stream=ins, out_stream=outs)
     outs.synchronize()
     st.synchronize()

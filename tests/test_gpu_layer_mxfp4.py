@@ -124,8 +124,15 @@ def test_step_calls_tiny_against_oracle_intermediates():
     check_outputs(g["y"], ref["y"], "y")
 
 
-def test_layer_call_equals_step_calls():
-    cfg = IN.CONFIGS["tiny"]
+# d = 2304: 72 blocks per token row, so the layer call's operand pass (work items of 64 blocks) has
+# a full and a partial segment per token; 300 tokens over 16 experts give ragged token tiles.
+SEGMENTS = IN.small_config("mx_segments", T=300, d=2304, E=16, k=4, I=256, index=161, zipf_s=1.2)
+
+
+@pytest.mark.parametrize("cfg", [IN.CONFIGS["tiny"], SEGMENTS], ids=["tiny", "mx_segments"])
+def test_layer_call_equals_step_calls(cfg):
+    """The layer call (counting top-k, one-launch permutation, each token row quantised once and
+    written to its k padded rows) gives the step calls' output bit for bit."""
     layer = get_layer(cfg)
     xb = IN.make_x(cfg, call=1)
     g = run_steps(layer, xb)

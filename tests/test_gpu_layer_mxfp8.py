@@ -224,9 +224,14 @@ def test_prefill_step_calls_against_oracle_intermediates(cfg):
     check_outputs(g["y"], ref["y"], "y")
 
 
-def test_prefill_layer_call_equals_step_calls():
-    layer = get_layer(PREFILL_SMALL)
-    xb = IN.make_x(PREFILL_SMALL, call=1)
+# 72 blocks per token row (a full and a partial 64-block segment of the operand pass), ragged tiles
+PREFILL_SEGMENTS = IN.small_config("mx8_segments", T=300, d=2304, E=16, k=4, I=256, index=162, zipf_s=1.2)
+
+
+@pytest.mark.parametrize("cfg", [PREFILL_SMALL, PREFILL_SEGMENTS], ids=["mx8_prefill", "mx8_segments"])
+def test_prefill_layer_call_equals_step_calls(cfg):
+    layer = get_layer(cfg)
+    xb = IN.make_x(cfg, call=1)
     g = run_prefill_steps(layer, xb)
     y = layer_forward(layer, bits_to_device(xb), FMT)
     np.testing.assert_array_equal(bf16_tensor_to_f32(y), g["y"])
