@@ -184,6 +184,16 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
+def traffic_workload(args, cfg, tag=""):
+    """The workload name an ncu summary must carry for its counters to stand for the timed launch:
+    the summaries are captured on the plain layer, so a launch at the latent width (--latent) or in
+    another mode (tag, e.g. the decode kernel on MXFP8 activations) matches none of them."""
+    name = cfg.name + tag
+    if getattr(args, "latent", 0):
+        name += "+latent%d" % args.latent
+    return name
+
+
 def ncu_traffic(profile_name: str, kernel_sources, workload: str):
     """dram bytes per launch recorded in profiles/<profile_name> for the kernel, or None when
     the summary is missing, was captured on another workload, or the kernel's sources changed
@@ -607,7 +617,7 @@ def kernel_roofline(args, cfg, layers, xs, fmt, dev, stream, pk):
     achieved = per_launch / (avg_ms / 1e3) / 1e9
     profile = "gemv_up_decode.md" if args.weights == "mxfp4" else "gemv_up_decode_nvfp4.md"
     traffic = ncu_traffic(profile, ["bit_expert_ffn_moe_gb300/csrc/gemv.cu",
-                                    "bit_expert_ffn_moe_gb300/csrc/common.cuh"], cfg.name)
+                                    "bit_expert_ffn_moe_gb300/csrc/common.cuh"], traffic_workload(args, cfg))
     return {"kernel": "gemv_up_kernel (gate/up + SwiGLU, decode)", "bound": "hbm",
             "timing": "each launch bracketed by events through the step API (eager; inside the timed graph the "
                       "launch overlaps its neighbours through programmatic dependent launch)",
@@ -665,7 +675,8 @@ def kernel_roofline_decode_mma(args, cfg, layers, xs, fmt, dev, stream, pk, n):
     per_launch = n_act * expert_read_bytes(d, I, "mxfp4") + T * d * 2
     achieved = per_launch / (avg_ms / 1e3) / 1e9
     profile = "umma_decode_layer.md" if cfg.name == "decode" else "umma_decode_layer_%s.md" % cfg.name
-    traffic = ncu_traffic(profile, DECODE_KERNEL_SOURCES, cfg.name)
+    traffic = ncu_traffic(profile, DECODE_KERNEL_SOURCES,
+                          traffic_workload(args, cfg, "+mxfp8" if fmt == B.MOE_ACT_MXFP8 else ""))
     return {"kernel": "umma_decode_layer_kernel (tcgen05 kind::mxf4 gate/up + SwiGLU + down%s, decode)"
                       % (" + weighted sum" if y is not None else ""),
             "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -732,7 +743,7 @@ def kernel_roofline_mxfp4(args, cfg, layers, xs, fmt, dev, stream, pk, n):
                                                            else "umma_grouped_prefill.md")
     if cfg.name != "prefill":  # another workload's capture (e.g. umma_grouped_long_prefill.md)
         profile = profile.replace("umma_grouped_prefill", "umma_grouped_" + cfg.name)
-    traffic = ncu_traffic(profile, GROUPED_KERNEL_SOURCES, cfg.name)
+    traffic = ncu_traffic(profile, GROUPED_KERNEL_SOURCES, traffic_workload(args, cfg))
     return {"kernel": "umma_grouped_kernel<1, %d> (tcgen05 %s gate/up + SwiGLU, prefill)"
                       % (kind, ["kind::mxf4", "kind::mxf8f6f4", "kind::mxf4nvf4"][kind]), "bound": "tensor",
             "achieved": round(achieved, 1), "peak": round(peak_tf, 1), "unit": "TFLOP/s",

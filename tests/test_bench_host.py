@@ -87,6 +87,20 @@ def test_recorded_traffic_only_for_its_workload_and_sources():
     assert bench.ncu_traffic("umma_grouped_prefill.md", src[:1], "prefill") is None  # other sources
 
 
+def test_traffic_only_for_the_plain_launch():
+    """A launch at the latent width, or the decode kernel on MXFP8 activations, matches no summary
+    (all were captured on the plain layer)."""
+    import argparse
+
+    import bench
+    from bit_expert_ffn_moe_gb300 import inputs as IN
+    cfg = IN.CONFIGS["decode"]
+    assert bench.traffic_workload(argparse.Namespace(latent=0), cfg) == "decode"
+    assert bench.traffic_workload(argparse.Namespace(latent=4096), cfg) == "decode+latent4096"
+    assert bench.traffic_workload(argparse.Namespace(latent=0), cfg, "+mxfp8") == "decode+mxfp8"
+    assert bench.ncu_traffic("umma_decode_layer.md", bench.DECODE_KERNEL_SOURCES, "decode+mxfp8") is None
+
+
 def test_variant_options_name_the_workload_and_count_launches():
     """--expert-norm and --latent change the layer the bench times: the workload name says so,
     the layer runs at the latent width, and the launch count includes the extra kernels."""
