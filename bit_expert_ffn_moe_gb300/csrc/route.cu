@@ -300,7 +300,24 @@ __global__ void dense_plan_kernel(int T, PlanView plan, int32_t* offsets, int32_
 
 // One CTA per expert: a stable block-wide compaction over the tokens that chose it, 2048 tokens
 // per pass (each thread's ids of two tokens loaded at once, as 16-byte vectors when k % 4 == 0),
-// compacted in token order: the first 1024 tokens of the pass, then the next 1024.
+// compacted in token order: the first 1024 tokens of the pass, then the next 1024.  Each round:
+// the warps' counts (ballots) to shared memory, one barrier, warp 0 scans the 32 counts, a second
+// barrier.  (A round's warp_tot writes come after every thread passed the previous round's second
+// barrier, by which point warp 0 has read the previous counts; warp 0's warp_pre writes come after
+// the first barrier, by which point every thread has read the previous warp_pre.)
+__device__ __forceinline__ void warp_exclusive_scan(const int* warp_tot, int* warp_pre) {
+    const int lane = threadIdx.x & 31;
+    const int v = warp_tot[lane];
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    warp_pre[lane] = incl - v;
+    if (lane == 31) warp_pre[32] = incl;
+}
+
 __device__ __forceinline__ int find_slot(const int32_t* __restrict__ ids, int t, int T, int k, int e) {
     int j_found = -1;
     if (t < T) {
@@ -324,7 +341,7 @@ __device__ __forceinline__ int find_slot(const int32_t* __restrict__ ids, int t,
 __global__ void __launch_bounds__(1024)
 scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __restrict__ offsets, PlanView plan,
                int32_t* perm_token, int32_t* inv_pos, const float* __restrict__ w, float* row_w) {
-    __shared__ int warp_tot[32];
+    __shared__ int warp_tot[32], warp_pre[33];
     pdl_wait();
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (plan.counts[e] == 0) return;
@@ -339,20 +356,15 @@ scatter_kernel(const int32_t* __restrict__ ids, int T, int k, const int32_t* __r
             const int before = __popc(bal & ((1u << lane) - 1u));
             if (lane == 0) warp_tot[warp] = __popc(bal);
             __syncthreads();
-            int wbase = 0, tot = 0;
-            for (int q = 0; q < 32; ++q) {
-                const int n = warp_tot[q];
-                if (q < warp) wbase += n;
-                tot += n;
-            }
+            if (warp == 0) warp_exclusive_scan(warp_tot, warp_pre);
+            __syncthreads();
             if (j_found >= 0) {
-                const int r = running + wbase + before;
+                const int r = running + warp_pre[warp] + before;
                 perm_token[r] = t;
                 inv_pos[(size_t)t * k + j_found] = r;
                 if (row_w) row_w[r] = w[(size_t)t * k + j_found];
             }
-            running += tot;
-            __syncthreads();
+            running += warp_pre[32];
         }
     }
 }
@@ -364,7 +376,7 @@ __global__ void __launch_bounds__(1024)
 scatter_plan_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int32_t* counts_out, int32_t* offsets,
                     PlanView plan, int32_t* perm_token, int32_t* inv_pos, const float* __restrict__ w,
                     float* row_w) {
-    __shared__ int warp_tot[32];
+    __shared__ int warp_tot[32], warp_pre[33];
     __shared__ int s_base;
     pdl_wait();
     const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -392,20 +404,15 @@ scatter_plan_kernel(const int32_t* __restrict__ ids, int T, int k, int E, int32_
             const int before = __popc(bal & ((1u << lane) - 1u));
             if (lane == 0) warp_tot[warp] = __popc(bal);
             __syncthreads();
-            int wbase = 0, tot = 0;
-            for (int q = 0; q < 32; ++q) {
-                const int n = warp_tot[q];
-                if (q < warp) wbase += n;
-                tot += n;
-            }
+            if (warp == 0) warp_exclusive_scan(warp_tot, warp_pre);
+            __syncthreads();
             if (j_found >= 0) {
-                const int r = running + wbase + before;
+                const int r = running + warp_pre[warp] + before;
                 perm_token[r] = t;
                 inv_pos[(size_t)t * k + j_found] = r;
                 if (row_w) row_w[r] = w[(size_t)t * k + j_found];
             }
-            running += tot;
-            __syncthreads();
+            running += warp_pre[32];
         }
     }
 }
