@@ -216,8 +216,11 @@ route_logits_tiled_kernel(const uint16_t* __restrict__ x, const float* __restric
     pdl_launch_dependents();
 }
 
-// counts != nullptr: the picks are also counted per expert (a shared-memory histogram per CTA, then
-// one global add per expert and CTA); the caller has zeroed counts.
+// One warp per token; NV = keys per lane (E <= 32 NV), one instantiation per width so that each
+// holds only the registers its own width needs.  counts != nullptr: the picks are also counted per
+// expert (a shared-memory histogram per CTA, then one global add per expert and CTA); the caller
+// has zeroed counts.
+template <int NV>
 __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w,
                             int32_t* counts) {
     __shared__ int hist[kMaxE];
@@ -228,7 +231,8 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
     }
     const int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (t < T)
-        topk_softmax_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k, counts ? hist : nullptr);
+        topk_softmax_regs<NV, false>(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k,
+                                     counts ? hist : nullptr);
     if (counts) {
         __syncthreads();
         for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -250,7 +254,14 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, 
                         int32_t* counts) {
     if (T == 0) return cudaSuccess;
     void* args[] = {&logits, &T, &E, &k, &ids, &w, &counts};
-    return launch_kernel((const void*)topk_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pdl, args);
+    const int nv = (E + 31) / 32;
+    const void* f = nv <= 1   ? (const void*)topk_kernel<1>
+                    : nv <= 2 ? (const void*)topk_kernel<2>
+                    : nv <= 4 ? (const void*)topk_kernel<4>
+                    : nv <= 8 ? (const void*)topk_kernel<8>
+                    : nv <= 16 ? (const void*)topk_kernel<16>
+                               : (const void*)topk_kernel<32>;
+    return launch_kernel(f, dim3((T + 7) / 8), dim3(256), 0, st, pdl, args);
 }
 
 // ------------------------------------------------------------------ permutation (any T)
