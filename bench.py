@@ -555,9 +555,9 @@ def launches_per_step(fmt, T, d, E, k, expert_norm=False, latent=False, mma_deco
     # plan and rows in one launch); the screened router (many tokens) adds three launches.
     # BF16 GEMVs: route (+ permutation), gate/up, down+sum; with the expert normalisation the down
     # GEMV and the (normalising) sum are separate launches.  MXFP4 (any T): logits, top-k,
-    # permutation, the operand rows (quantised and written to their padded rows), up, down, sum.  Each latent projection: plan + GEMV (BF16) or plan + quantise + gather +
-    # GEMM (MXFP4).
-    proj = (2 if fmt == 0 else 4) * 2 if latent else 0
+    # permutation, the operand rows (quantised and written to their padded rows), up, down, sum.
+    # Each latent projection: plan + GEMV (BF16) or plan + operand rows + GEMM (MXFP4).
+    proj = (2 if fmt == 0 else 3) * 2 if latent else 0
     proj += 3 if screened_route(T, d, E) else 0
     route = 1 if T <= 8 else 3
     if fmt == 0 or (fmt == 2 and mma_decode):

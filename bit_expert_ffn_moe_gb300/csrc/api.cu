@@ -688,9 +688,8 @@ moe_status moe_dense_linear(const uint16_t* x, int T, int K, int N, const moe_mx
     uint8_t* xa = reinterpret_cast<uint8_t*>(at(ws, L.xa));
     uint8_t* xa_s = reinterpret_cast<uint8_t*>(at(ws, L.xa_s));
     const bool fp8 = fmt == MOE_ACT_MXFP8;
-    MOE_CUDA(launch_act_quant_gather(x, T, K, 1, 1, offsets, perm, plan, L.pad_rows,
-                                     reinterpret_cast<uint8_t*>(at(ws, L.xq)), reinterpret_cast<uint8_t*>(at(ws, L.xs)),
-                                     xa, xa_s, fp8, st, true));
+    // each row quantised straight into its operand row (the identity permutation: row t = token t)
+    MOE_CUDA(launch_act_quant_scatter(x, T, K, 1, nullptr, nullptr, nullptr, plan, xa, xa_s, fp8, st, true));
     MOE_CUDA(launch_umma_down(xa, xa_s, plan, offsets, T, N, 1, 1, K, L.pad_rows, &Wd, fp8, nullptr, y,
                               &ctrl->status, st, true));
     return MOE_OK;

@@ -563,7 +563,7 @@ act_gather_kernel(const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs
 // seg + l and seg + 32 + l of the token row (both before any store), encodes them (as
 // act_quant_kernel) and writes each block's codes to all k rows; the scale bytes of four
 // consecutive blocks (four neighbouring lanes) go out as one 4-byte store per row.  Padding rows
-// are left as they are.
+// are left as they are.  ids == nullptr: the identity of a dense map (k = 1, token t to row t).
 template <bool FP8>
 __global__ void __launch_bounds__(256)
 act_quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int d, int k, const int32_t* __restrict__ ids,
@@ -578,8 +578,12 @@ act_quant_scatter_kernel(const uint16_t* __restrict__ x, int T, int d, int k, co
         const int b0 = (int)(it % nseg) * 64;
         int my_row = 0;
         if (lane < k) {
-            const int e = __ldg(ids + t * k + lane);
-            my_row = __ldg(plan.pad_offsets + e) + (__ldg(inv_pos + t * k + lane) - __ldg(offsets + e));
+            if (ids) {
+                const int e = __ldg(ids + t * k + lane);
+                my_row = __ldg(plan.pad_offsets + e) + (__ldg(inv_pos + t * k + lane) - __ldg(offsets + e));
+            } else {
+                my_row = (int)t;
+            }
         }
         const uint4* src = reinterpret_cast<const uint4*>(x + t * d);  // 4 chunks of 16 bytes per block
         uint4 u[2][4];

@@ -122,7 +122,7 @@ def test_variant_options_name_the_workload_and_count_launches():
     assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True) == 4
     assert bench.launches_per_step(0, 1, 8192, 128, 8, latent=True) == 7
     # prefill: 7 layer kernels (logits, counting top-k, permutation, operand rows, up, down, sum);
-    # + 2 x (plan, quantise, gather, GEMM)
+    # + 2 x (plan, operand rows, GEMM)
     # tensor-core decode: route, token pieces, the fused expert kernel (its sum fused up to 4 tokens)
     # up to eight tokens: the expert kernel routes its own tokens (one launch; + the normalising sum)
     assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 10          # screened router: + 3
@@ -136,7 +136,7 @@ def test_variant_options_name_the_workload_and_count_launches():
     assert bench.launches_per_step(0, 16, 8192, 128, 8) == 5                     # BF16 GEMVs beyond 8 tokens
     assert bench.launches_per_step(0, 1, 8192, 128, 8, expert_norm=True, mma_decode=True) == 2
     assert bench.launches_per_step(1, 4096, 8192, 128, 8) == 10
-    assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 18
+    assert bench.launches_per_step(1, 4096, 8192, 128, 8, latent=True) == 16
 
 
 def test_nvfp4_weight_option_changes_the_byte_model_and_the_names():
