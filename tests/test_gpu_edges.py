@@ -1,7 +1,8 @@
 """GPU parity at the edges of the supported shapes and at the degenerate cases of the method:
 the largest E and k (1024 experts, k = 32), the one-launch router at its largest T and the tiled
 router just above it, the smallest hidden size, k = 1, a single expert (the layer is then a
-dense SwiGLU FFN) and every expert chosen by every token (k = E), on both expert paths."""
+dense SwiGLU FFN) and every expert chosen by every token (k = E), on both expert paths; the layer
+call's permutation (read out of its workspace) bit for bit in each."""
 import numpy as np
 import pytest
 import torch
@@ -9,7 +10,8 @@ import torch
 from bit_expert_ffn_moe_gb300 import binding as B
 from bit_expert_ffn_moe_gb300 import inputs as IN
 from bit_expert_ffn_moe_gb300.layer import DeviceLayer, layer_forward, make_workspace
-from moe_testlib import bf16_tensor_to_f32, bits_to_device, check_outputs, check_weights, oracle_expert_weights
+from moe_testlib import (bf16_tensor_to_f32, bits_to_device, check_outputs, check_permutation, check_weights,
+                         oracle_expert_weights, workspace_routing)
 from oracle import oracle as O
 
 pytestmark = pytest.mark.gpu
@@ -60,6 +62,11 @@ LAYER_EDGES = [
     ("all_experts_t2_bf16", 2, 256, 4, 4, 256, "bf16", 114),  # two rows on every expert
     ("all_experts_t3_bf16", 3, 256, 4, 4, 256, "bf16", 115),
     ("all_experts_t40_mx", 40, 256, 4, 4, 256, "mxfp4", 116),
+    # the layer call's counting top-k (32 keys per lane) and one-launch permutation at 1000
+    # experts, k = 17 (the ids read one by one): GEMVs beyond 8 tokens, and the screened router
+    # with the tcgen05 path from 256 tokens on
+    ("e1000_k17_t70_bf16", 70, 256, 1000, 17, 256, "bf16", 117),
+    ("e1000_k17_t300_mx", 300, 256, 1000, 17, 256, "mxfp4", 118),
 ]
 
 
@@ -79,6 +86,8 @@ def test_layer_at_degenerate_routing(name, T, d, E, k, I, fmt, index):
     if k == E:
         np.testing.assert_array_equal(ids_h, np.tile(np.arange(E), (T, 1)))
     check_weights(w.cpu().numpy(), ref["w"])
+    # the permutation the layer call built in its workspace, bit for bit
+    check_permutation(workspace_routing(ws, T, d, E, k, I, act), ref)
     if E == 1:
         np.testing.assert_array_equal(w.cpu().numpy(), np.ones((T, 1), np.float32))
     check_outputs(bf16_tensor_to_f32(y), ref["y"], name)
