@@ -137,8 +137,9 @@ moe_status route_counted(const uint16_t* x, const float* W_r, const float* b, in
 // Events of a host-buffer call's staging buffer (moe_layer_forward_host with copy streams): "ready"
 // (its input copy landed, or the layer wrote it), "consumed" (the last layer that read it is done),
 // "drained" (the last copy out of it is done).  Created on first use of a buffer address, kept for
-// the process (a small table: beyond 64 buffers the oldest entries are released -- destroying an
-// event whose work is pending is deferred by the runtime, so no pending wait is affected).
+// the process in a small table: beyond 64 buffers the least recently used entry is released,
+// after the host has waited for its events -- a buffer met again later then has no pending work
+// that its fresh events would fail to order.
 struct StagingEvents {
     cudaEvent_t ready = nullptr, consumed = nullptr, drained = nullptr;
     bool consumed_recorded = false, drained_recorded = false;
@@ -148,16 +149,23 @@ StagingEvents* staging_events(const void* buf) {
     static std::mutex mu;
     static std::vector<std::pair<const void*, StagingEvents*>> table;
     std::lock_guard<std::mutex> lock(mu);
-    for (auto& e : table)
-        if (e.first == buf) return e.second;
-    if (table.size() >= 64) {
-        for (auto& e : table) {
-            cudaEventDestroy(e.second->ready);
-            cudaEventDestroy(e.second->consumed);
-            cudaEventDestroy(e.second->drained);
-            delete e.second;
+    for (size_t i = 0; i < table.size(); ++i)
+        if (table[i].first == buf) {  // most recently used at the back, so that the entries of one
+            auto hit = table[i];      // call (x and y) are never the one evicted for the other
+            table.erase(table.begin() + (ptrdiff_t)i);
+            table.push_back(hit);
+            return hit.second;
         }
-        table.clear();
+    if (table.size() >= 64) {
+        StagingEvents* old = table.front().second;
+        if (cudaEventSynchronize(old->ready) != cudaSuccess || cudaEventSynchronize(old->consumed) != cudaSuccess ||
+            cudaEventSynchronize(old->drained) != cudaSuccess)
+            return nullptr;
+        cudaEventDestroy(old->ready);
+        cudaEventDestroy(old->consumed);
+        cudaEventDestroy(old->drained);
+        delete old;
+        table.erase(table.begin());
     }
     StagingEvents* ev = new StagingEvents();
     if (cudaEventCreateWithFlags(&ev->ready, cudaEventDisableTiming) != cudaSuccess ||

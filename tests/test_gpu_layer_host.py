@@ -69,3 +69,28 @@ def test_host_buffer_layer_with_copy_streams(name, fmt):
     st.synchronize()
     for c in range(calls):
         assert torch.equal(y_host[c].view(torch.int16), refs[c].view(torch.int16)), "call %d" % c
+
+
+def test_host_buffer_staging_table_beyond_its_capacity():
+    """More staging buffers than the event table holds (64): the x buffers alternate between two
+    addresses while every call takes a fresh y buffer, so old entries are released while the x
+    buffers stay in use; every call still gets its own result."""
+    cfg = IN.CONFIGS["tiny"]
+    layer = DeviceLayer(cfg)
+    T, d = cfg.T, cfg.d
+    ws = make_workspace(T, d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
+    calls = 80
+    xbs = [IN.make_x(cfg, call=c % 7) for c in range(calls)]
+    refs = {c: layer_forward(layer, bits_to_device(xbs[c]), B.MOE_ACT_BF16, ws=ws).cpu() for c in range(7)}
+    x_host = [torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).pin_memory() for xb in xbs]
+    y_host = [torch.zeros((T, d), dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
+    x_dev = [torch.empty((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    y_dev = [torch.empty((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(calls)]  # all distinct
+    st, ins, outs = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for c in range(calls):
+        B.moe_layer_forward_host(x_host[c], layer.W_r, layer.b, T, d, cfg.E, cfg.k, cfg.I, layer.weights,
+                                 B.MOE_ACT_BF16, y_host[c], None, None, x_dev[c % 2], y_dev[c], ws, stream=st,
+                                 in_stream=ins, out_stream=outs)
+    torch.cuda.synchronize()
+    for c in range(calls):
+        assert torch.equal(y_host[c].view(torch.int16), refs[c % 7].view(torch.int16)), "call %d" % c
