@@ -621,11 +621,15 @@ moe_status moe_layer_forward_host(const uint16_t* x_host, const float* W_r, cons
     StagingEvents* ex = staging_events(x_dev);
     StagingEvents* ey = staging_events(y_dev);
     if (!ex || !ey) return MOE_ERR_CUDA;
+    // a buffer may serve as x_dev in one call and as y_dev in another: each write into it waits for
+    // every earlier reader of it (layers reading it as x, copies out of it as y)
     if (ex->consumed_recorded) MOE_CUDA(cudaStreamWaitEvent(is, ex->consumed, 0));  // the last layer read x_dev
+    if (ex->drained_recorded) MOE_CUDA(cudaStreamWaitEvent(is, ex->drained, 0));    // the last copy out of it
     MOE_CUDA(cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, is));
     MOE_CUDA(cudaEventRecord(ex->ready, is));
     MOE_CUDA(cudaStreamWaitEvent(st, ex->ready, 0));
     if (ey->drained_recorded) MOE_CUDA(cudaStreamWaitEvent(st, ey->drained, 0));  // the last copy out of y_dev
+    if (ey->consumed_recorded) MOE_CUDA(cudaStreamWaitEvent(st, ey->consumed, 0));  // the last layer read of it
     MOE_TRY(layer_forward(x_dev, W_r, b, T, d, E, k, I, W, fmt, false, 0.f, y_dev, ids, w, ws, ws_bytes, st));
     MOE_CUDA(cudaEventRecord(ex->consumed, st));
     ex->consumed_recorded = true;

@@ -381,10 +381,13 @@ moe_status moe_layer_forward(const uint16_t* x, const float* W_r, const float* b
  *     so that a caller alternating two (x_dev, y_dev) pairs over consecutive calls has the copies
  *     of one call overlap the layers of its neighbours (one stream per direction: a copy in never
  *     queues behind a copy out, which waits for its layer).  The library orders the streams with
- *     events it keeps per staging buffer (created on first use, reused): the copy into x_dev waits
- *     for the last layer that read x_dev, the layer waits for its input copy and for the last copy
- *     out of y_dev, the copy out waits for the layer.  y_host holds the result once out_stream has
- *     passed that point.  Calls on the same workspace must share `stream`.
+ *     events it keeps per staging buffer (created on first use, reused; beyond 64 buffers the least
+ *     recently used one's events are released after the host has waited for them): the copy into
+ *     x_dev waits for the last layer that read x_dev and for the last copy out of it (a buffer may
+ *     serve as x_dev in one call and y_dev in another), the layer waits for its input copy and for
+ *     the last copy out of and the last layer read of y_dev, the copy out waits for the layer.
+ *     y_host holds the result once out_stream has passed that point.  Calls on the same workspace
+ *     must share `stream`.
  * x_host and y_host should be page-locked (pinned) for the copies to be asynchronous; pageable
  * memory works, with copies that are synchronous with respect to the host.  The other arguments,
  * the shape rules, the workspace and the errors are moe_layer_forward's; MOE_ERR_INVALID_ARG also

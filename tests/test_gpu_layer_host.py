@@ -94,3 +94,26 @@ def test_host_buffer_staging_table_beyond_its_capacity():
     torch.cuda.synchronize()
     for c in range(calls):
         assert torch.equal(y_host[c].view(torch.int16), refs[c % 7].view(torch.int16)), "call %d" % c
+
+
+def test_host_buffer_staging_roles_swap():
+    """Two device buffers that swap roles on every call (x of one call is y of the next): the copy
+    into a buffer waits for the copy out of it, and the layer's write into it for every reader."""
+    cfg = IN.CONFIGS["decode"]
+    layer = DeviceLayer(cfg)
+    T, d = cfg.T, cfg.d
+    ws = make_workspace(T, d, cfg.E, cfg.k, cfg.I, B.MOE_ACT_BF16)
+    calls = 12
+    xbs = [IN.make_x(cfg, call=c) for c in range(calls)]
+    refs = [layer_forward(layer, bits_to_device(xb), B.MOE_ACT_BF16, ws=ws).cpu() for xb in xbs]
+    x_host = [torch.from_numpy(xb.view(np.int16).copy()).view(torch.bfloat16).pin_memory() for xb in xbs]
+    y_host = [torch.zeros((T, d), dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
+    bufs = [torch.empty((T, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    st, ins, outs = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    for c in range(calls):
+        B.moe_layer_forward_host(x_host[c], layer.W_r, layer.b, T, d, cfg.E, cfg.k, cfg.I, layer.weights,
+                                 B.MOE_ACT_BF16, y_host[c], None, None, bufs[c % 2], bufs[(c + 1) % 2], ws,
+                                 stream=st, in_stream=ins, out_stream=outs)
+    torch.cuda.synchronize()
+    for c in range(calls):
+        assert torch.equal(y_host[c].view(torch.int16), refs[c].view(torch.int16)), "call %d" % c
