@@ -311,11 +311,11 @@ __global__ void dense_plan_kernel(int T, PlanView plan, int32_t* offsets, int32_
 
 // One CTA per expert: a stable block-wide compaction over the tokens that chose it, 2048 tokens
 // per pass (each thread's ids of two tokens loaded at once, as 16-byte vectors when k % 4 == 0),
-// compacted in token order: the first 1024 tokens of the pass, then the next 1024.  Each round:
-// the warps' counts (ballots) to shared memory, one barrier, warp 0 scans the 32 counts, a second
-// barrier.  (A round's warp_tot writes come after every thread passed the previous round's second
-// barrier, by which point warp 0 has read the previous counts; warp 0's warp_pre writes come after
-// the first barrier, by which point every thread has read the previous warp_pre.)
+// compacted in token order: the first 1024 tokens of the pass, then the next 1024.  Per 1024
+// tokens: the warps' counts (ballots) to shared memory, one barrier, warp 0 scans the 32 counts, a
+// second barrier.  (The warp_tot writes for the next 1024 tokens come after every thread passed the
+// second barrier, by which point warp 0 has read the counts; warp 0's next warp_pre writes come
+// after the next first barrier, by which point every thread has read the previous warp_pre.)
 __device__ __forceinline__ void warp_exclusive_scan(const int* warp_tot, int* warp_pre) {
     const int lane = threadIdx.x & 31;
     const int v = warp_tot[lane];
