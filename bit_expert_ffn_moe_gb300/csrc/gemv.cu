@@ -907,7 +907,8 @@ __global__ void combine_kernel(const uint16_t* __restrict__ y_perm, const int32_
                 const int r = j < k ? __ldg(inv_pos + (size_t)t * k + j) : -1;
                 ok[q] = (unsigned)r < (unsigned)(T * k);  // else not a row of y_perm: contributes nothing
                 wj[q] = ok[q] ? __ldg(w + (size_t)t * k + j) : 0.f;
-                u[q] = ok[q] ? *reinterpret_cast<const uint4*>(y_perm + (size_t)r * d + 8 * c) : make_uint4(0, 0, 0, 0);
+                // each y_perm row is read once: streaming loads, so that they do not displace the rest of L2
+                u[q] = ok[q] ? __ldcs(reinterpret_cast<const uint4*>(y_perm + (size_t)r * d + 8 * c)) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
